@@ -1,0 +1,572 @@
+/*
+ * kvref.c -- float64 CPU oracle for KVarN-style KV-cache block quantization
+ * and for the decode attention that reads the quantized cache.
+ *
+ * TEST INFRASTRUCTURE ONLY.  Nothing in the product library links, loads or
+ * calls this file; only the tests, the smoke check and the bench's CPU
+ * baseline leg do.  It shares no code, header, table or constant with the
+ * CUDA path: every layout constant below is restated here on purpose.
+ *
+ * Method source: "KVarN: Huawei'den KV-Cache Kuantizasyonu icin Yerel vLLM
+ * Backend'i" (blog.edumints.com), section "KVarN Nasil Calisir?" (How KVarN
+ * works).  That section quantizes the KV cache in fixed-size token blocks and
+ * passes every block through four stages:
+ *   1. the raw FP16 block ("Onbellek"),
+ *   2. an orthonormal Hadamard rotation along the channel dimension
+ *      ("Dondurulmus Onbellek"), which spreads outliers and keeps attention
+ *      scores unchanged,
+ *   3. a Sinkhorn-like row and column variance normalization in the log
+ *      domain ("Normalize Edilmis Onbellek"),
+ *   4. low-bit asymmetric round-to-nearest, 4-bit keys and 2-bit values
+ *      ("Kuantize Edilmis Onbellek").
+ * The same page names the format kvarn_k4v2_g128 (section "Yazilim
+ * Gelistirme ve Ogrenme Acisindan Pratik Cikarimlar"): group size 128.
+ * Decode attention and paging follow "KV Cache (Anahtar-Deger Onbellegi)"
+ * (yapayzekasozluk.tr), sections "KV Cache Nasil Calisir?" and "Paged
+ * Attention (vLLM)".
+ *
+ * Readings where the pages are silent (each is also listed in the design
+ * notes of the repository):
+ *   - block = 128 tokens x 128 channels of one KV head; K and V are separate
+ *     tiles and both pass through all four stages;
+ *   - Hadamard = Sylvester construction in natural order, scaled by
+ *     1/sqrt(128); row y_t = H x_t;
+ *   - Sinkhorn: rows = tokens, columns = channels, log scales a_t, b_d start
+ *     at 0; one iteration = row step then column step; each step adds
+ *     log(sigma) where sigma is the centred population standard deviation
+ *     (divide by n) of Z = Y * exp(-a_t - b_d); a step is skipped for a row or
+ *     column whose variance is <= 1e-10 * mean(Z^2) of that row or column;
+ *   - group = the 128 channels of one token (per-token groups);
+ *   - RTN: z = min, s = (max - min)/(2^b - 1), q = clamp(rint(u)) with
+ *     u = (x - z)/s, ties to even; a constant group gives s = 0, q = 0;
+ *   - stored metadata is fp32: s' = fp32(r_t s), z' = fp32(r_t z), column
+ *     scale c_d = fp32(exp(b_d)); dequantized rotated value
+ *     yhat_td = c_d (s'_t q_td + z'_t);
+ *   - attention: softmax(q . k * scale) v over every cached token (the
+ *     quantized pages, then the newest len mod 128 tokens kept as fp16).
+ *
+ * Page record (one per page and KV head, 15360 bytes):
+ *   [0,     8192)  K codes, token-major: row t at 64 t; byte j holds channel
+ *                  2j in bits 0-3 and channel 2j+1 in bits 4-7
+ *   [8192, 12288)  V codes, channel-major: row d at 8192 + 32 d; byte j holds
+ *                  tokens 4j..4j+3 in bits 0-1, 2-3, 4-5, 6-7
+ *   [12288,13312)  K per-token {s', z'} fp32 pairs, token t at 12288 + 8 t
+ *   [13312,14336)  V per-token {s', z'} fp32 pairs
+ *   [14336,14848)  K per-channel c_d fp32
+ *   [14848,15360)  V per-channel c_d fp32
+ * Pool = [num_pages][num_kv_heads][15360 bytes].
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+
+#define NCH 128            /* head_dim = group size */
+#define NTOK 128           /* tokens per block / page */
+#define REC_BYTES 15360
+#define OFF_KCODES 0
+#define OFF_VCODES 8192
+#define OFF_KSZ 12288
+#define OFF_VSZ 13312
+#define OFF_KC 14336
+#define OFF_VC 14848
+
+/* ------------------------------------------------------------------ */
+/* fp16 <-> double, written out from the IEEE-754 binary16 definition */
+/* ------------------------------------------------------------------ */
+
+double kvref_half_to_double(uint16_t h)
+{
+    int sign = (h >> 15) & 1;
+    int expo = (h >> 10) & 0x1f;
+    int mant = h & 0x3ff;
+    double v;
+    if (expo == 0) {
+        v = ldexp((double)mant, -24);              /* subnormal or zero */
+    } else if (expo == 31) {
+        v = mant ? NAN : INFINITY;
+    } else {
+        v = ldexp((double)(1024 + mant), expo - 25);
+    }
+    return sign ? -v : v;
+}
+
+/* ------------------------------------------------------------------ */
+/* Stage 2: orthonormal Hadamard rotation along channels               */
+/* KVarN page, "KVarN Nasil Calisir?", stage "Dondurulmus Onbellek".    */
+/* ------------------------------------------------------------------ */
+
+/* Sylvester recursion H_1 = [1], H_2m = [[H_m, H_m], [H_m, -H_m]], then the
+ * whole matrix is scaled by 1/sqrt(n) so that H H^T = I.  n: power of two. */
+void kvref_hadamard(int n, double *H)
+{
+    int m, i, j;
+    for (i = 0; i < n * n; ++i) H[i] = 0.0;
+    H[0] = 1.0;
+    for (m = 1; m < n; m *= 2) {
+        for (i = 0; i < m; ++i) {
+            for (j = 0; j < m; ++j) {
+                double h = H[i * n + j];
+                H[i * n + (j + m)] = h;
+                H[(i + m) * n + j] = h;
+                H[(i + m) * n + (j + m)] = -h;
+            }
+        }
+    }
+    for (i = 0; i < n * n; ++i) H[i] /= sqrt((double)n);
+}
+
+/* Y = X H^T as an explicit matrix product: y_t = H x_t for every token row.
+ * x: NTOK x NCH fp16 bit patterns, token t at x + t * ld_tok.  Y: NTOK x NCH. */
+void kvref_rotate_tile(const uint16_t *x, long ld_tok, const double *H, double *Y)
+{
+    int t, d, j;
+    double xt[NCH];
+    for (t = 0; t < NTOK; ++t) {
+        for (j = 0; j < NCH; ++j) xt[j] = kvref_half_to_double(x[t * ld_tok + j]);
+        for (d = 0; d < NCH; ++d) {
+            double acc = 0.0;
+            for (j = 0; j < NCH; ++j) acc += H[d * NCH + j] * xt[j];
+            Y[t * NCH + d] = acc;
+        }
+    }
+}
+
+/* ------------------------------------------------------------------ */
+/* Stage 3: Sinkhorn-like row/column variance normalization, log domain */
+/* KVarN page, "KVarN Nasil Calisir?", stage "Normalize Edilmis Onbellek" */
+/* ------------------------------------------------------------------ */
+
+/* Centred population statistics of v[0..n-1], two passes. */
+static void centred_stats(const double *v, int n, double *var, double *mean_sq)
+{
+    int i;
+    double mean = 0.0, acc = 0.0, sq = 0.0;
+    for (i = 0; i < n; ++i) mean += v[i];
+    mean /= n;
+    for (i = 0; i < n; ++i) {
+        double e = v[i] - mean;
+        acc += e * e;
+        sq += v[i] * v[i];
+    }
+    *var = acc / n;
+    *mean_sq = sq / n;
+}
+
+/* Runs `iters` iterations (row step, then column step) on the rotated tile Y
+ * (NTOK x NCH).  Output: log row scales a[NTOK] and log column scales b[NCH].
+ * trace (nullable, 4*iters entries): for iteration k, trace[4k] is the largest
+ * |log sigma| over the rows that the row step updated and trace[4k+1] the
+ * spread (largest minus smallest log sigma) over those rows; trace[4k+2] and
+ * trace[4k+3] are the same two figures for the column step.  The centred
+ * statistics admit no exact joint fixed point in general (row and column means
+ * differ), so log sigma settles to a common per-step offset while the spread
+ * goes to zero: the spread is the convergence measure. */
+void kvref_sinkhorn(const double *Y, int iters, double *a, double *b, double *trace)
+{
+    int k, t, d;
+    double z[NTOK > NCH ? NTOK : NCH];
+    double ea[NTOK], eb[NCH];
+    for (t = 0; t < NTOK; ++t) a[t] = 0.0;
+    for (d = 0; d < NCH; ++d) b[d] = 0.0;
+    for (k = 0; k < iters; ++k) {
+        double worst = 0.0, lo = INFINITY, hi = -INFINITY;
+        /* row step: normalise each token row by its current std */
+        for (d = 0; d < NCH; ++d) eb[d] = exp(-b[d]);
+        for (t = 0; t < NTOK; ++t) {
+            double var, msq;
+            double e = exp(-a[t]);
+            for (d = 0; d < NCH; ++d) z[d] = Y[t * NCH + d] * e * eb[d];
+            centred_stats(z, NCH, &var, &msq);
+            if (var > 1e-10 * msq) {
+                double ls = log(sqrt(var));
+                a[t] += ls;
+                if (fabs(ls) > worst) worst = fabs(ls);
+                if (ls < lo) lo = ls;
+                if (ls > hi) hi = ls;
+            }
+        }
+        if (trace) {
+            trace[4 * k] = worst;
+            trace[4 * k + 1] = hi >= lo ? hi - lo : 0.0;
+        }
+        worst = 0.0;
+        lo = INFINITY;
+        hi = -INFINITY;
+        /* column step: normalise each channel column by its current std */
+        for (t = 0; t < NTOK; ++t) ea[t] = exp(-a[t]);
+        for (d = 0; d < NCH; ++d) {
+            double var, msq;
+            double e = exp(-b[d]);
+            for (t = 0; t < NTOK; ++t) z[t] = Y[t * NCH + d] * ea[t] * e;
+            centred_stats(z, NTOK, &var, &msq);
+            if (var > 1e-10 * msq) {
+                double ls = log(sqrt(var));
+                b[d] += ls;
+                if (fabs(ls) > worst) worst = fabs(ls);
+                if (ls < lo) lo = ls;
+                if (ls > hi) hi = ls;
+            }
+        }
+        if (trace) {
+            trace[4 * k + 2] = worst;
+            trace[4 * k + 3] = hi >= lo ? hi - lo : 0.0;
+        }
+    }
+}
+
+/* ------------------------------------------------------------------ */
+/* Stage 4: asymmetric round-to-nearest, per-token groups of 128        */
+/* KVarN page, "KVarN Nasil Calisir?", stage "Kuantize Edilmis Onbellek"; */
+/* format name kvarn_k4v2_g128 (4-bit K, 2-bit V, group 128).           */
+/* ------------------------------------------------------------------ */
+
+/* Normalised tile Xn_td = Y_td / (r_t c32_d), then per row t:
+ * z = min_d Xn, s = (max - min)/(2^bits - 1), u = (Xn - z)/s,
+ * q = clamp(rint(u), 0, 2^bits - 1); metadata s' = fp32(r s), z' = fp32(r z).
+ * u (nullable) receives the pre-rounding value for the boundary rule. */
+void kvref_rtn(const double *Y, const double *r, const float *c32, int bits,
+               uint8_t *q, float *s32, float *z32, double *u)
+{
+    int t, d;
+    int qmax = (1 << bits) - 1;
+    for (t = 0; t < NTOK; ++t) {
+        double xn[NCH];
+        double mn = INFINITY, mx = -INFINITY, s, z;
+        for (d = 0; d < NCH; ++d) {
+            xn[d] = Y[t * NCH + d] / (r[t] * (double)c32[d]);
+            if (xn[d] < mn) mn = xn[d];
+            if (xn[d] > mx) mx = xn[d];
+        }
+        z = mn;
+        s = (mx - mn) / qmax;
+        s32[t] = (float)(r[t] * s);
+        z32[t] = (float)(r[t] * z);
+        for (d = 0; d < NCH; ++d) {
+            double ud = 0.0;
+            long qi = 0;
+            if (s > 0.0) {
+                ud = (xn[d] - z) / s;
+                qi = (long)nearbyint(ud);          /* ties to even */
+                if (qi < 0) qi = 0;
+                if (qi > qmax) qi = qmax;
+            }
+            q[t * NCH + d] = (uint8_t)qi;
+            if (u) u[t * NCH + d] = ud;
+        }
+    }
+}
+
+/* ------------------------------------------------------------------ */
+/* Packing into a page record                                          */
+/* ------------------------------------------------------------------ */
+
+static void put_f32(uint8_t *p, float v) { memcpy(p, &v, 4); }
+static float get_f32(const uint8_t *p) { float v; memcpy(&v, p, 4); return v; }
+
+/* is_v = 0: K part (4-bit, token-major); is_v = 1: V part (2-bit, channel-major). */
+void kvref_pack_part(uint8_t *rec, int is_v, const uint8_t *q, const float *s32,
+                     const float *z32, const float *c32)
+{
+    int t, d, j;
+    if (!is_v) {
+        for (t = 0; t < NTOK; ++t)
+            for (j = 0; j < NCH / 2; ++j)
+                rec[OFF_KCODES + t * 64 + j] =
+                    (uint8_t)((q[t * NCH + 2 * j] & 15) | ((q[t * NCH + 2 * j + 1] & 15) << 4));
+    } else {
+        for (d = 0; d < NCH; ++d)
+            for (j = 0; j < NTOK / 4; ++j)
+                rec[OFF_VCODES + d * 32 + j] =
+                    (uint8_t)((q[(4 * j) * NCH + d] & 3) | ((q[(4 * j + 1) * NCH + d] & 3) << 2) |
+                              ((q[(4 * j + 2) * NCH + d] & 3) << 4) |
+                              ((q[(4 * j + 3) * NCH + d] & 3) << 6));
+    }
+    for (t = 0; t < NTOK; ++t) {
+        put_f32(rec + (is_v ? OFF_VSZ : OFF_KSZ) + 8 * t, s32[t]);
+        put_f32(rec + (is_v ? OFF_VSZ : OFF_KSZ) + 8 * t + 4, z32[t]);
+    }
+    for (d = 0; d < NCH; ++d) put_f32(rec + (is_v ? OFF_VC : OFF_KC) + 4 * d, c32[d]);
+}
+
+/* Inverse of kvref_pack_part for the codes and metadata. */
+void kvref_unpack_part(const uint8_t *rec, int is_v, uint8_t *q, float *s32, float *z32,
+                       float *c32)
+{
+    int t, d;
+    for (t = 0; t < NTOK; ++t) {
+        for (d = 0; d < NCH; ++d) {
+            if (!is_v) {
+                uint8_t byte = rec[OFF_KCODES + t * 64 + d / 2];
+                q[t * NCH + d] = (uint8_t)((byte >> (4 * (d % 2))) & 15);
+            } else {
+                uint8_t byte = rec[OFF_VCODES + d * 32 + t / 4];
+                q[t * NCH + d] = (uint8_t)((byte >> (2 * (t % 4))) & 3);
+            }
+        }
+        s32[t] = get_f32(rec + (is_v ? OFF_VSZ : OFF_KSZ) + 8 * t);
+        z32[t] = get_f32(rec + (is_v ? OFF_VSZ : OFF_KSZ) + 8 * t + 4);
+    }
+    for (d = 0; d < NCH; ++d) c32[d] = get_f32(rec + (is_v ? OFF_VC : OFF_KC) + 4 * d);
+}
+
+/* Dequantized rotated tile yhat_td = c_d (s'_t q_td + z'_t), from a record. */
+void kvref_dequant_part(const uint8_t *rec, int is_v, double *yhat)
+{
+    uint8_t q[NTOK * NCH];
+    float s32[NTOK], z32[NTOK], c32[NCH];
+    int t, d;
+    kvref_unpack_part(rec, is_v, q, s32, z32, c32);
+    for (t = 0; t < NTOK; ++t)
+        for (d = 0; d < NCH; ++d)
+            yhat[t * NCH + d] = (double)c32[d] * ((double)s32[t] * q[t * NCH + d] + (double)z32[t]);
+}
+
+/* ------------------------------------------------------------------ */
+/* One tile through all four stages                                    */
+/* ------------------------------------------------------------------ */
+
+/* Quantizes one 128x128 fp16 tile (token t at x + t*ld_tok) and packs it into
+ * the K (is_v = 0, 4 bits) or V (is_v = 1, 2 bits) part of `rec`.  The
+ * optional outputs expose every intermediate for the tests:
+ * Y (rotated), a, b (log scales), q (codes), u (pre-rounding values). */
+void kvref_quantize_tile(const uint16_t *x, long ld_tok, int is_v, int iters, uint8_t *rec,
+                         double *Y_out, double *a_out, double *b_out, uint8_t *q_out,
+                         double *u_out)
+{
+    static double H[NCH * NCH];
+    static int have_h = 0;
+    double *Y = (double *)malloc(sizeof(double) * NTOK * NCH);
+    double a[NTOK], b[NCH], r[NTOK];
+    float c32[NCH], s32[NTOK], z32[NTOK];
+    uint8_t q[NTOK * NCH];
+    int t, d, bits = is_v ? 2 : 4;
+#pragma omp critical(kvref_h)
+    {
+        if (!have_h) {
+            kvref_hadamard(NCH, H);
+            have_h = 1;
+        }
+    }
+    kvref_rotate_tile(x, ld_tok, H, Y);
+    kvref_sinkhorn(Y, iters, a, b, NULL);
+    for (t = 0; t < NTOK; ++t) r[t] = exp(a[t]);
+    for (d = 0; d < NCH; ++d) c32[d] = (float)exp(b[d]);
+    kvref_rtn(Y, r, c32, bits, q, s32, z32, u_out);
+    if (rec) kvref_pack_part(rec, is_v, q, s32, z32, c32);
+    if (Y_out) memcpy(Y_out, Y, sizeof(double) * NTOK * NCH);
+    if (a_out) memcpy(a_out, a, sizeof(a));
+    if (b_out) memcpy(b_out, b, sizeof(b));
+    if (q_out) memcpy(q_out, q, sizeof(q));
+    free(Y);
+}
+
+/* ------------------------------------------------------------------ */
+/* Prefill: every full 128-token block into its page, the rest to the tail */
+/* Paging: "KV Cache (Anahtar-Deger Onbellegi)", "Paged Attention (vLLM)". */
+/* ------------------------------------------------------------------ */
+
+/* k, v: fp16 [B][S][Hkv][128] addressed with element strides sb, st, sh.
+ * block_table: [B][max_blocks] page ids.  pool: [num_pages][Hkv][15360].
+ * tail_k, tail_v: fp16 [B][Hkv][128 slots][128].  u_k, u_v (nullable):
+ * pre-rounding values, [B][max_blocks][Hkv][128][128] doubles, for the
+ * boundary rule.  Returns 0, or -1 on a page id outside [0, num_pages). */
+int kvref_quantize_blocks(const uint16_t *k, const uint16_t *v, long sb, long st, long sh,
+                          int B, const int32_t *seq_lens, const int32_t *block_table,
+                          int max_blocks, int hkv, int iters, uint8_t *pool, long num_pages,
+                          uint16_t *tail_k, uint16_t *tail_v, double *u_k, double *u_v)
+{
+    int bad = 0;
+    long item, n_items = (long)B * max_blocks * hkv;
+#pragma omp parallel for schedule(dynamic, 4) reduction(| : bad)
+    for (item = 0; item < n_items; ++item) {
+        int b = (int)(item / ((long)max_blocks * hkv));
+        int j = (int)((item / hkv) % max_blocks);
+        int h = (int)(item % hkv);
+        int nfull = seq_lens[b] / NTOK;
+        long page;
+        uint8_t *rec;
+        long uoff = (((long)b * max_blocks + j) * hkv + h) * NTOK * NCH;
+        if (j >= nfull) continue;
+        page = block_table[(long)b * max_blocks + j];
+        if (page < 0 || page >= num_pages) { bad = 1; continue; }
+        rec = pool + (page * hkv + h) * (long)REC_BYTES;
+        kvref_quantize_tile(k + b * sb + (long)j * NTOK * st + h * sh, st, 0, iters, rec, NULL,
+                            NULL, NULL, NULL, u_k ? u_k + uoff : NULL);
+        kvref_quantize_tile(v + b * sb + (long)j * NTOK * st + h * sh, st, 1, iters, rec, NULL,
+                            NULL, NULL, NULL, u_v ? u_v + uoff : NULL);
+    }
+    {
+        int b, h, s, d;
+        for (b = 0; b < B; ++b) {
+            int nfull = seq_lens[b] / NTOK, rem = seq_lens[b] % NTOK;
+            for (h = 0; h < hkv; ++h)
+                for (s = 0; s < rem; ++s) {
+                    long src = b * sb + ((long)nfull * NTOK + s) * st + h * sh;
+                    long dst = (((long)b * hkv + h) * NTOK + s) * NCH;
+                    for (d = 0; d < NCH; ++d) {
+                        tail_k[dst + d] = k[src + d];
+                        tail_v[dst + d] = v[src + d];
+                    }
+                }
+        }
+    }
+    return bad ? -1 : 0;
+}
+
+/* Decode-time append: token `pos[b]` (the length before the append) goes to
+ * tail slot pos mod 128; when that slot is 127 the now-full tail is quantized
+ * into page block_table[b][pos / 128].  pos < 0 marks an idle slot. */
+int kvref_append_token(const uint16_t *k_new, const uint16_t *v_new, const int32_t *pos, int B,
+                       const int32_t *block_table, int max_blocks, int hkv, int iters,
+                       uint8_t *pool, long num_pages, uint16_t *tail_k, uint16_t *tail_v)
+{
+    int b, bad = 0;
+    for (b = 0; b < B; ++b) {
+        int p = pos[b], h, d, slot;
+        if (p < 0) continue;
+        slot = p % NTOK;
+        for (h = 0; h < hkv; ++h) {
+            long dst = (((long)b * hkv + h) * NTOK + slot) * NCH;
+            long src = ((long)b * hkv + h) * NCH;
+            for (d = 0; d < NCH; ++d) {
+                tail_k[dst + d] = k_new[src + d];
+                tail_v[dst + d] = v_new[src + d];
+            }
+        }
+        if (slot == NTOK - 1) {
+            long page;
+            if (p / NTOK >= max_blocks) { bad = 1; continue; }
+            page = block_table[(long)b * max_blocks + p / NTOK];
+            if (page < 0 || page >= num_pages) { bad = 1; continue; }
+            for (h = 0; h < hkv; ++h) {
+                uint8_t *rec = pool + (page * hkv + h) * (long)REC_BYTES;
+                const uint16_t *tk = tail_k + ((long)b * hkv + h) * NTOK * NCH;
+                const uint16_t *tv = tail_v + ((long)b * hkv + h) * NTOK * NCH;
+                kvref_quantize_tile(tk, NCH, 0, iters, rec, NULL, NULL, NULL, NULL, NULL);
+                kvref_quantize_tile(tv, NCH, 1, iters, rec, NULL, NULL, NULL, NULL, NULL);
+            }
+        }
+    }
+    return bad ? -1 : 0;
+}
+
+/* ------------------------------------------------------------------ */
+/* Decode attention over quantized pages plus the fp16 tail            */
+/* "KV Cache (Anahtar-Deger Onbellegi)", "KV Cache Nasil Calisir?": one new */
+/* token attends to every cached K,V; grouped heads per the GQA answer in */
+/* "Sik Sorulan Sorular".  Rotation invariance: KVarN page, stage 2.      */
+/* ------------------------------------------------------------------ */
+
+/* route 0 (textbook): x_hat = H yhat for every cached token, then
+ *   o = softmax(scale * q . x_hat) V_hat with the fp16 tail appended.
+ * route 1 (rotated): q_rot = H q, scores from yhat directly, the value sum
+ *   accumulated in rotated space and rotated back once: o = H o_rot + o_tail.
+ * q: fp16 [B][Hq][128].  out: double [B][Hq][128].  A sequence of length 0
+ * yields a zero output.  Returns -1 on a page id outside [0, num_pages). */
+int kvref_decode_attention(const uint16_t *q, const uint8_t *pool, long num_pages,
+                           const int32_t *block_table, int max_blocks, const int32_t *seq_lens,
+                           int B, int hq, int hkv, const uint16_t *tail_k, const uint16_t *tail_v,
+                           double scale, int route, double *out)
+{
+    static double H[NCH * NCH];
+    static int have_h = 0;
+    int bad = 0;
+    long item, n_items = (long)B * hq;
+    int g = hq / hkv;
+#pragma omp critical(kvref_h)
+    {
+        if (!have_h) {
+            kvref_hadamard(NCH, H);
+            have_h = 1;
+        }
+    }
+#pragma omp parallel for schedule(dynamic, 1) reduction(| : bad)
+    for (item = 0; item < n_items; ++item) {
+        int b = (int)(item / hq), h = (int)(item % hq), kvh = h / g;
+        int len = seq_lens[b], nfull = len / NTOK, rem = len % NTOK;
+        double qv[NCH], qr[NCH], acc[NCH], acc_tail[NCH];
+        double *scores = (double *)malloc(sizeof(double) * (len > 0 ? len : 1));
+        double *yk = (double *)malloc(sizeof(double) * NTOK * NCH);
+        double *yv = (double *)malloc(sizeof(double) * NTOK * NCH);
+        double mx = -INFINITY, l = 0.0, xk[NCH];
+        int j, t, d, e, pagebad = 0;
+        for (d = 0; d < NCH; ++d) qv[d] = kvref_half_to_double(q[item * NCH + d]);
+        for (d = 0; d < NCH; ++d) {
+            double s = 0.0;
+            for (e = 0; e < NCH; ++e) s += H[d * NCH + e] * qv[e];
+            qr[d] = s;
+        }
+        /* pass 1: scores */
+        for (j = 0; j < nfull; ++j) {
+            long page = block_table[(long)b * max_blocks + j];
+            if (page < 0 || page >= num_pages) { pagebad = 1; break; }
+            kvref_dequant_part(pool + (page * hkv + kvh) * (long)REC_BYTES, 0, yk);
+            for (t = 0; t < NTOK; ++t) {
+                double s = 0.0;
+                if (route == 0) {
+                    for (d = 0; d < NCH; ++d) {
+                        double x = 0.0;
+                        for (e = 0; e < NCH; ++e) x += H[d * NCH + e] * yk[t * NCH + e];
+                        xk[d] = x;
+                    }
+                    for (d = 0; d < NCH; ++d) s += qv[d] * xk[d];
+                } else {
+                    for (d = 0; d < NCH; ++d) s += qr[d] * yk[t * NCH + d];
+                }
+                scores[j * NTOK + t] = s * scale;
+            }
+        }
+        if (pagebad) {
+            bad = 1;
+            for (d = 0; d < NCH; ++d) out[item * NCH + d] = NAN;
+            free(scores); free(yk); free(yv);
+            continue;
+        }
+        for (t = 0; t < rem; ++t) {
+            const uint16_t *kt = tail_k + (((long)b * hkv + kvh) * NTOK + t) * NCH;
+            double s = 0.0;
+            for (d = 0; d < NCH; ++d) s += qv[d] * kvref_half_to_double(kt[d]);
+            scores[nfull * NTOK + t] = s * scale;
+        }
+        for (t = 0; t < len; ++t) if (scores[t] > mx) mx = scores[t];
+        for (t = 0; t < len; ++t) { scores[t] = exp(scores[t] - mx); l += scores[t]; }
+        /* pass 2: weighted value sum */
+        for (d = 0; d < NCH; ++d) { acc[d] = 0.0; acc_tail[d] = 0.0; }
+        for (j = 0; j < nfull; ++j) {
+            long page = block_table[(long)b * max_blocks + j];
+            kvref_dequant_part(pool + (page * hkv + kvh) * (long)REC_BYTES, 1, yv);
+            for (t = 0; t < NTOK; ++t) {
+                double p = scores[j * NTOK + t];
+                if (route == 0) {
+                    for (d = 0; d < NCH; ++d) {
+                        double x = 0.0;
+                        for (e = 0; e < NCH; ++e) x += H[d * NCH + e] * yv[t * NCH + e];
+                        acc[d] += p * x;
+                    }
+                } else {
+                    for (d = 0; d < NCH; ++d) acc[d] += p * yv[t * NCH + d];
+                }
+            }
+        }
+        for (t = 0; t < rem; ++t) {
+            const uint16_t *vt = tail_v + (((long)b * hkv + kvh) * NTOK + t) * NCH;
+            double p = scores[nfull * NTOK + t];
+            for (d = 0; d < NCH; ++d) acc_tail[d] += p * kvref_half_to_double(vt[d]);
+        }
+        for (d = 0; d < NCH; ++d) {
+            double o;
+            if (len == 0) { out[item * NCH + d] = 0.0; continue; }
+            if (route == 0) {
+                o = acc[d] + acc_tail[d];
+            } else {
+                double x = 0.0;
+                for (e = 0; e < NCH; ++e) x += H[d * NCH + e] * acc[e];
+                o = x + acc_tail[d];
+            }
+            out[item * NCH + d] = o / l;
+        }
+        free(scores); free(yk); free(yv);
+    }
+    return bad ? -1 : 0;
+}

@@ -1,0 +1,230 @@
+"""Python face of the float64 CPU oracle (``kvref.c``).
+
+TEST INFRASTRUCTURE ONLY.  Only the tests, ``__graft_entry__.smoke()`` and the
+CPU-baseline leg of ``bench.py`` may import this module.  It does not import
+the product package and the product package does not import it; the two sides
+share nothing but the seeded input generators in ``workloads/``.
+
+What the oracle computes, and where each step comes from, is written in the
+header of ``kvref.c``: the four stages of "KVarN Nasil Calisir?" (How KVarN
+works) on the KVarN page (blog.edumints.com) and decode attention over a paged
+cache as in "KV Cache (Anahtar-Deger Onbellegi)" (yapayzekasozluk.tr).
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+
+import numpy as np
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(HERE, "libkvref.so")
+SRC_PATH = os.path.join(HERE, "kvref.c")
+
+NCH = 128
+NTOK = 128
+REC_BYTES = 15360
+
+_lib = None
+
+
+def build(force: bool = False) -> str:
+    """Compile kvref.c with gcc (-O2, OpenMP, no intrinsics) into libkvref.so."""
+    if force or not os.path.exists(LIB_PATH) or os.path.getmtime(LIB_PATH) < os.path.getmtime(SRC_PATH):
+        cmd = ["gcc", "-O2", "-std=c99", "-fopenmp", "-fPIC", "-shared", "-fno-fast-math",
+               "-ffp-contract=off", SRC_PATH, "-o", LIB_PATH + ".tmp", "-lm"]
+        subprocess.check_call(cmd)
+        os.replace(LIB_PATH + ".tmp", LIB_PATH)
+    return LIB_PATH
+
+
+def lib():
+    global _lib
+    if _lib is None:
+        build()
+        L = ctypes.CDLL(LIB_PATH)
+        P = ctypes.c_void_p
+        L.kvref_half_to_double.restype = ctypes.c_double
+        L.kvref_half_to_double.argtypes = [ctypes.c_uint16]
+        L.kvref_hadamard.argtypes = [ctypes.c_int, P]
+        L.kvref_rotate_tile.argtypes = [P, ctypes.c_long, P, P]
+        L.kvref_sinkhorn.argtypes = [P, ctypes.c_int, P, P, P]
+        L.kvref_rtn.argtypes = [P, P, P, ctypes.c_int, P, P, P, P]
+        L.kvref_pack_part.argtypes = [P, ctypes.c_int, P, P, P, P]
+        L.kvref_unpack_part.argtypes = [P, ctypes.c_int, P, P, P, P]
+        L.kvref_dequant_part.argtypes = [P, ctypes.c_int, P]
+        L.kvref_quantize_tile.argtypes = [P, ctypes.c_long, ctypes.c_int, ctypes.c_int, P, P, P,
+                                          P, P, P]
+        L.kvref_quantize_blocks.restype = ctypes.c_int
+        L.kvref_quantize_blocks.argtypes = [P, P, ctypes.c_long, ctypes.c_long, ctypes.c_long,
+                                            ctypes.c_int, P, P, ctypes.c_int, ctypes.c_int,
+                                            ctypes.c_int, P, ctypes.c_long, P, P, P, P]
+        L.kvref_append_token.restype = ctypes.c_int
+        L.kvref_append_token.argtypes = [P, P, P, ctypes.c_int, P, ctypes.c_int, ctypes.c_int,
+                                         ctypes.c_int, P, ctypes.c_long, P, P]
+        L.kvref_decode_attention.restype = ctypes.c_int
+        L.kvref_decode_attention.argtypes = [P, P, ctypes.c_long, P, ctypes.c_int, P,
+                                             ctypes.c_int, ctypes.c_int, ctypes.c_int, P, P,
+                                             ctypes.c_double, ctypes.c_int, P]
+        _lib = L
+    return _lib
+
+
+def _p(a):
+    return None if a is None else a.ctypes.data_as(ctypes.c_void_p)
+
+
+def _c(a, dtype):
+    return np.ascontiguousarray(a, dtype=dtype)
+
+
+def _bits16(x):
+    """fp16 array (or uint16 bit patterns) -> contiguous uint16 bit patterns."""
+    x = np.asarray(x)
+    if x.dtype == np.float16:
+        return np.ascontiguousarray(x).view(np.uint16)
+    return _c(x, np.uint16)
+
+
+# ---------------------------------------------------------------- stages --
+
+def half_to_double(bits: int) -> float:
+    return lib().kvref_half_to_double(int(bits))
+
+
+def hadamard(n: int = NCH) -> np.ndarray:
+    H = np.zeros((n, n), dtype=np.float64)
+    lib().kvref_hadamard(n, _p(H))
+    return H
+
+
+def rotate_tile(x) -> np.ndarray:
+    """Stage 2 on one 128x128 fp16 tile: rows y_t = H x_t (float64)."""
+    xb = _bits16(x).reshape(NTOK, NCH)
+    H = hadamard(NCH)
+    Y = np.zeros((NTOK, NCH), dtype=np.float64)
+    lib().kvref_rotate_tile(_p(xb), NCH, _p(H), _p(Y))
+    return Y
+
+
+def sinkhorn(Y, iters: int):
+    """Stage 3: log row scales a, log column scales b, and the per-iteration
+    trace [iters][4] = (row max|log sigma|, row spread, column max|log sigma|,
+    column spread)."""
+    Y = _c(Y, np.float64).reshape(NTOK, NCH)
+    a = np.zeros(NTOK)
+    b = np.zeros(NCH)
+    tr = np.zeros(max(4 * iters, 1))
+    lib().kvref_sinkhorn(_p(Y), iters, _p(a), _p(b), _p(tr))
+    return a, b, tr[:4 * iters].reshape(iters, 4)
+
+
+def rtn(Y, r, c32, bits: int):
+    """Stage 4: codes q, fp32 s', z' and pre-rounding u."""
+    Y = _c(Y, np.float64).reshape(NTOK, NCH)
+    r = _c(r, np.float64)
+    c32 = _c(c32, np.float32)
+    q = np.zeros((NTOK, NCH), dtype=np.uint8)
+    s = np.zeros(NTOK, dtype=np.float32)
+    z = np.zeros(NTOK, dtype=np.float32)
+    u = np.zeros((NTOK, NCH), dtype=np.float64)
+    lib().kvref_rtn(_p(Y), _p(r), _p(c32), bits, _p(q), _p(s), _p(z), _p(u))
+    return q, s, z, u
+
+
+def pack_part(rec, is_v: bool, q, s32, z32, c32):
+    lib().kvref_pack_part(_p(rec), int(is_v), _p(_c(q, np.uint8)), _p(_c(s32, np.float32)),
+                          _p(_c(z32, np.float32)), _p(_c(c32, np.float32)))
+
+
+def unpack_part(rec, is_v: bool):
+    q = np.zeros((NTOK, NCH), dtype=np.uint8)
+    s = np.zeros(NTOK, dtype=np.float32)
+    z = np.zeros(NTOK, dtype=np.float32)
+    c = np.zeros(NCH, dtype=np.float32)
+    lib().kvref_unpack_part(_p(_c(rec, np.uint8)), int(is_v), _p(q), _p(s), _p(z), _p(c))
+    return q, s, z, c
+
+
+def dequant_part(rec, is_v: bool) -> np.ndarray:
+    y = np.zeros((NTOK, NCH), dtype=np.float64)
+    lib().kvref_dequant_part(_p(_c(rec, np.uint8)), int(is_v), _p(y))
+    return y
+
+
+def quantize_tile(x, is_v: bool, iters: int):
+    """All four stages on one tile; returns a dict of every intermediate."""
+    xb = _bits16(x).reshape(NTOK, NCH)
+    rec = np.zeros(REC_BYTES, dtype=np.uint8)
+    Y = np.zeros((NTOK, NCH))
+    a = np.zeros(NTOK)
+    b = np.zeros(NCH)
+    q = np.zeros((NTOK, NCH), dtype=np.uint8)
+    u = np.zeros((NTOK, NCH))
+    lib().kvref_quantize_tile(_p(xb), NCH, int(is_v), iters, _p(rec), _p(Y), _p(a), _p(b),
+                              _p(q), _p(u))
+    return {"rec": rec, "Y": Y, "a": a, "b": b, "q": q, "u": u}
+
+
+# ------------------------------------------------------------ whole ops --
+
+def quantize_blocks(k, v, seq_lens, block_table, num_pages: int, iters: int, pool=None,
+                    tail_k=None, tail_v=None, want_u: bool = False):
+    """Prefill: k, v fp16 [B][S][Hkv][128] (contiguous).  Returns a dict with
+    the pool [num_pages][Hkv][15360] uint8, the fp16 tails [B][Hkv][128][128]
+    and, with want_u, the pre-rounding values [B][max_blocks][Hkv][128][128]."""
+    kb = _bits16(k)
+    vb = _bits16(v)
+    B, S, hkv, d = kb.shape
+    assert d == NCH
+    seq_lens = _c(seq_lens, np.int32)
+    block_table = _c(block_table, np.int32)
+    max_blocks = block_table.shape[1]
+    if pool is None:
+        pool = np.zeros((num_pages, hkv, REC_BYTES), dtype=np.uint8)
+    if tail_k is None:
+        tail_k = np.zeros((B, hkv, NTOK, NCH), dtype=np.uint16)
+    if tail_v is None:
+        tail_v = np.zeros((B, hkv, NTOK, NCH), dtype=np.uint16)
+    u_k = u_v = None
+    if want_u:
+        u_k = np.zeros((B, max_blocks, hkv, NTOK, NCH))
+        u_v = np.zeros((B, max_blocks, hkv, NTOK, NCH))
+    rc = lib().kvref_quantize_blocks(_p(kb), _p(vb), S * hkv * NCH, hkv * NCH, NCH, B,
+                                     _p(seq_lens), _p(block_table), max_blocks, hkv, iters,
+                                     _p(pool), num_pages, _p(tail_k), _p(tail_v), _p(u_k),
+                                     _p(u_v))
+    return {"rc": rc, "pool": pool, "tail_k": tail_k, "tail_v": tail_v, "u_k": u_k, "u_v": u_v}
+
+
+def append_token(k_new, v_new, pos, block_table, iters: int, pool, tail_k, tail_v):
+    """Decode-time append (in place on pool / tails).  Returns the status."""
+    kb = _bits16(k_new)
+    vb = _bits16(v_new)
+    B, hkv, d = kb.shape
+    pos = _c(pos, np.int32)
+    block_table = _c(block_table, np.int32)
+    assert pool.flags["C_CONTIGUOUS"] and tail_k.flags["C_CONTIGUOUS"]
+    return lib().kvref_append_token(_p(kb), _p(vb), _p(pos), B, _p(block_table),
+                                    block_table.shape[1], hkv, iters, _p(pool), pool.shape[0],
+                                    _p(tail_k), _p(tail_v))
+
+
+def decode_attention(q, pool, block_table, seq_lens, tail_k, tail_v, hq: int, hkv: int,
+                     scale: float = 1.0 / np.sqrt(128.0), route: int = 1):
+    """Decode attention, float64 output [B][Hq][128].  route 0 = textbook
+    (un-rotate every token), route 1 = rotated space with one final H."""
+    qb = _bits16(q)
+    B = qb.shape[0]
+    pool = _c(pool, np.uint8)
+    block_table = _c(block_table, np.int32)
+    seq_lens = _c(seq_lens, np.int32)
+    out = np.zeros((B, hq, NCH))
+    rc = lib().kvref_decode_attention(_p(qb), _p(pool), pool.shape[0], _p(block_table),
+                                      block_table.shape[1], _p(seq_lens), B, hq, hkv,
+                                      _p(_bits16(tail_k)), _p(_bits16(tail_v)), float(scale),
+                                      int(route), _p(out))
+    if rc != 0:
+        raise ValueError("oracle: page id outside the pool")
+    return out
