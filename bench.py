@@ -1,0 +1,430 @@
+"""Throughput of the KVarN-style quantized KV-cache hot path on B300.
+
+One step = the whole path over one batch of the workload:
+  kvarn_quantize_blocks (prefill: rotate, normalize, RTN, pack every block)
+  -> kvarn_append_token (one new token per sequence)
+  -> kvarn_decode_attention (one query token per sequence over pages + tail).
+
+Default workload: the Llama-3-8B-like layer (8 KV heads, 32 query heads,
+batch 16 x 4096 tokens, head_dim 128), synthetic seeded data.
+
+Timing: each kernel is bracketed by CUDA events on the stream it runs on; L2
+is flushed (a 512 MB write) before every kernel so no kernel reads what the
+previous one left in L2.  ms_per_step = sum of the three kernels' device times.
+value = algorithmic bytes of the step / ms_per_step (GB/s).
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
+  python bench.py --impl reference ...   (the float64 CPU oracle as the
+                                          reference arm, on a bounded sample)
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+import torch  # noqa: E402
+
+from workloads import synth  # noqa: E402
+
+D = 128
+T = 128
+REC = 15360
+# algorithmic bytes per token-head (K+V): fp16 in, packed out
+FP16_TOKEN_HEAD = 512
+PACKED_TOKEN_HEAD = 120
+METRIC = "decode-attn KV GB/s & tokens/s, quantize GB/s, as % of B300 HBM roofline"
+
+
+# ------------------------------------------------------------------ utils --
+
+def measured_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    return 6400.0, "fallback"
+
+
+def source_hash(name):
+    p = os.path.join(ROOT, "quantized_decode_attention_blocks_b300", "csrc", name)
+    with open(p, "rb") as f:
+        return hashlib.sha256(f.read()).hexdigest()[:16]
+
+
+def ncu_traffic(kernel_key, src_name):
+    """Per-launch DRAM bytes recorded from an ncu capture (profiles/traffic.json),
+    or None when absent or when the kernel source changed since the capture."""
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(p):
+        return None
+    with open(p) as f:
+        d = json.load(f)
+    e = d.get(kernel_key)
+    if not e or e.get("source_sha256_16") != source_hash(src_name):
+        return None
+    return e.get("dram_bytes_per_launch")
+
+
+class ClockSampler:
+    """Samples nvidia-smi SM clocks and throttle reasons during the timed region."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index=0):
+        self.index = index
+        self.proc = None
+        self.lines = []
+        self.thread = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"], stdout=subprocess.PIPE,
+                stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        if self.thread:
+            self.thread.join(timeout=2)
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in self.lines:
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) != 6:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                mx.append(float(parts[1]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[2:]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ----------------------------------------------------------- GPU workload --
+
+class Job:
+    """Device-resident inputs and state of one replica of the workload."""
+
+    def __init__(self, w, dev, seed_offset=0):
+        import quantized_decode_attention_blocks_b300 as kv
+        self.kv = kv
+        self.w = w
+        self.dev = dev
+        if seed_offset:
+            w = synth.scaled(w, seed=w.seed + 1000 * seed_offset)
+        self.cfg = kv.config_from_string("k4v2_g128", w.hq, w.hkv)
+        self.k, self.v = synth.kv(w, device=dev)
+        self.lens = synth.seq_lens(w, device=dev)
+        tables, self.num_pages = synth.block_tables(w, device=dev)
+        self.table = tables[0].contiguous()
+        self.max_seq = w.seq
+        self.pool = kv.alloc_pool(self.cfg, self.num_pages, dev)
+        self.tk, self.tv = kv.alloc_tails(self.cfg, w.batch, dev)
+        self.kn, self.vn = synth.new_tokens(w, 0, device=dev)
+        self.q = synth.queries(w, device=dev)
+        self.out = torch.empty((w.batch, w.hq, D), dtype=torch.float16, device=dev)
+        self.lens1 = self.lens + 1
+        self.ws = kv.alloc_decode_workspace(self.cfg, w.batch, self.max_seq + 1, dev)
+        self.status = torch.zeros(1, dtype=torch.int32, device=dev)
+        lens = self.lens.cpu().numpy().astype(np.int64)
+        nfull = lens // T
+        self.bytes_quantize = int(((nfull * T) * w.hkv).sum() * (FP16_TOKEN_HEAD + PACKED_TOKEN_HEAD)
+                                  + ((lens % T) * w.hkv).sum() * 2 * FP16_TOKEN_HEAD)
+        # append: read k_new, v_new and write the tail slot (a fill adds a quantize)
+        fills = int(((lens % T) == T - 1).sum())
+        self.bytes_append = int(w.batch * w.hkv * 2 * 2 * D * 2
+                                + fills * w.hkv * (T * FP16_TOKEN_HEAD + REC))
+        lens1 = lens + 1
+        self.decode_pages = int((lens1 // T).sum()) * w.hkv
+        self.decode_tail = int((lens1 % T).sum()) * w.hkv
+        self.bytes_decode = int(self.decode_pages * REC + self.decode_tail * FP16_TOKEN_HEAD
+                                + 2 * w.batch * w.hq * D * 2)
+        self.kv_tokens = int(lens1.sum())
+
+    def quantize(self):
+        self.kv.kvarn_quantize_blocks(self.cfg, self.k, self.v, self.lens, self.max_seq,
+                                      self.table, self.pool, self.tk, self.tv, self.status)
+
+    def append(self):
+        self.kv.kvarn_append_token(self.cfg, self.kn, self.vn, self.lens, self.table, self.pool,
+                                   self.tk, self.tv, self.status)
+
+    def decode(self):
+        self.kv.kvarn_decode_attention(self.cfg, self.q, self.pool, self.table, self.lens1,
+                                       self.max_seq + 1, self.tk, self.tv, self.out, self.ws,
+                                       status=self.status)
+
+
+def run_gpu(args, rank, world):
+    dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0)))
+    torch.cuda.set_device(dev)
+    w = synth.WORKLOADS[args.workload]
+    job = Job(w, dev, seed_offset=rank)
+    stream = torch.cuda.current_stream()
+    flush = torch.empty(512 * 1024 * 1024, dtype=torch.uint8, device=dev)
+    ops = [("quantize", job.quantize), ("append", job.append), ("decode", job.decode)]
+
+    def step(record):
+        for name, fn in ops:
+            flush.zero_()
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            fn()
+            e1.record(stream)
+            record.append((name, e0, e1))
+
+    for _ in range(args.warmup):
+        step([])
+    torch.cuda.synchronize()
+    if int(job.status.item()) != 0:
+        raise RuntimeError(f"device status {job.status.item()}: "
+                           f"{job.kv.status_string(int(job.status.item()))}")
+    sampler = ClockSampler(dev.index)
+    if rank == 0:
+        sampler.start()
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    rec = []
+    for _ in range(args.steps):
+        step(rec)
+    torch.cuda.synchronize()
+    wall = time.perf_counter() - t0
+    if world > 1:
+        torch.distributed.barrier()
+    clocks = sampler.stop() if rank == 0 else None
+    per = {"quantize": [], "append": [], "decode": []}
+    for name, e0, e1 in rec:
+        per[name].append(e0.elapsed_time(e1))
+    ms = {k: sum(v) / len(v) for k, v in per.items()}
+    ms_step = sum(ms.values())
+    if world > 1:
+        t = torch.tensor([ms_step, ms["quantize"], ms["append"], ms["decode"]], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        ms_step, ms["quantize"], ms["append"], ms["decode"] = [float(x) for x in t.tolist()]
+
+    # end to end through the public API: host buffers, copies inside the region
+    e2e = measure_e2e(job, args, stream)
+
+    return job, ms, ms_step, wall, clocks, e2e
+
+
+def measure_e2e(job, args, stream):
+    kh = job.k.cpu().pin_memory()
+    vh = job.v.cpu().pin_memory()
+    knh = job.kn.cpu().pin_memory()
+    vnh = job.vn.cpu().pin_memory()
+    qh = job.q.cpu().pin_memory()
+    outh = torch.empty(job.out.shape, dtype=torch.float16).pin_memory()
+    kd = torch.empty_like(job.k)
+    vd = torch.empty_like(job.v)
+
+    def step():
+        kd.copy_(kh, non_blocking=True)
+        vd.copy_(vh, non_blocking=True)
+        job.kn.copy_(knh, non_blocking=True)
+        job.vn.copy_(vnh, non_blocking=True)
+        job.q.copy_(qh, non_blocking=True)
+        job.kv.kvarn_quantize_blocks(job.cfg, kd, vd, job.lens, job.max_seq, job.table, job.pool,
+                                     job.tk, job.tv, job.status)
+        job.append()
+        job.decode()
+        outh.copy_(job.out, non_blocking=True)
+
+    for _ in range(max(1, args.warmup)):
+        step()
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    n = max(1, min(args.steps, 5))
+    e0.record(stream)
+    for _ in range(n):
+        step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / n
+    h2d = (kh.numel() + vh.numel() + knh.numel() + vnh.numel() + qh.numel()) * 2
+    d2h = outh.numel() * 2
+    total = job.bytes_quantize + job.bytes_append + job.bytes_decode
+    return {"value": total / (ms * 1e-3) / 1e9, "unit": "GB/s", "ms_per_step": ms,
+            "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h)}
+
+
+# ------------------------------------------------------ CPU (oracle) arm --
+
+def oracle_sample(w, budget_s=12.0):
+    """Times the float64 oracle on a bounded sample of the workload: whole
+    sequences prefilled, then decoded.  Returns (bytes, seconds, cores, text)."""
+    from oracle import kvref
+    cores = len(os.sched_getaffinity(0))
+    os.environ.setdefault("OMP_NUM_THREADS", str(cores))
+    kvref.lib()
+    S = min(w.seq, 2048)
+    nseq = 1
+    total_b = 0
+    total_t = 0.0
+    done = 0
+    t_start = time.perf_counter()
+    while time.perf_counter() - t_start < budget_s:
+        ws = synth.scaled(w, batch=nseq, seq=S, seed=w.seed + done, min_seq=None, layers=1,
+                          table="identity", reserve_tokens=0)
+        k, v = synth.kv(ws)
+        lens = np.full(nseq, S, dtype=np.int32)
+        mb = S // T
+        table = np.arange(nseq * mb, dtype=np.int32).reshape(nseq, mb)
+        q = synth.queries(ws).numpy()
+        t0 = time.perf_counter()
+        st = kvref.quantize_blocks(k.numpy(), v.numpy(), lens, table, nseq * mb, 2)
+        kvref.decode_attention(q, st["pool"], table, lens, st["tail_k"], st["tail_v"], w.hq,
+                               w.hkv, route=1)
+        total_t += time.perf_counter() - t0
+        total_b += nseq * S * w.hkv * (FP16_TOKEN_HEAD + PACKED_TOKEN_HEAD + PACKED_TOKEN_HEAD)
+        done += 1
+    text = (f"{done} sequence(s) of {S} tokens x {w.hkv} KV heads ({w.hq} query heads): "
+            "oracle prefill quantize + one decode step, float64, OpenMP")
+    return total_b, total_t, cores, text
+
+
+def run_reference(args):
+    w = synth.WORKLOADS[args.workload]
+    vals = []
+    cores = None
+    text = None
+    for i in range(args.warmup + args.steps):
+        b, t, cores, text = oracle_sample(w, budget_s=max(2.0, 20.0 / (args.warmup + args.steps)))
+        if i >= args.warmup:
+            vals.append((b, t))
+    bsum = sum(b for b, _ in vals)
+    tsum = sum(t for _, t in vals)
+    value = bsum / tsum / 1e9
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "GB/s",
+            "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": tsum / len(vals) * 1e3, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": w.name, "batch": w.batch, "seq_len": w.seq,
+                       "kv_heads": w.hkv, "q_heads": w.hq, "head_dim": D,
+                       "sample": text},
+            "cpu_baseline": {"value": value, "unit": "GB/s", "cores": cores, "kind": "oracle",
+                             "sample": text},
+            "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line))
+
+
+# ------------------------------------------------------------------- main --
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", default="kvarn", choices=["kvarn", "reference"])
+    ap.add_argument("--workload", default="llama3_8b_layer", choices=sorted(synth.WORKLOADS))
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    if args.impl == "reference":
+        if rank == 0:
+            run_reference(args)
+        return 0
+    if world > 1:
+        torch.distributed.init_process_group("nccl")
+    job, ms, ms_step, wall, clocks, e2e = run_gpu(args, rank, world)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+    if rank != 0:
+        return 0
+    w = job.w
+    peak, peak_kind = measured_peaks()
+    step_bytes = job.bytes_quantize + job.bytes_append + job.bytes_decode
+    value = world * step_bytes / (ms_step * 1e-3) / 1e9
+    q_gbs = job.bytes_quantize / (ms["quantize"] * 1e-3) / 1e9
+    d_gbs = job.bytes_decode / (ms["decode"] * 1e-3) / 1e9
+    a_gbs = job.bytes_append / (ms["append"] * 1e-3) / 1e9
+    dom = "quantize" if ms["quantize"] >= ms["decode"] else "decode"
+    dom_gbs = q_gbs if dom == "quantize" else d_gbs
+    dom_bytes = job.bytes_quantize if dom == "quantize" else job.bytes_decode
+    traffic_q = ncu_traffic("quantize_blocks_kernel", "quantize.cu")
+    traffic_d = ncu_traffic("decode_kernel", "decode_mma.cu")
+    line = {
+        "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+        "data": "synthetic",
+        "config": {"workload": w.name, "batch": w.batch, "seq_len": w.seq, "kv_heads": w.hkv,
+                   "q_heads": w.hq, "head_dim": D, "format": "kvarn_k4v2_g128",
+                   "sinkhorn_iters": job.cfg.sinkhorn_iters, "parallelism": f"replicas{world}",
+                   "l2": "flushed (512 MB write) before every kernel",
+                   "timing": "sum of per-kernel CUDA-event times"},
+        "ops": {
+            "quantize": {"us": ms["quantize"] * 1e3, "gbs": q_gbs, "frac_of_hbm": q_gbs / peak,
+                         "bytes": job.bytes_quantize},
+            "append": {"us": ms["append"] * 1e3, "gbs": a_gbs, "bytes": job.bytes_append},
+            "decode": {"us": ms["decode"] * 1e3, "gbs": d_gbs, "frac_of_hbm": d_gbs / peak,
+                       "bytes": job.bytes_decode,
+                       "tokens_per_s": w.batch / (ms["decode"] * 1e-3),
+                       "kv_tokens_scanned_per_s": job.kv_tokens / (ms["decode"] * 1e-3)},
+        },
+        "roofline": {"bound": "hbm", "kernel": dom, "achieved": dom_gbs, "peak": peak,
+                     "peak_kind": f"{peak_kind} hbm_gbs (burst copy)", "unit": "GB/s",
+                     "frac": dom_gbs / peak,
+                     "traffic": traffic_q if dom == "quantize" else traffic_d,
+                     "algorithmic_bytes": dom_bytes},
+        "roofline_decode": {"bound": "hbm", "achieved": d_gbs, "peak": peak, "unit": "GB/s",
+                            "frac": d_gbs / peak, "traffic": traffic_d,
+                            "algorithmic_bytes": job.bytes_decode},
+        "e2e": e2e,
+        "gpu_launches": 3 * args.steps,
+        "clocks": clocks,
+        "wall_s_timed_region": wall,
+    }
+    if not args.no_cpu_baseline:
+        b, t, cores, text = oracle_sample(w, budget_s=15.0)
+        line["cpu_baseline"] = {"value": b / t / 1e9, "unit": "GB/s", "cores": cores,
+                                "kind": "oracle", "sample": text}
+    print(json.dumps(line))
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,183 @@
+/*
+ * kvarn.h -- C ABI of the KVarN-style quantized KV cache for B300 (sm_103a).
+ *
+ * What it computes.  "KVarN: Huawei'den KV-Cache Kuantizasyonu icin Yerel vLLM
+ * Backend'i" (blog.edumints.com), section "KVarN Nasil Calisir?" (How KVarN
+ * works): the KV cache is quantized in fixed-size token blocks, and each block
+ * goes through an orthonormal Hadamard rotation along channels, a Sinkhorn-like
+ * row/column variance normalization in the log domain, and asymmetric
+ * round-to-nearest with 4-bit keys and 2-bit values (format kvarn_k4v2_g128,
+ * section "Yazilim Gelistirme ve Ogrenme Acisindan Pratik Cikarimlar").  The
+ * quantized blocks live in a paged pool addressed through a block table, as in
+ * "KV Cache (Anahtar-Deger Onbellegi)" (yapayzekasozluk.tr), section "Paged
+ * Attention (vLLM)"; decode attention reads every cached token of a sequence
+ * for one new query token ("KV Cache Nasil Calisir?"), several query heads
+ * sharing one KV head (GQA, "Sik Sorulan Sorular").
+ *
+ * Fixed readings (the pages leave these open):
+ *   head_dim = block = group = 128; one block = 128 tokens x 128 channels of one
+ *   KV head; K and V are separate tiles.  H = Sylvester Hadamard / sqrt(128),
+ *   y_t = H x_t.  Sinkhorn: rows = tokens, columns = channels, K iterations of
+ *   (row step, column step), each step sets the log scale so that the centred
+ *   population std of Y * exp(-a_t - b_d) becomes 1 along that axis, skipping a
+ *   row/column whose variance is <= 1e-10 * its mean square.  Groups are the 128
+ *   channels of one token: z = min, s = (max - min) / (2^bits - 1),
+ *   q = rint((x - z) / s) (ties to even).  Metadata fp32, row scale folded in:
+ *   dequantized rotated value yhat_td = c_d * (s'_t * q_td + z'_t).
+ *
+ * Page record: one per (page, KV head), KVARN_PAGE_BYTES bytes, 16-byte aligned:
+ *   [0,     8192) K codes, token-major: token t at 64 t; byte j = channel 2j
+ *                 (bits 0-3) | channel 2j+1 (bits 4-7)
+ *   [8192, 12288) V codes, channel-major: channel d at 8192 + 32 d; byte j =
+ *                 tokens 4j..4j+3 in bits 0-1, 2-3, 4-5, 6-7
+ *   [12288,13312) K {s', z'} fp32 per token (token t at 12288 + 8 t)
+ *   [13312,14336) V {s', z'} fp32 per token
+ *   [14336,14848) K column scale c_d fp32
+ *   [14848,15360) V column scale c_d fp32
+ * Pool = [num_pages][num_kv_heads][KVARN_PAGE_BYTES].  The newest len mod 128
+ * tokens of a sequence stay fp16 in a caller-owned tail buffer
+ * [B][num_kv_heads][128 slots][128] per K and V.
+ *
+ * Conventions for every call:
+ *   - the library allocates nothing and keeps no state between calls; every
+ *     pointer is caller-owned DEVICE memory unless stated otherwise;
+ *   - every call is asynchronous on `stream` (a cudaStream_t; NULL = legacy
+ *     default stream) and never synchronises;
+ *   - the return value is KVARN_OK or a negative KVARN_ERR_*; all argument
+ *     checks run on the host before any launch, and a failed check launches
+ *     nothing;
+ *   - errors found on the device (a page id outside [0, num_pages), a length
+ *     beyond the table, a wait that gave up) are OR-ed into `*status`
+ *     (nullable, device int32, caller zeroes it) as KVARN_STATUS_* bits; the
+ *     offending unit is skipped, nothing traps;
+ *   - fp16 means IEEE binary16; all tensors are little-endian and densely
+ *     packed in their last dimension.
+ */
+#ifndef KVARN_H
+#define KVARN_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st *kvarn_stream_t; /* identical to cudaStream_t */
+
+#define KVARN_HEAD_DIM 128
+#define KVARN_BLOCK_TOKENS 128
+#define KVARN_PAGE_BYTES 15360
+
+/* return codes */
+#define KVARN_OK 0
+#define KVARN_ERR_INVALID_ARG (-1) /* null/misaligned pointer, bad size or stride */
+#define KVARN_ERR_UNSUPPORTED (-2) /* a config other than k4v2_g128, head_dim 128 */
+#define KVARN_ERR_WORKSPACE (-3)   /* decode workspace missing or too small */
+#define KVARN_ERR_LAUNCH (-4)      /* the CUDA launch itself failed */
+
+/* device status bits, OR-ed into *status */
+#define KVARN_STATUS_BAD_PAGE 1    /* block-table entry outside [0, num_pages) */
+#define KVARN_STATUS_BAD_LENGTH 2  /* sequence length beyond max_seq or the table */
+#define KVARN_STATUS_TIMEOUT 4     /* a bounded wait on the device gave up */
+
+typedef struct {
+    int head_dim;       /* 128 */
+    int block_tokens;   /* 128 */
+    int group;          /* 128: quantization group = one token's channels */
+    int k_bits;         /* 4 */
+    int v_bits;         /* 2 */
+    int sinkhorn_iters; /* 0..64; 2 from the iteration-selection rule */
+    int num_q_heads;    /* Hq, a multiple of num_kv_heads */
+    int num_kv_heads;   /* Hkv; Hq / Hkv <= 16 */
+} kvarn_config_t;
+
+/* Fills *out from a format string: "k4v2_g128" or "kvarn_k4v2_g128" (the
+ * KVarN page's --kv-cache-dtype value), optionally suffixed "_s<K>" to set the
+ * Sinkhorn iteration count.  Returns KVARN_ERR_UNSUPPORTED for any other
+ * format, KVARN_ERR_INVALID_ARG for bad head counts or a null pointer. */
+int kvarn_config_from_string(const char *s, int num_q_heads, int num_kv_heads,
+                             kvarn_config_t *out);
+
+/* KVARN_OK if the configuration is one this library runs. */
+int kvarn_config_validate(const kvarn_config_t *cfg);
+
+/* Bytes of one page record (per page and KV head): 15360. 0 on a bad config. */
+size_t kvarn_page_bytes(const kvarn_config_t *cfg);
+
+/* Prefill quantization ("KVarN Nasil Calisir?", all four stages).
+ *   k, v        fp16 [B][S][Hkv][128], element (b,t,h,c) at
+ *               b*stride_b + t*stride_t + h*stride_h + c; 16-byte aligned,
+ *               strides multiples of 8 elements
+ *   seq_lens    int32 [batch], tokens of each sequence (<= max_seq)
+ *   max_seq     host upper bound on seq_lens, sizes the grid
+ *   block_table int32 [batch][max_blocks]; block j of sequence b goes to page
+ *               block_table[b*max_blocks + j]; needs max_blocks >= max_seq/128
+ *   pool        [num_pages][Hkv][15360] bytes, written for every full block
+ *   tail_k/_v   fp16 [batch][Hkv][128][128]: the len mod 128 leftover tokens
+ *               of each sequence are copied to slots 0..len%128-1
+ * Every full block of 128 tokens is quantized: K to 4 bits, V to 2 bits. */
+int kvarn_quantize_blocks(const kvarn_config_t *cfg, const void *k, const void *v,
+                          int64_t stride_b, int64_t stride_t, int64_t stride_h, int batch,
+                          const int32_t *seq_lens, int max_seq, const int32_t *block_table,
+                          int max_blocks, void *pool, int64_t num_pages, void *tail_k,
+                          void *tail_v, int32_t *status, kvarn_stream_t stream);
+
+/* Decode-time append of one token per sequence ("KV Cache Nasil Calisir?":
+ * only the new token's K,V are computed and added to the cache).
+ *   k_new, v_new fp16 [batch][Hkv][128]
+ *   pos          int32 [batch]: the sequence length before this append; the
+ *                token goes to tail slot pos % 128; pos < 0 skips the sequence
+ *   When the slot is 127 the full tail is quantized (all four stages) into page
+ *   block_table[b*max_blocks + pos/128] in the same launch, so the page must
+ *   already be in the table.  The caller advances pos / seq_lens afterwards. */
+int kvarn_append_token(const kvarn_config_t *cfg, const void *k_new, const void *v_new,
+                       const int32_t *pos, int batch, const int32_t *block_table,
+                       int max_blocks, void *pool, int64_t num_pages, void *tail_k,
+                       void *tail_v, int32_t *status, kvarn_stream_t stream);
+
+/* Bytes of decode workspace for (batch, max_seq).  0 when no split is needed. */
+size_t kvarn_decode_workspace_bytes(const kvarn_config_t *cfg, int batch, int max_seq);
+
+/* Decode attention for one new query token per sequence:
+ *   out[b][h] = sum_t softmax_t(scale * q[b][h] . k_t) v_t
+ * over the len/128 quantized pages of sequence b (keys and values dequantized
+ * and rotated back: attention scores are unchanged by the orthonormal
+ * rotation, KVarN page stage 2) followed by its len%128 fp16 tail tokens.
+ * Query head h reads KV head h / (Hq/Hkv).
+ *   q          fp16 [batch][Hq][128]
+ *   seq_lens   int32 [batch], total tokens (pages + tail), <= max_seq
+ *   out        fp16 [batch][Hq][128]; a sequence of length 0 gives zeros
+ *   workspace  >= kvarn_decode_workspace_bytes(cfg, batch, max_seq) bytes,
+ *              16-byte aligned, ZERO-FILLED before its first use; every call
+ *              leaves it zero-filled again in its counter region, so one
+ *              buffer serves any number of calls on one stream (calls that
+ *              share a workspace must not overlap on the GPU).
+ * The work is split across CTAs along each sequence's pages (split-K) and the
+ * partial softmax states are merged with a log-sum-exp in the same launch. */
+int kvarn_decode_attention(const kvarn_config_t *cfg, const void *q, const void *pool,
+                           int64_t num_pages, const int32_t *block_table, int max_blocks,
+                           const int32_t *seq_lens, int batch, int max_seq,
+                           const void *tail_k, const void *tail_v, float softmax_scale,
+                           void *out, void *workspace, size_t workspace_bytes,
+                           int32_t *status, kvarn_stream_t stream);
+
+/* Diagnosis: dequantizes `n` page records into float32 rotated-space tiles.
+ *   records   [n][15360] bytes (e.g. pool + page*Hkv*15360, one record per
+ *             (page, head) in order)
+ *   yk, yv    float32 [n][128 tokens][128 channels]:
+ *             yhat_td = c_d * (s'_t * q_td + z'_t) */
+int kvarn_dequantize_pages(const void *records, int64_t n, float *yk, float *yv,
+                           kvarn_stream_t stream);
+
+/* Static text for a return code or a status bit set. */
+const char *kvarn_status_string(int code);
+
+/* Library version, "major.minor.patch". */
+const char *kvarn_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* KVARN_H */

@@ -1,0 +1,241 @@
+// api.cu -- the extern "C" boundary of libkvarn (declared in include/kvarn.h):
+// argument validation on the host, the split-K plan, launch dispatch.
+// Nothing here allocates memory or keeps state between calls.
+#include <string.h>
+
+#include "kvarn_internal.cuh"
+
+namespace kvarn {
+
+cudaError_t launch_decode_simple(const DecodeArgs& a, cudaStream_t s);
+cudaError_t launch_decode_mma(const DecodeArgs& a, cudaStream_t s);
+bool decode_mma_supported(int g);
+
+static inline bool aligned16(const void* p) { return ((uintptr_t)p & 15u) == 0; }
+
+DecodePlan decode_plan(int batch, int hq, int hkv, int max_seq) {
+  DecodePlan p{};
+  const int64_t units = (int64_t)max_seq / kT + 1;             // pages + the tail
+  const int64_t total = (int64_t)batch * hkv * units;
+  int64_t pps = (total + kNumSMs * 16 - 1) / (kNumSMs * 16);   // ~16 CTAs per SM
+  if (pps < 4) pps = 4;
+  if (pps > 64) pps = 64;
+  p.pages_per_split = (int)pps;
+  p.nsplit = (int)((units + pps - 1) / pps);
+  if (p.nsplit > 1) {
+    p.part_bytes = (size_t)batch * hq * p.nsplit * (2 + kD) * sizeof(float);
+    p.part_bytes = (p.part_bytes + 255) & ~(size_t)255;
+    p.count_bytes = ((size_t)batch * hkv * sizeof(int) + 255) & ~(size_t)255;
+  }
+  return p;
+}
+
+}  // namespace kvarn
+
+using namespace kvarn;
+
+extern "C" {
+
+int kvarn_config_validate(const kvarn_config_t* c) {
+  if (!c) return KVARN_ERR_INVALID_ARG;
+  if (c->num_q_heads <= 0 || c->num_kv_heads <= 0 || c->num_q_heads % c->num_kv_heads)
+    return KVARN_ERR_INVALID_ARG;
+  if (c->num_q_heads / c->num_kv_heads > kMaxG) return KVARN_ERR_UNSUPPORTED;
+  if (c->head_dim != kD || c->block_tokens != kT || c->group != kD || c->k_bits != 4 ||
+      c->v_bits != 2)
+    return KVARN_ERR_UNSUPPORTED;
+  if (c->sinkhorn_iters < 0 || c->sinkhorn_iters > kMaxIters) return KVARN_ERR_UNSUPPORTED;
+  return KVARN_OK;
+}
+
+int kvarn_config_from_string(const char* s, int hq, int hkv, kvarn_config_t* out) {
+  if (!s || !out) return KVARN_ERR_INVALID_ARG;
+  if (!strncmp(s, "kvarn_", 6)) s += 6;
+  if (strncmp(s, "k4v2_g128", 9)) return KVARN_ERR_UNSUPPORTED;
+  int iters = 2;
+  const char* rest = s + 9;
+  if (*rest) {
+    if (rest[0] != '_' || rest[1] != 's' || !rest[2]) return KVARN_ERR_UNSUPPORTED;
+    int v = 0;
+    for (const char* p = rest + 2; *p; ++p) {
+      if (*p < '0' || *p > '9' || v > kMaxIters) return KVARN_ERR_UNSUPPORTED;
+      v = v * 10 + (*p - '0');
+    }
+    iters = v;
+  }
+  kvarn_config_t c;
+  c.head_dim = kD;
+  c.block_tokens = kT;
+  c.group = kD;
+  c.k_bits = 4;
+  c.v_bits = 2;
+  c.sinkhorn_iters = iters;
+  c.num_q_heads = hq;
+  c.num_kv_heads = hkv;
+  const int rc = kvarn_config_validate(&c);
+  if (rc != KVARN_OK) return rc;
+  *out = c;
+  return KVARN_OK;
+}
+
+size_t kvarn_page_bytes(const kvarn_config_t* c) {
+  return kvarn_config_validate(c) == KVARN_OK ? (size_t)kRec : 0;
+}
+
+int kvarn_quantize_blocks(const kvarn_config_t* cfg, const void* k, const void* v,
+                          int64_t stride_b, int64_t stride_t, int64_t stride_h, int batch,
+                          const int32_t* seq_lens, int max_seq, const int32_t* block_table,
+                          int max_blocks, void* pool, int64_t num_pages, void* tail_k,
+                          void* tail_v, int32_t* status, kvarn_stream_t stream) {
+  int rc = kvarn_config_validate(cfg);
+  if (rc != KVARN_OK) return rc;
+  if (batch < 0 || max_seq < 0 || max_blocks < 0 || num_pages < 0) return KVARN_ERR_INVALID_ARG;
+  if (batch == 0 || max_seq == 0) return KVARN_OK;
+  if (!k || !v || !seq_lens || !tail_k || !tail_v) return KVARN_ERR_INVALID_ARG;
+  if (max_seq >= kT && (!block_table || !pool || num_pages <= 0)) return KVARN_ERR_INVALID_ARG;
+  if ((int64_t)max_blocks * kT < (int64_t)(max_seq / kT) * kT) return KVARN_ERR_INVALID_ARG;
+  if (!aligned16(k) || !aligned16(v) || !aligned16(pool) || !aligned16(tail_k) ||
+      !aligned16(tail_v))
+    return KVARN_ERR_INVALID_ARG;
+  if (stride_b < 0 || stride_t < kD || stride_h < kD || (stride_b | stride_t | stride_h) % 8)
+    return KVARN_ERR_INVALID_ARG;
+  if ((int64_t)max_seq / kT + 1 > 65535 || 2 * cfg->num_kv_heads > 65535 || batch > 65535)
+    return KVARN_ERR_UNSUPPORTED;
+  QuantizeArgs a;
+  a.k = static_cast<const __half*>(k);
+  a.v = static_cast<const __half*>(v);
+  a.sb = stride_b;
+  a.st = stride_t;
+  a.sh = stride_h;
+  a.batch = batch;
+  a.hkv = cfg->num_kv_heads;
+  a.iters = cfg->sinkhorn_iters;
+  a.max_seq = max_seq;
+  a.seq_lens = seq_lens;
+  a.block_table = block_table;
+  a.max_blocks = max_blocks;
+  a.pool = static_cast<uint8_t*>(pool);
+  a.num_pages = num_pages;
+  a.tail_k = static_cast<__half*>(tail_k);
+  a.tail_v = static_cast<__half*>(tail_v);
+  a.status = status;
+  return launch_quantize_blocks(a, (cudaStream_t)stream) == cudaSuccess ? KVARN_OK
+                                                                         : KVARN_ERR_LAUNCH;
+}
+
+int kvarn_append_token(const kvarn_config_t* cfg, const void* k_new, const void* v_new,
+                       const int32_t* pos, int batch, const int32_t* block_table,
+                       int max_blocks, void* pool, int64_t num_pages, void* tail_k,
+                       void* tail_v, int32_t* status, kvarn_stream_t stream) {
+  int rc = kvarn_config_validate(cfg);
+  if (rc != KVARN_OK) return rc;
+  if (batch < 0 || max_blocks < 0 || num_pages < 0) return KVARN_ERR_INVALID_ARG;
+  if (batch == 0) return KVARN_OK;
+  if (!k_new || !v_new || !pos || !block_table || !pool || !tail_k || !tail_v ||
+      max_blocks == 0 || num_pages == 0)
+    return KVARN_ERR_INVALID_ARG;
+  if (!aligned16(k_new) || !aligned16(v_new) || !aligned16(pool) || !aligned16(tail_k) ||
+      !aligned16(tail_v))
+    return KVARN_ERR_INVALID_ARG;
+  if (batch > 65535) return KVARN_ERR_UNSUPPORTED;
+  AppendArgs a;
+  a.k_new = static_cast<const __half*>(k_new);
+  a.v_new = static_cast<const __half*>(v_new);
+  a.pos = pos;
+  a.batch = batch;
+  a.hkv = cfg->num_kv_heads;
+  a.iters = cfg->sinkhorn_iters;
+  a.block_table = block_table;
+  a.max_blocks = max_blocks;
+  a.pool = static_cast<uint8_t*>(pool);
+  a.num_pages = num_pages;
+  a.tail_k = static_cast<__half*>(tail_k);
+  a.tail_v = static_cast<__half*>(tail_v);
+  a.status = status;
+  return launch_append_token(a, (cudaStream_t)stream) == cudaSuccess ? KVARN_OK
+                                                                      : KVARN_ERR_LAUNCH;
+}
+
+size_t kvarn_decode_workspace_bytes(const kvarn_config_t* cfg, int batch, int max_seq) {
+  if (kvarn_config_validate(cfg) != KVARN_OK || batch <= 0 || max_seq < 0) return 0;
+  const DecodePlan p = decode_plan(batch, cfg->num_q_heads, cfg->num_kv_heads, max_seq);
+  return p.part_bytes + p.count_bytes;
+}
+
+int kvarn_decode_attention(const kvarn_config_t* cfg, const void* q, const void* pool,
+                           int64_t num_pages, const int32_t* block_table, int max_blocks,
+                           const int32_t* seq_lens, int batch, int max_seq, const void* tail_k,
+                           const void* tail_v, float softmax_scale, void* out, void* workspace,
+                           size_t workspace_bytes, int32_t* status, kvarn_stream_t stream) {
+  int rc = kvarn_config_validate(cfg);
+  if (rc != KVARN_OK) return rc;
+  if (batch < 0 || max_seq < 0 || max_blocks < 0 || num_pages < 0) return KVARN_ERR_INVALID_ARG;
+  if (batch == 0) return KVARN_OK;
+  if (!q || !seq_lens || !tail_k || !tail_v || !out) return KVARN_ERR_INVALID_ARG;
+  if (max_seq >= kT && (!pool || !block_table || num_pages <= 0 || max_blocks < max_seq / kT))
+    return KVARN_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(pool) || !aligned16(tail_k) || !aligned16(tail_v) ||
+      !aligned16(out) || !aligned16(workspace))
+    return KVARN_ERR_INVALID_ARG;
+  if (!(softmax_scale > 0.f) || softmax_scale != softmax_scale) return KVARN_ERR_INVALID_ARG;
+  if (batch > 65535 || cfg->num_kv_heads > 65535) return KVARN_ERR_UNSUPPORTED;
+  const DecodePlan p = decode_plan(batch, cfg->num_q_heads, cfg->num_kv_heads, max_seq);
+  if (p.nsplit > 1 && (!workspace || workspace_bytes < p.part_bytes + p.count_bytes))
+    return KVARN_ERR_WORKSPACE;
+  DecodeArgs a;
+  a.q = static_cast<const __half*>(q);
+  a.pool = static_cast<const uint8_t*>(pool);
+  a.num_pages = num_pages;
+  a.block_table = block_table;
+  a.max_blocks = max_blocks;
+  a.seq_lens = seq_lens;
+  a.batch = batch;
+  a.max_seq = max_seq;
+  a.hq = cfg->num_q_heads;
+  a.hkv = cfg->num_kv_heads;
+  a.g = cfg->num_q_heads / cfg->num_kv_heads;
+  a.tail_k = static_cast<const __half*>(tail_k);
+  a.tail_v = static_cast<const __half*>(tail_v);
+  a.scale = softmax_scale;
+  a.out = static_cast<__half*>(out);
+  a.ws_part = p.nsplit > 1 ? static_cast<float*>(workspace) : nullptr;
+  a.ws_count = p.nsplit > 1
+                   ? reinterpret_cast<int*>(static_cast<uint8_t*>(workspace) + p.part_bytes)
+                   : nullptr;
+  a.pages_per_split = p.pages_per_split;
+  a.nsplit = p.nsplit;
+  a.status = status;
+  cudaError_t e = decode_mma_supported(a.g) ? launch_decode_mma(a, (cudaStream_t)stream)
+                                            : launch_decode_simple(a, (cudaStream_t)stream);
+  return e == cudaSuccess ? KVARN_OK : KVARN_ERR_LAUNCH;
+}
+
+int kvarn_dequantize_pages(const void* records, int64_t n, float* yk, float* yv,
+                           kvarn_stream_t stream) {
+  if (n < 0) return KVARN_ERR_INVALID_ARG;
+  if (n == 0) return KVARN_OK;
+  if (!records || !yk || !yv || !aligned16(records) || n > 0x7fffffff)
+    return KVARN_ERR_INVALID_ARG;
+  return launch_dequantize(static_cast<const uint8_t*>(records), n, yk, yv,
+                           (cudaStream_t)stream) == cudaSuccess
+             ? KVARN_OK
+             : KVARN_ERR_LAUNCH;
+}
+
+const char* kvarn_status_string(int code) {
+  switch (code) {
+    case KVARN_OK: return "ok";
+    case KVARN_ERR_INVALID_ARG: return "invalid argument";
+    case KVARN_ERR_UNSUPPORTED: return "unsupported configuration";
+    case KVARN_ERR_WORKSPACE: return "decode workspace missing or too small";
+    case KVARN_ERR_LAUNCH: return "CUDA launch failed";
+    case KVARN_STATUS_BAD_PAGE: return "device: block-table entry outside the pool";
+    case KVARN_STATUS_BAD_LENGTH: return "device: sequence length beyond max_seq or the table";
+    case KVARN_STATUS_TIMEOUT: return "device: a bounded wait gave up";
+    default: return code > 0 ? "device: several status bits set" : "unknown error";
+  }
+}
+
+const char* kvarn_version(void) { return "0.1.0"; }
+
+}  // extern "C"

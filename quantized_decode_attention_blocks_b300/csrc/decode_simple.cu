@@ -1,0 +1,297 @@
+// decode_simple.cu -- paged split-K decode attention over the quantized cache,
+// plain CUDA-core formulation (one thread per token for scores, one thread per
+// channel for the value sum).  It is the reference CUDA path used for small
+// GQA groups and as the fallback for configurations the tensor-core kernel
+// does not cover.
+//
+// Method: one new query token per sequence attends to every cached token
+// ("KV Cache (Anahtar-Deger Onbellegi)", yapayzekasozluk.tr, "KV Cache Nasil
+// Calisir?").  Keys and values are stored rotated, y = H x, with H the
+// orthonormal Hadamard matrix (KVarN page, blog.edumints.com, "KVarN Nasil
+// Calisir?", stage "Dondurulmus Onbellek", which notes that the rotation keeps
+// attention scores).  So the query is rotated once, q~ = H q, scores are taken
+// against the rotated keys, the value sum is accumulated in rotated space and
+// rotated back once at the end: o = H o~ + o_tail, the fp16 tail being added
+// in plain space.  With the stored metadata,
+//   q~ . yhat_t = s'_t * sum_d (q~_d c_d) q_td + z'_t * sum_d q~_d c_d.
+#include "kvarn_internal.cuh"
+
+namespace kvarn {
+namespace {
+
+constexpr int kThreads = 128;
+
+struct __align__(16) DecodeSmem {
+  uint8_t rec[kRec];
+  float qrot[kMaxG][kD];   // H q, per head
+  float qraw[kMaxG][kD];   // q, per head (tail scores)
+  float qc[kMaxG][kD];     // H q * c^K, per page
+  float pw[kMaxG][kT];     // p_t * s'^V_t, per page
+  float red[kThreads / 32][kMaxG];
+  float m[kMaxG], l[kMaxG], alpha[kMaxG], sq[kMaxG], zs[kMaxG];
+  int ticket;
+};
+
+// Block-wide reductions over the 128 threads, one value per head.
+template <bool kMax>
+__device__ __forceinline__ void block_reduce(DecodeSmem& S, float (&v)[kMaxG], int g,
+                                             float* out) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  for (int h = 0; h < g; ++h) {
+    float x = v[h];
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      float y = __shfl_xor_sync(0xffffffffu, x, o);
+      x = kMax ? fmaxf(x, y) : x + y;
+    }
+    if (lane == 0) S.red[warp][h] = x;
+  }
+  __syncthreads();
+  if (threadIdx.x < g) {
+    const int h = threadIdx.x;
+    float x = S.red[0][h];
+    for (int w = 1; w < kThreads / 32; ++w) x = kMax ? fmaxf(x, S.red[w][h]) : x + S.red[w][h];
+    out[h] = x;
+  }
+  __syncthreads();
+}
+
+// In-place Walsh-Hadamard transform of g vectors of 128 floats, scaled.
+__device__ void fwht_rows(float (*v)[kD], int g) {
+  for (int s = 1; s < kD; s <<= 1) {
+    for (int i = threadIdx.x; i < g * (kD / 2); i += kThreads) {
+      const int h = i / (kD / 2), k = i % (kD / 2);
+      const int lo = ((k & ~(s - 1)) << 1) | (k & (s - 1));
+      const float a = v[h][lo], b = v[h][lo + s];
+      v[h][lo] = a + b;
+      v[h][lo + s] = a - b;
+    }
+    __syncthreads();
+  }
+  for (int i = threadIdx.x; i < g * kD; i += kThreads) v[i / kD][i % kD] *= kInvSqrt128;
+  __syncthreads();
+}
+
+// grid: (nsplit, hkv, batch); block 128.
+__global__ void __launch_bounds__(kThreads) decode_simple_kernel(DecodeArgs a) {
+  extern __shared__ __align__(16) uint8_t smem_raw[];
+  DecodeSmem& S = *reinterpret_cast<DecodeSmem*>(smem_raw);
+  const int split = blockIdx.x, kvh = blockIdx.y, b = blockIdx.z;
+  const int tid = threadIdx.x;
+  const int g = a.g;
+
+  int len = a.seq_lens[b];
+  if (len < 0 || len > a.max_seq || len / kT > a.max_blocks) {
+    if (split == 0 && kvh == 0 && tid == 0) report(a.status, KVARN_STATUS_BAD_LENGTH);
+    len = 0;
+  }
+  const int nfull = len / kT, rem = len % kT;
+  const int units = nfull + (rem > 0 ? 1 : 0);
+  const int nsb = units > 0 ? (units + a.pages_per_split - 1) / a.pages_per_split : 1;
+  if (split >= nsb) return;
+  const int u0 = split * a.pages_per_split;
+  const int u1 = min(units, u0 + a.pages_per_split);
+
+  // queries of the group: raw and rotated
+  const __half* qb = a.q + ((int64_t)b * a.hq + (int64_t)kvh * g) * kD;
+  for (int i = tid; i < g * kD; i += kThreads) {
+    const float x = __half2float(qb[i]);
+    S.qraw[i / kD][i % kD] = x;
+    S.qrot[i / kD][i % kD] = x;
+  }
+  if (tid < g) {
+    S.m[tid] = -INFINITY;
+    S.l[tid] = 0.f;
+  }
+  __syncthreads();
+  fwht_rows(S.qrot, g);
+
+  float acc[kMaxG], acc_tail[kMaxG];
+#pragma unroll
+  for (int h = 0; h < kMaxG; ++h) acc[h] = acc_tail[h] = 0.f;
+
+  for (int u = u0; u < u1; ++u) {
+    float sc[kMaxG];
+    if (u < nfull) {
+      const int64_t page = a.block_table[(int64_t)b * a.max_blocks + u];
+      if (page < 0 || page >= a.num_pages) {
+        if (tid == 0) report(a.status, KVARN_STATUS_BAD_PAGE);
+        continue;
+      }
+      const uint4* src = reinterpret_cast<const uint4*>(a.pool + (page * a.hkv + kvh) * (int64_t)kRec);
+      uint4* dst = reinterpret_cast<uint4*>(S.rec);
+      for (int i = tid; i < kRec / 16; i += kThreads) dst[i] = __ldg(src + i);
+      __syncthreads();
+      // qc = H q * c^K (thread = channel), and its sum per head
+      {
+        const float ck = reinterpret_cast<const float*>(S.rec + kOffKC)[tid];
+        float part[kMaxG];
+        for (int h = 0; h < g; ++h) {
+          const float x = S.qrot[h][tid] * ck;
+          S.qc[h][tid] = x;
+          part[h] = x;
+        }
+        block_reduce<false>(S, part, g, S.sq);
+      }
+      // scores (thread = token)
+      {
+        const uint32_t* row = reinterpret_cast<const uint32_t*>(S.rec + kOffKCodes + 64 * tid);
+        const float2 sz = reinterpret_cast<const float2*>(S.rec + kOffKSZ)[tid];
+        for (int h = 0; h < g; ++h) sc[h] = 0.f;
+        for (int w = 0; w < 16; ++w) {
+          const uint32_t word = row[w];
+#pragma unroll
+          for (int e = 0; e < 8; ++e) {
+            const float code = (float)((word >> (4 * e)) & 15u);
+            const int d = 8 * w + e;
+            for (int h = 0; h < g; ++h) sc[h] = fmaf(S.qc[h][d], code, sc[h]);
+          }
+        }
+        for (int h = 0; h < g; ++h) sc[h] = a.scale * fmaf(sz.x, sc[h], sz.y * S.sq[h]);
+      }
+    } else {
+      // fp16 tail tokens 0..rem-1 (thread = token), plain space
+      for (int h = 0; h < g; ++h) sc[h] = -INFINITY;
+      if (tid < rem) {
+        const __half* kt = a.tail_k + (((int64_t)b * a.hkv + kvh) * kT + tid) * kD;
+        for (int h = 0; h < g; ++h) sc[h] = 0.f;
+        for (int d = 0; d < kD; ++d) {
+          const float kd = __half2float(kt[d]);
+          for (int h = 0; h < g; ++h) sc[h] = fmaf(S.qraw[h][d], kd, sc[h]);
+        }
+        for (int h = 0; h < g; ++h) sc[h] *= a.scale;
+      }
+    }
+    // online softmax update
+    {
+      float mx[kMaxG];
+      for (int h = 0; h < g; ++h) mx[h] = sc[h];
+      block_reduce<true>(S, mx, g, S.alpha);   // alpha <- page max (temporarily)
+      if (tid < g) {
+        const float mnew = fmaxf(S.m[tid], S.alpha[tid]);
+        const float al = S.m[tid] == -INFINITY ? 0.f : __expf(S.m[tid] - mnew);
+        S.m[tid] = mnew;
+        S.alpha[tid] = al;
+      }
+      __syncthreads();
+    }
+    float p[kMaxG];
+    for (int h = 0; h < g; ++h) p[h] = sc[h] == -INFINITY ? 0.f : __expf(sc[h] - S.m[h]);
+    if (u < nfull) {
+      const float2 szv = reinterpret_cast<const float2*>(S.rec + kOffVSZ)[tid];
+      float zp[kMaxG];
+      for (int h = 0; h < g; ++h) {
+        S.pw[h][tid] = p[h] * szv.x;
+        zp[h] = p[h] * szv.y;
+      }
+      block_reduce<false>(S, zp, g, S.zs);
+      block_reduce<false>(S, p, g, S.sq);  // S.sq: the page's sum of p per head
+      if (tid < g) S.l[tid] = S.l[tid] * S.alpha[tid] + S.sq[tid];
+      __syncthreads();
+      // value sum (thread = channel d), rotated space
+      {
+        const int d = tid;
+        const uint32_t* vrow = reinterpret_cast<const uint32_t*>(S.rec + kOffVCodes + 32 * d);
+        const float cv = reinterpret_cast<const float*>(S.rec + kOffVC)[d];
+        float pv[kMaxG];
+        for (int h = 0; h < g; ++h) pv[h] = 0.f;
+        for (int w = 0; w < 8; ++w) {
+          const uint32_t word = vrow[w];
+#pragma unroll
+          for (int e = 0; e < 16; ++e) {
+            const float code = (float)((word >> (2 * e)) & 3u);
+            const int t = 16 * w + e;
+            for (int h = 0; h < g; ++h) pv[h] = fmaf(S.pw[h][t], code, pv[h]);
+          }
+        }
+        for (int h = 0; h < g; ++h) {
+          acc[h] = fmaf(acc[h], S.alpha[h], cv * (pv[h] + S.zs[h]));
+          acc_tail[h] *= S.alpha[h];
+        }
+      }
+    } else {
+      for (int h = 0; h < g; ++h) S.pw[h][tid] = p[h];
+      block_reduce<false>(S, p, g, S.sq);
+      if (tid < g) S.l[tid] = S.l[tid] * S.alpha[tid] + S.sq[tid];
+      __syncthreads();
+      const int d = tid;
+      const __half* vt = a.tail_v + ((int64_t)b * a.hkv + kvh) * kT * kD;
+      float pv[kMaxG];
+      for (int h = 0; h < g; ++h) pv[h] = 0.f;
+      for (int t = 0; t < rem; ++t) {
+        const float vd = __half2float(vt[(int64_t)t * kD + d]);
+        for (int h = 0; h < g; ++h) pv[h] = fmaf(S.pw[h][t], vd, pv[h]);
+      }
+      for (int h = 0; h < g; ++h) {
+        acc[h] *= S.alpha[h];
+        acc_tail[h] = fmaf(acc_tail[h], S.alpha[h], pv[h]);
+      }
+    }
+    __syncthreads();  // the record and pw are rewritten by the next unit
+  }
+
+  // back to plain space: o = H acc + acc_tail
+  for (int h = 0; h < g; ++h) S.qc[h][tid] = acc[h];
+  __syncthreads();
+  fwht_rows(S.qc, g);
+  float o[kMaxG];
+  for (int h = 0; h < g; ++h) o[h] = S.qc[h][tid] + acc_tail[h];
+
+  __half* ob = a.out + ((int64_t)b * a.hq + (int64_t)kvh * g) * kD;
+  if (nsb == 1) {
+    for (int h = 0; h < g; ++h) {
+      const float l = S.l[h];
+      ob[h * kD + tid] = __float2half_rn(l > 0.f ? o[h] / l : 0.f);
+    }
+    return;
+  }
+  // split-K: publish the partial state, the last CTA of (b, kvh) merges
+  const int64_t stride_split = 2 + kD;
+  for (int h = 0; h < g; ++h) {
+    float* P = a.ws_part + (((int64_t)b * a.hq + kvh * g + h) * a.nsplit + split) * stride_split;
+    if (tid == 0) {
+      P[0] = S.m[h];
+      P[1] = S.l[h];
+    }
+    P[2 + tid] = o[h];
+  }
+  __threadfence();
+  __syncthreads();
+  if (tid == 0) S.ticket = atomicAdd(a.ws_count + (int64_t)b * a.hkv + kvh, 1);
+  __syncthreads();
+  if (S.ticket != nsb - 1) return;
+  __threadfence();
+  for (int h = 0; h < g; ++h) {
+    const float* P = a.ws_part + (((int64_t)b * a.hq + kvh * g + h) * a.nsplit) * stride_split;
+    float M = -INFINITY;
+    for (int s2 = 0; s2 < nsb; ++s2) M = fmaxf(M, __ldcg(P + s2 * stride_split));
+    float L = 0.f, O = 0.f;
+    for (int s2 = 0; s2 < nsb; ++s2) {
+      const float ms = __ldcg(P + s2 * stride_split);
+      if (ms == -INFINITY) continue;
+      const float w = __expf(ms - M);
+      L = fmaf(w, __ldcg(P + s2 * stride_split + 1), L);
+      O = fmaf(w, __ldcg(P + s2 * stride_split + 2 + tid), O);
+    }
+    ob[h * kD + tid] = __float2half_rn(L > 0.f ? O / L : 0.f);
+  }
+  if (tid == 0) a.ws_count[(int64_t)b * a.hkv + kvh] = 0;
+}
+
+}  // namespace
+
+cudaError_t launch_decode_simple(const DecodeArgs& a, cudaStream_t s) {
+  static bool attr_set = false;
+  const int smem = (int)sizeof(DecodeSmem);
+  if (!attr_set) {
+    cudaError_t e = cudaFuncSetAttribute(decode_simple_kernel,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return e;
+    attr_set = true;
+  }
+  dim3 grid(a.nsplit, a.hkv, a.batch);
+  decode_simple_kernel<<<grid, kThreads, smem, s>>>(a);
+  return cudaGetLastError();
+}
+
+}  // namespace kvarn

@@ -1,0 +1,99 @@
+// kvarn_internal.cuh -- layout constants and launcher declarations shared by
+// the CUDA translation units of libkvarn.  Not part of the public ABI.
+#pragma once
+
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/kvarn.h"
+
+namespace kvarn {
+
+// Page record layout (one per page and KV head); see include/kvarn.h.
+constexpr int kD = 128;           // head_dim = group size
+constexpr int kT = 128;           // tokens per page
+constexpr int kRec = 15360;       // bytes per record
+constexpr int kOffKCodes = 0;     // [128 tokens][64 B]
+constexpr int kOffVCodes = 8192;  // [128 channels][32 B]
+constexpr int kOffKSZ = 12288;    // [128 tokens]{s', z'} fp32
+constexpr int kOffVSZ = 13312;
+constexpr int kOffKC = 14336;     // [128 channels] fp32
+constexpr int kOffVC = 14848;
+constexpr int kMaxG = 16;         // query heads per KV head supported
+constexpr int kMaxIters = 64;     // Sinkhorn iterations accepted
+constexpr int kNumSMs = 148;      // B300
+
+// 1 / sqrt(128), rounded to fp32.
+constexpr float kInvSqrt128 = 0.08838834764831845f;
+
+struct QuantizeArgs {
+  const __half* k;
+  const __half* v;
+  int64_t sb, st, sh;       // element strides of k / v
+  int batch, hkv, iters, max_seq;
+  const int32_t* seq_lens;
+  const int32_t* block_table;
+  int max_blocks;
+  uint8_t* pool;
+  int64_t num_pages;
+  __half* tail_k;
+  __half* tail_v;
+  int32_t* status;
+};
+
+struct AppendArgs {
+  const __half* k_new;
+  const __half* v_new;
+  const int32_t* pos;
+  int batch, hkv, iters;
+  const int32_t* block_table;
+  int max_blocks;
+  uint8_t* pool;
+  int64_t num_pages;
+  __half* tail_k;
+  __half* tail_v;
+  int32_t* status;
+};
+
+struct DecodeArgs {
+  const __half* q;
+  const uint8_t* pool;
+  int64_t num_pages;
+  const int32_t* block_table;
+  int max_blocks;
+  const int32_t* seq_lens;
+  int batch, max_seq, hq, hkv, g;
+  const __half* tail_k;
+  const __half* tail_v;
+  float scale;
+  __half* out;
+  float* ws_part;     // [batch][hq][nsplit][2 + 128]: m, l, o[128]
+  int* ws_count;      // [batch][hkv] arrival tickets, zero between calls
+  int pages_per_split;
+  int nsplit;
+  int32_t* status;
+};
+
+// Split-K plan for decode: pages per CTA and the number of splits, both a
+// pure function of (batch, hkv, max_seq) so that the workspace query and the
+// launch agree.
+struct DecodePlan {
+  int pages_per_split;
+  int nsplit;
+  size_t part_bytes;   // partial-state region
+  size_t count_bytes;  // ticket region
+};
+DecodePlan decode_plan(int batch, int hq, int hkv, int max_seq);
+
+cudaError_t launch_quantize_blocks(const QuantizeArgs& a, cudaStream_t s);
+cudaError_t launch_append_token(const AppendArgs& a, cudaStream_t s);
+cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t s);
+cudaError_t launch_dequantize(const uint8_t* rec, int64_t n, float* yk, float* yv,
+                              cudaStream_t s);
+
+__device__ __forceinline__ void report(int32_t* status, int bits) {
+  if (status) atomicOr(status, bits);
+}
+
+}  // namespace kvarn

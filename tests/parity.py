@@ -1,0 +1,74 @@
+"""Comparison rules between the CUDA path and the float64 oracle.
+
+  * codes: bit-exact, except elements whose oracle pre-rounding value u lies
+    within 1e-5 of a rounding boundary (k + 1/2); such flips must be at most
+    1e-4 of all elements;
+  * s' and c: |gpu - ref| <= 1e-5 |ref| (1e-12 absolute when ref = 0);
+  * z': |gpu - ref| <= 1e-5 (|z'| + s' (2^b - 1));
+  * attention output (fp16): |gpu - ref| <= 2e-3 + 1e-3 |ref| elementwise, the
+    oracle being fed the GPU's own pool so that decode is judged apart from
+    boundary flips in quantization.
+"""
+from __future__ import annotations
+
+import numpy as np
+
+from oracle import kvref
+
+BOUNDARY = 1e-5
+FLIP_RATE = 1e-4
+
+
+def near_boundary(u):
+    return np.abs(u - np.floor(u) - 0.5) < BOUNDARY
+
+
+def compare_record(got: np.ndarray, ref: np.ndarray, u_k=None, u_v=None, stats=None):
+    """Compares one 15360-byte record (GPU) with the oracle's.  u_k, u_v:
+    oracle pre-rounding values [128][128] (token, channel).  Returns a dict."""
+    out = {} if stats is None else stats
+    for is_v, u in ((False, u_k), (True, u_v)):
+        bits = 2 if is_v else 4
+        qg, sg, zg, cg = kvref.unpack_part(got, is_v)
+        qr, sr, zr, cr = kvref.unpack_part(ref, is_v)
+        tag = "v" if is_v else "k"
+        diff = qg != qr
+        n_diff = int(diff.sum())
+        if n_diff:
+            assert u is not None, f"{tag}: {n_diff} code mismatches and no u to judge them"
+            ok = near_boundary(u)
+            bad = diff & ~ok
+            assert not bad.any(), (f"{tag}: {int(bad.sum())} code mismatches away from a "
+                                   f"rounding boundary, e.g. u={u[bad][:4]}, gpu={qg[bad][:4]}, "
+                                   f"ref={qr[bad][:4]}")
+        out[f"{tag}_flips"] = out.get(f"{tag}_flips", 0) + n_diff
+        out[f"{tag}_codes"] = out.get(f"{tag}_codes", 0) + qg.size
+        for name, g_, r_ in (("s", sg, sr), ("c", cg, cr)):
+            g64, r64 = g_.astype(np.float64), r_.astype(np.float64)
+            tol = np.where(r64 == 0, 1e-12, 1e-5 * np.abs(r64))
+            err = np.abs(g64 - r64)
+            assert np.all(err <= tol), (f"{tag}.{name}: worst rel err "
+                                        f"{(err / np.maximum(np.abs(r64), 1e-30)).max():.3e}")
+        tolz = 1e-5 * (np.abs(zr.astype(np.float64)) + sr.astype(np.float64) * (2 ** bits - 1))
+        tolz = np.maximum(tolz, 1e-12)
+        errz = np.abs(zg.astype(np.float64) - zr.astype(np.float64))
+        assert np.all(errz <= tolz), f"{tag}.z: worst err {errz.max():.3e}"
+    return out
+
+
+def check_flip_rate(stats):
+    for tag in ("k", "v"):
+        if stats.get(f"{tag}_codes"):
+            rate = stats[f"{tag}_flips"] / stats[f"{tag}_codes"]
+            assert rate <= FLIP_RATE, f"{tag}: boundary flips {rate:.2e} > {FLIP_RATE}"
+
+
+def compare_attention(got: np.ndarray, ref: np.ndarray):
+    got = got.astype(np.float64)
+    err = np.abs(got - ref)
+    tol = 2e-3 + 1e-3 * np.abs(ref)
+    assert np.all(err <= tol), (f"attention: {int((err > tol).sum())} of {err.size} outside "
+                                f"2e-3 + 1e-3|ref|; max abs err {err.max():.3e}")
+    rel = np.linalg.norm(got - ref) / max(np.linalg.norm(ref), 1e-30)
+    assert rel <= 1e-3, f"attention: relative norm error {rel:.3e}"
+    return {"max_abs": float(err.max()), "rel_norm": float(rel)}

@@ -1,0 +1,149 @@
+"""The C-ABI library: loads, exports every symbol include/kvarn.h declares, and
+rejects bad arguments on the host before any launch (no GPU needed)."""
+import ctypes
+import os
+import re
+import subprocess
+
+import pytest
+import torch
+
+import quantized_decode_attention_blocks_b300 as kv
+from quantized_decode_attention_blocks_b300 import kvarn as K
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "kvarn.h")
+
+
+def declared_symbols():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(kvarn_[a-z_]+)\s*\(", text)))
+
+
+def test_library_exports_every_declared_symbol():
+    L = kv.lib()
+    names = declared_symbols()
+    assert len(names) >= 10
+    for n in names:
+        assert hasattr(L, n), n
+    nm = subprocess.run(["nm", "-D", "--defined-only", K.LIB_PATH], capture_output=True,
+                        text=True).stdout
+    exported = set(re.findall(r" T (kvarn_\w+)", nm))
+    assert set(names) <= exported
+    assert set(names) == set(K.SIGNATURES)
+
+
+def test_header_constants_match_binding():
+    text = open(HEADER).read()
+    for name, val in (("KVARN_PAGE_BYTES", K.PAGE_BYTES), ("KVARN_OK", K.OK),
+                      ("KVARN_ERR_INVALID_ARG", K.ERR_INVALID_ARG),
+                      ("KVARN_ERR_UNSUPPORTED", K.ERR_UNSUPPORTED),
+                      ("KVARN_ERR_WORKSPACE", K.ERR_WORKSPACE), ("KVARN_ERR_LAUNCH", K.ERR_LAUNCH),
+                      ("KVARN_STATUS_BAD_PAGE", K.STATUS_BAD_PAGE),
+                      ("KVARN_STATUS_BAD_LENGTH", K.STATUS_BAD_LENGTH),
+                      ("KVARN_STATUS_TIMEOUT", K.STATUS_TIMEOUT)):
+        m = re.search(rf"#define {name} \(?(-?\d+)\)?", text)
+        assert m and int(m.group(1)) == val, name
+
+
+def test_config_parsing():
+    c = kv.config_from_string("kvarn_k4v2_g128", 32, 8)
+    assert (c.head_dim, c.block_tokens, c.group, c.k_bits, c.v_bits) == (128, 128, 128, 4, 2)
+    assert c.sinkhorn_iters == 2 and c.g == 4
+    assert kv.config_from_string("k4v2_g128_s7", 12, 2).sinkhorn_iters == 7
+    for bad in ("k4v4_g128", "k4v2_g64", "k4v2_g128_x", "k4v2_g128_s", "k4v2_g128_s999"):
+        with pytest.raises(kv.KvarnError) as e:
+            kv.config_from_string(bad, 32, 8)
+        assert e.value.code == K.ERR_UNSUPPORTED
+    with pytest.raises(kv.KvarnError) as e:
+        kv.config_from_string("k4v2_g128", 30, 8)
+    assert e.value.code == K.ERR_INVALID_ARG
+    with pytest.raises(kv.KvarnError) as e:
+        kv.config_from_string("k4v2_g128", 64, 2)        # group of 32 > 16
+    assert e.value.code == K.ERR_UNSUPPORTED
+    c.head_dim = 64
+    assert kv.config_validate(c) == K.ERR_UNSUPPORTED
+    assert kv.page_bytes(c) == 0
+
+
+def test_page_bytes_and_workspace_sizes():
+    c = kv.config_from_string("k4v2_g128", 32, 8)
+    assert kv.page_bytes(c) == 15360 == 120 * 128
+    assert kv.decode_workspace_bytes(c, 0, 100) == 0
+    small = kv.decode_workspace_bytes(c, 1, 200)
+    big = kv.decode_workspace_bytes(c, 16, 131072)
+    assert big > small >= 0
+    assert big % 256 == 0
+
+
+def test_status_strings():
+    for code in (0, -1, -2, -3, -4, 1, 2, 4, 3, -99):
+        s = kv.status_string(code)
+        assert isinstance(s, str) and s
+    assert kv.version().count(".") == 2
+
+
+def _cfg():
+    return kv.config_from_string("k4v2_g128", 8, 2)
+
+
+def test_host_validation_quantize():
+    L = kv.lib()
+    c = _cfg()
+    P = ctypes.c_void_p
+    a16 = P(4096)          # fake aligned addresses: validation must fail before any use
+    mis = P(4098)
+    call = lambda **kw: L.kvarn_quantize_blocks(
+        ctypes.byref(kw.get("cfg", c)), kw.get("k", a16), kw.get("v", a16),
+        kw.get("sb", 128 * 2 * 256), kw.get("st", 256), kw.get("sh", 128), kw.get("batch", 1),
+        kw.get("lens", a16), kw.get("max_seq", 256), kw.get("table", a16),
+        kw.get("max_blocks", 2), kw.get("pool", a16), kw.get("num_pages", 2),
+        kw.get("tk", a16), kw.get("tv", a16), None, None)
+    assert call(k=None) == K.ERR_INVALID_ARG
+    assert call(lens=None) == K.ERR_INVALID_ARG
+    assert call(k=mis) == K.ERR_INVALID_ARG
+    assert call(st=100) == K.ERR_INVALID_ARG          # not a multiple of 8
+    assert call(sh=4) == K.ERR_INVALID_ARG
+    assert call(max_blocks=1) == K.ERR_INVALID_ARG    # 256 tokens need 2 blocks
+    assert call(batch=-1) == K.ERR_INVALID_ARG
+    assert call(pool=None) == K.ERR_INVALID_ARG
+    assert call(batch=0, k=None) == K.OK              # nothing to do
+    bad = _cfg()
+    bad.k_bits = 8
+    assert call(cfg=bad) == K.ERR_UNSUPPORTED
+
+
+def test_host_validation_append_and_decode():
+    L = kv.lib()
+    c = _cfg()
+    P = ctypes.c_void_p
+    a16 = P(4096)
+    assert L.kvarn_append_token(ctypes.byref(c), None, a16, a16, 1, a16, 2, a16, 2, a16, a16,
+                                None, None) == K.ERR_INVALID_ARG
+    assert L.kvarn_append_token(ctypes.byref(c), a16, a16, a16, 1, a16, 0, a16, 2, a16, a16,
+                                None, None) == K.ERR_INVALID_ARG
+    dec = lambda **kw: L.kvarn_decode_attention(
+        ctypes.byref(c), kw.get("q", a16), a16, 4, a16, 4, a16, kw.get("batch", 2),
+        kw.get("max_seq", 512), a16, a16, kw.get("scale", 0.088), kw.get("out", a16),
+        kw.get("ws", None), kw.get("ws_bytes", 0), None, None)
+    assert dec(q=None) == K.ERR_INVALID_ARG
+    assert dec(out=P(4097)) == K.ERR_INVALID_ARG
+    assert dec(scale=0.0) == K.ERR_INVALID_ARG
+    assert dec(scale=float("nan")) == K.ERR_INVALID_ARG
+    need = kv.decode_workspace_bytes(c, 2, 512)
+    if need:
+        assert dec() == K.ERR_WORKSPACE
+        assert dec(ws=a16, ws_bytes=need - 1) == K.ERR_WORKSPACE
+    assert dec(batch=0) == K.OK
+    assert L.kvarn_dequantize_pages(a16, -1, a16, a16, None) == K.ERR_INVALID_ARG
+    assert L.kvarn_dequantize_pages(None, 3, a16, a16, None) == K.ERR_INVALID_ARG
+
+
+def test_binding_refuses_cpu_tensors():
+    c = _cfg()
+    k = torch.zeros((1, 128, 2, 128), dtype=torch.float16)
+    with pytest.raises(ValueError):
+        kv.kvarn_quantize_blocks(c, k, k, torch.zeros(1, dtype=torch.int32), 128,
+                                 torch.zeros((1, 1), dtype=torch.int32),
+                                 torch.zeros((1, 2, 15360), dtype=torch.uint8), k, k)

@@ -1,0 +1,110 @@
+"""Decode attention on the GPU against the float64 oracle.
+
+The oracle reads the GPU's own pool (rotated route), so decode is judged apart
+from boundary flips of quantization.  "KV Cache (Anahtar-Deger Onbellegi)"
+(yapayzekasozluk.tr), "KV Cache Nasil Calisir?" and "Paged Attention (vLLM)";
+KVarN page (blog.edumints.com), "KVarN Nasil Calisir?", stage 2.
+"""
+import numpy as np
+import pytest
+import torch
+
+from oracle import kvref
+from tests import parity
+from tests.gpu_helpers import DEV, config, decode, host, prefill
+from workloads import synth
+
+pytestmark = pytest.mark.gpu
+
+
+def _run(w, lens, table, num_pages, q=None, max_seq=None):
+    max_seq = int(lens.max()) if max_seq is None else max_seq
+    S = max(int(lens.max()), 1)
+    k, v = synth.kv(w, device=DEV, seq=S)
+    cfg = config(w.hq, w.hkv)
+    pool, tk, tv, st = prefill(cfg, k, v, lens, table, num_pages, max_seq=max_seq)
+    if q is None:
+        q = synth.queries(w)
+    out, st2, ws = decode(cfg, q, pool, table, lens, tk, tv, max_seq=max_seq)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0 and int(st2.item()) == 0
+    ref = kvref.decode_attention(host(q), host(pool), host(table), host(lens), host(tk),
+                                 host(tv), w.hq, w.hkv, route=1)
+    res = parity.compare_attention(host(out), ref)
+    return res, (cfg, q, pool, table, lens, tk, tv, out, ws, max_seq)
+
+
+@pytest.mark.parametrize("hq,hkv", [(1, 1), (8, 2), (12, 2), (8, 1), (16, 1), (32, 8)])
+def test_group_sizes_and_ragged_lengths(hq, hkv):
+    lens = torch.tensor([0, 1, 127, 128, 129, 300, 1000, 2048], dtype=torch.int32)
+    B = len(lens)
+    w = synth.scaled(synth.WORKLOADS["llama3_8b_layer"], batch=B, seq=2048, hkv=hkv, hq=hq)
+    mb = 16
+    g = torch.Generator().manual_seed(11)
+    table = torch.randperm(B * mb, generator=g).to(torch.int32).reshape(B, mb)
+    _run(w, lens, table, B * mb)
+
+
+def test_tiny_workload():
+    w = synth.WORKLOADS["tiny"]
+    tables, n = synth.block_tables(w)
+    _run(w, synth.seq_lens(w), tables[0], n)
+
+
+def test_many_splits_long_sequence():
+    # one sequence of 20000 tokens: 156 pages + a 32-token tail -> many splits
+    w = synth.scaled(synth.WORKLOADS["long_context"], batch=1, seq=20000, hkv=2, hq=8)
+    lens = torch.tensor([20000], dtype=torch.int32)
+    g = torch.Generator().manual_seed(3)
+    table = torch.randperm(157, generator=g).to(torch.int32).reshape(1, 157)
+    res, state = _run(w, lens, table, 157)
+    # the workspace tickets are left at zero: a second call gives the same output
+    cfg, q, pool, table, lens, tk, tv, out, ws, max_seq = state
+    import quantized_decode_attention_blocks_b300 as kv
+    out2 = torch.empty_like(out)
+    kv.kvarn_decode_attention(cfg, q.to(DEV), pool, table.to(DEV), lens.to(DEV), max_seq, tk, tv,
+                              out2, ws)
+    torch.cuda.synchronize()
+    assert torch.equal(out, out2)
+
+
+def test_max_seq_larger_than_lengths():
+    # the grid is sized from max_seq; shorter sequences finish early
+    w = synth.scaled(synth.WORKLOADS["llama3_8b_layer"], batch=3, seq=700, hkv=2, hq=8)
+    lens = torch.tensor([700, 5, 260], dtype=torch.int32)
+    table = torch.arange(3 * 40, dtype=torch.int32).reshape(3, 40)
+    _run(w, lens, table, 120, max_seq=5000)
+
+
+def test_bad_page_reported():
+    import quantized_decode_attention_blocks_b300 as kv
+    w = synth.scaled(synth.WORKLOADS["llama3_8b_layer"], batch=1, seq=512, hkv=2, hq=8)
+    k, v = synth.kv(w, device=DEV)
+    cfg = config(w.hq, w.hkv)
+    lens = torch.tensor([512], dtype=torch.int32)
+    pool, tk, tv, _ = prefill(cfg, k, v, lens, torch.tensor([[0, 1, 2, 3]], dtype=torch.int32),
+                              4)
+    bad = torch.tensor([[0, 1, -5, 3]], dtype=torch.int32)
+    out, st, _ = decode(cfg, synth.queries(w), pool, bad, lens, tk, tv)
+    torch.cuda.synchronize()
+    assert int(st.item()) & kv.kvarn.STATUS_BAD_PAGE
+    assert torch.isfinite(out.float()).all()
+
+
+def test_scale_argument():
+    w = synth.scaled(synth.WORKLOADS["llama3_8b_layer"], batch=2, seq=400, hkv=2, hq=8)
+    lens = torch.tensor([400, 333], dtype=torch.int32)
+    table = torch.arange(8, dtype=torch.int32).reshape(2, 4)
+    k, v = synth.kv(w, device=DEV)
+    cfg = config(w.hq, w.hkv)
+    pool, tk, tv, _ = prefill(cfg, k, v, lens, table, 8)
+    q = synth.queries(w)
+    import quantized_decode_attention_blocks_b300 as kv
+    out = torch.empty((2, 8, 128), dtype=torch.float16, device=DEV)
+    ws = kv.alloc_decode_workspace(cfg, 2, 400, DEV)
+    kv.kvarn_decode_attention(cfg, q.to(DEV), pool, table.to(DEV), lens.to(DEV), 400, tk, tv,
+                              out, ws, softmax_scale=0.3)
+    torch.cuda.synchronize()
+    ref = kvref.decode_attention(host(q), host(pool), host(table), host(lens), host(tk), host(tv),
+                                 8, 2, scale=0.3, route=1)
+    parity.compare_attention(host(out), ref)
