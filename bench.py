@@ -80,7 +80,7 @@ def ncu_traffic(kernel_key, src_name):
 class ClockSampler:
     """Samples nvidia-smi SM clocks and throttle reasons during the timed region."""
 
-    FIELDS = ("clocks.sm,clocks.max.sm,clocks_event_reasons.hw_slowdown,"
+    FIELDS = ("timestamp,clocks.sm,clocks.max.sm,clocks_event_reasons.hw_slowdown,"
               "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
               "clocks_event_reasons.sw_power_cap")
 
@@ -101,14 +101,23 @@ class ClockSampler:
             return
         self.thread = threading.Thread(target=self._read, daemon=True)
         self.thread.start()
+        t0 = time.time()
+        while not self.lines and time.time() - t0 < 10:   # wait for the first sample
+            time.sleep(0.02)
 
     def _read(self):
         for line in self.proc.stdout:
-            self.lines.append(line.strip())
+            self.lines.append((time.time(), line.strip()))
+
+    def mark(self, which):
+        setattr(self, which, time.time())
 
     def stop(self):
         if self.proc is None:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        t_end = time.time()
+        while time.time() - t_end < 0.3:      # one more sample after the region
+            time.sleep(0.02)
         self.proc.terminate()
         try:
             self.proc.wait(timeout=5)
@@ -118,16 +127,20 @@ class ClockSampler:
             self.thread.join(timeout=2)
         sm, mx, reasons = [], [], set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for line in self.lines:
+        t0 = getattr(self, "t_start", 0.0) - 0.15
+        t1 = getattr(self, "t_stop", time.time()) + 0.15
+        window = [ln for (t, ln) in self.lines if t0 <= t <= t1] or [ln for (_, ln) in
+                                                                      self.lines[-2:]]
+        for line in window:
             parts = [x.strip() for x in line.split(",")]
-            if len(parts) != 6:
+            if len(parts) != 7:
                 continue
             try:
-                sm.append(float(parts[0]))
-                mx.append(float(parts[1]))
+                sm.append(float(parts[1]))
+                mx.append(float(parts[2]))
             except ValueError:
                 continue
-            for n, v in zip(names, parts[2:]):
+            for n, v in zip(names, parts[3:]):
                 if v.lower().startswith("active"):
                     reasons.add(n)
         return {"sm_mhz": statistics.median(sm) if sm else None,
@@ -221,12 +234,14 @@ def run_gpu(args, rank, world):
     if world > 1:
         torch.distributed.barrier()
     torch.cuda.synchronize()
+    sampler.mark("t_start")
     t0 = time.perf_counter()
     rec = []
     for _ in range(args.steps):
         step(rec)
     torch.cuda.synchronize()
     wall = time.perf_counter() - t0
+    sampler.mark("t_stop")
     if world > 1:
         torch.distributed.barrier()
     clocks = sampler.stop() if rank == 0 else None

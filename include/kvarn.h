@@ -25,14 +25,16 @@
  *   q = rint((x - z) / s) (ties to even).  Metadata fp32, row scale folded in:
  *   dequantized rotated value yhat_td = c_d * (s'_t * q_td + z'_t).
  *
- * Page record: one per (page, KV head), KVARN_PAGE_BYTES bytes, 16-byte aligned:
+ * Page record: one per (page, KV head), KVARN_PAGE_BYTES bytes, 16-byte aligned;
+ * the K part then the V part, each contiguous (codes, row metadata, column
+ * scales), so that a reader can fetch either part with one bulk copy:
  *   [0,     8192) K codes, token-major: token t at 64 t; byte j = channel 2j
  *                 (bits 0-3) | channel 2j+1 (bits 4-7)
- *   [8192, 12288) V codes, channel-major: channel d at 8192 + 32 d; byte j =
+ *   [8192,  9216) K {s', z'} fp32 per token (token t at 8192 + 8 t)
+ *   [9216,  9728) K column scale c_d fp32
+ *   [9728, 13824) V codes, channel-major: channel d at 9728 + 32 d; byte j =
  *                 tokens 4j..4j+3 in bits 0-1, 2-3, 4-5, 6-7
- *   [12288,13312) K {s', z'} fp32 per token (token t at 12288 + 8 t)
- *   [13312,14336) V {s', z'} fp32 per token
- *   [14336,14848) K column scale c_d fp32
+ *   [13824,14848) V {s', z'} fp32 per token
  *   [14848,15360) V column scale c_d fp32
  * Pool = [num_pages][num_kv_heads][KVARN_PAGE_BYTES].  The newest len mod 128
  * tokens of a sequence stay fp16 in a caller-owned tail buffer

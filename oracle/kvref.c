@@ -45,14 +45,15 @@
  *   - attention: softmax(q . k * scale) v over every cached token (the
  *     quantized pages, then the newest len mod 128 tokens kept as fp16).
  *
- * Page record (one per page and KV head, 15360 bytes):
+ * Page record (one per page and KV head, 15360 bytes): the K part, then the
+ * V part, each holding codes, per-token metadata and per-channel scales:
  *   [0,     8192)  K codes, token-major: row t at 64 t; byte j holds channel
  *                  2j in bits 0-3 and channel 2j+1 in bits 4-7
- *   [8192, 12288)  V codes, channel-major: row d at 8192 + 32 d; byte j holds
+ *   [8192,  9216)  K per-token {s', z'} fp32 pairs, token t at 8192 + 8 t
+ *   [9216,  9728)  K per-channel c_d fp32
+ *   [9728, 13824)  V codes, channel-major: row d at 9728 + 32 d; byte j holds
  *                  tokens 4j..4j+3 in bits 0-1, 2-3, 4-5, 6-7
- *   [12288,13312)  K per-token {s', z'} fp32 pairs, token t at 12288 + 8 t
- *   [13312,14336)  V per-token {s', z'} fp32 pairs
- *   [14336,14848)  K per-channel c_d fp32
+ *   [13824,14848)  V per-token {s', z'} fp32 pairs
  *   [14848,15360)  V per-channel c_d fp32
  * Pool = [num_pages][num_kv_heads][15360 bytes].
  */
@@ -65,10 +66,10 @@
 #define NTOK 128           /* tokens per block / page */
 #define REC_BYTES 15360
 #define OFF_KCODES 0
-#define OFF_VCODES 8192
-#define OFF_KSZ 12288
-#define OFF_VSZ 13312
-#define OFF_KC 14336
+#define OFF_KSZ 8192
+#define OFF_KC 9216
+#define OFF_VCODES 9728
+#define OFF_VSZ 13824
 #define OFF_VC 14848
 
 /* ------------------------------------------------------------------ */

@@ -10,15 +10,23 @@ namespace kvarn {
 cudaError_t launch_decode_simple(const DecodeArgs& a, cudaStream_t s);
 cudaError_t launch_decode_mma(const DecodeArgs& a, cudaStream_t s);
 bool decode_mma_supported(int g);
+int decode_mma_ctas_per_sm(int g);
 
 static inline bool aligned16(const void* p) { return ((uintptr_t)p & 15u) == 0; }
 
 DecodePlan decode_plan(int batch, int hq, int hkv, int max_seq) {
   DecodePlan p{};
-  const int64_t units = (int64_t)max_seq / kT + 1;             // pages + the tail
+  // Work unit = one page of one (sequence, KV head); the fp16 tail rides with
+  // the split that holds the last page.  Pages per split are chosen so that
+  // the whole grid is resident at once (one wave: no straggling second wave),
+  // with at least 2 pages per split to bound the merge traffic.
+  const int g = hq / hkv;
+  const int64_t units = max_seq / kT > 0 ? (int64_t)max_seq / kT : 1;
   const int64_t total = (int64_t)batch * hkv * units;
-  int64_t pps = (total + kNumSMs * 16 - 1) / (kNumSMs * 16);   // ~16 CTAs per SM
-  if (pps < 4) pps = 4;
+  const int64_t slots =
+      (int64_t)kNumSMs * (decode_mma_supported(g) ? decode_mma_ctas_per_sm(g) : 4);
+  int64_t pps = (total + slots - 1) / slots;
+  if (pps < 2) pps = 2;
   if (pps > 64) pps = 64;
   p.pages_per_split = (int)pps;
   p.nsplit = (int)((units + pps - 1) / pps);

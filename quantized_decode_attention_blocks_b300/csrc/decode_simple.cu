@@ -85,12 +85,13 @@ __global__ void __launch_bounds__(kThreads) decode_simple_kernel(DecodeArgs a) {
     if (split == 0 && kvh == 0 && tid == 0) report(a.status, KVARN_STATUS_BAD_LENGTH);
     len = 0;
   }
+  // pages are split in runs of pages_per_split; the split holding the last
+  // page also takes the fp16 tail (one extra unit)
   const int nfull = len / kT, rem = len % kT;
-  const int units = nfull + (rem > 0 ? 1 : 0);
-  const int nsb = units > 0 ? (units + a.pages_per_split - 1) / a.pages_per_split : 1;
+  const int nsb = nfull > 0 ? (nfull + a.pages_per_split - 1) / a.pages_per_split : 1;
   if (split >= nsb) return;
   const int u0 = split * a.pages_per_split;
-  const int u1 = min(units, u0 + a.pages_per_split);
+  const int u1 = min(nfull, u0 + a.pages_per_split) + ((split == nsb - 1 && rem > 0) ? 1 : 0);
 
   // queries of the group: raw and rotated
   const __half* qb = a.q + ((int64_t)b * a.hq + (int64_t)kvh * g) * kD;

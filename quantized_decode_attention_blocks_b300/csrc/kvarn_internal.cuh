@@ -15,11 +15,13 @@ constexpr int kD = 128;           // head_dim = group size
 constexpr int kT = 128;           // tokens per page
 constexpr int kRec = 15360;       // bytes per record
 constexpr int kOffKCodes = 0;     // [128 tokens][64 B]
-constexpr int kOffVCodes = 8192;  // [128 channels][32 B]
-constexpr int kOffKSZ = 12288;    // [128 tokens]{s', z'} fp32
-constexpr int kOffVSZ = 13312;
-constexpr int kOffKC = 14336;     // [128 channels] fp32
+constexpr int kOffKSZ = 8192;     // [128 tokens]{s', z'} fp32
+constexpr int kOffKC = 9216;      // [128 channels] fp32
+constexpr int kOffVCodes = 9728;  // [128 channels][32 B]
+constexpr int kOffVSZ = 13824;
 constexpr int kOffVC = 14848;
+constexpr int kKPart = 9728;      // K part: [0, 9728)
+constexpr int kVPart = kRec - kKPart;  // V part: [9728, 15360)
 constexpr int kMaxG = 16;         // query heads per KV head supported
 constexpr int kMaxIters = 64;     // Sinkhorn iterations accepted
 constexpr int kNumSMs = 148;      // B300

@@ -390,9 +390,7 @@ def test_prefill_tail_copy_and_page_placement(oracle):
             for h in range(w.hkv):
                 solo = oracle.quantize_tile(k[b, j * 128:(j + 1) * 128, h], False, 2)["rec"]
                 got = st["pool"][table[b, j], h]
-                assert np.array_equal(got[:8192], solo[:8192])
-                assert np.array_equal(got[12288:13312], solo[12288:13312])
-                assert np.array_equal(got[14336:14848], solo[14336:14848])
+                assert np.array_equal(got[:9728], solo[:9728])   # the whole K part
 
 
 def test_append_fills_page_like_prefill(oracle):
