@@ -164,6 +164,32 @@ int kvarn_decode_attention(const kvarn_config_t *cfg, const void *q, const void 
                            void *out, void *workspace, size_t workspace_bytes,
                            int32_t *status, kvarn_stream_t stream);
 
+/* Size of the scratch array built into the library for
+ * kvarn_decode_attention_noalloc: 16 MiB, held on every GPU that loads it. */
+#define KVARN_NOALLOC_SCRATCH_BYTES (16u << 20)
+
+/* Decode attention without any caller-provided workspace.  The pages have no
+ * counterpart to this call; it exists for callers that cannot allocate GPU
+ * memory, such as plugin hosts that hand a kernel only its inputs and outputs,
+ * or serving loops that cannot afford the device synchronisation cudaMalloc
+ * brings.  It computes exactly what kvarn_decode_attention computes, with the
+ * same arguments minus the workspace, using instead a fixed array of
+ * KVARN_NOALLOC_SCRATCH_BYTES inside the library.
+ *   - Returns KVARN_ERR_WORKSPACE, launching nothing, when (batch, max_seq)
+ *     would need more scratch than that (kvarn_decode_workspace_bytes gives
+ *     the need).  Allocates nothing and frees nothing.
+ *   - The first call on each device looks up the array's device address with
+ *     that device current; make that first call before any stream capture.
+ *   - Every call shares the one array and clears its ticket counters itself;
+ *     calls whose executions overlap on the GPU race on it, so serialise them
+ *     (one stream, or events between streams). */
+int kvarn_decode_attention_noalloc(const kvarn_config_t *cfg, const void *q, const void *pool,
+                                   int64_t num_pages, const int32_t *block_table,
+                                   int max_blocks, const int32_t *seq_lens, int batch,
+                                   int max_seq, const void *tail_k, const void *tail_v,
+                                   float softmax_scale, void *out, int32_t *status,
+                                   kvarn_stream_t stream);
+
 /* Diagnosis: dequantizes `n` page records into float32 rotated-space tiles.
  *   records   [n][15360] bytes (e.g. pool + page*Hkv*15360, one record per
  *             (page, head) in order)

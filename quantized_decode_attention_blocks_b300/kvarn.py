@@ -62,6 +62,8 @@ SIGNATURES = {
     "kvarn_decode_workspace_bytes": (ctypes.c_size_t, [ctypes.POINTER(Config), _I, _I]),
     "kvarn_decode_attention": (_I, [ctypes.POINTER(Config), _P, _P, _L, _P, _I, _P, _I, _I, _P,
                                     _P, ctypes.c_float, _P, _P, ctypes.c_size_t, _P, _P]),
+    "kvarn_decode_attention_noalloc": (_I, [ctypes.POINTER(Config), _P, _P, _L, _P, _I, _P, _I,
+                                            _I, _P, _P, ctypes.c_float, _P, _P, _P]),
     "kvarn_dequantize_pages": (_I, [_P, _L, _P, _P, _P]),
     "kvarn_status_string": (ctypes.c_char_p, [_I]),
     "kvarn_version": (ctypes.c_char_p, []),
@@ -203,6 +205,26 @@ def kvarn_decode_attention(cfg: Config, q: torch.Tensor, pool: torch.Tensor,
         block_table.shape[-1], _ptr(seq_lens), q.shape[0], int(max_seq), _ptr(tail_k),
         _ptr(tail_v), float(softmax_scale), _ptr(out), _ptr(workspace), ws_bytes, _ptr(status),
         _stream(stream)), "kvarn_decode_attention")
+    return out
+
+
+def kvarn_decode_attention_noalloc(cfg: Config, q: torch.Tensor, pool: torch.Tensor,
+                                   block_table: torch.Tensor, seq_lens: torch.Tensor,
+                                   max_seq: int, tail_k: torch.Tensor, tail_v: torch.Tensor,
+                                   out: torch.Tensor, softmax_scale: float = None,
+                                   status: Optional[torch.Tensor] = None,
+                                   stream=None) -> torch.Tensor:
+    """Decode attention for callers that cannot allocate: the split-K scratch
+    is a fixed array inside the library (see include/kvarn.h)."""
+    _dev(q, torch.float16, "q")
+    _dev(out, torch.float16, "out")
+    if softmax_scale is None:
+        softmax_scale = HEAD_DIM ** -0.5
+    _check(lib().kvarn_decode_attention_noalloc(
+        ctypes.byref(cfg), _ptr(q), _ptr(pool), pool.shape[0], _ptr(block_table),
+        block_table.shape[-1], _ptr(seq_lens), q.shape[0], int(max_seq), _ptr(tail_k),
+        _ptr(tail_v), float(softmax_scale), _ptr(out), _ptr(status), _stream(stream)),
+        "kvarn_decode_attention_noalloc")
     return out
 
 
