@@ -32,8 +32,13 @@
  *                 (bits 0-3) | channel 2j+1 (bits 4-7)
  *   [8192,  9216) K {s', z'} fp32 per token (token t at 8192 + 8 t)
  *   [9216,  9728) K column scale c_d fp32
- *   [9728, 13824) V codes, channel-major: channel d at 9728 + 32 d; byte j =
- *                 tokens 4j..4j+3 in bits 0-1, 2-3, 4-5, 6-7
+ *   [9728, 13824) V codes, 2 bits each, 1024 little-endian 32-bit words:
+ *                 with channel c = 16m + 8e + r (m < 8, e < 2, r < 8) and
+ *                 token t = 16k + 8f + 2j + s (k < 8, f < 2, j < 4, s < 2),
+ *                 the code of (c, t) is bits 2i, 2i+1 with i = 2(k mod 4) +
+ *                 f + 8s of word 128m + 16r + 4j + 2e + floor(k/4) (a fixed
+ *                 permutation of channel-major order that lets a decode warp
+ *                 fetch each tensor-core fragment with one 16-byte load)
  *   [13824,14848) V {s', z'} fp32 per token
  *   [14848,15360) V column scale c_d fp32
  * Pool = [num_pages][num_kv_heads][KVARN_PAGE_BYTES].  The newest len mod 128
@@ -165,8 +170,11 @@ int kvarn_decode_attention(const kvarn_config_t *cfg, const void *q, const void 
                            int32_t *status, kvarn_stream_t stream);
 
 /* Size of the scratch array built into the library for
- * kvarn_decode_attention_noalloc: 16 MiB, held on every GPU that loads it. */
-#define KVARN_NOALLOC_SCRATCH_BYTES (16u << 20)
+ * kvarn_decode_attention_noalloc: 4 MiB, held on every GPU that loads it.
+ * Every configuration with Hq/Hkv <= 8 fits in it whatever its batch and
+ * lengths (the split plan keeps the grid to one wave); larger groups with
+ * long sequences may not. */
+#define KVARN_NOALLOC_SCRATCH_BYTES (4u << 20)
 
 /* Decode attention without any caller-provided workspace.  The pages have no
  * counterpart to this call; it exists for callers that cannot allocate GPU

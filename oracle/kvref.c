@@ -51,8 +51,13 @@
  *                  2j in bits 0-3 and channel 2j+1 in bits 4-7
  *   [8192,  9216)  K per-token {s', z'} fp32 pairs, token t at 8192 + 8 t
  *   [9216,  9728)  K per-channel c_d fp32
- *   [9728, 13824)  V codes, channel-major: row d at 9728 + 32 d; byte j holds
- *                  tokens 4j..4j+3 in bits 0-1, 2-3, 4-5, 6-7
+ *   [9728, 13824)  V codes, 2 bits each, as 1024 little-endian 32-bit words
+ *                  in 16-channel groups: write channel c = 16m + 8e + r
+ *                  (m < 8, e < 2, r < 8) and token t = 16k + 8f + 2j + s
+ *                  (k < 8, f < 2, j < 4, s < 2); the code of (c, t) is crumb
+ *                  i = 2(k mod 4) + f + 8s (bits 2i, 2i+1) of word
+ *                  128m + 16r + 4j + 2e + floor(k/4).  This is a fixed
+ *                  permutation of the 4096 code bytes (see kvref_v_code_pos)
  *   [13824,14848)  V per-token {s', z'} fp32 pairs
  *   [14848,15360)  V per-channel c_d fp32
  * Pool = [num_pages][num_kv_heads][15360 bytes].
@@ -265,7 +270,22 @@ void kvref_rtn(const double *Y, const double *r, const float *c32, int bits,
 static void put_f32(uint8_t *p, float v) { memcpy(p, &v, 4); }
 static float get_f32(const uint8_t *p) { float v; memcpy(&v, p, 4); return v; }
 
-/* is_v = 0: K part (4-bit, token-major); is_v = 1: V part (2-bit, channel-major). */
+/* Where the 2-bit V code of channel c, token t lives inside the V code region:
+ * byte offset and bit shift.  The split of c and t into digits and the word /
+ * crumb formulas are the layout stated in the header comment of this file:
+ * c = 16m + 8e + r, t = 16k + 8f + 2j + s, word 128m + 16r + 4j + 2e + k/4,
+ * crumb 2(k%4) + f + 8s, little-endian words. */
+void kvref_v_code_pos(int c, int t, int *byte, int *shift)
+{
+    int m = c / 16, e = (c / 8) % 2, r = c % 8;
+    int k = t / 16, f = (t / 8) % 2, j = (t / 2) % 4, s = t % 2;
+    int word = 128 * m + 16 * r + 4 * j + 2 * e + k / 4;
+    int crumb = 2 * (k % 4) + f + 8 * s;
+    *byte = 4 * word + crumb / 4;
+    *shift = 2 * (crumb % 4);
+}
+
+/* is_v = 0: K part (4-bit, token-major); is_v = 1: V part (2-bit, permuted). */
 void kvref_pack_part(uint8_t *rec, int is_v, const uint8_t *q, const float *s32,
                      const float *z32, const float *c32)
 {
@@ -276,12 +296,13 @@ void kvref_pack_part(uint8_t *rec, int is_v, const uint8_t *q, const float *s32,
                 rec[OFF_KCODES + t * 64 + j] =
                     (uint8_t)((q[t * NCH + 2 * j] & 15) | ((q[t * NCH + 2 * j + 1] & 15) << 4));
     } else {
-        for (d = 0; d < NCH; ++d)
-            for (j = 0; j < NTOK / 4; ++j)
-                rec[OFF_VCODES + d * 32 + j] =
-                    (uint8_t)((q[(4 * j) * NCH + d] & 3) | ((q[(4 * j + 1) * NCH + d] & 3) << 2) |
-                              ((q[(4 * j + 2) * NCH + d] & 3) << 4) |
-                              ((q[(4 * j + 3) * NCH + d] & 3) << 6));
+        memset(rec + OFF_VCODES, 0, NTOK * NCH / 4);
+        for (t = 0; t < NTOK; ++t)
+            for (d = 0; d < NCH; ++d) {
+                int byte, shift;
+                kvref_v_code_pos(d, t, &byte, &shift);
+                rec[OFF_VCODES + byte] |= (uint8_t)((q[t * NCH + d] & 3) << shift);
+            }
     }
     for (t = 0; t < NTOK; ++t) {
         put_f32(rec + (is_v ? OFF_VSZ : OFF_KSZ) + 8 * t, s32[t]);
@@ -301,8 +322,9 @@ void kvref_unpack_part(const uint8_t *rec, int is_v, uint8_t *q, float *s32, flo
                 uint8_t byte = rec[OFF_KCODES + t * 64 + d / 2];
                 q[t * NCH + d] = (uint8_t)((byte >> (4 * (d % 2))) & 15);
             } else {
-                uint8_t byte = rec[OFF_VCODES + d * 32 + t / 4];
-                q[t * NCH + d] = (uint8_t)((byte >> (2 * (t % 4))) & 3);
+                int byte, shift;
+                kvref_v_code_pos(d, t, &byte, &shift);
+                q[t * NCH + d] = (uint8_t)((rec[OFF_VCODES + byte] >> shift) & 3);
             }
         }
         s32[t] = get_f32(rec + (is_v ? OFF_VSZ : OFF_KSZ) + 8 * t);

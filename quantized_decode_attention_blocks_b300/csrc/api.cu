@@ -11,27 +11,32 @@ cudaError_t launch_decode_simple(const DecodeArgs& a, cudaStream_t s);
 cudaError_t launch_decode_mma(const DecodeArgs& a, cudaStream_t s);
 bool decode_mma_supported(int g);
 int decode_mma_ctas_per_sm(int g);
+int decode_mma_warps();
 
 static inline bool aligned16(const void* p) { return ((uintptr_t)p & 15u) == 0; }
 
 DecodePlan decode_plan(int batch, int hq, int hkv, int max_seq) {
   DecodePlan p{};
   // Work unit = one page of one (sequence, KV head); the fp16 tail rides with
-  // the split that holds the last page.  Pages per split are chosen so that
-  // the whole grid is resident at once (one wave: no straggling second wave),
-  // with at least 2 pages per split to bound the merge traffic.
+  // the split that holds the last page.  The number of splits per (sequence,
+  // KV head) is the largest that keeps the whole grid resident at once (one
+  // wave, no straggling second wave), but no more than gives every warp of a
+  // tensor-core CTA (or two pages of a CUDA-core CTA) something to do.
   const int g = hq / hkv;
+  const bool mma = decode_mma_supported(g);
   const int64_t units = max_seq / kT > 0 ? (int64_t)max_seq / kT : 1;
-  const int64_t total = (int64_t)batch * hkv * units;
-  const int64_t slots =
-      (int64_t)kNumSMs * (decode_mma_supported(g) ? decode_mma_ctas_per_sm(g) : 4);
-  int64_t pps = (total + slots - 1) / slots;
-  if (pps < 2) pps = 2;
-  if (pps > 64) pps = 64;
+  const int64_t groups = (int64_t)batch * hkv;
+  const int64_t slots = (int64_t)kNumSMs * (mma ? decode_mma_ctas_per_sm(g) : 4);
+  const int64_t min_pages = mma ? decode_mma_warps() : 2;
+  int64_t ns = slots / groups;
+  const int64_t ns_cap = (units + min_pages - 1) / min_pages;
+  if (ns > ns_cap) ns = ns_cap;
+  if (ns < 1) ns = 1;
+  const int64_t pps = (units + ns - 1) / ns;
   p.pages_per_split = (int)pps;
   p.nsplit = (int)((units + pps - 1) / pps);
   if (p.nsplit > 1) {
-    p.part_bytes = (size_t)batch * hq * p.nsplit * (2 + kD) * sizeof(float);
+    p.part_bytes = (size_t)batch * hq * p.nsplit * kPartStride * sizeof(float);
     p.part_bytes = (p.part_bytes + 255) & ~(size_t)255;
     p.count_bytes = ((size_t)batch * hkv * sizeof(int) + 255) & ~(size_t)255;
   }

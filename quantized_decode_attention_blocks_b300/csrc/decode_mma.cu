@@ -12,21 +12,26 @@
 //   o = H (sum_t p_t yhatV_t) + sum_tail p_t v_t,
 //   sum_t p_t yhatV_td = cV_d (sum_t (p_t s'V_t) qV_td + sum_t p_t z'V_t).
 // The two inner sums over codes are dense contractions of a 128x128 page of
-// small integers (exact in fp16) with a query-side factor; they run as
-// mma.sync with the codes unpacked straight into A fragments by bit tricks
-// (1024 + q is an exact fp16; subtracting 1024 leaves q).  The query-side
-// factor is split into an fp16 pair hi + lo (and scaled by a power of two to
-// stay in fp16 range), giving ~22 significant bits with fp32 accumulation.
+// small integers with a query-side factor.  They run as mma.sync with the
+// codes fed straight from the packed words: one AND leaves a code q at bit
+// position 4i (K) or 2i (V) of each 16-bit half, which read as an fp16 is the
+// subnormal q * 2^(4i-24) (resp. 2^(2i-24)), exact.  The power of two is
+// undone on the query side, which is split into an fp16 pair hi + lo (~21
+// significant bits, scaled by a power of two into range); the tensor core
+// accumulates the exact products in fp32.
 //
-// One CTA = one warp = one (sequence, KV head, split of pages); the g query
-// heads of the group share every page it reads.  Each warp streams its pages
-// through a private double buffer: cp.async.bulk (TMA engine) copies the
-// 15360-byte record of (page, KV head) into shared memory, completing on an
-// mbarrier, while the warp computes on the other buffer.  Every wait is
-// bounded; on expiry the CTA reports KVARN_STATUS_TIMEOUT and drains.
-// The split owning the end of the sequence also adds the fp16 tail.  Partial
-// softmax states of the splits are merged (log-sum-exp) by the last CTA of
-// each (sequence, KV head) to arrive, in the same launch.
+// CTA = 4 warps, each an independent stream over the pages of its split of
+// one (sequence, KV head): warp w takes pages u0 + w, u0 + w + 4, ...  Each
+// warp double-buffers one 15360-byte page record in shared memory: the K part
+// and the V part arrive by cp.async.bulk (TMA engine) on two mbarriers; the
+// next page's K part loads while this page's values are summed, its V part
+// while the next scores are computed.  The probabilities move from the score
+// fragments to the value-sum fragments in registers (movmatrix transpose).
+// Every wait is bounded; on expiry the warp reports KVARN_STATUS_TIMEOUT and
+// drains its copies.  The four warps' softmax states are merged in shared
+// memory, rotated back to plain space once per CTA, the split holding the end
+// of the sequence adds the fp16 tail, and the splits of one (sequence, KV
+// head) are merged (log-sum-exp) by the last CTA to arrive, in the same launch.
 #include "kvarn_internal.cuh"
 #include "ptx.cuh"
 
@@ -35,37 +40,53 @@ namespace {
 
 using namespace ptx;
 
-constexpr uint32_t kMagic = 0x64006400u;       // fp16x2 (1024, 1024)
-constexpr uint32_t kH16 = 0x2C002C00u;         // fp16x2 (1/16, 1/16)
-constexpr uint32_t kNeg64 = 0xD400D400u;       // fp16x2 (-64, -64)
-constexpr uint32_t kQuarter = 0x34003400u;     // fp16x2 (1/4, 1/4)
-constexpr uint32_t kNeg256 = 0xDC00DC00u;      // fp16x2 (-256, -256)
+constexpr int kWarps = 4;
+constexpr int kThreads = 32 * kWarps;
 constexpr uint64_t kWaitLimitNs = 2000000000ull;
 constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kTwo24 = 16777216.0f;
 
 template <int NT>
 struct __align__(128) MmaSmem {
-  uint8_t kst[kKPart];           // K part of the current page record
-  uint8_t vst[kVPart];           // V part of the current page record
-  float qrot[4 * NT][kD];        // H q per (padded) head
-  uint32_t pbuf[kT * 4 * NT];    // P' hi/lo, [token][n-tile][4 x f16x2]
-  uint64_t bar[2];               // 0: K part landed, 1: V part landed
-  float mh[4 * NT], lh[4 * NT];
+  uint8_t rec[kWarps][kRec];     // per warp: K part at 0, V part at kKPart
+  float qrot[4 * NT][kD];        // H q per (padded) query head of the group
+  float O[4 * NT][kD];           // the CTA's merged accumulator
+  float ptail[4 * NT][kT];       // fp16-tail probabilities
+  uint64_t bar[kWarps][2];       // per warp: 0 = K part landed, 1 = V part landed
+  float mh[4 * NT], lh[4 * NT], al[4 * NT];
+  float red[kWarps][4 * NT];
+  int ticket;
 };
 
-// nibble pairs of a 32-bit word: (n_j, n_{j+4}) as an fp16x2
-__device__ __forceinline__ uint32_t nib_lo(uint32_t w) {   // j = 0 (or 2 after >> 8)
-  return hsub2_u32(lop_and_or(w, 0x000F000Fu, kMagic), kMagic);
+__device__ __forceinline__ float ex2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
 }
-__device__ __forceinline__ uint32_t nib_hi(uint32_t w) {   // j = 1 (or 3 after >> 8)
-  return hfma2_u32(lop_and_or(w, 0x00F000F0u, kMagic), kH16, kNeg64);
+
+__device__ __forceinline__ float max3(float a, float b, float c) {
+  float d;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
 }
-// crumb pairs of a 32-bit word shifted right by 4i: (c_{2i}, c_{2i+8}) and (c_{2i+1}, c_{2i+9})
-__device__ __forceinline__ uint32_t crumb_a(uint32_t x) {
-  return hsub2_u32(lop_and_or(x, 0x00030003u, kMagic), kMagic);
+
+// fp16x2 with `first` in the low half
+__device__ __forceinline__ uint32_t pack2(float first, float second) {
+  uint32_t r;
+  asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(second), "f"(first));
+  return r;
 }
-__device__ __forceinline__ uint32_t crumb_b(uint32_t x) {
-  return hfma2_u32(lop_and_or(x, 0x000C000Cu, kMagic), kQuarter, kNeg256);
+
+__device__ __forceinline__ uint32_t movm_trans(uint32_t x) {
+  uint32_t r;
+  asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(r) : "r"(x));
+  return r;
+}
+
+// x with its 13 low mantissa bits cleared: 11 significant bits, exactly an
+// fp16 when |x| is in the fp16 normal range; x - head is exact in fp32.
+__device__ __forceinline__ float head11(float x) {
+  return __uint_as_float(__float_as_uint(x) & 0xFFFFE000u);
 }
 
 // 2^k scale that maps amax into [2^14, 2^15), and its inverse.
@@ -74,15 +95,6 @@ __device__ __forceinline__ void pow2_scale(float amax, float& s, float& inv) {
   const int se = min(max(268 - e, 1), 253);
   s = __int_as_float(se << 23);
   inv = __int_as_float((254 - se) << 23);
-}
-
-// Veltkamp split of x into an 11-bit head (exact in fp16 when in range) and a
-// tail.  The _rn intrinsics keep the compiler from contracting c - x into an
-// FMA, which would return x itself as the head.
-__device__ __forceinline__ void split11(float x, float& hi, float& lo) {
-  const float c = __fmul_rn(x, 8193.0f);   // 2^13 + 1: 24 - 13 = 11 head bits
-  hi = __fsub_rn(c, __fsub_rn(c, x));
-  lo = __fsub_rn(x, hi);
 }
 
 __device__ __forceinline__ float warp_max_r(float x) {   // over lanes sharing lane & 3
@@ -96,36 +108,52 @@ __device__ __forceinline__ float warp_sum_r(float x) {
   return x + __shfl_xor_sync(0xffffffffu, x, 16);
 }
 
-// In-place scaled Walsh-Hadamard transform of n rows of 128 floats, one warp.
-__device__ __forceinline__ void warp_fwht(float (*v)[kD], int n) {
-  const int lane = threadIdx.x;
+// In-place scaled Walsh-Hadamard transform of n rows of 128 floats by the
+// whole CTA (n * 64 butterflies per stage).
+__device__ __forceinline__ void cta_fwht(float (*v)[kD], int n) {
+  const int tid = threadIdx.x;
   for (int s = 1; s < kD; s <<= 1) {
-    for (int i = lane; i < n * (kD / 2); i += 32) {
+    for (int i = tid; i < n * (kD / 2); i += kThreads) {
       const int h = i >> 6, k = i & 63;
       const int lo = ((k & ~(s - 1)) << 1) | (k & (s - 1));
       const float x = v[h][lo], y = v[h][lo + s];
-      v[h][lo] = x + y;
-      v[h][lo + s] = x - y;
+      if (s == kD / 2) {
+        v[h][lo] = (x + y) * kInvSqrt128;
+        v[h][lo + s] = (x - y) * kInvSqrt128;
+      } else {
+        v[h][lo] = x + y;
+        v[h][lo + s] = x - y;
+      }
     }
-    __syncwarp();
+    __syncthreads();
   }
-  for (int i = lane; i < n * kD; i += 32) v[i >> 7][i & 127] *= kInvSqrt128;
-  __syncwarp();
+}
+
+// mask selecting crumb p (0..4) of both 16-bit halves
+__device__ __forceinline__ constexpr uint32_t cmask(int p) { return 0x00030003u << (2 * p); }
+
+// 1 / (power of two carried by the V code of a token in k-tile kb, half f)
+__device__ __forceinline__ constexpr float vpos_inv(int kb, int f) {
+  return (kb & 3) == 0 ? (f ? 0.25f : 1.f)
+       : (kb & 3) == 1 ? (f ? 1.f / 64 : 1.f / 16)
+       : (kb & 3) == 2 ? (f ? 1.f : 1.f / 256)
+                       : (f ? 1.f / 16 : 0.25f);
 }
 
 template <int NT>
-__global__ void __launch_bounds__(32) decode_mma_kernel(DecodeArgs a) {
+__global__ void __launch_bounds__(kThreads, 3) decode_mma_kernel(DecodeArgs a) {
   extern __shared__ __align__(128) uint8_t smem_raw[];
   MmaSmem<NT>& S = *reinterpret_cast<MmaSmem<NT>*>(smem_raw);
   constexpr int G = 4 * NT;
   const int split = blockIdx.x, kvh = blockIdx.y, b = blockIdx.z;
-  const int lane = threadIdx.x, r = lane >> 2, qi = lane & 3;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int r = lane >> 2, qi = lane & 3;
   const int g = a.g;
   const float sl2 = a.scale * kLog2e;   // scores are kept in log2 units
 
   int len = a.seq_lens[b];
   if (len < 0 || len > a.max_seq || len / kT > a.max_blocks) {
-    if (split == 0 && kvh == 0 && lane == 0) report(a.status, KVARN_STATUS_BAD_LENGTH);
+    if (split == 0 && kvh == 0 && tid == 0) report(a.status, KVARN_STATUS_BAD_LENGTH);
     len = 0;
   }
   const int nfull = len / kT, rem = len % kT;
@@ -135,9 +163,13 @@ __global__ void __launch_bounds__(32) decode_mma_kernel(DecodeArgs a) {
   const int u0 = split * pps, u1 = min(nfull, u0 + pps);
   const bool has_tail = split == nsb - 1 && rem > 0;
 
+  uint8_t* const kst = S.rec[warp];
+  uint8_t* const vst = S.rec[warp] + kKPart;
+  uint64_t* const kbar = &S.bar[warp][0];
+  uint64_t* const vbar = &S.bar[warp][1];
   if (lane == 0) {
-    mbar_init(&S.bar[0], 1);
-    mbar_init(&S.bar[1], 1);
+    mbar_init(kbar, 1);
+    mbar_init(vbar, 1);
     fence_mbar_init();
   }
   __syncwarp();
@@ -155,19 +187,20 @@ __global__ void __launch_bounds__(32) decode_mma_kernel(DecodeArgs a) {
   auto rec_of = [&](int64_t page) { return a.pool + (page * a.hkv + kvh) * (int64_t)kRec; };
   auto issue_k = [&](int64_t page) {
     if (lane == 0) {
-      mbar_arrive_expect_tx(&S.bar[0], kKPart);
-      bulk_g2s(S.kst, rec_of(page), kKPart, &S.bar[0]);
+      mbar_arrive_expect_tx(kbar, kKPart);
+      bulk_g2s(kst, rec_of(page), kKPart, kbar);
     }
   };
   auto issue_v = [&](int64_t page) {
     if (lane == 0) {
-      mbar_arrive_expect_tx(&S.bar[1], kVPart);
-      bulk_g2s(S.vst, rec_of(page) + kKPart, kVPart, &S.bar[1]);
+      mbar_arrive_expect_tx(vbar, kVPart);
+      bulk_g2s(vst, rec_of(page) + kKPart, kVPart, vbar);
     }
   };
 
-  // first page in flight while the query is rotated
-  int64_t cur = page_of(u0);
+  // this warp's first page in flight while the query is rotated
+  int u = u0 + warp;
+  int64_t cur = page_of(u);
   bool k_busy = false, v_busy = false;
   uint32_t kph = 0, vph = 0;
   if (cur >= 0) {
@@ -175,15 +208,32 @@ __global__ void __launch_bounds__(32) decode_mma_kernel(DecodeArgs a) {
     issue_v(cur);
     k_busy = v_busy = true;
   }
-  {
-    const __half* qb = a.q + ((int64_t)b * a.hq + (int64_t)kvh * g) * kD;
-    for (int i = lane; i < G * kD; i += 32) {
-      const int h = i >> 7;
-      S.qrot[h][i & 127] = h < g ? __half2float(qb[i]) : 0.f;
+
+  // ---- q~ = H q: warp w rotates heads w, w + 4 (lane holds channels 32i + lane) ----
+  const __half* qb = a.q + ((int64_t)b * a.hq + (int64_t)kvh * g) * kD;
+#pragma unroll
+  for (int hh = 0; hh < NT; ++hh) {
+    const int h = warp + kWarps * hh;
+    float x[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) x[i] = h < g ? __half2float(qb[h * kD + 32 * i + lane]) : 0.f;
+    // channel bits 5, 6 are local
+    float y0 = x[0] + x[1], y1 = x[0] - x[1], y2 = x[2] + x[3], y3 = x[2] - x[3];
+    x[0] = y0 + y2; x[2] = y0 - y2; x[1] = y1 + y3; x[3] = y1 - y3;
+    // channel bits 0..4 across lanes
+#pragma unroll
+    for (int m = 1; m < 32; m <<= 1) {
+      const bool up = lane & m;
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const float o = __shfl_xor_sync(0xffffffffu, x[i], m);
+        x[i] = up ? o - x[i] : x[i] + o;
+      }
     }
-    __syncwarp();
-    warp_fwht(S.qrot, G);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) S.qrot[h][32 * i + lane] = x[i] * kInvSqrt128;
   }
+  __syncthreads();
 
   float m[NT], l[NT], oacc[NT][16];
 #pragma unroll
@@ -195,69 +245,76 @@ __global__ void __launch_bounds__(32) decode_mma_kernel(DecodeArgs a) {
   }
   bool timed_out = false;
 
-  for (int u = u0; u < u1; ++u) {
+  for (; u < u1; u += kWarps) {
     float sc[NT][16];
     if (cur >= 0) {
-      if (!mbar_wait_bounded(&S.bar[0], kph, kWaitLimitNs)) {
+      if (!mbar_wait_warp(kbar, kph, kWaitLimitNs)) {
         timed_out = true;
         break;
       }
       kph ^= 1;
       k_busy = false;
-      const uint8_t* P = S.kst;
 
       // ---- query-side B fragments: qc = q~ * cK, scaled, split hi / lo ----
+      // B column n = r: head 4nt + (r >> 1), hi part (r even) or lo part (r
+      // odd); k rows 2qi.. of k-tile kb hold channels 32qi + c0, c0 + 4 with
+      // c0 = 8 (kb >> 1) + 2 (kb & 1) + slot.  The slot-1 channels meet codes
+      // carrying 16x (nibble at bits 4-7) and are pre-scaled by 1/16.
       uint32_t bq[NT][8][2];
-      float sumq[NT], invq[NT];
+      float sA[NT], sZ[NT];
+      const bool odd = r & 1;
 #pragma unroll
       for (int nt = 0; nt < NT; ++nt) {
         const int h = 4 * nt + (r >> 1);
         const float4* qv = reinterpret_cast<const float4*>(&S.qrot[h][32 * qi]);
-        const float4* cv = reinterpret_cast<const float4*>(P + kOffKC + 128 * qi);
+        const float4* cv = reinterpret_cast<const float4*>(kst + kOffKC + 128 * qi);
         float v[32];
-        float amax = 0.f, sum = 0.f;
+        float amax = 0.f;
+        float2 sum2 = make_float2(0.f, 0.f);
 #pragma unroll
         for (int k = 0; k < 8; ++k) {
           const float4 q4 = qv[k], c4 = cv[k];
-          v[4 * k + 0] = q4.x * c4.x;
-          v[4 * k + 1] = q4.y * c4.y;
-          v[4 * k + 2] = q4.z * c4.z;
-          v[4 * k + 3] = q4.w * c4.w;
-#pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            amax = fmaxf(amax, fabsf(v[4 * k + e]));
-            sum += v[4 * k + e];
-          }
+          const float2 p0 = __fmul2_rn(make_float2(q4.x, q4.y), make_float2(c4.x, c4.y));
+          const float2 p1 = __fmul2_rn(make_float2(q4.z, q4.w), make_float2(c4.z, c4.w));
+          v[4 * k + 0] = p0.x;
+          v[4 * k + 1] = p0.y;
+          v[4 * k + 2] = p1.x;
+          v[4 * k + 3] = p1.y;
+          amax = max3(amax, fabsf(p0.x), fabsf(p0.y));
+          amax = max3(amax, fabsf(p1.x), fabsf(p1.y));
+          sum2 = __fadd2_rn(sum2, __fadd2_rn(p0, p1));
         }
+        float sum = sum2.x + sum2.y;
         amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
         amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
         sum += __shfl_xor_sync(0xffffffffu, sum, 1);
         sum += __shfl_xor_sync(0xffffffffu, sum, 2);
         float scl, inv;
         pow2_scale(amax, scl, inv);
-        const bool lo_part = r & 1;
+        const float scl16 = scl * 0.0625f;
 #pragma unroll
         for (int kb = 0; kb < 8; ++kb) {
 #pragma unroll
           for (int slot = 0; slot < 2; ++slot) {
             const int c0 = 8 * (kb >> 1) + 2 * (kb & 1) + slot;
-            float h0, l0, h1, l1;
-            split11(v[c0] * scl, h0, l0);
-            split11(v[c0 + 4] * scl, h1, l1);
-            bq[nt][kb][slot] = lo_part ? pack_f16x2(l0, l1) : pack_f16x2(h0, h1);
+            const float f = slot ? scl16 : scl;
+            const float x0 = v[c0] * f, x1 = v[c0 + 4] * f;
+            const float h0 = head11(x0), h1 = head11(x1);
+            bq[nt][kb][slot] = odd ? pack2(x0 - h0, x1 - h1) : pack2(h0, h1);
           }
         }
-        // this lane's score head is 4nt + qi: fetch its sum and scale
-        sumq[nt] = __shfl_sync(0xffffffffu, sum, 8 * qi);
-        invq[nt] = __shfl_sync(0xffffffffu, inv, 8 * qi);
+        // this lane's score column pair (2qi, 2qi+1) is head 4nt + qi, held
+        // by lanes with r = 2qi: fetch that head's scale and sum
+        sA[nt] = __shfl_sync(0xffffffffu, inv, 8 * qi) * (kTwo24 * sl2);
+        sZ[nt] = __shfl_sync(0xffffffffu, sum, 8 * qi) * sl2;
       }
 
-      // ---- scores: K codes (A) x qc (B) ----
+      // ---- scores: K codes (A, rows = tokens) x qc (B) ----
 #pragma unroll
       for (int mt = 0; mt < 8; ++mt) {
         const int tA = 16 * mt + r, tB = tA + 8;
-        const uint4 wa = *reinterpret_cast<const uint4*>(P + kOffKCodes + 64 * tA + 16 * qi);
-        const uint4 wb = *reinterpret_cast<const uint4*>(P + kOffKCodes + 64 * tB + 16 * qi);
+        const uint4 wa = *reinterpret_cast<const uint4*>(kst + kOffKCodes + 64 * tA + 16 * qi);
+        const uint4 wb = *reinterpret_cast<const uint4*>(kst + kOffKCodes + 64 * tB + 16 * qi);
         const uint32_t WA[4] = {wa.x, wa.y, wa.z, wa.w};
         const uint32_t WB[4] = {wb.x, wb.y, wb.z, wb.w};
         float d[NT][4];
@@ -266,144 +323,141 @@ __global__ void __launch_bounds__(32) decode_mma_kernel(DecodeArgs a) {
 #pragma unroll
         for (int mw = 0; mw < 4; ++mw) {
           {
-            const uint32_t A[4] = {nib_lo(WA[mw]), nib_lo(WB[mw]), nib_hi(WA[mw]),
-                                   nib_hi(WB[mw])};
+            const uint32_t A[4] = {WA[mw] & 0x000F000Fu, WB[mw] & 0x000F000Fu,
+                                   WA[mw] & 0x00F000F0u, WB[mw] & 0x00F000F0u};
 #pragma unroll
             for (int nt = 0; nt < NT; ++nt)
               mma_16816(d[nt], A, bq[nt][2 * mw][0], bq[nt][2 * mw][1]);
           }
           {
             const uint32_t xa = WA[mw] >> 8, xb = WB[mw] >> 8;
-            const uint32_t A[4] = {nib_lo(xa), nib_lo(xb), nib_hi(xa), nib_hi(xb)};
+            const uint32_t A[4] = {xa & 0x000F000Fu, xb & 0x000F000Fu, xa & 0x00F000F0u,
+                                   xb & 0x00F000F0u};
 #pragma unroll
             for (int nt = 0; nt < NT; ++nt)
               mma_16816(d[nt], A, bq[nt][2 * mw + 1][0], bq[nt][2 * mw + 1][1]);
           }
         }
-        const float2 szA = *reinterpret_cast<const float2*>(P + kOffKSZ + 8 * tA);
-        const float2 szB = *reinterpret_cast<const float2*>(P + kOffKSZ + 8 * tB);
+        const float2 szA = *reinterpret_cast<const float2*>(kst + kOffKSZ + 8 * tA);
+        const float2 szB = *reinterpret_cast<const float2*>(kst + kOffKSZ + 8 * tB);
 #pragma unroll
         for (int nt = 0; nt < NT; ++nt) {
-          const float dA = (d[nt][0] + d[nt][1]) * invq[nt];
-          const float dB = (d[nt][2] + d[nt][3]) * invq[nt];
-          sc[nt][2 * mt] = sl2 * fmaf(szA.x, dA, szA.y * sumq[nt]);
-          sc[nt][2 * mt + 1] = sl2 * fmaf(szB.x, dB, szB.y * sumq[nt]);
+          sc[nt][2 * mt] = fmaf(szA.x * sA[nt], d[nt][0] + d[nt][1], szA.y * sZ[nt]);
+          sc[nt][2 * mt + 1] = fmaf(szB.x * sA[nt], d[nt][2] + d[nt][3], szB.y * sZ[nt]);
         }
       }
     }
     __syncwarp();   // the K part of this page is consumed
-    const int64_t nxt = page_of(u + 1);
+    const int64_t nxt = page_of(u + kWarps);
     if (nxt >= 0) {
       issue_k(nxt);
       k_busy = true;
     }
     if (cur >= 0) {
-      // ---- online softmax (log2 units) ----
+      // ---- online softmax (log2 units); l is a per-lane partial sum ----
       float alpha[NT];
 #pragma unroll
       for (int nt = 0; nt < NT; ++nt) {
-        float pm = sc[nt][0];
+        float pm = max3(sc[nt][0], sc[nt][1], sc[nt][2]);
 #pragma unroll
-        for (int j = 1; j < 16; ++j) pm = fmaxf(pm, sc[nt][j]);
+        for (int j = 3; j < 15; j += 2) pm = max3(pm, sc[nt][j], sc[nt][j + 1]);
+        pm = fmaxf(pm, sc[nt][15]);
         pm = warp_max_r(pm);
         const float mnew = fmaxf(m[nt], pm);
-        alpha[nt] = m[nt] == -INFINITY ? 0.f : exp2f(m[nt] - mnew);
+        alpha[nt] = ex2(m[nt] - mnew);
         m[nt] = mnew;
         float ls = 0.f;
 #pragma unroll
         for (int j = 0; j < 16; ++j) {
-          sc[nt][j] = exp2f(sc[nt][j] - mnew);   // now p
+          sc[nt][j] = ex2(sc[nt][j] - mnew);   // now p
           ls += sc[nt][j];
         }
         l[nt] = fmaf(l[nt], alpha[nt], ls);
       }
 
-      if (!mbar_wait_bounded(&S.bar[1], vph, kWaitLimitNs)) {
+      if (!mbar_wait_warp(vbar, vph, kWaitLimitNs)) {
         timed_out = true;
         break;
       }
       vph ^= 1;
       v_busy = false;
 
-      // ---- P' = p * s'V (scaled, hi/lo) into shared memory; z' sums ----
-      float smax = 0.f;
+      // ---- P' = p s'V (scaled, hi | lo) transposed into B fragments ----
+      // score slot j of this lane is token 16 (j >> 1) + 8 (j & 1) + r
       float2 szv[16];
+      float smax = 0.f;
 #pragma unroll
-      for (int mt = 0; mt < 8; ++mt) {
-        szv[2 * mt] = *reinterpret_cast<const float2*>(S.vst + (kOffVSZ - kKPart) + 8 * (16 * mt + r));
-        szv[2 * mt + 1] = *reinterpret_cast<const float2*>(S.vst + (kOffVSZ - kKPart) + 8 * (16 * mt + r + 8));
-        smax = fmaxf(smax, fmaxf(fabsf(szv[2 * mt].x), fabsf(szv[2 * mt + 1].x)));
+      for (int j = 0; j < 16; ++j) {
+        szv[j] = *reinterpret_cast<const float2*>(vst + (kOffVSZ - kKPart) +
+                                                  8 * (16 * (j >> 1) + 8 * (j & 1) + r));
+        smax = fmaxf(smax, szv[j].x);
       }
       smax = warp_max_r(smax);
       float fs, finv;
       pow2_scale(smax, fs, finv);
+      float sf[16];
+#pragma unroll
+      for (int j = 0; j < 16; ++j) sf[j] = szv[j].x * (fs * vpos_inv(j >> 1, j & 1));
+      uint32_t bp[NT][8][2];
       float zpage[NT];
 #pragma unroll
       for (int nt = 0; nt < NT; ++nt) {
         float zp = 0.f;
 #pragma unroll
         for (int j = 0; j < 16; ++j) {
-          const int tok = 16 * (j >> 1) + r + 8 * (j & 1);
-          float hi, lo;
-          split11(sc[nt][j] * szv[j].x * fs, hi, lo);
-          S.pbuf[tok * 4 * NT + nt * 4 + qi] = pack_f16x2(hi, lo);
+          const float x = sc[nt][j] * sf[j];
+          const float hi = head11(x);
+          bp[nt][j >> 1][j & 1] = movm_trans(pack2(hi, x - hi));
           zp = fmaf(sc[nt][j], szv[j].y, zp);
         }
         zpage[nt] = warp_sum_r(zp);
       }
-      __syncwarp();
 
-      // ---- value sum: V codes (A) x P' (B) ----
-      uint32_t bp[NT][8][2];
-      {
-        const int mu = lane >> 3, rho = lane & 7;
-        const int slot = mu & 1;
-#pragma unroll
-        for (int nt = 0; nt < NT; ++nt) {
-#pragma unroll
-          for (int kb0 = 0; kb0 < 8; kb0 += 2) {
-            const int kbm = kb0 + (mu >> 1);
-            const int tok = 16 * kbm + 2 * (rho >> 1) + slot + 8 * (rho & 1);
-            uint32_t rr[4];
-            ldmatrix_x4_trans(rr, smem_u32(&S.pbuf[tok * 4 * NT + nt * 4]));
-            bp[nt][kb0][0] = rr[0];
-            bp[nt][kb0][1] = rr[1];
-            bp[nt][kb0 + 1][0] = rr[2];
-            bp[nt][kb0 + 1][1] = rr[3];
-          }
-        }
-      }
-      const float* cvv = reinterpret_cast<const float*>(S.vst + (kOffVC - kKPart));
+      // ---- value sum: V codes (A, rows = channels) x P' (B) ----
+      const float fin = finv * kTwo24;
+      const float* cvv = reinterpret_cast<const float*>(vst + (kOffVC - kKPart));
 #pragma unroll
       for (int mc = 0; mc < 8; ++mc) {
-        const int cA = 16 * mc + r, cB = cA + 8;
-        const uint4 a0 = *reinterpret_cast<const uint4*>(S.vst + (kOffVCodes - kKPart) + 32 * cA);
-        const uint4 a1 = *reinterpret_cast<const uint4*>(S.vst + (kOffVCodes - kKPart) + 32 * cA + 16);
-        const uint4 b0 = *reinterpret_cast<const uint4*>(S.vst + (kOffVCodes - kKPart) + 32 * cB);
-        const uint4 b1 = *reinterpret_cast<const uint4*>(S.vst + (kOffVCodes - kKPart) + 32 * cB + 16);
-        const uint32_t WA[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
-        const uint32_t WB[8] = {b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w};
+        const uint4 w4 = *reinterpret_cast<const uint4*>(vst + (kOffVCodes - kKPart) + 512 * mc +
+                                                        16 * lane);
+        const uint32_t W[4] = {w4.x, w4.y, w4.z, w4.w};     // (e, h) = 00, 01, 10, 11
+        const uint32_t Wsh[4] = {w4.x >> 10, w4.y >> 10, w4.z >> 10, w4.w >> 10};
         float d[NT][4];
 #pragma unroll
         for (int nt = 0; nt < NT; ++nt) d[nt][0] = d[nt][1] = d[nt][2] = d[nt][3] = 0.f;
 #pragma unroll
         for (int kb = 0; kb < 8; ++kb) {
-          const uint32_t xa = WA[kb] >> (4 * qi), xb = WB[kb] >> (4 * qi);
-          const uint32_t A[4] = {crumb_a(xa), crumb_a(xb), crumb_b(xa), crumb_b(xb)};
+          const int hh = kb >> 2;
+          const uint32_t e0 = W[hh], e1 = W[2 + hh], s0 = Wsh[hh], s1 = Wsh[2 + hh];
+          uint32_t A[4];
+          switch (kb & 3) {
+            case 0:
+              A[0] = e0 & cmask(0); A[1] = e1 & cmask(0); A[2] = e0 & cmask(1); A[3] = e1 & cmask(1);
+              break;
+            case 1:
+              A[0] = e0 & cmask(2); A[1] = e1 & cmask(2); A[2] = e0 & cmask(3); A[3] = e1 & cmask(3);
+              break;
+            case 2:
+              A[0] = e0 & cmask(4); A[1] = e1 & cmask(4); A[2] = s0 & cmask(0); A[3] = s1 & cmask(0);
+              break;
+            default:
+              A[0] = s0 & cmask(1); A[1] = s1 & cmask(1); A[2] = s0 & cmask(2); A[3] = s1 & cmask(2);
+              break;
+          }
 #pragma unroll
           for (int nt = 0; nt < NT; ++nt) mma_16816(d[nt], A, bp[nt][kb][0], bp[nt][kb][1]);
         }
-        const float cvA = cvv[cA], cvB = cvv[cB];
+        const float cvA = cvv[16 * mc + r], cvB = cvv[16 * mc + 8 + r];
 #pragma unroll
         for (int nt = 0; nt < NT; ++nt) {
           oacc[nt][2 * mc] =
-              fmaf(oacc[nt][2 * mc], alpha[nt], cvA * fmaf(d[nt][0] + d[nt][1], finv, zpage[nt]));
+              fmaf(oacc[nt][2 * mc], alpha[nt], cvA * fmaf(d[nt][0] + d[nt][1], fin, zpage[nt]));
           oacc[nt][2 * mc + 1] = fmaf(oacc[nt][2 * mc + 1], alpha[nt],
-                                      cvB * fmaf(d[nt][2] + d[nt][3], finv, zpage[nt]));
+                                      cvB * fmaf(d[nt][2] + d[nt][3], fin, zpage[nt]));
         }
       }
     }
-    __syncwarp();   // the V part (and pbuf) of this page is consumed
+    __syncwarp();   // the V part of this page is consumed
     if (nxt >= 0) {
       issue_v(nxt);
       v_busy = true;
@@ -412,179 +466,244 @@ __global__ void __launch_bounds__(32) decode_mma_kernel(DecodeArgs a) {
   }
 
   if (timed_out) {
-    report(a.status, KVARN_STATUS_TIMEOUT);
-    // drain copies still in flight before the CTA's shared memory is released
-    if (k_busy) mbar_wait_bounded(&S.bar[0], kph, kWaitLimitNs);
-    if (v_busy) mbar_wait_bounded(&S.bar[1], vph, kWaitLimitNs);
+    if (lane == 0) report(a.status, KVARN_STATUS_TIMEOUT);
+    // drain copies still in flight before the buffer is reused or released
+    if (k_busy) mbar_wait_bounded(kbar, kph, kWaitLimitNs);
+    if (v_busy) mbar_wait_bounded(vbar, vph, kWaitLimitNs);
 #pragma unroll
-    for (int nt = 0; nt < NT; ++nt) m[nt] = -INFINITY, l[nt] = 0.f;
+    for (int nt = 0; nt < NT; ++nt) {
+      m[nt] = -INFINITY;
+      l[nt] = 0.f;
+#pragma unroll
+      for (int j = 0; j < 16; ++j) oacc[nt][j] = 0.f;
+    }
   }
+  __syncwarp();
 
-  // ---- flatten: rotated accumulator to shared memory, per-head m and l ----
-  float (*O)[kD] = reinterpret_cast<float (*)[kD]>(S.kst);              // G x 128 floats
-  float (*ptail)[kT] = reinterpret_cast<float (*)[kT]>(S.kst + G * kD * 4);  // G x 128
-  float (*qraw)[kD] = reinterpret_cast<float (*)[kD]>(S.pbuf);          // G x 128
+  // ---- this warp's state into its own buffer: [G]{m, l} then o[G][128] (rotated) ----
+  float* st = reinterpret_cast<float*>(kst);
+  float (*ow)[kD] = reinterpret_cast<float (*)[kD]>(kst + 2 * G * sizeof(float));
 #pragma unroll
   for (int nt = 0; nt < NT; ++nt) {
     const float lsum = warp_sum_r(l[nt]);
 #pragma unroll
     for (int mc = 0; mc < 8; ++mc) {
-      O[4 * nt + qi][16 * mc + r] = timed_out ? 0.f : oacc[nt][2 * mc];
-      O[4 * nt + qi][16 * mc + r + 8] = timed_out ? 0.f : oacc[nt][2 * mc + 1];
+      ow[4 * nt + qi][16 * mc + r] = oacc[nt][2 * mc];
+      ow[4 * nt + qi][16 * mc + 8 + r] = oacc[nt][2 * mc + 1];
     }
     if (r == 0) {
-      S.mh[4 * nt + qi] = m[nt];
-      S.lh[4 * nt + qi] = lsum;
+      st[2 * (4 * nt + qi)] = m[nt];
+      st[2 * (4 * nt + qi) + 1] = lsum;
     }
   }
-  __syncwarp();
-  warp_fwht(O, G);   // back to plain space
+  __syncthreads();
 
-  // ---- fp16 tail (plain space): lanes over tokens for scores, channels for V ----
-  float otail[G][4];
+  // ---- merge the warps' states, then rotate back to plain space ----
+  for (int i = tid; i < G * kD; i += kThreads) {
+    const int h = i >> 7, ch = i & 127;
+    float M = -INFINITY;
 #pragma unroll
-  for (int h = 0; h < G; ++h) otail[h][0] = otail[h][1] = otail[h][2] = otail[h][3] = 0.f;
-  if (has_tail && !timed_out) {
-    const __half* qb = a.q + ((int64_t)b * a.hq + (int64_t)kvh * g) * kD;
-    for (int i = lane; i < G * kD; i += 32) {
-      const int h = i >> 7;
-      qraw[h][i & 127] = h < g ? __half2float(qb[i]) : 0.f;
+    for (int w = 0; w < kWarps; ++w)
+      M = fmaxf(M, reinterpret_cast<const float*>(S.rec[w])[2 * h]);
+    float o = 0.f, L = 0.f;
+    if (M != -INFINITY) {
+#pragma unroll
+      for (int w = 0; w < kWarps; ++w) {
+        const float* sw = reinterpret_cast<const float*>(S.rec[w]);
+        const float wt = ex2(sw[2 * h] - M);
+        o = fmaf(wt, sw[2 * G + h * kD + ch], o);
+        L = fmaf(wt, sw[2 * h + 1], L);
+      }
     }
-    __syncwarp();
+    S.O[h][ch] = o;
+    if (ch == 0) {
+      S.mh[h] = M;
+      S.lh[h] = L;
+    }
+  }
+  __syncthreads();
+  cta_fwht(S.O, G);
+
+  // ---- fp16 tail (plain space): thread t scores tail token t ----
+  if (has_tail) {
     const __half* tkb = a.tail_k + ((int64_t)b * a.hkv + kvh) * kT * kD;
     const __half* tvb = a.tail_v + ((int64_t)b * a.hkv + kvh) * kT * kD;
-    float ts[4][G];
+    float ts[G];
 #pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      const int t = lane + 32 * j;
+    for (int h = 0; h < G; ++h) ts[h] = -INFINITY;
+    if (tid < rem) {
 #pragma unroll
-      for (int h = 0; h < G; ++h) ts[j][h] = -INFINITY;
-      if (t < rem) {
+      for (int h = 0; h < G; ++h) ts[h] = 0.f;
+      const uint4* kr = reinterpret_cast<const uint4*>(tkb + (int64_t)tid * kD);
+      for (int c = 0; c < kD / 8; ++c) {
+        const uint4 uq = __ldg(kr + c);
+        const __half2* h2 = reinterpret_cast<const __half2*>(&uq);
 #pragma unroll
-        for (int h = 0; h < G; ++h) ts[j][h] = 0.f;
-        const uint4* kr = reinterpret_cast<const uint4*>(tkb + (int64_t)t * kD);
-        for (int c = 0; c < kD / 8; ++c) {
-          const uint4 u = __ldg(kr + c);
-          const __half2* h2 = reinterpret_cast<const __half2*>(&u);
+        for (int e = 0; e < 4; ++e) {
+          const float2 kf = __half22float2(h2[e]);
 #pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            const float2 kf = __half22float2(h2[e]);
-#pragma unroll
-            for (int h = 0; h < G; ++h) {
-              ts[j][h] = fmaf(qraw[h][8 * c + 2 * e], kf.x, ts[j][h]);
-              ts[j][h] = fmaf(qraw[h][8 * c + 2 * e + 1], kf.y, ts[j][h]);
+          for (int h = 0; h < G; ++h) {
+            if (h < g) {
+              const __half2 q2 = *reinterpret_cast<const __half2*>(qb + h * kD + 8 * c + 2 * e);
+              const float2 qf = __half22float2(q2);
+              ts[h] = fmaf(qf.x, kf.x, fmaf(qf.y, kf.y, ts[h]));
             }
           }
         }
-#pragma unroll
-        for (int h = 0; h < G; ++h) ts[j][h] *= sl2;
       }
+#pragma unroll
+      for (int h = 0; h < G; ++h) ts[h] *= sl2;
     }
+    // per-head tail max over the CTA
 #pragma unroll
     for (int h = 0; h < G; ++h) {
-      float tm = fmaxf(fmaxf(ts[0][h], ts[1][h]), fmaxf(ts[2][h], ts[3][h]));
+      float x = ts[h];
 #pragma unroll
-      for (int o = 16; o > 0; o >>= 1) tm = fmaxf(tm, __shfl_xor_sync(0xffffffffu, tm, o));
-      const float mold = S.mh[h];
-      const float mnew = fmaxf(mold, tm);
-      const float al = mold == -INFINITY ? 0.f : exp2f(mold - mnew);
-      float ls = 0.f;
-#pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        ts[j][h] = ts[j][h] == -INFINITY ? 0.f : exp2f(ts[j][h] - mnew);
-        ls += ts[j][h];
-      }
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) ls += __shfl_xor_sync(0xffffffffu, ls, o);
-      __syncwarp();
-      if (lane == 0) {
-        S.mh[h] = mnew;
-        S.lh[h] = fmaf(S.lh[h], al, ls);
-      }
-#pragma unroll
-      for (int e = 0; e < 4; ++e) O[h][4 * lane + e] *= al;
+      for (int o = 16; o > 0; o >>= 1) x = fmaxf(x, __shfl_xor_sync(0xffffffffu, x, o));
+      if (lane == 0) S.red[warp][h] = x;
     }
-    // value sum of the tail: p through shared memory, lane owns channels 4*lane..+3
+    __syncthreads();
+    if (tid < G) {
+      float tm = S.red[0][tid];
+#pragma unroll
+      for (int w = 1; w < kWarps; ++w) tm = fmaxf(tm, S.red[w][tid]);
+      const float mold = S.mh[tid];
+      const float mnew = fmaxf(mold, tm);
+      S.al[tid] = ex2(mold - mnew);
+      S.mh[tid] = mnew;
+    }
+    __syncthreads();
+#pragma unroll
+    for (int h = 0; h < G; ++h) {
+      const float p = tid < rem ? ex2(ts[h] - S.mh[h]) : 0.f;
+      S.ptail[h][tid] = p;
+      float x = p;
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
+      ts[h] = x;
+    }
+    __syncthreads();   // red is reused below, ptail complete
 #pragma unroll
     for (int h = 0; h < G; ++h)
+      if (lane == 0) S.red[warp][h] = ts[h];
+    __syncthreads();
+    if (tid < G) {
+      float ls = 0.f;
 #pragma unroll
-      for (int j = 0; j < 4; ++j) ptail[h][lane + 32 * j] = ts[j][h];
-    __syncwarp();
-    for (int t = 0; t < rem; ++t) {
-      const uint2 vv = __ldg(reinterpret_cast<const uint2*>(tvb + (int64_t)t * kD + 4 * lane));
-      const float2 v01 = __half22float2(*reinterpret_cast<const __half2*>(&vv.x));
-      const float2 v23 = __half22float2(*reinterpret_cast<const __half2*>(&vv.y));
-#pragma unroll
-      for (int h = 0; h < G; ++h) {
-        const float p = ptail[h][t];
-        otail[h][0] = fmaf(p, v01.x, otail[h][0]);
-        otail[h][1] = fmaf(p, v01.y, otail[h][1]);
-        otail[h][2] = fmaf(p, v23.x, otail[h][2]);
-        otail[h][3] = fmaf(p, v23.y, otail[h][3]);
-      }
+      for (int w = 0; w < kWarps; ++w) ls += S.red[w][tid];
+      S.lh[tid] = fmaf(S.lh[tid], S.al[tid], ls);
     }
+    // value sum of the tail: thread (h, channel)
+    for (int i = tid; i < G * kD; i += kThreads) {
+      const int h = i >> 7, ch = i & 127;
+      float o = S.O[h][ch] * S.al[h];
+      for (int t = 0; t < rem; ++t)
+        o = fmaf(S.ptail[h][t], __half2float(tvb[(int64_t)t * kD + ch]), o);
+      S.O[h][ch] = o;
+    }
+    __syncthreads();
   }
-  __syncwarp();
 
   // ---- output: direct, or partial state + last-arriving merge ----
   __half* ob = a.out + ((int64_t)b * a.hq + (int64_t)kvh * g) * kD;
   if (nsb == 1) {
-    for (int h = 0; h < g; ++h) {
+    for (int i = tid; i < g * kD; i += kThreads) {
+      const int h = i >> 7, ch = i & 127;
       const float lh = S.lh[h];
-      const float il = lh > 0.f ? 1.f / lh : 0.f;
-      __half2 o01 = __floats2half2_rn((O[h][4 * lane] + otail[h][0]) * il,
-                                      (O[h][4 * lane + 1] + otail[h][1]) * il);
-      __half2 o23 = __floats2half2_rn((O[h][4 * lane + 2] + otail[h][2]) * il,
-                                      (O[h][4 * lane + 3] + otail[h][3]) * il);
+      ob[i] = __float2half_rn(lh > 0.f ? S.O[h][ch] / lh : 0.f);
+    }
+    return;
+  }
+  for (int i = tid; i < g * kD; i += kThreads) {
+    const int h = i >> 7, ch = i & 127;
+    float* Pp = a.ws_part + (((int64_t)b * a.hq + kvh * g + h) * a.nsplit + split) * kPartStride;
+    if (ch == 0) {
+      Pp[0] = S.mh[h];
+      Pp[1] = S.lh[h];
+    }
+    Pp[4 + ch] = S.O[h][ch];
+  }
+  __threadfence();
+  __syncthreads();
+  if (tid == 0) S.ticket = atomicAdd(a.ws_count + (int64_t)b * a.hkv + kvh, 1);
+  __syncthreads();
+  if (S.ticket != nsb - 1) return;
+  __threadfence();
+
+  // merge: warp w takes splits w, w + 4, ...; lane holds channels 4 lane .. + 3
+  for (int h = 0; h < g; ++h) {
+    const float* P0 = a.ws_part + (((int64_t)b * a.hq + kvh * g + h) * a.nsplit) * kPartStride;
+    float M = -INFINITY, L = 0.f;
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    constexpr int kU = 4;
+    for (int s0 = warp; s0 < nsb; s0 += kWarps * kU) {
+      float ms[kU], ls[kU];
+      float4 os[kU];
+#pragma unroll
+      for (int k = 0; k < kU; ++k) {
+        const int s2 = s0 + kWarps * k;
+        if (s2 < nsb) {
+          const float* Ps = P0 + (int64_t)s2 * kPartStride;
+          const float2 ml = __ldcg(reinterpret_cast<const float2*>(Ps));
+          ms[k] = ml.x;
+          ls[k] = ml.y;
+          os[k] = __ldcg(reinterpret_cast<const float4*>(Ps + 4) + lane);
+        } else {
+          ms[k] = -INFINITY;
+          ls[k] = 0.f;
+          os[k] = make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+      }
+#pragma unroll
+      for (int k = 0; k < kU; ++k) {
+        if (ms[k] == -INFINITY) continue;
+        const float Mn = fmaxf(M, ms[k]);
+        const float al = ex2(M - Mn), wt = ex2(ms[k] - Mn);
+        L = fmaf(L, al, wt * ls[k]);
+        acc.x = fmaf(acc.x, al, wt * os[k].x);
+        acc.y = fmaf(acc.y, al, wt * os[k].y);
+        acc.z = fmaf(acc.z, al, wt * os[k].z);
+        acc.w = fmaf(acc.w, al, wt * os[k].w);
+        M = Mn;
+      }
+    }
+    float* red = reinterpret_cast<float*>(S.rec[warp]);
+    if (lane == 0) {
+      red[0] = M;
+      red[1] = L;
+    }
+    reinterpret_cast<float4*>(red + 4)[lane] = acc;
+    __syncthreads();
+    if (warp == 0) {
+      float Mt = -INFINITY;
+#pragma unroll
+      for (int w = 0; w < kWarps; ++w) Mt = fmaxf(Mt, reinterpret_cast<const float*>(S.rec[w])[0]);
+      float Lt = 0.f;
+      float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
+      if (Mt != -INFINITY) {
+#pragma unroll
+        for (int w = 0; w < kWarps; ++w) {
+          const float* rw = reinterpret_cast<const float*>(S.rec[w]);
+          const float wt = ex2(rw[0] - Mt);
+          const float4 ow4 = reinterpret_cast<const float4*>(rw + 4)[lane];
+          Lt = fmaf(wt, rw[1], Lt);
+          o.x = fmaf(wt, ow4.x, o.x);
+          o.y = fmaf(wt, ow4.y, o.y);
+          o.z = fmaf(wt, ow4.z, o.z);
+          o.w = fmaf(wt, ow4.w, o.w);
+        }
+      }
+      const float il = Lt > 0.f ? 1.f / Lt : 0.f;
+      __half2 o01 = __floats2half2_rn(o.x * il, o.y * il);
+      __half2 o23 = __floats2half2_rn(o.z * il, o.w * il);
       uint2 pk;
       pk.x = *reinterpret_cast<uint32_t*>(&o01);
       pk.y = *reinterpret_cast<uint32_t*>(&o23);
       *reinterpret_cast<uint2*>(ob + h * kD + 4 * lane) = pk;
     }
-    return;
+    __syncthreads();
   }
-  constexpr int kStride = 2 + kD;
-  for (int h = 0; h < g; ++h) {
-    float* Pp = a.ws_part + (((int64_t)b * a.hq + kvh * g + h) * a.nsplit + split) * kStride;
-    if (lane == 0) {
-      Pp[0] = S.mh[h];
-      Pp[1] = S.lh[h];
-    }
-#pragma unroll
-    for (int e = 0; e < 4; ++e) Pp[2 + 4 * lane + e] = O[h][4 * lane + e] + otail[h][e];
-  }
-  __threadfence();
-  __syncwarp();
-  int ticket = 0;
-  if (lane == 0) ticket = atomicAdd(a.ws_count + (int64_t)b * a.hkv + kvh, 1);
-  ticket = __shfl_sync(0xffffffffu, ticket, 0);
-  if (ticket != nsb - 1) return;
-  __threadfence();
-  for (int h = 0; h < g; ++h) {
-    const float* Pp = a.ws_part + (((int64_t)b * a.hq + kvh * g + h) * a.nsplit) * kStride;
-    float M = -INFINITY;
-    for (int s2 = lane; s2 < nsb; s2 += 32) M = fmaxf(M, __ldcg(Pp + s2 * kStride));
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
-    float L = 0.f, acc[4] = {0.f, 0.f, 0.f, 0.f};
-    for (int s2 = 0; s2 < nsb; ++s2) {
-      const float ms = __ldcg(Pp + s2 * kStride);
-      if (ms == -INFINITY) continue;
-      const float w = exp2f(ms - M);
-      L = fmaf(w, __ldcg(Pp + s2 * kStride + 1), L);
-#pragma unroll
-      for (int e = 0; e < 4; ++e)
-        acc[e] = fmaf(w, __ldcg(Pp + s2 * kStride + 2 + 4 * lane + e), acc[e]);
-    }
-    const float il = L > 0.f ? 1.f / L : 0.f;
-    __half2 o01 = __floats2half2_rn(acc[0] * il, acc[1] * il);
-    __half2 o23 = __floats2half2_rn(acc[2] * il, acc[3] * il);
-    uint2 pk;
-    pk.x = *reinterpret_cast<uint32_t*>(&o01);
-    pk.y = *reinterpret_cast<uint32_t*>(&o23);
-    *reinterpret_cast<uint2*>(ob + h * kD + 4 * lane) = pk;
-  }
-  if (lane == 0) a.ws_count[(int64_t)b * a.hkv + kvh] = 0;
+  if (tid == 0) a.ws_count[(int64_t)b * a.hkv + kvh] = 0;
 }
 
 template <int NT>
@@ -598,7 +717,7 @@ cudaError_t launch_nt(const DecodeArgs& a, cudaStream_t s) {
     attr_set = true;
   }
   dim3 grid(a.nsplit, a.hkv, a.batch);
-  decode_mma_kernel<NT><<<grid, 32, smem, s>>>(a);
+  decode_mma_kernel<NT><<<grid, kThreads, smem, s>>>(a);
   return cudaGetLastError();
 }
 
@@ -606,8 +725,10 @@ cudaError_t launch_nt(const DecodeArgs& a, cudaStream_t s) {
 
 bool decode_mma_supported(int g) { return g >= 1 && g <= 8; }
 
-// Resident one-warp CTAs per SM, from the shared-memory footprint (228 KB per
-// SM, 1 KB reserved per CTA).  Host-only arithmetic: no CUDA call.
+int decode_mma_warps() { return kWarps; }
+
+// Resident CTAs per SM, from the shared-memory footprint (228 KB per SM, 1 KB
+// reserved per CTA).  Host-only arithmetic: no CUDA call.
 int decode_mma_ctas_per_sm(int g) {
   const int bytes = g <= 4 ? (int)sizeof(MmaSmem<1>) : (int)sizeof(MmaSmem<2>);
   return 233472 / (bytes + 1024);

@@ -192,16 +192,17 @@ __global__ void __launch_bounds__(kThreads) decode_simple_kernel(DecodeArgs a) {
       // value sum (thread = channel d), rotated space
       {
         const int d = tid;
-        const uint32_t* vrow = reinterpret_cast<const uint32_t*>(S.rec + kOffVCodes + 32 * d);
+        const uint32_t* vw = reinterpret_cast<const uint32_t*>(S.rec + kOffVCodes);
         const float cv = reinterpret_cast<const float*>(S.rec + kOffVC)[d];
         float pv[kMaxG];
         for (int h = 0; h < g; ++h) pv[h] = 0.f;
         for (int w = 0; w < 8; ++w) {
-          const uint32_t word = vrow[w];
+          const int j = w >> 1, hh = w & 1;
+          const uint32_t word = vw[v_word(d, j, hh)];
 #pragma unroll
           for (int e = 0; e < 16; ++e) {
             const float code = (float)((word >> (2 * e)) & 3u);
-            const int t = 16 * w + e;
+            const int t = v_token(j, hh, e);
             for (int h = 0; h < g; ++h) pv[h] = fmaf(S.pw[h][t], code, pv[h]);
           }
         }
@@ -247,14 +248,14 @@ __global__ void __launch_bounds__(kThreads) decode_simple_kernel(DecodeArgs a) {
     return;
   }
   // split-K: publish the partial state, the last CTA of (b, kvh) merges
-  const int64_t stride_split = 2 + kD;
+  const int64_t stride_split = kPartStride;
   for (int h = 0; h < g; ++h) {
     float* P = a.ws_part + (((int64_t)b * a.hq + kvh * g + h) * a.nsplit + split) * stride_split;
     if (tid == 0) {
       P[0] = S.m[h];
       P[1] = S.l[h];
     }
-    P[2 + tid] = o[h];
+    P[4 + tid] = o[h];
   }
   __threadfence();
   __syncthreads();
@@ -272,7 +273,7 @@ __global__ void __launch_bounds__(kThreads) decode_simple_kernel(DecodeArgs a) {
       if (ms == -INFINITY) continue;
       const float w = __expf(ms - M);
       L = fmaf(w, __ldcg(P + s2 * stride_split + 1), L);
-      O = fmaf(w, __ldcg(P + s2 * stride_split + 2 + tid), O);
+      O = fmaf(w, __ldcg(P + s2 * stride_split + 4 + tid), O);
     }
     ob[h * kD + tid] = __float2half_rn(L > 0.f ? O / L : 0.f);
   }

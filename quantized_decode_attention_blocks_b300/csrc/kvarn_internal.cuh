@@ -22,6 +22,22 @@ constexpr int kOffVSZ = 13824;
 constexpr int kOffVC = 14848;
 constexpr int kKPart = 9728;      // K part: [0, 9728)
 constexpr int kVPart = kRec - kKPart;  // V part: [9728, 15360)
+// Split-K partial state per (sequence, query head, split): m, l, 2 pad, o[128]
+// (o 16-byte aligned).
+constexpr int kPartStride = 4 + kD;
+
+// V codes: 2 bits each, 1024 little-endian 32-bit words.  With channel
+// c = 16m + 8e + r and token t = 16k + 8f + 2j + s, the code of (c, t) is crumb
+// 2(k & 3) + f + 8s of word 128m + 16r + 4j + 2e + (k >> 2).  One lane of a
+// decode warp (lane = 4r + j) then finds all the codes it feeds to the tensor
+// cores for channels 16m + r and 16m + 8 + r in four consecutive words.
+__host__ __device__ constexpr int v_word(int c, int j, int h) {
+  return 128 * (c >> 4) + 16 * (c & 7) + 4 * j + 2 * ((c >> 3) & 1) + h;
+}
+// token held by crumb i (0..15) of the words (j, h) of any channel
+__host__ __device__ constexpr int v_token(int j, int h, int i) {
+  return 16 * (4 * h + ((i & 7) >> 1)) + 8 * (i & 1) + 2 * j + (i >> 3);
+}
 constexpr int kMaxG = 16;         // query heads per KV head supported
 constexpr int kMaxIters = 64;     // Sinkhorn iterations accepted
 constexpr int kNumSMs = 148;      // B300

@@ -58,6 +58,12 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t phase,
   return true;
 }
 
+// The bounded wait taken by a whole warp: true only if every lane saw the
+// phase complete, so that the warp leaves its loop as one.
+__device__ __forceinline__ bool mbar_wait_warp(uint64_t* bar, uint32_t phase, uint64_t limit_ns) {
+  return __all_sync(0xffffffffu, mbar_wait_bounded(bar, phase, limit_ns));
+}
+
 // 1-D bulk copy global -> shared (TMA engine), completion on `bar`.
 __device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t bytes,
                                          uint64_t* bar) {

@@ -175,24 +175,26 @@ __device__ void quantize_tile(const __half* x, int64_t ld, bool coherent, uint8_
     __syncthreads();
     const int d = t;
     const float cbd = cb[d];
-    uint32_t w[8];
+    uint32_t* vw = reinterpret_cast<uint32_t*>(rec + kOffVCodes);
 #pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      uint32_t acc = 0;
+    for (int j = 0; j < 4; ++j) {
+      uint32_t w[2];
 #pragma unroll
-      for (int e = 0; e < 16; ++e) {
-        const int r = 16 * i + e;
-        float xv = sY[r * kPitch + d] * cbd;
-        float u = (xv - zmin[r]) * sinv[r];
-        int qv = __float2int_rn(u);
-        qv = min(max(qv, 0), 3);
-        acc |= (uint32_t)qv << (2 * e);
+      for (int hh = 0; hh < 2; ++hh) {
+        uint32_t acc = 0;
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+          const int r = v_token(j, hh, i);
+          float xv = sY[r * kPitch + d] * cbd;
+          float u = (xv - zmin[r]) * sinv[r];
+          int qv = __float2int_rn(u);
+          qv = min(max(qv, 0), 3);
+          acc |= (uint32_t)qv << (2 * i);
+        }
+        w[hh] = acc;
       }
-      w[i] = acc;
+      *reinterpret_cast<uint2*>(vw + v_word(d, j, 0)) = make_uint2(w[0], w[1]);
     }
-    uint4* dst = reinterpret_cast<uint4*>(rec + kOffVCodes + 32 * d);
-    dst[0] = make_uint4(w[0], w[1], w[2], w[3]);
-    dst[1] = make_uint4(w[4], w[5], w[6], w[7]);
   }
 }
 
@@ -277,7 +279,9 @@ __global__ void __launch_bounds__(128) dequantize_kernel(const uint8_t* recs, fl
   const float* cv = reinterpret_cast<const float*>(rec + kOffVC);
   for (int d = 0; d < kD; ++d) {
     const int qk = (rec[kOffKCodes + 64 * t + d / 2] >> (4 * (d & 1))) & 15;
-    const int qv = (rec[kOffVCodes + 32 * d + t / 4] >> (2 * (t & 3))) & 3;
+    const int kk = t >> 4, f = (t >> 3) & 1, j = (t >> 1) & 3, sb = t & 1;
+    const uint32_t vw = reinterpret_cast<const uint32_t*>(rec + kOffVCodes)[v_word(d, j, kk >> 2)];
+    const int qv = (vw >> (2 * (2 * (kk & 3) + f + 8 * sb))) & 3;
     ok[t * kD + d] = ck[d] * fmaf(mk.x, (float)qk, mk.y);
     ov[t * kD + d] = cv[d] * fmaf(mv.x, (float)qv, mv.y);
   }

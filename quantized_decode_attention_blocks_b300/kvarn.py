@@ -19,6 +19,7 @@ LIB_PATH = os.path.join(HERE, "libkvarn.so")
 HEAD_DIM = 128
 BLOCK_TOKENS = 128
 PAGE_BYTES = 15360
+NOALLOC_SCRATCH_BYTES = 4 << 20   # KVARN_NOALLOC_SCRATCH_BYTES
 
 OK = 0
 ERR_INVALID_ARG = -1

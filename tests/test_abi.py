@@ -45,6 +45,8 @@ def test_header_constants_match_binding():
                       ("KVARN_STATUS_TIMEOUT", K.STATUS_TIMEOUT)):
         m = re.search(rf"#define {name} \(?(-?\d+)\)?", text)
         assert m and int(m.group(1)) == val, name
+    m = re.search(r"#define KVARN_NOALLOC_SCRATCH_BYTES \((\d+)u << (\d+)\)", text)
+    assert m and int(m.group(1)) << int(m.group(2)) == K.NOALLOC_SCRATCH_BYTES
 
 
 def test_config_parsing():

@@ -264,17 +264,20 @@ def test_pack_golden_bytes(oracle):
     assert list(rec[off["k_codes"]:off["k_codes"] + 8]) == want
     want = [int(h, 16) for h in g["k_row_alternating_15_0"]["bytes_first_2"]]
     assert list(rec[off["k_codes"] + 64:off["k_codes"] + 66]) == want
-    # V: channel 3, tokens 0..7
-    q = np.zeros((128, 128), np.uint8)
-    q[:8, 3] = g["v_channel_tokens_0_1_2_3"]["codes_first_8_tokens"]
-    rec = np.zeros(15360, np.uint8)
+    # V: hand-derived positions of single codes in the permuted layout
     s = np.arange(128, dtype=np.float32)
     z = -np.arange(128, dtype=np.float32)
     c = np.arange(128, dtype=np.float32) + 0.5
-    oracle.pack_part(rec, True, q, s, z, c)
-    want = [int(h, 16) for h in g["v_channel_tokens_0_1_2_3"]["bytes_first_2"]]
-    base = off["v_codes"] + 3 * 32
-    assert list(rec[base:base + 2]) == want
+    for ex in g["v_examples"]:
+        q = np.zeros((128, 128), np.uint8)
+        q[ex["tokens"], ex["channel"]] = ex["codes"]
+        rec = np.zeros(15360, np.uint8)
+        oracle.pack_part(rec, True, q, s, z, c)
+        want = [int(h, 16) for h in ex["bytes"]]
+        base = off["v_codes"] + ex["byte_offset"]
+        assert list(rec[base:base + len(want)]) == want, ex["_derivation"]
+        # and nothing else in the code region is set
+        assert int(rec[off["v_codes"]:off["v_scale_zero"]].astype(np.int64).sum()) == sum(want)
     # metadata offsets: {s', z'} per token, then column scales
     sz = rec[off["v_scale_zero"]:off["v_scale_zero"] + 1024].view(np.float32).reshape(128, 2)
     assert np.array_equal(sz[:, 0], s) and np.array_equal(sz[:, 1], z)

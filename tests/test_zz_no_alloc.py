@@ -24,14 +24,16 @@ def _ptr(t):
 
 
 def test_noalloc_rejects_requests_beyond_its_scratch():
-    # 128 sequences of up to 131072 tokens need more than the built-in scratch;
-    # the call must say so before touching the GPU (the pointers are never used)
-    cfg = kv.config_from_string("k4v2_g128", 32, 8)
-    need = kv.decode_workspace_bytes(cfg, 128, 131072)
-    assert need > (16 << 20)
+    # one sequence of 131072 tokens with 16 query heads per KV head is split
+    # into so many parts that its partial states need more than the built-in
+    # scratch; the call must say so before touching the GPU (the pointers are
+    # never used)
+    cfg = kv.config_from_string("k4v2_g128", 16, 1)
+    need = kv.decode_workspace_bytes(cfg, 1, 131072)
+    assert need > K.NOALLOC_SCRATCH_BYTES
     fake = ctypes.c_void_p(4096)
     rc = kv.lib().kvarn_decode_attention_noalloc(
-        ctypes.byref(cfg), fake, fake, 1 << 20, fake, 1024, fake, 128, 131072, fake, fake,
+        ctypes.byref(cfg), fake, fake, 1 << 20, fake, 1024, fake, 1, 131072, fake, fake,
         ctypes.c_float(128 ** -0.5), fake, None, None)
     assert rc == K.ERR_WORKSPACE
 
