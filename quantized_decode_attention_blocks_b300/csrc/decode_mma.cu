@@ -50,13 +50,12 @@ template <int NT>
 struct __align__(128) MmaSmem {
   uint8_t rec[kWarps][kRec];     // per warp: K part at 0, V part at kKPart
   float qrot[4 * NT][kD];        // H q per (padded) query head of the group
-  float O[4 * NT][kD];           // the CTA's merged accumulator
-  float ptail[4 * NT][kT];       // fp16-tail probabilities
   uint64_t bar[kWarps][2];       // per warp: 0 = K part landed, 1 = V part landed
-  float mh[4 * NT], lh[4 * NT], al[4 * NT];
-  float red[kWarps][4 * NT];
   int ticket;
 };
+// row pitch (floats) of a warp's output state in its page buffer: rows 8 banks
+// apart, so that the four heads (qi) of one store hit different banks
+constexpr int kOPitch = kD + 8;
 
 __device__ __forceinline__ float ex2(float x) {
   float y;
@@ -108,25 +107,15 @@ __device__ __forceinline__ float warp_sum_r(float x) {
   return x + __shfl_xor_sync(0xffffffffu, x, 16);
 }
 
-// In-place scaled Walsh-Hadamard transform of n rows of 128 floats by the
-// whole CTA (n * 64 butterflies per stage).
-__device__ __forceinline__ void cta_fwht(float (*v)[kD], int n) {
-  const int tid = threadIdx.x;
-  for (int s = 1; s < kD; s <<= 1) {
-    for (int i = tid; i < n * (kD / 2); i += kThreads) {
-      const int h = i >> 6, k = i & 63;
-      const int lo = ((k & ~(s - 1)) << 1) | (k & (s - 1));
-      const float x = v[h][lo], y = v[h][lo + s];
-      if (s == kD / 2) {
-        v[h][lo] = (x + y) * kInvSqrt128;
-        v[h][lo + s] = (x - y) * kInvSqrt128;
-      } else {
-        v[h][lo] = x + y;
-        v[h][lo + s] = x - y;
-      }
-    }
-    __syncthreads();
-  }
+// Position of channel ch in a row of qrot: the float4 index is XOR-ed with
+// ch >> 5, so that the four lanes reading float4 k of their 32-channel slices
+// (8 qi + k) hit four different bank groups.
+__device__ __forceinline__ int qrot_pos(int ch) {
+  return ((((ch >> 2) ^ (ch >> 5)) & 7) | ((ch >> 2) & ~7)) * 4 + (ch & 3);
+}
+
+__device__ __forceinline__ uint32_t word_of(const uint4& w, int i) {
+  return i == 0 ? w.x : i == 1 ? w.y : i == 2 ? w.z : w.w;
 }
 
 // mask selecting crumb p (0..4) of both 16-bit halves
@@ -210,6 +199,7 @@ __global__ void __launch_bounds__(kThreads, 3) decode_mma_kernel(DecodeArgs a) {
   }
 
   // ---- q~ = H q: warp w rotates heads w, w + 4 (lane holds channels 32i + lane) ----
+  {
   const __half* qb = a.q + ((int64_t)b * a.hq + (int64_t)kvh * g) * kD;
 #pragma unroll
   for (int hh = 0; hh < NT; ++hh) {
@@ -231,7 +221,8 @@ __global__ void __launch_bounds__(kThreads, 3) decode_mma_kernel(DecodeArgs a) {
       }
     }
 #pragma unroll
-    for (int i = 0; i < 4; ++i) S.qrot[h][32 * i + lane] = x[i] * kInvSqrt128;
+    for (int i = 0; i < 4; ++i) S.qrot[h][qrot_pos(32 * i + lane)] = x[i] * kInvSqrt128;
+  }
   }
   __syncthreads();
 
@@ -266,14 +257,14 @@ __global__ void __launch_bounds__(kThreads, 3) decode_mma_kernel(DecodeArgs a) {
 #pragma unroll
       for (int nt = 0; nt < NT; ++nt) {
         const int h = 4 * nt + (r >> 1);
-        const float4* qv = reinterpret_cast<const float4*>(&S.qrot[h][32 * qi]);
+        const float4* qv = reinterpret_cast<const float4*>(S.qrot[h]);
         const float4* cv = reinterpret_cast<const float4*>(kst + kOffKC + 128 * qi);
         float v[32];
         float amax = 0.f;
         float2 sum2 = make_float2(0.f, 0.f);
 #pragma unroll
         for (int k = 0; k < 8; ++k) {
-          const float4 q4 = qv[k], c4 = cv[k];
+          const float4 q4 = qv[(8 * qi + k) ^ qi], c4 = cv[k];
           const float2 p0 = __fmul2_rn(make_float2(q4.x, q4.y), make_float2(c4.x, c4.y));
           const float2 p1 = __fmul2_rn(make_float2(q4.z, q4.w), make_float2(c4.z, c4.w));
           v[4 * k + 0] = p0.x;
@@ -309,41 +300,48 @@ __global__ void __launch_bounds__(kThreads, 3) decode_mma_kernel(DecodeArgs a) {
         sZ[nt] = __shfl_sync(0xffffffffu, sum, 8 * qi) * sl2;
       }
 
-      // ---- scores: K codes (A, rows = tokens) x qc (B) ----
+      // ---- scores: K codes (A, rows = tokens) x qc (B).  MTG token tiles at
+      // a time, k-tile outer, so that MTG accumulator chains interleave ----
+      constexpr int MTG = NT == 1 ? 8 : 4;
 #pragma unroll
-      for (int mt = 0; mt < 8; ++mt) {
-        const int tA = 16 * mt + r, tB = tA + 8;
-        const uint4 wa = *reinterpret_cast<const uint4*>(kst + kOffKCodes + 64 * tA + 16 * qi);
-        const uint4 wb = *reinterpret_cast<const uint4*>(kst + kOffKCodes + 64 * tB + 16 * qi);
-        const uint32_t WA[4] = {wa.x, wa.y, wa.z, wa.w};
-        const uint32_t WB[4] = {wb.x, wb.y, wb.z, wb.w};
-        float d[NT][4];
+      for (int m0 = 0; m0 < 8; m0 += MTG) {
+        uint4 kw[MTG][2];
 #pragma unroll
-        for (int nt = 0; nt < NT; ++nt) d[nt][0] = d[nt][1] = d[nt][2] = d[nt][3] = 0.f;
+        for (int i = 0; i < MTG; ++i) {
+          const int tA = 16 * (m0 + i) + r;
+          kw[i][0] = *reinterpret_cast<const uint4*>(kst + kOffKCodes + 64 * tA + 16 * qi);
+          kw[i][1] = *reinterpret_cast<const uint4*>(kst + kOffKCodes + 64 * (tA + 8) + 16 * qi);
+        }
+        float d[NT][MTG][4];
 #pragma unroll
-        for (int mw = 0; mw < 4; ++mw) {
-          {
-            const uint32_t A[4] = {WA[mw] & 0x000F000Fu, WB[mw] & 0x000F000Fu,
-                                   WA[mw] & 0x00F000F0u, WB[mw] & 0x00F000F0u};
+        for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
-            for (int nt = 0; nt < NT; ++nt)
-              mma_16816(d[nt], A, bq[nt][2 * mw][0], bq[nt][2 * mw][1]);
-          }
-          {
-            const uint32_t xa = WA[mw] >> 8, xb = WB[mw] >> 8;
-            const uint32_t A[4] = {xa & 0x000F000Fu, xb & 0x000F000Fu, xa & 0x00F000F0u,
-                                   xb & 0x00F000F0u};
+          for (int i = 0; i < MTG; ++i) d[nt][i][0] = d[nt][i][1] = d[nt][i][2] = d[nt][i][3] = 0.f;
 #pragma unroll
-            for (int nt = 0; nt < NT; ++nt)
-              mma_16816(d[nt], A, bq[nt][2 * mw + 1][0], bq[nt][2 * mw + 1][1]);
+        for (int kb = 0; kb < 8; ++kb) {
+#pragma unroll
+          for (int i = 0; i < MTG; ++i) {
+            uint32_t wa = word_of(kw[i][0], kb >> 1), wb = word_of(kw[i][1], kb >> 1);
+            if (kb & 1) {
+              wa >>= 8;
+              wb >>= 8;
+            }
+            const uint32_t A[4] = {wa & 0x000F000Fu, wb & 0x000F000Fu, wa & 0x00F000F0u,
+                                   wb & 0x00F000F0u};
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt) mma_16816(d[nt][i], A, bq[nt][kb][0], bq[nt][kb][1]);
           }
         }
-        const float2 szA = *reinterpret_cast<const float2*>(kst + kOffKSZ + 8 * tA);
-        const float2 szB = *reinterpret_cast<const float2*>(kst + kOffKSZ + 8 * tB);
 #pragma unroll
-        for (int nt = 0; nt < NT; ++nt) {
-          sc[nt][2 * mt] = fmaf(szA.x * sA[nt], d[nt][0] + d[nt][1], szA.y * sZ[nt]);
-          sc[nt][2 * mt + 1] = fmaf(szB.x * sA[nt], d[nt][2] + d[nt][3], szB.y * sZ[nt]);
+        for (int i = 0; i < MTG; ++i) {
+          const int mt = m0 + i, tA = 16 * mt + r, tB = tA + 8;
+          const float2 szA = *reinterpret_cast<const float2*>(kst + kOffKSZ + 8 * tA);
+          const float2 szB = *reinterpret_cast<const float2*>(kst + kOffKSZ + 8 * tB);
+#pragma unroll
+          for (int nt = 0; nt < NT; ++nt) {
+            sc[nt][2 * mt] = fmaf(szA.x * sA[nt], d[nt][i][0] + d[nt][i][1], szA.y * sZ[nt]);
+            sc[nt][2 * mt + 1] = fmaf(szB.x * sA[nt], d[nt][i][2] + d[nt][i][3], szB.y * sZ[nt]);
+          }
         }
       }
     }
@@ -413,47 +411,59 @@ __global__ void __launch_bounds__(kThreads, 3) decode_mma_kernel(DecodeArgs a) {
         zpage[nt] = warp_sum_r(zp);
       }
 
-      // ---- value sum: V codes (A, rows = channels) x P' (B) ----
+      // ---- value sum: V codes (A, rows = channels) x P' (B).  MCG channel
+      // tiles at a time, k-tile outer, so that their chains interleave ----
       const float fin = finv * kTwo24;
       const float* cvv = reinterpret_cast<const float*>(vst + (kOffVC - kKPart));
+      constexpr int MCG = NT == 1 ? 8 : 4;
 #pragma unroll
-      for (int mc = 0; mc < 8; ++mc) {
-        const uint4 w4 = *reinterpret_cast<const uint4*>(vst + (kOffVCodes - kKPart) + 512 * mc +
-                                                        16 * lane);
-        const uint32_t W[4] = {w4.x, w4.y, w4.z, w4.w};     // (e, h) = 00, 01, 10, 11
-        const uint32_t Wsh[4] = {w4.x >> 10, w4.y >> 10, w4.z >> 10, w4.w >> 10};
-        float d[NT][4];
+      for (int c0 = 0; c0 < 8; c0 += MCG) {
+        uint4 vw[MCG];   // words (e, h) = 00, 01, 10, 11 of channels 16mc + r, + 8
 #pragma unroll
-        for (int nt = 0; nt < NT; ++nt) d[nt][0] = d[nt][1] = d[nt][2] = d[nt][3] = 0.f;
+        for (int i = 0; i < MCG; ++i)
+          vw[i] = *reinterpret_cast<const uint4*>(vst + (kOffVCodes - kKPart) + 512 * (c0 + i) +
+                                                  16 * lane);
+        float d[NT][MCG][4];
 #pragma unroll
-        for (int kb = 0; kb < 8; ++kb) {
-          const int hh = kb >> 2;
-          const uint32_t e0 = W[hh], e1 = W[2 + hh], s0 = Wsh[hh], s1 = Wsh[2 + hh];
-          uint32_t A[4];
-          switch (kb & 3) {
-            case 0:
-              A[0] = e0 & cmask(0); A[1] = e1 & cmask(0); A[2] = e0 & cmask(1); A[3] = e1 & cmask(1);
-              break;
-            case 1:
-              A[0] = e0 & cmask(2); A[1] = e1 & cmask(2); A[2] = e0 & cmask(3); A[3] = e1 & cmask(3);
-              break;
-            case 2:
-              A[0] = e0 & cmask(4); A[1] = e1 & cmask(4); A[2] = s0 & cmask(0); A[3] = s1 & cmask(0);
-              break;
-            default:
-              A[0] = s0 & cmask(1); A[1] = s1 & cmask(1); A[2] = s0 & cmask(2); A[3] = s1 & cmask(2);
-              break;
+        for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+          for (int i = 0; i < MCG; ++i) d[nt][i][0] = d[nt][i][1] = d[nt][i][2] = d[nt][i][3] = 0.f;
+#pragma unroll
+        for (int hh = 0; hh < 2; ++hh) {
+#pragma unroll
+          for (int jj = 0; jj < 4; ++jj) {
+            const int kb = 4 * hh + jj;
+#pragma unroll
+            for (int i = 0; i < MCG; ++i) {
+              const uint32_t e0 = word_of(vw[i], hh), e1 = word_of(vw[i], 2 + hh);
+              uint32_t A[4];
+              if (jj == 0) {
+                A[0] = e0 & cmask(0); A[1] = e1 & cmask(0); A[2] = e0 & cmask(1); A[3] = e1 & cmask(1);
+              } else if (jj == 1) {
+                A[0] = e0 & cmask(2); A[1] = e1 & cmask(2); A[2] = e0 & cmask(3); A[3] = e1 & cmask(3);
+              } else if (jj == 2) {
+                A[0] = e0 & cmask(4); A[1] = e1 & cmask(4);
+                A[2] = (e0 >> 10) & cmask(0); A[3] = (e1 >> 10) & cmask(0);
+              } else {
+                A[0] = (e0 >> 10) & cmask(1); A[1] = (e1 >> 10) & cmask(1);
+                A[2] = (e0 >> 10) & cmask(2); A[3] = (e1 >> 10) & cmask(2);
+              }
+#pragma unroll
+              for (int nt = 0; nt < NT; ++nt) mma_16816(d[nt][i], A, bp[nt][kb][0], bp[nt][kb][1]);
+            }
           }
-#pragma unroll
-          for (int nt = 0; nt < NT; ++nt) mma_16816(d[nt], A, bp[nt][kb][0], bp[nt][kb][1]);
         }
-        const float cvA = cvv[16 * mc + r], cvB = cvv[16 * mc + 8 + r];
 #pragma unroll
-        for (int nt = 0; nt < NT; ++nt) {
-          oacc[nt][2 * mc] =
-              fmaf(oacc[nt][2 * mc], alpha[nt], cvA * fmaf(d[nt][0] + d[nt][1], fin, zpage[nt]));
-          oacc[nt][2 * mc + 1] = fmaf(oacc[nt][2 * mc + 1], alpha[nt],
-                                      cvB * fmaf(d[nt][2] + d[nt][3], fin, zpage[nt]));
+        for (int i = 0; i < MCG; ++i) {
+          const int mc = c0 + i;
+          const float cvA = cvv[16 * mc + r], cvB = cvv[16 * mc + 8 + r];
+#pragma unroll
+          for (int nt = 0; nt < NT; ++nt) {
+            oacc[nt][2 * mc] = fmaf(oacc[nt][2 * mc], alpha[nt],
+                                    cvA * fmaf(d[nt][i][0] + d[nt][i][1], fin, zpage[nt]));
+            oacc[nt][2 * mc + 1] = fmaf(oacc[nt][2 * mc + 1], alpha[nt],
+                                        cvB * fmaf(d[nt][i][2] + d[nt][i][3], fin, zpage[nt]));
+          }
         }
       }
     }
@@ -480,26 +490,131 @@ __global__ void __launch_bounds__(kThreads, 3) decode_mma_kernel(DecodeArgs a) {
   }
   __syncwarp();
 
-  // ---- this warp's state into its own buffer: [G]{m, l} then o[G][128] (rotated) ----
+  // ---- back to plain space, in registers: lane (r, qi) holds for head
+  // 4nt + qi the channels 16 mc + 8 e + r at oacc[nt][2 mc + e], so channel
+  // bits 3..6 are local and bits 0..2 are lane bits 2..4 ----
+#pragma unroll
+  for (int nt = 0; nt < NT; ++nt) {
+    float* o = oacc[nt];
+#pragma unroll
+    for (int hb = 1; hb < 16; hb <<= 1)
+#pragma unroll
+      for (int j = 0; j < 16; ++j)
+        if ((j & hb) == 0) {
+          const float x = o[j], y = o[j + hb];
+          o[j] = x + y;
+          o[j + hb] = x - y;
+        }
+#pragma unroll
+    for (int lb = 4; lb < 32; lb <<= 1) {
+      const bool up = lane & lb;
+#pragma unroll
+      for (int j = 0; j < 16; ++j) {
+        const float other = __shfl_xor_sync(0xffffffffu, o[j], lb);
+        o[j] = up ? other - o[j] : o[j] + other;
+      }
+    }
+#pragma unroll
+    for (int j = 0; j < 16; ++j) o[j] *= kInvSqrt128;
+  }
+
+  // ---- this warp's state into its own buffer: [G]{m, l}, then o[G][kOPitch] ----
   float* st = reinterpret_cast<float*>(kst);
-  float (*ow)[kD] = reinterpret_cast<float (*)[kD]>(kst + 2 * G * sizeof(float));
+  float* ow = st + 2 * G;
 #pragma unroll
   for (int nt = 0; nt < NT; ++nt) {
     const float lsum = warp_sum_r(l[nt]);
 #pragma unroll
     for (int mc = 0; mc < 8; ++mc) {
-      ow[4 * nt + qi][16 * mc + r] = oacc[nt][2 * mc];
-      ow[4 * nt + qi][16 * mc + 8 + r] = oacc[nt][2 * mc + 1];
+      ow[(4 * nt + qi) * kOPitch + 16 * mc + r] = oacc[nt][2 * mc];
+      ow[(4 * nt + qi) * kOPitch + 16 * mc + 8 + r] = oacc[nt][2 * mc + 1];
     }
     if (r == 0) {
       st[2 * (4 * nt + qi)] = m[nt];
       st[2 * (4 * nt + qi) + 1] = lsum;
     }
   }
+  __syncwarp();
+
+  // ---- fp16 tail (plain space): warp w takes tail tokens w, w + 4, ... and
+  // folds them into its own state; lane holds channels 4 lane .. 4 lane + 3 ----
+  const __half* qb2 = a.q + ((int64_t)b * a.hq + (int64_t)kvh * g) * kD;
+  if (has_tail && !timed_out) {
+    const __half* tkb = a.tail_k + ((int64_t)b * a.hkv + kvh) * kT * kD;
+    const __half* tvb = a.tail_v + ((int64_t)b * a.hkv + kvh) * kT * kD;
+    float qr[G][4], mt[G], lt[G], ot[G][4];
+#pragma unroll
+    for (int h = 0; h < G; ++h) {
+      float2 q01 = make_float2(0.f, 0.f), q23 = q01;
+      if (h < g) {
+        const uint2 qq = __ldg(reinterpret_cast<const uint2*>(qb2 + h * kD + 4 * lane));
+        q01 = __half22float2(*reinterpret_cast<const __half2*>(&qq.x));
+        q23 = __half22float2(*reinterpret_cast<const __half2*>(&qq.y));
+      }
+      qr[h][0] = q01.x * sl2;
+      qr[h][1] = q01.y * sl2;
+      qr[h][2] = q23.x * sl2;
+      qr[h][3] = q23.y * sl2;
+      mt[h] = st[2 * h];
+      lt[h] = st[2 * h + 1];
+      const float4 o4 = *reinterpret_cast<const float4*>(ow + h * kOPitch + 4 * lane);
+      ot[h][0] = o4.x;
+      ot[h][1] = o4.y;
+      ot[h][2] = o4.z;
+      ot[h][3] = o4.w;
+    }
+    constexpr int kC = 8;   // tail tokens per batch of loads
+    for (int t0 = warp; t0 < rem; t0 += kWarps * kC) {
+      uint2 kk[kC], vv[kC];
+#pragma unroll
+      for (int i = 0; i < kC; ++i) {
+        const int t = t0 + kWarps * i;
+        if (t < rem) {
+          kk[i] = __ldg(reinterpret_cast<const uint2*>(tkb + (int64_t)t * kD + 4 * lane));
+          vv[i] = __ldg(reinterpret_cast<const uint2*>(tvb + (int64_t)t * kD + 4 * lane));
+        }
+      }
+#pragma unroll
+      for (int i = 0; i < kC; ++i) {
+        if (t0 + kWarps * i >= rem) break;
+        const float2 k01 = __half22float2(*reinterpret_cast<const __half2*>(&kk[i].x));
+        const float2 k23 = __half22float2(*reinterpret_cast<const __half2*>(&kk[i].y));
+        const float2 v01 = __half22float2(*reinterpret_cast<const __half2*>(&vv[i].x));
+        const float2 v23 = __half22float2(*reinterpret_cast<const __half2*>(&vv[i].y));
+#pragma unroll
+        for (int h = 0; h < G; ++h) {
+          float sc1 = fmaf(qr[h][0], k01.x, fmaf(qr[h][1], k01.y,
+                      fmaf(qr[h][2], k23.x, qr[h][3] * k23.y)));
+#pragma unroll
+          for (int o = 16; o > 0; o >>= 1) sc1 += __shfl_xor_sync(0xffffffffu, sc1, o);
+          const float mn = fmaxf(mt[h], sc1);
+          const float al = ex2(mt[h] - mn), pt = ex2(sc1 - mn);
+          mt[h] = mn;
+          lt[h] = fmaf(lt[h], al, pt);
+          ot[h][0] = fmaf(ot[h][0], al, pt * v01.x);
+          ot[h][1] = fmaf(ot[h][1], al, pt * v01.y);
+          ot[h][2] = fmaf(ot[h][2], al, pt * v23.x);
+          ot[h][3] = fmaf(ot[h][3], al, pt * v23.y);
+        }
+      }
+    }
+    __syncwarp();
+#pragma unroll
+    for (int h = 0; h < G; ++h) {
+      if (lane == 0) {
+        st[2 * h] = mt[h];
+        st[2 * h + 1] = lt[h];
+      }
+      *reinterpret_cast<float4*>(ow + h * kOPitch + 4 * lane) =
+          make_float4(ot[h][0], ot[h][1], ot[h][2], ot[h][3]);
+    }
+  }
   __syncthreads();
 
-  // ---- merge the warps' states, then rotate back to plain space ----
-  for (int i = tid; i < G * kD; i += kThreads) {
+  // ---- merge the warps' states; the result goes straight to the output
+  // (one split) or to this split's partial state ----
+  __half* ob = a.out + ((int64_t)b * a.hq + (int64_t)kvh * g) * kD;
+  for (int i = tid; i < g * kD; i += kThreads) {
     const int h = i >> 7, ch = i & 127;
     float M = -INFINITY;
 #pragma unroll
@@ -511,118 +626,23 @@ __global__ void __launch_bounds__(kThreads, 3) decode_mma_kernel(DecodeArgs a) {
       for (int w = 0; w < kWarps; ++w) {
         const float* sw = reinterpret_cast<const float*>(S.rec[w]);
         const float wt = ex2(sw[2 * h] - M);
-        o = fmaf(wt, sw[2 * G + h * kD + ch], o);
+        o = fmaf(wt, sw[2 * G + h * kOPitch + ch], o);
         L = fmaf(wt, sw[2 * h + 1], L);
       }
     }
-    S.O[h][ch] = o;
-    if (ch == 0) {
-      S.mh[h] = M;
-      S.lh[h] = L;
-    }
-  }
-  __syncthreads();
-  cta_fwht(S.O, G);
-
-  // ---- fp16 tail (plain space): thread t scores tail token t ----
-  if (has_tail) {
-    const __half* tkb = a.tail_k + ((int64_t)b * a.hkv + kvh) * kT * kD;
-    const __half* tvb = a.tail_v + ((int64_t)b * a.hkv + kvh) * kT * kD;
-    float ts[G];
-#pragma unroll
-    for (int h = 0; h < G; ++h) ts[h] = -INFINITY;
-    if (tid < rem) {
-#pragma unroll
-      for (int h = 0; h < G; ++h) ts[h] = 0.f;
-      const uint4* kr = reinterpret_cast<const uint4*>(tkb + (int64_t)tid * kD);
-      for (int c = 0; c < kD / 8; ++c) {
-        const uint4 uq = __ldg(kr + c);
-        const __half2* h2 = reinterpret_cast<const __half2*>(&uq);
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const float2 kf = __half22float2(h2[e]);
-#pragma unroll
-          for (int h = 0; h < G; ++h) {
-            if (h < g) {
-              const __half2 q2 = *reinterpret_cast<const __half2*>(qb + h * kD + 8 * c + 2 * e);
-              const float2 qf = __half22float2(q2);
-              ts[h] = fmaf(qf.x, kf.x, fmaf(qf.y, kf.y, ts[h]));
-            }
-          }
-        }
+    if (nsb == 1) {
+      ob[i] = __float2half_rn(L > 0.f ? o / L : 0.f);
+    } else {
+      float* Pp =
+          a.ws_part + (((int64_t)b * a.hq + kvh * g + h) * a.nsplit + split) * kPartStride;
+      if (ch == 0) {
+        Pp[0] = M;
+        Pp[1] = L;
       }
-#pragma unroll
-      for (int h = 0; h < G; ++h) ts[h] *= sl2;
+      Pp[4 + ch] = o;
     }
-    // per-head tail max over the CTA
-#pragma unroll
-    for (int h = 0; h < G; ++h) {
-      float x = ts[h];
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) x = fmaxf(x, __shfl_xor_sync(0xffffffffu, x, o));
-      if (lane == 0) S.red[warp][h] = x;
-    }
-    __syncthreads();
-    if (tid < G) {
-      float tm = S.red[0][tid];
-#pragma unroll
-      for (int w = 1; w < kWarps; ++w) tm = fmaxf(tm, S.red[w][tid]);
-      const float mold = S.mh[tid];
-      const float mnew = fmaxf(mold, tm);
-      S.al[tid] = ex2(mold - mnew);
-      S.mh[tid] = mnew;
-    }
-    __syncthreads();
-#pragma unroll
-    for (int h = 0; h < G; ++h) {
-      const float p = tid < rem ? ex2(ts[h] - S.mh[h]) : 0.f;
-      S.ptail[h][tid] = p;
-      float x = p;
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
-      ts[h] = x;
-    }
-    __syncthreads();   // red is reused below, ptail complete
-#pragma unroll
-    for (int h = 0; h < G; ++h)
-      if (lane == 0) S.red[warp][h] = ts[h];
-    __syncthreads();
-    if (tid < G) {
-      float ls = 0.f;
-#pragma unroll
-      for (int w = 0; w < kWarps; ++w) ls += S.red[w][tid];
-      S.lh[tid] = fmaf(S.lh[tid], S.al[tid], ls);
-    }
-    // value sum of the tail: thread (h, channel)
-    for (int i = tid; i < G * kD; i += kThreads) {
-      const int h = i >> 7, ch = i & 127;
-      float o = S.O[h][ch] * S.al[h];
-      for (int t = 0; t < rem; ++t)
-        o = fmaf(S.ptail[h][t], __half2float(tvb[(int64_t)t * kD + ch]), o);
-      S.O[h][ch] = o;
-    }
-    __syncthreads();
   }
-
-  // ---- output: direct, or partial state + last-arriving merge ----
-  __half* ob = a.out + ((int64_t)b * a.hq + (int64_t)kvh * g) * kD;
-  if (nsb == 1) {
-    for (int i = tid; i < g * kD; i += kThreads) {
-      const int h = i >> 7, ch = i & 127;
-      const float lh = S.lh[h];
-      ob[i] = __float2half_rn(lh > 0.f ? S.O[h][ch] / lh : 0.f);
-    }
-    return;
-  }
-  for (int i = tid; i < g * kD; i += kThreads) {
-    const int h = i >> 7, ch = i & 127;
-    float* Pp = a.ws_part + (((int64_t)b * a.hq + kvh * g + h) * a.nsplit + split) * kPartStride;
-    if (ch == 0) {
-      Pp[0] = S.mh[h];
-      Pp[1] = S.lh[h];
-    }
-    Pp[4 + ch] = S.O[h][ch];
-  }
+  if (nsb == 1) return;
   __threadfence();
   __syncthreads();
   if (tid == 0) S.ticket = atomicAdd(a.ws_count + (int64_t)b * a.hkv + kvh, 1);
@@ -630,36 +650,33 @@ __global__ void __launch_bounds__(kThreads, 3) decode_mma_kernel(DecodeArgs a) {
   if (S.ticket != nsb - 1) return;
   __threadfence();
 
-  // merge: warp w takes splits w, w + 4, ...; lane holds channels 4 lane .. + 3
-  for (int h = 0; h < g; ++h) {
+  // ---- last split to arrive: merge all splits, warp w takes heads w, w + 4;
+  // lane holds channels 4 lane .. + 3; loads batched kU splits deep ----
+  for (int h = warp; h < g; h += kWarps) {
     const float* P0 = a.ws_part + (((int64_t)b * a.hq + kvh * g + h) * a.nsplit) * kPartStride;
     float M = -INFINITY, L = 0.f;
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-    constexpr int kU = 4;
-    for (int s0 = warp; s0 < nsb; s0 += kWarps * kU) {
-      float ms[kU], ls[kU];
+    constexpr int kU = 8;
+    for (int s0 = 0; s0 < nsb; s0 += kU) {
+      float2 ml[kU];
       float4 os[kU];
 #pragma unroll
       for (int k = 0; k < kU; ++k) {
-        const int s2 = s0 + kWarps * k;
-        if (s2 < nsb) {
-          const float* Ps = P0 + (int64_t)s2 * kPartStride;
-          const float2 ml = __ldcg(reinterpret_cast<const float2*>(Ps));
-          ms[k] = ml.x;
-          ls[k] = ml.y;
+        if (s0 + k < nsb) {
+          const float* Ps = P0 + (int64_t)(s0 + k) * kPartStride;
+          ml[k] = __ldcg(reinterpret_cast<const float2*>(Ps));
           os[k] = __ldcg(reinterpret_cast<const float4*>(Ps + 4) + lane);
         } else {
-          ms[k] = -INFINITY;
-          ls[k] = 0.f;
+          ml[k] = make_float2(-INFINITY, 0.f);
           os[k] = make_float4(0.f, 0.f, 0.f, 0.f);
         }
       }
 #pragma unroll
       for (int k = 0; k < kU; ++k) {
-        if (ms[k] == -INFINITY) continue;
-        const float Mn = fmaxf(M, ms[k]);
-        const float al = ex2(M - Mn), wt = ex2(ms[k] - Mn);
-        L = fmaf(L, al, wt * ls[k]);
+        if (ml[k].x == -INFINITY) continue;
+        const float Mn = fmaxf(M, ml[k].x);
+        const float al = ex2(M - Mn), wt = ex2(ml[k].x - Mn);
+        L = fmaf(L, al, wt * ml[k].y);
         acc.x = fmaf(acc.x, al, wt * os[k].x);
         acc.y = fmaf(acc.y, al, wt * os[k].y);
         acc.z = fmaf(acc.z, al, wt * os[k].z);
@@ -667,41 +684,13 @@ __global__ void __launch_bounds__(kThreads, 3) decode_mma_kernel(DecodeArgs a) {
         M = Mn;
       }
     }
-    float* red = reinterpret_cast<float*>(S.rec[warp]);
-    if (lane == 0) {
-      red[0] = M;
-      red[1] = L;
-    }
-    reinterpret_cast<float4*>(red + 4)[lane] = acc;
-    __syncthreads();
-    if (warp == 0) {
-      float Mt = -INFINITY;
-#pragma unroll
-      for (int w = 0; w < kWarps; ++w) Mt = fmaxf(Mt, reinterpret_cast<const float*>(S.rec[w])[0]);
-      float Lt = 0.f;
-      float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
-      if (Mt != -INFINITY) {
-#pragma unroll
-        for (int w = 0; w < kWarps; ++w) {
-          const float* rw = reinterpret_cast<const float*>(S.rec[w]);
-          const float wt = ex2(rw[0] - Mt);
-          const float4 ow4 = reinterpret_cast<const float4*>(rw + 4)[lane];
-          Lt = fmaf(wt, rw[1], Lt);
-          o.x = fmaf(wt, ow4.x, o.x);
-          o.y = fmaf(wt, ow4.y, o.y);
-          o.z = fmaf(wt, ow4.z, o.z);
-          o.w = fmaf(wt, ow4.w, o.w);
-        }
-      }
-      const float il = Lt > 0.f ? 1.f / Lt : 0.f;
-      __half2 o01 = __floats2half2_rn(o.x * il, o.y * il);
-      __half2 o23 = __floats2half2_rn(o.z * il, o.w * il);
-      uint2 pk;
-      pk.x = *reinterpret_cast<uint32_t*>(&o01);
-      pk.y = *reinterpret_cast<uint32_t*>(&o23);
-      *reinterpret_cast<uint2*>(ob + h * kD + 4 * lane) = pk;
-    }
-    __syncthreads();
+    const float il = L > 0.f ? 1.f / L : 0.f;
+    __half2 o01 = __floats2half2_rn(acc.x * il, acc.y * il);
+    __half2 o23 = __floats2half2_rn(acc.z * il, acc.w * il);
+    uint2 pk;
+    pk.x = *reinterpret_cast<uint32_t*>(&o01);
+    pk.y = *reinterpret_cast<uint32_t*>(&o23);
+    *reinterpret_cast<uint2*>(ob + h * kD + 4 * lane) = pk;
   }
   if (tid == 0) a.ws_count[(int64_t)b * a.hkv + kvh] = 0;
 }
