@@ -63,6 +63,8 @@ def measured_peaks():
 
 def source_hash(name):
     p = os.path.join(ROOT, "quantized_decode_attention_blocks_b300", "csrc", name)
+    if not os.path.exists(p):
+        return None
     with open(p, "rb") as f:
         return hashlib.sha256(f.read()).hexdigest()[:16]
 
@@ -432,8 +434,8 @@ def main():
     dom = "quantize" if ms["quantize"] >= ms["decode"] else "decode"
     dom_gbs = q_gbs if dom == "quantize" else d_gbs
     dom_bytes = job.bytes_quantize if dom == "quantize" else job.bytes_decode
-    traffic_q = ncu_traffic("quantize_blocks_kernel", "quantize.cu")
-    traffic_d = ncu_traffic("decode_kernel", "decode_mma.cu")
+    traffic_q = ncu_traffic("quantize_tc_kernel", "quantize_tc.cu")
+    traffic_d = ncu_traffic("decode_mma_kernel", "decode_mma.cu")
     line = {
         "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step,
