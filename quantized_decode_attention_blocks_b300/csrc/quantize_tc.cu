@@ -66,13 +66,13 @@ struct TileInfo {
 
 struct __align__(1024) QSmem {
   uint8_t hs[kTileBytes];                // +-1 Sylvester matrix, fp16, swizzled
-  uint8_t x[kWG][2][kTileBytes];         // input tiles, two stages per pipeline
+  uint8_t x[kWG][2][kTileBytes];         // input tiles (then the packed output), 2 stages
   __align__(16) float ra[kWG][kT];       // 1 / r_t, in units of Y
   __align__(16) float cb[kWG][kD];       // 1 / c_d
-  __align__(16) float cc[kWG][kD];       // c_d
   __align__(16) float vmin[kWG][kT];     // V: per-token min of x
   __align__(16) float vinv[kWG][kT];     // V: per-token 3 / (max - min)
-  TileInfo info[kWG][2];                 // current / next tile of each pipeline
+  __align__(16) float cc[kWG][kD];       // c_d
+  TileInfo info[kWG][2];                 // tile held in each stage
   uint64_t xbar[kWG][2];                 // tile landed
   uint64_t mbar[kWG];                    // MMAs done
   uint32_t tmem_base;
@@ -136,16 +136,18 @@ __device__ __forceinline__ float min3f(float a, float b, float c) {
   return d;
 }
 
-// 32 columns of this thread's TMEM lane, scaled in place by f (shared
-// memory, the same weights for every thread: broadcast loads) when HAS_F.
+// 64 columns (64 c .. 64 c + 63) of this thread's TMEM lane, scaled in place
+// by f (shared memory, the same weights for every thread: broadcast loads)
+// when HAS_F.
 template <bool HAS_F>
-__device__ __forceinline__ void tmem_chunk(uint32_t taddr, const float* f, float (&v)[32]) {
-  tmem_ld32(taddr, v);
+__device__ __forceinline__ void row_chunk(uint32_t taddr, int c, const float* f,
+                                          float (&v)[64]) {
+  tmem_ld64(taddr + 64 * c, v);
   tmem_wait_ld();
   if (HAS_F) {
 #pragma unroll
-    for (int i = 0; i < 32; i += 4) {
-      const float4 f4 = *reinterpret_cast<const float4*>(f + i);
+    for (int i = 0; i < 64; i += 4) {
+      const float4 f4 = *reinterpret_cast<const float4*>(f + 64 * c + i);
       const float2 a0 = __fmul2_rn(make_float2(v[i], v[i + 1]), make_float2(f4.x, f4.y));
       const float2 a1 = __fmul2_rn(make_float2(v[i + 2], v[i + 3]), make_float2(f4.z, f4.w));
       v[i] = a0.x;
@@ -156,23 +158,28 @@ __device__ __forceinline__ void tmem_chunk(uint32_t taddr, const float* f, float
   }
 }
 
-// Centred population moments of the 128 values w_c = Y[lane][c] f_c of this
-// thread's TMEM lane, two passes, reading the lane in chunks of 32 columns.
-template <bool HAS_F>
+// Centred population moments of w_c = Y[lane][c] f_c over the 128 columns of
+// this thread's TMEM lane, two passes, 64 columns at a time.  The weights are
+// fused into the arithmetic (s += v f; e = v f - mean; q += e e: three FP32
+// operations per value, the FMA pipe being the bound of this kernel).
 __device__ __forceinline__ void moments_tm(uint32_t taddr, const float* f, float& mean,
                                            float& var) {
   float2 s[4];
 #pragma unroll
   for (int k = 0; k < 4; ++k) s[k] = make_float2(0.f, 0.f);
 #pragma unroll
-  for (int c = 0; c < 4; ++c) {
-    float v[32];
-    tmem_chunk<HAS_F>(taddr + 32 * c, f + 32 * c, v);
+  for (int c = 0; c < 2; ++c) {
+    float v[64];
+    row_chunk<false>(taddr, c, nullptr, v);
 #pragma unroll
-    for (int i = 0; i < 32; i += 8)
-#pragma unroll
-      for (int k = 0; k < 4; ++k)
-        s[k] = __fadd2_rn(make_float2(v[i + 2 * k], v[i + 2 * k + 1]), s[k]);
+    for (int i = 0; i < 64; i += 8) {
+      const float4 f0 = *reinterpret_cast<const float4*>(f + 64 * c + i);
+      const float4 f1 = *reinterpret_cast<const float4*>(f + 64 * c + i + 4);
+      s[0] = __ffma2_rn(make_float2(v[i], v[i + 1]), make_float2(f0.x, f0.y), s[0]);
+      s[1] = __ffma2_rn(make_float2(v[i + 2], v[i + 3]), make_float2(f0.z, f0.w), s[1]);
+      s[2] = __ffma2_rn(make_float2(v[i + 4], v[i + 5]), make_float2(f1.x, f1.y), s[2]);
+      s[3] = __ffma2_rn(make_float2(v[i + 6], v[i + 7]), make_float2(f1.z, f1.w), s[3]);
+    }
   }
   mean = (((s[0].x + s[0].y) + (s[1].x + s[1].y)) + ((s[2].x + s[2].y) + (s[3].x + s[3].y))) *
          (1.f / 128.f);
@@ -180,31 +187,36 @@ __device__ __forceinline__ void moments_tm(uint32_t taddr, const float* f, float
 #pragma unroll
   for (int k = 0; k < 4; ++k) s[k] = make_float2(0.f, 0.f);
 #pragma unroll
-  for (int c = 0; c < 4; ++c) {
-    float v[32];
-    tmem_chunk<HAS_F>(taddr + 32 * c, f + 32 * c, v);
+  for (int c = 0; c < 2; ++c) {
+    float v[64];
+    row_chunk<false>(taddr, c, nullptr, v);
 #pragma unroll
-    for (int i = 0; i < 32; i += 8)
+    for (int i = 0; i < 64; i += 8) {
+      const float4 f0 = *reinterpret_cast<const float4*>(f + 64 * c + i);
+      const float4 f1 = *reinterpret_cast<const float4*>(f + 64 * c + i + 4);
+      float2 e[4];
+      e[0] = __ffma2_rn(make_float2(v[i], v[i + 1]), make_float2(f0.x, f0.y), nm);
+      e[1] = __ffma2_rn(make_float2(v[i + 2], v[i + 3]), make_float2(f0.z, f0.w), nm);
+      e[2] = __ffma2_rn(make_float2(v[i + 4], v[i + 5]), make_float2(f1.x, f1.y), nm);
+      e[3] = __ffma2_rn(make_float2(v[i + 6], v[i + 7]), make_float2(f1.z, f1.w), nm);
 #pragma unroll
-      for (int k = 0; k < 4; ++k) {
-        const float2 e = __fadd2_rn(make_float2(v[i + 2 * k], v[i + 2 * k + 1]), nm);
-        s[k] = __ffma2_rn(e, e, s[k]);
-      }
+      for (int k = 0; k < 4; ++k) s[k] = __ffma2_rn(e[k], e[k], s[k]);
+    }
   }
   var = (((s[0].x + s[0].y) + (s[1].x + s[1].y)) + ((s[2].x + s[2].y) + (s[3].x + s[3].y))) *
         (1.f / 128.f);
 }
 
-// min and max of w_c = Y[lane][c] f_c over the 128 columns
+// min and max of w_c = Y[lane][c] f_c
 __device__ __forceinline__ void minmax_tm(uint32_t taddr, const float* f, float& mn, float& mx) {
   mn = INFINITY;
   mx = -INFINITY;
 #pragma unroll
-  for (int c = 0; c < 4; ++c) {
-    float v[32];
-    tmem_chunk<true>(taddr + 32 * c, f + 32 * c, v);
+  for (int c = 0; c < 2; ++c) {
+    float v[64];
+    row_chunk<true>(taddr, c, f, v);
 #pragma unroll
-    for (int i = 0; i < 32; i += 4) {
+    for (int i = 0; i < 64; i += 4) {
       mn = min3f(mn, v[i], v[i + 1]);
       mx = max3f(mx, v[i], v[i + 1]);
       mn = min3f(mn, v[i + 2], v[i + 3]);
@@ -229,9 +241,10 @@ __global__ void __launch_bounds__(kQThreads, 1)
   extern __shared__ uint8_t smem_raw[];
   QSmem& S = *reinterpret_cast<QSmem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                        ~static_cast<uintptr_t>(1023));
-  const int tid = threadIdx.x, wg = tid / kWGThreads, t = tid % kWGThreads;
+  const int tid = threadIdx.x, wg = tid / kWGThreads, wt = tid % kWGThreads;
   const int warp = tid >> 5;
-  const bool leader = t == 0;
+  const bool leader = wt == 0;
+  const int row = wt;   // this thread's TMEM lane: token in Y, channel in Y^T
 
   // ---- once per CTA: Hs in the 128-byte swizzled K-major layout (two boxes
   // of 64 columns; 16-byte chunk c of row n sits at chunk c ^ (n & 7)) ----
@@ -275,11 +288,12 @@ __global__ void __launch_bounds__(kQThreads, 1)
   const uint32_t bar_id = 1 + wg;
   const int rh = a.roles & 3, rt = (a.roles >> 2) & 3;   // tensor-map dims of head, token
 
-  // leader only: the next valid tile from `id` on, its TMA load into `dst`,
-  // and its hand-off record for the other threads
-  auto prepare = [&](int id, uint8_t* dst, uint64_t* bar, TileInfo& info) {
+  // leader only: the next valid tile from `id` on, its TMA load into stage
+  // `st`, and its hand-off record for the other threads
+  auto prepare = [&](int id, int st) {
     Tile tl;
     while (id < a.ntiles && !tile_of(a, id, tl)) id += nw;
+    TileInfo& info = S.info[wg][st];
     info.id = id;
     info.part = 0;
     info.rec = -1;
@@ -296,12 +310,14 @@ __global__ void __launch_bounds__(kQThreads, 1)
     const int c1 = rh == 1 ? tl.h : rt == 1 ? tl.t0 : tl.b;
     const int c2 = rh == 2 ? tl.h : rt == 2 ? tl.t0 : tl.b;
     const int c3 = rh == 3 ? tl.h : rt == 3 ? tl.t0 : tl.b;
+    bulk_wait_read();   // an earlier tile's packed output may still be leaving this stage
+    uint64_t* bar = &S.xbar[wg][st];
     mbar_arrive_expect_tx(bar, kTileBytes);
-    tma_load_4d(dst, tm, 0, c1, c2, c3, bar);
-    tma_load_4d(dst + kBoxBytes, tm, 64, c1, c2, c3, bar);
+    tma_load_4d(S.x[wg][st], tm, 0, c1, c2, c3, bar);
+    tma_load_4d(S.x[wg][st] + kBoxBytes, tm, 64, c1, c2, c3, bar);
   };
 
-  if (leader) prepare(gw, S.x[wg][0], &S.xbar[wg][0], S.info[wg][0]);
+  if (leader) prepare(gw, 0);
   named_sync(bar_id, kWGThreads);
   int stage = 0;
   uint32_t xph0 = 0, xph1 = 0, mph = 0;
@@ -309,12 +325,16 @@ __global__ void __launch_bounds__(kQThreads, 1)
   while (true) {
     const TileInfo cur = S.info[wg][stage];
     if (cur.id >= a.ntiles) break;
-    if (leader) {
-      uint64_t* xb = &S.xbar[wg][stage];
+    uint8_t* const xs = S.x[wg][stage];
+    {
       const uint32_t ph = stage ? xph1 : xph0;
-      if (!mbar_wait_bounded(xb, ph, kQWaitNs)) report(a.status, KVARN_STATUS_TIMEOUT);
+      if (!mbar_wait_bounded(&S.xbar[wg][stage], ph, kQWaitNs) && leader)
+        report(a.status, KVARN_STATUS_TIMEOUT);
+    }
+    if (stage) xph1 ^= 1; else xph0 ^= 1;
+    if (leader) {
       tc_fence_after();
-      const uint32_t xa = smem_u32(S.x[wg][stage]), ha = smem_u32(S.hs);
+      const uint32_t xa = smem_u32(xs), ha = smem_u32(S.hs);
 #pragma unroll
       for (int kk = 0; kk < 8; ++kk) {   // Y = X Hs: A = X (tokens x channels), B = Hs
         const uint32_t off = (kk >> 2) * kBoxBytes + (kk & 3) * 32;
@@ -327,107 +347,144 @@ __global__ void __launch_bounds__(kQThreads, 1)
       }
       umma_commit(&S.mbar[wg]);
       // the next tile of this pipeline, loading while this one is processed
-      prepare(cur.id + nw, S.x[wg][stage ^ 1], &S.xbar[wg][stage ^ 1], S.info[wg][stage ^ 1]);
+      prepare(cur.id + nw, stage ^ 1);
     }
-    if (stage) xph1 ^= 1; else xph0 ^= 1;
-    uint8_t* const rec = cur.rec >= 0 ? a.pool + cur.rec : nullptr;
     const int part = cur.part;
-    ra[t] = kInvSqrt128;   // r = 1 in units of y, i.e. 1/sqrt(128) in units of Y
-    cb[t] = 1.f;
-    cc[t] = 1.f;
-    if (!mbar_wait_bounded(&S.mbar[wg], mph, kQWaitNs)) {
-      if (leader) report(a.status, KVARN_STATUS_TIMEOUT);
-    }
-    mph ^= 1;
-    tc_fence_after();
-    named_sync(bar_id, kWGThreads);
 
-    // ---- Sinkhorn-like normalization: row step (thread = token), then
-    // column step (thread = channel), `iters` times ----
-    for (int it = 0; it < a.iters; ++it) {
-      {
-        float mean, var;
-        if (it == 0)
-          moments_tm<false>(tY, cb, mean, var);
-        else
-          moments_tm<true>(tY, cb, mean, var);
-        if (!keep_scale(mean, var)) ra[t] = rsqrtf(var);
-      }
-      named_sync(bar_id, kWGThreads);
-      {
-        float mean, var;
-        moments_tm<true>(tYT, ra, mean, var);
-        if (!keep_scale(mean, var)) {
-          const float rs = rsqrtf(var);
-          cc[t] = var * rs;
-          cb[t] = rs;
+    // ---- first row step from X itself, while the MMAs run: the rotated row
+    // y = Hs x / sqrt(128) has mean x_0 / sqrt(128) and variance
+    // sum_{k >= 1} x_k^2 / 128 (Hs has orthogonal rows of norm^2 128, and
+    // column sums 128, 0, 0, ...); in units of Y = Hs x: mean x_0, variance
+    // sum_{k >= 1} x_k^2 ----
+    cb[row] = 1.f;
+    cc[row] = 1.f;
+    if (a.iters > 0) {
+      float2 s2[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
+                      make_float2(0.f, 0.f)};
+      float x0 = 0.f;
+#pragma unroll
+      for (int c = 0; c < 16; ++c) {   // 16-byte chunk c: channels 8c .. 8c + 7
+        const uint8_t* xr = xs + (c >> 3) * kBoxBytes + row * 128;
+        uint4 u = *reinterpret_cast<const uint4*>(xr + (((c & 7) ^ (row & 7)) << 4));
+        if (c == 0) {
+          x0 = __half2float(__ushort_as_half((unsigned short)(u.x & 0xFFFFu)));
+          u.x &= 0xFFFF0000u;   // channel 0 is the mean, not part of the variance
+        }
+        const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&w[e]));
+          s2[e] = __ffma2_rn(f, f, s2[e]);
         }
       }
+      const float var = ((s2[0].x + s2[0].y) + (s2[1].x + s2[1].y)) +
+                        ((s2[2].x + s2[2].y) + (s2[3].x + s2[3].y));
+      ra[row] = keep_scale(x0, var) ? kInvSqrt128 : rsqrtf(var);
+    } else {
+      ra[row] = kInvSqrt128;
+    }
+    named_sync(bar_id, kWGThreads);
+    if (!mbar_wait_bounded(&S.mbar[wg], mph, kQWaitNs) && leader)
+      report(a.status, KVARN_STATUS_TIMEOUT);
+    mph ^= 1;
+    tc_fence_after();
+
+    // ---- Sinkhorn-like normalization: column step (row = channel), then
+    // for the later iterations row step (row = token) and column step ----
+    for (int it = 0; it < a.iters; ++it) {
+      if (it > 0) {
+        float mean, var;
+        moments_tm(tY, cb, mean, var);
+        if (!keep_scale(mean, var)) ra[row] = rsqrtf(var);
+        named_sync(bar_id, kWGThreads);
+      }
+      float mean, var;
+      moments_tm(tYT, ra, mean, var);
+      if (!keep_scale(mean, var)) {
+        const float rs = rsqrtf(var);
+        cc[row] = var * rs;
+        cb[row] = rs;
+      }
       named_sync(bar_id, kWGThreads);
     }
 
-    // ---- RTN + pack: per-token groups over x_td = Y_td / c_d ----
-    float mn, mx;
-    minmax_tm(tY, cb, mn, mx);
-    const float range = mx - mn;
-    const float qmax = part ? 3.f : 15.f;
-    const float inv = range > 0.f ? __fdividef(qmax, range) : 0.f;
-    if (rec) {
-      *reinterpret_cast<float2*>(rec + (part ? kOffVSZ : kOffKSZ) + 8 * t) =
-          make_float2(range * (kInvSqrt128 / qmax), mn * kInvSqrt128);
-      reinterpret_cast<float*>(rec + (part ? kOffVC : kOffKC))[t] = cc[t];
-    }
+    // ---- RTN + pack into the staging copy of the record part (the smem of
+    // this tile's input, free now), written out by one bulk copy ----
+    uint8_t* const out = xs;
     const float2 mg = make_float2(kMagic, kMagic);
     if (part == 0) {
       // K: token-major, 64 bytes per token; nibble e of word w = channel 8w + e
+      float mn, mx;
+      minmax_tm(tY, cb, mn, mx);
+      const float range = mx - mn;
+      const float inv = range > 0.f ? __fdividef(15.f, range) : 0.f;
+      *reinterpret_cast<float2*>(out + kOffKSZ + 8 * row) =
+          make_float2(range * (kInvSqrt128 / 15.f), mn * kInvSqrt128);
+      reinterpret_cast<float*>(out + kOffKC)[row] = cc[row];
+      // u = (y c^-1 - min) (15 / range): y c^-1 - min in one rounding
       const float2 nm = make_float2(-mn, -mn), iv = make_float2(inv, inv);
 #pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        float v[32];
-        tmem_chunk<true>(tY + 32 * c, cb + 32 * c, v);
-        uint32_t w[4];
+      for (int c = 0; c < 2; ++c) {
+        float v[64];
+        row_chunk<false>(tY, c, nullptr, v);
+        uint32_t w[8];
 #pragma unroll
-        for (int wd = 0; wd < 4; ++wd) {
+        for (int wd = 0; wd < 8; ++wd) {
           uint32_t acc = 0u - kMagicK;
+          const float4 c0 = *reinterpret_cast<const float4*>(cb + 64 * c + 8 * wd);
+          const float4 c1 = *reinterpret_cast<const float4*>(cb + 64 * c + 8 * wd + 4);
+          const float cw[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
 #pragma unroll
           for (int e = 0; e < 8; e += 2) {
             const int d = 8 * wd + e;
-            const float2 dd = __fadd2_rn(make_float2(v[d], v[d + 1]), nm);
+            const float2 dd = __ffma2_rn(make_float2(v[d], v[d + 1]),
+                                         make_float2(cw[e], cw[e + 1]), nm);
             const float2 f = __ffma2_rn(dd, iv, mg);
             acc += __float_as_uint(f.x) << (4 * e);
             acc += __float_as_uint(f.y) << (4 * e + 4);
           }
           w[wd] = acc;
         }
-        if (rec)
-          *reinterpret_cast<uint4*>(rec + kOffKCodes + 64 * t + 16 * c) =
-              make_uint4(w[0], w[1], w[2], w[3]);
+        // rows of 64 bytes: start at a chunk that depends on the row so that
+        // eight consecutive threads hit different banks
+        uint4* dst = reinterpret_cast<uint4*>(out + kOffKCodes + 64 * row + 32 * c);
+        const int sw = row & 1;
+        dst[sw] = make_uint4(w[4 * sw], w[4 * sw + 1], w[4 * sw + 2], w[4 * sw + 3]);
+        dst[sw ^ 1] = make_uint4(w[4 * (sw ^ 1)], w[4 * (sw ^ 1) + 1], w[4 * (sw ^ 1) + 2],
+                                 w[4 * (sw ^ 1) + 3]);
       }
     } else {
       // V: publish the per-token min and 3 / range, then thread d packs channel d
-      S.vmin[wg][t] = mn;
-      S.vinv[wg][t] = inv;
+      float mn, mx;
+      minmax_tm(tY, cb, mn, mx);
+      const float range = mx - mn;
+      const float inv = range > 0.f ? __fdividef(3.f, range) : 0.f;
+      S.vmin[wg][row] = mn;
+      S.vinv[wg][row] = inv;
+      *reinterpret_cast<float2*>(out + (kOffVSZ - kKPart) + 8 * row) =
+          make_float2(range * (kInvSqrt128 / 3.f), mn * kInvSqrt128);
+      reinterpret_cast<float*>(out + (kOffVC - kKPart))[row] = cc[row];
       named_sync(bar_id, kWGThreads);
-      const float c = cb[t];
-      const float2 cd = make_float2(c, c);
+      const float cd = cb[row];
+      const float2 cd2 = make_float2(cd, cd);
       const float* vm = S.vmin[wg];
       const float* vi = S.vinv[wg];
       uint32_t acc[4][2];
 #pragma unroll
       for (int j = 0; j < 4; ++j) acc[j][0] = acc[j][1] = 0u - kMagicV;
 #pragma unroll
-      for (int ch = 0; ch < 4; ++ch) {
-        float v[32];
-        tmem_chunk<false>(tYT + 32 * ch, nullptr, v);
+      for (int c = 0; c < 2; ++c) {
+        float v[64];
+        row_chunk<false>(tYT, c, nullptr, v);
 #pragma unroll
-        for (int q4 = 0; q4 < 32; q4 += 4) {
-          const int tt = 32 * ch + q4;
+        for (int i = 0; i < 64; i += 4) {
+          const int tt = 64 * c + i;
           const float4 m4 = *reinterpret_cast<const float4*>(vm + tt);
           const float4 i4 = *reinterpret_cast<const float4*>(vi + tt);
-          const float2 x0 = __fmul2_rn(make_float2(v[q4], v[q4 + 1]), cd);
-          const float2 x1 = __fmul2_rn(make_float2(v[q4 + 2], v[q4 + 3]), cd);
-          const float2 d0 = __fadd2_rn(x0, make_float2(-m4.x, -m4.y));
-          const float2 d1 = __fadd2_rn(x1, make_float2(-m4.z, -m4.w));
+          const float2 d0 = __ffma2_rn(make_float2(v[i], v[i + 1]), cd2,
+                                       make_float2(-m4.x, -m4.y));
+          const float2 d1 = __ffma2_rn(make_float2(v[i + 2], v[i + 3]), cd2,
+                                       make_float2(-m4.z, -m4.w));
           const float2 f0 = __ffma2_rn(d0, make_float2(i4.x, i4.y), mg);
           const float2 f1 = __ffma2_rn(d1, make_float2(i4.z, i4.w), mg);
           const float fv[4] = {f0.x, f0.y, f1.x, f1.y};
@@ -440,20 +497,25 @@ __global__ void __launch_bounds__(kQThreads, 1)
           }
         }
       }
-      if (rec) {
-        uint32_t* vw = reinterpret_cast<uint32_t*>(rec + kOffVCodes);
+      uint32_t* vw = reinterpret_cast<uint32_t*>(out + (kOffVCodes - kKPart));
 #pragma unroll
-        for (int j = 0; j < 4; ++j)
-          *reinterpret_cast<uint2*>(vw + v_word(t, j, 0)) = make_uint2(acc[j][0], acc[j][1]);
-      }
+      for (int j = 0; j < 4; ++j)
+        *reinterpret_cast<uint2*>(vw + v_word(row, j, 0)) = make_uint2(acc[j][0], acc[j][1]);
     }
-    // TMEM, the shared vectors and this tile's info are free for the next tile
+    // the staging copy is complete and TMEM is free for the next tile
+    fence_proxy_async_smem();
     tc_fence_before();
     named_sync(bar_id, kWGThreads);
+    if (leader && cur.rec >= 0) {
+      bulk_s2g(a.pool + cur.rec + (part ? kKPart : 0), out, part ? kVPart : kKPart);
+      bulk_commit();
+    }
     stage ^= 1;
   }
 
-  // ---- teardown: every MMA was waited for; free TMEM ----
+  // ---- teardown: every MMA was waited for; the packed outputs are written
+  // before the CTA's shared memory is released; free TMEM ----
+  if (leader) bulk_wait_all();
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
