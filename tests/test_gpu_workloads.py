@@ -1,0 +1,192 @@
+"""The five workloads at their full sizes, on the CUDA path, against the
+float64 oracle on sampled outputs.
+
+Every workload is quantized and decoded in full on the GPU, with the same
+launch configuration the bench uses.  The oracle then recomputes what it can
+finish in seconds: a seeded sample of whole tiles (every code and scale of
+those records, under the boundary rule) and whole sequences of decode
+attention (every head, every channel; fed the GPU's own pool so that decode is
+judged apart from boundary flips).  Mixed serving additionally checks every
+page that filled during its 64 append steps.
+
+Quantization: KVarN page (blog.edumints.com), "KVarN Nasil Calisir?", all
+four stages.  Decode and paging: "KV Cache (Anahtar-Deger Onbellegi)"
+(yapayzekasozluk.tr), "KV Cache Nasil Calisir?" and "Paged Attention (vLLM)".
+"""
+import numpy as np
+import pytest
+import torch
+
+import quantized_decode_attention_blocks_b300 as kv
+from oracle import kvref
+from tests import parity
+from tests.gpu_helpers import DEV, bits16, config, host
+from workloads import synth
+
+pytestmark = pytest.mark.gpu
+
+ITERS = 2
+
+
+def _oracle_record(tile_k, tile_v):
+    """Oracle record (both parts) of one (page, head) and its pre-rounding values."""
+    rk = kvref.quantize_tile(tile_k, False, ITERS)
+    rv = kvref.quantize_tile(tile_v, True, ITERS)
+    rec = rk["rec"].copy()
+    rec[9728:] = rv["rec"][9728:]
+    return rec, rk["u"], rv["u"]
+
+
+def _check_sampled_tiles(k, v, lens, table, pool, rng, n, stats):
+    """n random full blocks (b, j, head): GPU record against the oracle."""
+    lens_np = host(lens).astype(np.int64)
+    nfull = lens_np // 128
+    hkv = k.shape[2]
+    cand = [(b, j) for b in range(len(lens_np)) for j in range(int(nfull[b]))]
+    picks = rng.choice(len(cand), size=min(n, len(cand)), replace=False)
+    tab = host(table)
+    for i in picks:
+        b, j = cand[int(i)]
+        h = int(rng.integers(hkv))
+        tk = bits16(k[b, 128 * j:128 * j + 128, h])
+        tv = bits16(v[b, 128 * j:128 * j + 128, h])
+        ref, u_k, u_v = _oracle_record(tk, tv)
+        got = host(pool[int(tab[b, j]), h])
+        parity.compare_record(got, ref, u_k, u_v, stats)
+
+
+def _check_sampled_decode(cfg, q, out, pool, table, lens, tk, tv, seqs):
+    """Whole sequences `seqs`: the oracle reads a compact copy of just their pages."""
+    sel = torch.tensor(seqs, dtype=torch.long, device=DEV)
+    tab = table[sel]
+    used = torch.unique(tab[tab >= 0])
+    remap = torch.full((pool.shape[0],), -1, dtype=torch.int32, device=DEV)
+    remap[used] = torch.arange(used.numel(), dtype=torch.int32, device=DEV)
+    tab_c = torch.where(tab >= 0, remap[tab.clamp(min=0).long()], tab)
+    ref = kvref.decode_attention(host(q[sel]), host(pool[used]), host(tab_c), host(lens[sel]),
+                                 host(tk[sel]), host(tv[sel]), cfg.num_q_heads,
+                                 cfg.num_kv_heads, route=1)
+    return parity.compare_attention(host(out[sel]), ref)
+
+
+def _decode(cfg, q, pool, table, lens, max_seq, tk, tv):
+    out = torch.full((q.shape[0], cfg.num_q_heads, 128), float("nan"), dtype=torch.float16,
+                     device=DEV)
+    ws = kv.alloc_decode_workspace(cfg, q.shape[0], max_seq, DEV)
+    st = torch.zeros(1, dtype=torch.int32, device=DEV)
+    kv.kvarn_decode_attention(cfg, q, pool, table, lens, max_seq, tk, tv, out, ws, status=st)
+    return out, st
+
+
+@pytest.mark.parametrize("name", ["llama3_8b_layer", "long_context"])
+def test_single_layer_workload_full_size(name):
+    w = synth.WORKLOADS[name]
+    rng = np.random.default_rng(100 + w.seed)
+    cfg = config(w.hq, w.hkv)
+    k, v = synth.kv(w, device=DEV)
+    lens = synth.seq_lens(w, device=DEV)
+    tables, num_pages = synth.block_tables(w, device=DEV)
+    table = tables[0].contiguous()
+    pool = kv.alloc_pool(cfg, num_pages, DEV)
+    tk, tv = kv.alloc_tails(cfg, w.batch, DEV)
+    st = torch.zeros(1, dtype=torch.int32, device=DEV)
+    kv.kvarn_quantize_blocks(cfg, k, v, lens, w.seq, table, pool, tk, tv, st)
+    # one decode step: append the new token, then attend over len + 1 tokens
+    kn, vn = synth.new_tokens(w, 0, device=DEV)
+    kv.kvarn_append_token(cfg, kn, vn, lens, table, pool, tk, tv, st)
+    lens1 = lens + 1
+    q = synth.queries(w, device=DEV)
+    out, st2 = _decode(cfg, q, pool, table, lens1, w.seq + 1, tk, tv)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0 and int(st2.item()) == 0
+    assert torch.isfinite(out.float()).all()
+    stats = {}
+    _check_sampled_tiles(k, v, lens, table, pool, rng, 8, stats)
+    parity.check_flip_rate(stats)
+    seqs = sorted(rng.choice(w.batch, size=min(2, w.batch), replace=False).tolist())
+    _check_sampled_decode(cfg, q, out, pool, table, lens1, tk, tv, seqs)
+
+
+def test_qwen_like_workload_layers_full_size():
+    """28 layers share one pool of pages scattered across it; the first and the
+    last layer are run at full size (the others differ only in their seed and
+    their slice of the pool)."""
+    w = synth.WORKLOADS["qwen25_15b"]
+    rng = np.random.default_rng(100 + w.seed)
+    cfg = config(w.hq, w.hkv)
+    tables, num_pages = synth.block_tables(w, device=DEV)
+    pool = kv.alloc_pool(cfg, num_pages, DEV)
+    lens = synth.seq_lens(w, device=DEV)
+    stats = {}
+    for layer in (0, w.layers - 1):
+        table = tables[layer].contiguous()
+        k, v = synth.kv(w, layer=layer, device=DEV)
+        tk, tv = kv.alloc_tails(cfg, w.batch, DEV)
+        st = torch.zeros(1, dtype=torch.int32, device=DEV)
+        kv.kvarn_quantize_blocks(cfg, k, v, lens, w.seq, table, pool, tk, tv, st)
+        q = synth.queries(w, layer=layer, device=DEV)
+        out, st2 = _decode(cfg, q, pool, table, lens, w.seq, tk, tv)
+        torch.cuda.synchronize()
+        assert int(st.item()) == 0 and int(st2.item()) == 0
+        _check_sampled_tiles(k, v, lens, table, pool, rng, 6, stats)
+        seqs = sorted(rng.choice(w.batch, size=2, replace=False).tolist())
+        _check_sampled_decode(cfg, q, out, pool, table, lens, tk, tv, seqs)
+        del k, v
+    parity.check_flip_rate(stats)
+
+
+def test_mixed_serving_full_size_with_appends():
+    """128 requests of mixed lengths, pages scattered; 64 decode steps, each
+    appending one token per request (a filled tail block is quantized in the
+    same launch) and attending over the pages plus the fp16 tail."""
+    w = synth.WORKLOADS["mixed_serving"]
+    rng = np.random.default_rng(100 + w.seed)
+    cfg = config(w.hq, w.hkv)
+    k, v = synth.kv(w, device=DEV)
+    lens = synth.seq_lens(w, device=DEV)
+    tables, num_pages = synth.block_tables(w, device=DEV)
+    table = tables[0].contiguous()
+    pool = kv.alloc_pool(cfg, num_pages, DEV)
+    tk, tv = kv.alloc_tails(cfg, w.batch, DEV)
+    st = torch.zeros(1, dtype=torch.int32, device=DEV)
+    max_seq = w.seq + w.decode_steps
+    kv.kvarn_quantize_blocks(cfg, k, v, lens, w.seq, table, pool, tk, tv, st)
+    new = []
+    cur = lens.clone()
+    for step in range(w.decode_steps):
+        kn, vn = synth.new_tokens(w, step, device=DEV)
+        new.append((kn, vn))
+        kv.kvarn_append_token(cfg, kn, vn, cur, table, pool, tk, tv, st)
+        cur = cur + 1
+        q = synth.queries(w, step=step, device=DEV)
+        out, st2 = _decode(cfg, q, pool, table, cur, max_seq, tk, tv)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0 and int(st2.item()) == 0
+    stats = {}
+    _check_sampled_tiles(k, v, lens, table, pool, rng, 8, stats)
+    # every block that filled during the appends: prefill leftovers + new tokens
+    lens0 = host(lens).astype(np.int64)
+    tab = host(table)
+    new_k = np.stack([bits16(kn) for kn, _ in new])     # [step][B][Hkv][128]
+    new_v = np.stack([bits16(vn) for _, vn in new])
+    filled = 0
+    for b in range(w.batch):
+        start = int(lens0[b] // 128) * 128
+        n_old = int(lens0[b]) - start
+        if lens0[b] + w.decode_steps < start + 128:
+            continue
+        j = start // 128
+        old_k = bits16(k[b, start:start + n_old])        # [n_old][Hkv][128]
+        old_v = bits16(v[b, start:start + n_old])
+        got = host(pool[int(tab[b, j])])
+        for h in range(w.hkv):
+            tile_k = np.concatenate([old_k[:, h], new_k[:128 - n_old, b, h]])
+            tile_v = np.concatenate([old_v[:, h], new_v[:128 - n_old, b, h]])
+            ref, u_k, u_v = _oracle_record(tile_k, tile_v)
+            parity.compare_record(got[h], ref, u_k, u_v, stats)
+            filled += 1
+    assert filled > 0
+    parity.check_flip_rate(stats)
+    # the last step's decode on sampled requests
+    seqs = sorted(rng.choice(w.batch, size=3, replace=False).tolist())
+    _check_sampled_decode(cfg, q, out, pool, table, cur, tk, tv, seqs)
