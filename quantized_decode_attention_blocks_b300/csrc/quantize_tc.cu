@@ -159,52 +159,56 @@ __device__ __forceinline__ void row_chunk(uint32_t taddr, int c, const float* f,
 }
 
 // Centred population moments of w_c = Y[lane][c] f_c over the 128 columns of
-// this thread's TMEM lane, two passes, 64 columns at a time.  The weights are
-// fused into the arithmetic (s += v f; e = v f - mean; q += e e: three FP32
-// operations per value, the FMA pipe being the bound of this kernel).
+// this thread's TMEM lane.  Each half of 64 columns is done in two passes
+// over registers with its 64 weights loaded once (the weight loads, shared
+// memory broadcasts, are the costly part), and the halves are merged with the
+// parallel-variance formula M2 = M2_a + M2_b + (mean_a - mean_b)^2 n_a n_b / n
+// (Chan, Golub and LeVeque), which is as stable as one two-pass sweep.  The
+// weights are fused into the arithmetic: three FP32 operations per value.
 __device__ __forceinline__ void moments_tm(uint32_t taddr, const float* f, float& mean,
                                            float& var) {
-  float2 s[4];
-#pragma unroll
-  for (int k = 0; k < 4; ++k) s[k] = make_float2(0.f, 0.f);
+  float hm[2], hq[2];
 #pragma unroll
   for (int c = 0; c < 2; ++c) {
-    float v[64];
-    row_chunk<false>(taddr, c, nullptr, v);
+    float v[64], w[64];
+    tmem_ld64(taddr + 64 * c, v);
 #pragma unroll
-    for (int i = 0; i < 64; i += 8) {
-      const float4 f0 = *reinterpret_cast<const float4*>(f + 64 * c + i);
-      const float4 f1 = *reinterpret_cast<const float4*>(f + 64 * c + i + 4);
-      s[0] = __ffma2_rn(make_float2(v[i], v[i + 1]), make_float2(f0.x, f0.y), s[0]);
-      s[1] = __ffma2_rn(make_float2(v[i + 2], v[i + 3]), make_float2(f0.z, f0.w), s[1]);
-      s[2] = __ffma2_rn(make_float2(v[i + 4], v[i + 5]), make_float2(f1.x, f1.y), s[2]);
-      s[3] = __ffma2_rn(make_float2(v[i + 6], v[i + 7]), make_float2(f1.z, f1.w), s[3]);
+    for (int i = 0; i < 64; i += 4) {
+      const float4 f4 = *reinterpret_cast<const float4*>(f + 64 * c + i);
+      w[i] = f4.x;
+      w[i + 1] = f4.y;
+      w[i + 2] = f4.z;
+      w[i + 3] = f4.w;
     }
+    tmem_wait_ld();
+    float2 s[4];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) s[k] = make_float2(0.f, 0.f);
+#pragma unroll
+    for (int i = 0; i < 64; i += 8)
+#pragma unroll
+      for (int k = 0; k < 4; ++k)
+        s[k] = __ffma2_rn(make_float2(v[i + 2 * k], v[i + 2 * k + 1]),
+                          make_float2(w[i + 2 * k], w[i + 2 * k + 1]), s[k]);
+    const float m = (((s[0].x + s[0].y) + (s[1].x + s[1].y)) +
+                     ((s[2].x + s[2].y) + (s[3].x + s[3].y))) * (1.f / 64.f);
+    const float2 nm = make_float2(-m, -m);
+#pragma unroll
+    for (int k = 0; k < 4; ++k) s[k] = make_float2(0.f, 0.f);
+#pragma unroll
+    for (int i = 0; i < 64; i += 8)
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        const float2 e = __ffma2_rn(make_float2(v[i + 2 * k], v[i + 2 * k + 1]),
+                                    make_float2(w[i + 2 * k], w[i + 2 * k + 1]), nm);
+        s[k] = __ffma2_rn(e, e, s[k]);
+      }
+    hm[c] = m;
+    hq[c] = ((s[0].x + s[0].y) + (s[1].x + s[1].y)) + ((s[2].x + s[2].y) + (s[3].x + s[3].y));
   }
-  mean = (((s[0].x + s[0].y) + (s[1].x + s[1].y)) + ((s[2].x + s[2].y) + (s[3].x + s[3].y))) *
-         (1.f / 128.f);
-  const float2 nm = make_float2(-mean, -mean);
-#pragma unroll
-  for (int k = 0; k < 4; ++k) s[k] = make_float2(0.f, 0.f);
-#pragma unroll
-  for (int c = 0; c < 2; ++c) {
-    float v[64];
-    row_chunk<false>(taddr, c, nullptr, v);
-#pragma unroll
-    for (int i = 0; i < 64; i += 8) {
-      const float4 f0 = *reinterpret_cast<const float4*>(f + 64 * c + i);
-      const float4 f1 = *reinterpret_cast<const float4*>(f + 64 * c + i + 4);
-      float2 e[4];
-      e[0] = __ffma2_rn(make_float2(v[i], v[i + 1]), make_float2(f0.x, f0.y), nm);
-      e[1] = __ffma2_rn(make_float2(v[i + 2], v[i + 3]), make_float2(f0.z, f0.w), nm);
-      e[2] = __ffma2_rn(make_float2(v[i + 4], v[i + 5]), make_float2(f1.x, f1.y), nm);
-      e[3] = __ffma2_rn(make_float2(v[i + 6], v[i + 7]), make_float2(f1.z, f1.w), nm);
-#pragma unroll
-      for (int k = 0; k < 4; ++k) s[k] = __ffma2_rn(e[k], e[k], s[k]);
-    }
-  }
-  var = (((s[0].x + s[0].y) + (s[1].x + s[1].y)) + ((s[2].x + s[2].y) + (s[3].x + s[3].y))) *
-        (1.f / 128.f);
+  const float d = hm[0] - hm[1];
+  mean = 0.5f * (hm[0] + hm[1]);
+  var = (hq[0] + hq[1] + 32.f * d * d) * (1.f / 128.f);
 }
 
 // min and max of w_c = Y[lane][c] f_c
