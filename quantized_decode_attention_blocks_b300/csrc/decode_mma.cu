@@ -50,6 +50,7 @@ template <int NT>
 struct __align__(128) MmaSmem {
   uint8_t rec[kWarps][kRec];     // per warp: K part at 0, V part at kKPart
   float qrot[4 * NT][kD];        // H q per (padded) query head of the group
+  float qplain[4 * NT][kD];      // q itself, for the fp16 tail
   uint64_t bar[kWarps][2];       // per warp: 0 = K part landed, 1 = V part landed
   int ticket;
 };
@@ -164,12 +165,17 @@ __global__ void __launch_bounds__(kThreads, 3) decode_mma_kernel(DecodeArgs a) {
   __syncwarp();
 
   const int32_t* trow = a.block_table + (int64_t)b * a.max_blocks;
-  auto page_of = [&](int u) -> int64_t {
-    if (u >= u1) return -1;
-    const int64_t p = trow[u];
-    if (p < 0 || p >= a.num_pages) {
-      if (lane == 0) report(a.status, KVARN_STATUS_BAD_PAGE);
-      return -1;
+  // page ids of this warp's pages u, u + 4, ... (32 of them from `ubase`, one
+  // per lane); entries outside the pool are reported and skipped (-1)
+  auto fetch_ids = [&](int ubase) -> int {
+    const int uu = ubase + kWarps * lane;
+    int p = -1;
+    if (uu < u1) {
+      p = trow[uu];
+      if (p < 0 || (int64_t)p >= a.num_pages) {
+        report(a.status, KVARN_STATUS_BAD_PAGE);
+        p = -1;
+      }
     }
     return p;
   };
@@ -187,9 +193,30 @@ __global__ void __launch_bounds__(kThreads, 3) decode_mma_kernel(DecodeArgs a) {
     }
   };
 
-  // this warp's first page in flight while the query is rotated
+  // the query (warp w: heads w, w + 4; lane holds channels 32i + lane) and
+  // this warp's page ids are fetched together
+  const __half* qb = a.q + ((int64_t)b * a.hq + (int64_t)kvh * g) * kD;
+  float xq[NT][4];
+#pragma unroll
+  for (int hh = 0; hh < NT; ++hh) {
+    const int h = warp + kWarps * hh;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) xq[hh][i] = h < g ? __half2float(qb[h * kD + 32 * i + lane]) : 0.f;
+  }
   int u = u0 + warp;
-  int64_t cur = page_of(u);
+  int ids = fetch_ids(u);
+  int jb = 0;   // index of page u within the current batch of ids
+  const __half* tkb = a.tail_k + ((int64_t)b * a.hkv + kvh) * kT * kD;
+  const __half* tvb = a.tail_v + ((int64_t)b * a.hkv + kvh) * kT * kD;
+  if (has_tail && warp == kWarps - 1 && lane == 0 &&
+      ((reinterpret_cast<uintptr_t>(tkb) | reinterpret_cast<uintptr_t>(tvb)) & 15) == 0) {
+    // the tail is read at the end: have it in L2 by then
+    bulk_prefetch_l2(tkb, (uint32_t)rem * kD * 2);
+    bulk_prefetch_l2(tvb, (uint32_t)rem * kD * 2);
+  }
+
+  // this warp's first page in flight while the query is rotated
+  int64_t cur = __shfl_sync(0xffffffffu, ids, 0);
   bool k_busy = false, v_busy = false;
   uint32_t kph = 0, vph = 0;
   if (cur >= 0) {
@@ -198,15 +225,13 @@ __global__ void __launch_bounds__(kThreads, 3) decode_mma_kernel(DecodeArgs a) {
     k_busy = v_busy = true;
   }
 
-  // ---- q~ = H q: warp w rotates heads w, w + 4 (lane holds channels 32i + lane) ----
-  {
-  const __half* qb = a.q + ((int64_t)b * a.hq + (int64_t)kvh * g) * kD;
+  // ---- q~ = H q ----
 #pragma unroll
   for (int hh = 0; hh < NT; ++hh) {
     const int h = warp + kWarps * hh;
-    float x[4];
+    float* x = xq[hh];
 #pragma unroll
-    for (int i = 0; i < 4; ++i) x[i] = h < g ? __half2float(qb[h * kD + 32 * i + lane]) : 0.f;
+    for (int i = 0; i < 4; ++i) S.qplain[h][32 * i + lane] = x[i] * sl2;
     // channel bits 5, 6 are local
     float y0 = x[0] + x[1], y1 = x[0] - x[1], y2 = x[2] + x[3], y3 = x[2] - x[3];
     x[0] = y0 + y2; x[2] = y0 - y2; x[1] = y1 + y3; x[3] = y1 - y3;
@@ -222,7 +247,6 @@ __global__ void __launch_bounds__(kThreads, 3) decode_mma_kernel(DecodeArgs a) {
     }
 #pragma unroll
     for (int i = 0; i < 4; ++i) S.qrot[h][qrot_pos(32 * i + lane)] = x[i] * kInvSqrt128;
-  }
   }
   __syncthreads();
 
@@ -260,8 +284,8 @@ __global__ void __launch_bounds__(kThreads, 3) decode_mma_kernel(DecodeArgs a) {
         const float4* qv = reinterpret_cast<const float4*>(S.qrot[h]);
         const float4* cv = reinterpret_cast<const float4*>(kst + kOffKC + 128 * qi);
         float v[32];
-        float amax = 0.f;
-        float2 sum2 = make_float2(0.f, 0.f);
+        float am0 = 0.f, am1 = 0.f;
+        float2 s0 = make_float2(0.f, 0.f), s1 = s0;
 #pragma unroll
         for (int k = 0; k < 8; ++k) {
           const float4 q4 = qv[(8 * qi + k) ^ qi], c4 = cv[k];
@@ -271,11 +295,14 @@ __global__ void __launch_bounds__(kThreads, 3) decode_mma_kernel(DecodeArgs a) {
           v[4 * k + 1] = p0.y;
           v[4 * k + 2] = p1.x;
           v[4 * k + 3] = p1.y;
-          amax = max3(amax, fabsf(p0.x), fabsf(p0.y));
-          amax = max3(amax, fabsf(p1.x), fabsf(p1.y));
-          sum2 = __fadd2_rn(sum2, __fadd2_rn(p0, p1));
+          am0 = max3(am0, fabsf(p0.x), fabsf(p0.y));
+          am1 = max3(am1, fabsf(p1.x), fabsf(p1.y));
+          s0 = __fadd2_rn(s0, p0);
+          s1 = __fadd2_rn(s1, p1);
         }
-        float sum = sum2.x + sum2.y;
+        float amax = fmaxf(am0, am1);
+        const float2 s01 = __fadd2_rn(s0, s1);
+        float sum = s01.x + s01.y;
         amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
         amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
         sum += __shfl_xor_sync(0xffffffffu, sum, 1);
@@ -346,7 +373,11 @@ __global__ void __launch_bounds__(kThreads, 3) decode_mma_kernel(DecodeArgs a) {
       }
     }
     __syncwarp();   // the K part of this page is consumed
-    const int64_t nxt = page_of(u + kWarps);
+    if (++jb == 32) {
+      ids = fetch_ids(u + kWarps);
+      jb = 0;
+    }
+    const int64_t nxt = __shfl_sync(0xffffffffu, ids, jb);
     if (nxt >= 0) {
       issue_k(nxt);
       k_busy = true;
@@ -356,21 +387,22 @@ __global__ void __launch_bounds__(kThreads, 3) decode_mma_kernel(DecodeArgs a) {
       float alpha[NT];
 #pragma unroll
       for (int nt = 0; nt < NT; ++nt) {
-        float pm = max3(sc[nt][0], sc[nt][1], sc[nt][2]);
+        float pq[4];
 #pragma unroll
-        for (int j = 3; j < 15; j += 2) pm = max3(pm, sc[nt][j], sc[nt][j + 1]);
-        pm = fmaxf(pm, sc[nt][15]);
+        for (int k = 0; k < 4; ++k)
+          pq[k] = fmaxf(max3(sc[nt][4 * k], sc[nt][4 * k + 1], sc[nt][4 * k + 2]), sc[nt][4 * k + 3]);
+        float pm = fmaxf(max3(pq[0], pq[1], pq[2]), pq[3]);
         pm = warp_max_r(pm);
         const float mnew = fmaxf(m[nt], pm);
         alpha[nt] = ex2(m[nt] - mnew);
         m[nt] = mnew;
-        float ls = 0.f;
+        float lq[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
         for (int j = 0; j < 16; ++j) {
           sc[nt][j] = ex2(sc[nt][j] - mnew);   // now p
-          ls += sc[nt][j];
+          lq[j & 3] += sc[nt][j];
         }
-        l[nt] = fmaf(l[nt], alpha[nt], ls);
+        l[nt] = fmaf(l[nt], alpha[nt], (lq[0] + lq[1]) + (lq[2] + lq[3]));
       }
 
       if (!mbar_wait_warp(vbar, vph, kWaitLimitNs)) {
@@ -383,13 +415,14 @@ __global__ void __launch_bounds__(kThreads, 3) decode_mma_kernel(DecodeArgs a) {
       // ---- P' = p s'V (scaled, hi | lo) transposed into B fragments ----
       // score slot j of this lane is token 16 (j >> 1) + 8 (j & 1) + r
       float2 szv[16];
-      float smax = 0.f;
+      float sm4[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
       for (int j = 0; j < 16; ++j) {
         szv[j] = *reinterpret_cast<const float2*>(vst + (kOffVSZ - kKPart) +
                                                   8 * (16 * (j >> 1) + 8 * (j & 1) + r));
-        smax = fmaxf(smax, szv[j].x);
+        sm4[j & 3] = fmaxf(sm4[j & 3], szv[j].x);
       }
+      float smax = fmaxf(fmaxf(sm4[0], sm4[1]), fmaxf(sm4[2], sm4[3]));
       smax = warp_max_r(smax);
       float fs, finv;
       pow2_scale(smax, fs, finv);
@@ -400,15 +433,15 @@ __global__ void __launch_bounds__(kThreads, 3) decode_mma_kernel(DecodeArgs a) {
       float zpage[NT];
 #pragma unroll
       for (int nt = 0; nt < NT; ++nt) {
-        float zp = 0.f;
+        float zq[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
         for (int j = 0; j < 16; ++j) {
           const float x = sc[nt][j] * sf[j];
           const float hi = head11(x);
           bp[nt][j >> 1][j & 1] = movm_trans(pack2(hi, x - hi));
-          zp = fmaf(sc[nt][j], szv[j].y, zp);
+          zq[j & 3] = fmaf(sc[nt][j], szv[j].y, zq[j & 3]);
         }
-        zpage[nt] = warp_sum_r(zp);
+        zpage[nt] = warp_sum_r((zq[0] + zq[1]) + (zq[2] + zq[3]));
       }
 
       // ---- value sum: V codes (A, rows = channels) x P' (B).  MCG channel
@@ -538,23 +571,15 @@ __global__ void __launch_bounds__(kThreads, 3) decode_mma_kernel(DecodeArgs a) {
 
   // ---- fp16 tail (plain space): warp w takes tail tokens w, w + 4, ... and
   // folds them into its own state; lane holds channels 4 lane .. 4 lane + 3 ----
-  const __half* qb2 = a.q + ((int64_t)b * a.hq + (int64_t)kvh * g) * kD;
   if (has_tail && !timed_out) {
-    const __half* tkb = a.tail_k + ((int64_t)b * a.hkv + kvh) * kT * kD;
-    const __half* tvb = a.tail_v + ((int64_t)b * a.hkv + kvh) * kT * kD;
     float qr[G][4], mt[G], lt[G], ot[G][4];
 #pragma unroll
     for (int h = 0; h < G; ++h) {
-      float2 q01 = make_float2(0.f, 0.f), q23 = q01;
-      if (h < g) {
-        const uint2 qq = __ldg(reinterpret_cast<const uint2*>(qb2 + h * kD + 4 * lane));
-        q01 = __half22float2(*reinterpret_cast<const __half2*>(&qq.x));
-        q23 = __half22float2(*reinterpret_cast<const __half2*>(&qq.y));
-      }
-      qr[h][0] = q01.x * sl2;
-      qr[h][1] = q01.y * sl2;
-      qr[h][2] = q23.x * sl2;
-      qr[h][3] = q23.y * sl2;
+      const float4 q4 = *reinterpret_cast<const float4*>(&S.qplain[h][4 * lane]);
+      qr[h][0] = q4.x;
+      qr[h][1] = q4.y;
+      qr[h][2] = q4.z;
+      qr[h][3] = q4.w;
       mt[h] = st[2 * h];
       lt[h] = st[2 * h + 1];
       const float4 o4 = *reinterpret_cast<const float4*>(ow + h * kOPitch + 4 * lane);

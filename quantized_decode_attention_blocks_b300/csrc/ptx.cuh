@@ -74,6 +74,12 @@ __device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t by
       : "memory");
 }
 
+// Asks the TMA engine to bring [src, src + bytes) into L2 (both 16-byte
+// multiples); no completion to wait for.
+__device__ __forceinline__ void bulk_prefetch_l2(const void* src, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
+}
+
 // ------------------------------------------------------------ tensor cores --
 
 // D += A(16x16, row) * B(16x8, col), fp16 inputs, fp32 accumulate.
