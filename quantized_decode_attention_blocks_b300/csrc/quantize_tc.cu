@@ -9,17 +9,25 @@
 // (normalization) and "Kuantize Edilmis Onbellek" (RTN); format kvarn_k4v2_g128.
 //
 // Layout of the work.  A persistent CTA runs two independent tile pipelines
-// (warpgroups of 128 threads).  For each tile, one thread of the pipeline
-// issues the TMA load of the fp16 tile X (two 64-channel boxes, 128-byte
-// swizzle) and then two chains of tcgen05.mma against the +-1 Sylvester
-// matrix Hs (held once per CTA in shared memory, symmetric):
-//     Y  = X Hs      (TMEM lane t = token t, column d = channel d)
-//     Y^T = Hs X^T   (TMEM lane d = channel d, column t = token t)
-// so that thread t reads its token row and thread d its channel column from
-// TMEM without any transpose.  The products of fp16 inputs and +-1 are exact
-// and accumulate in fp32; Y = sqrt(128) y with y_t = H x_t, and the factor
-// cancels in every normalized quantity (it is removed from the stored s', z').
-// The next tile's TMA load runs under this tile's MMAs and arithmetic.
+// of 256 threads.  For each tile, one thread of the pipeline has issued the
+// TMA load of the fp16 tile X (two 64-channel boxes, 128-byte swizzle) a tile
+// ahead; another issues two chains of tcgen05.mma against the +-1 Sylvester
+// matrix Hs (held once per CTA in shared memory, symmetric, its rows in the
+// order chan_of):
+//     Y  = X Hs      (TMEM lane t = token t, column n = channel chan_of(n))
+//     Y^T = Hs X^T   (TMEM lane n = channel chan_of(n), column t = token t)
+// The products of fp16 inputs and +-1 are exact and accumulate in fp32;
+// Y = sqrt(128) y with y_t = H x_t, and the factor cancels in every normalized
+// quantity (it is removed from the stored s', z').
+//
+// Each warp reads 16 TMEM lanes of Y or Y^T in the 16x256b shape: a thread
+// holds two rows, 32 columns of each, and the four threads of a quad hold one
+// row's 128 columns.  Row statistics are quad reductions, and each thread
+// needs only the 32 weights of its columns (the other axis's scales), so the
+// shared-memory traffic of the weights is a quarter of a thread-per-row
+// layout's.  The column order chan_of makes a thread's 32 columns of Y the
+// consecutive channels of whole K code words, and its 32 columns of Y^T
+// (tokens) whole V code words, so that every thread packs complete words.
 //
 // Arithmetic (fp32, centred two-pass moments as in the definition):
 //  * row step t:    1/r_t = 1 / std_d(Y_td / c_d)       (the old r_t cancels)
@@ -42,7 +50,9 @@ namespace {
 using namespace ptx;
 
 constexpr int kWG = 2;                            // tile pipelines per CTA
-constexpr int kWGThreads = 128;                   // one thread per TMEM lane (row)
+// 256 threads per pipeline: warp w of a pipeline reads the TMEM lane quarter
+// w & 3, and the 16-lane half w >> 2 of it
+constexpr int kWGThreads = 256;
 constexpr int kQThreads = kWGThreads * kWG;
 constexpr uint32_t kTileBytes = kT * kD * 2;      // one fp16 tile
 constexpr uint32_t kBoxBytes = kTileBytes / 2;    // 64 channels x 128 tokens
@@ -66,22 +76,24 @@ struct TileInfo {
 
 struct __align__(1024) QSmem {
   uint8_t hs[kTileBytes];                // +-1 Sylvester matrix, fp16, swizzled
-  uint8_t x[kWG][2][kTileBytes];         // input tiles (then the packed output), 2 stages
+  uint8_t x[kWG][2][kTileBytes];         // input tiles, 2 stages per pipeline
+  __align__(128) uint8_t out[kWG][kKPart];   // packed record part, staged for the bulk store
   __align__(16) float ra[kWG][kT];       // 1 / r_t, in units of Y
-  __align__(16) float cb[kWG][kD];       // 1 / c_d
+  __align__(16) float cb[kWG][kD];       // 1 / c, indexed by Y column (channel chan_of(n))
   __align__(16) float vmin[kWG][kT];     // V: per-token min of x
   __align__(16) float vinv[kWG][kT];     // V: per-token 3 / (max - min)
-  __align__(16) float cc[kWG][kD];       // c_d
+  __align__(16) float cc[kWG][kD];       // c_d, natural channel order
   TileInfo info[kWG][2];                 // tile held in each stage
-  uint64_t xbar[kWG][2];                 // tile landed
+  uint64_t full[kWG][2];                 // stage loaded (producer -> pipeline)
   uint64_t mbar[kWG];                    // MMAs done
   uint32_t tmem_base;
+  int abort;                             // a bounded wait ran out: stop waiting
 };
 static_assert(offsetof(QSmem, ra) % 16 == 0 && offsetof(QSmem, cb) % 16 == 0 &&
                   offsetof(QSmem, cc) % 16 == 0 && offsetof(QSmem, vmin) % 16 == 0 &&
                   offsetof(QSmem, vinv) % 16 == 0 && offsetof(QSmem, x) % 1024 == 0 &&
-                  offsetof(QSmem, xbar) % 8 == 0,
-              "vector loads and barriers need these alignments");
+                  offsetof(QSmem, out) % 128 == 0 && offsetof(QSmem, full) % 8 == 0,
+              "vector loads, bulk copies and barriers need these alignments");
 
 struct QTileArgs {
   int mode;            // 0: the full blocks of a prefill, 1: tails filled by an append
@@ -102,7 +114,8 @@ struct Tile {
   int b, j, h, part, t0;
 };
 
-__device__ __forceinline__ bool tile_of(const QTileArgs& a, int id, Tile& tl) {
+// (b, j, h, part) of tile id from the id alone
+__device__ __forceinline__ void tile_decode(const QTileArgs& a, int id, Tile& tl) {
   tl.part = id & 1;
   int rest = id >> 1;
   tl.h = rest % a.hkv;
@@ -110,7 +123,15 @@ __device__ __forceinline__ bool tile_of(const QTileArgs& a, int id, Tile& tl) {
   if (a.mode == 0) {
     tl.j = rest % a.nb;
     tl.b = rest / a.nb;
-    const int len = a.seq_lens[tl.b];
+  } else {
+    tl.b = rest;
+  }
+}
+
+// Whether the decoded tile is a block to quantize, given its sequence's length
+// (mode 0) or length before the append (mode 1).
+__device__ __forceinline__ bool tile_valid(const QTileArgs& a, Tile& tl, int len) {
+  if (a.mode == 0) {
     if (len < 0 || len > a.max_seq) {
       if (tl.j == 0 && tl.h == 0 && tl.part == 0) report(a.status, KVARN_STATUS_BAD_LENGTH);
       return false;
@@ -118,11 +139,29 @@ __device__ __forceinline__ bool tile_of(const QTileArgs& a, int id, Tile& tl) {
     tl.t0 = kT * tl.j;
     return tl.j < len / kT;
   }
-  tl.b = rest;
-  const int p = a.pos[tl.b];
-  tl.j = p / kT;
+  tl.j = len / kT;
   tl.t0 = 0;
-  return p >= 0 && p % kT == kT - 1;
+  return len >= 0 && len % kT == kT - 1;
+}
+
+// Metadata of a candidate tile, loaded one tile ahead of its use: the length
+// of its sequence and (mode 0) its block-table entry.
+struct Cand {
+  int id, len, page;
+};
+
+__device__ __forceinline__ Cand fetch_cand(const QTileArgs& a, int id) {
+  Cand c{id, -1, -1};
+  if (id >= a.ntiles) return c;
+  Tile tl;
+  tile_decode(a, id, tl);
+  if (a.mode == 0) {
+    c.len = __ldg(a.seq_lens + tl.b);
+    if (tl.j < a.max_blocks) c.page = __ldg(a.block_table + (int64_t)tl.b * a.max_blocks + tl.j);
+  } else {
+    c.len = __ldg(a.pos + tl.b);
+  }
+  return c;
 }
 
 __device__ __forceinline__ float max3f(float a, float b, float c) {
@@ -136,98 +175,71 @@ __device__ __forceinline__ float min3f(float a, float b, float c) {
   return d;
 }
 
-// 64 columns (64 c .. 64 c + 63) of this thread's TMEM lane, scaled in place
-// by f (shared memory, the same weights for every thread: broadcast loads)
-// when HAS_F.
-template <bool HAS_F>
-__device__ __forceinline__ void row_chunk(uint32_t taddr, int c, const float* f,
-                                          float (&v)[64]) {
-  tmem_ld64(taddr + 64 * c, v);
-  tmem_wait_ld();
-  if (HAS_F) {
-#pragma unroll
-    for (int i = 0; i < 64; i += 4) {
-      const float4 f4 = *reinterpret_cast<const float4*>(f + 64 * c + i);
-      const float2 a0 = __fmul2_rn(make_float2(v[i], v[i + 1]), make_float2(f4.x, f4.y));
-      const float2 a1 = __fmul2_rn(make_float2(v[i + 2], v[i + 3]), make_float2(f4.z, f4.w));
-      v[i] = a0.x;
-      v[i + 1] = a0.y;
-      v[i + 2] = a1.x;
-      v[i + 3] = a1.y;
-    }
-  }
+// Channel held by column n of Y and by lane n of Y^T.  The rows of the Hadamard
+// operand are stored in this order, so that the columns 8k + 2 (i & 3) + b of
+// the 16x256b fragment of thread i are the 32 consecutive channels
+// 32 (i & 3) + 2k + b: whole bytes and words of a packed K row.
+__device__ __forceinline__ int chan_of(int n) {
+  return 32 * ((n >> 1) & 3) + 2 * (n >> 3) + (n & 1);
 }
 
-// Centred population moments of w_c = Y[lane][c] f_c over the 128 columns of
-// this thread's TMEM lane.  Each half of 64 columns is done in two passes
-// over registers with its 64 weights loaded once (the weight loads, shared
-// memory broadcasts, are the costly part), and the halves are merged with the
-// parallel-variance formula M2 = M2_a + M2_b + (mean_a - mean_b)^2 n_a n_b / n
-// (Chan, Golub and LeVeque), which is as stable as one two-pass sweep.  The
-// weights are fused into the arithmetic: three FP32 operations per value.
-__device__ __forceinline__ void moments_tm(uint32_t taddr, const float* f, float& mean,
-                                           float& var) {
-  float hm[2], hq[2];
-#pragma unroll
-  for (int c = 0; c < 2; ++c) {
-    float v[64], w[64];
-    tmem_ld64(taddr + 64 * c, v);
-#pragma unroll
-    for (int i = 0; i < 64; i += 4) {
-      const float4 f4 = *reinterpret_cast<const float4*>(f + 64 * c + i);
-      w[i] = f4.x;
-      w[i + 1] = f4.y;
-      w[i + 2] = f4.z;
-      w[i + 3] = f4.w;
-    }
-    tmem_wait_ld();
-    float2 s[4];
-#pragma unroll
-    for (int k = 0; k < 4; ++k) s[k] = make_float2(0.f, 0.f);
-#pragma unroll
-    for (int i = 0; i < 64; i += 8)
-#pragma unroll
-      for (int k = 0; k < 4; ++k)
-        s[k] = __ffma2_rn(make_float2(v[i + 2 * k], v[i + 2 * k + 1]),
-                          make_float2(w[i + 2 * k], w[i + 2 * k + 1]), s[k]);
-    const float m = (((s[0].x + s[0].y) + (s[1].x + s[1].y)) +
-                     ((s[2].x + s[2].y) + (s[3].x + s[3].y))) * (1.f / 64.f);
-    const float2 nm = make_float2(-m, -m);
-#pragma unroll
-    for (int k = 0; k < 4; ++k) s[k] = make_float2(0.f, 0.f);
-#pragma unroll
-    for (int i = 0; i < 64; i += 8)
-#pragma unroll
-      for (int k = 0; k < 4; ++k) {
-        const float2 e = __ffma2_rn(make_float2(v[i + 2 * k], v[i + 2 * k + 1]),
-                                    make_float2(w[i + 2 * k], w[i + 2 * k + 1]), nm);
-        s[k] = __ffma2_rn(e, e, s[k]);
-      }
-    hm[c] = m;
-    hq[c] = ((s[0].x + s[0].y) + (s[1].x + s[1].y)) + ((s[2].x + s[2].y) + (s[3].x + s[3].y));
-  }
-  const float d = hm[0] - hm[1];
-  mean = 0.5f * (hm[0] + hm[1]);
-  var = (hq[0] + hq[1] + 32.f * d * d) * (1.f / 128.f);
+// sums, minima and maxima over the four threads of a quad (one fragment row)
+__device__ __forceinline__ float quad_sum(float x) {
+  x += __shfl_xor_sync(0xffffffffu, x, 1);
+  return x + __shfl_xor_sync(0xffffffffu, x, 2);
+}
+__device__ __forceinline__ float quad_min(float x) {
+  x = fminf(x, __shfl_xor_sync(0xffffffffu, x, 1));
+  return fminf(x, __shfl_xor_sync(0xffffffffu, x, 2));
+}
+__device__ __forceinline__ float quad_max(float x) {
+  x = fmaxf(x, __shfl_xor_sync(0xffffffffu, x, 1));
+  return fmaxf(x, __shfl_xor_sync(0xffffffffu, x, 2));
 }
 
-// min and max of w_c = Y[lane][c] f_c
-__device__ __forceinline__ void minmax_tm(uint32_t taddr, const float* f, float& mn, float& mx) {
-  mn = INFINITY;
-  mx = -INFINITY;
+// The weights of this thread's fragment columns 8k + 2q + b (f indexed by
+// column): 32 of the 128, one 8-byte load per k.
+__device__ __forceinline__ void frag_weights(const float* f, int q, float2 (&w)[16]) {
 #pragma unroll
-  for (int c = 0; c < 2; ++c) {
-    float v[64];
-    row_chunk<true>(taddr, c, f, v);
-#pragma unroll
-    for (int i = 0; i < 64; i += 4) {
-      mn = min3f(mn, v[i], v[i + 1]);
-      mx = max3f(mx, v[i], v[i + 1]);
-      mn = min3f(mn, v[i + 2], v[i + 3]);
-      mx = max3f(mx, v[i + 2], v[i + 3]);
-    }
-  }
+  for (int k = 0; k < 16; ++k) w[k] = *reinterpret_cast<const float2*>(f + 8 * k + 2 * q);
 }
+
+__device__ __forceinline__ float2 pair(const float (&v)[64], int k, int e) {
+  return make_float2(v[4 * k + 2 * e], v[4 * k + 2 * e + 1]);
+}
+
+// Centred population moments, over the 128 columns, of v * w in the two rows
+// (e = 0, 1) of this thread's fragment: two passes over registers, the four
+// threads of a quad adding their partial sums after each.
+__device__ __forceinline__ void frag_moments(const float (&v)[64], const float2 (&w)[16],
+                                             float (&mean)[2], float (&var)[2]) {
+  float2 s[2][2];
+#pragma unroll
+  for (int e = 0; e < 2; ++e) s[e][0] = s[e][1] = make_float2(0.f, 0.f);
+#pragma unroll
+  for (int k = 0; k < 16; ++k)
+#pragma unroll
+    for (int e = 0; e < 2; ++e) s[e][k & 1] = __ffma2_rn(pair(v, k, e), w[k], s[e][k & 1]);
+  float2 nm[2];
+#pragma unroll
+  for (int e = 0; e < 2; ++e) {
+    mean[e] = quad_sum((s[e][0].x + s[e][0].y) + (s[e][1].x + s[e][1].y)) * (1.f / 128.f);
+    nm[e] = make_float2(-mean[e], -mean[e]);
+    s[e][0] = s[e][1] = make_float2(0.f, 0.f);
+  }
+#pragma unroll
+  for (int k = 0; k < 16; ++k)
+#pragma unroll
+    for (int e = 0; e < 2; ++e) {
+      const float2 d = __ffma2_rn(pair(v, k, e), w[k], nm[e]);
+      s[e][k & 1] = __ffma2_rn(d, d, s[e][k & 1]);
+    }
+#pragma unroll
+  for (int e = 0; e < 2; ++e)
+    var[e] = quad_sum((s[e][0].x + s[e][0].y) + (s[e][1].x + s[e][1].y)) * (1.f / 128.f);
+}
+
+__device__ __forceinline__ int lane4(int tid) { return tid & 3; }
 
 __device__ __forceinline__ bool keep_scale(float mean, float var) {
   // variance <= 1e-10 * mean square (mean square = var + mean^2): skip
@@ -247,18 +259,25 @@ __global__ void __launch_bounds__(kQThreads, 1)
                                        ~static_cast<uintptr_t>(1023));
   const int tid = threadIdx.x, wg = tid / kWGThreads, wt = tid % kWGThreads;
   const int warp = tid >> 5;
+  // roles in a pipeline: wt 0 issues the bulk stores of the packed output;
+  // lane 0 of warps 4 and 5 (idle during the first row step, which warps 0-3
+  // do) issue the tile's MMAs and the next tile's load
   const bool leader = wt == 0;
-  const int row = wt;   // this thread's TMEM lane: token in Y, channel in Y^T
+  const bool mma_thread = wt == 128;
+  const bool load_thread = wt == 160;
+  const int row = wt & 127;   // first row step, copies: token or channel
+  const bool lower = wt < 128;
 
-  // ---- once per CTA: Hs in the 128-byte swizzled K-major layout (two boxes
-  // of 64 columns; 16-byte chunk c of row n sits at chunk c ^ (n & 7)) ----
+  // ---- once per CTA: Hs with its rows in chan_of order, in the 128-byte
+  // swizzled K-major layout (two boxes of 64 columns; 16-byte chunk c of row n
+  // sits at chunk c ^ (n & 7)) ----
   for (int i = tid; i < kT * 16; i += kQThreads) {
     const int n = i >> 4, c = i & 15, box = c >> 3, cw = c & 7;
     uint32_t w[4];
 #pragma unroll
     for (int e = 0; e < 4; ++e) {
       const int k = 8 * c + 2 * e;
-      w[e] = hs_bits(n, k) | (hs_bits(n, k + 1) << 16);
+      w[e] = hs_bits(chan_of(n), k) | (hs_bits(chan_of(n), k + 1) << 16);
     }
     *reinterpret_cast<uint4*>(S.hs + box * kBoxBytes + n * 128 + ((cw ^ (n & 7)) << 4)) =
         make_uint4(w[0], w[1], w[2], w[3]);
@@ -267,10 +286,11 @@ __global__ void __launch_bounds__(kQThreads, 1)
   if (tid == 0) {
 #pragma unroll
     for (int g = 0; g < kWG; ++g) {
-      mbar_init(&S.xbar[g][0], 1);
-      mbar_init(&S.xbar[g][1], 1);
+      mbar_init(&S.full[g][0], 1);
+      mbar_init(&S.full[g][1], 1);
       mbar_init(&S.mbar[g], 1);
     }
+    S.abort = 0;
     fence_mbar_init();
   }
   if (warp == 0) {
@@ -282,31 +302,54 @@ __global__ void __launch_bounds__(kQThreads, 1)
   tc_fence_after();
   const uint32_t tmem = S.tmem_base;
 
-  const int gw = blockIdx.x * kWG + wg, nw = gridDim.x * kWG;
-  const uint32_t dY = tmem + wg * 256, dYT = dY + 128;                  // MMA destinations
-  const uint32_t lanes = (uint32_t)(32 * (warp & 3)) << 16;
-  const uint32_t tY = dY + lanes, tYT = dYT + lanes;                      // this warp's lanes
-  float* const ra = S.ra[wg];
-  float* const cb = S.cb[wg];
-  float* const cc = S.cc[wg];
-  const uint32_t bar_id = 1 + wg;
+  const int nw = gridDim.x * kWG;
   const int rh = a.roles & 3, rt = (a.roles >> 2) & 3;   // tensor-map dims of head, token
+  // bounded waits; once one has run out every later wait is skipped, so that
+  // the kernel still ends (with KVARN_STATUS_TIMEOUT reported)
+  auto wait = [&](uint64_t* bar, uint32_t ph) {
+    if (*reinterpret_cast<volatile int*>(&S.abort)) return;
+    if (!mbar_wait_bounded(bar, ph, kQWaitNs)) {
+      *reinterpret_cast<volatile int*>(&S.abort) = 1;
+      report(a.status, KVARN_STATUS_TIMEOUT);
+    }
+  };
 
-  // leader only: the next valid tile from `id` on, its TMA load into stage
-  // `st`, and its hand-off record for the other threads
-  auto prepare = [&](int id, int st) {
+  // load thread only: the next valid tile from the candidate on, its TMA load into
+  // stage `st` (free: its last tile's MMAs and first row step are done), and
+  // its hand-off record for the other threads.  The candidate's metadata was
+  // loaded a tile earlier; a candidate that is not a block falls back to a
+  // walk with fresh loads.  Returns the id taken (>= ntiles: none).
+  auto prepare = [&](Cand c, int st) -> int {
+    int id = c.id;
     Tile tl;
-    while (id < a.ntiles && !tile_of(a, id, tl)) id += nw;
+    int len = c.len;
+    int64_t page = c.page;
+    bool ok = false;
+    if (id < a.ntiles) {
+      tile_decode(a, id, tl);
+      ok = tile_valid(a, tl, len);
+    }
+    if (!ok && id < a.ntiles) {
+      for (id += nw; id < a.ntiles; id += nw) {
+        const Cand f = fetch_cand(a, id);
+        tile_decode(a, id, tl);
+        if (tile_valid(a, tl, f.len)) {
+          page = f.page;
+          ok = true;
+          break;
+        }
+      }
+    }
     TileInfo& info = S.info[wg][st];
     info.id = id;
     info.part = 0;
     info.rec = -1;
-    if (id >= a.ntiles) return;
+    if (id >= a.ntiles) return id;
     info.part = tl.part;
     const bool in_table = tl.j < a.max_blocks;
-    const int64_t page =
-        in_table ? (int64_t)a.block_table[(int64_t)tl.b * a.max_blocks + tl.j] : -1;
-    if (page >= 0 && page < a.num_pages)
+    if (a.mode != 0)
+      page = in_table ? (int64_t)a.block_table[(int64_t)tl.b * a.max_blocks + tl.j] : -1;
+    if (in_table && page >= 0 && page < a.num_pages)
       info.rec = (long long)((page * a.hkv + tl.h) * (int64_t)kRec);
     else
       report(a.status, in_table ? KVARN_STATUS_BAD_PAGE : KVARN_STATUS_BAD_LENGTH);
@@ -314,29 +357,43 @@ __global__ void __launch_bounds__(kQThreads, 1)
     const int c1 = rh == 1 ? tl.h : rt == 1 ? tl.t0 : tl.b;
     const int c2 = rh == 2 ? tl.h : rt == 2 ? tl.t0 : tl.b;
     const int c3 = rh == 3 ? tl.h : rt == 3 ? tl.t0 : tl.b;
-    bulk_wait_read();   // an earlier tile's packed output may still be leaving this stage
-    uint64_t* bar = &S.xbar[wg][st];
+    uint64_t* bar = &S.full[wg][st];
     mbar_arrive_expect_tx(bar, kTileBytes);
     tma_load_4d(S.x[wg][st], tm, 0, c1, c2, c3, bar);
     tma_load_4d(S.x[wg][st] + kBoxBytes, tm, 64, c1, c2, c3, bar);
+    return id;
   };
 
-  if (leader) prepare(gw, 0);
-  named_sync(bar_id, kWGThreads);
+  const uint32_t dY = tmem + wg * 256, dYT = dY + 128;                  // MMA destinations
+  // this warp's 16 TMEM lanes: quarter warp & 3, half (warp >> 2) & 1
+  const int hl = (warp >> 2) & 1;
+  const uint32_t lanes = (uint32_t)(32 * (warp & 3) + 16 * hl) << 16;
+  const uint32_t tY = dY + lanes, tYT = dYT + lanes;
+  const int q = lane4(tid), r4 = (tid & 31) >> 2;
+  // fragment row e of this thread: TMEM lane 32 (warp & 3) + 16 hl + r4 + 8 e
+  auto frow = [&](int e) { return 32 * (warp & 3) + 16 * hl + r4 + 8 * e; };
+  float* const ra = S.ra[wg];
+  float* const cb = S.cb[wg];
+  float* const cc = S.cc[wg];
+  uint8_t* const out = S.out[wg];
+  const uint32_t bar_id = 1 + wg;
   int stage = 0;
-  uint32_t xph0 = 0, xph1 = 0, mph = 0;
+  uint32_t fph[2] = {0u, 0u}, mph = 0;
+
+  Cand next{a.ntiles, -1, -1};   // load thread: candidate after the tile in flight
+  if (load_thread) {
+    const int id0 = prepare(fetch_cand(a, blockIdx.x * kWG + wg), 0);
+    next = fetch_cand(a, id0 + nw);
+  }
+  named_sync(bar_id, kWGThreads);
 
   while (true) {
     const TileInfo cur = S.info[wg][stage];
     if (cur.id >= a.ntiles) break;
+    wait(&S.full[wg][stage], fph[stage]);
+    fph[stage] ^= 1;
     uint8_t* const xs = S.x[wg][stage];
-    {
-      const uint32_t ph = stage ? xph1 : xph0;
-      if (!mbar_wait_bounded(&S.xbar[wg][stage], ph, kQWaitNs) && leader)
-        report(a.status, KVARN_STATUS_TIMEOUT);
-    }
-    if (stage) xph1 ^= 1; else xph0 ^= 1;
-    if (leader) {
+    if (mma_thread) {
       tc_fence_after();
       const uint32_t xa = smem_u32(xs), ha = smem_u32(S.hs);
 #pragma unroll
@@ -350,8 +407,12 @@ __global__ void __launch_bounds__(kQThreads, 1)
         umma_f16(dYT, umma_desc_sw128(ha + off), umma_desc_sw128(xa + off), kIdesc, kk > 0);
       }
       umma_commit(&S.mbar[wg]);
+    } else if (load_thread) {
       // the next tile of this pipeline, loading while this one is processed
-      prepare(cur.id + nw, stage ^ 1);
+      // (its stage's last tile finished with it one tile ago); then the
+      // metadata of the candidate after it, used one tile from now
+      const int id1 = prepare(next, stage ^ 1);
+      next = fetch_cand(a, id1 < a.ntiles ? id1 + nw : a.ntiles);
     }
     const int part = cur.part;
 
@@ -360,6 +421,7 @@ __global__ void __launch_bounds__(kQThreads, 1)
     // sum_{k >= 1} x_k^2 / 128 (Hs has orthogonal rows of norm^2 128, and
     // column sums 128, 0, 0, ...); in units of Y = Hs x: mean x_0, variance
     // sum_{k >= 1} x_k^2 ----
+    if (lower) {
     cb[row] = 1.f;
     cc[row] = 1.f;
     if (a.iters > 0) {
@@ -387,124 +449,174 @@ __global__ void __launch_bounds__(kQThreads, 1)
     } else {
       ra[row] = kInvSqrt128;
     }
+    }
     named_sync(bar_id, kWGThreads);
-    if (!mbar_wait_bounded(&S.mbar[wg], mph, kQWaitNs) && leader)
-      report(a.status, KVARN_STATUS_TIMEOUT);
+    wait(&S.mbar[wg], mph);
     mph ^= 1;
     tc_fence_after();
 
-    // ---- Sinkhorn-like normalization: column step (row = channel), then
-    // for the later iterations row step (row = token) and column step ----
+    // ---- Sinkhorn-like normalization: column step (Y^T: rows = channels),
+    // then for the later iterations row step (Y: rows = tokens) and column
+    // step.  Each thread holds two rows of each 16-lane half of its warp's
+    // lanes, 32 columns of each (16x256b fragments); cb is indexed by Y column
+    // (channel chan_of(n)), ra by token ----
     for (int it = 0; it < a.iters; ++it) {
       if (it > 0) {
-        float mean, var;
-        moments_tm(tY, cb, mean, var);
-        if (!keep_scale(mean, var)) ra[row] = rsqrtf(var);
+        float2 w[16];
+        frag_weights(cb, q, w);
+        float v[64], mean[2], var[2];
+        tmem_ld256(tY, v);
+        tmem_wait_ld();
+        frag_moments(v, w, mean, var);
+        if (q == 0) {
+#pragma unroll
+          for (int e = 0; e < 2; ++e)
+            if (!keep_scale(mean[e], var[e])) ra[frow(e)] = rsqrtf(var[e]);
+        }
         named_sync(bar_id, kWGThreads);
       }
-      float mean, var;
-      moments_tm(tYT, ra, mean, var);
-      if (!keep_scale(mean, var)) {
-        const float rs = rsqrtf(var);
-        cc[row] = var * rs;
-        cb[row] = rs;
+      float2 w[16];
+      frag_weights(ra, q, w);
+      float v[64], mean[2], var[2];
+      tmem_ld256(tYT, v);
+      tmem_wait_ld();
+      frag_moments(v, w, mean, var);
+      if (q == 0) {
+#pragma unroll
+        for (int e = 0; e < 2; ++e)
+          if (!keep_scale(mean[e], var[e])) {
+            const int n = frow(e);
+            const float rs = rsqrtf(var[e]);
+            cb[n] = rs;
+            cc[chan_of(n)] = var[e] * rs;
+          }
       }
+      if (it == a.iters - 1 && leader) bulk_wait_read();
       named_sync(bar_id, kWGThreads);
     }
 
-    // ---- RTN + pack into the staging copy of the record part (the smem of
-    // this tile's input, free now), written out by one bulk copy ----
-    uint8_t* const out = xs;
+    // ---- RTN + pack into the staging copy of the record part, written out
+    // by one bulk copy; the previous tile's copy has read it by now ----
+    if (a.iters == 0) {
+      if (leader) bulk_wait_read();
+      named_sync(bar_id, kWGThreads);
+    }
     const float2 mg = make_float2(kMagic, kMagic);
+    float2 w[16];
+    frag_weights(cb, q, w);
+    float v[64];
+    tmem_ld256(tY, v);
+    tmem_wait_ld();
     if (part == 0) {
-      // K: token-major, 64 bytes per token; nibble e of word w = channel 8w + e
-      float mn, mx;
-      minmax_tm(tY, cb, mn, mx);
-      const float range = mx - mn;
-      const float inv = range > 0.f ? __fdividef(15.f, range) : 0.f;
-      *reinterpret_cast<float2*>(out + kOffKSZ + 8 * row) =
-          make_float2(range * (kInvSqrt128 / 15.f), mn * kInvSqrt128);
-      reinterpret_cast<float*>(out + kOffKC)[row] = cc[row];
-      // u = (y c^-1 - min) (15 / range): y c^-1 - min in one rounding
-      const float2 nm = make_float2(-mn, -mn), iv = make_float2(inv, inv);
+      // K: token-major, 64 bytes per token; nibble e of word w = channel 8w + e.
+      // The fragment of a row is the channels 32q .. 32q + 31: its words 4q ..
+      // 4q + 3, nibble 2 (k & 3) + b of word 4q + (k >> 2) from column pair k.
+      if (lower) reinterpret_cast<float*>(out + kOffKC)[row] = cc[row];
+      {
+        float mn[2], mx[2];
 #pragma unroll
-      for (int c = 0; c < 2; ++c) {
-        float v[64];
-        row_chunk<false>(tY, c, nullptr, v);
-        uint32_t w[8];
-#pragma unroll
-        for (int wd = 0; wd < 8; ++wd) {
-          uint32_t acc = 0u - kMagicK;
-          const float4 c0 = *reinterpret_cast<const float4*>(cb + 64 * c + 8 * wd);
-          const float4 c1 = *reinterpret_cast<const float4*>(cb + 64 * c + 8 * wd + 4);
-          const float cw[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
-#pragma unroll
-          for (int e = 0; e < 8; e += 2) {
-            const int d = 8 * wd + e;
-            const float2 dd = __ffma2_rn(make_float2(v[d], v[d + 1]),
-                                         make_float2(cw[e], cw[e + 1]), nm);
-            const float2 f = __ffma2_rn(dd, iv, mg);
-            acc += __float_as_uint(f.x) << (4 * e);
-            acc += __float_as_uint(f.y) << (4 * e + 4);
-          }
-          w[wd] = acc;
+        for (int e = 0; e < 2; ++e) {
+          mn[e] = INFINITY;
+          mx[e] = -INFINITY;
         }
-        // rows of 64 bytes: start at a chunk that depends on the row so that
-        // eight consecutive threads hit different banks
-        uint4* dst = reinterpret_cast<uint4*>(out + kOffKCodes + 64 * row + 32 * c);
-        const int sw = row & 1;
-        dst[sw] = make_uint4(w[4 * sw], w[4 * sw + 1], w[4 * sw + 2], w[4 * sw + 3]);
-        dst[sw ^ 1] = make_uint4(w[4 * (sw ^ 1)], w[4 * (sw ^ 1) + 1], w[4 * (sw ^ 1) + 2],
-                                 w[4 * (sw ^ 1) + 3]);
+#pragma unroll
+        for (int k = 0; k < 16; ++k)
+#pragma unroll
+          for (int e = 0; e < 2; ++e) {
+            const float2 x = __fmul2_rn(pair(v, k, e), w[k]);
+            v[4 * k + 2 * e] = x.x;
+            v[4 * k + 2 * e + 1] = x.y;
+            mn[e] = min3f(mn[e], x.x, x.y);
+            mx[e] = max3f(mx[e], x.x, x.y);
+          }
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+          const float lo = quad_min(mn[e]), hi = quad_max(mx[e]);
+          const float range = hi - lo;
+          const float inv = range > 0.f ? __fdividef(15.f, range) : 0.f;
+          const int t = frow(e);
+          if (q == 0)
+            *reinterpret_cast<float2*>(out + kOffKSZ + 8 * t) =
+                make_float2(range * (kInvSqrt128 / 15.f), lo * kInvSqrt128);
+          // u = (x - min) (15 / range) + 1.5 * 2^23: the code in the low bits
+          const float2 nm = make_float2(-lo, -lo), iv = make_float2(inv, inv);
+          uint32_t acc[4];
+#pragma unroll
+          for (int j = 0; j < 4; ++j) acc[j] = 0u - kMagicK;
+#pragma unroll
+          for (int k = 0; k < 16; ++k) {
+            const float2 f = __ffma2_rn(__fadd2_rn(pair(v, k, e), nm), iv, mg);
+            acc[k >> 2] += __float_as_uint(f.x) << (8 * (k & 3));
+            acc[k >> 2] += __float_as_uint(f.y) << (8 * (k & 3) + 4);
+          }
+          *reinterpret_cast<uint4*>(out + kOffKCodes + 64 * t + 16 * q) =
+              make_uint4(acc[0], acc[1], acc[2], acc[3]);
+        }
       }
     } else {
-      // V: publish the per-token min and 3 / range, then thread d packs channel d
-      float mn, mx;
-      minmax_tm(tY, cb, mn, mx);
-      const float range = mx - mn;
-      const float inv = range > 0.f ? __fdividef(3.f, range) : 0.f;
-      S.vmin[wg][row] = mn;
-      S.vinv[wg][row] = inv;
-      *reinterpret_cast<float2*>(out + (kOffVSZ - kKPart) + 8 * row) =
-          make_float2(range * (kInvSqrt128 / 3.f), mn * kInvSqrt128);
-      reinterpret_cast<float*>(out + (kOffVC - kKPart))[row] = cc[row];
-      named_sync(bar_id, kWGThreads);
-      const float cd = cb[row];
-      const float2 cd2 = make_float2(cd, cd);
-      const float* vm = S.vmin[wg];
-      const float* vi = S.vinv[wg];
-      uint32_t acc[4][2];
+      // V: the per-token min and 3 / range from Y, then each thread packs
+      // whole words of its channels from Y^T: the fragment columns (tokens)
+      // 8k + 2q + b are crumb (k & 7) + 8b of word v_word(channel, q, k >> 3)
+      if (lower) reinterpret_cast<float*>(out + (kOffVC - kKPart))[row] = cc[row];
+      {
+        float mn[2], mx[2];
 #pragma unroll
-      for (int j = 0; j < 4; ++j) acc[j][0] = acc[j][1] = 0u - kMagicV;
+        for (int e = 0; e < 2; ++e) {
+          mn[e] = INFINITY;
+          mx[e] = -INFINITY;
+        }
 #pragma unroll
-      for (int c = 0; c < 2; ++c) {
-        float v[64];
-        row_chunk<false>(tYT, c, nullptr, v);
+        for (int k = 0; k < 16; ++k)
 #pragma unroll
-        for (int i = 0; i < 64; i += 4) {
-          const int tt = 64 * c + i;
-          const float4 m4 = *reinterpret_cast<const float4*>(vm + tt);
-          const float4 i4 = *reinterpret_cast<const float4*>(vi + tt);
-          const float2 d0 = __ffma2_rn(make_float2(v[i], v[i + 1]), cd2,
-                                       make_float2(-m4.x, -m4.y));
-          const float2 d1 = __ffma2_rn(make_float2(v[i + 2], v[i + 3]), cd2,
-                                       make_float2(-m4.z, -m4.w));
-          const float2 f0 = __ffma2_rn(d0, make_float2(i4.x, i4.y), mg);
-          const float2 f1 = __ffma2_rn(d1, make_float2(i4.z, i4.w), mg);
-          const float fv[4] = {f0.x, f0.y, f1.x, f1.y};
+          for (int e = 0; e < 2; ++e) {
+            const float2 x = __fmul2_rn(pair(v, k, e), w[k]);
+            mn[e] = min3f(mn[e], x.x, x.y);
+            mx[e] = max3f(mx[e], x.x, x.y);
+          }
 #pragma unroll
-          for (int s2 = 0; s2 < 4; ++s2) {
-            const int tok = tt + s2;
-            const int k = tok >> 4, fh = (tok >> 3) & 1, j = (tok >> 1) & 3, sb = tok & 1;
-            const int crumb = 2 * (k & 3) + fh + 8 * sb;
-            acc[j][k >> 2] += __float_as_uint(fv[s2]) << (2 * crumb);
+        for (int e = 0; e < 2; ++e) {
+          const float lo = quad_min(mn[e]), hi = quad_max(mx[e]);
+          const float range = hi - lo;
+          const int t = frow(e);
+          if (q == 0) {
+            S.vmin[wg][t] = lo;
+            S.vinv[wg][t] = range > 0.f ? __fdividef(3.f, range) : 0.f;
+            *reinterpret_cast<float2*>(out + (kOffVSZ - kKPart) + 8 * t) =
+                make_float2(range * (kInvSqrt128 / 3.f), lo * kInvSqrt128);
           }
         }
       }
+      named_sync(bar_id, kWGThreads);
       uint32_t* vw = reinterpret_cast<uint32_t*>(out + (kOffVCodes - kKPart));
+      {
+        tmem_ld256(tYT, v);
+        tmem_wait_ld();
+        float2 cd2[2];
+        uint32_t acc[2][2];
 #pragma unroll
-      for (int j = 0; j < 4; ++j)
-        *reinterpret_cast<uint2*>(vw + v_word(row, j, 0)) = make_uint2(acc[j][0], acc[j][1]);
+        for (int e = 0; e < 2; ++e) {
+          const float cd = cb[frow(e)];
+          cd2[e] = make_float2(cd, cd);
+          acc[e][0] = acc[e][1] = 0u - kMagicV;
+        }
+#pragma unroll
+        for (int k = 0; k < 16; ++k) {
+          const float2 m2 = *reinterpret_cast<const float2*>(S.vmin[wg] + 8 * k + 2 * q);
+          const float2 i2 = *reinterpret_cast<const float2*>(S.vinv[wg] + 8 * k + 2 * q);
+          const float2 nm = make_float2(-m2.x, -m2.y);
+#pragma unroll
+          for (int e = 0; e < 2; ++e) {
+            const float2 d = __ffma2_rn(pair(v, k, e), cd2[e], nm);
+            const float2 f = __ffma2_rn(d, i2, mg);
+            acc[e][k >> 3] += __float_as_uint(f.x) << (2 * (k & 7));
+            acc[e][k >> 3] += __float_as_uint(f.y) << (2 * (k & 7) + 16);
+          }
+        }
+#pragma unroll
+        for (int e = 0; e < 2; ++e)
+          *reinterpret_cast<uint2*>(vw + v_word(chan_of(frow(e)), q, 0)) =
+              make_uint2(acc[e][0], acc[e][1]);
+      }
     }
     // the staging copy is complete and TMEM is free for the next tile
     fence_proxy_async_smem();
@@ -516,10 +628,10 @@ __global__ void __launch_bounds__(kQThreads, 1)
     }
     stage ^= 1;
   }
+  if (leader) bulk_wait_all();
 
   // ---- teardown: every MMA was waited for; the packed outputs are written
   // before the CTA's shared memory is released; free TMEM ----
-  if (leader) bulk_wait_all();
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
