@@ -213,6 +213,20 @@ class Job:
                                        status=self.status)
 
 
+def max_over_ranks(values, device):
+    """Element-wise maximum of `values` over all ranks (the slowest rank's
+    times); every rank gets the result."""
+    t = torch.tensor([float(x) for x in values], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return [float(x) for x in t.tolist()]
+
+
+def whole_job_gbs(world, step_bytes, ms_step):
+    """Weak scaling: every rank runs its own replica of the step, so the job
+    moves world x step_bytes in the slowest rank's step time."""
+    return world * step_bytes / (ms_step * 1e-3) / 1e9
+
+
 L2_BYTES = 126 * 1024 * 1024
 # ~0.5 ms of GPU spin at B300 clocks, ahead of each timed region
 SPIN_CYCLES = 1_000_000
@@ -290,9 +304,8 @@ def run_gpu(args, rank, world):
     ms = {name: ev[name][0].elapsed_time(ev[name][1]) / args.steps for name in names}
     ms_step = sum(ms.values())
     if world > 1:
-        t = torch.tensor([ms_step, ms["quantize"], ms["append"], ms["decode"]], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        ms_step, ms["quantize"], ms["append"], ms["decode"] = [float(x) for x in t.tolist()]
+        ms_step, ms["quantize"], ms["append"], ms["decode"] = max_over_ranks(
+            [ms_step, ms["quantize"], ms["append"], ms["decode"]], dev)
 
     # cold single launches (clean L2 flush before each), for reference
     cold = {name: [] for name in names}
@@ -444,7 +457,7 @@ def main():
     w = job.w
     peak, peak_kind = measured_peaks()
     step_bytes = job.bytes_quantize + job.bytes_append + job.bytes_decode
-    value = world * step_bytes / (ms_step * 1e-3) / 1e9
+    value = whole_job_gbs(world, step_bytes, ms_step)
     q_gbs = job.bytes_quantize / (ms["quantize"] * 1e-3) / 1e9
     d_gbs = job.bytes_decode / (ms["decode"] * 1e-3) / 1e9
     a_gbs = job.bytes_append / (ms["append"] * 1e-3) / 1e9
