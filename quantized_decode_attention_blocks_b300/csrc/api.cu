@@ -217,6 +217,7 @@ int kvarn_decode_attention(const kvarn_config_t* cfg, const void* q, const void*
                    : nullptr;
   a.pages_per_split = p.pages_per_split;
   a.nsplit = p.nsplit;
+  a.cluster = 0;   // the kernel's launcher decides
   a.status = status;
   cudaError_t e = decode_mma_supported(a.g) ? launch_decode_mma(a, (cudaStream_t)stream)
                                             : launch_decode_simple(a, (cudaStream_t)stream);

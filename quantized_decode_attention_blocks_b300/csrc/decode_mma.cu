@@ -41,6 +41,9 @@ namespace {
 using namespace ptx;
 
 constexpr int kWarps = 4;
+// Largest split count merged inside a thread-block cluster; more splits merge
+// through the workspace (partial states and arrival tickets).
+constexpr int kMaxClusterSplits = 4;
 constexpr int kThreads = 32 * kWarps;
 constexpr uint64_t kWaitLimitNs = 2000000000ull;
 constexpr float kLog2e = 1.4426950408889634f;
@@ -149,7 +152,8 @@ __global__ void __launch_bounds__(kThreads, 3) decode_mma_kernel(DecodeArgs a) {
   const int nfull = len / kT, rem = len % kT;
   const int pps = a.pages_per_split;
   const int nsb = nfull > 0 ? (nfull + pps - 1) / pps : 1;
-  if (split >= nsb) return;
+  // in a cluster every CTA takes part in the merge, with or without pages
+  if (split >= nsb && !a.cluster) return;
   const int u0 = split * pps, u1 = min(nfull, u0 + pps);
   const bool has_tail = split == nsb - 1 && rem > 0;
 
@@ -569,8 +573,8 @@ __global__ void __launch_bounds__(kThreads, 3) decode_mma_kernel(DecodeArgs a) {
   }
   __syncwarp();
 
-  // ---- fp16 tail (plain space): warp w takes tail tokens w, w + 4, ... and
-  // folds them into its own state; lane holds channels 4 lane .. 4 lane + 3 ----
+  // ---- fp16 tail (plain space): warp w takes tail tokens 3 - w, 7 - w, ...
+  // and folds them into its own state; lane holds channels 4 lane .. + 3 ----
   if (has_tail && !timed_out) {
     float qr[G][4], mt[G], lt[G], ot[G][4];
 #pragma unroll
@@ -589,7 +593,9 @@ __global__ void __launch_bounds__(kThreads, 3) decode_mma_kernel(DecodeArgs a) {
       ot[h][3] = o4.w;
     }
     constexpr int kC = 8;   // tail tokens per batch of loads
-    for (int t0 = warp; t0 < rem; t0 += kWarps * kC) {
+    // warp w takes tail tokens from kWarps - 1 - w: the higher warps of a split
+    // hold no more pages than the lower ones
+    for (int t0 = kWarps - 1 - warp; t0 < rem; t0 += kWarps * kC) {
       uint2 kk[kC], vv[kC];
 #pragma unroll
       for (int i = 0; i < kC; ++i) {
@@ -637,8 +643,93 @@ __global__ void __launch_bounds__(kThreads, 3) decode_mma_kernel(DecodeArgs a) {
   __syncthreads();
 
   // ---- merge the warps' states; the result goes straight to the output
-  // (one split) or to this split's partial state ----
+  // (one split), to shared memory for the cluster merge, or to this split's
+  // partial state ----
   __half* ob = a.out + ((int64_t)b * a.hq + (int64_t)kvh * g) * kD;
+  if (a.cluster) {
+    // CTA state in registers (thread: entries tid, tid + 128, ...), then in
+    // warp 0's buffer as [G]{M, L}, o[G][kD]
+    constexpr int kPer = G * kD / kThreads;
+    float cM[kPer], cL[kPer], cO[kPer];
+#pragma unroll
+    for (int k = 0; k < kPer; ++k) {
+      const int i = tid + kThreads * k, h = i >> 7, ch = i & 127;
+      float M = -INFINITY, o = 0.f, L = 0.f;
+      if (h < g) {
+#pragma unroll
+        for (int w = 0; w < kWarps; ++w)
+          M = fmaxf(M, reinterpret_cast<const float*>(S.rec[w])[2 * h]);
+        if (M != -INFINITY) {
+#pragma unroll
+          for (int w = 0; w < kWarps; ++w) {
+            const float* sw = reinterpret_cast<const float*>(S.rec[w]);
+            const float wt = ex2(sw[2 * h] - M);
+            o = fmaf(wt, sw[2 * G + h * kOPitch + ch], o);
+            L = fmaf(wt, sw[2 * h + 1], L);
+          }
+        }
+      }
+      cM[k] = M;
+      cL[k] = L;
+      cO[k] = o;
+    }
+    __syncthreads();
+    float* cs = reinterpret_cast<float*>(S.rec[0]);
+#pragma unroll
+    for (int k = 0; k < kPer; ++k) {
+      const int i = tid + kThreads * k, h = i >> 7, ch = i & 127;
+      if (ch == 0) {
+        cs[2 * h] = cM[k];
+        cs[2 * h + 1] = cL[k];
+      }
+      cs[2 * G + i] = cO[k];
+    }
+    cluster_sync();
+    if (cluster_ctarank() == 0) {
+      // rank 0 merges the cluster's states (distributed shared memory); a
+      // thread's remote loads are all issued before the first is used
+      const uint32_t nc = (uint32_t)a.nsplit;
+#pragma unroll
+      for (int k0 = 0; k0 < kPer; k0 += 4) {
+        float Mr[4][kMaxClusterSplits], Lr[4][kMaxClusterSplits], Or[4][kMaxClusterSplits];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          const int i = tid + kThreads * (k0 + k), h = i >> 7;
+#pragma unroll
+          for (uint32_t c = 0; c < (uint32_t)kMaxClusterSplits; ++c) {
+            Mr[k][c] = -INFINITY;
+            Lr[k][c] = Or[k][c] = 0.f;
+            if (h < g && c < nc) {
+              Mr[k][c] = ld_dsmem_f32(cs + 2 * h, c);
+              Lr[k][c] = ld_dsmem_f32(cs + 2 * h + 1, c);
+              Or[k][c] = ld_dsmem_f32(cs + 2 * G + i, c);
+            }
+          }
+        }
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          const int i = tid + kThreads * (k0 + k), h = i >> 7;
+          if (h >= g) continue;
+          float M = -INFINITY;
+#pragma unroll
+          for (int c = 0; c < kMaxClusterSplits; ++c) M = fmaxf(M, Mr[k][c]);
+          float o = 0.f, L = 0.f;
+          if (M != -INFINITY) {
+#pragma unroll
+            for (int c = 0; c < kMaxClusterSplits; ++c) {
+              const float wt = ex2(Mr[k][c] - M);   // 0 for an empty state
+              o = fmaf(wt, Or[k][c], o);
+              L = fmaf(wt, Lr[k][c], L);
+            }
+          }
+          ob[i] = __float2half_rn(L > 0.f ? o / L : 0.f);
+        }
+      }
+    }
+    // no CTA leaves while rank 0 may still read its shared memory
+    cluster_sync();
+    return;
+  }
   for (int i = tid; i < g * kD; i += kThreads) {
     const int h = i >> 7, ch = i & 127;
     float M = -INFINITY;
@@ -721,7 +812,7 @@ __global__ void __launch_bounds__(kThreads, 3) decode_mma_kernel(DecodeArgs a) {
 }
 
 template <int NT>
-cudaError_t launch_nt(const DecodeArgs& a, cudaStream_t s) {
+cudaError_t launch_nt(const DecodeArgs& args, cudaStream_t s) {
   static bool attr_set = false;
   const int smem = (int)sizeof(MmaSmem<NT>);
   if (!attr_set) {
@@ -730,9 +821,23 @@ cudaError_t launch_nt(const DecodeArgs& a, cudaStream_t s) {
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
-  dim3 grid(a.nsplit, a.hkv, a.batch);
-  decode_mma_kernel<NT><<<grid, kThreads, smem, s>>>(a);
-  return cudaGetLastError();
+  DecodeArgs a = args;
+  a.cluster = a.nsplit >= 2 && a.nsplit <= kMaxClusterSplits;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(a.nsplit, a.hkv, a.batch);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  if (a.cluster) {
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = a.nsplit;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+  }
+  return cudaLaunchKernelEx(&cfg, decode_mma_kernel<NT>, a);
 }
 
 }  // namespace

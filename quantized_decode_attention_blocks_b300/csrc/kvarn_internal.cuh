@@ -90,6 +90,7 @@ struct DecodeArgs {
   int* ws_count;      // [batch][hkv] arrival tickets, zero between calls
   int pages_per_split;
   int nsplit;
+  int cluster;        // 1: the nsplit CTAs of a (sequence, KV head) form a cluster
   int32_t* status;
 };
 
