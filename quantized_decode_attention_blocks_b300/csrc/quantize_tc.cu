@@ -79,6 +79,8 @@ struct __align__(1024) QSmem {
   uint8_t x[kWG][2][kTileBytes];         // input tiles, 2 stages per pipeline
   __align__(128) uint8_t out[kWG][kKPart];   // packed record part, staged for the bulk store
   __align__(16) float ra[kWG][kT];       // 1 / r_t, in units of Y
+  float r1part[kWG][2][kT];              // first row step of the next tile: half sums
+  float r1x0[kWG][kT];                   //   and channel 0
   __align__(16) float cb[kWG][kD];       // 1 / c, indexed by Y column (channel chan_of(n))
   __align__(16) float vmin[kWG][kT];     // V: per-token min of x
   __align__(16) float vinv[kWG][kT];     // V: per-token 3 / (max - min)
@@ -378,7 +380,36 @@ __global__ void __launch_bounds__(kQThreads, 1)
   uint8_t* const out = S.out[wg];
   const uint32_t bar_id = 1 + wg;
   int stage = 0;
-  uint32_t fph[2] = {0u, 0u}, mph = 0;
+  uint32_t fph0 = 0u, fph1 = 0u, mph = 0;   // phases of full[wg][0], full[wg][1], mbar
+  bool have_r1 = false;                      // first row step sums of this tile ready
+
+  // First row step, partial: thread wt sums the squares of channels 64 h ..
+  // 64 h + 63 (h = wt >> 7, one 64-channel box) of row `row` of the tile in
+  // shared memory; channel 0, the row mean, is kept apart.
+  auto r1_partial = [&](const uint8_t* x) {
+    const int h = wt >> 7;
+    float2 s2[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
+                    make_float2(0.f, 0.f)};
+    float x0 = 0.f;
+    const uint8_t* xr = x + h * kBoxBytes + row * 128;
+#pragma unroll
+    for (int c = 0; c < 8; ++c) {   // 16-byte chunk c of the box: channels 64 h + 8c ..
+      uint4 u = *reinterpret_cast<const uint4*>(xr + ((c ^ (row & 7)) << 4));
+      if (c == 0 && h == 0) {
+        x0 = __half2float(__ushort_as_half((unsigned short)(u.x & 0xFFFFu)));
+        u.x &= 0xFFFF0000u;
+      }
+      const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&w[e]));
+        s2[e] = __ffma2_rn(f, f, s2[e]);
+      }
+    }
+    S.r1part[wg][h][row] = ((s2[0].x + s2[0].y) + (s2[1].x + s2[1].y)) +
+                           ((s2[2].x + s2[2].y) + (s2[3].x + s2[3].y));
+    if (h == 0) S.r1x0[wg][row] = x0;
+  };
 
   Cand next{a.ntiles, -1, -1};   // load thread: candidate after the tile in flight
   if (load_thread) {
@@ -390,8 +421,13 @@ __global__ void __launch_bounds__(kQThreads, 1)
   while (true) {
     const TileInfo cur = S.info[wg][stage];
     if (cur.id >= a.ntiles) break;
-    wait(&S.full[wg][stage], fph[stage]);
-    fph[stage] ^= 1;
+    if (stage == 0) {
+      wait(&S.full[wg][0], fph0);
+      fph0 ^= 1u;
+    } else {
+      wait(&S.full[wg][1], fph1);
+      fph1 ^= 1u;
+    }
     uint8_t* const xs = S.x[wg][stage];
     if (mma_thread) {
       tc_fence_after();
@@ -416,39 +452,25 @@ __global__ void __launch_bounds__(kQThreads, 1)
     }
     const int part = cur.part;
 
-    // ---- first row step from X itself, while the MMAs run: the rotated row
-    // y = Hs x / sqrt(128) has mean x_0 / sqrt(128) and variance
-    // sum_{k >= 1} x_k^2 / 128 (Hs has orthogonal rows of norm^2 128, and
-    // column sums 128, 0, 0, ...); in units of Y = Hs x: mean x_0, variance
-    // sum_{k >= 1} x_k^2 ----
-    if (lower) {
-    cb[row] = 1.f;
-    cc[row] = 1.f;
-    if (a.iters > 0) {
-      float2 s2[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
-                      make_float2(0.f, 0.f)};
-      float x0 = 0.f;
-#pragma unroll
-      for (int c = 0; c < 16; ++c) {   // 16-byte chunk c: channels 8c .. 8c + 7
-        const uint8_t* xr = xs + (c >> 3) * kBoxBytes + row * 128;
-        uint4 u = *reinterpret_cast<const uint4*>(xr + (((c & 7) ^ (row & 7)) << 4));
-        if (c == 0) {
-          x0 = __half2float(__ushort_as_half((unsigned short)(u.x & 0xFFFFu)));
-          u.x &= 0xFFFF0000u;   // channel 0 is the mean, not part of the variance
-        }
-        const uint32_t w[4] = {u.x, u.y, u.z, u.w};
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&w[e]));
-          s2[e] = __ffma2_rn(f, f, s2[e]);
-        }
-      }
-      const float var = ((s2[0].x + s2[0].y) + (s2[1].x + s2[1].y)) +
-                        ((s2[2].x + s2[2].y) + (s2[3].x + s2[3].y));
-      ra[row] = keep_scale(x0, var) ? kInvSqrt128 : rsqrtf(var);
-    } else {
-      ra[row] = kInvSqrt128;
+    // ---- first row step from X itself: the rotated row y = Hs x / sqrt(128)
+    // has mean x_0 / sqrt(128) and variance sum_{k >= 1} x_k^2 / 128 (Hs has
+    // orthogonal rows of norm^2 128, and column sums 128, 0, 0, ...); in units
+    // of Y = Hs x: mean x_0, variance sum_{k >= 1} x_k^2.  Its sums were taken
+    // at the end of the previous tile (the first tile of a pipeline takes
+    // them now) ----
+    if (!have_r1 && a.iters > 0) {
+      r1_partial(xs);
+      named_sync(bar_id, kWGThreads);
     }
+    if (lower) {
+      cb[row] = 1.f;
+      cc[row] = 1.f;
+      if (a.iters > 0) {
+        const float var = S.r1part[wg][0][row] + S.r1part[wg][1][row];
+        ra[row] = keep_scale(S.r1x0[wg][row], var) ? kInvSqrt128 : rsqrtf(var);
+      } else {
+        ra[row] = kInvSqrt128;
+      }
     }
     named_sync(bar_id, kWGThreads);
     wait(&S.mbar[wg], mph);
@@ -616,6 +638,20 @@ __global__ void __launch_bounds__(kQThreads, 1)
         for (int e = 0; e < 2; ++e)
           *reinterpret_cast<uint2*>(vw + v_word(chan_of(frow(e)), q, 0)) =
               make_uint2(acc[e][0], acc[e][1]);
+      }
+    }
+    // the first row step sums of the next tile, whose input is already in the
+    // other stage (no MMA reads it yet)
+    have_r1 = false;
+    if (a.iters > 0) {
+      const int nid = S.info[wg][stage ^ 1].id;
+      if (nid < a.ntiles) {
+        if (stage == 0)
+          wait(&S.full[wg][1], fph1);
+        else
+          wait(&S.full[wg][0], fph0);
+        r1_partial(S.x[wg][stage ^ 1]);
+        have_r1 = true;
       }
     }
     // the staging copy is complete and TMEM is free for the next tile
