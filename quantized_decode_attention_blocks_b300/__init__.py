@@ -5,10 +5,12 @@ include/kvarn.h); this package is its thin Python binding.
 """
 from .kvarn import (Config, KvarnError, alloc_decode_workspace, alloc_pool, alloc_tails,
                     config_from_string, config_validate, decode_workspace_bytes,
-                    kvarn_append_token, kvarn_decode_attention, kvarn_dequantize_pages,
+                    kvarn_append_token, kvarn_decode_attention, kvarn_decode_attention_noalloc,
+                    kvarn_dequantize_pages,
                     kvarn_quantize_blocks, lib, page_bytes, status_string, version)
 
 __all__ = ["Config", "KvarnError", "alloc_decode_workspace", "alloc_pool", "alloc_tails",
            "config_from_string", "config_validate", "decode_workspace_bytes",
-           "kvarn_append_token", "kvarn_decode_attention", "kvarn_dequantize_pages",
+           "kvarn_append_token", "kvarn_decode_attention", "kvarn_decode_attention_noalloc",
+           "kvarn_dequantize_pages",
            "kvarn_quantize_blocks", "lib", "page_bytes", "status_string", "version"]
