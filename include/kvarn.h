@@ -161,7 +161,11 @@ size_t kvarn_decode_workspace_bytes(const kvarn_config_t *cfg, int batch, int ma
  *              buffer serves any number of calls on one stream (calls that
  *              share a workspace must not overlap on the GPU).
  * The work is split across CTAs along each sequence's pages (split-K) and the
- * partial softmax states are merged with a log-sum-exp in the same launch. */
+ * partial softmax states are merged with a log-sum-exp in the same launch:
+ * inside a thread-block cluster (distributed shared memory) when a sequence
+ * has 2 to 4 splits, through the workspace otherwise.  The launch uses
+ * thread-block clusters, so the GPU must be able to co-schedule up to 4 CTAs
+ * of the kernel; a launch failure returns KVARN_ERR_LAUNCH. */
 int kvarn_decode_attention(const kvarn_config_t *cfg, const void *q, const void *pool,
                            int64_t num_pages, const int32_t *block_table, int max_blocks,
                            const int32_t *seq_lens, int batch, int max_seq,
