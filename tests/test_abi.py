@@ -79,6 +79,25 @@ def test_page_bytes_and_workspace_sizes():
     assert big % 256 == 0
 
 
+@pytest.mark.parametrize("g", [1, 2, 4, 6, 8])
+def test_noalloc_scratch_covers_every_group_up_to_eight(g):
+    # the split plan keeps the grid to one wave, so the partial states of every
+    # (batch, length) with at most 8 query heads per KV head fit in the
+    # built-in scratch of the no-alloc decode (a host-only computation)
+    for hkv in (1, 2, 8, 32):
+        c = kv.config_from_string("k4v2_g128", g * hkv, hkv)
+        for batch in (1, 3, 64, 1000, 65535):
+            for max_seq in (128, 4097, 131072, 1 << 22):
+                need = kv.decode_workspace_bytes(c, batch, max_seq)
+                assert need <= K.NOALLOC_SCRATCH_BYTES, (g, hkv, batch, max_seq, need)
+
+
+def test_no_workspace_when_the_batch_fills_the_gpu():
+    # enough (sequence, KV head) pairs for one CTA each: no split, no partials
+    c = kv.config_from_string("k4v2_g128", 32, 8)
+    assert kv.decode_workspace_bytes(c, 4096, 32768) == 0
+
+
 def test_status_strings():
     for code in (0, -1, -2, -3, -4, 1, 2, 4, 3, -99):
         s = kv.status_string(code)
