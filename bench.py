@@ -198,6 +198,15 @@ class Job:
         self.bytes_decode = int(self.decode_pages * REC + self.decode_tail * FP16_TOKEN_HEAD
                                 + 2 * w.batch * w.hq * D * 2)
         self.kv_tokens = int(lens1.sum())
+        # the FP16 paged cache of the same tokens (the baseline the quantized
+        # cache is compared with): every prefill token as fp16, no tail
+        self.pool16 = kv.alloc_fp16_pool(w.hkv, self.num_pages, dev)
+        kv.kvarn_fp16_write_blocks(self.k, self.v, self.lens, self.max_seq, self.table,
+                                   self.pool16, self.status)
+        self.ws16 = kv.alloc_fp16_decode_workspace(w.hq, w.hkv, w.batch, self.max_seq, dev)
+        self.out16 = torch.empty_like(self.out)
+        self.bytes_decode_fp16 = int(lens.sum() * w.hkv * FP16_TOKEN_HEAD
+                                     + 2 * w.batch * w.hq * D * 2)
 
     def quantize(self):
         self.kv.kvarn_quantize_blocks(self.cfg, self.k, self.v, self.lens, self.max_seq,
@@ -206,6 +215,11 @@ class Job:
     def append(self):
         self.kv.kvarn_append_token(self.cfg, self.kn, self.vn, self.lens, self.table, self.pool,
                                    self.tk, self.tv, self.status)
+
+    def decode_fp16(self):
+        self.kv.kvarn_fp16_decode_attention(self.q, self.w.hkv, self.pool16, self.table,
+                                            self.lens, self.max_seq, self.out16, self.ws16,
+                                            status=self.status)
 
     def decode(self):
         self.kv.kvarn_decode_attention(self.cfg, self.q, self.pool, self.table, self.lens1,
@@ -320,6 +334,26 @@ def run_gpu(args, rank, world):
             cold[name].append((e0, e1))
     torch.cuda.synchronize()
     ms_cold = {k: statistics.median(a.elapsed_time(b) for a, b in v) for k, v in cold.items()}
+
+    # the FP16 baseline's decode over the same tokens, timed the same way
+    # (outside the step: a comparison, not part of the path)
+    g16 = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g16):
+        for i in range(args.steps):
+            jobs[i % nrep].decode_fp16()
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    torch.cuda._sleep(SPIN_CYCLES)
+    e0.record(stream)
+    g16.replay()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    ms["decode_fp16"] = e0.elapsed_time(e1) / args.steps
+    for j in jobs:
+        if int(j.status.item()) != 0:
+            raise RuntimeError(f"device status {j.status.item()}: "
+                               f"{j.kv.status_string(int(j.status.item()))}")
 
     # end to end through the public API: host buffers, copies inside the region
     e2e = measure_e2e(job, args, stream)
@@ -461,6 +495,7 @@ def main():
     q_gbs = job.bytes_quantize / (ms["quantize"] * 1e-3) / 1e9
     d_gbs = job.bytes_decode / (ms["decode"] * 1e-3) / 1e9
     a_gbs = job.bytes_append / (ms["append"] * 1e-3) / 1e9
+    f16_gbs = job.bytes_decode_fp16 / (ms["decode_fp16"] * 1e-3) / 1e9
     dom = "quantize" if ms["quantize"] >= ms["decode"] else "decode"
     dom_gbs = q_gbs if dom == "quantize" else d_gbs
     dom_bytes = job.bytes_quantize if dom == "quantize" else job.bytes_decode
@@ -489,7 +524,12 @@ def main():
                        "bytes": job.bytes_decode,
                        "tokens_per_s": w.batch / (ms["decode"] * 1e-3),
                        "kv_tokens_scanned_per_s": job.kv_tokens / (ms["decode"] * 1e-3)},
+            "decode_fp16": {"us": ms["decode_fp16"] * 1e3, "gbs": f16_gbs,
+                            "frac_of_hbm": f16_gbs / peak, "bytes": job.bytes_decode_fp16,
+                            "note": "baseline: the same decode over an FP16 paged cache of "
+                                    "the prefill tokens (not part of the step)"},
         },
+        "decode_speedup_vs_fp16_cache": ms["decode_fp16"] / ms["decode"],
         "roofline": {"bound": "hbm", "kernel": dom, "achieved": dom_gbs, "peak": peak,
                      "peak_kind": f"{peak_kind} hbm_gbs (burst copy)", "unit": "GB/s",
                      "frac": dom_gbs / peak,

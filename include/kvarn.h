@@ -210,6 +210,47 @@ int kvarn_decode_attention_noalloc(const kvarn_config_t *cfg, const void *q, con
 int kvarn_dequantize_pages(const void *records, int64_t n, float *yk, float *yv,
                            kvarn_stream_t stream);
 
+/* ---- The FP16 paged cache the quantized one is measured against ----
+ * The KVarN page (blog.edumints.com) states its capacity and throughput gains
+ * relative to an FP16 KV cache; these calls are that baseline on the same
+ * harness: the same block table and lengths, every token kept as fp16.
+ * Page: one per (page, KV head), KVARN_FP16_PAGE_BYTES bytes, 16-byte aligned:
+ *   [0, 32768)      K, [128 tokens][128 channels] fp16
+ *   [32768, 65536)  V, same
+ * Pool = [num_pages][num_kv_heads][KVARN_FP16_PAGE_BYTES].  Block j of a
+ * sequence holds its tokens 128j .. 128j + 127; the last block is filled up
+ * to the length and the rest of it is never read. */
+#define KVARN_FP16_PAGE_BYTES 65536
+
+/* Copies tokens [0, seq_lens[b]) of every sequence into its fp16 pages.
+ *   k, v       fp16, element (b, t, h, c) at b*stride_b + t*stride_t +
+ *              h*stride_h + c (strides in elements, multiples of 8)
+ *   seq_lens   int32 [batch] (device), 0 <= len <= max_seq
+ *   block_table int32 [batch][max_blocks] (device); every block holding a
+ *              token must be in the table (max_blocks >= ceil(max_seq/128))
+ * Bad page ids and lengths are reported in *status and skipped. */
+int kvarn_fp16_write_blocks(const void *k, const void *v, int64_t stride_b, int64_t stride_t,
+                            int64_t stride_h, int batch, int num_kv_heads,
+                            const int32_t *seq_lens, int max_seq, const int32_t *block_table,
+                            int max_blocks, void *pool, int64_t num_pages, int32_t *status,
+                            kvarn_stream_t stream);
+
+/* Bytes of workspace kvarn_fp16_decode_attention needs (0: none). */
+size_t kvarn_fp16_decode_workspace_bytes(int num_q_heads, int num_kv_heads, int batch,
+                                         int max_seq);
+
+/* Decode attention over the fp16 pages, one query token per sequence:
+ *   out[b][h] = sum_t softmax_t(scale * q[b][h] . k_t) v_t, t < seq_lens[b]
+ * Query head h reads KV head h / (Hq/Hkv); Hq/Hkv at most 8.  Arguments as
+ * for kvarn_decode_attention (q, out fp16 [batch][Hq][128]; the workspace
+ * zero-filled before its first use and left so).  Split-K over the pages with
+ * a log-sum-exp merge in the same launch. */
+int kvarn_fp16_decode_attention(const void *q, int num_q_heads, int num_kv_heads,
+                                const void *pool, int64_t num_pages, const int32_t *block_table,
+                                int max_blocks, const int32_t *seq_lens, int batch, int max_seq,
+                                float softmax_scale, void *out, void *workspace,
+                                size_t workspace_bytes, int32_t *status, kvarn_stream_t stream);
+
 /* Static text for a return code or a status bit set. */
 const char *kvarn_status_string(int code);
 

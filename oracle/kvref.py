@@ -228,3 +228,37 @@ def decode_attention(q, pool, block_table, seq_lens, tail_k, tail_v, hq: int, hk
     if rc != 0:
         raise ValueError("oracle: page id outside the pool")
     return out
+
+
+def attention_fp16(q, k, v, seq_lens, hq: int, hkv: int,
+                   scale: float = 1.0 / np.sqrt(128.0)) -> np.ndarray:
+    """Decode attention over an uncompressed fp16 cache, float64 output
+    [B][Hq][128]: out[b][h] = sum_t softmax_t(scale q[b][h] . k[b][t][h/g]) v[b][t][h/g]
+    over t < seq_lens[b], the textbook definition ("KV Cache (Anahtar-Deger
+    Onbellegi)", yapayzekasozluk.tr, "KV Cache Nasil Calisir?") written out in
+    numpy float64 (max-subtracted softmax).  q: fp16 [B][Hq][128]; k, v: fp16
+    [B][S][Hkv][128]; fp16 values are taken exactly."""
+    def f64(x):
+        if hasattr(x, "numpy"):
+            x = x.cpu().numpy()
+        x = np.asarray(x)
+        if x.dtype == np.uint16:
+            x = x.view(np.float16)
+        return x.astype(np.float64)
+
+    qd, kd, vd = f64(q), f64(k), f64(v)
+    lens = np.asarray(seq_lens.cpu().numpy() if hasattr(seq_lens, "numpy") else seq_lens)
+    B = qd.shape[0]
+    g = hq // hkv
+    out = np.zeros((B, hq, NCH))
+    for b in range(B):
+        n = int(lens[b])
+        if n <= 0:
+            continue
+        for h in range(hq):
+            kh = kd[b, :n, h // g, :]
+            vh = vd[b, :n, h // g, :]
+            s = (kh @ qd[b, h]) * scale
+            p = np.exp(s - s.max())
+            out[b, h] = (p @ vh) / p.sum()
+    return out

@@ -3,13 +3,17 @@
 The compute lives in libkvarn.so (CUDA kernels behind the C ABI of
 include/kvarn.h); this package is its thin Python binding.
 """
-from .kvarn import (Config, KvarnError, alloc_decode_workspace, alloc_pool, alloc_tails,
+from .kvarn import (Config, KvarnError, alloc_decode_workspace, alloc_fp16_decode_workspace,
+                    alloc_fp16_pool, alloc_pool, alloc_tails, fp16_decode_workspace_bytes,
+                    kvarn_fp16_decode_attention, kvarn_fp16_write_blocks,
                     config_from_string, config_validate, decode_workspace_bytes,
                     kvarn_append_token, kvarn_decode_attention, kvarn_decode_attention_noalloc,
                     kvarn_dequantize_pages,
                     kvarn_quantize_blocks, lib, page_bytes, status_string, version)
 
-__all__ = ["Config", "KvarnError", "alloc_decode_workspace", "alloc_pool", "alloc_tails",
+__all__ = ["Config", "KvarnError", "alloc_decode_workspace", "alloc_fp16_decode_workspace",
+           "alloc_fp16_pool", "alloc_pool", "alloc_tails", "fp16_decode_workspace_bytes",
+           "kvarn_fp16_decode_attention", "kvarn_fp16_write_blocks",
            "config_from_string", "config_validate", "decode_workspace_bytes",
            "kvarn_append_token", "kvarn_decode_attention", "kvarn_decode_attention_noalloc",
            "kvarn_dequantize_pages",

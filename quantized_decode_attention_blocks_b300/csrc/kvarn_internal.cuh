@@ -2,6 +2,7 @@
 // the CUDA translation units of libkvarn.  Not part of the public ABI.
 #pragma once
 
+#include <cuda.h>
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
@@ -110,6 +111,47 @@ cudaError_t launch_append_token(const AppendArgs& a, cudaStream_t s);
 cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t s);
 cudaError_t launch_dequantize(const uint8_t* rec, int64_t n, float* yk, float* yv,
                               cudaStream_t s);
+
+// A 4-D tensor map over fp16 data with 128-byte swizzle (dims and box
+// innermost first, strides of dimensions 1..3 in bytes); false if the driver
+// rejects it.
+bool encode_fp16_map_4d(CUtensorMap* map, const void* base, const uint64_t dims[4],
+                        const uint64_t strides[3], const uint32_t box[4]);
+
+// The FP16 paged cache the quantized one is compared with.
+constexpr int kF16PageBytes = 2 * kT * kD * 2;   // K then V, [128 tokens][128] fp16 each
+
+struct F16WriteArgs {
+  const __half* k;
+  const __half* v;
+  int64_t sb, st, sh;
+  int batch, hkv, max_seq;
+  const int32_t* seq_lens;
+  const int32_t* block_table;
+  int max_blocks;
+  uint8_t* pool;
+  int64_t num_pages;
+  int32_t* status;
+};
+
+struct F16DecodeArgs {
+  const __half* q;
+  int64_t num_pages;
+  const int32_t* block_table;
+  int max_blocks;
+  const int32_t* seq_lens;
+  int batch, max_seq, hq, hkv, g;
+  float scale;
+  __half* out;
+  float* ws_part;     // [batch][hq][nsplit][kPartStride]
+  int* ws_count;      // [batch][hkv] arrival tickets, zero between calls
+  int pages_per_split;
+  int nsplit;
+  int32_t* status;
+};
+DecodePlan fp16_decode_plan(int batch, int hq, int hkv, int max_seq);
+cudaError_t launch_fp16_write(const F16WriteArgs& a, cudaStream_t s);
+cudaError_t launch_fp16_decode(const F16DecodeArgs& a, const void* pool, cudaStream_t s);
 
 __device__ __forceinline__ void report(int32_t* status, int bits) {
   if (status) atomicOr(status, bits);

@@ -782,6 +782,23 @@ cudaError_t launch_tiles(const CUtensorMap& mk, const CUtensorMap& mv, const QTi
 
 }  // namespace
 
+bool encode_fp16_map_4d(CUtensorMap* map, const void* base, const uint64_t dims[4],
+                        const uint64_t strides[3], const uint32_t box[4]) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t d[4], st[3];
+  cuuint32_t bx[4], estr[4] = {1, 1, 1, 1};
+  for (int i = 0; i < 4; ++i) {
+    d[i] = (cuuint64_t)dims[i];
+    bx[i] = (cuuint32_t)box[i];
+  }
+  for (int i = 0; i < 3; ++i) st[i] = (cuuint64_t)strides[i];
+  return fn(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 4, const_cast<void*>(base), d, st, bx, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) ==
+         CUDA_SUCCESS;
+}
+
 cudaError_t launch_quantize_blocks(const QuantizeArgs& a, cudaStream_t s) {
   QTileArgs qa{};
   qa.mode = 0;

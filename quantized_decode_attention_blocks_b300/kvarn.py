@@ -19,6 +19,7 @@ LIB_PATH = os.path.join(HERE, "libkvarn.so")
 HEAD_DIM = 128
 BLOCK_TOKENS = 128
 PAGE_BYTES = 15360
+FP16_PAGE_BYTES = 65536            # KVARN_FP16_PAGE_BYTES
 NOALLOC_SCRATCH_BYTES = 4 << 20   # KVARN_NOALLOC_SCRATCH_BYTES
 
 OK = 0
@@ -66,6 +67,11 @@ SIGNATURES = {
     "kvarn_decode_attention_noalloc": (_I, [ctypes.POINTER(Config), _P, _P, _L, _P, _I, _P, _I,
                                             _I, _P, _P, ctypes.c_float, _P, _P, _P]),
     "kvarn_dequantize_pages": (_I, [_P, _L, _P, _P, _P]),
+    "kvarn_fp16_write_blocks": (_I, [_P, _P, _L, _L, _L, _I, _I, _P, _I, _P, _I, _P, _L, _P,
+                                     _P]),
+    "kvarn_fp16_decode_workspace_bytes": (ctypes.c_size_t, [_I, _I, _I, _I]),
+    "kvarn_fp16_decode_attention": (_I, [_P, _I, _I, _P, _L, _P, _I, _P, _I, _I,
+                                         ctypes.c_float, _P, _P, ctypes.c_size_t, _P, _P]),
     "kvarn_status_string": (ctypes.c_char_p, [_I]),
     "kvarn_version": (ctypes.c_char_p, []),
 }
@@ -237,3 +243,56 @@ def kvarn_dequantize_pages(records: torch.Tensor, stream=None):
     _check(lib().kvarn_dequantize_pages(_ptr(records), n, _ptr(yk), _ptr(yv), _stream(stream)),
            "kvarn_dequantize_pages")
     return yk, yv
+
+
+# ------------------------------------------- the FP16 cache (the baseline) --
+
+def alloc_fp16_pool(num_kv_heads: int, num_pages: int, device="cuda") -> torch.Tensor:
+    """uint8 [num_pages][Hkv][65536]: K then V, [128 tokens][128] fp16 each."""
+    return torch.zeros((num_pages, num_kv_heads, FP16_PAGE_BYTES), dtype=torch.uint8,
+                       device=device)
+
+
+def kvarn_fp16_write_blocks(k: torch.Tensor, v: torch.Tensor, seq_lens: torch.Tensor,
+                            max_seq: int, block_table: torch.Tensor, pool: torch.Tensor,
+                            status: Optional[torch.Tensor] = None, stream=None) -> None:
+    """k, v: fp16 [B][S][Hkv][128] (any strides with a dense last dim)."""
+    _dev(k, torch.float16, "k")
+    _dev(v, torch.float16, "v")
+    if k.shape != v.shape or k.stride() != v.stride() or k.dim() != 4 or k.stride(3) != 1:
+        raise ValueError("k and v must share shape/strides [B][S][Hkv][128], last dim dense")
+    _check(lib().kvarn_fp16_write_blocks(
+        _ptr(k), _ptr(v), k.stride(0), k.stride(1), k.stride(2), k.shape[0], k.shape[2],
+        _ptr(seq_lens), int(max_seq), _ptr(block_table), block_table.shape[-1], _ptr(pool),
+        pool.shape[0], _ptr(status), _stream(stream)), "kvarn_fp16_write_blocks")
+
+
+def fp16_decode_workspace_bytes(num_q_heads: int, num_kv_heads: int, batch: int,
+                                max_seq: int) -> int:
+    return lib().kvarn_fp16_decode_workspace_bytes(num_q_heads, num_kv_heads, batch, max_seq)
+
+
+def alloc_fp16_decode_workspace(num_q_heads: int, num_kv_heads: int, batch: int, max_seq: int,
+                                device="cuda") -> torch.Tensor:
+    n = fp16_decode_workspace_bytes(num_q_heads, num_kv_heads, batch, max_seq)
+    return torch.zeros((max(n, 16),), dtype=torch.uint8, device=device)
+
+
+def kvarn_fp16_decode_attention(q: torch.Tensor, num_kv_heads: int, pool: torch.Tensor,
+                                block_table: torch.Tensor, seq_lens: torch.Tensor, max_seq: int,
+                                out: torch.Tensor, workspace: Optional[torch.Tensor],
+                                softmax_scale: float = None,
+                                status: Optional[torch.Tensor] = None,
+                                stream=None) -> torch.Tensor:
+    """q, out: fp16 [B][Hq][128]; pool from alloc_fp16_pool."""
+    _dev(q, torch.float16, "q")
+    _dev(out, torch.float16, "out")
+    if softmax_scale is None:
+        softmax_scale = HEAD_DIM ** -0.5
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _check(lib().kvarn_fp16_decode_attention(
+        _ptr(q), q.shape[1], int(num_kv_heads), _ptr(pool), pool.shape[0], _ptr(block_table),
+        block_table.shape[-1], _ptr(seq_lens), q.shape[0], int(max_seq), float(softmax_scale),
+        _ptr(out), _ptr(workspace), ws_bytes, _ptr(status), _stream(stream)),
+        "kvarn_fp16_decode_attention")
+    return out

@@ -432,3 +432,42 @@ def test_method_beats_plain_rtn_on_outlier_keys(oracle):
     plain = s32.astype(np.float64)[:, None] * q + z32.astype(np.float64)[:, None]
     err_plain = np.linalg.norm(x.astype(np.float64) - plain)
     assert err_kvarn < 0.5 * err_plain
+
+
+# ------------------------------------------- the FP16 baseline's attention --
+
+def test_fp16_attention_matches_torch_sdpa(oracle):
+    """attention_fp16 equals torch's scaled_dot_product_attention (a library
+    routine) in float64, with GQA and ragged lengths (keys beyond the length
+    masked out)."""
+    import torch
+    g = torch.Generator().manual_seed(5)
+    B, S, hq, hkv = 3, 37, 6, 2
+    q = torch.randn(B, hq, 128, generator=g).half()
+    k = torch.randn(B, S, hkv, 128, generator=g).half()
+    v = torch.randn(B, S, hkv, 128, generator=g).half()
+    lens = np.array([37, 5, 20])
+    got = oracle.attention_fp16(q, k, v, lens, hq, hkv)
+    for b in range(B):
+        n = int(lens[b])
+        kk = k[b, :n].double().repeat_interleave(hq // hkv, dim=1).permute(1, 0, 2)
+        vv = v[b, :n].double().repeat_interleave(hq // hkv, dim=1).permute(1, 0, 2)
+        ref = torch.nn.functional.scaled_dot_product_attention(
+            q[b].double()[:, None, :], kk, vv, scale=128 ** -0.5)[:, 0, :]
+        assert np.abs(got[b] - ref.numpy()).max() < 1e-12
+
+
+def test_fp16_attention_special_cases(oracle):
+    import torch
+    g = torch.Generator().manual_seed(6)
+    q = torch.randn(2, 2, 128, generator=g).half()
+    k = torch.randn(2, 4, 1, 128, generator=g).half()
+    v = torch.randn(2, 4, 1, 128, generator=g).half()
+    out = oracle.attention_fp16(q, k, v, np.array([1, 0]), 2, 1)
+    # one token: its value; no token: zeros
+    assert np.array_equal(out[0, 0], v[0, 0, 0].double().numpy())
+    assert np.array_equal(out[1], np.zeros((2, 128)))
+    # equal keys: the mean of the values
+    k[:] = k[0, 0, 0]
+    out = oracle.attention_fp16(q, k, v, np.array([4, 4]), 2, 1)
+    assert np.abs(out[0, 1] - v[0, :, 0].double().mean(0).numpy()).max() < 1e-12
