@@ -86,11 +86,23 @@ __device__ __forceinline__ uint32_t movm_trans(uint32_t x) {
   return r;
 }
 
-// x with its 13 low mantissa bits cleared: 11 significant bits, exactly an
-// fp16 when |x| is in the fp16 normal range; x - head is exact in fp32.
-__device__ __forceinline__ float head11(float x) {
-  return __uint_as_float(__float_as_uint(x) & 0xFFFFE000u);
+// Split of an fp32 operand into two fp16 halves, hi + lo, for the tensor
+// cores.  hi is x rounded to the nearest multiple of a fixed power of two g
+// (adding and removing magic = 1.5 * 2^23 * g leaves the bits at and above g,
+// for |x| < 2^22 g); lo = x - hi is exact in fp32 and |lo| <= g / 2.
+//
+// The grid is fixed per operand column rather than relative to each x.  On
+// B300 an mma.sync with fp32 accumulation behaves as if it aligned its 16
+// products to the largest one and dropped the bits more than about 16 bits
+// below it: with an 11-significant-bit hi, sums of non-negative products came
+// out low by ~1e-4 relative, the same on every channel.  With hi on a grid of
+// g and |x| <= 2^11 g, every hi product is a multiple of g (codes are
+// integers) and the 16 of them span about 13 bits, so the sum is exact; what
+// the lo column can lose is at most ~2^-18 of the total.
+__device__ __forceinline__ float grid_hi(float x, float magic) {
+  return __fadd_rn(__fadd_rn(x, magic), -magic);
 }
+constexpr float kMagic1 = 12582912.f;   // 1.5 * 2^23: magic for g = 1
 
 // 2^k scale that maps amax into [2^14, 2^15), and its inverse.
 __device__ __forceinline__ void pow2_scale(float amax, float& s, float& inv) {
@@ -320,8 +332,11 @@ __global__ void __launch_bounds__(kThreads, 3) decode_mma_kernel(DecodeArgs a) {
           for (int slot = 0; slot < 2; ++slot) {
             const int c0 = 8 * (kb >> 1) + 2 * (kb & 1) + slot;
             const float f = slot ? scl16 : scl;
+            // |x| < 2^15 (slot 0) or 2^11 (slot 1): grid 16 or 1, i.e. 16
+            // in the units of the code it meets
             const float x0 = v[c0] * f, x1 = v[c0 + 4] * f;
-            const float h0 = head11(x0), h1 = head11(x1);
+            const float mg = slot ? kMagic1 : 16.f * kMagic1;
+            const float h0 = grid_hi(x0, mg), h1 = grid_hi(x1, mg);
             bq[nt][kb][slot] = odd ? pack2(x0 - h0, x1 - h1) : pack2(h0, h1);
           }
         }
@@ -440,8 +455,9 @@ __global__ void __launch_bounds__(kThreads, 3) decode_mma_kernel(DecodeArgs a) {
         float zq[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
         for (int j = 0; j < 16; ++j) {
+          // x <= 2^15 / 4^pos for a code carrying 4^pos: grid 16 / 4^pos
           const float x = sc[nt][j] * sf[j];
-          const float hi = head11(x);
+          const float hi = grid_hi(x, (16.f * kMagic1) * vpos_inv(j >> 1, j & 1));
           bp[nt][j >> 1][j & 1] = movm_trans(pack2(hi, x - hi));
           zq[j & 3] = fmaf(sc[nt][j], szv[j].y, zq[j & 3]);
         }
