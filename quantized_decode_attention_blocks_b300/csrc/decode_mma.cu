@@ -16,9 +16,9 @@
 // codes fed straight from the packed words: one AND leaves a code q at bit
 // position 4i (K) or 2i (V) of each 16-bit half, which read as an fp16 is the
 // subnormal q * 2^(4i-24) (resp. 2^(2i-24)), exact.  The power of two is
-// undone on the query side, which is split into an fp16 pair hi + lo (~21
-// significant bits, scaled by a power of two into range); the tensor core
-// accumulates the exact products in fp32.
+// undone on the query side, which is scaled by a power of two into range and
+// split into an fp16 pair hi + lo, hi on a fixed grid (grid_hi below) so that
+// the tensor core's fp32 sums of the hi products are exact.
 //
 // CTA = 4 warps, each an independent stream over the pages of its split of
 // one (sequence, KV head): warp w takes pages u0 + w, u0 + w + 4, ...  Each
@@ -101,6 +101,9 @@ __device__ __forceinline__ uint32_t movm_trans(uint32_t x) {
 // the lo column can lose is at most ~2^-18 of the total.
 __device__ __forceinline__ float grid_hi(float x, float magic) {
   return __fadd_rn(__fadd_rn(x, magic), -magic);
+}
+__device__ __forceinline__ float2 grid_hi2(float2 x, float magic) {   // both halves, one grid
+  return __fadd2_rn(__fadd2_rn(x, make_float2(magic, magic)), make_float2(-magic, -magic));
 }
 constexpr float kMagic1 = 12582912.f;   // 1.5 * 2^23: magic for g = 1
 
@@ -334,10 +337,10 @@ __global__ void __launch_bounds__(kThreads, 3) decode_mma_kernel(DecodeArgs a) {
             const float f = slot ? scl16 : scl;
             // |x| < 2^15 (slot 0) or 2^11 (slot 1): grid 16 or 1, i.e. 16
             // in the units of the code it meets
-            const float x0 = v[c0] * f, x1 = v[c0 + 4] * f;
-            const float mg = slot ? kMagic1 : 16.f * kMagic1;
-            const float h0 = grid_hi(x0, mg), h1 = grid_hi(x1, mg);
-            bq[nt][kb][slot] = odd ? pack2(x0 - h0, x1 - h1) : pack2(h0, h1);
+            const float2 x = __fmul2_rn(make_float2(v[c0], v[c0 + 4]), make_float2(f, f));
+            const float2 h = grid_hi2(x, slot ? kMagic1 : 16.f * kMagic1);
+            const float2 o = odd ? __ffma2_rn(h, make_float2(-1.f, -1.f), x) : h;   // lo | hi
+            bq[nt][kb][slot] = pack2(o.x, o.y);
           }
         }
         // this lane's score column pair (2qi, 2qi+1) is head 4nt + qi, held
