@@ -7,6 +7,7 @@ no CPU fallback.
 """
 from __future__ import annotations
 
+import contextlib
 import ctypes
 import os
 from typing import Optional
@@ -112,17 +113,86 @@ def _ptr(t: Optional[torch.Tensor]):
     return None if t is None else ctypes.c_void_p(t.data_ptr())
 
 
-def _stream(stream) -> ctypes.c_void_p:
+def _stream(stream, device) -> ctypes.c_void_p:
     if stream is None:
-        stream = torch.cuda.current_stream()
+        stream = torch.cuda.current_stream(device)
     return ctypes.c_void_p(stream.cuda_stream)
 
 
-def _dev(t: torch.Tensor, dtype, name: str):
-    if not t.is_cuda:
+def _on(device):
+    """Makes `device` current for the call when it is not already: the library
+    launches on the current device, and the pointers belong to `device`."""
+    if (device.type == "cuda" and device.index is not None
+            and device.index != torch.cuda.current_device()):
+        return torch.cuda.device(device)
+    return contextlib.nullcontext()
+
+
+# Checked on every tensor argument.  The C ABI addresses each buffer from its
+# base pointer with a fixed layout, and cannot see the allocation, so a wrong
+# dtype, shape or stride would make the kernels read or write outside it.  The
+# CPU tests of these checks clear _REQUIRE_CUDA and replace the library.
+_REQUIRE_CUDA = True
+
+
+class _AtLeast:
+    def __init__(self, n: int):
+        self.n = int(n)
+
+    def ok(self, x: int) -> bool:
+        return x >= self.n
+
+    def __repr__(self) -> str:
+        return f">={self.n}"
+
+
+def _arg(t, name: str, dtype, shape=None, device=None, contiguous: bool = True):
+    """t must be a tensor of `dtype` (None: any) on `device` (None: any CUDA
+    device); shape entries are an exact size, _AtLeast(n) or None (any).
+    Returns t.device."""
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor, got {type(t).__name__}")
+    if _REQUIRE_CUDA and not t.is_cuda:
         raise ValueError(f"{name} must be a CUDA tensor")
-    if t.dtype != dtype:
+    if device is not None and t.device != device:
+        raise ValueError(f"{name} is on {t.device}; the other arguments are on {device}")
+    if dtype is not None and t.dtype != dtype:
         raise ValueError(f"{name} must be {dtype}, got {t.dtype}")
+    if shape is not None:
+        fits = t.dim() == len(shape) and all(
+            s is None or (s.ok(n) if isinstance(s, _AtLeast) else n == s)
+            for n, s in zip(t.shape, shape))
+        if not fits:
+            want = "[" + "][".join("*" if s is None else repr(s) for s in shape) + "]"
+            raise ValueError(f"{name} must have shape {want}, got {list(t.shape)}")
+    if contiguous and not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    return t.device
+
+
+def _kv_pair(k, v, hkv: int):
+    """Prefill inputs: fp16 [B][S][Hkv][128] with a dense last dim, sharing strides."""
+    dev = _arg(k, "k", torch.float16, (None, None, hkv, HEAD_DIM), contiguous=False)
+    _arg(v, "v", torch.float16, tuple(k.shape), device=dev, contiguous=False)
+    if k.stride() != v.stride() or k.stride(3) != 1:
+        raise ValueError("k and v must share shape/strides [B][S][Hkv][128], last dim dense")
+    return dev
+
+
+def _lens_table(dev, B: int, seq_lens, lens_name: str, block_table):
+    _arg(seq_lens, lens_name, torch.int32, (_AtLeast(B),), device=dev)
+    _arg(block_table, "block_table", torch.int32, (_AtLeast(B), None), device=dev)
+
+
+def _tails(dev, cfg, B: int, tail_k, tail_v):
+    shape = (_AtLeast(B), cfg.num_kv_heads, BLOCK_TOKENS, HEAD_DIM)
+    _arg(tail_k, "tail_k", torch.float16, shape, device=dev)
+    _arg(tail_v, "tail_v", torch.float16, tuple(tail_k.shape), device=dev)
+
+
+def _status(dev, status):
+    if status is not None:
+        _arg(status, "status", torch.int32, (_AtLeast(1),), device=dev)
 
 
 # ------------------------------------------------------------------ config --
@@ -170,17 +240,21 @@ def kvarn_quantize_blocks(cfg: Config, k: torch.Tensor, v: torch.Tensor, seq_len
                           max_seq: int, block_table: torch.Tensor, pool: torch.Tensor,
                           tail_k: torch.Tensor, tail_v: torch.Tensor,
                           status: Optional[torch.Tensor] = None, stream=None) -> None:
-    """k, v: fp16 [B][S][Hkv][128] (any strides with a dense last dim)."""
-    _dev(k, torch.float16, "k")
-    _dev(v, torch.float16, "v")
-    if k.shape != v.shape or k.stride() != v.stride() or k.dim() != 4 or k.stride(3) != 1:
-        raise ValueError("k and v must share shape/strides [B][S][Hkv][128], last dim dense")
+    """k, v: fp16 [B][S][Hkv][128] (any strides with a dense last dim);
+    seq_lens int32 [B] (each <= S); block_table int32 [B][max_blocks]; pool
+    uint8 [num_pages][Hkv][15360]; tails fp16 [B][Hkv][128][128]."""
+    dev = _kv_pair(k, v, cfg.num_kv_heads)
     B = k.shape[0]
-    _check(lib().kvarn_quantize_blocks(
-        ctypes.byref(cfg), _ptr(k), _ptr(v), k.stride(0), k.stride(1), k.stride(2), B,
-        _ptr(seq_lens), int(max_seq), _ptr(block_table), block_table.shape[-1], _ptr(pool),
-        pool.shape[0], _ptr(tail_k), _ptr(tail_v), _ptr(status), _stream(stream)),
-        "kvarn_quantize_blocks")
+    _lens_table(dev, B, seq_lens, "seq_lens", block_table)
+    _arg(pool, "pool", torch.uint8, (None, cfg.num_kv_heads, PAGE_BYTES), device=dev)
+    _tails(dev, cfg, B, tail_k, tail_v)
+    _status(dev, status)
+    with _on(dev):
+        _check(lib().kvarn_quantize_blocks(
+            ctypes.byref(cfg), _ptr(k), _ptr(v), k.stride(0), k.stride(1), k.stride(2), B,
+            _ptr(seq_lens), int(max_seq), _ptr(block_table), block_table.shape[-1], _ptr(pool),
+            pool.shape[0], _ptr(tail_k), _ptr(tail_v), _ptr(status), _stream(stream, dev)),
+            "kvarn_quantize_blocks")
 
 
 def kvarn_append_token(cfg: Config, k_new: torch.Tensor, v_new: torch.Tensor, pos: torch.Tensor,
@@ -188,12 +262,29 @@ def kvarn_append_token(cfg: Config, k_new: torch.Tensor, v_new: torch.Tensor, po
                        tail_v: torch.Tensor, status: Optional[torch.Tensor] = None,
                        stream=None) -> None:
     """k_new, v_new: fp16 [B][Hkv][128]; pos: int32 [B] length before the append."""
-    _dev(k_new, torch.float16, "k_new")
-    _dev(v_new, torch.float16, "v_new")
-    _check(lib().kvarn_append_token(
-        ctypes.byref(cfg), _ptr(k_new), _ptr(v_new), _ptr(pos), k_new.shape[0],
-        _ptr(block_table), block_table.shape[-1], _ptr(pool), pool.shape[0], _ptr(tail_k),
-        _ptr(tail_v), _ptr(status), _stream(stream)), "kvarn_append_token")
+    dev = _arg(k_new, "k_new", torch.float16, (None, cfg.num_kv_heads, HEAD_DIM))
+    _arg(v_new, "v_new", torch.float16, tuple(k_new.shape), device=dev)
+    B = k_new.shape[0]
+    _lens_table(dev, B, pos, "pos", block_table)
+    _arg(pool, "pool", torch.uint8, (None, cfg.num_kv_heads, PAGE_BYTES), device=dev)
+    _tails(dev, cfg, B, tail_k, tail_v)
+    _status(dev, status)
+    with _on(dev):
+        _check(lib().kvarn_append_token(
+            ctypes.byref(cfg), _ptr(k_new), _ptr(v_new), _ptr(pos), B, _ptr(block_table),
+            block_table.shape[-1], _ptr(pool), pool.shape[0], _ptr(tail_k), _ptr(tail_v),
+            _ptr(status), _stream(stream, dev)), "kvarn_append_token")
+
+
+def _decode_args(cfg, q, pool, block_table, seq_lens, tail_k, tail_v, out, status):
+    dev = _arg(q, "q", torch.float16, (None, cfg.num_q_heads, HEAD_DIM))
+    _arg(out, "out", torch.float16, tuple(q.shape), device=dev)
+    B = q.shape[0]
+    _lens_table(dev, B, seq_lens, "seq_lens", block_table)
+    _arg(pool, "pool", torch.uint8, (None, cfg.num_kv_heads, PAGE_BYTES), device=dev)
+    _tails(dev, cfg, B, tail_k, tail_v)
+    _status(dev, status)
+    return dev
 
 
 def kvarn_decode_attention(cfg: Config, q: torch.Tensor, pool: torch.Tensor,
@@ -201,17 +292,19 @@ def kvarn_decode_attention(cfg: Config, q: torch.Tensor, pool: torch.Tensor,
                            tail_k: torch.Tensor, tail_v: torch.Tensor, out: torch.Tensor,
                            workspace: Optional[torch.Tensor], softmax_scale: float = None,
                            status: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
-    """q, out: fp16 [B][Hq][128]."""
-    _dev(q, torch.float16, "q")
-    _dev(out, torch.float16, "out")
+    """q, out: fp16 [B][Hq][128]; seq_lens int32 [B] (pages + tail tokens)."""
+    dev = _decode_args(cfg, q, pool, block_table, seq_lens, tail_k, tail_v, out, status)
+    if workspace is not None:
+        _arg(workspace, "workspace", None, device=dev)
     if softmax_scale is None:
         softmax_scale = HEAD_DIM ** -0.5
     ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
-    _check(lib().kvarn_decode_attention(
-        ctypes.byref(cfg), _ptr(q), _ptr(pool), pool.shape[0], _ptr(block_table),
-        block_table.shape[-1], _ptr(seq_lens), q.shape[0], int(max_seq), _ptr(tail_k),
-        _ptr(tail_v), float(softmax_scale), _ptr(out), _ptr(workspace), ws_bytes, _ptr(status),
-        _stream(stream)), "kvarn_decode_attention")
+    with _on(dev):
+        _check(lib().kvarn_decode_attention(
+            ctypes.byref(cfg), _ptr(q), _ptr(pool), pool.shape[0], _ptr(block_table),
+            block_table.shape[-1], _ptr(seq_lens), q.shape[0], int(max_seq), _ptr(tail_k),
+            _ptr(tail_v), float(softmax_scale), _ptr(out), _ptr(workspace), ws_bytes,
+            _ptr(status), _stream(stream, dev)), "kvarn_decode_attention")
     return out
 
 
@@ -223,25 +316,27 @@ def kvarn_decode_attention_noalloc(cfg: Config, q: torch.Tensor, pool: torch.Ten
                                    stream=None) -> torch.Tensor:
     """Decode attention for callers that cannot allocate: the split-K scratch
     is a fixed array inside the library (see include/kvarn.h)."""
-    _dev(q, torch.float16, "q")
-    _dev(out, torch.float16, "out")
+    dev = _decode_args(cfg, q, pool, block_table, seq_lens, tail_k, tail_v, out, status)
     if softmax_scale is None:
         softmax_scale = HEAD_DIM ** -0.5
-    _check(lib().kvarn_decode_attention_noalloc(
-        ctypes.byref(cfg), _ptr(q), _ptr(pool), pool.shape[0], _ptr(block_table),
-        block_table.shape[-1], _ptr(seq_lens), q.shape[0], int(max_seq), _ptr(tail_k),
-        _ptr(tail_v), float(softmax_scale), _ptr(out), _ptr(status), _stream(stream)),
-        "kvarn_decode_attention_noalloc")
+    with _on(dev):
+        _check(lib().kvarn_decode_attention_noalloc(
+            ctypes.byref(cfg), _ptr(q), _ptr(pool), pool.shape[0], _ptr(block_table),
+            block_table.shape[-1], _ptr(seq_lens), q.shape[0], int(max_seq), _ptr(tail_k),
+            _ptr(tail_v), float(softmax_scale), _ptr(out), _ptr(status), _stream(stream, dev)),
+            "kvarn_decode_attention_noalloc")
     return out
 
 
 def kvarn_dequantize_pages(records: torch.Tensor, stream=None):
     """records: uint8 [n][15360] (contiguous) -> (yk, yv) float32 [n][128][128]."""
+    dev = _arg(records, "records", torch.uint8, (None, PAGE_BYTES))
     n = records.shape[0]
-    yk = torch.empty((n, BLOCK_TOKENS, HEAD_DIM), dtype=torch.float32, device=records.device)
+    yk = torch.empty((n, BLOCK_TOKENS, HEAD_DIM), dtype=torch.float32, device=dev)
     yv = torch.empty_like(yk)
-    _check(lib().kvarn_dequantize_pages(_ptr(records), n, _ptr(yk), _ptr(yv), _stream(stream)),
-           "kvarn_dequantize_pages")
+    with _on(dev):
+        _check(lib().kvarn_dequantize_pages(_ptr(records), n, _ptr(yk), _ptr(yv),
+                                            _stream(stream, dev)), "kvarn_dequantize_pages")
     return yk, yv
 
 
@@ -256,15 +351,18 @@ def alloc_fp16_pool(num_kv_heads: int, num_pages: int, device="cuda") -> torch.T
 def kvarn_fp16_write_blocks(k: torch.Tensor, v: torch.Tensor, seq_lens: torch.Tensor,
                             max_seq: int, block_table: torch.Tensor, pool: torch.Tensor,
                             status: Optional[torch.Tensor] = None, stream=None) -> None:
-    """k, v: fp16 [B][S][Hkv][128] (any strides with a dense last dim)."""
-    _dev(k, torch.float16, "k")
-    _dev(v, torch.float16, "v")
-    if k.shape != v.shape or k.stride() != v.stride() or k.dim() != 4 or k.stride(3) != 1:
-        raise ValueError("k and v must share shape/strides [B][S][Hkv][128], last dim dense")
-    _check(lib().kvarn_fp16_write_blocks(
-        _ptr(k), _ptr(v), k.stride(0), k.stride(1), k.stride(2), k.shape[0], k.shape[2],
-        _ptr(seq_lens), int(max_seq), _ptr(block_table), block_table.shape[-1], _ptr(pool),
-        pool.shape[0], _ptr(status), _stream(stream)), "kvarn_fp16_write_blocks")
+    """k, v: fp16 [B][S][Hkv][128] (any strides with a dense last dim); pool
+    from alloc_fp16_pool with the same Hkv."""
+    dev = _kv_pair(k, v, None)
+    B, hkv = k.shape[0], k.shape[2]
+    _lens_table(dev, B, seq_lens, "seq_lens", block_table)
+    _arg(pool, "pool", torch.uint8, (None, hkv, FP16_PAGE_BYTES), device=dev)
+    _status(dev, status)
+    with _on(dev):
+        _check(lib().kvarn_fp16_write_blocks(
+            _ptr(k), _ptr(v), k.stride(0), k.stride(1), k.stride(2), B, hkv, _ptr(seq_lens),
+            int(max_seq), _ptr(block_table), block_table.shape[-1], _ptr(pool), pool.shape[0],
+            _ptr(status), _stream(stream, dev)), "kvarn_fp16_write_blocks")
 
 
 def fp16_decode_workspace_bytes(num_q_heads: int, num_kv_heads: int, batch: int,
@@ -285,14 +383,21 @@ def kvarn_fp16_decode_attention(q: torch.Tensor, num_kv_heads: int, pool: torch.
                                 status: Optional[torch.Tensor] = None,
                                 stream=None) -> torch.Tensor:
     """q, out: fp16 [B][Hq][128]; pool from alloc_fp16_pool."""
-    _dev(q, torch.float16, "q")
-    _dev(out, torch.float16, "out")
+    dev = _arg(q, "q", torch.float16, (None, None, HEAD_DIM))
+    _arg(out, "out", torch.float16, tuple(q.shape), device=dev)
+    B = q.shape[0]
+    _lens_table(dev, B, seq_lens, "seq_lens", block_table)
+    _arg(pool, "pool", torch.uint8, (None, int(num_kv_heads), FP16_PAGE_BYTES), device=dev)
+    _status(dev, status)
+    if workspace is not None:
+        _arg(workspace, "workspace", None, device=dev)
     if softmax_scale is None:
         softmax_scale = HEAD_DIM ** -0.5
     ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
-    _check(lib().kvarn_fp16_decode_attention(
-        _ptr(q), q.shape[1], int(num_kv_heads), _ptr(pool), pool.shape[0], _ptr(block_table),
-        block_table.shape[-1], _ptr(seq_lens), q.shape[0], int(max_seq), float(softmax_scale),
-        _ptr(out), _ptr(workspace), ws_bytes, _ptr(status), _stream(stream)),
-        "kvarn_fp16_decode_attention")
+    with _on(dev):
+        _check(lib().kvarn_fp16_decode_attention(
+            _ptr(q), q.shape[1], int(num_kv_heads), _ptr(pool), pool.shape[0], _ptr(block_table),
+            block_table.shape[-1], _ptr(seq_lens), B, int(max_seq), float(softmax_scale),
+            _ptr(out), _ptr(workspace), ws_bytes, _ptr(status), _stream(stream, dev)),
+            "kvarn_fp16_decode_attention")
     return out
