@@ -832,14 +832,10 @@ __global__ void __launch_bounds__(kThreads, 3) decode_mma_kernel(DecodeArgs a) {
 
 template <int NT>
 cudaError_t launch_nt(const DecodeArgs& args, cudaStream_t s) {
-  static bool attr_set = false;
+  static std::atomic<uint64_t> smem_set{0};
   const int smem = (int)sizeof(MmaSmem<NT>);
-  if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(decode_mma_kernel<NT>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-    if (e != cudaSuccess) return e;
-    attr_set = true;
-  }
+  cudaError_t e = ensure_dynamic_smem(decode_mma_kernel<NT>, smem, smem_set);
+  if (e != cudaSuccess) return e;
   DecodeArgs a = args;
   a.cluster = a.nsplit >= 2 && a.nsplit <= kMaxClusterSplits;
   cudaLaunchConfig_t cfg = {};

@@ -283,14 +283,10 @@ __global__ void __launch_bounds__(kThreads) decode_simple_kernel(DecodeArgs a) {
 }  // namespace
 
 cudaError_t launch_decode_simple(const DecodeArgs& a, cudaStream_t s) {
-  static bool attr_set = false;
+  static std::atomic<uint64_t> smem_set{0};
   const int smem = (int)sizeof(DecodeSmem);
-  if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(decode_simple_kernel,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-    if (e != cudaSuccess) return e;
-    attr_set = true;
-  }
+  cudaError_t e = ensure_dynamic_smem(decode_simple_kernel, smem, smem_set);
+  if (e != cudaSuccess) return e;
   dim3 grid(a.nsplit, a.hkv, a.batch);
   decode_simple_kernel<<<grid, kThreads, smem, s>>>(a);
   return cudaGetLastError();

@@ -399,13 +399,9 @@ cudaError_t launch_fp16_write(const F16WriteArgs& a, cudaStream_t s) {
 }
 
 cudaError_t launch_fp16_decode(const F16DecodeArgs& a, const void* pool, cudaStream_t s) {
-  static bool attr_set = false;
-  if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(fp16_decode_kernel,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, kFSmemBytes);
-    if (e != cudaSuccess) return e;
-    attr_set = true;
-  }
+  static std::atomic<uint64_t> smem_set{0};
+  cudaError_t e = ensure_dynamic_smem(fp16_decode_kernel, kFSmemBytes, smem_set);
+  if (e != cudaSuccess) return e;
   // pool as (channel, token, 2 * head + part, page), 64 x 64 boxes
   CUtensorMap tm;
   const uint64_t dims[4] = {(uint64_t)kD, (uint64_t)kT, (uint64_t)2 * a.hkv,

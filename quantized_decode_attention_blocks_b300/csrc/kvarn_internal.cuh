@@ -7,6 +7,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <atomic>
+
 #include "../../include/kvarn.h"
 
 namespace kvarn {
@@ -45,6 +47,24 @@ constexpr int kNumSMs = 148;      // B300
 
 // 1 / sqrt(128), rounded to fp32.
 constexpr float kInvSqrt128 = 0.08838834764831845f;
+
+// Raises a kernel's dynamic shared-memory limit to `bytes` on the current
+// device.  cudaFuncSetAttribute acts on the current device only, so `done`
+// keeps one bit per device id (0-63) where it has been applied; other ids
+// apply it on every call.  Safe to call from several host threads, and after
+// the first call on a device it makes no CUDA call besides cudaGetDevice (so
+// it may run inside a stream capture).
+template <typename Kernel>
+cudaError_t ensure_dynamic_smem(Kernel* kernel, int bytes, std::atomic<uint64_t>& done) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  const uint64_t bit = (dev >= 0 && dev < 64) ? (uint64_t(1) << dev) : 0;
+  if (bit != 0 && (done.load(std::memory_order_acquire) & bit) != 0) return cudaSuccess;
+  e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  if (e == cudaSuccess) done.fetch_or(bit, std::memory_order_release);
+  return e;
+}
 
 struct QuantizeArgs {
   const __half* k;
