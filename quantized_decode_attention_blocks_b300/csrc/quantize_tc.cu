@@ -711,17 +711,16 @@ typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t,
                                   const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
 
-// Looked up once per process (a function-local static: thread-safe).
 EncodeTiledFn encode_fn() {
-  static const EncodeTiledFn fn = [] {
+  static EncodeTiledFn fn = nullptr;
+  if (!fn) {
     void* p = nullptr;
     cudaDriverEntryPointQueryResult q;
     if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
                                          &q) == cudaSuccess &&
         q == cudaDriverEntryPointSuccess)
-      return reinterpret_cast<EncodeTiledFn>(p);
-    return EncodeTiledFn(nullptr);
-  }();
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  }
   return fn;
 }
 
@@ -767,9 +766,13 @@ constexpr int kQSmemBytes = (int)sizeof(QSmem) + 1024;
 
 cudaError_t launch_tiles(const CUtensorMap& mk, const CUtensorMap& mv, const QTileArgs& qa,
                          cudaStream_t s) {
-  static std::atomic<uint64_t> smem_set{0};
-  cudaError_t e = ensure_dynamic_smem(quantize_tc_kernel, kQSmemBytes, smem_set);
-  if (e != cudaSuccess) return e;
+  static bool attr_set = false;
+  if (!attr_set) {
+    cudaError_t e = cudaFuncSetAttribute(quantize_tc_kernel,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, kQSmemBytes);
+    if (e != cudaSuccess) return e;
+    attr_set = true;
+  }
   if (qa.ntiles <= 0) return cudaSuccess;
   const int want = (qa.ntiles + kWG - 1) / kWG;
   const int grid = want < kNumSMs ? want : kNumSMs;
