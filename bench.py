@@ -135,27 +135,33 @@ class ClockSampler:
             self.proc.kill()
         if self.thread:
             self.thread.join(timeout=2)
-        sm, mx, reasons = [], [], set()
-        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
         t0 = getattr(self, "t_start", 0.0) - 0.15
         t1 = getattr(self, "t_stop", time.time()) + 0.15
         window = [ln for (t, ln) in self.lines if t0 <= t <= t1] or [ln for (_, ln) in
                                                                       self.lines[-2:]]
-        for line in window:
-            parts = [x.strip() for x in line.split(",")]
-            if len(parts) != 7:
-                continue
-            try:
-                sm.append(float(parts[1]))
-                mx.append(float(parts[2]))
-            except ValueError:
-                continue
-            for n, v in zip(names, parts[3:]):
-                if v.lower().startswith("active"):
-                    reasons.add(n)
-        return {"sm_mhz": statistics.median(sm) if sm else None,
-                "sm_max_mhz": max(mx) if mx else None, "reasons": sorted(reasons),
-                "samples": len(sm)}
+        return summarize_clock_lines(window)
+
+
+def summarize_clock_lines(lines):
+    """Median SM clock, max SM clock and the active throttle reasons over lines
+    of `nvidia-smi --query-gpu=<ClockSampler.FIELDS> --format=csv,noheader,nounits`."""
+    sm, mx, reasons = [], [], set()
+    names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+    for line in lines:
+        parts = [x.strip() for x in line.split(",")]
+        if len(parts) != 7:
+            continue
+        try:
+            sm.append(float(parts[1]))
+            mx.append(float(parts[2]))
+        except ValueError:
+            continue
+        for n, v in zip(names, parts[3:]):
+            if v.lower().startswith("active"):
+                reasons.add(n)
+    return {"sm_mhz": statistics.median(sm) if sm else None,
+            "sm_max_mhz": max(mx) if mx else None, "reasons": sorted(reasons),
+            "samples": len(sm)}
 
 
 # ----------------------------------------------------------- GPU workload --
