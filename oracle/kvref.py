@@ -262,3 +262,60 @@ def attention_fp16(q, k, v, seq_lens, hq: int, hkv: int,
             p = np.exp(s - s.max())
             out[b, h] = (p @ vh) / p.sum()
     return out
+
+
+def chunk_attention(q, start, chunk_lens, pool, block_table, tail_k, tail_v, hq: int, hkv: int,
+                    scale: float = 1.0 / np.sqrt(128.0)) -> np.ndarray:
+    """Attention of a chunk of new query tokens over the quantized cache
+    (chunked prefill), float64 output [B][M][Hq][128].
+
+    Sequence b holds start[b] tokens before the chunk and chunk_lens[b] <= M
+    new ones; the cache (pool pages + fp16 tails) is its state after the
+    chunk's tokens were appended, n_b = start[b] + chunk_lens[b] tokens.
+    Query i sits at position P = start[b] + i and attends causally to tokens
+    0..P: out = sum_{t<=P} softmax_t(scale q . k_t) v_t, the textbook
+    definition ("KV Cache (Anahtar-Deger Onbellegi)", yapayzekasozluk.tr, "KV
+    Cache Nasil Calisir?") with the decode reading "append, then attend"
+    applied to a whole chunk.  Token t is read, in plain space, from its page
+    (x = H yhat, stage-4 dequantization of the KVarN page, blog.edumints.com)
+    when its block is full in the cache, else from tail slot t mod 128.  Rows
+    i >= chunk_lens[b] are zero.  q: fp16 [B][M][Hq][128]."""
+    qd = np.asarray(q)
+    if qd.dtype == np.uint16:
+        qd = qd.view(np.float16)
+    qd = qd.astype(np.float64)
+    tk = np.asarray(tail_k)
+    tv = np.asarray(tail_v)
+    tk = (tk.view(np.float16) if tk.dtype == np.uint16 else tk).astype(np.float64)
+    tv = (tv.view(np.float16) if tv.dtype == np.uint16 else tv).astype(np.float64)
+    start = np.asarray(start, dtype=np.int64)
+    chunk_lens = np.asarray(chunk_lens, dtype=np.int64)
+    block_table = np.asarray(block_table)
+    B, M = qd.shape[0], qd.shape[1]
+    g = hq // hkv
+    H = hadamard(NCH)
+    out = np.zeros((B, M, hq, NCH))
+    for b in range(B):
+        n = int(start[b] + chunk_lens[b])
+        if chunk_lens[b] <= 0 or n <= 0:
+            continue
+        nfull = n // NTOK
+        K = np.zeros((hkv, n, NCH))
+        V = np.zeros((hkv, n, NCH))
+        for j in range(nfull):
+            page = int(block_table[b, j])
+            if page < 0 or page >= pool.shape[0]:
+                raise ValueError("oracle: page id outside the pool")
+            for h in range(hkv):
+                K[h, j * NTOK:(j + 1) * NTOK] = dequant_part(pool[page, h], False) @ H
+                V[h, j * NTOK:(j + 1) * NTOK] = dequant_part(pool[page, h], True) @ H
+        r = n - nfull * NTOK
+        K[:, nfull * NTOK:] = tk[b, :, :r]
+        V[:, nfull * NTOK:] = tv[b, :, :r]
+        for i in range(int(chunk_lens[b])):
+            P = int(start[b]) + i
+            for h in range(hq):
+                s = (K[h // g, :P + 1] @ qd[b, i, h]) * scale
+                p = np.exp(s - s.max())
+                out[b, i, h] = (p / p.sum()) @ V[h // g, :P + 1]
+    return out

@@ -471,3 +471,83 @@ def test_fp16_attention_special_cases(oracle):
     k[:] = k[0, 0, 0]
     out = oracle.attention_fp16(q, k, v, np.array([4, 4]), 2, 1)
     assert np.abs(out[0, 1] - v[0, :, 0].double().mean(0).numpy()).max() < 1e-12
+
+
+# ------------------------------------------------- chunked prefill (next) --
+
+def _chunk_state(oracle, start=(250, 100, 0), m=(150, 60, 60), hkv=2, hq=4, seed=31):
+    """Caches holding start + m tokens (the chunk already appended: a page is
+    what 128 appends make, pinned above), and M = max(m) query rows."""
+    n = [s + c for s, c in zip(start, m)]
+    B, M = len(n), max(m)
+    w = synth.scaled(synth.WORKLOADS["llama3_8b_layer"], batch=B, seq=max(n), hkv=hkv, hq=hq,
+                     seed=seed)
+    k, v = synth.kv(w)
+    lens = np.array(n, dtype=np.int32)
+    mb = (max(n) + 127) // 128
+    table = np.arange(B * mb, dtype=np.int32).reshape(B, mb)[:, ::-1].copy()
+    st = oracle.quantize_blocks(k.numpy(), v.numpy(), lens, table, B * mb, 2)
+    q = np.random.default_rng(seed).standard_normal((B, M, hq, 128)).astype(np.float16)
+    return k.numpy(), v.numpy(), q, np.array(start), np.array(m), table, st
+
+
+def test_chunk_rows_at_whole_pages_and_the_last_row_equal_decode(oracle):
+    # a query whose prefix is whole pages, or the whole cache, sees exactly
+    # what decode attention over that many tokens sees
+    k, v, q, start, m, table, st = _chunk_state(oracle)
+    hq, hkv = q.shape[2], st["pool"].shape[1]
+    out = oracle.chunk_attention(q, start, m, st["pool"], table, st["tail_k"], st["tail_v"], hq,
+                                 hkv)
+    checked = 0
+    for b in range(len(start)):
+        for i in range(int(m[b])):
+            P = int(start[b]) + i
+            if (P + 1) % 128 and i != m[b] - 1:
+                continue
+            ref = oracle.decode_attention(q[b:b + 1, i], st["pool"], table[b:b + 1],
+                                          np.array([P + 1], np.int32), st["tail_k"][b:b + 1],
+                                          st["tail_v"][b:b + 1], hq, hkv, route=0)[0]
+            assert np.abs(out[b, i] - ref).max() <= 1e-12 * max(1.0, np.abs(ref).max())
+            checked += 1
+    assert checked == 6     # P + 1 = 256, 384, 400 | 128, 160 | 60
+    assert not out[1, 60:].any() and not out[2, 60:].any()   # rows past the chunk
+
+
+def test_chunk_within_one_block_is_causal_fp16_attention(oracle):
+    # sequence 2 has 60 tokens, all in the fp16 tail: row i is plain attention
+    # over the first i + 1 raw tokens (the fp16 oracle, pinned to torch above)
+    k, v, q, start, m, table, st = _chunk_state(oracle)
+    hq, hkv = q.shape[2], st["pool"].shape[1]
+    out = oracle.chunk_attention(q, start, m, st["pool"], table, st["tail_k"], st["tail_v"], hq,
+                                 hkv)
+    for i in (0, 1, 17, 59):
+        ref = oracle.attention_fp16(q[2:3, i], k[2:3], v[2:3], np.array([i + 1]), hq, hkv)[0]
+        assert np.abs(out[2, i] - ref).max() <= 1e-12 * max(1.0, np.abs(ref).max())
+    assert np.array_equal(out[2, 0, 0], v[2, 0, 0].astype(np.float64))   # one token: its value
+
+
+def test_chunk_attention_is_causal(oracle):
+    # changing token 394 (tail slot 10 of sequence 0) moves rows P >= 394 only
+    k, v, q, start, m, table, st = _chunk_state(oracle)
+    hq, hkv = q.shape[2], st["pool"].shape[1]
+    args = (st["pool"], table)
+    o1 = oracle.chunk_attention(q, start, m, *args, st["tail_k"], st["tail_v"], hq, hkv)
+    tk, tv = st["tail_k"].copy(), st["tail_v"].copy()
+    tk[0, :, 10] = tk[0, :, 3]
+    tv[0, :, 10] = (tv[0, :, 10].view(np.float16) * 3).view(tv.dtype)
+    o2 = oracle.chunk_attention(q, start, m, *args, tk, tv, hq, hkv)
+    cut = 394 - int(start[0])
+    assert np.array_equal(o1[0, :cut], o2[0, :cut])
+    assert (np.abs(o1[0, cut:150] - o2[0, cut:150]).max(axis=(1, 2)) > 0).all()
+    assert np.array_equal(o1[1:], o2[1:])
+
+
+def test_chunk_attention_gqa_heads_share_their_kv_head(oracle):
+    k, v, q, start, m, table, st = _chunk_state(oracle)
+    hq, hkv = q.shape[2], st["pool"].shape[1]
+    q[:, :, 1] = q[:, :, 0]      # heads 0 and 1 read KV head 0 (g = 2)
+    q[:, :, 3] = q[:, :, 0]      # head 3 reads KV head 1
+    out = oracle.chunk_attention(q, start, m, st["pool"], table, st["tail_k"], st["tail_v"], hq,
+                                 hkv)
+    assert np.array_equal(out[:, :, 0], out[:, :, 1])
+    assert not np.array_equal(out[0, :150, 0], out[0, :150, 3])
