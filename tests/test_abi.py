@@ -168,3 +168,40 @@ def test_binding_refuses_cpu_tensors():
         kv.kvarn_quantize_blocks(c, k, k, torch.zeros(1, dtype=torch.int32), 128,
                                  torch.zeros((1, 1), dtype=torch.int32),
                                  torch.zeros((1, 2, 15360), dtype=torch.uint8), k, k)
+
+
+def test_host_validation_fp16_cache():
+    # the FP16-cache baseline's calls check their arguments on the host too;
+    # every call here is invalid, so none reaches a launch
+    L = kv.lib()
+    P = ctypes.c_void_p
+    a16, mis = P(4096), P(4100)
+    wr = lambda **kw: L.kvarn_fp16_write_blocks(
+        kw.get("k", a16), kw.get("v", a16), kw.get("sb", 256 * 2 * 128), kw.get("st", 256),
+        kw.get("sh", 128), kw.get("batch", 1), kw.get("hkv", 2), kw.get("lens", a16),
+        kw.get("max_seq", 256), kw.get("table", a16), kw.get("max_blocks", 2),
+        kw.get("pool", a16), kw.get("num_pages", 2), None, None)
+    assert wr(k=None) == K.ERR_INVALID_ARG
+    assert wr(v=mis) == K.ERR_INVALID_ARG
+    assert wr(hkv=0) == K.ERR_INVALID_ARG
+    assert wr(st=100) == K.ERR_INVALID_ARG            # not a multiple of 8 elements
+    assert wr(max_blocks=1) == K.ERR_INVALID_ARG      # 256 tokens need 2 pages
+    assert wr(num_pages=0) == K.ERR_INVALID_ARG
+    assert wr(batch=0, k=None) == K.OK                # nothing to do
+    dec = lambda **kw: L.kvarn_fp16_decode_attention(
+        kw.get("q", a16), kw.get("hq", 8), kw.get("hkv", 2), kw.get("pool", a16), 40, a16,
+        kw.get("max_blocks", 40), a16, kw.get("batch", 1), kw.get("max_seq", 5000),
+        kw.get("scale", 0.088), kw.get("out", a16), kw.get("ws", None),
+        kw.get("ws_bytes", 0), None, None)
+    assert dec(hq=7) == K.ERR_INVALID_ARG             # not a multiple of hkv
+    assert dec(hq=18) == K.ERR_UNSUPPORTED            # groups above 8
+    assert dec(q=None) == K.ERR_INVALID_ARG
+    assert dec(out=mis) == K.ERR_INVALID_ARG
+    assert dec(max_blocks=39) == K.ERR_INVALID_ARG    # 5000 tokens need 40 pages
+    assert dec(scale=-1.0) == K.ERR_INVALID_ARG
+    need = kv.fp16_decode_workspace_bytes(8, 2, 1, 5000)
+    assert need > 0                                   # one long sequence is split
+    assert dec() == K.ERR_WORKSPACE
+    assert dec(ws=a16, ws_bytes=need - 1) == K.ERR_WORKSPACE
+    assert dec(batch=0) == K.OK
+    assert kv.fp16_decode_workspace_bytes(8, 3, 1, 5000) == 0      # bad group
