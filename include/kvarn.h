@@ -46,7 +46,10 @@
  * [B][num_kv_heads][128 slots][128] per K and V.
  *
  * Conventions for every call:
- *   - the library allocates nothing and keeps no state between calls; every
+ *   - the library allocates nothing and keeps no state between calls that
+ *     affects a result (it remembers, per device, launch settings it has
+ *     already applied; kvarn_decode_attention_noalloc's scratch is a fixed
+ *     array, see there); calls are safe from several host threads; every
  *     pointer is caller-owned DEVICE memory unless stated otherwise;
  *   - every call is asynchronous on `stream` (a cudaStream_t; NULL = legacy
  *     default stream) and never synchronises;
@@ -116,7 +119,8 @@ size_t kvarn_page_bytes(const kvarn_config_t *cfg);
  *   k, v        fp16 [B][S][Hkv][128], element (b,t,h,c) at
  *               b*stride_b + t*stride_t + h*stride_h + c; 16-byte aligned,
  *               strides multiples of 8 elements
- *   seq_lens    int32 [batch], tokens of each sequence (<= max_seq)
+ *   seq_lens    int32 [batch], tokens of each sequence (<= max_seq); k and v
+ *               must hold that many tokens (the library cannot see their size)
  *   max_seq     host upper bound on seq_lens, sizes the grid
  *   block_table int32 [batch][max_blocks]; block j of sequence b goes to page
  *               block_table[b*max_blocks + j]; needs max_blocks >= max_seq/128
