@@ -14,6 +14,16 @@ stand-ins for long-context LLM KV caches):
     exp(sigma_v * N(0,1));
   * queries N(0,1).
 Everything is drawn in fp32 and rounded to fp16.
+
+Shapes (WORKLOADS below), each after a setting the pages name:
+  * long sequences, because the KVarN page (blog.edumints.com) presents the
+    method for agents and long contexts (its feature list);
+  * GQA with several query heads per KV head ("KV Cache (Anahtar-Deger
+    Onbellegi)", yapayzekasozluk.tr, "Sik Sorulan Sorular");
+  * the Qwen2.5-1.5B KV geometry, 28 layers x 2 KV heads x 128, as in the KVTC
+    page's per-token KV example (trimsalonaandekust.nl);
+  * requests of mixed lengths on scattered pages, the case paged attention
+    serves (same glossary, "Paged Attention (vLLM)").
 """
 from __future__ import annotations
 
