@@ -152,6 +152,107 @@ def test_sinkhorn_rank_one_closed_form(oracle):
         assert np.abs(a - (np.log(u) + np.log(v.std()))).max() < 1e-12
 
 
+def _row_std(Z):
+    return Z.std(axis=1)
+
+
+@pytest.mark.parametrize("k", [1, 2, 3])
+def test_row_step_normalizes_rows_against_current_column_scales(oracle, k):
+    # The row step of iteration k+1 starts from the state (a_k, b_k) that k
+    # whole iterations leave and changes only a.  After it, every row of
+    # Z = Y exp(-a_{k+1}) exp(-b_k) must have centred std exactly 1: that is
+    # what normalizing a row means (KVarN page, "KVarN Nasil Calisir?", stage
+    # "Normalize Edilmis Onbellek"; rows first, centred population std).  A
+    # row step that ignored the current column scales would leave these rows
+    # at std(Y_t e^-b) / std(Y_t), not 1.
+    for x in (_tile(41), _tile(42, sigma=1.5, outliers=4, fac=30.0)):
+        Y = oracle.rotate_tile(x)
+        a_k, b_k, _ = oracle.sinkhorn(Y, k)
+        a_next, b_next, _ = oracle.sinkhorn(Y, k + 1)
+        assert np.abs(b_k).max() > 1e-3   # the column scales are not trivial
+        Z = Y * np.exp(-a_next)[:, None] * np.exp(-b_k)[None, :]
+        assert np.abs(_row_std(Z) - 1.0).max() < 1e-12
+        # ... and the column step that follows then gives unit column std
+        Z2 = Y * np.exp(-a_next)[:, None] * np.exp(-b_next)[None, :]
+        assert np.abs(Z2.std(axis=0) - 1.0).max() < 1e-12
+
+
+def test_sinkhorn_limit_has_equal_row_and_unit_column_stds(oracle):
+    # At the limit of the alternating normalization both steps are no-ops up
+    # to a common factor: columns of Z have std 1 and the rows all share one
+    # std (the common offset between r and c does not vanish for centred
+    # statistics).  Checked on Z rebuilt from the returned scales.
+    for x in (_tile(43), _tile(44, sigma=1.0, outliers=4, fac=25.0)):
+        Y = oracle.rotate_tile(x)
+        a, b, _ = oracle.sinkhorn(Y, 64)
+        Z = Y * np.exp(-a)[:, None] * np.exp(-b)[None, :]
+        rs = _row_std(Z)
+        assert np.abs(Z.std(axis=0) - 1.0).max() < 1e-12
+        assert (rs.max() - rs.min()) / rs.mean() < 1e-9
+        # and the rows are not already equal after the first iteration: the
+        # later row steps have work to do
+        a1, b1, _ = oracle.sinkhorn(Y, 1)
+        rs1 = _row_std(Y * np.exp(-a1)[:, None] * np.exp(-b1)[None, :])
+        assert (rs1.max() - rs1.min()) / rs1.mean() > 1e-3
+
+
+def test_sinkhorn_second_row_step_has_positive_spread(oracle):
+    # On a tile that is not separable the column step of iteration 1 unsettles
+    # the rows again, so the row step of iteration 2 moves them by different
+    # amounts (its spread of log sigma is > 0).
+    Y = oracle.rotate_tile(_tile(45, sigma=1.0, outliers=4, fac=30.0))
+    _, _, tr = oracle.sinkhorn(Y, 3)
+    assert tr[1, 1] > 1e-4 and tr[2, 1] > 0.0
+
+
+def _near_constant(n, c, rel, rng):
+    """n values c (1 + rel s_i), s_i = +-1 in equal numbers: centred variance
+    over mean square = rel^2 / (1 + rel^2)."""
+    s = np.array([1.0, -1.0] * (n // 2))
+    rng.shuffle(s)
+    return c * (1.0 + rel * s)
+
+
+def test_sinkhorn_skip_threshold_rows(oracle):
+    # The skip rule leaves a row alone only when its variance is at most
+    # 1e-10 of its mean square.  A row at var/msq ~ 1e-8 must be normalized
+    # (a_t = log of its std, as the first row step sees Y itself); one at
+    # ~ 1e-12 must be skipped (a_t stays exactly 0).
+    rng = np.random.default_rng(46)
+    Y = rng.standard_normal((128, 128)) * 2.0
+    Y[5] = _near_constant(128, 3.0, 1e-4, rng)    # var/msq ~ 1e-8: updated
+    Y[9] = _near_constant(128, -7.0, 1e-6, rng)   # var/msq ~ 1e-12: skipped
+    Y[17] = _near_constant(128, 2.0, 3e-5, rng)   # var/msq ~ 9e-10: updated
+    Y[23] = _near_constant(128, 1.5, 3e-6, rng)   # var/msq ~ 9e-12: skipped
+    a, _, _ = oracle.sinkhorn(Y, 1)
+    assert a[9] == 0.0 and a[23] == 0.0
+    for t in (5, 17):
+        assert abs(a[t] - np.log(Y[t].std())) < 1e-9
+        assert a[t] < -5.0
+
+
+def test_sinkhorn_skip_threshold_columns(oracle):
+    # Same rule for columns.  Every row is a permutation of one vector w
+    # outside columns 0..3, so the first row step scales all rows alike and
+    # leaves the near-constant columns near-constant: column 1 at var/msq
+    # ~ 1e-8 must get b = log of its std, columns 2 and 3 at ~ 1e-12 and
+    # ~ 9e-12 must keep b = 0.
+    rng = np.random.default_rng(47)
+    w = rng.standard_normal(124) * 3.0
+    Y = np.empty((128, 128))
+    for t in range(128):
+        Y[t, 4:] = np.roll(w, t)
+    Y[:, 0] = 5.0
+    Y[:, 1] = _near_constant(128, 4.0, 1e-4, rng)
+    Y[:, 2] = _near_constant(128, -6.0, 1e-6, rng)
+    Y[:, 3] = _near_constant(128, 2.5, 3e-6, rng)
+    a, b, _ = oracle.sinkhorn(Y, 1)
+    Z = Y * np.exp(-a)[:, None]
+    assert b[0] == 0.0 and b[2] == 0.0 and b[3] == 0.0
+    assert abs(b[1] - np.log(Z[:, 1].std())) < 1e-9
+    assert b[1] < -5.0
+
+
 def test_sinkhorn_zero_and_constant_tiles_are_skipped(oracle):
     a, b, _ = oracle.sinkhorn(np.zeros((128, 128)), 3)
     assert not a.any() and not b.any()
