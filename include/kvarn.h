@@ -147,7 +147,19 @@ int kvarn_append_token(const kvarn_config_t *cfg, const void *k_new, const void 
                        int max_blocks, void *pool, int64_t num_pages, void *tail_k,
                        void *tail_v, int32_t *status, kvarn_stream_t stream);
 
-/* Bytes of decode workspace for (batch, max_seq).  0 when no split is needed. */
+/* The split-K plan decode uses for (batch, max_seq) on a GPU with `num_sms`
+ * streaming multiprocessors (num_sms <= 0: the current device's count).  The
+ * pages of each (sequence, KV head) are cut into *nsplit runs of
+ * *pages_per_split pages, as many as keep the whole grid resident at once;
+ * *workspace_bytes is the decode workspace that plan needs (0: none).  Any
+ * output pointer may be NULL.  Host arithmetic only when num_sms > 0 (no CUDA
+ * call); KVARN_ERR_LAUNCH when num_sms <= 0 and no device answers. */
+int kvarn_decode_split_plan(const kvarn_config_t *cfg, int batch, int max_seq, int num_sms,
+                            int *pages_per_split, int *nsplit, size_t *workspace_bytes);
+
+/* Bytes of decode workspace for (batch, max_seq) on the current device: the
+ * plan above for that device's SM count.  0 when no split is needed, and 0
+ * when no CUDA device is current (nothing can launch then either). */
 size_t kvarn_decode_workspace_bytes(const kvarn_config_t *cfg, int batch, int max_seq);
 
 /* Decode attention for one new query token per sequence:
@@ -196,7 +208,12 @@ int kvarn_decode_attention(const kvarn_config_t *cfg, const void *q, const void 
  *     the need).  Allocates nothing and frees nothing.
  *   - The first call on each device looks up the array's device address with
  *     that device current; make that first call before any stream capture.
- *   - Every call shares the one array and clears its ticket counters itself;
+ *     The address is remembered per device and context: the first call after
+ *     a cudaDeviceReset looks it up again, so it too should come before any
+ *     stream capture.
+ *   - Every call shares the one array and clears its ticket counters itself
+ *     when its plan merges splits through them (a cudaMemsetAsync on
+ *     `stream`, which allocates nothing);
  *     calls whose executions overlap on the GPU race on it, so serialise them
  *     (one stream, or events between streams). */
 int kvarn_decode_attention_noalloc(const kvarn_config_t *cfg, const void *q, const void *pool,
@@ -239,7 +256,8 @@ int kvarn_fp16_write_blocks(const void *k, const void *v, int64_t stride_b, int6
                             int max_blocks, void *pool, int64_t num_pages, int32_t *status,
                             kvarn_stream_t stream);
 
-/* Bytes of workspace kvarn_fp16_decode_attention needs (0: none). */
+/* Bytes of workspace kvarn_fp16_decode_attention needs on the current device
+ * (0: none, or no CUDA device is current). */
 size_t kvarn_fp16_decode_workspace_bytes(int num_q_heads, int num_kv_heads, int batch,
                                          int max_seq);
 

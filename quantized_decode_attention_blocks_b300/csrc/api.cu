@@ -12,10 +12,31 @@ cudaError_t launch_decode_mma(const DecodeArgs& a, cudaStream_t s);
 bool decode_mma_supported(int g);
 int decode_mma_ctas_per_sm(int g);
 int decode_mma_warps();
+int decode_mma_max_cluster();
 
 static inline bool aligned16(const void* p) { return ((uintptr_t)p & 15u) == 0; }
 
-DecodePlan decode_plan(int batch, int hq, int hkv, int max_seq) {
+int device_sm_count() {
+  // one slot per device id 0-63; other ids query every time
+  static std::atomic<int> cache[64];
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+  if (dev >= 0 && dev < 64) {
+    const int c = cache[dev].load(std::memory_order_relaxed);
+    if (c > 0) return c;
+  }
+  int n = 0;
+  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
+    return 0;
+  if (dev >= 0 && dev < 64) cache[dev].store(n, std::memory_order_relaxed);
+  return n;
+}
+
+bool decode_uses_cluster(int g, int nsplit) {
+  return decode_mma_supported(g) && nsplit >= 2 && nsplit <= decode_mma_max_cluster();
+}
+
+DecodePlan decode_plan(int batch, int hq, int hkv, int max_seq, int num_sms) {
   DecodePlan p{};
   // Work unit = one page of one (sequence, KV head); the fp16 tail rides with
   // the split that holds the last page.  The number of splits per (sequence,
@@ -26,7 +47,7 @@ DecodePlan decode_plan(int batch, int hq, int hkv, int max_seq) {
   const bool mma = decode_mma_supported(g);
   const int64_t units = max_seq / kT > 0 ? (int64_t)max_seq / kT : 1;
   const int64_t groups = (int64_t)batch * hkv;
-  const int64_t slots = (int64_t)kNumSMs * (mma ? decode_mma_ctas_per_sm(g) : 4);
+  const int64_t slots = (int64_t)(num_sms > 0 ? num_sms : 1) * (mma ? decode_mma_ctas_per_sm(g) : 4);
   const int64_t min_pages = mma ? decode_mma_warps() : 2;
   int64_t ns = slots / groups;
   const int64_t ns_cap = (units + min_pages - 1) / min_pages;
@@ -169,10 +190,27 @@ int kvarn_append_token(const kvarn_config_t* cfg, const void* k_new, const void*
                                                                       : KVARN_ERR_LAUNCH;
 }
 
+int kvarn_decode_split_plan(const kvarn_config_t* cfg, int batch, int max_seq, int num_sms,
+                            int* pages_per_split, int* nsplit, size_t* workspace_bytes) {
+  const int rc = kvarn_config_validate(cfg);
+  if (rc != KVARN_OK) return rc;
+  if (batch <= 0 || max_seq < 0) return KVARN_ERR_INVALID_ARG;
+  if (num_sms <= 0) {
+    num_sms = device_sm_count();
+    if (num_sms <= 0) return KVARN_ERR_LAUNCH;
+  }
+  const DecodePlan p = decode_plan(batch, cfg->num_q_heads, cfg->num_kv_heads, max_seq, num_sms);
+  if (pages_per_split) *pages_per_split = p.pages_per_split;
+  if (nsplit) *nsplit = p.nsplit;
+  if (workspace_bytes) *workspace_bytes = p.part_bytes + p.count_bytes;
+  return KVARN_OK;
+}
+
 size_t kvarn_decode_workspace_bytes(const kvarn_config_t* cfg, int batch, int max_seq) {
-  if (kvarn_config_validate(cfg) != KVARN_OK || batch <= 0 || max_seq < 0) return 0;
-  const DecodePlan p = decode_plan(batch, cfg->num_q_heads, cfg->num_kv_heads, max_seq);
-  return p.part_bytes + p.count_bytes;
+  size_t bytes = 0;
+  if (kvarn_decode_split_plan(cfg, batch, max_seq, 0, nullptr, nullptr, &bytes) != KVARN_OK)
+    return 0;
+  return bytes;
 }
 
 int kvarn_decode_attention(const kvarn_config_t* cfg, const void* q, const void* pool,
@@ -192,7 +230,9 @@ int kvarn_decode_attention(const kvarn_config_t* cfg, const void* q, const void*
     return KVARN_ERR_INVALID_ARG;
   if (!(softmax_scale > 0.f) || softmax_scale != softmax_scale) return KVARN_ERR_INVALID_ARG;
   if (batch > 65535 || cfg->num_kv_heads > 65535) return KVARN_ERR_UNSUPPORTED;
-  const DecodePlan p = decode_plan(batch, cfg->num_q_heads, cfg->num_kv_heads, max_seq);
+  const int sms = device_sm_count();
+  if (sms <= 0) return KVARN_ERR_LAUNCH;
+  const DecodePlan p = decode_plan(batch, cfg->num_q_heads, cfg->num_kv_heads, max_seq, sms);
   if (p.nsplit > 1 && (!workspace || workspace_bytes < p.part_bytes + p.count_bytes))
     return KVARN_ERR_WORKSPACE;
   DecodeArgs a;
@@ -262,7 +302,9 @@ size_t kvarn_fp16_decode_workspace_bytes(int num_q_heads, int num_kv_heads, int 
   if (num_q_heads <= 0 || num_kv_heads <= 0 || num_q_heads % num_kv_heads || batch <= 0 ||
       max_seq < 0)
     return 0;
-  const DecodePlan p = fp16_decode_plan(batch, num_q_heads, num_kv_heads, max_seq);
+  const int sms = device_sm_count();
+  if (sms <= 0) return 0;
+  const DecodePlan p = fp16_decode_plan(batch, num_q_heads, num_kv_heads, max_seq, sms);
   return p.part_bytes + p.count_bytes;
 }
 
@@ -285,7 +327,9 @@ int kvarn_fp16_decode_attention(const void* q, int num_q_heads, int num_kv_heads
   if (!(softmax_scale > 0.f) || softmax_scale != softmax_scale) return KVARN_ERR_INVALID_ARG;
   if (batch > 65535 || num_kv_heads > 65535 || num_pages > 0x7fffffff)
     return KVARN_ERR_UNSUPPORTED;
-  const DecodePlan p = fp16_decode_plan(batch, num_q_heads, num_kv_heads, max_seq);
+  const int sms = device_sm_count();
+  if (sms <= 0) return KVARN_ERR_LAUNCH;
+  const DecodePlan p = fp16_decode_plan(batch, num_q_heads, num_kv_heads, max_seq, sms);
   if (p.nsplit > 1 && (!workspace || workspace_bytes < p.part_bytes + p.count_bytes))
     return KVARN_ERR_WORKSPACE;
   F16DecodeArgs a;

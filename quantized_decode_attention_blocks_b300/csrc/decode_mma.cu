@@ -837,7 +837,7 @@ cudaError_t launch_nt(const DecodeArgs& args, cudaStream_t s) {
   cudaError_t e = ensure_dynamic_smem(decode_mma_kernel<NT>, smem, smem_set);
   if (e != cudaSuccess) return e;
   DecodeArgs a = args;
-  a.cluster = a.nsplit >= 2 && a.nsplit <= kMaxClusterSplits;
+  a.cluster = decode_uses_cluster(a.g, a.nsplit);
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(a.nsplit, a.hkv, a.batch);
   cfg.blockDim = dim3(kThreads);
@@ -860,6 +860,8 @@ cudaError_t launch_nt(const DecodeArgs& args, cudaStream_t s) {
 bool decode_mma_supported(int g) { return g >= 1 && g <= 8; }
 
 int decode_mma_warps() { return kWarps; }
+
+int decode_mma_max_cluster() { return kMaxClusterSplits; }
 
 // Resident CTAs per SM, from the shared-memory footprint (228 KB per SM, 1 KB
 // reserved per CTA).  Host-only arithmetic: no CUDA call.

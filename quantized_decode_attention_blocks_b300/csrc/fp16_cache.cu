@@ -370,12 +370,12 @@ constexpr int kFSmemBytes = (int)sizeof(FSmem) + 1024;
 // Resident CTAs per SM of the decode kernel (shared memory bound).
 constexpr int kF16CtasPerSm = 233472 / (kFSmemBytes + 1024);
 
-DecodePlan fp16_decode_plan(int batch, int hq, int hkv, int max_seq) {
+DecodePlan fp16_decode_plan(int batch, int hq, int hkv, int max_seq, int num_sms) {
   DecodePlan p{};
   (void)hq;
   const int64_t units = max_seq > 0 ? ((int64_t)max_seq + kT - 1) / kT : 1;
   const int64_t groups = (int64_t)batch * hkv;
-  const int64_t slots = (int64_t)kNumSMs * kF16CtasPerSm;
+  const int64_t slots = (int64_t)(num_sms > 0 ? num_sms : 1) * kF16CtasPerSm;
   int64_t ns = slots / (groups > 0 ? groups : 1);
   const int64_t ns_cap = (units + 1) / 2;    // at least two pages per split
   if (ns > ns_cap) ns = ns_cap;

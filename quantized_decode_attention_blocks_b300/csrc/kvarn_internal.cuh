@@ -43,7 +43,11 @@ __host__ __device__ constexpr int v_token(int j, int h, int i) {
 }
 constexpr int kMaxG = 16;         // query heads per KV head supported
 constexpr int kMaxIters = 64;     // Sinkhorn iterations accepted
-constexpr int kNumSMs = 148;      // B300
+
+// Streaming multiprocessors of the current device, queried once per device
+// (cudaDevAttrMultiProcessorCount) and cached; 0 when no device answers.
+// Grids and split plans are sized from it, so they follow the actual chip.
+int device_sm_count();
 
 // 1 / sqrt(128), rounded to fp32.
 constexpr float kInvSqrt128 = 0.08838834764831845f;
@@ -124,7 +128,11 @@ struct DecodePlan {
   size_t part_bytes;   // partial-state region
   size_t count_bytes;  // ticket region
 };
-DecodePlan decode_plan(int batch, int hq, int hkv, int max_seq);
+// `num_sms`: streaming multiprocessors the plan fills (device_sm_count()).
+DecodePlan decode_plan(int batch, int hq, int hkv, int max_seq, int num_sms);
+// Whether the decode launch merges the splits of a (sequence, KV head) inside
+// a thread-block cluster (no workspace tickets are then read).
+bool decode_uses_cluster(int g, int nsplit);
 
 cudaError_t launch_quantize_blocks(const QuantizeArgs& a, cudaStream_t s);
 cudaError_t launch_append_token(const AppendArgs& a, cudaStream_t s);
@@ -169,7 +177,7 @@ struct F16DecodeArgs {
   int nsplit;
   int32_t* status;
 };
-DecodePlan fp16_decode_plan(int batch, int hq, int hkv, int max_seq);
+DecodePlan fp16_decode_plan(int batch, int hq, int hkv, int max_seq, int num_sms);
 cudaError_t launch_fp16_write(const F16WriteArgs& a, cudaStream_t s);
 cudaError_t launch_fp16_decode(const F16DecodeArgs& a, const void* pool, cudaStream_t s);
 

@@ -766,16 +766,14 @@ constexpr int kQSmemBytes = (int)sizeof(QSmem) + 1024;
 
 cudaError_t launch_tiles(const CUtensorMap& mk, const CUtensorMap& mv, const QTileArgs& qa,
                          cudaStream_t s) {
-  static bool attr_set = false;
-  if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(quantize_tc_kernel,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, kQSmemBytes);
-    if (e != cudaSuccess) return e;
-    attr_set = true;
-  }
+  static std::atomic<uint64_t> smem_set{0};
+  cudaError_t e = ensure_dynamic_smem(quantize_tc_kernel, kQSmemBytes, smem_set);
+  if (e != cudaSuccess) return e;
   if (qa.ntiles <= 0) return cudaSuccess;
+  const int sms = device_sm_count();
+  if (sms <= 0) return cudaErrorNoDevice;
   const int want = (qa.ntiles + kWG - 1) / kWG;
-  const int grid = want < kNumSMs ? want : kNumSMs;
+  const int grid = want < sms ? want : sms;
   quantize_tc_kernel<<<grid, kQThreads, kQSmemBytes, s>>>(mk, mv, qa);
   return cudaGetLastError();
 }

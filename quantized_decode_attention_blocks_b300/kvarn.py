@@ -62,6 +62,8 @@ SIGNATURES = {
                                    _I, _P, _L, _P, _P, _P, _P]),
     "kvarn_append_token": (_I, [ctypes.POINTER(Config), _P, _P, _P, _I, _P, _I, _P, _L, _P, _P,
                                 _P, _P]),
+    "kvarn_decode_split_plan": (_I, [ctypes.POINTER(Config), _I, _I, _I, ctypes.POINTER(_I),
+                                     ctypes.POINTER(_I), ctypes.POINTER(ctypes.c_size_t)]),
     "kvarn_decode_workspace_bytes": (ctypes.c_size_t, [ctypes.POINTER(Config), _I, _I]),
     "kvarn_decode_attention": (_I, [ctypes.POINTER(Config), _P, _P, _L, _P, _I, _P, _I, _I, _P,
                                     _P, ctypes.c_float, _P, _P, ctypes.c_size_t, _P, _P]),
@@ -223,6 +225,16 @@ def alloc_tails(cfg: Config, batch: int, device="cuda"):
     shape = (batch, cfg.num_kv_heads, BLOCK_TOKENS, HEAD_DIM)
     return (torch.zeros(shape, dtype=torch.float16, device=device),
             torch.zeros(shape, dtype=torch.float16, device=device))
+
+
+def decode_split_plan(cfg: Config, batch: int, max_seq: int, num_sms: int = 0):
+    """(pages_per_split, nsplit, workspace_bytes) of decode on a GPU with
+    `num_sms` SMs (0: the current device)."""
+    pps, ns, ws = _I(0), _I(0), ctypes.c_size_t(0)
+    _check(lib().kvarn_decode_split_plan(ctypes.byref(cfg), batch, max_seq, num_sms,
+                                         ctypes.byref(pps), ctypes.byref(ns), ctypes.byref(ws)),
+           "kvarn_decode_split_plan")
+    return pps.value, ns.value, ws.value
 
 
 def decode_workspace_bytes(cfg: Config, batch: int, max_seq: int) -> int:

@@ -69,14 +69,47 @@ def test_config_parsing():
     assert kv.page_bytes(c) == 0
 
 
+B300_SMS = 148
+
+
+def _ws(c, batch, max_seq, sms=B300_SMS):
+    return kv.decode_split_plan(c, batch, max_seq, sms)[2]
+
+
 def test_page_bytes_and_workspace_sizes():
     c = kv.config_from_string("k4v2_g128", 32, 8)
     assert kv.page_bytes(c) == 15360 == 120 * 128
-    assert kv.decode_workspace_bytes(c, 0, 100) == 0
-    small = kv.decode_workspace_bytes(c, 1, 200)
-    big = kv.decode_workspace_bytes(c, 16, 131072)
+    with pytest.raises(kv.KvarnError):
+        kv.decode_split_plan(c, 0, 100, B300_SMS)
+    small = _ws(c, 1, 200)
+    big = _ws(c, 16, 131072)
     assert big > small >= 0
     assert big % 256 == 0
+
+
+@pytest.mark.parametrize("sms", [148, 132, 160])
+@pytest.mark.parametrize("g", [1, 4, 6, 8, 12])
+def test_split_plan_fills_one_wave_and_covers_every_page(sms, g):
+    # The plan follows the SM count it is given: it cuts each (sequence, KV
+    # head) into at most as many splits as keep the whole grid resident (the
+    # tensor-core kernel fits 3 CTAs per SM for g <= 8, the CUDA-core one 4),
+    # covers every page, and leaves no split empty.
+    per_sm = 3 if g <= 8 else 4
+    for hkv in (1, 2, 8):
+        c = kv.config_from_string("k4v2_g128", g * hkv, hkv)
+        for batch in (1, 3, 16, 64, 1000):
+            for max_seq in (100, 128, 4097, 131072):
+                pps, ns, ws = kv.decode_split_plan(c, batch, max_seq, sms)
+                pages = max(max_seq // 128, 1)
+                assert pps * ns >= pages and pps * (ns - 1) < pages
+                assert ns == 1 or batch * hkv * ns <= sms * per_sm
+                assert (ws == 0) == (ns == 1)
+
+
+def test_split_plan_grows_with_the_sm_count():
+    c = kv.config_from_string("k4v2_g128", 32, 8)
+    n = [kv.decode_split_plan(c, 1, 131072, sms)[1] for sms in (74, 148, 296)]
+    assert n[0] < n[1] < n[2]
 
 
 @pytest.mark.parametrize("g", [1, 2, 4, 6, 8])
@@ -88,14 +121,14 @@ def test_noalloc_scratch_covers_every_group_up_to_eight(g):
         c = kv.config_from_string("k4v2_g128", g * hkv, hkv)
         for batch in (1, 3, 64, 1000, 65535):
             for max_seq in (128, 4097, 131072, 1 << 22):
-                need = kv.decode_workspace_bytes(c, batch, max_seq)
+                need = _ws(c, batch, max_seq)
                 assert need <= K.NOALLOC_SCRATCH_BYTES, (g, hkv, batch, max_seq, need)
 
 
 def test_no_workspace_when_the_batch_fills_the_gpu():
     # enough (sequence, KV head) pairs for one CTA each: no split, no partials
     c = kv.config_from_string("k4v2_g128", 32, 8)
-    assert kv.decode_workspace_bytes(c, 4096, 32768) == 0
+    assert _ws(c, 4096, 32768) == 0
 
 
 def test_status_strings():
@@ -152,10 +185,16 @@ def test_host_validation_append_and_decode():
     assert dec(out=P(4097)) == K.ERR_INVALID_ARG
     assert dec(scale=0.0) == K.ERR_INVALID_ARG
     assert dec(scale=float("nan")) == K.ERR_INVALID_ARG
-    need = kv.decode_workspace_bytes(c, 2, 512)
-    if need:
-        assert dec() == K.ERR_WORKSPACE
-        assert dec(ws=a16, ws_bytes=need - 1) == K.ERR_WORKSPACE
+    if torch.cuda.is_available():
+        need = kv.decode_workspace_bytes(c, 2, 512)
+        if need:
+            assert dec() == K.ERR_WORKSPACE
+            assert dec(ws=a16, ws_bytes=need - 1) == K.ERR_WORKSPACE
+    else:
+        # the split plan needs the device's SM count: with no device the call
+        # fails before anything could launch
+        assert kv.decode_workspace_bytes(c, 2, 512) == 0
+        assert dec() == K.ERR_LAUNCH
     assert dec(batch=0) == K.OK
     assert L.kvarn_dequantize_pages(a16, -1, a16, a16, None) == K.ERR_INVALID_ARG
     assert L.kvarn_dequantize_pages(None, 3, a16, a16, None) == K.ERR_INVALID_ARG
@@ -199,9 +238,13 @@ def test_host_validation_fp16_cache():
     assert dec(out=mis) == K.ERR_INVALID_ARG
     assert dec(max_blocks=39) == K.ERR_INVALID_ARG    # 5000 tokens need 40 pages
     assert dec(scale=-1.0) == K.ERR_INVALID_ARG
-    need = kv.fp16_decode_workspace_bytes(8, 2, 1, 5000)
-    assert need > 0                                   # one long sequence is split
-    assert dec() == K.ERR_WORKSPACE
-    assert dec(ws=a16, ws_bytes=need - 1) == K.ERR_WORKSPACE
+    if torch.cuda.is_available():
+        need = kv.fp16_decode_workspace_bytes(8, 2, 1, 5000)
+        assert need > 0                               # one long sequence is split
+        assert dec() == K.ERR_WORKSPACE
+        assert dec(ws=a16, ws_bytes=need - 1) == K.ERR_WORKSPACE
+    else:
+        assert kv.fp16_decode_workspace_bytes(8, 2, 1, 5000) == 0
+        assert dec() == K.ERR_LAUNCH                  # no device to plan for
     assert dec(batch=0) == K.OK
     assert kv.fp16_decode_workspace_bytes(8, 3, 1, 5000) == 0      # bad group

@@ -35,8 +35,11 @@ def _run(w, lens, table, num_pages, q=None, max_seq=None):
     return res, (cfg, q, pool, table, lens, tk, tv, out, ws, max_seq)
 
 
-@pytest.mark.parametrize("hq,hkv", [(1, 1), (8, 2), (12, 2), (8, 1), (16, 1), (32, 8)])
+@pytest.mark.parametrize("hq,hkv", [(1, 1), (4, 2), (6, 2), (8, 2), (10, 2), (12, 2), (14, 2),
+                                    (8, 1), (16, 1), (32, 8), (24, 8), (40, 8), (56, 8)])
 def test_group_sizes_and_ragged_lengths(hq, hkv):
+    # every GQA group the tensor-core kernel pads (g = 2, 3, 5, 6, 7 to 4 or 8
+    # query heads) next to the exact fits (1, 4, 8) and the CUDA-core g = 16
     lens = torch.tensor([0, 1, 127, 128, 129, 300, 1000, 2048], dtype=torch.int32)
     B = len(lens)
     w = synth.scaled(synth.WORKLOADS["llama3_8b_layer"], batch=B, seq=2048, hkv=hkv, hq=hq)

@@ -108,9 +108,9 @@ def test_single_layer_workload_full_size(name):
 
 
 def test_qwen_like_workload_layers_full_size():
-    """28 layers share one pool of pages scattered across it; the first and the
-    last layer are run at full size (the others differ only in their seed and
-    their slice of the pool)."""
+    """28 layers share one pool of pages scattered across it; the first, a
+    middle and the last layer are run at full size (the others differ only in
+    their seed and their slice of the pool)."""
     w = synth.WORKLOADS["qwen25_15b"]
     rng = np.random.default_rng(100 + w.seed)
     cfg = config(w.hq, w.hkv)
@@ -118,7 +118,7 @@ def test_qwen_like_workload_layers_full_size():
     pool = kv.alloc_pool(cfg, num_pages, DEV)
     lens = synth.seq_lens(w, device=DEV)
     stats = {}
-    for layer in (0, w.layers - 1):
+    for layer in (0, w.layers // 2 - 1, w.layers - 1):
         table = tables[layer].contiguous()
         k, v = synth.kv(w, layer=layer, device=DEV)
         tk, tv = kv.alloc_tails(cfg, w.batch, DEV)
@@ -151,6 +151,15 @@ def test_mixed_serving_full_size_with_appends():
     st = torch.zeros(1, dtype=torch.int32, device=DEV)
     max_seq = w.seq + w.decode_steps
     kv.kvarn_quantize_blocks(cfg, k, v, lens, w.seq, table, pool, tk, tv, st)
+    # decode is checked against the oracle on 8 requests at the first step, at
+    # the first step whose append fills a tail block (one of those requests
+    # is among the 8: it reads its fresh page and an empty tail) and at the
+    # last step
+    lens_h = host(lens).astype(np.int64)
+    fills = [(s, b) for s in range(1, w.decode_steps) for b in range(w.batch)
+             if (lens_h[b] + s) % 128 == 127]
+    s_fill, b_fill = fills[0]
+    checks = {0: None, s_fill: b_fill, w.decode_steps - 1: None}
     new = []
     cur = lens.clone()
     for step in range(w.decode_steps):
@@ -160,6 +169,16 @@ def test_mixed_serving_full_size_with_appends():
         cur = cur + 1
         q = synth.queries(w, step=step, device=DEV)
         out, st2 = _decode(cfg, q, pool, table, cur, max_seq, tk, tv)
+        if step in checks:
+            torch.cuda.synchronize()
+            assert int(st.item()) == 0 and int(st2.item()) == 0
+            must = checks[step]
+            pool_ids = [b for b in range(w.batch) if b != must]
+            seqs = rng.choice(pool_ids, size=8 if must is None else 7, replace=False).tolist()
+            if must is not None:
+                assert int(host(cur)[must]) % 128 == 0     # the block just filled
+                seqs.append(must)
+            _check_sampled_decode(cfg, q, out, pool, table, cur, tk, tv, sorted(seqs))
     torch.cuda.synchronize()
     assert int(st.item()) == 0 and int(st2.item()) == 0
     stats = {}
@@ -187,6 +206,3 @@ def test_mixed_serving_full_size_with_appends():
             filled += 1
     assert filled > 0
     parity.check_flip_rate(stats)
-    # the last step's decode on sampled requests
-    seqs = sorted(rng.choice(w.batch, size=3, replace=False).tolist())
-    _check_sampled_decode(cfg, q, out, pool, table, cur, tk, tv, seqs)

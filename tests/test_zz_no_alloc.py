@@ -5,7 +5,8 @@ inference engines), or cannot afford the device synchronisation of cudaMalloc
 in their serving loop, so they cannot provide the split-K workspace that
 kvarn_decode_attention takes.  kvarn_decode_attention_noalloc keeps that
 scratch in a fixed array inside the library.  These tests call it through the
-C ABI and hold it to the output of kvarn_decode_attention, call after call.
+C ABI and hold it to the float64 oracle and to the output of
+kvarn_decode_attention, call after call.
 This file is collected last so that a run stopping at its first failure has
 already run every other test.
 """
@@ -27,38 +28,45 @@ def test_noalloc_rejects_requests_beyond_its_scratch():
     # one sequence of 131072 tokens with 16 query heads per KV head is split
     # into so many parts that its partial states need more than the built-in
     # scratch; the call must say so before touching the GPU (the pointers are
-    # never used)
+    # never used).  Without a GPU the call cannot plan and says that instead.
     cfg = kv.config_from_string("k4v2_g128", 16, 1)
-    need = kv.decode_workspace_bytes(cfg, 1, 131072)
+    need = kv.decode_split_plan(cfg, 1, 131072, 148)[2]
     assert need > K.NOALLOC_SCRATCH_BYTES
     fake = ctypes.c_void_p(4096)
     rc = kv.lib().kvarn_decode_attention_noalloc(
         ctypes.byref(cfg), fake, fake, 1 << 20, fake, 1024, fake, 1, 131072, fake, fake,
         ctypes.c_float(128 ** -0.5), fake, None, None)
-    assert rc == K.ERR_WORKSPACE
+    assert rc == (K.ERR_WORKSPACE if torch.cuda.is_available() else K.ERR_LAUNCH)
 
 
-@pytest.mark.gpu
-def test_noalloc_matches_workspace_entry_point_twice():
-    from tests.gpu_helpers import DEV, config, prefill
+def _noalloc_twice(lens, max_seq, hkv, hq, seed):
+    """Prefills a seeded cache, then calls the no-alloc decode twice through
+    the C ABI and checks both outputs against the float64 oracle (fed the
+    GPU's own pool) and against kvarn_decode_attention."""
+    from oracle import kvref
+    from tests import parity
+    from tests.gpu_helpers import DEV, config, host, prefill
     from workloads import synth
-    # long sequences so that decode splits every sequence many ways and the
-    # scratch (partial softmax states and tickets) is really used
-    lens = torch.tensor([20000, 13000, 300], dtype=torch.int32)
-    w = synth.scaled(synth.WORKLOADS["long_context"], batch=3, seq=20000, hkv=2, hq=8)
-    k, v = synth.kv(w, device=DEV)
+    B = len(lens)
+    lens = torch.tensor(lens, dtype=torch.int32)
+    w = synth.scaled(synth.WORKLOADS["long_context"], batch=B, seq=max_seq, hkv=hkv, hq=hq)
+    k, v = synth.kv(w, layer=seed, device=DEV)
     cfg = config(w.hq, w.hkv)
-    mb = 157
-    g = torch.Generator().manual_seed(7)
-    table = torch.randperm(3 * mb, generator=g).to(torch.int32).reshape(3, mb)
-    pool, tk, tv, st = prefill(cfg, k, v, lens, table, 3 * mb, max_seq=20000)
+    mb = (max_seq + 127) // 128
+    g = torch.Generator().manual_seed(seed)
+    table = torch.randperm(B * mb, generator=g).to(torch.int32).reshape(B, mb)
+    pool, tk, tv, st = prefill(cfg, k, v, lens, table, B * mb, max_seq=max_seq)
     q = synth.queries(w).to(DEV)
     tdev, ldev = table.to(DEV), lens.to(DEV)
-    assert kv.decode_workspace_bytes(cfg, 3, 20000) > 0
+    plan = kv.decode_split_plan(cfg, B, max_seq)
 
-    ref = torch.empty((3, w.hq, 128), dtype=torch.float16, device=DEV)
-    ws = kv.alloc_decode_workspace(cfg, 3, 20000, DEV)
-    kv.kvarn_decode_attention(cfg, q, pool, tdev, ldev, 20000, tk, tv, ref, ws, status=st)
+    ref = torch.empty((B, w.hq, 128), dtype=torch.float16, device=DEV)
+    ws = kv.alloc_decode_workspace(cfg, B, max_seq, DEV)
+    kv.kvarn_decode_attention(cfg, q, pool, tdev, ldev, max_seq, tk, tv, ref, ws, status=st)
+    torch.cuda.synchronize()
+    want_oracle = kvref.decode_attention(host(q), host(pool), host(table), host(lens), host(tk),
+                                         host(tv), w.hq, w.hkv)
+    want_cuda = ref.float().cpu().numpy().astype(np.float64)
 
     L = kv.lib()
     status = torch.zeros(1, dtype=torch.int32, device=DEV)
@@ -67,13 +75,30 @@ def test_noalloc_matches_workspace_entry_point_twice():
         out = torch.full_like(ref, float("nan"))
         rc = L.kvarn_decode_attention_noalloc(
             ctypes.byref(cfg), _ptr(q), _ptr(pool), pool.shape[0], _ptr(tdev), mb, _ptr(ldev),
-            3, 20000, _ptr(tk), _ptr(tv), ctypes.c_float(128 ** -0.5), _ptr(out), _ptr(status),
-            stream)
+            B, max_seq, _ptr(tk), _ptr(tv), ctypes.c_float(128 ** -0.5), _ptr(out),
+            _ptr(status), stream)
         assert rc == K.OK, kv.status_string(rc)
         torch.cuda.synchronize()
         assert int(status.item()) == 0 and int(st.item()) == 0
         got = out.float().cpu().numpy().astype(np.float64)
-        want = ref.float().cpu().numpy().astype(np.float64)
         assert np.isfinite(got).all(), f"call {call}: non-finite output"
-        err = np.abs(got - want)
-        assert np.all(err <= 2e-3 + 1e-3 * np.abs(want)), f"call {call}: max err {err.max()}"
+        parity.compare_attention(got, want_oracle)
+        err = np.abs(got - want_cuda)
+        assert np.all(err <= 2e-3 + 1e-3 * np.abs(want_cuda)), f"call {call}: max err {err.max()}"
+    return plan
+
+
+@pytest.mark.gpu
+def test_noalloc_matches_oracle_twice_with_ticket_merge():
+    # long sequences: decode splits every sequence more than four ways, so the
+    # scratch holds partial softmax states and the arrival tickets
+    plan = _noalloc_twice([20000, 13000, 300], 20000, hkv=2, hq=8, seed=7)
+    assert plan[1] > 4 and plan[2] > 0
+
+
+@pytest.mark.gpu
+def test_noalloc_matches_oracle_twice_with_cluster_merge():
+    # 16 sequences x 8 KV heads of 1536 tokens: 2 to 4 splits per (sequence,
+    # KV head), merged inside a thread-block cluster (no tickets are read)
+    plan = _noalloc_twice([1536] * 12 + [1400, 1290, 700, 5], 1536, hkv=8, hq=32, seed=11)
+    assert 2 <= plan[1] <= 4
