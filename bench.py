@@ -5,16 +5,18 @@ One step = the whole path over one batch of the workload:
   -> kvarn_append_token (one new token per sequence)
   -> kvarn_decode_attention (one query token per sequence over pages + tail).
 
-Default workload: the Llama-3-8B-like layer (8 KV heads, 32 query heads,
-batch 16 x 4096 tokens, head_dim 128), synthetic seeded data.
+Default workload: the Qwen2.5-1.5B-like KV shape, the largest one-GPU
+configuration: 28 layers, 2 KV heads, 12 query heads, batch 64 x 8192 tokens,
+head_dim 128, every layer's pages scattered over one shared pool; synthetic
+seeded data.  A step runs the three calls on every layer.
 
-Timing: each kernel is launched K times back to back (captured in one CUDA
-graph, replayed behind a GPU spin so that submission never idles the GPU)
-between two CUDA events on the launching stream, rotating over enough replicas of the workload (own
-inputs, pools and tails) that the kernel's working set is over 2.5x the 126 MB
-L2, so no launch finds its inputs in L2.  ms_per_step = sum of the three
-kernels' mean device times; value = algorithmic bytes of the step /
-ms_per_step (GB/s).  ops.*.us_cold is one launch after a clean L2 flush (a
+Timing: each kernel's launches for K steps run back to back (captured in one
+CUDA graph, replayed behind a GPU spin so that submission never idles the GPU)
+between two CUDA events on the launching stream.  Consecutive launches work on
+different layers (one-layer workloads: on replicas with their own inputs and
+pools, over 2.5x the 126 MB L2 in all), so no launch finds its inputs in L2.
+ms_per_step = sum of the three kernels' time per step; value = algorithmic
+bytes of the step / ms_per_step (GB/s).  ops.*.us_cold is one launch after a clean L2 flush (a
 512 MB write, then a 256 MB read so the write-back happens before the timed
 launch), which adds the launch latency and ramp-up of a lone kernel.
 
@@ -166,29 +168,30 @@ def summarize_clock_lines(lines):
 
 # ----------------------------------------------------------- GPU workload --
 
-class Job:
-    """Device-resident inputs and state of one replica of the workload."""
+class Unit:
+    """Device-resident inputs and state of one layer of the workload (or of one
+    replica of a one-layer workload): its fp16 K, V, lengths, block table,
+    tails, new token, query, output and decode workspace.  `pool` and `pool16`
+    may be shared with other units (the layers of one model share one pool)."""
 
-    def __init__(self, w, dev, seed_offset=0):
+    def __init__(self, w, dev, cfg, layer, table, pool, pool16, num_pages):
         import quantized_decode_attention_blocks_b300 as kv
         self.kv = kv
         self.w = w
-        self.dev = dev
-        if seed_offset:
-            w = synth.scaled(w, seed=w.seed + 1000 * seed_offset)
-        self.cfg = kv.config_from_string("k4v2_g128", w.hq, w.hkv)
-        self.k, self.v = synth.kv(w, device=dev)
+        self.cfg = cfg
+        self.layer = layer
+        self.k, self.v = synth.kv(w, layer=layer, device=dev)
         self.lens = synth.seq_lens(w, device=dev)
-        tables, self.num_pages = synth.block_tables(w, device=dev)
-        self.table = tables[0].contiguous()
+        self.table = table.contiguous()
+        self.num_pages = num_pages
         self.max_seq = w.seq
-        self.pool = kv.alloc_pool(self.cfg, self.num_pages, dev)
-        self.tk, self.tv = kv.alloc_tails(self.cfg, w.batch, dev)
-        self.kn, self.vn = synth.new_tokens(w, 0, device=dev)
-        self.q = synth.queries(w, device=dev)
+        self.pool = pool
+        self.tk, self.tv = kv.alloc_tails(cfg, w.batch, dev)
+        self.kn, self.vn = synth.new_tokens(w, 0, layer=layer, device=dev)
+        self.q = synth.queries(w, layer=layer, device=dev)
         self.out = torch.empty((w.batch, w.hq, D), dtype=torch.float16, device=dev)
         self.lens1 = self.lens + 1
-        self.ws = kv.alloc_decode_workspace(self.cfg, w.batch, self.max_seq + 1, dev)
+        self.ws = kv.alloc_decode_workspace(cfg, w.batch, self.max_seq + 1, dev)
         self.status = torch.zeros(1, dtype=torch.int32, device=dev)
         lens = self.lens.cpu().numpy().astype(np.int64)
         nfull = lens // T
@@ -206,7 +209,7 @@ class Job:
         self.kv_tokens = int(lens1.sum())
         # the FP16 paged cache of the same tokens (the baseline the quantized
         # cache is compared with): every prefill token as fp16, no tail
-        self.pool16 = kv.alloc_fp16_pool(w.hkv, self.num_pages, dev)
+        self.pool16 = pool16
         kv.kvarn_fp16_write_blocks(self.k, self.v, self.lens, self.max_seq, self.table,
                                    self.pool16, self.status)
         self.ws16 = kv.alloc_fp16_decode_workspace(w.hq, w.hkv, w.batch, self.max_seq, dev)
@@ -231,6 +234,36 @@ class Job:
         self.kv.kvarn_decode_attention(self.cfg, self.q, self.pool, self.table, self.lens1,
                                        self.max_seq + 1, self.tk, self.tv, self.out, self.ws,
                                        status=self.status)
+
+
+def build_units(w, dev, rank):
+    """The units one step runs, and the units the timed launches rotate over.
+
+    A model with several layers: one unit per layer, every layer's pages in
+    one shared pool (each layer's table a slice of it); a step runs every
+    layer once, and no two launches of a kernel in a row touch the same data.
+    A one-layer workload: one unit per step, rotated over enough replicas (own
+    inputs and pools) that a kernel's working set over them is above 2.5 x L2.
+    Returns (units, units_per_step)."""
+    import quantized_decode_attention_blocks_b300 as kv
+    if rank:
+        w = synth.scaled(w, seed=w.seed + 1000 * 16 * rank)
+    cfg = kv.config_from_string("k4v2_g128", w.hq, w.hkv)
+
+    def one_model(wm):
+        tables, num_pages = synth.block_tables(wm, device=dev)
+        pool = kv.alloc_pool(cfg, num_pages, dev)
+        pool16 = kv.alloc_fp16_pool(wm.hkv, num_pages, dev)
+        return [Unit(wm, dev, cfg, layer, tables[layer], pool, pool16, num_pages)
+                for layer in range(wm.layers)]
+
+    units = one_model(w)
+    if w.layers > 1:
+        return units, w.layers
+    nrep = max(2, min(8, -(-int(2.5 * L2_BYTES) // max(units[0].bytes_decode, 1))))
+    for i in range(1, nrep):
+        units += one_model(synth.scaled(w, seed=w.seed + 1000 * i))
+    return units, 1
 
 
 def max_over_ranks(values, device):
@@ -260,32 +293,50 @@ def clean_flush(flush, flush_rd):
     flush_rd.sum()
 
 
+def check_status(units):
+    for u in units:
+        st = int(u.status.item())
+        if st != 0:
+            raise RuntimeError(f"device status {st}: {u.kv.status_string(st)}")
+
+
+def time_graph(fn, n, stream):
+    """Captures n calls of fn(i) in one CUDA graph and replays it between two
+    CUDA events on `stream`, behind a GPU spin so that submission never idles
+    the GPU; returns milliseconds for the n calls."""
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        for i in range(n):
+            fn(i)
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    torch.cuda._sleep(SPIN_CYCLES)
+    e0.record(stream)
+    g.replay()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    return e0.elapsed_time(e1)
+
+
 def run_gpu(args, rank, world):
     dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0)))
     torch.cuda.set_device(dev)
     w = synth.WORKLOADS[args.workload]
-    job = Job(w, dev, seed_offset=16 * rank)
-    # replicas with their own inputs and pools, so that consecutive launches
-    # of one kernel never find their inputs in L2 (working set > 2.5 x L2)
-    nrep = max(2, min(8, -(-int(2.5 * L2_BYTES) // max(job.bytes_decode, 1))))
-    jobs = [job] + [Job(w, dev, seed_offset=16 * rank + i) for i in range(1, nrep)]
+    units, per_step = build_units(w, dev, rank)
+    nu = len(units)
     stream = torch.cuda.current_stream()
     flush = torch.empty(512 * 1024 * 1024, dtype=torch.uint8, device=dev)
     flush_rd = torch.zeros(256 * 1024 * 1024 // 4, dtype=torch.float32, device=dev)
     names = ["quantize", "append", "decode"]
-
-    def op(name, j):
-        getattr(j, name)()
+    n_launch = args.steps * per_step            # launches of each kernel in the region
 
     for _ in range(args.warmup):
         for name in names:
-            for j in jobs:
-                op(name, j)
+            for u in units:
+                getattr(u, name)()
     torch.cuda.synchronize()
-    for j in jobs:
-        if int(j.status.item()) != 0:
-            raise RuntimeError(f"device status {j.status.item()}: "
-                               f"{j.kv.status_string(int(j.status.item()))}")
+    check_status(units)
     sampler = ClockSampler(dev.index)
     if rank == 0:
         sampler.start()
@@ -294,38 +345,30 @@ def run_gpu(args, rank, world):
     torch.cuda.synchronize()
     sampler.mark("t_start")
     t0 = time.perf_counter()
-    # steady state: K back-to-back launches of each kernel over the replicas,
-    # captured once in a CUDA graph so that host launch overhead never leaves
-    # the GPU idle between them; a spin kernel ahead of the start event keeps
-    # the GPU busy while the replay is submitted
-    ev = {}
-    graphs = {}
+    # steady state: K steps' launches of each kernel back to back (one CUDA
+    # graph per kernel), rotating over the units
+    ms = {}
     for name in names:
-        g = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(g):
-            for i in range(args.steps):
-                op(name, jobs[i % nrep])
-        graphs[name] = g
-    torch.cuda.synchronize()
-    for name in names:
-        e0 = torch.cuda.Event(enable_timing=True)
-        e1 = torch.cuda.Event(enable_timing=True)
-        torch.cuda._sleep(SPIN_CYCLES)
-        e0.record(stream)
-        graphs[name].replay()
-        e1.record(stream)
-        ev[name] = (e0, e1)
-    torch.cuda.synchronize()
+        ms[name] = time_graph(lambda i, name=name: getattr(units[i % nu], name)(), n_launch,
+                              stream) / args.steps
     wall = time.perf_counter() - t0
     sampler.mark("t_stop")
     if world > 1:
         torch.distributed.barrier()
     clocks = sampler.stop() if rank == 0 else None
-    ms = {name: ev[name][0].elapsed_time(ev[name][1]) / args.steps for name in names}
     ms_step = sum(ms.values())
     if world > 1:
         ms_step, ms["quantize"], ms["append"], ms["decode"] = max_over_ranks(
             [ms_step, ms["quantize"], ms["append"], ms["decode"]], dev)
+
+    # the step as one sequence per layer (quantize -> append -> decode), for
+    # reference: decode may then find some of the fresh pages in L2
+    def fused(i):
+        u = units[i % nu]
+        u.quantize()
+        u.append()
+        u.decode()
+    ms_fused = time_graph(fused, n_launch, stream) / args.steps
 
     # cold single launches (clean L2 flush before each), for reference
     cold = {name: [] for name in names}
@@ -335,7 +378,7 @@ def run_gpu(args, rank, world):
             e0 = torch.cuda.Event(enable_timing=True)
             e1 = torch.cuda.Event(enable_timing=True)
             e0.record(stream)
-            op(name, job)
+            getattr(units[0], name)()
             e1.record(stream)
             cold[name].append((e0, e1))
     torch.cuda.synchronize()
@@ -343,66 +386,57 @@ def run_gpu(args, rank, world):
 
     # the FP16 baseline's decode over the same tokens, timed the same way
     # (outside the step: a comparison, not part of the path)
-    g16 = torch.cuda.CUDAGraph()
-    with torch.cuda.graph(g16):
-        for i in range(args.steps):
-            jobs[i % nrep].decode_fp16()
-    torch.cuda.synchronize()
-    e0 = torch.cuda.Event(enable_timing=True)
-    e1 = torch.cuda.Event(enable_timing=True)
-    torch.cuda._sleep(SPIN_CYCLES)
-    e0.record(stream)
-    g16.replay()
-    e1.record(stream)
-    torch.cuda.synchronize()
-    ms["decode_fp16"] = e0.elapsed_time(e1) / args.steps
-    for j in jobs:
-        if int(j.status.item()) != 0:
-            raise RuntimeError(f"device status {j.status.item()}: "
-                               f"{j.kv.status_string(int(j.status.item()))}")
+    ms["decode_fp16"] = time_graph(lambda i: units[i % nu].decode_fp16(), n_launch,
+                                   stream) / args.steps
+    check_status(units)
 
     # end to end through the public API: host buffers, copies inside the region
-    e2e = measure_e2e(job, args, stream)
-    return job, ms, ms_step, wall, clocks, e2e, ms_cold, nrep
+    e2e = measure_e2e(units[:per_step], args, stream)
+    return units[:per_step], ms, ms_step, ms_fused, wall, clocks, e2e, ms_cold, nu
 
 
-def measure_e2e(job, args, stream):
-    kh = job.k.cpu().pin_memory()
-    vh = job.v.cpu().pin_memory()
-    knh = job.kn.cpu().pin_memory()
-    vnh = job.vn.cpu().pin_memory()
-    qh = job.q.cpu().pin_memory()
-    outh = torch.empty(job.out.shape, dtype=torch.float16).pin_memory()
-    kd = torch.empty_like(job.k)
-    vd = torch.empty_like(job.v)
+def measure_e2e(step_units, args, stream):
+    """One step through the Python API from pinned host memory: per layer the
+    H2D copies of K, V, the new token and the query, the three calls, and the
+    D2H copy of the output, all inside the timed region."""
+    host = []
+    for u in step_units:
+        host.append({"k": u.k.cpu().pin_memory(), "v": u.v.cpu().pin_memory(),
+                     "kn": u.kn.cpu().pin_memory(), "vn": u.vn.cpu().pin_memory(),
+                     "q": u.q.cpu().pin_memory(),
+                     "out": torch.empty(u.out.shape, dtype=torch.float16).pin_memory()})
+    kd = torch.empty_like(step_units[0].k)
+    vd = torch.empty_like(step_units[0].v)
 
     def step():
-        kd.copy_(kh, non_blocking=True)
-        vd.copy_(vh, non_blocking=True)
-        job.kn.copy_(knh, non_blocking=True)
-        job.vn.copy_(vnh, non_blocking=True)
-        job.q.copy_(qh, non_blocking=True)
-        job.kv.kvarn_quantize_blocks(job.cfg, kd, vd, job.lens, job.max_seq, job.table, job.pool,
-                                     job.tk, job.tv, job.status)
-        job.append()
-        job.decode()
-        outh.copy_(job.out, non_blocking=True)
+        for u, h in zip(step_units, host):
+            kd.copy_(h["k"], non_blocking=True)
+            vd.copy_(h["v"], non_blocking=True)
+            u.kn.copy_(h["kn"], non_blocking=True)
+            u.vn.copy_(h["vn"], non_blocking=True)
+            u.q.copy_(h["q"], non_blocking=True)
+            u.kv.kvarn_quantize_blocks(u.cfg, kd, vd, u.lens, u.max_seq, u.table, u.pool,
+                                       u.tk, u.tv, u.status)
+            u.append()
+            u.decode()
+            h["out"].copy_(u.out, non_blocking=True)
 
-    for _ in range(max(1, args.warmup)):
+    for _ in range(max(1, min(args.warmup, 2))):
         step()
     torch.cuda.synchronize()
     e0 = torch.cuda.Event(enable_timing=True)
     e1 = torch.cuda.Event(enable_timing=True)
-    n = max(1, min(args.steps, 5))
+    n = max(1, min(args.steps, 3))
     e0.record(stream)
     for _ in range(n):
         step()
     e1.record(stream)
     torch.cuda.synchronize()
     ms = e0.elapsed_time(e1) / n
-    h2d = (kh.numel() + vh.numel() + knh.numel() + vnh.numel() + qh.numel()) * 2
-    d2h = outh.numel() * 2
-    total = job.bytes_quantize + job.bytes_append + job.bytes_decode
+    h2d = sum((h["k"].numel() + h["v"].numel() + h["kn"].numel() + h["vn"].numel()
+               + h["q"].numel()) * 2 for h in host)
+    d2h = sum(h["out"].numel() * 2 for h in host)
+    total = sum(u.bytes_quantize + u.bytes_append + u.bytes_decode for u in step_units)
     return {"value": total / (ms * 1e-3) / 1e9, "unit": "GB/s", "ms_per_step": ms,
             "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h)}
 
@@ -476,7 +510,7 @@ def main():
     ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", default="kvarn", choices=["kvarn", "reference"])
-    ap.add_argument("--workload", default="llama3_8b_layer", choices=sorted(synth.WORKLOADS))
+    ap.add_argument("--workload", default="qwen25_15b", choices=sorted(synth.WORKLOADS))
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()
     if args.warmup < 3:
@@ -489,63 +523,77 @@ def main():
         return 0
     if world > 1:
         torch.distributed.init_process_group("nccl")
-    job, ms, ms_step, wall, clocks, e2e, ms_cold, nrep = run_gpu(args, rank, world)
+    units, ms, ms_step, ms_fused, wall, clocks, e2e, ms_cold, nu = run_gpu(args, rank, world)
     if world > 1:
         torch.distributed.destroy_process_group()
     if rank != 0:
         return 0
-    w = job.w
+    w = units[0].w
+    L = len(units)                      # launches of each kernel per step
     peak, peak_kind = measured_peaks()
-    step_bytes = job.bytes_quantize + job.bytes_append + job.bytes_decode
+    bq = sum(u.bytes_quantize for u in units)
+    ba = sum(u.bytes_append for u in units)
+    bd = sum(u.bytes_decode for u in units)
+    bd16 = sum(u.bytes_decode_fp16 for u in units)
+    kv_tokens = sum(u.kv_tokens for u in units)
+    step_bytes = bq + ba + bd
     value = whole_job_gbs(world, step_bytes, ms_step)
-    q_gbs = job.bytes_quantize / (ms["quantize"] * 1e-3) / 1e9
-    d_gbs = job.bytes_decode / (ms["decode"] * 1e-3) / 1e9
-    a_gbs = job.bytes_append / (ms["append"] * 1e-3) / 1e9
-    f16_gbs = job.bytes_decode_fp16 / (ms["decode_fp16"] * 1e-3) / 1e9
+    q_gbs = bq / (ms["quantize"] * 1e-3) / 1e9
+    d_gbs = bd / (ms["decode"] * 1e-3) / 1e9
+    a_gbs = ba / (ms["append"] * 1e-3) / 1e9
+    f16_gbs = bd16 / (ms["decode_fp16"] * 1e-3) / 1e9
     dom = "quantize" if ms["quantize"] >= ms["decode"] else "decode"
     dom_gbs = q_gbs if dom == "quantize" else d_gbs
-    dom_bytes = job.bytes_quantize if dom == "quantize" else job.bytes_decode
     traffic_q = ncu_traffic("quantize_tc_kernel", "quantize_tc.cu")
     traffic_d = ncu_traffic("decode_mma_kernel", "decode_mma.cu")
+    per_launch = {k: ms[k] / L * 1e3 for k in ms}
     line = {
         "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
         "data": "synthetic",
-        "config": {"workload": w.name, "batch": w.batch, "seq_len": w.seq, "kv_heads": w.hkv,
-                   "q_heads": w.hq, "head_dim": D, "format": "kvarn_k4v2_g128",
-                   "sinkhorn_iters": job.cfg.sinkhorn_iters, "parallelism": f"replicas{world}",
-                   "l2": f"inputs larger than L2: {nrep} replicas rotated, each kernel's "
-                         f"working set {nrep} x its per-launch bytes",
-                   "timing": "per kernel: K back-to-back launches (one CUDA graph) between two "
+        "config": {"workload": w.name, "layers": w.layers, "batch": w.batch, "seq_len": w.seq,
+                   "kv_heads": w.hkv, "q_heads": w.hq, "head_dim": D,
+                   "format": "kvarn_k4v2_g128", "sinkhorn_iters": units[0].cfg.sinkhorn_iters,
+                   "parallelism": f"replicas{world}",
+                   "l2": (f"inputs larger than L2: each launch of a kernel works on another "
+                          f"layer's data ({nu} units rotated, "
+                          f"{bq // L / 1e6:.0f} MB quantized per launch)"),
+                   "timing": "per kernel: K steps of launches (one CUDA graph) between two "
                              "CUDA events on the launching stream; ms_per_step = sum over the "
-                             "three kernels"},
+                             "three kernels of their time per step"},
         "ops": {
-            "quantize": {"us": ms["quantize"] * 1e3, "gbs": q_gbs, "frac_of_hbm": q_gbs / peak,
-                         "bytes": job.bytes_quantize, "us_cold": ms_cold["quantize"] * 1e3},
-            "append": {"us": ms["append"] * 1e3, "gbs": a_gbs, "bytes": job.bytes_append,
-                       "us_cold": ms_cold["append"] * 1e3},
-            "decode": {"us": ms["decode"] * 1e3, "gbs": d_gbs, "frac_of_hbm": d_gbs / peak,
-                       "us_cold": ms_cold["decode"] * 1e3,
-                       "bytes": job.bytes_decode,
+            "quantize": {"us_per_step": ms["quantize"] * 1e3, "us_per_launch": per_launch["quantize"],
+                         "gbs": q_gbs, "frac_of_hbm": q_gbs / peak, "bytes_per_step": bq,
+                         "us_cold": ms_cold["quantize"] * 1e3},
+            "append": {"us_per_step": ms["append"] * 1e3, "us_per_launch": per_launch["append"],
+                       "gbs": a_gbs, "bytes_per_step": ba, "us_cold": ms_cold["append"] * 1e3},
+            "decode": {"us_per_step": ms["decode"] * 1e3, "us_per_launch": per_launch["decode"],
+                       "gbs": d_gbs, "frac_of_hbm": d_gbs / peak,
+                       "us_cold": ms_cold["decode"] * 1e3, "bytes_per_step": bd,
                        "tokens_per_s": w.batch / (ms["decode"] * 1e-3),
-                       "kv_tokens_scanned_per_s": job.kv_tokens / (ms["decode"] * 1e-3)},
-            "decode_fp16": {"us": ms["decode_fp16"] * 1e3, "gbs": f16_gbs,
-                            "frac_of_hbm": f16_gbs / peak, "bytes": job.bytes_decode_fp16,
+                       "kv_tokens_scanned_per_s": kv_tokens / (ms["decode"] * 1e-3)},
+            "decode_fp16": {"us_per_step": ms["decode_fp16"] * 1e3,
+                            "us_per_launch": per_launch["decode_fp16"], "gbs": f16_gbs,
+                            "frac_of_hbm": f16_gbs / peak, "bytes_per_step": bd16,
                             "note": "baseline: the same decode over an FP16 paged cache of "
                                     "the prefill tokens (not part of the step)"},
+            "step_fused": {"ms_per_step": ms_fused,
+                           "note": "quantize -> append -> decode per layer in one graph"},
         },
         "decode_speedup_vs_fp16_cache": ms["decode_fp16"] / ms["decode"],
         "roofline": {"bound": "hbm", "kernel": dom, "achieved": dom_gbs, "peak": peak,
                      "peak_kind": f"{peak_kind} hbm_gbs (burst copy)", "unit": "GB/s",
                      "frac": dom_gbs / peak,
                      "traffic": traffic_q if dom == "quantize" else traffic_d,
-                     "algorithmic_bytes": dom_bytes},
+                     "algorithmic_bytes_per_launch": (bq if dom == "quantize" else bd) // L,
+                     "us_per_launch": per_launch[dom]},
         "roofline_decode": {"bound": "hbm", "achieved": d_gbs, "peak": peak, "unit": "GB/s",
                             "frac": d_gbs / peak, "traffic": traffic_d,
-                            "algorithmic_bytes": job.bytes_decode},
+                            "algorithmic_bytes_per_launch": bd // L,
+                            "us_per_launch": per_launch["decode"]},
         "e2e": e2e,
-        "gpu_launches": LAUNCHES_PER_STEP * args.steps,
+        "gpu_launches": LAUNCHES_PER_STEP * L * args.steps,
         "clocks": clocks,
         "wall_s_timed_region": wall,
     }
