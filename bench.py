@@ -50,9 +50,9 @@ REC = 15360
 # algorithmic bytes per token-head (K+V): fp16 in, packed out
 FP16_TOKEN_HEAD = 512
 PACKED_TOKEN_HEAD = 120
-# library kernels per step: quantize (tiles + tail copy), append (copy +
-# filled-tail tiles), decode (one kernel, splits merged in the same launch)
-LAUNCHES_PER_STEP = 5
+# library kernels per step: quantize (tiles and leftover-token copies), append
+# (token copies and filled-tail tiles), decode (splits merged in the same launch)
+LAUNCHES_PER_STEP = 3
 METRIC = "decode-attn KV GB/s & tokens/s, quantize GB/s, as % of B300 HBM roofline"
 
 

@@ -223,6 +223,36 @@ int kvarn_decode_attention_noalloc(const kvarn_config_t *cfg, const void *q, con
                                    float softmax_scale, void *out, int32_t *status,
                                    kvarn_stream_t stream);
 
+/* Chunked prefill: attention of a chunk of new query tokens per sequence over
+ * the quantized cache ("KV Cache Nasil Calisir?": each token attends to every
+ * cached token up to its own position; "Paged Attention (vLLM)" for the
+ * pages).  Sequence b holds start[b] tokens before the chunk and chunk_lens[b]
+ * new ones, and the cache (pool pages + fp16 tails) is already in its state
+ * after the chunk was appended: n_b = start[b] + chunk_lens[b] tokens, the
+ * n_b / 128 full blocks in the pool (block_table) and the n_b mod 128 newest
+ * tokens in the tails (as kvarn_quantize_blocks leaves a sequence of length
+ * n_b).  Query token i < chunk_lens[b] sits at position P = start[b] + i:
+ *   out[b][i][h] = sum_{t <= P} softmax_t(scale * q[b][i][h] . k_t) v_t,
+ * query head h reading KV head h / (Hq/Hkv); keys and values are dequantized
+ * and rotated back as in kvarn_decode_attention.
+ *   q, out      fp16 [batch][chunk_max][Hq][128]; rows i >= chunk_lens[b] of
+ *               out are written as zeros
+ *   start, chunk_lens  int32 [batch] (device); 0 <= chunk_lens[b] <= chunk_max
+ *               and start[b] + chunk_lens[b] <= max_seq, else the sequence is
+ *               reported (KVARN_STATUS_BAD_LENGTH) and its rows are zeros
+ *   max_seq     host upper bound on start + chunk_lens
+ * No workspace.  A page id outside the pool is reported
+ * (KVARN_STATUS_BAD_PAGE) and the query tiles that would read it give zeros.
+ * The work is one CTA per 128 query rows (128 / (Hq/Hkv) tokens of one KV
+ * head's query group) and KV head; it uses 229 KB of shared memory and 256
+ * TMEM columns, so one CTA runs per SM. */
+int kvarn_chunk_attention(const kvarn_config_t *cfg, const void *q, int chunk_max,
+                          const int32_t *start, const int32_t *chunk_lens, int batch,
+                          int max_seq, const void *pool, int64_t num_pages,
+                          const int32_t *block_table, int max_blocks, const void *tail_k,
+                          const void *tail_v, float softmax_scale, void *out, int32_t *status,
+                          kvarn_stream_t stream);
+
 /* Diagnosis: dequantizes `n` page records into float32 rotated-space tiles.
  *   records   [n][15360] bytes (e.g. pool + page*Hkv*15360, one record per
  *             (page, head) in order)

@@ -7,14 +7,14 @@ from .kvarn import (Config, KvarnError, alloc_decode_workspace, alloc_fp16_decod
                     alloc_fp16_pool, alloc_pool, alloc_tails, fp16_decode_workspace_bytes,
                     kvarn_fp16_decode_attention, kvarn_fp16_write_blocks,
                     config_from_string, config_validate, decode_split_plan, decode_workspace_bytes,
-                    kvarn_append_token, kvarn_decode_attention, kvarn_decode_attention_noalloc,
-                    kvarn_dequantize_pages,
+                    kvarn_append_token, kvarn_chunk_attention, kvarn_decode_attention,
+                    kvarn_decode_attention_noalloc, kvarn_dequantize_pages,
                     kvarn_quantize_blocks, lib, page_bytes, status_string, version)
 
 __all__ = ["Config", "KvarnError", "alloc_decode_workspace", "alloc_fp16_decode_workspace",
            "alloc_fp16_pool", "alloc_pool", "alloc_tails", "fp16_decode_workspace_bytes",
            "kvarn_fp16_decode_attention", "kvarn_fp16_write_blocks",
            "config_from_string", "config_validate", "decode_split_plan", "decode_workspace_bytes",
-           "kvarn_append_token", "kvarn_decode_attention", "kvarn_decode_attention_noalloc",
-           "kvarn_dequantize_pages",
+           "kvarn_append_token", "kvarn_chunk_attention", "kvarn_decode_attention",
+           "kvarn_decode_attention_noalloc", "kvarn_dequantize_pages",
            "kvarn_quantize_blocks", "lib", "page_bytes", "status_string", "version"]

@@ -264,6 +264,53 @@ int kvarn_decode_attention(const kvarn_config_t* cfg, const void* q, const void*
   return e == cudaSuccess ? KVARN_OK : KVARN_ERR_LAUNCH;
 }
 
+int kvarn_chunk_attention(const kvarn_config_t* cfg, const void* q, int chunk_max,
+                          const int32_t* start, const int32_t* chunk_lens, int batch,
+                          int max_seq, const void* pool, int64_t num_pages,
+                          const int32_t* block_table, int max_blocks, const void* tail_k,
+                          const void* tail_v, float softmax_scale, void* out, int32_t* status,
+                          kvarn_stream_t stream) {
+  int rc = kvarn_config_validate(cfg);
+  if (rc != KVARN_OK) return rc;
+  if (batch < 0 || chunk_max < 0 || max_seq < 0 || max_blocks < 0 || num_pages < 0)
+    return KVARN_ERR_INVALID_ARG;
+  if (batch == 0 || chunk_max == 0) return KVARN_OK;
+  if (!q || !start || !chunk_lens || !tail_k || !tail_v || !out) return KVARN_ERR_INVALID_ARG;
+  if (max_seq >= kT && (!pool || !block_table || num_pages <= 0 || max_blocks < max_seq / kT))
+    return KVARN_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(pool) || !aligned16(tail_k) || !aligned16(tail_v) ||
+      !aligned16(out))
+    return KVARN_ERR_INVALID_ARG;
+  if (!(softmax_scale > 0.f) || softmax_scale != softmax_scale) return KVARN_ERR_INVALID_ARG;
+  const int g = cfg->num_q_heads / cfg->num_kv_heads;
+  const int tq = chunk_rows_per_tile(g);
+  const int64_t ntq = ((int64_t)chunk_max + tq - 1) / tq;
+  if (batch > 65535 || cfg->num_kv_heads > 65535 || ntq > 0x7fffffff) return KVARN_ERR_UNSUPPORTED;
+  ChunkArgs a;
+  a.q = static_cast<const __half*>(q);
+  a.M = chunk_max;
+  a.start = start;
+  a.chunk_lens = chunk_lens;
+  a.batch = batch;
+  a.max_seq = max_seq;
+  a.hq = cfg->num_q_heads;
+  a.hkv = cfg->num_kv_heads;
+  a.g = g;
+  a.tq = tq;
+  a.ntq = (int)ntq;
+  a.pool = static_cast<const uint8_t*>(pool);
+  a.num_pages = num_pages;
+  a.block_table = block_table;
+  a.max_blocks = max_blocks;
+  a.tail_k = static_cast<const __half*>(tail_k);
+  a.tail_v = static_cast<const __half*>(tail_v);
+  a.scale_log2 = softmax_scale * 1.4426950408889634f;
+  a.out = static_cast<__half*>(out);
+  a.status = status;
+  return launch_chunk_attention(a, (cudaStream_t)stream) == cudaSuccess ? KVARN_OK
+                                                                         : KVARN_ERR_LAUNCH;
+}
+
 int kvarn_fp16_write_blocks(const void* k, const void* v, int64_t stride_b, int64_t stride_t,
                             int64_t stride_h, int batch, int num_kv_heads,
                             const int32_t* seq_lens, int max_seq, const int32_t* block_table,

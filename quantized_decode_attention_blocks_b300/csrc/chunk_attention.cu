@@ -1,0 +1,592 @@
+// chunk_attention.cu -- attention of a chunk of new query tokens over the
+// quantized paged cache (chunked prefill), on the fifth-generation tensor
+// cores.
+//
+// Method: every query token attends causally to the cached tokens up to its
+// own position ("KV Cache (Anahtar-Deger Onbellegi)", yapayzekasozluk.tr, "KV
+// Cache Nasil Calisir?"), the cache being paged ("Paged Attention (vLLM)") and
+// quantized per the KVarN page (blog.edumints.com, "KVarN Nasil Calisir?"):
+// keys and values are stored rotated, y = H x, and the orthonormal rotation
+// keeps scores, so with q~ = H q
+//     s_it = q~_i . yhatK_t,   o_i = H (sum_t p_it yhatV_t) / sum_t p_it,
+// yhat_td = c_d (s'_t q_td + z'_t) for a page token; a token of the fp16 tail
+// is rotated on the way in (yhat = H x).
+//
+// CTA = one tile of 128 query rows of one (sequence, KV head): row r holds
+// query token i0 + r / g of head r mod g of the KV head's group.  It walks the
+// cache blocks (pages, then the tail) that the tile's last token can see, in
+// the structure of a streaming-softmax attention:
+//   S   = Q~ K^T   tcgen05.mma, M = 128 rows, N = 128 tokens, K = 128 channels,
+//                  as three products Qhi Khi + Qhi Klo + Qlo Khi (fp16 operands
+//                  split hi + lo: one fp16 keeps 11 bits, too few for scores
+//                  against keys with outlier channels), fp32 in TMEM;
+//   P   = 2^(S - m) fp16, causal mask, running max m with a lazy rescale of O
+//         (only when the max grows by more than 2^8, which fp16 P holds),
+//         written to TMEM;
+//   O  += P V^      tcgen05.mma with A = P from TMEM, N = 128 channels, K = 128
+//                  tokens, as P Vhi + P Vlo, fp32 in TMEM.
+// Roles: warps 0-3 build Q~ once and run the softmax (thread r = TMEM lane r =
+// row r); warps 4-6 bring each page record in with one bulk copy (two buffers,
+// two blocks ahead) and dequantize it into the K^ and V^ (hi, lo) operands in
+// shared memory; one thread of warp 7 issues the MMAs, S one block ahead of
+// PV into two S buffers in TMEM, so the tensor cores work on the next block's
+// scores while the softmax warps work on this block's.  The hand-offs are
+// mbarriers, every wait bounded (KVARN_STATUS_TIMEOUT).  At the end each
+// softmax thread reads its row of O, divides by l, rotates it back with a
+// register FWHT and writes fp16.
+#include "kvarn_internal.cuh"
+#include "ptx.cuh"
+
+namespace kvarn {
+namespace {
+
+using namespace ptx;
+
+constexpr int kSoftWarps = 4;                         // rows: TMEM lane quarters
+constexpr int kDeqWarps = 3;                          // 8 warps in all: 255 registers
+constexpr int kCThreads = 32 * (kSoftWarps + kDeqWarps + 1);
+constexpr int kDeq0 = 32 * kSoftWarps;                // first dequant thread
+constexpr int kMmaThread = 32 * (kSoftWarps + kDeqWarps);
+constexpr uint32_t kOp = 128 * 128 * 2;               // one fp16 operand, 128 x 128
+constexpr uint32_t kOpBox = kOp / 2;                  // 64-element-wide half
+// TMEM columns: S (two buffers) [0, 256), O [256, 384), P (fp16 pairs) [384, 448)
+constexpr uint32_t kCTmemCols = 512;
+constexpr uint32_t kColO = 256, kColP = 384;
+constexpr uint64_t kCWaitNs = 2000000000ull;
+// kind::f16, fp16 A and B (both K-major), fp32 D, M = 128, N = 128
+constexpr uint32_t kCIdesc = (1u << 4) | ((128u >> 3) << 17) | ((128u >> 4) << 24);
+constexpr float kLazy = 8.f;                          // log2 units
+
+struct __align__(1024) CSmem {
+  uint8_t qh[kOp];        // A of S: q~ high part   [row][channel]
+  uint8_t ql[kOp];        //         q~ low part
+  uint8_t kh[kOp];        // B of S: yhatK high     [token][channel]
+  uint8_t kl[kOp];        //         yhatK low
+  uint8_t vh[kOp];        // B of PV: yhatV high    [channel][token]
+  uint8_t vl[kOp];        //          yhatV low
+  uint8_t raw[2][kRec];   // page records in flight
+  uint64_t raw_full[2];
+  uint64_t sdone[2];      // S of a block ready, per S buffer
+  uint64_t qready, kready, vready, pready, pvdone, drain;
+  uint32_t tmem_base;
+  int abort;
+};
+static_assert(offsetof(CSmem, raw) % 16 == 0 && offsetof(CSmem, raw_full) % 8 == 0,
+              "bulk copies and barriers need these alignments");
+constexpr int kCSmemBytes = (int)sizeof(CSmem) + 1024;
+static_assert(kCSmemBytes <= 232448, "shared memory of one CTA");
+
+// Byte offset of the 16-byte chunk holding elements 8c .. 8c + 7 (c < 16) of
+// row r of a 128 x 128 fp16 operand in the 128-byte swizzled K-major layout:
+// two 64-element halves of 16 KB, rows of 128 bytes, chunk c & 7 of row r at
+// position (c & 7) ^ (r & 7).
+__device__ __forceinline__ uint32_t sw_off(int r, int c) {
+  return (uint32_t)((c >> 3) * kOpBox + r * 128 + (((c & 7) ^ (r & 7)) << 4));
+}
+
+__device__ __forceinline__ float ex2c(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+// In-place Walsh-Hadamard butterflies over 128 values in natural (Sylvester)
+// order, unnormalised: x <- Hs x.
+__device__ __forceinline__ void fwht128(float (&x)[128]) {
+#pragma unroll
+  for (int h = 1; h < 128; h <<= 1)
+#pragma unroll
+    for (int i = 0; i < 128; ++i)
+      if ((i & h) == 0) {
+        const float a = x[i], b = x[i + h];
+        x[i] = a + b;
+        x[i + h] = a - b;
+      }
+}
+
+__device__ __forceinline__ void load_row(const __half* src, float (&x)[128]) {
+  const uint4* s4 = reinterpret_cast<const uint4*>(src);
+#pragma unroll
+  for (int c = 0; c < 16; ++c) {
+    const uint4 u = __ldg(s4 + c);
+    const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&w[e]));
+      x[8 * c + 2 * e] = f.x;
+      x[8 * c + 2 * e + 1] = f.y;
+    }
+  }
+}
+
+__device__ __forceinline__ uint32_t h2bits(__half2 h) { return *reinterpret_cast<uint32_t*>(&h); }
+
+// The fp16 pair (hi, lo) of two fp32 values: hi = fp16(x), lo = fp16(x - hi).
+__device__ __forceinline__ void split2(float a, float b, uint32_t& hi, uint32_t& lo) {
+  const __half2 h = __floats2half2_rn(a, b);
+  const float2 hf = __half22float2(h);
+  hi = h2bits(h);
+  lo = h2bits(__floats2half2_rn(a - hf.x, b - hf.y));
+}
+
+// 8 values of row r, chunk c, written as hi and lo parts
+__device__ __forceinline__ void store_hilo8(uint8_t* hi, uint8_t* lo, int r, int c,
+                                            const float* y) {
+  uint32_t h[4], l[4];
+#pragma unroll
+  for (int e = 0; e < 4; ++e) split2(y[2 * e], y[2 * e + 1], h[e], l[e]);
+  const uint32_t o = sw_off(r, c);
+  *reinterpret_cast<uint4*>(hi + o) = make_uint4(h[0], h[1], h[2], h[3]);
+  *reinterpret_cast<uint4*>(lo + o) = make_uint4(l[0], l[1], l[2], l[3]);
+}
+
+__device__ __forceinline__ float code_f(uint32_t q) {   // small integer -> float, exact
+  return __int_as_float(0x4B000000 | q) - 8388608.f;
+}
+
+// Page tokens: yhatK_td = c_d (s'_t q_td + z'_t) into the K^ operands, item
+// x = 4 t + c4 = channels 32 c4 .. 32 c4 + 31 of token t; dequant thread dt
+// takes items dt, dt + 96, ...  rk: the record's K part.
+__device__ __forceinline__ void dequant_k(const uint8_t* rk, uint8_t* kh, uint8_t* kl, int dt) {
+  const float4* cv = reinterpret_cast<const float4*>(rk + kOffKC);
+#pragma unroll 1
+  for (int x = dt; x < 4 * kT; x += 32 * kDeqWarps) {
+    const int t = x >> 2, c4 = x & 3;
+    const float2 sz = *reinterpret_cast<const float2*>(rk + kOffKSZ + 8 * t);
+    const uint4 w4 = reinterpret_cast<const uint4*>(rk + kOffKCodes + 64 * t)[c4];
+    const uint32_t ws[4] = {w4.x, w4.y, w4.z, w4.w};
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const int cc = 4 * c4 + e;   // channels 8 cc .. 8 cc + 7: nibble k = channel 8 cc + k
+      const float4 ca = cv[2 * cc], cb = cv[2 * cc + 1];
+      const float cs[8] = {ca.x, ca.y, ca.z, ca.w, cb.x, cb.y, cb.z, cb.w};
+      float y[8];
+#pragma unroll
+      for (int k = 0; k < 8; ++k) y[k] = cs[k] * fmaf(sz.x, code_f((ws[e] >> (4 * k)) & 15u), sz.y);
+      store_hilo8(kh, kl, t, cc, y);
+    }
+  }
+}
+
+// Page tokens: yhatV into the V^ operand [channel][token].  Lane:
+// j = lane & 3, h = (lane >> 2) & 1, e = (lane >> 3) & 1, r0 = lane >> 4; round
+// k (of 32, dequant warp dw takes k = dw, dw + 3, ...) is m = k >> 2 and
+// r = 2 (k & 3) + r0, and reads word 128m + 16r + 4j + 2e + h of the permuted
+// V code layout: channel c = 16m + 8e + r, tokens 16k' + 8f + 2j + s for
+// k' = 4h .. 4h + 3.  Lanes of one load differ in (j, h, e, r0): 32 banks.
+__device__ __forceinline__ void dequant_v(const uint8_t* rv, uint8_t* vh, uint8_t* vl, int dw,
+                                          int lane) {
+  const int j2 = lane & 3, hb = (lane >> 2) & 1, e = (lane >> 3) & 1, r0 = lane >> 4;
+  const uint8_t* vsz = rv + (kOffVSZ - kKPart);
+  const uint32_t* words = reinterpret_cast<const uint32_t*>(rv + (kOffVCodes - kKPart));
+  const float* vc = reinterpret_cast<const float*>(rv + (kOffVC - kKPart));
+  float2 sz[4][2][2];
+#pragma unroll
+  for (int kk = 0; kk < 4; ++kk)
+#pragma unroll
+    for (int f = 0; f < 2; ++f)
+#pragma unroll
+      for (int s = 0; s < 2; ++s)
+        sz[kk][f][s] = *reinterpret_cast<const float2*>(
+            vsz + 8 * (16 * (4 * hb + kk) + 8 * f + 2 * j2 + s));
+#pragma unroll 1
+  for (int k = dw; k < 32; k += kDeqWarps) {
+    const int m = k >> 2, r = 2 * (k & 3) + r0;
+    const int c = 16 * m + 8 * e + r;
+    const uint32_t w = words[128 * m + 16 * r + 4 * j2 + 2 * e + hb];
+    const float cd = vc[c];
+#pragma unroll
+    for (int kk = 0; kk < 4; ++kk)
+#pragma unroll
+      for (int f = 0; f < 2; ++f) {
+        const int i0 = 2 * kk + f;   // crumb of s = 0; s = 1 is crumb i0 + 8
+        const float y0 = cd * fmaf(sz[kk][f][0].x, code_f((w >> (2 * i0)) & 3u), sz[kk][f][0].y);
+        const float y1 =
+            cd * fmaf(sz[kk][f][1].x, code_f((w >> (2 * i0 + 16)) & 3u), sz[kk][f][1].y);
+        const int u = 2 * (4 * hb + kk) + f;   // tokens 8u .. 8u + 7; these are 2 j2, 2 j2 + 1
+        const uint32_t off =
+            (uint32_t)((u >> 3) * kOpBox + c * 128 + (((u & 7) ^ (c & 7)) << 4) + 4 * j2);
+        uint32_t hi, lo;
+        split2(y0, y1, hi, lo);
+        *reinterpret_cast<uint32_t*>(vh + off) = hi;
+        *reinterpret_cast<uint32_t*>(vl + off) = lo;
+      }
+  }
+}
+
+__global__ void __launch_bounds__(kCThreads, 1)
+    chunk_attention_kernel(const ChunkArgs a) {
+  extern __shared__ uint8_t smem_raw[];
+  CSmem& S = *reinterpret_cast<CSmem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                       ~static_cast<uintptr_t>(1023));
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int b = blockIdx.z, kvh = blockIdx.y;
+  const int tile = a.ntq - 1 - (int)blockIdx.x;   // longest tiles first
+  const int g = a.g, tq = a.tq;
+  const int i0 = tile * tq;
+  const int start = a.start[b];
+  int cl = a.chunk_lens[b];
+  const int64_t n64 = (int64_t)start + cl;
+  const bool bad =
+      start < 0 || cl < 0 || cl > a.M || n64 > a.max_seq || n64 / kT > a.max_blocks;
+  const int n = bad ? 0 : (int)n64;
+  if (bad) {
+    if (tile == 0 && kvh == 0 && tid == 0) report(a.status, KVARN_STATUS_BAD_LENGTH);
+    cl = 0;
+  }
+  const int nfull = bad ? 0 : n / kT;
+  const int last = min(i0 + tq, cl) - 1;           // last query token of the tile
+  const int nblk = last >= 0 ? (start + last) / kT + 1 : 0;
+  const int32_t* trow = a.block_table + (int64_t)b * a.max_blocks;
+  // every page the tile reads must be in the pool
+  int pbad = 0;
+  for (int j = tid; j < min(nblk, nfull); j += kCThreads) {
+    const int p = trow[j];
+    if (p < 0 || (int64_t)p >= a.num_pages) pbad = 1;
+  }
+  if (__syncthreads_or(pbad)) {
+    if (tid == 0) report(a.status, KVARN_STATUS_BAD_PAGE);
+    cl = 0;
+  }
+  __half* const orow0 = a.out + (int64_t)b * a.M * a.hq * kD;
+  if (cl <= i0) {
+    // no query token of this tile: its rows (tokens below M) are zeros
+    for (int x = tid; x < 128 * 16; x += kCThreads) {
+      const int r = x >> 4, c = x & 15, i = i0 + r / g;
+      if (r < tq * g && i < a.M)
+        reinterpret_cast<uint4*>(orow0 + ((int64_t)i * a.hq + kvh * g + r % g) * kD)[c] =
+            make_uint4(0u, 0u, 0u, 0u);
+    }
+    return;
+  }
+
+  if (tid == 0) {
+    mbar_init(&S.raw_full[0], 1);
+    mbar_init(&S.raw_full[1], 1);
+    mbar_init(&S.qready, kSoftWarps);
+    mbar_init(&S.kready, kDeqWarps);
+    mbar_init(&S.vready, kDeqWarps);
+    mbar_init(&S.sdone[0], 1);
+    mbar_init(&S.sdone[1], 1);
+    mbar_init(&S.pready, kSoftWarps);
+    mbar_init(&S.pvdone, 1);
+    mbar_init(&S.drain, 1);
+    S.abort = 0;
+    fence_mbar_init();
+  }
+  if (warp == 0) {
+    tmem_alloc(&S.tmem_base, kCTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = S.tmem_base;
+  auto wait = [&](uint64_t* bar, uint32_t ph) {
+    if (*reinterpret_cast<volatile int*>(&S.abort)) return;
+    if (!mbar_wait_bounded(bar, ph, kCWaitNs)) {
+      *reinterpret_cast<volatile int*>(&S.abort) = 1;
+      report(a.status, KVARN_STATUS_TIMEOUT);
+    }
+  };
+  const int rem = n - nfull * kT;
+
+  if (warp < kSoftWarps) {
+    // ================= softmax warps: row r = TMEM lane r =================
+    const int r = tid, i = i0 + r / g, hh = r % g;
+    const bool valid = r < tq * g && i < cl;
+    const int Pr = valid ? start + i : -1;         // last key position of the row
+    {
+      float x[128];
+      if (valid) {
+        load_row(a.q + (((int64_t)b * a.M + i) * a.hq + kvh * g + hh) * kD, x);
+        fwht128(x);
+        const float f = kInvSqrt128 * a.scale_log2;   // scores in log2 units
+#pragma unroll
+        for (int d = 0; d < 128; ++d) x[d] *= f;
+      } else {
+#pragma unroll
+        for (int d = 0; d < 128; ++d) x[d] = 0.f;
+      }
+#pragma unroll
+      for (int c = 0; c < 16; ++c) store_hilo8(S.qh, S.ql, r, c, x + 8 * c);
+    }
+    fence_proxy_async_smem();
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&S.qready);
+
+    const uint32_t tl = tmem + ((uint32_t)(32 * warp) << 16), tO = tl + kColO, tP = tl + kColP;
+    float m_ref = -INFINITY, l = 0.f;
+    for (int j = 0; j < nblk; ++j) {
+      // S of block j is in buffer j & 1; two passes over it in 32-column pieces
+      // (the maximum, then the probabilities), so no row sits in registers
+      wait(&S.sdone[j & 1], (j >> 1) & 1);
+      tc_fence_after();
+      const uint32_t tS = tl + 128 * (j & 1);
+      const int lim = Pr - kT * j;                  // columns 0 .. lim are visible
+      float mb = -INFINITY;
+#pragma unroll
+      for (int c4 = 0; c4 < 4; ++c4) {
+        float sv[32];
+        tmem_ld32(tS + 32 * c4, sv);
+        tmem_wait_ld();
+#pragma unroll
+        for (int k = 0; k < 32; ++k)
+          if (32 * c4 + k <= lim) mb = fmaxf(mb, sv[k]);
+      }
+      // lazy rescale: a row moves its reference only when its maximum grows by
+      // more than 2^kLazy; O holding earlier blocks is then rescaled.  The
+      // TMEM accesses are warp-wide, so the warp rescales when any lane must
+      // (alpha = 1 on the others)
+      const bool grow = mb > m_ref + kLazy;
+      const bool resc = grow && m_ref != -INFINITY;
+      float alpha = 1.f;
+      if (resc) {
+        alpha = ex2c(m_ref - mb);
+        l *= alpha;
+      }
+      if (grow) m_ref = mb;
+      bool o_free = j == 0;                         // PV of the block before is done
+      if (__any_sync(0xffffffffu, resc)) {
+        wait(&S.pvdone, (j - 1) & 1);
+        o_free = true;
+        tc_fence_after();
+#pragma unroll
+        for (int c4 = 0; c4 < 4; ++c4) {
+          float o[32];
+          tmem_ld32(tO + 32 * c4, o);
+          tmem_wait_ld();
+#pragma unroll
+          for (int k = 0; k < 32; ++k) o[k] *= alpha;
+          tmem_st32(tO + 32 * c4, o);
+        }
+        tmem_wait_st();
+      }
+      if (!o_free) wait(&S.pvdone, (j - 1) & 1);   // the P buffer is free again
+      const bool any = m_ref != -INFINITY;
+      float ls = 0.f;
+#pragma unroll
+      for (int hf = 0; hf < 2; ++hf) {
+        // columns 64 hf .. 64 hf + 63 of S -> fp16 pairs in P columns 32 hf ..
+        float sv[64];
+        tmem_ld32(tS + 64 * hf, sv);
+        tmem_ld32(tS + 64 * hf + 32, sv + 32);
+        tmem_wait_ld();
+        float pw[32];
+#pragma unroll
+        for (int k = 0; k < 32; ++k) {
+          const int c0 = 64 * hf + 2 * k;
+          const float p0 = any && c0 <= lim ? ex2c(sv[2 * k] - m_ref) : 0.f;
+          const float p1 = any && c0 + 1 <= lim ? ex2c(sv[2 * k + 1] - m_ref) : 0.f;
+          const __half2 ph = __floats2half2_rn(p0, p1);
+          const float2 pf = __half22float2(ph);     // l sums what the MMA multiplies
+          ls += pf.x + pf.y;
+          pw[k] = __uint_as_float(h2bits(ph));
+        }
+        tmem_st32(tP + 32 * hf, pw);
+      }
+      tmem_wait_st();
+      l += ls;
+      tc_fence_before();
+      __syncwarp();
+      // P is written and S buffer j & 1 is read
+      if (lane == 0) mbar_arrive(&S.pready);
+    }
+    // ---- epilogue: o = H (O / l) / sqrt(128), fp16 ----
+    wait(&S.pvdone, (nblk - 1) & 1);
+    tc_fence_after();
+    float o[128];
+    tmem_ld32(tO, o);
+    tmem_ld32(tO + 32, o + 32);
+    tmem_ld32(tO + 64, o + 64);
+    tmem_ld32(tO + 96, o + 96);
+    tmem_wait_ld();
+    if (r < tq * g && i < a.M) {
+      uint4* dst = reinterpret_cast<uint4*>(orow0 + ((int64_t)i * a.hq + kvh * g + hh) * kD);
+      if (valid && l > 0.f) {
+        fwht128(o);
+        const float f = kInvSqrt128 / l;
+#pragma unroll
+        for (int c = 0; c < 16; ++c) {
+          uint32_t w[4];
+#pragma unroll
+          for (int e = 0; e < 4; ++e)
+            w[e] = h2bits(__floats2half2_rn(o[8 * c + 2 * e] * f, o[8 * c + 2 * e + 1] * f));
+          dst[c] = make_uint4(w[0], w[1], w[2], w[3]);
+        }
+      } else {
+#pragma unroll
+        for (int c = 0; c < 16; ++c) dst[c] = make_uint4(0u, 0u, 0u, 0u);
+      }
+    }
+  } else if (warp < kSoftWarps + kDeqWarps) {
+    // ================= dequant warps: pages and the tail into operands =================
+    const int dt = tid - kDeq0, dw = dt >> 5;
+    auto rec_of = [&](int j) {
+      return a.pool + ((int64_t)trow[j] * a.hkv + kvh) * (int64_t)kRec;
+    };
+    // loads issued and seen complete per buffer (thread dt == 0), as
+    // issued0 | issued1 << 16 etc. so that no array sits in local memory
+    uint32_t issued = 0, seen = 0;
+    auto issue = [&](int j) {
+      uint64_t* bar = &S.raw_full[j & 1];
+      mbar_arrive_expect_tx(bar, kRec);
+      bulk_g2s(S.raw[j & 1], rec_of(j), kRec, bar);
+      issued += 1u << (16 * (j & 1));
+    };
+    if (dt == 0) {
+      if (0 < min(nblk, nfull)) issue(0);
+      if (1 < min(nblk, nfull)) issue(1);
+    }
+    const __half* tkb = a.tail_k + ((int64_t)b * a.hkv + kvh) * kT * kD;
+    const __half* tvb = a.tail_v + ((int64_t)b * a.hkv + kvh) * kT * kD;
+    for (int j = 0; j < nblk; ++j) {
+      const bool page = j < nfull;
+      const uint8_t* rk = S.raw[j & 1];
+      if (page) {
+        wait(&S.raw_full[j & 1], (j >> 1) & 1);
+        if (dt == 0 && !*reinterpret_cast<volatile int*>(&S.abort)) seen += 1u << (16 * (j & 1));
+      }
+      if (j > 0) wait(&S.sdone[(j - 1) & 1], ((j - 1) >> 1) & 1);   // S of block j-1 read K^
+      if (page) {
+        dequant_k(rk, S.kh, S.kl, dt);
+      } else {
+        // the fp16 tail, rotated into the pages' space: yhat = H x / sqrt(128)
+#pragma unroll 1
+        for (int t = dt; t < kT; t += 32 * kDeqWarps) {
+          float x[128];
+          if (t < rem) {
+            load_row(tkb + (int64_t)t * kD, x);
+            fwht128(x);
+#pragma unroll
+            for (int d = 0; d < 128; ++d) x[d] *= kInvSqrt128;
+          } else {
+#pragma unroll
+            for (int d = 0; d < 128; ++d) x[d] = 0.f;
+          }
+#pragma unroll
+          for (int c = 0; c < 16; ++c) store_hilo8(S.kh, S.kl, t, c, x + 8 * c);
+        }
+      }
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&S.kready);
+      if (j > 0) wait(&S.pvdone, (j - 1) & 1);     // PV of the block before read V^
+      if (page) {
+        dequant_v(rk + kKPart, S.vh, S.vl, dw, lane);
+      } else {
+#pragma unroll 1
+        for (int t = dt; t < kT; t += 32 * kDeqWarps) {
+          float x[128];
+          if (t < rem) {
+            load_row(tvb + (int64_t)t * kD, x);
+            fwht128(x);
+#pragma unroll
+            for (int d = 0; d < 128; ++d) x[d] *= kInvSqrt128;
+          } else {
+#pragma unroll
+            for (int d = 0; d < 128; ++d) x[d] = 0.f;
+          }
+          // column t of V^ [channel][token]
+          const uint32_t tb = (uint32_t)((t >> 6) * kOpBox + (t & 7) * 2);
+          const int tc = (t & 63) >> 3;
+#pragma unroll
+          for (int d = 0; d < 128; ++d) {
+            const __half h = __float2half_rn(x[d]);
+            const uint32_t o = tb + d * 128 + ((tc ^ (d & 7)) << 4);
+            *reinterpret_cast<__half*>(S.vh + o) = h;
+            *reinterpret_cast<__half*>(S.vl + o) = __float2half_rn(x[d] - __half2float(h));
+          }
+        }
+      }
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&S.vready);
+      // every dequant thread is done with raw[j & 1]: load block j + 2 into it
+      named_sync(1, 32 * kDeqWarps);
+      if (dt == 0 && j + 2 < min(nblk, nfull) && !*reinterpret_cast<volatile int*>(&S.abort))
+        issue(j + 2);
+    }
+    if (dt == 0) {
+      // copies still in flight (a wait gave up) land before the CTA leaves
+#pragma unroll
+      for (int s2 = 0; s2 < 2; ++s2)
+        for (int k = (int)((seen >> (16 * s2)) & 0xFFFF); k < (int)((issued >> (16 * s2)) & 0xFFFF);
+             ++k)
+          mbar_wait_bounded(&S.raw_full[s2], (uint32_t)(k & 1), kCWaitNs);
+    }
+  } else if (tid == kMmaThread) {
+    // ================= MMA issue =================
+    // S runs one block ahead of PV: S of block j + 1 (into S buffer (j+1) & 1,
+    // whose softmax of block j - 1 is done: its P was waited for) is issued
+    // before PV of block j, so that it overlaps the softmax of block j
+    const uint32_t tO = tmem + kColO, tP = tmem + kColP;
+    const uint32_t qh = smem_u32(S.qh), ql = smem_u32(S.ql), kh = smem_u32(S.kh),
+                   kl = smem_u32(S.kl), vh = smem_u32(S.vh), vl = smem_u32(S.vl);
+    auto issue_s = [&](int j) {
+      wait(&S.kready, j & 1);
+      tc_fence_after();
+      const uint32_t tS = tmem + 128 * (j & 1);
+#pragma unroll
+      for (int kk = 0; kk < 8; ++kk) {
+        const uint32_t off = (kk >> 2) * kOpBox + (kk & 3) * 32;
+        umma_f16(tS, umma_desc_sw128(qh + off), umma_desc_sw128(kh + off), kCIdesc, kk > 0);
+      }
+#pragma unroll
+      for (int kk = 0; kk < 8; ++kk) {
+        const uint32_t off = (kk >> 2) * kOpBox + (kk & 3) * 32;
+        umma_f16(tS, umma_desc_sw128(qh + off), umma_desc_sw128(kl + off), kCIdesc, true);
+      }
+#pragma unroll
+      for (int kk = 0; kk < 8; ++kk) {
+        const uint32_t off = (kk >> 2) * kOpBox + (kk & 3) * 32;
+        umma_f16(tS, umma_desc_sw128(ql + off), umma_desc_sw128(kh + off), kCIdesc, true);
+      }
+      umma_commit(&S.sdone[j & 1]);
+    };
+    wait(&S.qready, 0);
+    issue_s(0);
+    for (int j = 0; j < nblk; ++j) {
+      if (j + 1 < nblk) issue_s(j + 1);
+      wait(&S.pready, j & 1);
+      wait(&S.vready, j & 1);
+      tc_fence_after();
+      // A = P from TMEM: K step kk is tokens 16 kk .. 16 kk + 15, columns 8 kk ..
+#pragma unroll
+      for (int kk = 0; kk < 8; ++kk) {
+        const uint32_t off = (kk >> 2) * kOpBox + (kk & 3) * 32;
+        umma_f16_ts(tO, tP + 8 * kk, umma_desc_sw128(vh + off), kCIdesc, j > 0 || kk > 0);
+      }
+#pragma unroll
+      for (int kk = 0; kk < 8; ++kk) {
+        const uint32_t off = (kk >> 2) * kOpBox + (kk & 3) * 32;
+        umma_f16_ts(tO, tP + 8 * kk, umma_desc_sw128(vl + off), kCIdesc, true);
+      }
+      umma_commit(&S.pvdone);
+    }
+    // every MMA of this thread is complete before TMEM is released
+    umma_commit(&S.drain);
+    mbar_wait_bounded(&S.drain, 0, kCWaitNs);
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 0) tmem_dealloc(tmem, kCTmemCols);
+}
+
+}  // namespace
+
+int chunk_rows_per_tile(int g) { return 128 / g; }
+
+cudaError_t launch_chunk_attention(const ChunkArgs& args, cudaStream_t s) {
+  static std::atomic<uint64_t> smem_set{0};
+  cudaError_t e = ensure_dynamic_smem(chunk_attention_kernel, kCSmemBytes, smem_set);
+  if (e != cudaSuccess) return e;
+  if (args.ntq <= 0 || args.batch <= 0) return cudaSuccess;
+  dim3 grid(args.ntq, args.hkv, args.batch);
+  chunk_attention_kernel<<<grid, kCThreads, kCSmemBytes, s>>>(args);
+  return cudaGetLastError();
+}
+
+}  // namespace kvarn

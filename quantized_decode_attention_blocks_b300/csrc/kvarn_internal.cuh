@@ -181,6 +181,28 @@ DecodePlan fp16_decode_plan(int batch, int hq, int hkv, int max_seq, int num_sms
 cudaError_t launch_fp16_write(const F16WriteArgs& a, cudaStream_t s);
 cudaError_t launch_fp16_decode(const F16DecodeArgs& a, const void* pool, cudaStream_t s);
 
+// Chunked prefill: attention of a chunk of query tokens over the quantized cache.
+struct ChunkArgs {
+  const __half* q;            // [batch][M][hq][128]
+  int M;                      // query tokens per sequence in q / out
+  const int32_t* start;       // [batch] tokens before the chunk
+  const int32_t* chunk_lens;  // [batch] query tokens of the chunk (<= M)
+  int batch, max_seq, hq, hkv, g;
+  int tq;                     // query tokens per 128-row tile (128 / g)
+  int ntq;                    // tiles per sequence, ceil(M / tq)
+  const uint8_t* pool;
+  int64_t num_pages;
+  const int32_t* block_table;
+  int max_blocks;
+  const __half* tail_k;
+  const __half* tail_v;
+  float scale_log2;           // softmax scale * log2(e)
+  __half* out;                // [batch][M][hq][128]
+  int32_t* status;
+};
+int chunk_rows_per_tile(int g);
+cudaError_t launch_chunk_attention(const ChunkArgs& a, cudaStream_t s);
+
 __device__ __forceinline__ void report(int32_t* status, int bits) {
   if (status) atomicOr(status, bits);
 }

@@ -40,6 +40,7 @@
 //    with 1.5 * 2^23, whose low mantissa bits are then the code.
 #include <cuda.h>
 #include <stddef.h>
+#include <string.h>
 
 #include "kvarn_internal.cuh"
 #include "ptx.cuh"
@@ -108,6 +109,17 @@ struct QTileArgs {
   uint8_t* pool;
   int64_t num_pages;
   int32_t* status;
+};
+
+// The plain copies folded into the same launch: mode 0 copies every
+// sequence's leftover len % 128 tokens to its tail, mode 1 copies the new
+// token into tail slot pos % 128.
+struct QCopyArgs {
+  const __half* src_k;         // mode 0: k, v with strides sb, st, sh; mode 1: k_new, v_new
+  const __half* src_v;
+  int64_t sb, st, sh;
+  __half* tail_k;
+  __half* tail_v;
 };
 
 // One tile of the tile space.  Mode 0: id = ((b * nb + j) * hkv + h) * 2 + part.
@@ -243,6 +255,52 @@ __device__ __forceinline__ void frag_moments(const float (&v)[64], const float2 
 
 __device__ __forceinline__ int lane4(int tid) { return tid & 3; }
 
+// Mode 1: copies the new token of every candidate tile of this CTA (pipeline
+// tiles blockIdx.x * kWG + wg + k * nw, i.e. (sequence, head, part)) into its
+// tail slot pos % 128; 16 threads per 256-byte row.  Returns whether one of
+// them filled its block (slot 127), i.e. whether the CTA has a tile to
+// quantize.  The writes are made visible to the TMA engine (async proxy)
+// before the CTA's barrier that follows.
+__device__ __forceinline__ bool append_copy(const QTileArgs& a, const QCopyArgs& cp, int nw) {
+  int fills = 0;
+  for (int i = threadIdx.x;; i += blockDim.x) {
+    const int ci = i >> 4, c = i & 15;
+    const int id = blockIdx.x * kWG + (ci & 1) + (ci >> 1) * nw;   // increasing in ci
+    if (id >= a.ntiles) break;
+    const int part = id & 1, bh = id >> 1;                      // bh = b * hkv + h
+    const int p = __ldg(a.pos + bh / a.hkv);
+    if (p < 0) continue;
+    const __half* src = (part ? cp.src_v : cp.src_k) + (int64_t)bh * kD;
+    __half* dst = (part ? cp.tail_v : cp.tail_k) + ((int64_t)bh * kT + p % kT) * kD;
+    reinterpret_cast<uint4*>(dst)[c] = __ldg(reinterpret_cast<const uint4*>(src) + c);
+    if (c == 0 && p % kT == kT - 1) fills = 1;
+  }
+  asm volatile("fence.proxy.async.global;" ::: "memory");
+  return fills != 0;
+}
+
+// Mode 0: the leftover len % 128 tokens of every (sequence, head, part) to the
+// tail buffer, 16-byte chunks spread over the whole grid (grid-stride).
+__device__ __forceinline__ void tail_copy(const QTileArgs& a, const QCopyArgs& cp) {
+  const int64_t rows = (int64_t)a.batch * a.hkv * 2 * kT;
+  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < rows * 16;
+       i += (int64_t)gridDim.x * blockDim.x) {
+    const int c = (int)(i & 15);
+    const int64_t row = i >> 4;
+    const int r = (int)(row % kT);
+    const int64_t unit = row / kT;                  // (b * hkv + h) * 2 + part
+    const int part = (int)(unit & 1);
+    const int64_t bh = unit >> 1;
+    const int b = (int)(bh / a.hkv), h = (int)(bh % a.hkv);
+    const int len = __ldg(a.seq_lens + b);
+    if (len < 0 || len > a.max_seq || r >= len % kT) continue;
+    const __half* src = (part ? cp.src_v : cp.src_k) + (int64_t)b * cp.sb + (int64_t)h * cp.sh +
+                        ((int64_t)(len / kT) * kT + r) * cp.st;
+    __half* dst = (part ? cp.tail_v : cp.tail_k) + (bh * kT + r) * kD;
+    reinterpret_cast<uint4*>(dst)[c] = __ldg(reinterpret_cast<const uint4*>(src) + c);
+  }
+}
+
 __device__ __forceinline__ bool keep_scale(float mean, float var) {
   // variance <= 1e-10 * mean square (mean square = var + mean^2): skip
   return !(var > 1e-10f * (var + mean * mean));
@@ -255,12 +313,22 @@ __device__ __forceinline__ uint32_t hs_bits(int n, int k) {
 
 __global__ void __launch_bounds__(kQThreads, 1)
     quantize_tc_kernel(const __grid_constant__ CUtensorMap tmk,
-                       const __grid_constant__ CUtensorMap tmv, const QTileArgs a) {
+                       const __grid_constant__ CUtensorMap tmv, const QTileArgs a,
+                       const __grid_constant__ QCopyArgs cp) {
   extern __shared__ uint8_t smem_raw[];
   QSmem& S = *reinterpret_cast<QSmem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                        ~static_cast<uintptr_t>(1023));
   const int tid = threadIdx.x, wg = tid / kWGThreads, wt = tid % kWGThreads;
   const int warp = tid >> 5;
+  const int nw = gridDim.x * kWG;
+  // the plain copies of this launch; a CTA with no block to quantize leaves
+  // before it sets anything up
+  if (a.mode == 1) {
+    if (!__syncthreads_or(append_copy(a, cp, nw))) return;
+  } else if (a.ntiles == 0) {
+    tail_copy(a, cp);
+    return;
+  }
   // roles in a pipeline: wt 0 issues the bulk stores of the packed output;
   // lane 0 of warps 4 and 5 (idle during the first row step, which warps 0-3
   // do) issue the tile's MMAs and the next tile's load
@@ -304,7 +372,6 @@ __global__ void __launch_bounds__(kQThreads, 1)
   tc_fence_after();
   const uint32_t tmem = S.tmem_base;
 
-  const int nw = gridDim.x * kWG;
   const int rh = a.roles & 3, rt = (a.roles >> 2) & 3;   // tensor-map dims of head, token
   // bounded waits; once one has run out every later wait is skipped, so that
   // the kernel still ends (with KVARN_STATUS_TIMEOUT reported)
@@ -672,36 +739,7 @@ __global__ void __launch_bounds__(kQThreads, 1)
   __syncthreads();
   tc_fence_after();
   if (warp == 0) tmem_dealloc(tmem, kTmemCols);
-}
-
-// Leftover tokens (len mod 128) of every sequence copied to its tail buffer.
-// grid: (2 * hkv, batch); block 128.
-__global__ void __launch_bounds__(128) tail_copy_kernel(QuantizeArgs a) {
-  const int b = blockIdx.y, h = blockIdx.x >> 1, part = blockIdx.x & 1;
-  const int len = a.seq_lens[b];
-  if (len < 0 || len > a.max_seq) return;
-  const int nfull = len / kT, rem = len % kT;
-  const __half* src = (part ? a.v : a.k) + (int64_t)b * a.sb + (int64_t)h * a.sh;
-  __half* tail = (part ? a.tail_v : a.tail_k) + ((int64_t)b * a.hkv + h) * kT * kD;
-  for (int i = threadIdx.x; i < rem * (kD / 8); i += blockDim.x) {
-    const int r = i / (kD / 8), c = i % (kD / 8);
-    const uint4* s4 = reinterpret_cast<const uint4*>(src + ((int64_t)nfull * kT + r) * a.st);
-    reinterpret_cast<uint4*>(tail + (int64_t)r * kD)[c] = __ldg(s4 + c);
-  }
-}
-
-// Decode-time append: token pos[b] into tail slot pos % 128.  grid: (2 * hkv,
-// batch); block 32 (16 lanes copy the 256 bytes).
-__global__ void __launch_bounds__(32) append_copy_kernel(AppendArgs a) {
-  const int b = blockIdx.y, h = blockIdx.x >> 1, part = blockIdx.x & 1;
-  const int p = a.pos[b];
-  if (p < 0) return;
-  const int slot = p % kT;
-  __half* tail = (part ? a.tail_v : a.tail_k) + ((int64_t)b * a.hkv + h) * kT * kD;
-  const __half* src = (part ? a.v_new : a.k_new) + ((int64_t)b * a.hkv + h) * kD;
-  if (threadIdx.x < kD / 8)
-    reinterpret_cast<uint4*>(tail + (int64_t)slot * kD)[threadIdx.x] =
-        __ldg(reinterpret_cast<const uint4*>(src) + threadIdx.x);
+  if (a.mode == 0) tail_copy(a, cp);
 }
 
 // ------------------------------------------------------------- host side --
@@ -765,16 +803,16 @@ bool encode_tile_map(CUtensorMap* map, const void* base, int64_t sb, int64_t st,
 constexpr int kQSmemBytes = (int)sizeof(QSmem) + 1024;
 
 cudaError_t launch_tiles(const CUtensorMap& mk, const CUtensorMap& mv, const QTileArgs& qa,
-                         cudaStream_t s) {
+                         const QCopyArgs& cp, cudaStream_t s) {
   static std::atomic<uint64_t> smem_set{0};
   cudaError_t e = ensure_dynamic_smem(quantize_tc_kernel, kQSmemBytes, smem_set);
   if (e != cudaSuccess) return e;
-  if (qa.ntiles <= 0) return cudaSuccess;
   const int sms = device_sm_count();
   if (sms <= 0) return cudaErrorNoDevice;
   const int want = (qa.ntiles + kWG - 1) / kWG;
-  const int grid = want < sms ? want : sms;
-  quantize_tc_kernel<<<grid, kQThreads, kQSmemBytes, s>>>(mk, mv, qa);
+  // one CTA at least: with no tile to quantize it still does the copies
+  const int grid = want < 1 ? 1 : want < sms ? want : sms;
+  quantize_tc_kernel<<<grid, kQThreads, kQSmemBytes, s>>>(mk, mv, qa, cp);
   return cudaGetLastError();
 }
 
@@ -812,28 +850,32 @@ cudaError_t launch_quantize_blocks(const QuantizeArgs& a, cudaStream_t s) {
   qa.pool = a.pool;
   qa.num_pages = a.num_pages;
   qa.status = a.status;
+  QCopyArgs cp{};
+  cp.src_k = a.k;
+  cp.src_v = a.v;
+  cp.sb = a.sb;
+  cp.st = a.st;
+  cp.sh = a.sh;
+  cp.tail_k = a.tail_k;
+  cp.tail_v = a.tail_v;
+  CUtensorMap mk, mv;
+  memset(&mk, 0, sizeof(mk));
+  memset(&mv, 0, sizeof(mv));
   if (qa.ntiles > 0) {
-    CUtensorMap mk, mv;
     int rk = 0, rv = 0;
     if (!encode_tile_map(&mk, a.k, a.sb, a.st, a.sh, a.batch, a.max_seq, a.hkv, &rk) ||
         !encode_tile_map(&mv, a.v, a.sb, a.st, a.sh, a.batch, a.max_seq, a.hkv, &rv) || rk != rv)
       return cudaErrorInvalidValue;
     qa.roles = rk;
-    cudaError_t e = launch_tiles(mk, mv, qa, s);
-    if (e != cudaSuccess) return e;
   }
-  dim3 grid(2 * a.hkv, a.batch);
-  tail_copy_kernel<<<grid, 128, 0, s>>>(a);
-  return cudaGetLastError();
+  // the tiles and the leftover-token copies, one launch
+  return launch_tiles(mk, mv, qa, cp, s);
 }
 
 cudaError_t launch_append_token(const AppendArgs& a, cudaStream_t s) {
-  dim3 grid(2 * a.hkv, a.batch);
-  append_copy_kernel<<<grid, 32, 0, s>>>(a);
-  cudaError_t e = cudaGetLastError();
-  if (e != cudaSuccess) return e;
-  // tails whose block just filled: same kernel as the prefill, reading the tail
-  // buffers [B][Hkv][128][128]
+  // one launch: every CTA copies the new tokens of its candidate tiles into
+  // the tails, and the tails whose block just filled are quantized by the
+  // same kernel as the prefill, reading the tail buffers [B][Hkv][128][128]
   QTileArgs qa{};
   qa.mode = 1;
   qa.batch = a.batch;
@@ -848,6 +890,11 @@ cudaError_t launch_append_token(const AppendArgs& a, cudaStream_t s) {
   qa.pool = a.pool;
   qa.num_pages = a.num_pages;
   qa.status = a.status;
+  QCopyArgs cp{};
+  cp.src_k = a.k_new;
+  cp.src_v = a.v_new;
+  cp.tail_k = a.tail_k;
+  cp.tail_v = a.tail_v;
   CUtensorMap mk, mv;
   int rk = 0, rv = 0;
   const int64_t sh = (int64_t)kT * kD, sb = sh * a.hkv;
@@ -855,7 +902,7 @@ cudaError_t launch_append_token(const AppendArgs& a, cudaStream_t s) {
       !encode_tile_map(&mv, a.tail_v, sb, kD, sh, a.batch, kT, a.hkv, &rv))
     return cudaErrorInvalidValue;
   qa.roles = rk;
-  return launch_tiles(mk, mv, qa, s);
+  return launch_tiles(mk, mv, qa, cp, s);
 }
 
 }  // namespace kvarn

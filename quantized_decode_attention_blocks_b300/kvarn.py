@@ -69,6 +69,8 @@ SIGNATURES = {
                                     _P, ctypes.c_float, _P, _P, ctypes.c_size_t, _P, _P]),
     "kvarn_decode_attention_noalloc": (_I, [ctypes.POINTER(Config), _P, _P, _L, _P, _I, _P, _I,
                                             _I, _P, _P, ctypes.c_float, _P, _P, _P]),
+    "kvarn_chunk_attention": (_I, [ctypes.POINTER(Config), _P, _I, _P, _P, _I, _I, _P, _L, _P,
+                                   _I, _P, _P, ctypes.c_float, _P, _P, _P]),
     "kvarn_dequantize_pages": (_I, [_P, _L, _P, _P, _P]),
     "kvarn_fp16_write_blocks": (_I, [_P, _P, _L, _L, _L, _I, _I, _P, _I, _P, _I, _P, _L, _P,
                                      _P]),
@@ -317,6 +319,32 @@ def kvarn_decode_attention(cfg: Config, q: torch.Tensor, pool: torch.Tensor,
             block_table.shape[-1], _ptr(seq_lens), q.shape[0], int(max_seq), _ptr(tail_k),
             _ptr(tail_v), float(softmax_scale), _ptr(out), _ptr(workspace), ws_bytes,
             _ptr(status), _stream(stream, dev)), "kvarn_decode_attention")
+    return out
+
+
+def kvarn_chunk_attention(cfg: Config, q: torch.Tensor, start: torch.Tensor,
+                          chunk_lens: torch.Tensor, max_seq: int, pool: torch.Tensor,
+                          block_table: torch.Tensor, tail_k: torch.Tensor, tail_v: torch.Tensor,
+                          out: torch.Tensor, softmax_scale: float = None,
+                          status: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+    """Chunked prefill: q, out fp16 [B][M][Hq][128]; start, chunk_lens int32
+    [B]; the cache holds start + chunk_lens tokens per sequence."""
+    dev = _arg(q, "q", torch.float16, (None, None, cfg.num_q_heads, HEAD_DIM))
+    _arg(out, "out", torch.float16, tuple(q.shape), device=dev)
+    B = q.shape[0]
+    _lens_table(dev, B, start, "start", block_table)
+    _arg(chunk_lens, "chunk_lens", torch.int32, (_AtLeast(B),), device=dev)
+    _arg(pool, "pool", torch.uint8, (None, cfg.num_kv_heads, PAGE_BYTES), device=dev)
+    _tails(dev, cfg, B, tail_k, tail_v)
+    _status(dev, status)
+    if softmax_scale is None:
+        softmax_scale = HEAD_DIM ** -0.5
+    with _on(dev):
+        _check(lib().kvarn_chunk_attention(
+            ctypes.byref(cfg), _ptr(q), q.shape[1], _ptr(start), _ptr(chunk_lens), B,
+            int(max_seq), _ptr(pool), pool.shape[0], _ptr(block_table), block_table.shape[-1],
+            _ptr(tail_k), _ptr(tail_v), float(softmax_scale), _ptr(out), _ptr(status),
+            _stream(stream, dev)), "kvarn_chunk_attention")
     return out
 
 
