@@ -26,14 +26,16 @@
 //   O  += P V^      tcgen05.mma with A = P from TMEM, N = 128 channels, K = 128
 //                  tokens, as P Vhi + P Vlo, fp32 in TMEM.
 // Roles: warps 0-3 build Q~ once and run the softmax (thread r = TMEM lane r =
-// row r); warps 4-6 bring each page record in with one bulk copy (two buffers,
-// two blocks ahead) and dequantize it into the K^ and V^ (hi, lo) operands in
-// shared memory; one thread of warp 7 issues the MMAs, S one block ahead of
-// PV into two S buffers in TMEM, so the tensor cores work on the next block's
-// scores while the softmax warps work on this block's.  The hand-offs are
-// mbarriers, every wait bounded (KVARN_STATUS_TIMEOUT).  At the end each
-// softmax thread reads its row of O, divides by l, rotates it back with a
-// register FWHT and writes fp16.
+// row r); between the two passes over a block's scores they also dequantize
+// its values into the V^ (hi, lo) operands.  Warps 4-6 bring each page record
+// in with one bulk copy (two buffers, one block ahead) and dequantize its keys
+// into the K^ (hi, lo) operands (the fp16 tail is rotated on the way in).  One
+// thread of warp 7 issues the MMAs, polling for whichever of the next S (one
+// block ahead, two S buffers in TMEM) or the next PV has its inputs ready, so
+// the tensor cores work on the next block's scores while the softmax warps
+// work on this block's.  The hand-offs are mbarriers, every wait bounded
+// (KVARN_STATUS_TIMEOUT).  At the end each softmax thread reads its row of O,
+// divides by l, rotates it back with a register FWHT and writes fp16.
 #include "kvarn_internal.cuh"
 #include "ptx.cuh"
 
@@ -67,6 +69,7 @@ struct __align__(1024) CSmem {
   uint8_t raw[2][kRec];   // page records in flight
   uint64_t raw_full[2];
   uint64_t sdone[2];      // S of a block ready, per S buffer
+  uint64_t rawfree[2];    // a page buffer's keys and values are dequantized
   uint64_t qready, kready, vready, pready, pvdone, drain;
   uint32_t tmem_base;
   int abort;
@@ -144,73 +147,97 @@ __device__ __forceinline__ float code_f(uint32_t q) {   // small integer -> floa
   return __int_as_float(0x4B000000 | q) - 8388608.f;
 }
 
-// Page tokens: yhatK_td = c_d (s'_t q_td + z'_t) into the K^ operands, item
-// x = 4 t + c4 = channels 32 c4 .. 32 c4 + 31 of token t; dequant thread dt
-// takes items dt, dt + 96, ...  rk: the record's K part.
-__device__ __forceinline__ void dequant_k(const uint8_t* rk, uint8_t* kh, uint8_t* kl, int dt) {
-  const float4* cv = reinterpret_cast<const float4*>(rk + kOffKC);
+// Page tokens: yhatK_td = c_d (s'_t q_td + z'_t) into the K^ operands.  Lane:
+// chunk cc = lane & 15 (channels 8 cc .. 8 cc + 7, code word cc of a token
+// row), t0 = lane >> 4; dequant warp dw takes the token pairs p = dw, dw + 3,
+// ... of 64, token 2p + t0.  The code loads hit 32 banks, the column scales
+// of the lane's chunk are loaded once.  rk: the record's K part.
+__device__ __forceinline__ void dequant_k(const uint8_t* rk, uint8_t* kh, uint8_t* kl, int dw,
+                                          int lane) {
+  const int cc = lane & 15, t0 = lane >> 4;
+  const float4 ca = reinterpret_cast<const float4*>(rk + kOffKC)[2 * cc];
+  const float4 cb = reinterpret_cast<const float4*>(rk + kOffKC)[2 * cc + 1];
+  const float cs[8] = {ca.x, ca.y, ca.z, ca.w, cb.x, cb.y, cb.z, cb.w};
+  // four token pairs per step: independent loads and math in flight
+  constexpr int kStep = 4 * kDeqWarps;
 #pragma unroll 1
-  for (int x = dt; x < 4 * kT; x += 32 * kDeqWarps) {
-    const int t = x >> 2, c4 = x & 3;
-    const float2 sz = *reinterpret_cast<const float2*>(rk + kOffKSZ + 8 * t);
-    const uint4 w4 = reinterpret_cast<const uint4*>(rk + kOffKCodes + 64 * t)[c4];
-    const uint32_t ws[4] = {w4.x, w4.y, w4.z, w4.w};
+  for (int p0 = dw; p0 < kT / 2; p0 += kStep) {
+    uint32_t w[4];
+    float2 sz[4];
 #pragma unroll
-    for (int e = 0; e < 4; ++e) {
-      const int cc = 4 * c4 + e;   // channels 8 cc .. 8 cc + 7: nibble k = channel 8 cc + k
-      const float4 ca = cv[2 * cc], cb = cv[2 * cc + 1];
-      const float cs[8] = {ca.x, ca.y, ca.z, ca.w, cb.x, cb.y, cb.z, cb.w};
+    for (int u = 0; u < 4; ++u) {
+      const int t = 2 * min(p0 + kDeqWarps * u, kT / 2 - 1) + t0;
+      w[u] = *reinterpret_cast<const uint32_t*>(rk + kOffKCodes + 64 * t + 4 * cc);
+      sz[u] = *reinterpret_cast<const float2*>(rk + kOffKSZ + 8 * t);
+    }
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int p = p0 + kDeqWarps * u;
+      if (p >= kT / 2) break;
       float y[8];
 #pragma unroll
-      for (int k = 0; k < 8; ++k) y[k] = cs[k] * fmaf(sz.x, code_f((ws[e] >> (4 * k)) & 15u), sz.y);
-      store_hilo8(kh, kl, t, cc, y);
+      for (int k = 0; k < 8; k += 2) {
+        const float2 q2 = make_float2(code_f((w[u] >> (4 * k)) & 15u),
+                                      code_f((w[u] >> (4 * k + 4)) & 15u));
+        const float2 v = __fmul2_rn(make_float2(cs[k], cs[k + 1]),
+                                    __ffma2_rn(make_float2(sz[u].x, sz[u].x), q2,
+                                               make_float2(sz[u].y, sz[u].y)));
+        y[k] = v.x;
+        y[k + 1] = v.y;
+      }
+      store_hilo8(kh, kl, 2 * p + t0, cc, y);
     }
   }
 }
 
-// Page tokens: yhatV into the V^ operand [channel][token].  Lane:
-// j = lane & 3, h = (lane >> 2) & 1, e = (lane >> 3) & 1, r0 = lane >> 4; round
-// k (of 32, dequant warp dw takes k = dw, dw + 3, ...) is m = k >> 2 and
-// r = 2 (k & 3) + r0, and reads word 128m + 16r + 4j + 2e + h of the permuted
-// V code layout: channel c = 16m + 8e + r, tokens 16k' + 8f + 2j + s for
-// k' = 4h .. 4h + 3.  Lanes of one load differ in (j, h, e, r0): 32 banks.
+// Page tokens: yhatV into the V^ operands [channel][token].  Lane: j = lane &
+// 3, r = lane >> 2; for each h (0, 1) warp dw of NW takes the rounds k2 =
+// dw, dw + NW, ... of 16, m = k2 >> 1, e = k2 & 1, and reads word
+// 128m + 16r + 4j + 2e + h of the permuted V code layout: channel
+// c = 16m + 8e + r, tokens 16k + 8f + 2j + s for k = 4h .. 4h + 3.  The lanes
+// of one store differ in (r, j), i.e. in 32 banks.
+template <int NW>
 __device__ __forceinline__ void dequant_v(const uint8_t* rv, uint8_t* vh, uint8_t* vl, int dw,
                                           int lane) {
-  const int j2 = lane & 3, hb = (lane >> 2) & 1, e = (lane >> 3) & 1, r0 = lane >> 4;
+  const int j2 = lane & 3, r = lane >> 2;
   const uint8_t* vsz = rv + (kOffVSZ - kKPart);
   const uint32_t* words = reinterpret_cast<const uint32_t*>(rv + (kOffVCodes - kKPart));
   const float* vc = reinterpret_cast<const float*>(rv + (kOffVC - kKPart));
-  float2 sz[4][2][2];
-#pragma unroll
-  for (int kk = 0; kk < 4; ++kk)
-#pragma unroll
-    for (int f = 0; f < 2; ++f)
-#pragma unroll
-      for (int s = 0; s < 2; ++s)
-        sz[kk][f][s] = *reinterpret_cast<const float2*>(
-            vsz + 8 * (16 * (4 * hb + kk) + 8 * f + 2 * j2 + s));
 #pragma unroll 1
-  for (int k = dw; k < 32; k += kDeqWarps) {
-    const int m = k >> 2, r = 2 * (k & 3) + r0;
-    const int c = 16 * m + 8 * e + r;
-    const uint32_t w = words[128 * m + 16 * r + 4 * j2 + 2 * e + hb];
-    const float cd = vc[c];
+  for (int hb = 0; hb < 2; ++hb) {
+    float2 sz[4][2][2];
 #pragma unroll
     for (int kk = 0; kk < 4; ++kk)
 #pragma unroll
-      for (int f = 0; f < 2; ++f) {
-        const int i0 = 2 * kk + f;   // crumb of s = 0; s = 1 is crumb i0 + 8
-        const float y0 = cd * fmaf(sz[kk][f][0].x, code_f((w >> (2 * i0)) & 3u), sz[kk][f][0].y);
-        const float y1 =
-            cd * fmaf(sz[kk][f][1].x, code_f((w >> (2 * i0 + 16)) & 3u), sz[kk][f][1].y);
-        const int u = 2 * (4 * hb + kk) + f;   // tokens 8u .. 8u + 7; these are 2 j2, 2 j2 + 1
-        const uint32_t off =
-            (uint32_t)((u >> 3) * kOpBox + c * 128 + (((u & 7) ^ (c & 7)) << 4) + 4 * j2);
-        uint32_t hi, lo;
-        split2(y0, y1, hi, lo);
-        *reinterpret_cast<uint32_t*>(vh + off) = hi;
-        *reinterpret_cast<uint32_t*>(vl + off) = lo;
-      }
+      for (int f = 0; f < 2; ++f)
+#pragma unroll
+        for (int s = 0; s < 2; ++s)
+          sz[kk][f][s] = *reinterpret_cast<const float2*>(
+              vsz + 8 * (16 * (4 * hb + kk) + 8 * f + 2 * j2 + s));
+#pragma unroll 2
+    for (int k2 = dw; k2 < 16; k2 += NW) {
+      const int m = k2 >> 1, e = k2 & 1;
+      const int c = 16 * m + 8 * e + r;
+      const uint32_t w = words[128 * m + 16 * r + 4 * j2 + 2 * e + hb];
+      const float cd = vc[c];
+#pragma unroll
+      for (int kk = 0; kk < 4; ++kk)
+#pragma unroll
+        for (int f = 0; f < 2; ++f) {
+          const int i0 = 2 * kk + f;   // crumb of s = 0; s = 1 is crumb i0 + 8
+          const float y0 =
+              cd * fmaf(sz[kk][f][0].x, code_f((w >> (2 * i0)) & 3u), sz[kk][f][0].y);
+          const float y1 =
+              cd * fmaf(sz[kk][f][1].x, code_f((w >> (2 * i0 + 16)) & 3u), sz[kk][f][1].y);
+          const int u = 2 * (4 * hb + kk) + f;   // tokens 8u .. 8u + 7; these are 2 j2, 2 j2 + 1
+          const uint32_t off =
+              (uint32_t)((u >> 3) * kOpBox + c * 128 + (((u & 7) ^ (c & 7)) << 4) + 4 * j2);
+          uint32_t hi, lo;
+          split2(y0, y1, hi, lo);
+          *reinterpret_cast<uint32_t*>(vh + off) = hi;
+          *reinterpret_cast<uint32_t*>(vl + off) = lo;
+        }
+    }
   }
 }
 
@@ -263,9 +290,11 @@ __global__ void __launch_bounds__(kCThreads, 1)
   if (tid == 0) {
     mbar_init(&S.raw_full[0], 1);
     mbar_init(&S.raw_full[1], 1);
+    mbar_init(&S.rawfree[0], kSoftWarps + kDeqWarps);
+    mbar_init(&S.rawfree[1], kSoftWarps + kDeqWarps);
     mbar_init(&S.qready, kSoftWarps);
     mbar_init(&S.kready, kDeqWarps);
-    mbar_init(&S.vready, kDeqWarps);
+    mbar_init(&S.vready, kSoftWarps);
     mbar_init(&S.sdone[0], 1);
     mbar_init(&S.sdone[1], 1);
     mbar_init(&S.pready, kSoftWarps);
@@ -316,8 +345,10 @@ __global__ void __launch_bounds__(kCThreads, 1)
     if (lane == 0) mbar_arrive(&S.qready);
 
     const uint32_t tl = tmem + ((uint32_t)(32 * warp) << 16), tO = tl + kColO, tP = tl + kColP;
+    const __half* tvb = a.tail_v + ((int64_t)b * a.hkv + kvh) * kT * kD;
     float m_ref = -INFINITY, l = 0.f;
     for (int j = 0; j < nblk; ++j) {
+      const bool page = j < nfull;
       // S of block j is in buffer j & 1; two passes over it in 32-column pieces
       // (the maximum, then the probabilities), so no row sits in registers
       wait(&S.sdone[j & 1], (j >> 1) & 1);
@@ -346,11 +377,10 @@ __global__ void __launch_bounds__(kCThreads, 1)
         l *= alpha;
       }
       if (grow) m_ref = mb;
-      bool o_free = j == 0;                         // PV of the block before is done
+      // PV of the block before is done: O is stable, V^ and P are free
+      if (j > 0) wait(&S.pvdone, (j - 1) & 1);
+      tc_fence_after();
       if (__any_sync(0xffffffffu, resc)) {
-        wait(&S.pvdone, (j - 1) & 1);
-        o_free = true;
-        tc_fence_after();
 #pragma unroll
         for (int c4 = 0; c4 < 4; ++c4) {
           float o[32];
@@ -362,7 +392,40 @@ __global__ void __launch_bounds__(kCThreads, 1)
         }
         tmem_wait_st();
       }
-      if (!o_free) wait(&S.pvdone, (j - 1) & 1);   // the P buffer is free again
+      // ---- this block's values into V^ ----
+      if (page) {
+        wait(&S.raw_full[j & 1], (j >> 1) & 1);
+        dequant_v<kSoftWarps>(S.raw[j & 1] + kKPart, S.vh, S.vl, warp, lane);
+      } else {
+        // the fp16 tail, rotated: column t = tid of V^ [channel][token]
+        const int t = tid;
+        float x[128];
+        if (t < rem) {
+          load_row(tvb + (int64_t)t * kD, x);
+          fwht128(x);
+#pragma unroll
+          for (int d = 0; d < 128; ++d) x[d] *= kInvSqrt128;
+        } else {
+#pragma unroll
+          for (int d = 0; d < 128; ++d) x[d] = 0.f;
+        }
+        const uint32_t tb = (uint32_t)((t >> 6) * kOpBox + (t & 7) * 2);
+        const int tc = (t & 63) >> 3;
+#pragma unroll
+        for (int d = 0; d < 128; ++d) {
+          const __half h = __float2half_rn(x[d]);
+          const uint32_t o = tb + d * 128 + ((tc ^ (d & 7)) << 4);
+          *reinterpret_cast<__half*>(S.vh + o) = h;
+          *reinterpret_cast<__half*>(S.vl + o) = __float2half_rn(x[d] - __half2float(h));
+        }
+      }
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) {
+        mbar_arrive(&S.vready);
+        if (page) mbar_arrive(&S.rawfree[j & 1]);
+      }
+      // ---- pass 2: P = 2^(S - m) as fp16 pairs into TMEM ----
       const bool any = m_ref != -INFINITY;
       float ls = 0.f;
 #pragma unroll
@@ -420,13 +483,13 @@ __global__ void __launch_bounds__(kCThreads, 1)
       }
     }
   } else if (warp < kSoftWarps + kDeqWarps) {
-    // ================= dequant warps: pages and the tail into operands =================
+    // ================= dequant warps: page records in, keys into K^ =================
     const int dt = tid - kDeq0, dw = dt >> 5;
     auto rec_of = [&](int j) {
       return a.pool + ((int64_t)trow[j] * a.hkv + kvh) * (int64_t)kRec;
     };
     // loads issued and seen complete per buffer (thread dt == 0), as
-    // issued0 | issued1 << 16 etc. so that no array sits in local memory
+    // count0 | count1 << 16 so that no array sits in local memory
     uint32_t issued = 0, seen = 0;
     auto issue = [&](int j) {
       uint64_t* bar = &S.raw_full[j & 1];
@@ -434,22 +497,21 @@ __global__ void __launch_bounds__(kCThreads, 1)
       bulk_g2s(S.raw[j & 1], rec_of(j), kRec, bar);
       issued += 1u << (16 * (j & 1));
     };
+    const int npages = min(nblk, nfull);
     if (dt == 0) {
-      if (0 < min(nblk, nfull)) issue(0);
-      if (1 < min(nblk, nfull)) issue(1);
+      if (0 < npages) issue(0);
+      if (1 < npages) issue(1);
     }
     const __half* tkb = a.tail_k + ((int64_t)b * a.hkv + kvh) * kT * kD;
-    const __half* tvb = a.tail_v + ((int64_t)b * a.hkv + kvh) * kT * kD;
     for (int j = 0; j < nblk; ++j) {
       const bool page = j < nfull;
-      const uint8_t* rk = S.raw[j & 1];
       if (page) {
         wait(&S.raw_full[j & 1], (j >> 1) & 1);
         if (dt == 0 && !*reinterpret_cast<volatile int*>(&S.abort)) seen += 1u << (16 * (j & 1));
       }
       if (j > 0) wait(&S.sdone[(j - 1) & 1], ((j - 1) >> 1) & 1);   // S of block j-1 read K^
       if (page) {
-        dequant_k(rk, S.kh, S.kl, dt);
+        dequant_k(S.raw[j & 1], S.kh, S.kl, dw, lane);
       } else {
         // the fp16 tail, rotated into the pages' space: yhat = H x / sqrt(128)
 #pragma unroll 1
@@ -470,42 +532,16 @@ __global__ void __launch_bounds__(kCThreads, 1)
       }
       fence_proxy_async_smem();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&S.kready);
-      if (j > 0) wait(&S.pvdone, (j - 1) & 1);     // PV of the block before read V^
-      if (page) {
-        dequant_v(rk + kKPart, S.vh, S.vl, dw, lane);
-      } else {
-#pragma unroll 1
-        for (int t = dt; t < kT; t += 32 * kDeqWarps) {
-          float x[128];
-          if (t < rem) {
-            load_row(tvb + (int64_t)t * kD, x);
-            fwht128(x);
-#pragma unroll
-            for (int d = 0; d < 128; ++d) x[d] *= kInvSqrt128;
-          } else {
-#pragma unroll
-            for (int d = 0; d < 128; ++d) x[d] = 0.f;
-          }
-          // column t of V^ [channel][token]
-          const uint32_t tb = (uint32_t)((t >> 6) * kOpBox + (t & 7) * 2);
-          const int tc = (t & 63) >> 3;
-#pragma unroll
-          for (int d = 0; d < 128; ++d) {
-            const __half h = __float2half_rn(x[d]);
-            const uint32_t o = tb + d * 128 + ((tc ^ (d & 7)) << 4);
-            *reinterpret_cast<__half*>(S.vh + o) = h;
-            *reinterpret_cast<__half*>(S.vl + o) = __float2half_rn(x[d] - __half2float(h));
-          }
-        }
+      if (lane == 0) {
+        mbar_arrive(&S.kready);
+        if (page) mbar_arrive(&S.rawfree[j & 1]);
       }
-      fence_proxy_async_smem();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&S.vready);
-      // every dequant thread is done with raw[j & 1]: load block j + 2 into it
-      named_sync(1, 32 * kDeqWarps);
-      if (dt == 0 && j + 2 < min(nblk, nfull) && !*reinterpret_cast<volatile int*>(&S.abort))
-        issue(j + 2);
+      // the buffer of block j - 1 is free once its values are dequantized
+      // too: load block j + 1 into it
+      if (dt == 0 && j >= 1 && j + 1 < npages && !*reinterpret_cast<volatile int*>(&S.abort)) {
+        wait(&S.rawfree[(j - 1) & 1], ((j - 1) >> 1) & 1);
+        issue(j + 1);
+      }
     }
     if (dt == 0) {
       // copies still in flight (a wait gave up) land before the CTA leaves
@@ -517,52 +553,62 @@ __global__ void __launch_bounds__(kCThreads, 1)
     }
   } else if (tid == kMmaThread) {
     // ================= MMA issue =================
-    // S runs one block ahead of PV: S of block j + 1 (into S buffer (j+1) & 1,
-    // whose softmax of block j - 1 is done: its P was waited for) is issued
-    // before PV of block j, so that it overlaps the softmax of block j
+    // S_js (one block ahead, into S buffer js & 1, whose softmax of block
+    // js - 2 is done) and PV_jp are issued as soon as their inputs are ready,
+    // polled in turn, so neither waits for the other's inputs
     const uint32_t tO = tmem + kColO, tP = tmem + kColP;
     const uint32_t qh = smem_u32(S.qh), ql = smem_u32(S.ql), kh = smem_u32(S.kh),
                    kl = smem_u32(S.kl), vh = smem_u32(S.vh), vl = smem_u32(S.vl);
-    auto issue_s = [&](int j) {
-      wait(&S.kready, j & 1);
-      tc_fence_after();
-      const uint32_t tS = tmem + 128 * (j & 1);
-#pragma unroll
-      for (int kk = 0; kk < 8; ++kk) {
-        const uint32_t off = (kk >> 2) * kOpBox + (kk & 3) * 32;
-        umma_f16(tS, umma_desc_sw128(qh + off), umma_desc_sw128(kh + off), kCIdesc, kk > 0);
-      }
-#pragma unroll
-      for (int kk = 0; kk < 8; ++kk) {
-        const uint32_t off = (kk >> 2) * kOpBox + (kk & 3) * 32;
-        umma_f16(tS, umma_desc_sw128(qh + off), umma_desc_sw128(kl + off), kCIdesc, true);
-      }
-#pragma unroll
-      for (int kk = 0; kk < 8; ++kk) {
-        const uint32_t off = (kk >> 2) * kOpBox + (kk & 3) * 32;
-        umma_f16(tS, umma_desc_sw128(ql + off), umma_desc_sw128(kh + off), kCIdesc, true);
-      }
-      umma_commit(&S.sdone[j & 1]);
-    };
     wait(&S.qready, 0);
-    issue_s(0);
-    for (int j = 0; j < nblk; ++j) {
-      if (j + 1 < nblk) issue_s(j + 1);
-      wait(&S.pready, j & 1);
-      wait(&S.vready, j & 1);
-      tc_fence_after();
-      // A = P from TMEM: K step kk is tokens 16 kk .. 16 kk + 15, columns 8 kk ..
+    int js = 0, jp = 0;
+    uint64_t t_last = globaltimer();
+    while (jp < nblk && !*reinterpret_cast<volatile int*>(&S.abort)) {
+      bool progress = false;
+      if (js < nblk && js <= jp + 1 && mbar_try_wait(&S.kready, js & 1)) {
+        tc_fence_after();
+        const uint32_t tS = tmem + 128 * (js & 1);
 #pragma unroll
-      for (int kk = 0; kk < 8; ++kk) {
-        const uint32_t off = (kk >> 2) * kOpBox + (kk & 3) * 32;
-        umma_f16_ts(tO, tP + 8 * kk, umma_desc_sw128(vh + off), kCIdesc, j > 0 || kk > 0);
-      }
+        for (int kk = 0; kk < 8; ++kk) {
+          const uint32_t off = (kk >> 2) * kOpBox + (kk & 3) * 32;
+          umma_f16(tS, umma_desc_sw128(qh + off), umma_desc_sw128(kh + off), kCIdesc, kk > 0);
+        }
 #pragma unroll
-      for (int kk = 0; kk < 8; ++kk) {
-        const uint32_t off = (kk >> 2) * kOpBox + (kk & 3) * 32;
-        umma_f16_ts(tO, tP + 8 * kk, umma_desc_sw128(vl + off), kCIdesc, true);
+        for (int kk = 0; kk < 8; ++kk) {
+          const uint32_t off = (kk >> 2) * kOpBox + (kk & 3) * 32;
+          umma_f16(tS, umma_desc_sw128(qh + off), umma_desc_sw128(kl + off), kCIdesc, true);
+        }
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk) {
+          const uint32_t off = (kk >> 2) * kOpBox + (kk & 3) * 32;
+          umma_f16(tS, umma_desc_sw128(ql + off), umma_desc_sw128(kh + off), kCIdesc, true);
+        }
+        umma_commit(&S.sdone[js & 1]);
+        ++js;
+        progress = true;
       }
-      umma_commit(&S.pvdone);
+      if (jp < js && mbar_try_wait(&S.pready, jp & 1) && mbar_try_wait(&S.vready, jp & 1)) {
+        tc_fence_after();
+        // A = P from TMEM: K step kk is tokens 16 kk .. 16 kk + 15, columns 8 kk ..
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk) {
+          const uint32_t off = (kk >> 2) * kOpBox + (kk & 3) * 32;
+          umma_f16_ts(tO, tP + 8 * kk, umma_desc_sw128(vh + off), kCIdesc, jp > 0 || kk > 0);
+        }
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk) {
+          const uint32_t off = (kk >> 2) * kOpBox + (kk & 3) * 32;
+          umma_f16_ts(tO, tP + 8 * kk, umma_desc_sw128(vl + off), kCIdesc, true);
+        }
+        umma_commit(&S.pvdone);
+        ++jp;
+        progress = true;
+      }
+      if (progress) {
+        t_last = globaltimer();
+      } else if (globaltimer() - t_last > kCWaitNs) {
+        *reinterpret_cast<volatile int*>(&S.abort) = 1;
+        report(a.status, KVARN_STATUS_TIMEOUT);
+      }
     }
     // every MMA of this thread is complete before TMEM is released
     umma_commit(&S.drain);
