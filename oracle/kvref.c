@@ -36,6 +36,9 @@
  *     log(sigma) where sigma is the centred population standard deviation
  *     (divide by n) of Z = Y * exp(-a_t - b_d); a step is skipped for a row or
  *     column whose variance is <= 1e-10 * mean(Z^2) of that row or column;
+ *     format variant "_rms": sigma is the uncentred root mean square instead
+ *     (Sinkhorn-Knopp on the squares), a step skipped only for a zero row or
+ *     column;
  *   - group = the 128 channels of one token (per-token groups);
  *   - RTN: z = min, s = (max - min)/(2^b - 1), q = clamp(rint(u)) with
  *     u = (x - z)/s, ties to even; a constant group gives s = 0, q = 0;
@@ -143,6 +146,17 @@ void kvref_rotate_tile(const uint16_t *x, long ld_tok, const double *H, double *
 /* KVarN page, "KVarN Nasil Calisir?", stage "Normalize Edilmis Onbellek" */
 /* ------------------------------------------------------------------ */
 
+/* Whether a row or column step updates its scale.  Centred statistic (the
+ * reading of the KVarN page's "variance"): the step is skipped when the
+ * variance is at most 1e-10 of the mean square (constant or zero rows).
+ * Uncentred statistic (format variant "_rms": the literal Sinkhorn-Knopp
+ * scaling of the squares, sigma = root mean square): skipped only for an
+ * all-zero row or column. */
+static int step_applies(int stat, double var, double msq)
+{
+    return stat ? msq > 0.0 : var > 1e-10 * msq;
+}
+
 /* Centred population statistics of v[0..n-1], two passes. */
 static void centred_stats(const double *v, int n, double *var, double *mean_sq)
 {
@@ -160,7 +174,9 @@ static void centred_stats(const double *v, int n, double *var, double *mean_sq)
 }
 
 /* Runs `iters` iterations (row step, then column step) on the rotated tile Y
- * (NTOK x NCH).  Output: log row scales a[NTOK] and log column scales b[NCH].
+ * (NTOK x NCH) with the centred statistic (stat = 0) or the uncentred one
+ * (stat = 1, below).  Output: log row scales a[NTOK] and log column scales
+ * b[NCH].
  * trace (nullable, 4*iters entries): for iteration k, trace[4k] is the largest
  * |log sigma| over the rows that the row step updated and trace[4k+1] the
  * spread (largest minus smallest log sigma) over those rows; trace[4k+2] and
@@ -168,7 +184,8 @@ static void centred_stats(const double *v, int n, double *var, double *mean_sq)
  * statistics admit no exact joint fixed point in general (row and column means
  * differ), so log sigma settles to a common per-step offset while the spread
  * goes to zero: the spread is the convergence measure. */
-void kvref_sinkhorn(const double *Y, int iters, double *a, double *b, double *trace)
+void kvref_sinkhorn_stat(const double *Y, int iters, int stat, double *a, double *b,
+                         double *trace)
 {
     int k, t, d;
     double z[NTOK > NCH ? NTOK : NCH];
@@ -184,8 +201,8 @@ void kvref_sinkhorn(const double *Y, int iters, double *a, double *b, double *tr
             double e = exp(-a[t]);
             for (d = 0; d < NCH; ++d) z[d] = Y[t * NCH + d] * e * eb[d];
             centred_stats(z, NCH, &var, &msq);
-            if (var > 1e-10 * msq) {
-                double ls = log(sqrt(var));
+            if (step_applies(stat, var, msq)) {
+                double ls = log(sqrt(stat ? msq : var));
                 a[t] += ls;
                 if (fabs(ls) > worst) worst = fabs(ls);
                 if (ls < lo) lo = ls;
@@ -206,8 +223,8 @@ void kvref_sinkhorn(const double *Y, int iters, double *a, double *b, double *tr
             double e = exp(-b[d]);
             for (t = 0; t < NTOK; ++t) z[t] = Y[t * NCH + d] * ea[t] * e;
             centred_stats(z, NTOK, &var, &msq);
-            if (var > 1e-10 * msq) {
-                double ls = log(sqrt(var));
+            if (step_applies(stat, var, msq)) {
+                double ls = log(sqrt(stat ? msq : var));
                 b[d] += ls;
                 if (fabs(ls) > worst) worst = fabs(ls);
                 if (ls < lo) lo = ls;
@@ -219,6 +236,12 @@ void kvref_sinkhorn(const double *Y, int iters, double *a, double *b, double *tr
             trace[4 * k + 3] = hi >= lo ? hi - lo : 0.0;
         }
     }
+}
+
+/* The default (centred) statistic. */
+void kvref_sinkhorn(const double *Y, int iters, double *a, double *b, double *trace)
+{
+    kvref_sinkhorn_stat(Y, iters, 0, a, b, trace);
 }
 
 /* ------------------------------------------------------------------ */
@@ -353,9 +376,9 @@ void kvref_dequant_part(const uint8_t *rec, int is_v, double *yhat)
  * the K (is_v = 0, 4 bits) or V (is_v = 1, 2 bits) part of `rec`.  The
  * optional outputs expose every intermediate for the tests:
  * Y (rotated), a, b (log scales), q (codes), u (pre-rounding values). */
-void kvref_quantize_tile(const uint16_t *x, long ld_tok, int is_v, int iters, uint8_t *rec,
-                         double *Y_out, double *a_out, double *b_out, uint8_t *q_out,
-                         double *u_out)
+void kvref_quantize_tile_stat(const uint16_t *x, long ld_tok, int is_v, int iters, int stat,
+                              uint8_t *rec, double *Y_out, double *a_out, double *b_out,
+                              uint8_t *q_out, double *u_out)
 {
     static double H[NCH * NCH];
     static int have_h = 0;
@@ -372,7 +395,7 @@ void kvref_quantize_tile(const uint16_t *x, long ld_tok, int is_v, int iters, ui
         }
     }
     kvref_rotate_tile(x, ld_tok, H, Y);
-    kvref_sinkhorn(Y, iters, a, b, NULL);
+    kvref_sinkhorn_stat(Y, iters, stat, a, b, NULL);
     for (t = 0; t < NTOK; ++t) r[t] = exp(a[t]);
     for (d = 0; d < NCH; ++d) c32[d] = (float)exp(b[d]);
     kvref_rtn(Y, r, c32, bits, q, s32, z32, u_out);
@@ -382,6 +405,13 @@ void kvref_quantize_tile(const uint16_t *x, long ld_tok, int is_v, int iters, ui
     if (b_out) memcpy(b_out, b, sizeof(b));
     if (q_out) memcpy(q_out, q, sizeof(q));
     free(Y);
+}
+
+void kvref_quantize_tile(const uint16_t *x, long ld_tok, int is_v, int iters, uint8_t *rec,
+                         double *Y_out, double *a_out, double *b_out, uint8_t *q_out,
+                         double *u_out)
+{
+    kvref_quantize_tile_stat(x, ld_tok, is_v, iters, 0, rec, Y_out, a_out, b_out, q_out, u_out);
 }
 
 /* ------------------------------------------------------------------ */
@@ -394,10 +424,11 @@ void kvref_quantize_tile(const uint16_t *x, long ld_tok, int is_v, int iters, ui
  * tail_k, tail_v: fp16 [B][Hkv][128 slots][128].  u_k, u_v (nullable):
  * pre-rounding values, [B][max_blocks][Hkv][128][128] doubles, for the
  * boundary rule.  Returns 0, or -1 on a page id outside [0, num_pages). */
-int kvref_quantize_blocks(const uint16_t *k, const uint16_t *v, long sb, long st, long sh,
-                          int B, const int32_t *seq_lens, const int32_t *block_table,
-                          int max_blocks, int hkv, int iters, uint8_t *pool, long num_pages,
-                          uint16_t *tail_k, uint16_t *tail_v, double *u_k, double *u_v)
+int kvref_quantize_blocks_stat(const uint16_t *k, const uint16_t *v, long sb, long st, long sh,
+                               int B, const int32_t *seq_lens, const int32_t *block_table,
+                               int max_blocks, int hkv, int iters, int stat, uint8_t *pool,
+                               long num_pages, uint16_t *tail_k, uint16_t *tail_v, double *u_k,
+                               double *u_v)
 {
     int bad = 0;
     long item, n_items = (long)B * max_blocks * hkv;
@@ -414,10 +445,10 @@ int kvref_quantize_blocks(const uint16_t *k, const uint16_t *v, long sb, long st
         page = block_table[(long)b * max_blocks + j];
         if (page < 0 || page >= num_pages) { bad = 1; continue; }
         rec = pool + (page * hkv + h) * (long)REC_BYTES;
-        kvref_quantize_tile(k + b * sb + (long)j * NTOK * st + h * sh, st, 0, iters, rec, NULL,
-                            NULL, NULL, NULL, u_k ? u_k + uoff : NULL);
-        kvref_quantize_tile(v + b * sb + (long)j * NTOK * st + h * sh, st, 1, iters, rec, NULL,
-                            NULL, NULL, NULL, u_v ? u_v + uoff : NULL);
+        kvref_quantize_tile_stat(k + b * sb + (long)j * NTOK * st + h * sh, st, 0, iters, stat,
+                                 rec, NULL, NULL, NULL, NULL, u_k ? u_k + uoff : NULL);
+        kvref_quantize_tile_stat(v + b * sb + (long)j * NTOK * st + h * sh, st, 1, iters, stat,
+                                 rec, NULL, NULL, NULL, NULL, u_v ? u_v + uoff : NULL);
     }
     {
         int b, h, s, d;
@@ -437,12 +468,22 @@ int kvref_quantize_blocks(const uint16_t *k, const uint16_t *v, long sb, long st
     return bad ? -1 : 0;
 }
 
+int kvref_quantize_blocks(const uint16_t *k, const uint16_t *v, long sb, long st, long sh,
+                          int B, const int32_t *seq_lens, const int32_t *block_table,
+                          int max_blocks, int hkv, int iters, uint8_t *pool, long num_pages,
+                          uint16_t *tail_k, uint16_t *tail_v, double *u_k, double *u_v)
+{
+    return kvref_quantize_blocks_stat(k, v, sb, st, sh, B, seq_lens, block_table, max_blocks,
+                                      hkv, iters, 0, pool, num_pages, tail_k, tail_v, u_k, u_v);
+}
+
 /* Decode-time append: token `pos[b]` (the length before the append) goes to
  * tail slot pos mod 128; when that slot is 127 the now-full tail is quantized
  * into page block_table[b][pos / 128].  pos < 0 marks an idle slot. */
-int kvref_append_token(const uint16_t *k_new, const uint16_t *v_new, const int32_t *pos, int B,
-                       const int32_t *block_table, int max_blocks, int hkv, int iters,
-                       uint8_t *pool, long num_pages, uint16_t *tail_k, uint16_t *tail_v)
+int kvref_append_token_stat(const uint16_t *k_new, const uint16_t *v_new, const int32_t *pos,
+                            int B, const int32_t *block_table, int max_blocks, int hkv,
+                            int iters, int stat, uint8_t *pool, long num_pages,
+                            uint16_t *tail_k, uint16_t *tail_v)
 {
     int b, bad = 0;
     for (b = 0; b < B; ++b) {
@@ -466,12 +507,20 @@ int kvref_append_token(const uint16_t *k_new, const uint16_t *v_new, const int32
                 uint8_t *rec = pool + (page * hkv + h) * (long)REC_BYTES;
                 const uint16_t *tk = tail_k + ((long)b * hkv + h) * NTOK * NCH;
                 const uint16_t *tv = tail_v + ((long)b * hkv + h) * NTOK * NCH;
-                kvref_quantize_tile(tk, NCH, 0, iters, rec, NULL, NULL, NULL, NULL, NULL);
-                kvref_quantize_tile(tv, NCH, 1, iters, rec, NULL, NULL, NULL, NULL, NULL);
+                kvref_quantize_tile_stat(tk, NCH, 0, iters, stat, rec, NULL, NULL, NULL, NULL, NULL);
+                kvref_quantize_tile_stat(tv, NCH, 1, iters, stat, rec, NULL, NULL, NULL, NULL, NULL);
             }
         }
     }
     return bad ? -1 : 0;
+}
+
+int kvref_append_token(const uint16_t *k_new, const uint16_t *v_new, const int32_t *pos, int B,
+                       const int32_t *block_table, int max_blocks, int hkv, int iters,
+                       uint8_t *pool, long num_pages, uint16_t *tail_k, uint16_t *tail_v)
+{
+    return kvref_append_token_stat(k_new, v_new, pos, B, block_table, max_blocks, hkv, iters, 0,
+                                   pool, num_pages, tail_k, tail_v);
 }
 
 /* ------------------------------------------------------------------ */

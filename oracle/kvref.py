@@ -50,19 +50,23 @@ def lib():
         L.kvref_hadamard.argtypes = [ctypes.c_int, P]
         L.kvref_rotate_tile.argtypes = [P, ctypes.c_long, P, P]
         L.kvref_sinkhorn.argtypes = [P, ctypes.c_int, P, P, P]
+        L.kvref_sinkhorn_stat.argtypes = [P, ctypes.c_int, ctypes.c_int, P, P, P]
         L.kvref_rtn.argtypes = [P, P, P, ctypes.c_int, P, P, P, P]
         L.kvref_pack_part.argtypes = [P, ctypes.c_int, P, P, P, P]
         L.kvref_unpack_part.argtypes = [P, ctypes.c_int, P, P, P, P]
         L.kvref_dequant_part.argtypes = [P, ctypes.c_int, P]
         L.kvref_quantize_tile.argtypes = [P, ctypes.c_long, ctypes.c_int, ctypes.c_int, P, P, P,
                                           P, P, P]
-        L.kvref_quantize_blocks.restype = ctypes.c_int
-        L.kvref_quantize_blocks.argtypes = [P, P, ctypes.c_long, ctypes.c_long, ctypes.c_long,
-                                            ctypes.c_int, P, P, ctypes.c_int, ctypes.c_int,
-                                            ctypes.c_int, P, ctypes.c_long, P, P, P, P]
-        L.kvref_append_token.restype = ctypes.c_int
-        L.kvref_append_token.argtypes = [P, P, P, ctypes.c_int, P, ctypes.c_int, ctypes.c_int,
-                                         ctypes.c_int, P, ctypes.c_long, P, P]
+        L.kvref_quantize_tile_stat.argtypes = [P, ctypes.c_long, ctypes.c_int, ctypes.c_int,
+                                               ctypes.c_int, P, P, P, P, P, P]
+        L.kvref_quantize_blocks_stat.restype = ctypes.c_int
+        L.kvref_quantize_blocks_stat.argtypes = [P, P, ctypes.c_long, ctypes.c_long, ctypes.c_long,
+                                                 ctypes.c_int, P, P, ctypes.c_int, ctypes.c_int,
+                                                 ctypes.c_int, ctypes.c_int, P, ctypes.c_long, P,
+                                                 P, P, P]
+        L.kvref_append_token_stat.restype = ctypes.c_int
+        L.kvref_append_token_stat.argtypes = [P, P, P, ctypes.c_int, P, ctypes.c_int, ctypes.c_int,
+                                              ctypes.c_int, ctypes.c_int, P, ctypes.c_long, P, P]
         L.kvref_decode_attention.restype = ctypes.c_int
         L.kvref_decode_attention.argtypes = [P, P, ctypes.c_long, P, ctypes.c_int, P,
                                              ctypes.c_int, ctypes.c_int, ctypes.c_int, P, P,
@@ -108,15 +112,15 @@ def rotate_tile(x) -> np.ndarray:
     return Y
 
 
-def sinkhorn(Y, iters: int):
+def sinkhorn(Y, iters: int, rms: bool = False):
     """Stage 3: log row scales a, log column scales b, and the per-iteration
     trace [iters][4] = (row max|log sigma|, row spread, column max|log sigma|,
-    column spread)."""
+    column spread).  rms: the uncentred statistic of the "_rms" variant."""
     Y = _c(Y, np.float64).reshape(NTOK, NCH)
     a = np.zeros(NTOK)
     b = np.zeros(NCH)
     tr = np.zeros(max(4 * iters, 1))
-    lib().kvref_sinkhorn(_p(Y), iters, _p(a), _p(b), _p(tr))
+    lib().kvref_sinkhorn_stat(_p(Y), iters, int(rms), _p(a), _p(b), _p(tr))
     return a, b, tr[:4 * iters].reshape(iters, 4)
 
 
@@ -153,7 +157,7 @@ def dequant_part(rec, is_v: bool) -> np.ndarray:
     return y
 
 
-def quantize_tile(x, is_v: bool, iters: int):
+def quantize_tile(x, is_v: bool, iters: int, rms: bool = False):
     """All four stages on one tile; returns a dict of every intermediate."""
     xb = _bits16(x).reshape(NTOK, NCH)
     rec = np.zeros(REC_BYTES, dtype=np.uint8)
@@ -162,15 +166,15 @@ def quantize_tile(x, is_v: bool, iters: int):
     b = np.zeros(NCH)
     q = np.zeros((NTOK, NCH), dtype=np.uint8)
     u = np.zeros((NTOK, NCH))
-    lib().kvref_quantize_tile(_p(xb), NCH, int(is_v), iters, _p(rec), _p(Y), _p(a), _p(b),
-                              _p(q), _p(u))
+    lib().kvref_quantize_tile_stat(_p(xb), NCH, int(is_v), iters, int(rms), _p(rec), _p(Y),
+                                   _p(a), _p(b), _p(q), _p(u))
     return {"rec": rec, "Y": Y, "a": a, "b": b, "q": q, "u": u}
 
 
 # ------------------------------------------------------------ whole ops --
 
 def quantize_blocks(k, v, seq_lens, block_table, num_pages: int, iters: int, pool=None,
-                    tail_k=None, tail_v=None, want_u: bool = False):
+                    tail_k=None, tail_v=None, want_u: bool = False, rms: bool = False):
     """Prefill: k, v fp16 [B][S][Hkv][128] (contiguous).  Returns a dict with
     the pool [num_pages][Hkv][15360] uint8, the fp16 tails [B][Hkv][128][128]
     and, with want_u, the pre-rounding values [B][max_blocks][Hkv][128][128]."""
@@ -191,14 +195,15 @@ def quantize_blocks(k, v, seq_lens, block_table, num_pages: int, iters: int, poo
     if want_u:
         u_k = np.zeros((B, max_blocks, hkv, NTOK, NCH))
         u_v = np.zeros((B, max_blocks, hkv, NTOK, NCH))
-    rc = lib().kvref_quantize_blocks(_p(kb), _p(vb), S * hkv * NCH, hkv * NCH, NCH, B,
-                                     _p(seq_lens), _p(block_table), max_blocks, hkv, iters,
-                                     _p(pool), num_pages, _p(tail_k), _p(tail_v), _p(u_k),
-                                     _p(u_v))
+    rc = lib().kvref_quantize_blocks_stat(_p(kb), _p(vb), S * hkv * NCH, hkv * NCH, NCH, B,
+                                          _p(seq_lens), _p(block_table), max_blocks, hkv, iters,
+                                          int(rms), _p(pool), num_pages, _p(tail_k), _p(tail_v),
+                                          _p(u_k), _p(u_v))
     return {"rc": rc, "pool": pool, "tail_k": tail_k, "tail_v": tail_v, "u_k": u_k, "u_v": u_v}
 
 
-def append_token(k_new, v_new, pos, block_table, iters: int, pool, tail_k, tail_v):
+def append_token(k_new, v_new, pos, block_table, iters: int, pool, tail_k, tail_v,
+                 rms: bool = False):
     """Decode-time append (in place on pool / tails).  Returns the status."""
     kb = _bits16(k_new)
     vb = _bits16(v_new)
@@ -206,9 +211,9 @@ def append_token(k_new, v_new, pos, block_table, iters: int, pool, tail_k, tail_
     pos = _c(pos, np.int32)
     block_table = _c(block_table, np.int32)
     assert pool.flags["C_CONTIGUOUS"] and tail_k.flags["C_CONTIGUOUS"]
-    return lib().kvref_append_token(_p(kb), _p(vb), _p(pos), B, _p(block_table),
-                                    block_table.shape[1], hkv, iters, _p(pool), pool.shape[0],
-                                    _p(tail_k), _p(tail_v))
+    return lib().kvref_append_token_stat(_p(kb), _p(vb), _p(pos), B, _p(block_table),
+                                         block_table.shape[1], hkv, iters, int(rms), _p(pool),
+                                         pool.shape[0], _p(tail_k), _p(tail_v))
 
 
 def decode_attention(q, pool, block_table, seq_lens, tail_k, tail_v, hq: int, hkv: int,

@@ -253,6 +253,76 @@ def test_sinkhorn_skip_threshold_columns(oracle):
     assert b[1] < -5.0
 
 
+# ------------------------------------------- uncentred (RMS) variant ----
+# Format variant "_rms": each step divides by the root mean square instead of
+# the centred std, i.e. the Sinkhorn-Knopp scaling of the squared tile (the
+# plain-Sinkhorn reading of "Sinkhorn-like variance normalization", KVarN
+# page, "KVarN Nasil Calisir?", stage "Normalize Edilmis Onbellek").
+
+def _rms(Z, axis):
+    return np.sqrt((Z * Z).mean(axis=axis))
+
+
+def test_rms_variant_rank_one_fixed_point(oracle):
+    # Y = u v^T, u > 0, no zero in v: the row step leaves every column
+    # constant in magnitude, |v_d| / rms(v); the column step then makes every
+    # |Z| = 1, a fixed point of both steps.
+    rng = np.random.default_rng(48)
+    u = np.exp(rng.standard_normal(128))
+    v = rng.standard_normal(128)
+    Y = np.outer(u, v)
+    rv = np.sqrt((v * v).mean())
+    for iters in (1, 2, 5):
+        a, b, _ = oracle.sinkhorn(Y, iters, rms=True)
+        assert np.abs(a - (np.log(u) + np.log(rv))).max() < 1e-12
+        assert np.abs(b - (np.log(np.abs(v)) - np.log(rv))).max() < 1e-12
+
+
+@pytest.mark.parametrize("k", [1, 2, 3])
+def test_rms_row_and_column_steps_give_unit_rms(oracle, k):
+    for x in (_tile(49), _tile(50, sigma=1.5, outliers=4, fac=30.0)):
+        Y = oracle.rotate_tile(x)
+        a_k, b_k, _ = oracle.sinkhorn(Y, k, rms=True)
+        a_n, b_n, _ = oracle.sinkhorn(Y, k + 1, rms=True)
+        assert np.abs(_rms(Y * np.exp(-a_n)[:, None] * np.exp(-b_k)[None, :], 1) - 1).max() < 1e-12
+        assert np.abs(_rms(Y * np.exp(-a_n)[:, None] * np.exp(-b_n)[None, :], 0) - 1).max() < 1e-12
+
+
+def test_rms_variant_converges_to_a_doubly_normalized_tile(oracle):
+    # Sinkhorn-Knopp on a positive matrix (the squares) converges to a scaling
+    # with all row and all column sums equal: every row and every column of Z
+    # reaches RMS 1 (no common offset, unlike the centred statistic)
+    for x in (_tile(51), _tile(52, sigma=1.0, outliers=4, fac=25.0)):
+        Y = oracle.rotate_tile(x)
+        a, b, _ = oracle.sinkhorn(Y, 64, rms=True)
+        Z = Y * np.exp(-a)[:, None] * np.exp(-b)[None, :]
+        assert np.abs(_rms(Z, 0) - 1).max() < 1e-12
+        assert np.abs(_rms(Z, 1) - 1).max() < 1e-9
+
+
+def test_rms_variant_skips_only_zero_rows(oracle):
+    rng = np.random.default_rng(53)
+    Y = rng.standard_normal((128, 128))
+    Y[3] = 0.0                      # zero row: skipped, stays zero
+    Y[7] = 2.5                      # constant row: updated (centred would skip it)
+    a, b, _ = oracle.sinkhorn(Y, 1, rms=True)
+    assert a[3] == 0.0
+    assert abs(a[7] - np.log(2.5)) < 1e-12
+    ac, _, _ = oracle.sinkhorn(Y, 1)
+    assert ac[7] == 0.0
+
+
+def test_rms_variant_quantizes_through_all_stages(oracle):
+    # the variant changes only the scales: codes stay within half a step of
+    # the tile normalized by the variant's own scales
+    x = _tile(54)
+    r = oracle.quantize_tile(x, False, 2, rms=True)
+    a, b, _ = oracle.sinkhorn(r["Y"], 2, rms=True)
+    assert np.array_equal(r["a"], a) and np.array_equal(r["b"], b)
+    c = oracle.quantize_tile(x, False, 2)
+    assert not np.array_equal(r["b"], c["b"])
+
+
 def test_sinkhorn_zero_and_constant_tiles_are_skipped(oracle):
     a, b, _ = oracle.sinkhorn(np.zeros((128, 128)), 3)
     assert not a.any() and not b.any()
