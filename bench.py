@@ -392,7 +392,77 @@ def run_gpu(args, rank, world):
 
     # end to end through the public API: host buffers, copies inside the region
     e2e = measure_e2e(units[:per_step], args, stream)
-    return units[:per_step], ms, ms_step, ms_fused, wall, clocks, e2e, ms_cold, nu
+    # the chunked-prefill kernel on its own workload (not part of the step)
+    chunk = measure_chunk(args, dev, stream) if not args.no_chunk else None
+    return units[:per_step], ms, ms_step, ms_fused, wall, clocks, e2e, ms_cold, nu, chunk
+
+
+def measured_tensor_peak():
+    """Dense fp16/bf16 tensor-core peak (TFLOP/s) from MEASURED_PEAKS.json: the
+    burst figure, for a kernel timed on its own; fp16 runs at the bf16 rate."""
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            return float(json.load(f)["bf16_tflops"]), "measured"
+    return 1800.0, "fallback"
+
+
+def measure_chunk(args, dev, stream):
+    """Chunked-prefill attention (kvarn_chunk_attention) on its own workload:
+    16 sequences of the Llama-3-8B-like layer (8 KV heads, 32 query heads),
+    3584 cached tokens each plus a 512-token chunk, so the cache holds 4096
+    tokens (32 pages) per sequence.  Tensor-bound: algorithmic FLOPs are 4 x
+    128 x (P + 1) per query row and head at position P (the score and value
+    products of causal attention)."""
+    import quantized_decode_attention_blocks_b300 as kv
+    w = synth.WORKLOADS["llama3_8b_layer"]
+    B, M, start = 16, 512, 3584
+    S = start + M
+    cfg = kv.config_from_string("k4v2_g128", w.hq, w.hkv)
+    mb = S // T
+    reps = []
+    for r in range(2):   # two replicas, rotated, so no launch finds its q in L2
+        wr = synth.scaled(w, batch=B, seq=S, seed=w.seed + 500 + r)
+        k, v = synth.kv(wr, device=dev)
+        table = torch.arange(B * mb, dtype=torch.int32, device=dev).reshape(B, mb)
+        lens = torch.full((B,), S, dtype=torch.int32, device=dev)
+        pool = kv.alloc_pool(cfg, B * mb, dev)
+        tk, tv = kv.alloc_tails(cfg, B, dev)
+        st = torch.zeros(1, dtype=torch.int32, device=dev)
+        kv.kvarn_quantize_blocks(cfg, k, v, lens, S, table, pool, tk, tv, st)
+        del k, v
+        g = torch.Generator(device=dev)
+        g.manual_seed(900 + r)
+        q = torch.randn((B, M, w.hq, D), generator=g, device=dev).to(torch.float16)
+        reps.append(dict(q=q, out=torch.empty_like(q), table=table, pool=pool, tk=tk, tv=tv, st=st,
+                         starts=torch.full((B,), start, dtype=torch.int32, device=dev),
+                         cls=torch.full((B,), M, dtype=torch.int32, device=dev)))
+
+    def call(i):
+        r = reps[i % 2]
+        kv.kvarn_chunk_attention(cfg, r["q"], r["starts"], r["cls"], S, r["pool"], r["table"],
+                                 r["tk"], r["tv"], r["out"], status=r["st"])
+
+    for i in range(max(args.warmup, 3)):
+        call(i)
+    torch.cuda.synchronize()
+    n = max(4, min(args.steps, 20))
+    ms = time_graph(call, n, stream) / n
+    for r in reps:
+        if int(r["st"].item()) != 0:
+            raise RuntimeError(f"chunk attention status {int(r['st'].item())}")
+    pos = np.arange(start, start + M, dtype=np.float64)
+    flops = float((4 * D * (pos + 1)).sum()) * B * w.hq
+    tflops = flops / (ms * 1e-3) / 1e12
+    peak, kind = measured_tensor_peak()
+    return {"workload": "llama3_8b_layer chunked prefill: 16 x (3584 cached + 512-token chunk), "
+                        "8 KV heads, 32 query heads, head_dim 128",
+            "us_per_launch": ms * 1e3, "algorithmic_tflop_per_launch": flops / 1e12,
+            "mma_passes": "scores as 3 fp16 products (hi/lo splits), values as 2: 2.5x the "
+                          "algorithmic FLOPs run on the tensor cores",
+            "roofline": {"bound": "tensor", "achieved": tflops, "peak": peak,
+                         "peak_kind": f"{kind} bf16_tflops (burst; fp16 runs at the bf16 rate)",
+                         "unit": "TFLOP/s", "frac": tflops / peak, "traffic": None}}
 
 
 def measure_e2e(step_units, args, stream):
@@ -512,6 +582,7 @@ def main():
     ap.add_argument("--impl", default="kvarn", choices=["kvarn", "reference"])
     ap.add_argument("--workload", default="qwen25_15b", choices=sorted(synth.WORKLOADS))
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-chunk", action="store_true", help="skip the chunked-prefill line")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
@@ -523,7 +594,7 @@ def main():
         return 0
     if world > 1:
         torch.distributed.init_process_group("nccl")
-    units, ms, ms_step, ms_fused, wall, clocks, e2e, ms_cold, nu = run_gpu(args, rank, world)
+    units, ms, ms_step, ms_fused, wall, clocks, e2e, ms_cold, nu, chunk = run_gpu(args, rank, world)
     if world > 1:
         torch.distributed.destroy_process_group()
     if rank != 0:
@@ -593,6 +664,7 @@ def main():
                             "algorithmic_bytes_per_launch": bd // L,
                             "us_per_launch": per_launch["decode"]},
         "e2e": e2e,
+        "chunk_prefill": chunk,
         "gpu_launches": LAUNCHES_PER_STEP * L * args.steps,
         "clocks": clocks,
         "wall_s_timed_region": wall,

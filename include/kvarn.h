@@ -100,11 +100,15 @@ typedef struct {
     int sinkhorn_iters; /* 0..64; 2 from the iteration-selection rule */
     int num_q_heads;    /* Hq, a multiple of num_kv_heads */
     int num_kv_heads;   /* Hkv; Hq / Hkv <= 16 */
+    int sinkhorn_rms;   /* 0: centred std (default); 1: format variant "_rms",
+                           the uncentred root mean square (Sinkhorn-Knopp on
+                           the squares; only all-zero rows/columns skipped).
+                           The page record is the same either way. */
 } kvarn_config_t;
 
 /* Fills *out from a format string: "k4v2_g128" or "kvarn_k4v2_g128" (the
- * KVarN page's --kv-cache-dtype value), optionally suffixed "_s<K>" to set the
- * Sinkhorn iteration count.  Returns KVARN_ERR_UNSUPPORTED for any other
+ * KVarN page's --kv-cache-dtype value), optionally followed by "_rms" (the
+ * uncentred statistic) and then "_s<K>" to set the Sinkhorn iteration count.  Returns KVARN_ERR_UNSUPPORTED for any other
  * format, KVARN_ERR_INVALID_ARG for bad head counts or a null pointer. */
 int kvarn_config_from_string(const char *s, int num_q_heads, int num_kv_heads,
                              kvarn_config_t *out);

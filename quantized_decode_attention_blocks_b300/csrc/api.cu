@@ -79,6 +79,7 @@ int kvarn_config_validate(const kvarn_config_t* c) {
       c->v_bits != 2)
     return KVARN_ERR_UNSUPPORTED;
   if (c->sinkhorn_iters < 0 || c->sinkhorn_iters > kMaxIters) return KVARN_ERR_UNSUPPORTED;
+  if (c->sinkhorn_rms != 0 && c->sinkhorn_rms != 1) return KVARN_ERR_UNSUPPORTED;
   return KVARN_OK;
 }
 
@@ -86,8 +87,12 @@ int kvarn_config_from_string(const char* s, int hq, int hkv, kvarn_config_t* out
   if (!s || !out) return KVARN_ERR_INVALID_ARG;
   if (!strncmp(s, "kvarn_", 6)) s += 6;
   if (strncmp(s, "k4v2_g128", 9)) return KVARN_ERR_UNSUPPORTED;
-  int iters = 2;
+  int iters = 2, rms = 0;
   const char* rest = s + 9;
+  if (!strncmp(rest, "_rms", 4)) {
+    rms = 1;
+    rest += 4;
+  }
   if (*rest) {
     if (rest[0] != '_' || rest[1] != 's' || !rest[2]) return KVARN_ERR_UNSUPPORTED;
     int v = 0;
@@ -104,6 +109,7 @@ int kvarn_config_from_string(const char* s, int hq, int hkv, kvarn_config_t* out
   c.k_bits = 4;
   c.v_bits = 2;
   c.sinkhorn_iters = iters;
+  c.sinkhorn_rms = rms;
   c.num_q_heads = hq;
   c.num_kv_heads = hkv;
   const int rc = kvarn_config_validate(&c);
@@ -144,6 +150,7 @@ int kvarn_quantize_blocks(const kvarn_config_t* cfg, const void* k, const void* 
   a.batch = batch;
   a.hkv = cfg->num_kv_heads;
   a.iters = cfg->sinkhorn_iters;
+  a.rms = cfg->sinkhorn_rms;
   a.max_seq = max_seq;
   a.seq_lens = seq_lens;
   a.block_table = block_table;
@@ -179,6 +186,7 @@ int kvarn_append_token(const kvarn_config_t* cfg, const void* k_new, const void*
   a.batch = batch;
   a.hkv = cfg->num_kv_heads;
   a.iters = cfg->sinkhorn_iters;
+  a.rms = cfg->sinkhorn_rms;
   a.block_table = block_table;
   a.max_blocks = max_blocks;
   a.pool = static_cast<uint8_t*>(pool);

@@ -75,6 +75,7 @@ struct QuantizeArgs {
   const __half* v;
   int64_t sb, st, sh;       // element strides of k / v
   int batch, hkv, iters, max_seq;
+  int rms;                  // Sinkhorn statistic: 0 centred std, 1 uncentred RMS
   const int32_t* seq_lens;
   const int32_t* block_table;
   int max_blocks;
@@ -90,6 +91,7 @@ struct AppendArgs {
   const __half* v_new;
   const int32_t* pos;
   int batch, hkv, iters;
+  int rms;
   const int32_t* block_table;
   int max_blocks;
   uint8_t* pool;

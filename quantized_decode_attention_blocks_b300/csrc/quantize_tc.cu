@@ -34,6 +34,8 @@
 //  * column step d: c_d   = std_t(Y_td / r_t)
 //  * a row / column whose variance is <= 1e-10 * its mean square keeps its
 //    previous scale;
+//  * the "_rms" variant divides by the root mean square (mean^2 + variance)
+//    instead of the std, and keeps the scale only of an all-zero row / column;
 //  * RTN per token on x_td = Y_td / c_d: s' = (max - min) / (2^b - 1) and
 //    z' = min (the row scale r_t cancels from the codes and folds into s', z'),
 //    q = rint((x - min) * (2^b - 1) / (max - min)) as one fused multiply-add
@@ -109,6 +111,7 @@ struct QTileArgs {
   uint8_t* pool;
   int64_t num_pages;
   int32_t* status;
+  int rms;             // Sinkhorn statistic: 0 centred std, 1 uncentred RMS ("_rms")
 };
 
 // The plain copies folded into the same launch: mode 0 copies every
@@ -304,6 +307,19 @@ __device__ __forceinline__ void tail_copy(const QTileArgs& a, const QCopyArgs& c
 __device__ __forceinline__ bool keep_scale(float mean, float var) {
   // variance <= 1e-10 * mean square (mean square = var + mean^2): skip
   return !(var > 1e-10f * (var + mean * mean));
+}
+
+// The statistic a step divides by, as its square: the centred variance, or
+// for the "_rms" variant the mean square (= variance + mean^2), and whether
+// the step applies (centred: not for a (near-)constant row or column; RMS:
+// not for an all-zero one).
+__device__ __forceinline__ bool step_stat(bool rms, float mean, float var, float& sq) {
+  if (rms) {
+    sq = fmaf(mean, mean, var);
+    return sq > 0.f;
+  }
+  sq = var;
+  return !keep_scale(mean, var);
 }
 
 // +-1 Sylvester matrix element (n, k) as fp16 bits
@@ -534,7 +550,8 @@ __global__ void __launch_bounds__(kQThreads, 1)
       cc[row] = 1.f;
       if (a.iters > 0) {
         const float var = S.r1part[wg][0][row] + S.r1part[wg][1][row];
-        ra[row] = keep_scale(S.r1x0[wg][row], var) ? kInvSqrt128 : rsqrtf(var);
+        float sq;
+        ra[row] = step_stat(a.rms, S.r1x0[wg][row], var, sq) ? rsqrtf(sq) : kInvSqrt128;
       } else {
         ra[row] = kInvSqrt128;
       }
@@ -559,8 +576,10 @@ __global__ void __launch_bounds__(kQThreads, 1)
         frag_moments(v, w, mean, var);
         if (q == 0) {
 #pragma unroll
-          for (int e = 0; e < 2; ++e)
-            if (!keep_scale(mean[e], var[e])) ra[frow(e)] = rsqrtf(var[e]);
+          for (int e = 0; e < 2; ++e) {
+            float sq;
+            if (step_stat(a.rms, mean[e], var[e], sq)) ra[frow(e)] = rsqrtf(sq);
+          }
         }
         named_sync(bar_id, kWGThreads);
       }
@@ -572,13 +591,15 @@ __global__ void __launch_bounds__(kQThreads, 1)
       frag_moments(v, w, mean, var);
       if (q == 0) {
 #pragma unroll
-        for (int e = 0; e < 2; ++e)
-          if (!keep_scale(mean[e], var[e])) {
+        for (int e = 0; e < 2; ++e) {
+          float sq;
+          if (step_stat(a.rms, mean[e], var[e], sq)) {
             const int n = frow(e);
-            const float rs = rsqrtf(var[e]);
+            const float rs = rsqrtf(sq);
             cb[n] = rs;
-            cc[chan_of(n)] = var[e] * rs;
+            cc[chan_of(n)] = sq * rs;
           }
+        }
       }
       if (it == a.iters - 1 && leader) bulk_wait_read();
       named_sync(bar_id, kWGThreads);
@@ -841,6 +862,7 @@ cudaError_t launch_quantize_blocks(const QuantizeArgs& a, cudaStream_t s) {
   qa.batch = a.batch;
   qa.hkv = a.hkv;
   qa.iters = a.iters;
+  qa.rms = a.rms;
   qa.nb = a.max_seq / kT;
   qa.ntiles = a.batch * qa.nb * a.hkv * 2;
   qa.seq_lens = a.seq_lens;
@@ -881,6 +903,7 @@ cudaError_t launch_append_token(const AppendArgs& a, cudaStream_t s) {
   qa.batch = a.batch;
   qa.hkv = a.hkv;
   qa.iters = a.iters;
+  qa.rms = a.rms;
   qa.nb = 1;
   qa.ntiles = a.batch * a.hkv * 2;
   qa.pos = a.pos;

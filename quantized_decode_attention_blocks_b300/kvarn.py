@@ -43,7 +43,7 @@ class Config(ctypes.Structure):
     _fields_ = [("head_dim", ctypes.c_int), ("block_tokens", ctypes.c_int),
                 ("group", ctypes.c_int), ("k_bits", ctypes.c_int), ("v_bits", ctypes.c_int),
                 ("sinkhorn_iters", ctypes.c_int), ("num_q_heads", ctypes.c_int),
-                ("num_kv_heads", ctypes.c_int)]
+                ("num_kv_heads", ctypes.c_int), ("sinkhorn_rms", ctypes.c_int)]
 
     @property
     def g(self) -> int:

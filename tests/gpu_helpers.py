@@ -9,8 +9,8 @@ import quantized_decode_attention_blocks_b300 as kv
 DEV = torch.device("cuda:0") if torch.cuda.is_available() else None
 
 
-def config(hq, hkv, iters=None):
-    fmt = "k4v2_g128" if iters is None else f"k4v2_g128_s{iters}"
+def config(hq, hkv, iters=None, rms=False):
+    fmt = "k4v2_g128" + ("_rms" if rms else "") + ("" if iters is None else f"_s{iters}")
     return kv.config_from_string(fmt, hq, hkv)
 
 

@@ -54,6 +54,15 @@ def test_config_parsing():
     assert (c.head_dim, c.block_tokens, c.group, c.k_bits, c.v_bits) == (128, 128, 128, 4, 2)
     assert c.sinkhorn_iters == 2 and c.g == 4
     assert kv.config_from_string("k4v2_g128_s7", 12, 2).sinkhorn_iters == 7
+    assert c.sinkhorn_rms == 0
+    r = kv.config_from_string("kvarn_k4v2_g128_rms_s3", 12, 2)
+    assert r.sinkhorn_rms == 1 and r.sinkhorn_iters == 3
+    assert kv.config_from_string("k4v2_g128_rms", 12, 2).sinkhorn_iters == 2
+    for bad in ("k4v2_g128_s3_rms", "k4v2_g128_rm", "k4v2_g128_rms_"):
+        with pytest.raises(kv.KvarnError):
+            kv.config_from_string(bad, 12, 2)
+    r.sinkhorn_rms = 2
+    assert kv.config_validate(r) == K.ERR_UNSUPPORTED
     for bad in ("k4v4_g128", "k4v2_g64", "k4v2_g128_x", "k4v2_g128_s", "k4v2_g128_s999"):
         with pytest.raises(kv.KvarnError) as e:
             kv.config_from_string(bad, 32, 8)

@@ -15,15 +15,16 @@ from workloads import synth
 pytestmark = pytest.mark.gpu
 
 
-def _check_prefill(w, lens, table, num_pages, iters=2, k=None, v=None):
+def _check_prefill(w, lens, table, num_pages, iters=2, k=None, v=None, rms=False):
     if k is None:
         k, v = synth.kv(w, device=DEV)
-    cfg = config(w.hq, w.hkv, iters)
+    cfg = config(w.hq, w.hkv, iters, rms=rms)
     pool, tk, tv, status = prefill(cfg, k, v, lens, table, num_pages, max_seq=w.seq)
     torch.cuda.synchronize()
     assert int(status.item()) == 0
     kh, vh = host(k), host(v)
-    ref = kvref.quantize_blocks(kh, vh, host(lens), host(table), num_pages, iters, want_u=True)
+    ref = kvref.quantize_blocks(kh, vh, host(lens), host(table), num_pages, iters, want_u=True,
+                                rms=rms)
     got_pool = host(pool)
     stats = {}
     nfull = host(lens) // 128
@@ -34,6 +35,7 @@ def _check_prefill(w, lens, table, num_pages, iters=2, k=None, v=None):
                 parity.compare_record(got_pool[page, h], ref["pool"][page, h],
                                       ref["u_k"][b, j, h], ref["u_v"][b, j, h], stats)
     parity.check_flip_rate(stats)
+    _check_prefill.last = (pool, tk, tv, cfg)
     # leftover tokens copied verbatim into the tails
     for b in range(w.batch):
         rem = int(host(lens)[b]) % 128
@@ -64,6 +66,27 @@ def test_other_iteration_counts(iters):
     lens = torch.tensor([384], dtype=torch.int32)
     table = torch.tensor([[2, 0, 1]], dtype=torch.int32)
     _check_prefill(w, lens, table, 3, iters=iters)
+
+
+@pytest.mark.parametrize("iters", [1, 2, 4])
+def test_rms_variant(iters):
+    # format variant "_rms" (uncentred Sinkhorn statistic): same record, the
+    # scales and codes of the oracle's variant; then decode reads it
+    w = synth.scaled(synth.WORKLOADS["llama3_8b_layer"], batch=3, seq=700, hkv=2, hq=8)
+    lens = torch.tensor([700, 256, 300], dtype=torch.int32)
+    g = torch.Generator().manual_seed(9)
+    table = torch.randperm(3 * 6, generator=g).to(torch.int32).reshape(3, 6)
+    _check_prefill(w, lens, table, 18, iters=iters, rms=True)
+    pool, tk, tv, cfg = _check_prefill.last
+    assert cfg.sinkhorn_rms == 1 and cfg.sinkhorn_iters == iters
+    from tests.gpu_helpers import decode
+    q = synth.queries(w)
+    out, st, _ = decode(cfg, q, pool, table, lens, tk, tv)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    ref = kvref.decode_attention(host(q), host(pool), host(table), host(lens), host(tk),
+                                 host(tv), w.hq, w.hkv)
+    parity.compare_attention(host(out), ref)
 
 
 def test_strided_input():
