@@ -642,3 +642,140 @@ int kvref_decode_attention(const uint16_t *q, const uint8_t *pool, long num_page
     }
     return bad ? -1 : 0;
 }
+
+/* ------------------------------------------------------------------ */
+/* The FP8 paged cache: the common halving of the KV cache by 8-bit    */
+/* floats ("KV Cache (Anahtar-Deger Onbellegi)", yapayzekasozluk.tr,   */
+/* "Sik Sorulan Sorular": INT8/FP8 KV quantization), the second baseline */
+/* the quantized cache is compared with.                                 */
+/* Readings: e4m3 ("fn": bias 7, 3 mantissa bits, largest finite 448,    */
+/* no infinities), one fp32 scale per token and KV head, s = max|x| / 448 */
+/* and codes e4m3(x / s) rounded to nearest even and saturated to +-448;  */
+/* both divisions are single-precision, as the codes are a decision taken */
+/* in fp32 on both sides.  Page (per page and KV head, 33792 bytes):      */
+/*   [0, 16384) K codes [128 tokens][128 channels]                        */
+/*   [16384, 32768) V codes, same                                         */
+/*   [32768, 33280) K scales fp32 [128 tokens], [33280, 33792) V scales.  */
+/* ------------------------------------------------------------------ */
+
+#define FP8_PAGE_BYTES 33792
+
+/* value of an e4m3 code (NaN for the two NaN codes) */
+double kvref_e4m3_decode(uint8_t c)
+{
+    int sign = c >> 7, e = (c >> 3) & 15, m = c & 7;
+    double v;
+    if (e == 15 && m == 7) return NAN;
+    v = e == 0 ? ldexp((double)m, -9) : ldexp(8.0 + m, e - 10);
+    return sign ? -v : v;
+}
+
+/* nearest e4m3 code to u, ties to even, magnitudes above 448 saturated */
+uint8_t kvref_e4m3_encode(float u)
+{
+    double a = fabs((double)u), t;
+    int sign = u < 0 || (u == 0 && signbit(u)), e, m;
+    if (u != u) return 0x7F;
+    if (a >= 448.0) return (uint8_t)((sign << 7) | 0x7E);
+    if (a < ldexp(1.0, -6)) {                 /* subnormal: multiples of 2^-9 */
+        m = (int)nearbyint(ldexp(a, 9));      /* 0..8; 8 is the smallest normal */
+        return (uint8_t)((sign << 7) | m);
+    }
+    e = (int)floor(log2(a));
+    if (ldexp(1.0, e) > a) --e;               /* guard log2 rounding */
+    if (ldexp(1.0, e + 1) <= a) ++e;
+    t = ldexp(a, 3 - e);                      /* 8 (1 + f), in [8, 16) */
+    m = (int)nearbyint(t) - 8;
+    if (m == 8) { m = 0; ++e; }
+    if (e > 8 || (e == 8 && m == 7)) return (uint8_t)((sign << 7) | 0x7E);
+    return (uint8_t)((sign << 7) | ((e + 7) << 3) | m);
+}
+
+/* one token of one head: scale and codes */
+void kvref_fp8_quantize_token(const uint16_t *x, uint8_t *codes, float *scale)
+{
+    float amax = 0.0f, s;
+    int d;
+    for (d = 0; d < NCH; ++d) {
+        float a = (float)fabs(kvref_half_to_double(x[d]));
+        if (a > amax) amax = a;
+    }
+    s = amax / 448.0f;
+    *scale = s;
+    for (d = 0; d < NCH; ++d)
+        codes[d] = s > 0.0f ? kvref_e4m3_encode((float)kvref_half_to_double(x[d]) / s) : 0;
+}
+
+/* tokens [0, seq_lens[b]) of k, v fp16 [B][S][Hkv][128] (element strides
+ * sb, st, sh) into the pages block_table[b][t / 128]; returns -1 on a page id
+ * outside [0, num_pages) */
+int kvref_fp8_write_blocks(const uint16_t *k, const uint16_t *v, long sb, long st, long sh,
+                           int B, int hkv, const int32_t *seq_lens, const int32_t *block_table,
+                           int max_blocks, uint8_t *pool, long num_pages)
+{
+    int b, h, t, bad = 0;
+    for (b = 0; b < B; ++b)
+        for (t = 0; t < seq_lens[b]; ++t) {
+            long page = block_table[(long)b * max_blocks + t / NTOK];
+            int tt = t % NTOK;
+            if (page < 0 || page >= num_pages) { bad = 1; continue; }
+            for (h = 0; h < hkv; ++h) {
+                uint8_t *pg = pool + (page * hkv + h) * (long)FP8_PAGE_BYTES;
+                float s;
+                long src = b * sb + (long)t * st + h * sh;
+                kvref_fp8_quantize_token(k + src, pg + tt * NCH, &s);
+                memcpy(pg + 32768 + 4 * tt, &s, 4);
+                kvref_fp8_quantize_token(v + src, pg + 16384 + tt * NCH, &s);
+                memcpy(pg + 33280 + 4 * tt, &s, 4);
+            }
+        }
+    return bad ? -1 : 0;
+}
+
+/* decode attention over the fp8 pages: out[b][h] = sum_t softmax_t(scale
+ * q . k_t) v_t with k_t = s^K_t e4m3(codes), the textbook definition in
+ * float64; returns -1 on a page id outside the pool */
+int kvref_fp8_decode_attention(const uint16_t *q, const uint8_t *pool, long num_pages,
+                               const int32_t *block_table, int max_blocks,
+                               const int32_t *seq_lens, int B, int hq, int hkv, double scale,
+                               double *out)
+{
+    int bad = 0;
+    long item, n_items = (long)B * hq;
+    int g = hq / hkv;
+#pragma omp parallel for schedule(dynamic, 1) reduction(| : bad)
+    for (item = 0; item < n_items; ++item) {
+        int b = (int)(item / hq), h = (int)(item % hq), kvh = h / g;
+        int len = seq_lens[b], t, d;
+        double qv[NCH], acc[NCH], mx = -INFINITY, l = 0.0;
+        double *sc = (double *)malloc(sizeof(double) * (len > 0 ? len : 1));
+        for (d = 0; d < NCH; ++d) { qv[d] = kvref_half_to_double(q[item * NCH + d]); acc[d] = 0.0; }
+        for (t = 0; t < len && !bad; ++t) {
+            long page = block_table[(long)b * max_blocks + t / NTOK];
+            const uint8_t *pg;
+            float s;
+            double x = 0.0;
+            if (page < 0 || page >= num_pages) { bad = 1; break; }
+            pg = pool + (page * hkv + kvh) * (long)FP8_PAGE_BYTES;
+            memcpy(&s, pg + 32768 + 4 * (t % NTOK), 4);
+            for (d = 0; d < NCH; ++d) x += qv[d] * (double)s * kvref_e4m3_decode(pg[(t % NTOK) * NCH + d]);
+            sc[t] = x * scale;
+            if (sc[t] > mx) mx = sc[t];
+        }
+        if (!bad) {
+            for (t = 0; t < len; ++t) {
+                long page = block_table[(long)b * max_blocks + t / NTOK];
+                const uint8_t *pg = pool + (page * hkv + kvh) * (long)FP8_PAGE_BYTES;
+                float s;
+                double p = exp(sc[t] - mx);
+                memcpy(&s, pg + 33280 + 4 * (t % NTOK), 4);
+                l += p;
+                for (d = 0; d < NCH; ++d)
+                    acc[d] += p * (double)s * kvref_e4m3_decode(pg[16384 + (t % NTOK) * NCH + d]);
+            }
+        }
+        for (d = 0; d < NCH; ++d) out[item * NCH + d] = len > 0 && !bad ? acc[d] / l : 0.0;
+        free(sc);
+    }
+    return bad ? -1 : 0;
+}

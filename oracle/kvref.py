@@ -71,6 +71,19 @@ def lib():
         L.kvref_decode_attention.argtypes = [P, P, ctypes.c_long, P, ctypes.c_int, P,
                                              ctypes.c_int, ctypes.c_int, ctypes.c_int, P, P,
                                              ctypes.c_double, ctypes.c_int, P]
+        L.kvref_e4m3_decode.restype = ctypes.c_double
+        L.kvref_e4m3_decode.argtypes = [ctypes.c_uint8]
+        L.kvref_e4m3_encode.restype = ctypes.c_uint8
+        L.kvref_e4m3_encode.argtypes = [ctypes.c_float]
+        L.kvref_fp8_quantize_token.argtypes = [P, P, P]
+        L.kvref_fp8_write_blocks.restype = ctypes.c_int
+        L.kvref_fp8_write_blocks.argtypes = [P, P, ctypes.c_long, ctypes.c_long, ctypes.c_long,
+                                             ctypes.c_int, ctypes.c_int, P, P, ctypes.c_int, P,
+                                             ctypes.c_long]
+        L.kvref_fp8_decode_attention.restype = ctypes.c_int
+        L.kvref_fp8_decode_attention.argtypes = [P, P, ctypes.c_long, P, ctypes.c_int, P,
+                                                 ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                                                 ctypes.c_double, P]
         _lib = L
     return _lib
 
@@ -323,4 +336,61 @@ def chunk_attention(q, start, chunk_lens, pool, block_table, tail_k, tail_v, hq:
                 s = (K[h // g, :P + 1] @ qd[b, i, h]) * scale
                 p = np.exp(s - s.max())
                 out[b, i, h] = (p / p.sum()) @ V[h // g, :P + 1]
+    return out
+
+
+# ------------------------------------------------------------ FP8 cache --
+# The FP8 paged cache the quantized one is compared with (per-token e4m3 with
+# an fp32 absmax scale; layout and readings in the header of that part of
+# kvref.c).
+
+FP8_PAGE_BYTES = 33792
+
+
+def e4m3_decode(code: int) -> float:
+    return lib().kvref_e4m3_decode(int(code))
+
+
+def e4m3_encode(u: float) -> int:
+    return int(lib().kvref_e4m3_encode(float(u)))
+
+
+def fp8_quantize_token(x):
+    """fp16 [128] -> (codes uint8 [128], fp32 scale)."""
+    xb = _bits16(x).reshape(NCH)
+    codes = np.zeros(NCH, dtype=np.uint8)
+    s = np.zeros(1, dtype=np.float32)
+    lib().kvref_fp8_quantize_token(_p(xb), _p(codes), _p(s))
+    return codes, float(s[0])
+
+
+def fp8_write_blocks(k, v, seq_lens, block_table, num_pages: int):
+    """fp16 k, v [B][S][Hkv][128] -> pool uint8 [num_pages][Hkv][33792]."""
+    kb, vb = _bits16(k), _bits16(v)
+    B, S, hkv, _ = kb.shape
+    seq_lens = _c(seq_lens, np.int32)
+    block_table = _c(block_table, np.int32)
+    pool = np.zeros((num_pages, hkv, FP8_PAGE_BYTES), dtype=np.uint8)
+    rc = lib().kvref_fp8_write_blocks(_p(kb), _p(vb), S * hkv * NCH, hkv * NCH, NCH, B, hkv,
+                                      _p(seq_lens), _p(block_table), block_table.shape[1],
+                                      _p(pool), num_pages)
+    if rc != 0:
+        raise ValueError("oracle: page id outside the pool")
+    return pool
+
+
+def fp8_decode_attention(q, pool, block_table, seq_lens, hq: int, hkv: int,
+                         scale: float = 1.0 / np.sqrt(128.0)) -> np.ndarray:
+    """Decode attention over the fp8 pages, float64 [B][Hq][128]."""
+    qb = _bits16(q)
+    B = qb.shape[0]
+    pool = _c(pool, np.uint8)
+    block_table = _c(block_table, np.int32)
+    seq_lens = _c(seq_lens, np.int32)
+    out = np.zeros((B, hq, NCH))
+    rc = lib().kvref_fp8_decode_attention(_p(qb), _p(pool), pool.shape[0], _p(block_table),
+                                          block_table.shape[1], _p(seq_lens), B, hq, hkv,
+                                          float(scale), _p(out))
+    if rc != 0:
+        raise ValueError("oracle: page id outside the pool")
     return out

@@ -722,3 +722,83 @@ def test_chunk_attention_gqa_heads_share_their_kv_head(oracle):
                                  hkv)
     assert np.array_equal(out[:, :, 0], out[:, :, 1])
     assert not np.array_equal(out[0, :150, 0], out[0, :150, 3])
+
+
+# ---------------------------------------------------------- FP8 cache --
+# The FP8 paged cache (the glossary's INT8/FP8 KV quantization, "KV Cache
+# (Anahtar-Deger Onbellegi)", "Sik Sorulan Sorular"): e4m3 codes with a
+# per-token absmax scale.  Its arithmetic is pinned to torch's float8_e4m3fn
+# conversion (round to nearest even) and to textbook attention.
+
+def test_e4m3_decode_matches_torch_for_every_code(oracle):
+    codes = torch.arange(256, dtype=torch.int32).to(torch.uint8)
+    ref = codes.view(torch.float8_e4m3fn).to(torch.float64).numpy()
+    got = np.array([oracle.e4m3_decode(c) for c in range(256)])
+    fin = np.isfinite(ref)
+    assert np.array_equal(got[fin], ref[fin]) and np.all(np.isnan(got[~fin]))
+    assert oracle.e4m3_decode(0x7E) == 448.0 and oracle.e4m3_decode(0x01) == 2.0 ** -9
+
+
+def test_e4m3_encode_matches_torch_rounding(oracle):
+    rng = np.random.default_rng(60)
+    u = np.concatenate([rng.standard_normal(4000) * 30, rng.uniform(-463.9, 463.9, 2000),
+                        rng.standard_normal(2000) * 1e-2, rng.standard_normal(500) * 1e-3])
+    # every midpoint between neighbouring codes: ties go to the even code
+    vals = np.array([oracle.e4m3_decode(c) for c in range(0x7F)])
+    mids = (vals[:-1] + vals[1:]) / 2
+    u = np.concatenate([u, mids, -mids]).astype(np.float32)
+    ref = torch.from_numpy(u).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    got = np.array([oracle.e4m3_encode(x) for x in u], dtype=np.uint8)
+    same = (got == ref) | ((got & 0x7F) == 0) & ((ref & 0x7F) == 0)   # +-0
+    assert same.all(), (u[~same][:5], got[~same][:5], ref[~same][:5])
+
+
+def test_e4m3_encode_saturates(oracle):
+    for x, c in ((464.0, 0x7E), (1e6, 0x7E), (-1e6, 0xFE), (448.0, 0x7E), (-449.0, 0xFE)):
+        assert oracle.e4m3_encode(x) == c
+
+
+def test_fp8_token_scale_and_half_step_bound(oracle):
+    rng = np.random.default_rng(61)
+    x = (rng.standard_normal(128) * np.exp(rng.standard_normal(128))).astype(np.float16)
+    codes, s = oracle.fp8_quantize_token(x)
+    xd = x.astype(np.float64)
+    assert s == np.float32(np.float32(np.abs(xd).max()) / np.float32(448.0))
+    deq = np.array([oracle.e4m3_decode(c) for c in codes]) * s
+    # the largest element maps to the top code; every element lies within
+    # half a code step (relative 2^-4) of its decoded value, or half the
+    # smallest subnormal step below 2^-6
+    assert abs(deq[np.argmax(np.abs(xd))]) == pytest.approx(np.abs(xd).max(), rel=2 ** -4)
+    assert np.all(np.abs(deq - xd) <= np.maximum(np.abs(xd) * 2 ** -4, s * 2 ** -10) + 1e-12)
+    codes0, s0 = oracle.fp8_quantize_token(np.zeros(128, np.float16))
+    assert s0 == 0.0 and not codes0.any()
+
+
+def test_fp8_attention_matches_torch_sdpa_on_dequantized_cache(oracle):
+    rng = np.random.default_rng(62)
+    B, S, hkv, hq = 2, 300, 2, 8
+    k = (rng.standard_normal((B, S, hkv, 128)) * 3).astype(np.float16)
+    v = rng.standard_normal((B, S, hkv, 128)).astype(np.float16)
+    q = rng.standard_normal((B, hq, 128)).astype(np.float16)
+    lens = np.array([300, 129], dtype=np.int32)
+    table = np.array([[0, 1, 2], [3, 4, 5]], dtype=np.int32)
+    pool = oracle.fp8_write_blocks(k, v, lens, table, 6)
+    out = oracle.fp8_decode_attention(q, pool, table, lens, hq, hkv)
+    for b in range(B):
+        n = int(lens[b])
+        for kvh in range(hkv):
+            K = np.zeros((n, 128))
+            V = np.zeros((n, 128))
+            for t in range(n):
+                pg = pool[table[b, t // 128], kvh]
+                sk = pg[32768 + 4 * (t % 128):32772 + 4 * (t % 128)].view(np.float32)[0]
+                sv = pg[33280 + 4 * (t % 128):33284 + 4 * (t % 128)].view(np.float32)[0]
+                kc = torch.from_numpy(pg[(t % 128) * 128:(t % 128 + 1) * 128].copy())
+                vc = torch.from_numpy(pg[16384 + (t % 128) * 128:16384 + (t % 128 + 1) * 128].copy())
+                K[t] = kc.view(torch.float8_e4m3fn).to(torch.float64).numpy() * sk
+                V[t] = vc.view(torch.float8_e4m3fn).to(torch.float64).numpy() * sv
+            qq = torch.from_numpy(q[b, kvh * 4:(kvh + 1) * 4].astype(np.float64))[None, :, None]
+            ref = torch.nn.functional.scaled_dot_product_attention(
+                qq, torch.from_numpy(K)[None, None].expand(1, 4, n, 128),
+                torch.from_numpy(V)[None, None].expand(1, 4, n, 128))
+            assert np.abs(out[b, kvh * 4:(kvh + 1) * 4] - ref[0, :, 0].numpy()).max() < 1e-12
