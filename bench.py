@@ -50,6 +50,7 @@ REC = 15360
 # algorithmic bytes per token-head (K+V): fp16 in, packed out
 FP16_TOKEN_HEAD = 512
 PACKED_TOKEN_HEAD = 120
+FP8_TOKEN_HEAD = 2 * 128 + 2 * 4     # e4m3 K, V codes + their fp32 scales
 # library kernels per step: quantize (tiles and leftover-token copies), append
 # (token copies and filled-tail tiles), decode (splits merged in the same launch)
 LAUNCHES_PER_STEP = 3
@@ -174,7 +175,7 @@ class Unit:
     tails, new token, query, output and decode workspace.  `pool` and `pool16`
     may be shared with other units (the layers of one model share one pool)."""
 
-    def __init__(self, w, dev, cfg, layer, table, pool, pool16, num_pages):
+    def __init__(self, w, dev, cfg, layer, table, pool, pool16, pool8, num_pages):
         import quantized_decode_attention_blocks_b300 as kv
         self.kv = kv
         self.w = w
@@ -216,6 +217,14 @@ class Unit:
         self.out16 = torch.empty_like(self.out)
         self.bytes_decode_fp16 = int(lens.sum() * w.hkv * FP16_TOKEN_HEAD
                                      + 2 * w.batch * w.hq * D * 2)
+        # and the FP8 paged cache (e4m3 + a per-token fp32 scale)
+        self.pool8 = pool8
+        kv.kvarn_fp8_write_blocks(self.k, self.v, self.lens, self.max_seq, self.table,
+                                  self.pool8, self.status)
+        self.ws8 = kv.alloc_fp8_decode_workspace(w.hq, w.hkv, w.batch, self.max_seq, dev)
+        self.out8 = torch.empty_like(self.out)
+        self.bytes_decode_fp8 = int(lens.sum() * w.hkv * FP8_TOKEN_HEAD
+                                    + 2 * w.batch * w.hq * D * 2)
 
     def quantize(self):
         self.kv.kvarn_quantize_blocks(self.cfg, self.k, self.v, self.lens, self.max_seq,
@@ -229,6 +238,11 @@ class Unit:
         self.kv.kvarn_fp16_decode_attention(self.q, self.w.hkv, self.pool16, self.table,
                                             self.lens, self.max_seq, self.out16, self.ws16,
                                             status=self.status)
+
+    def decode_fp8(self):
+        self.kv.kvarn_fp8_decode_attention(self.q, self.w.hkv, self.pool8, self.table,
+                                           self.lens, self.max_seq, self.out8, self.ws8,
+                                           status=self.status)
 
     def decode(self):
         self.kv.kvarn_decode_attention(self.cfg, self.q, self.pool, self.table, self.lens1,
@@ -254,7 +268,8 @@ def build_units(w, dev, rank):
         tables, num_pages = synth.block_tables(wm, device=dev)
         pool = kv.alloc_pool(cfg, num_pages, dev)
         pool16 = kv.alloc_fp16_pool(wm.hkv, num_pages, dev)
-        return [Unit(wm, dev, cfg, layer, tables[layer], pool, pool16, num_pages)
+        pool8 = kv.alloc_fp8_pool(wm.hkv, num_pages, dev)
+        return [Unit(wm, dev, cfg, layer, tables[layer], pool, pool16, pool8, num_pages)
                 for layer in range(wm.layers)]
 
     units = one_model(w)
@@ -388,6 +403,8 @@ def run_gpu(args, rank, world):
     # (outside the step: a comparison, not part of the path)
     ms["decode_fp16"] = time_graph(lambda i: units[i % nu].decode_fp16(), n_launch,
                                    stream) / args.steps
+    ms["decode_fp8"] = time_graph(lambda i: units[i % nu].decode_fp8(), n_launch,
+                                  stream) / args.steps
     check_status(units)
 
     # end to end through the public API: host buffers, copies inside the region
@@ -613,6 +630,8 @@ def main():
     d_gbs = bd / (ms["decode"] * 1e-3) / 1e9
     a_gbs = ba / (ms["append"] * 1e-3) / 1e9
     f16_gbs = bd16 / (ms["decode_fp16"] * 1e-3) / 1e9
+    bd8 = sum(u.bytes_decode_fp8 for u in units)
+    f8_gbs = bd8 / (ms["decode_fp8"] * 1e-3) / 1e9
     dom = "quantize" if ms["quantize"] >= ms["decode"] else "decode"
     dom_gbs = q_gbs if dom == "quantize" else d_gbs
     traffic_q = ncu_traffic("quantize_tc_kernel", "quantize_tc.cu")
@@ -649,10 +668,17 @@ def main():
                             "frac_of_hbm": f16_gbs / peak, "bytes_per_step": bd16,
                             "note": "baseline: the same decode over an FP16 paged cache of "
                                     "the prefill tokens (not part of the step)"},
+            "decode_fp8": {"us_per_step": ms["decode_fp8"] * 1e3,
+                           "us_per_launch": per_launch["decode_fp8"], "gbs": f8_gbs,
+                           "frac_of_hbm": f8_gbs / peak, "bytes_per_step": bd8,
+                           "note": "baseline: the same decode over an FP8 (e4m3, per-token "
+                                   "scale) paged cache of the prefill tokens (not part of "
+                                   "the step)"},
             "step_fused": {"ms_per_step": ms_fused,
                            "note": "quantize -> append -> decode per layer in one graph"},
         },
         "decode_speedup_vs_fp16_cache": ms["decode_fp16"] / ms["decode"],
+        "decode_speedup_vs_fp8_cache": ms["decode_fp8"] / ms["decode"],
         "roofline": {"bound": "hbm", "kernel": dom, "achieved": dom_gbs, "peak": peak,
                      "peak_kind": f"{peak_kind} hbm_gbs (burst copy)", "unit": "GB/s",
                      "frac": dom_gbs / peak,

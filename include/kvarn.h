@@ -307,6 +307,45 @@ int kvarn_fp16_decode_attention(const void *q, int num_q_heads, int num_kv_heads
                                 float softmax_scale, void *out, void *workspace,
                                 size_t workspace_bytes, int32_t *status, kvarn_stream_t stream);
 
+/* ---- The FP8 paged cache, the second baseline ----
+ * The glossary "KV Cache (Anahtar-Deger Onbellegi)" (yapayzekasozluk.tr),
+ * "Sik Sorulan Sorular", names INT8/FP8 KV quantization as the common way to
+ * halve the cache; these calls are that cache on the same harness.  Each
+ * token of each KV head is stored as e4m3 codes (largest finite 448) with one
+ * fp32 scale s = max|x| / 448: codes = e4m3(x / s), nearest even, saturated;
+ * both divisions fp32.  Page: one per (page, KV head), KVARN_FP8_PAGE_BYTES
+ * bytes, 16-byte aligned:
+ *   [0, 16384)      K codes [128 tokens][128 channels]
+ *   [16384, 32768)  V codes, same
+ *   [32768, 33280)  K scales fp32 [128 tokens]
+ *   [33280, 33792)  V scales fp32 [128 tokens]
+ * Pool = [num_pages][num_kv_heads][KVARN_FP8_PAGE_BYTES]; 264 bytes per
+ * token-head against 512 in fp16.  The calls take the arguments of the
+ * kvarn_fp16_* calls above, with this page layout. */
+#define KVARN_FP8_PAGE_BYTES 33792
+
+/* Quantizes tokens [0, seq_lens[b]) of every sequence into its fp8 pages. */
+int kvarn_fp8_write_blocks(const void *k, const void *v, int64_t stride_b, int64_t stride_t,
+                           int64_t stride_h, int batch, int num_kv_heads,
+                           const int32_t *seq_lens, int max_seq, const int32_t *block_table,
+                           int max_blocks, void *pool, int64_t num_pages, int32_t *status,
+                           kvarn_stream_t stream);
+
+/* Bytes of workspace kvarn_fp8_decode_attention needs on the current device
+ * (0: none, or no CUDA device is current). */
+size_t kvarn_fp8_decode_workspace_bytes(int num_q_heads, int num_kv_heads, int batch,
+                                        int max_seq);
+
+/* Decode attention over the fp8 pages, one query token per sequence:
+ *   out[b][h] = sum_t softmax_t(scale * q[b][h] . k_t) v_t, t < seq_lens[b],
+ * k_t = s^K_t e4m3(K codes), v_t likewise; Hq/Hkv at most 8; split-K with a
+ * log-sum-exp merge in the same launch, the workspace as for the FP16 call. */
+int kvarn_fp8_decode_attention(const void *q, int num_q_heads, int num_kv_heads,
+                               const void *pool, int64_t num_pages, const int32_t *block_table,
+                               int max_blocks, const int32_t *seq_lens, int batch, int max_seq,
+                               float softmax_scale, void *out, void *workspace,
+                               size_t workspace_bytes, int32_t *status, kvarn_stream_t stream);
+
 /* Static text for a return code or a status bit set. */
 const char *kvarn_status_string(int code);
 

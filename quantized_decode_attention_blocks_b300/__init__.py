@@ -4,6 +4,8 @@ The compute lives in libkvarn.so (CUDA kernels behind the C ABI of
 include/kvarn.h); this package is its thin Python binding.
 """
 from .kvarn import (Config, KvarnError, alloc_decode_workspace, alloc_fp16_decode_workspace,
+                    alloc_fp8_decode_workspace, alloc_fp8_pool, fp8_decode_workspace_bytes,
+                    kvarn_fp8_decode_attention, kvarn_fp8_write_blocks,
                     alloc_fp16_pool, alloc_pool, alloc_tails, fp16_decode_workspace_bytes,
                     kvarn_fp16_decode_attention, kvarn_fp16_write_blocks,
                     config_from_string, config_validate, decode_split_plan, decode_workspace_bytes,
@@ -12,6 +14,8 @@ from .kvarn import (Config, KvarnError, alloc_decode_workspace, alloc_fp16_decod
                     kvarn_quantize_blocks, lib, page_bytes, status_string, version)
 
 __all__ = ["Config", "KvarnError", "alloc_decode_workspace", "alloc_fp16_decode_workspace",
+           "alloc_fp8_decode_workspace", "alloc_fp8_pool", "fp8_decode_workspace_bytes",
+           "kvarn_fp8_decode_attention", "kvarn_fp8_write_blocks",
            "alloc_fp16_pool", "alloc_pool", "alloc_tails", "fp16_decode_workspace_bytes",
            "kvarn_fp16_decode_attention", "kvarn_fp16_write_blocks",
            "config_from_string", "config_validate", "decode_split_plan", "decode_workspace_bytes",

@@ -411,6 +411,98 @@ int kvarn_fp16_decode_attention(const void* q, int num_q_heads, int num_kv_heads
                                                                           : KVARN_ERR_LAUNCH;
 }
 
+int kvarn_fp8_write_blocks(const void* k, const void* v, int64_t stride_b, int64_t stride_t,
+                            int64_t stride_h, int batch, int num_kv_heads,
+                            const int32_t* seq_lens, int max_seq, const int32_t* block_table,
+                            int max_blocks, void* pool, int64_t num_pages, int32_t* status,
+                            kvarn_stream_t stream) {
+  if (batch < 0 || max_seq < 0 || max_blocks < 0 || num_pages < 0 || num_kv_heads <= 0)
+    return KVARN_ERR_INVALID_ARG;
+  if (batch == 0 || max_seq == 0) return KVARN_OK;
+  if (!k || !v || !seq_lens || !block_table || !pool || num_pages <= 0)
+    return KVARN_ERR_INVALID_ARG;
+  if ((int64_t)max_blocks * kT < (int64_t)max_seq) return KVARN_ERR_INVALID_ARG;
+  if (!aligned16(k) || !aligned16(v) || !aligned16(pool)) return KVARN_ERR_INVALID_ARG;
+  if (stride_b < 0 || stride_t < kD || stride_h < kD || (stride_b | stride_t | stride_h) % 8)
+    return KVARN_ERR_INVALID_ARG;
+  if (num_kv_heads > 65535 || batch > 65535) return KVARN_ERR_UNSUPPORTED;
+  F16WriteArgs a;
+  a.k = static_cast<const __half*>(k);
+  a.v = static_cast<const __half*>(v);
+  a.sb = stride_b;
+  a.st = stride_t;
+  a.sh = stride_h;
+  a.batch = batch;
+  a.hkv = num_kv_heads;
+  a.max_seq = max_seq;
+  a.seq_lens = seq_lens;
+  a.block_table = block_table;
+  a.max_blocks = max_blocks;
+  a.pool = static_cast<uint8_t*>(pool);
+  a.num_pages = num_pages;
+  a.status = status;
+  return launch_fp8_write(a, (cudaStream_t)stream) == cudaSuccess ? KVARN_OK : KVARN_ERR_LAUNCH;
+}
+
+size_t kvarn_fp8_decode_workspace_bytes(int num_q_heads, int num_kv_heads, int batch,
+                                         int max_seq) {
+  if (num_q_heads <= 0 || num_kv_heads <= 0 || num_q_heads % num_kv_heads || batch <= 0 ||
+      max_seq < 0)
+    return 0;
+  const int sms = device_sm_count();
+  if (sms <= 0) return 0;
+  const DecodePlan p = fp8_decode_plan(batch, num_q_heads, num_kv_heads, max_seq, sms);
+  return p.part_bytes + p.count_bytes;
+}
+
+int kvarn_fp8_decode_attention(const void* q, int num_q_heads, int num_kv_heads,
+                                const void* pool, int64_t num_pages, const int32_t* block_table,
+                                int max_blocks, const int32_t* seq_lens, int batch, int max_seq,
+                                float softmax_scale, void* out, void* workspace,
+                                size_t workspace_bytes, int32_t* status, kvarn_stream_t stream) {
+  if (num_q_heads <= 0 || num_kv_heads <= 0 || num_q_heads % num_kv_heads)
+    return KVARN_ERR_INVALID_ARG;
+  if (num_q_heads / num_kv_heads > 8) return KVARN_ERR_UNSUPPORTED;
+  if (batch < 0 || max_seq < 0 || max_blocks < 0 || num_pages < 0) return KVARN_ERR_INVALID_ARG;
+  if (batch == 0) return KVARN_OK;
+  if (!q || !seq_lens || !out) return KVARN_ERR_INVALID_ARG;
+  if (max_seq > 0 && (!pool || !block_table || num_pages <= 0 ||
+                      (int64_t)max_blocks * kT < (int64_t)max_seq))
+    return KVARN_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(pool) || !aligned16(out) || !aligned16(workspace))
+    return KVARN_ERR_INVALID_ARG;
+  if (!(softmax_scale > 0.f) || softmax_scale != softmax_scale) return KVARN_ERR_INVALID_ARG;
+  if (batch > 65535 || num_kv_heads > 65535 || num_pages > 0x7fffffff)
+    return KVARN_ERR_UNSUPPORTED;
+  const int sms = device_sm_count();
+  if (sms <= 0) return KVARN_ERR_LAUNCH;
+  const DecodePlan p = fp8_decode_plan(batch, num_q_heads, num_kv_heads, max_seq, sms);
+  if (p.nsplit > 1 && (!workspace || workspace_bytes < p.part_bytes + p.count_bytes))
+    return KVARN_ERR_WORKSPACE;
+  F16DecodeArgs a;
+  a.q = static_cast<const __half*>(q);
+  a.num_pages = num_pages;
+  a.block_table = block_table;
+  a.max_blocks = max_blocks;
+  a.seq_lens = seq_lens;
+  a.batch = batch;
+  a.max_seq = max_seq;
+  a.hq = num_q_heads;
+  a.hkv = num_kv_heads;
+  a.g = num_q_heads / num_kv_heads;
+  a.scale = softmax_scale;
+  a.out = static_cast<__half*>(out);
+  a.ws_part = p.nsplit > 1 ? static_cast<float*>(workspace) : nullptr;
+  a.ws_count = p.nsplit > 1
+                   ? reinterpret_cast<int*>(static_cast<uint8_t*>(workspace) + p.part_bytes)
+                   : nullptr;
+  a.pages_per_split = p.pages_per_split;
+  a.nsplit = p.nsplit;
+  a.status = status;
+  return launch_fp8_decode(a, pool, (cudaStream_t)stream) == cudaSuccess ? KVARN_OK
+                                                                          : KVARN_ERR_LAUNCH;
+}
+
 int kvarn_dequantize_pages(const void* records, int64_t n, float* yk, float* yv,
                            kvarn_stream_t stream) {
   if (n < 0) return KVARN_ERR_INVALID_ARG;

@@ -182,6 +182,10 @@ struct F16DecodeArgs {
 DecodePlan fp16_decode_plan(int batch, int hq, int hkv, int max_seq, int num_sms);
 cudaError_t launch_fp16_write(const F16WriteArgs& a, cudaStream_t s);
 cudaError_t launch_fp16_decode(const F16DecodeArgs& a, const void* pool, cudaStream_t s);
+// The FP8 paged cache (same argument records; pages of KVARN_FP8_PAGE_BYTES).
+DecodePlan fp8_decode_plan(int batch, int hq, int hkv, int max_seq, int num_sms);
+cudaError_t launch_fp8_write(const F16WriteArgs& a, cudaStream_t s);
+cudaError_t launch_fp8_decode(const F16DecodeArgs& a, const void* pool, cudaStream_t s);
 
 // Chunked prefill: attention of a chunk of query tokens over the quantized cache.
 struct ChunkArgs {

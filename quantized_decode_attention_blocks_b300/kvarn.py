@@ -20,6 +20,7 @@ LIB_PATH = os.path.join(HERE, "libkvarn.so")
 HEAD_DIM = 128
 BLOCK_TOKENS = 128
 PAGE_BYTES = 15360
+FP8_PAGE_BYTES = 33792     # KVARN_FP8_PAGE_BYTES
 FP16_PAGE_BYTES = 65536            # KVARN_FP16_PAGE_BYTES
 NOALLOC_SCRATCH_BYTES = 4 << 20   # KVARN_NOALLOC_SCRATCH_BYTES
 
@@ -77,6 +78,11 @@ SIGNATURES = {
     "kvarn_fp16_decode_workspace_bytes": (ctypes.c_size_t, [_I, _I, _I, _I]),
     "kvarn_fp16_decode_attention": (_I, [_P, _I, _I, _P, _L, _P, _I, _P, _I, _I,
                                          ctypes.c_float, _P, _P, ctypes.c_size_t, _P, _P]),
+    "kvarn_fp8_write_blocks": (_I, [_P, _P, _L, _L, _L, _I, _I, _P, _I, _P, _I, _P, _L, _P,
+                                    _P]),
+    "kvarn_fp8_decode_workspace_bytes": (ctypes.c_size_t, [_I, _I, _I, _I]),
+    "kvarn_fp8_decode_attention": (_I, [_P, _I, _I, _P, _L, _P, _I, _P, _I, _I,
+                                        ctypes.c_float, _P, _P, ctypes.c_size_t, _P, _P]),
     "kvarn_status_string": (ctypes.c_char_p, [_I]),
     "kvarn_version": (ctypes.c_char_p, []),
 }
@@ -440,4 +446,66 @@ def kvarn_fp16_decode_attention(q: torch.Tensor, num_kv_heads: int, pool: torch.
             block_table.shape[-1], _ptr(seq_lens), B, int(max_seq), float(softmax_scale),
             _ptr(out), _ptr(workspace), ws_bytes, _ptr(status), _stream(stream, dev)),
             "kvarn_fp16_decode_attention")
+    return out
+
+
+# ------------------------------------------------------------ FP8 cache --
+
+def alloc_fp8_pool(num_kv_heads: int, num_pages: int, device="cuda") -> torch.Tensor:
+    return torch.zeros((num_pages, num_kv_heads, FP8_PAGE_BYTES), dtype=torch.uint8,
+                       device=device)
+
+
+def kvarn_fp8_write_blocks(k: torch.Tensor, v: torch.Tensor, seq_lens: torch.Tensor,
+                           max_seq: int, block_table: torch.Tensor, pool: torch.Tensor,
+                           status: Optional[torch.Tensor] = None, stream=None) -> None:
+    """k, v fp16 [B][S][Hkv][128] -> fp8 pool uint8 [num_pages][Hkv][33792]."""
+    hkv = k.shape[2]
+    dev = _kv_pair(k, v, hkv)
+    B = k.shape[0]
+    _lens_table(dev, B, seq_lens, "seq_lens", block_table)
+    _arg(pool, "pool", torch.uint8, (None, hkv, FP8_PAGE_BYTES), device=dev)
+    _status(dev, status)
+    with _on(dev):
+        _check(lib().kvarn_fp8_write_blocks(
+            _ptr(k), _ptr(v), k.stride(0), k.stride(1), k.stride(2), B, hkv, _ptr(seq_lens),
+            int(max_seq), _ptr(block_table), block_table.shape[-1], _ptr(pool), pool.shape[0],
+            _ptr(status), _stream(stream, dev)), "kvarn_fp8_write_blocks")
+
+
+def fp8_decode_workspace_bytes(num_q_heads: int, num_kv_heads: int, batch: int,
+                               max_seq: int) -> int:
+    return lib().kvarn_fp8_decode_workspace_bytes(num_q_heads, num_kv_heads, batch, max_seq)
+
+
+def alloc_fp8_decode_workspace(num_q_heads: int, num_kv_heads: int, batch: int, max_seq: int,
+                               device="cuda") -> Optional[torch.Tensor]:
+    n = fp8_decode_workspace_bytes(num_q_heads, num_kv_heads, batch, max_seq)
+    return torch.zeros(max(n, 16), dtype=torch.uint8, device=device) if n else None
+
+
+def kvarn_fp8_decode_attention(q: torch.Tensor, num_kv_heads: int, pool: torch.Tensor,
+                               block_table: torch.Tensor, seq_lens: torch.Tensor, max_seq: int,
+                               out: torch.Tensor, workspace: Optional[torch.Tensor],
+                               softmax_scale: float = None,
+                               status: Optional[torch.Tensor] = None, stream=None):
+    """q, out fp16 [B][Hq][128] over the fp8 pages."""
+    hq = q.shape[1]
+    dev = _arg(q, "q", torch.float16, (None, hq, HEAD_DIM))
+    _arg(out, "out", torch.float16, tuple(q.shape), device=dev)
+    B = q.shape[0]
+    _lens_table(dev, B, seq_lens, "seq_lens", block_table)
+    _arg(pool, "pool", torch.uint8, (None, num_kv_heads, FP8_PAGE_BYTES), device=dev)
+    _status(dev, status)
+    if workspace is not None:
+        _arg(workspace, "workspace", None, device=dev)
+    if softmax_scale is None:
+        softmax_scale = HEAD_DIM ** -0.5
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    with _on(dev):
+        _check(lib().kvarn_fp8_decode_attention(
+            _ptr(q), hq, num_kv_heads, _ptr(pool), pool.shape[0], _ptr(block_table),
+            block_table.shape[-1], _ptr(seq_lens), B, int(max_seq), float(softmax_scale),
+            _ptr(out), _ptr(workspace), ws_bytes, _ptr(status), _stream(stream, dev)),
+            "kvarn_fp8_decode_attention")
     return out
