@@ -394,3 +394,79 @@ def fp8_decode_attention(q, pool, block_table, seq_lens, hq: int, hkv: int,
     if rc != 0:
         raise ValueError("oracle: page id outside the pool")
     return out
+
+
+# ------------------------------------------------- SnapKV-style selection --
+# "Makale Bulteni - SnapKV" (cmlonder.com): at the end of prefill the
+# attention of the prompt's last 32 or 64 tokens (the observation window) over
+# the earlier tokens is scanned once, and each head keeps its most critical,
+# clustered KV positions (pooling, then selection); the rest of the cache is
+# dropped and decode runs on a compact cache of fixed size, each head with its
+# own positions.  Readings (the page fixes none of the numbers below):
+#   * votes of KV head h: v_t = sum over the window queries i (positions
+#     P_i = n - W + i) and the query heads of h's group of
+#     softmax_{t' <= P_i}(scale q . k_t')[t], for the prefix positions
+#     t < n - W (scale 1/sqrt(128), the decode attention's);
+#   * clustering: a 1-D max pooling of the votes with an odd kernel (7 unless
+#     given), the window [t - K//2, t + K//2] clipped to the prefix;
+#   * selection: the capacity - W prefix positions with the largest pooled
+#     votes, ties to the lower position, then the W window positions, all in
+#     increasing order; a prefix no longer than capacity - W is kept whole;
+#   * compaction: the kept tokens' K and V, in that order.
+
+def snapkv_votes(q_window, k, seq_lens, hq: int, hkv: int,
+                 scale: float = 1.0 / np.sqrt(128.0)) -> np.ndarray:
+    """Votes [B][Hkv][S] (float64; zero at and beyond n - W).  q_window: fp16
+    [B][W][Hq][128] (the queries of the last W prompt tokens); k: fp16
+    [B][S][Hkv][128]; seq_lens: prompt lengths n (window included)."""
+    qd = np.asarray(q_window)
+    qd = (qd.view(np.float16) if qd.dtype == np.uint16 else qd).astype(np.float64)
+    kd = np.asarray(k)
+    kd = (kd.view(np.float16) if kd.dtype == np.uint16 else kd).astype(np.float64)
+    B, W = qd.shape[0], qd.shape[1]
+    S = kd.shape[1]
+    g = hq // hkv
+    votes = np.zeros((B, hkv, S))
+    for b in range(B):
+        n = int(seq_lens[b])
+        if n <= W:
+            continue
+        for h in range(hkv):
+            for i in range(W):
+                P = n - W + i
+                for hh in range(g):
+                    s = (kd[b, :P + 1, h] @ qd[b, i, h * g + hh]) * scale
+                    p = np.exp(s - s.max())
+                    p /= p.sum()
+                    votes[b, h, :n - W] += p[:n - W]
+    return votes
+
+
+def snapkv_pool(votes_1d, kernel: int = 7) -> np.ndarray:
+    """1-D max pooling over a prefix of votes (window clipped to its ends)."""
+    v = np.asarray(votes_1d, dtype=np.float64)
+    n = len(v)
+    r = kernel // 2
+    return np.array([v[max(0, t - r):min(n, t + r + 1)].max() for t in range(n)])
+
+
+def snapkv_select(votes, seq_lens, window: int, capacity: int, kernel: int = 7):
+    """Kept positions [B][Hkv][capacity] (int32, increasing; -1 past a short
+    sequence's n) from the votes of snapkv_votes."""
+    votes = np.asarray(votes)
+    B, hkv, _ = votes.shape
+    out = np.full((B, hkv, capacity), -1, dtype=np.int32)
+    for b in range(B):
+        n = int(seq_lens[b])
+        npre = max(n - window, 0)
+        keep_pre = capacity - window
+        for h in range(hkv):
+            if npre <= keep_pre:
+                kept = list(range(n))
+            else:
+                pooled = snapkv_pool(votes[b, h, :npre], kernel)
+                # largest first, ties to the lower position
+                order = sorted(range(npre), key=lambda t: (-pooled[t], t))
+                kept = sorted(order[:keep_pre]) + list(range(npre, n))
+            out[b, h, :len(kept)] = kept
+    return out

@@ -802,3 +802,71 @@ def test_fp8_attention_matches_torch_sdpa_on_dequantized_cache(oracle):
                 qq, torch.from_numpy(K)[None, None].expand(1, 4, n, 128),
                 torch.from_numpy(V)[None, None].expand(1, 4, n, 128))
             assert np.abs(out[b, kvh * 4:(kvh + 1) * 4] - ref[0, :, 0].numpy()).max() < 1e-12
+
+
+# ------------------------------------------------- SnapKV-style selection --
+# "Makale Bulteni - SnapKV" (cmlonder.com): the observation window's attention
+# over the prefix, pooled, then each head's top positions kept.
+
+def _snap_inputs(seed, B=2, S=300, hkv=2, hq=8, W=16):
+    rng = np.random.default_rng(seed)
+    k = (rng.standard_normal((B, S, hkv, 128)) * 2).astype(np.float16)
+    q = rng.standard_normal((B, W, hq, 128)).astype(np.float16)
+    return q, k
+
+
+def test_snapkv_votes_are_softmax_mass_on_the_prefix(oracle):
+    # each window query's softmax sums to 1 over its causal context, so the
+    # votes of a KV head plus that mass on the window tokens is W x g
+    q, k = _snap_inputs(70)
+    lens = np.array([300, 200])
+    W, g = 16, 4
+    votes = oracle.snapkv_votes(q, k, lens, 8, 2)
+    for b in range(2):
+        n = int(lens[b])
+        for h in range(2):
+            win_mass = 0.0
+            for i in range(W):
+                P = n - W + i
+                for hh in range(g):
+                    qq = torch.from_numpy(q[b, i, h * g + hh].astype(np.float64))
+                    kk = torch.from_numpy(k[b, :P + 1, h].astype(np.float64))
+                    a = torch.softmax(kk @ qq / np.sqrt(128.0), 0).numpy()
+                    win_mass += a[n - W:].sum()
+            assert abs(votes[b, h].sum() + win_mass - W * g) < 1e-9
+            assert not votes[b, h, n - W:].any()
+
+
+def test_snapkv_pool_equals_scipy_maximum_filter(oracle):
+    from scipy.ndimage import maximum_filter1d
+    v = np.random.default_rng(71).random(257)
+    for kern in (1, 3, 7, 9):
+        ref = maximum_filter1d(v, size=kern, mode="nearest")
+        assert np.array_equal(oracle.snapkv_pool(v, kern), ref)
+
+
+def test_snapkv_select_brute_force_and_ties(oracle):
+    rng = np.random.default_rng(72)
+    votes = rng.random((1, 2, 100))
+    votes[0, 1, :] = 0.5                                  # all tied: lowest positions
+    lens = np.array([90])
+    idx = oracle.snapkv_select(votes, lens, window=10, capacity=30, kernel=1)
+    pooled = votes[0, 0, :80]
+    assert np.array_equal(idx[0, 0, :20], np.sort(np.argsort(-pooled, kind="stable")[:20]))
+    assert np.array_equal(idx[0, 0, 20:], np.arange(80, 90))
+    assert np.array_equal(idx[0, 1], np.concatenate([np.arange(20), np.arange(80, 90)]))
+    # a short prompt is kept whole, the rest marked -1
+    idx = oracle.snapkv_select(votes, np.array([25]), window=10, capacity=30)
+    assert np.array_equal(idx[0, 0, :25], np.arange(25)) and (idx[0, 0, 25:] == -1).all()
+
+
+def test_snapkv_keeps_the_cluster_around_a_planted_key(oracle):
+    # a key aligned with every window query at position 100 draws the votes;
+    # pooling with kernel 7 spreads its score to 97..103, which are kept
+    q, k = _snap_inputs(73, B=1, S=300, hkv=1, hq=2)
+    qm = q.astype(np.float64).mean(axis=(1, 2))[0]
+    k[0, 100, 0] = (qm / np.linalg.norm(qm) * 40).astype(np.float16)
+    votes = oracle.snapkv_votes(q, k, np.array([300]), 2, 1)
+    assert votes[0, 0].argmax() == 100
+    idx = oracle.snapkv_select(votes, np.array([300]), window=16, capacity=40, kernel=7)
+    assert set(range(97, 104)) <= set(idx[0, 0].tolist())
