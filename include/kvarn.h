@@ -257,6 +257,62 @@ int kvarn_chunk_attention(const kvarn_config_t *cfg, const void *q, int chunk_ma
                           const void *tail_v, float softmax_scale, void *out, int32_t *status,
                           kvarn_stream_t stream);
 
+/* ---- SnapKV-style one-shot selection at the end of prefill ----
+ * "Makale Bulteni - SnapKV" (cmlonder.com): the attention of the prompt's last
+ * `window` tokens (the observation window, 32 or 64 on the page) over the
+ * earlier tokens is scanned once, and each KV head keeps its most critical,
+ * clustered positions; decode then runs on a compact cache of `capacity`
+ * tokens per head (kvarn_snapkv_gather, then kvarn_quantize_blocks).
+ * Readings: votes[b][h][t] = sum over the window queries (position
+ * n - window + i) and the query heads of KV head h's group of their softmax
+ * (over each query's causal context, scale softmax_scale) at prefix position
+ * t < n - window; clustering = max pooling of the votes with the odd kernel
+ * pool_kernel (window [t - k/2, t + k/2] clipped to the prefix); kept = the
+ * capacity - window prefix positions with the largest pooled votes (ties to
+ * the lower position), then the window, in increasing order; a prompt whose
+ * prefix is no longer than capacity - window is kept whole. */
+
+/* Workspace of kvarn_snapkv_select (16-byte aligned). */
+size_t kvarn_snapkv_workspace_bytes(const kvarn_config_t *cfg, int batch, int window,
+                                    int max_seq);
+
+/*   q_window   fp16 [batch][window][Hq][128] (device), the queries of each
+ *              prompt's last `window` tokens (row i = position n - window + i)
+ *   k          fp16 (device), element (b, t, h, c) at b*stride_b + t*stride_t +
+ *              h*stride_h + c (strides in elements, multiples of 8), t < max_seq
+ *   seq_lens   int32 [batch] (device) prompt lengths n, window included
+ *   capacity   tokens kept per (sequence, KV head), >= window
+ *   pool_kernel odd pooling width >= 1
+ *   votes      float32 [batch][Hkv][max_seq] (device), written whole (0 from
+ *              n - window on)
+ *   indices    int32 [batch][Hkv][capacity] (device): kept positions,
+ *              increasing; -1 past the end of a prompt shorter than capacity
+ *   workspace  kvarn_snapkv_workspace_bytes() bytes (device, 16-byte aligned;
+ *              caller-owned, no contents kept between calls)
+ * Three launches on `stream`: the window's scores on the tensor cores
+ * (statistics, then votes), then pooling and selection.  A length outside
+ * [0, max_seq] is reported (KVARN_STATUS_BAD_LENGTH) and that sequence treated
+ * as empty; a wait that runs out is reported (KVARN_STATUS_TIMEOUT).
+ * Returns KVARN_ERR_INVALID_ARG for null or misaligned pointers, bad strides,
+ * window <= 0, capacity < window or an even kernel; KVARN_ERR_WORKSPACE for a
+ * short workspace. */
+int kvarn_snapkv_select(const kvarn_config_t *cfg, const void *q_window, int window,
+                        const void *k, int64_t stride_b, int64_t stride_t, int64_t stride_h,
+                        const int32_t *seq_lens, int batch, int max_seq, int capacity,
+                        int pool_kernel, float softmax_scale, float *votes, int32_t *indices,
+                        void *workspace, size_t workspace_bytes, int32_t *status,
+                        kvarn_stream_t stream);
+
+/* The kept tokens into the compact cache: k_out, v_out fp16
+ * [batch][capacity][Hkv][128] (device, dense), token j of head h = token
+ * indices[b][h][j] of k, v (same layout and strides as in
+ * kvarn_snapkv_select, t < max_seq); a position outside [0, max_seq) (the -1
+ * padding) gives zeros.  One launch on `stream`. */
+int kvarn_snapkv_gather(const void *k, const void *v, int64_t stride_b, int64_t stride_t,
+                        int64_t stride_h, int batch, int max_seq, int num_kv_heads,
+                        const int32_t *indices, int capacity, void *k_out, void *v_out,
+                        kvarn_stream_t stream);
+
 /* Diagnosis: dequantizes `n` page records into float32 rotated-space tiles.
  *   records   [n][15360] bytes (e.g. pool + page*Hkv*15360, one record per
  *             (page, head) in order)

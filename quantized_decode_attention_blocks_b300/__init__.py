@@ -6,6 +6,7 @@ include/kvarn.h); this package is its thin Python binding.
 from .kvarn import (Config, KvarnError, alloc_decode_workspace, alloc_fp16_decode_workspace,
                     alloc_fp8_decode_workspace, alloc_fp8_pool, fp8_decode_workspace_bytes,
                     kvarn_fp8_decode_attention, kvarn_fp8_write_blocks,
+                    kvarn_snapkv_gather, kvarn_snapkv_select, snapkv_workspace_bytes,
                     alloc_fp16_pool, alloc_pool, alloc_tails, fp16_decode_workspace_bytes,
                     kvarn_fp16_decode_attention, kvarn_fp16_write_blocks,
                     config_from_string, config_validate, decode_split_plan, decode_workspace_bytes,
@@ -16,6 +17,7 @@ from .kvarn import (Config, KvarnError, alloc_decode_workspace, alloc_fp16_decod
 __all__ = ["Config", "KvarnError", "alloc_decode_workspace", "alloc_fp16_decode_workspace",
            "alloc_fp8_decode_workspace", "alloc_fp8_pool", "fp8_decode_workspace_bytes",
            "kvarn_fp8_decode_attention", "kvarn_fp8_write_blocks",
+           "kvarn_snapkv_gather", "kvarn_snapkv_select", "snapkv_workspace_bytes",
            "alloc_fp16_pool", "alloc_pool", "alloc_tails", "fp16_decode_workspace_bytes",
            "kvarn_fp16_decode_attention", "kvarn_fp16_write_blocks",
            "config_from_string", "config_validate", "decode_split_plan", "decode_workspace_bytes",

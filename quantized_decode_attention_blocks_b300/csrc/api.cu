@@ -503,6 +503,98 @@ int kvarn_fp8_decode_attention(const void* q, int num_q_heads, int num_kv_heads,
                                                                           : KVARN_ERR_LAUNCH;
 }
 
+size_t kvarn_snapkv_workspace_bytes(const kvarn_config_t* cfg, int batch, int window,
+                                     int max_seq) {
+  if (kvarn_config_validate(cfg) != KVARN_OK || batch <= 0 || window <= 0 || max_seq <= 0)
+    return 0;
+  const int g = cfg->num_q_heads / cfg->num_kv_heads;
+  const int64_t nrt = ((int64_t)window * g + 127) / 128;
+  const int64_t nchunks = ((int64_t)max_seq + kSnapChunkTiles * 128 - 1) / (kSnapChunkTiles * 128);
+  const size_t stats = ((size_t)batch * cfg->num_kv_heads * nrt * nchunks * 256 * 4 + 255) & ~(size_t)255;
+  const size_t pooled = ((size_t)batch * cfg->num_kv_heads * max_seq * 4 + 255) & ~(size_t)255;
+  return stats + pooled;
+}
+
+int kvarn_snapkv_select(const kvarn_config_t* cfg, const void* q_window, int window,
+                        const void* k, int64_t stride_b, int64_t stride_t, int64_t stride_h,
+                        const int32_t* seq_lens, int batch, int max_seq, int capacity,
+                        int pool_kernel, float softmax_scale, float* votes, int32_t* indices,
+                        void* workspace, size_t workspace_bytes, int32_t* status,
+                        kvarn_stream_t stream) {
+  int rc = kvarn_config_validate(cfg);
+  if (rc != KVARN_OK) return rc;
+  if (batch < 0 || max_seq < 0 || window <= 0 || capacity < window || pool_kernel < 1 ||
+      pool_kernel % 2 == 0)
+    return KVARN_ERR_INVALID_ARG;
+  if (batch == 0 || max_seq == 0) return KVARN_OK;
+  if (!q_window || !k || !seq_lens || !votes || !indices || !workspace)
+    return KVARN_ERR_INVALID_ARG;
+  if (!aligned16(q_window) || !aligned16(k) || !aligned16(workspace) ||
+      ((uintptr_t)votes & 3) || ((uintptr_t)indices & 3))
+    return KVARN_ERR_INVALID_ARG;
+  if (stride_b < 0 || stride_t < kD || stride_h < kD || (stride_b | stride_t | stride_h) % 8)
+    return KVARN_ERR_INVALID_ARG;
+  if (!(softmax_scale > 0.f) || softmax_scale != softmax_scale) return KVARN_ERR_INVALID_ARG;
+  if (batch > 65535 || cfg->num_kv_heads > 65535) return KVARN_ERR_UNSUPPORTED;
+  const size_t need = kvarn_snapkv_workspace_bytes(cfg, batch, window, max_seq);
+  if (workspace_bytes < need) return KVARN_ERR_WORKSPACE;
+  SnapArgs a;
+  a.q = static_cast<const __half*>(q_window);
+  a.W = window;
+  a.batch = batch;
+  a.max_seq = max_seq;
+  a.hq = cfg->num_q_heads;
+  a.hkv = cfg->num_kv_heads;
+  a.g = cfg->num_q_heads / cfg->num_kv_heads;
+  a.seq_lens = seq_lens;
+  a.scale_log2 = softmax_scale * 1.4426950408889634f;
+  a.nrt = (window * a.g + 127) / 128;
+  a.nchunks = (max_seq + kSnapChunkTiles * 128 - 1) / (kSnapChunkTiles * 128);
+  a.stats = static_cast<float*>(workspace);
+  const size_t stats = ((size_t)batch * a.hkv * a.nrt * a.nchunks * 256 * 4 + 255) & ~(size_t)255;
+  a.votes = votes;
+  a.status = status;
+  CUtensorMap tm;
+  if (!encode_kv_tile_map(&tm, k, stride_b, stride_t, stride_h, batch, max_seq, a.hkv, &a.roles))
+    return KVARN_ERR_INVALID_ARG;
+  cudaStream_t s = (cudaStream_t)stream;
+  if (launch_snapkv_scores(a, tm, 0, s) != cudaSuccess) return KVARN_ERR_LAUNCH;
+  if (launch_snapkv_scores(a, tm, 1, s) != cudaSuccess) return KVARN_ERR_LAUNCH;
+  SnapSelectArgs sa;
+  sa.votes = votes;
+  sa.pooled = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + stats);
+  sa.seq_lens = seq_lens;
+  sa.batch = batch;
+  sa.hkv = a.hkv;
+  sa.max_seq = max_seq;
+  sa.W = window;
+  sa.capacity = capacity;
+  sa.kernel = pool_kernel;
+  sa.indices = indices;
+  return launch_snapkv_select(sa, s) == cudaSuccess ? KVARN_OK : KVARN_ERR_LAUNCH;
+}
+
+int kvarn_snapkv_gather(const void* k, const void* v, int64_t stride_b, int64_t stride_t,
+                        int64_t stride_h, int batch, int max_seq, int num_kv_heads,
+                        const int32_t* indices, int capacity, void* k_out, void* v_out,
+                        kvarn_stream_t stream) {
+  if (batch < 0 || max_seq < 0 || num_kv_heads <= 0 || capacity < 0)
+    return KVARN_ERR_INVALID_ARG;
+  if (batch == 0 || capacity == 0) return KVARN_OK;
+  if (!k || !v || !indices || !k_out || !v_out) return KVARN_ERR_INVALID_ARG;
+  if (!aligned16(k) || !aligned16(v) || !aligned16(k_out) || !aligned16(v_out))
+    return KVARN_ERR_INVALID_ARG;
+  if (stride_b < 0 || stride_t < kD || stride_h < kD || (stride_b | stride_t | stride_h) % 8)
+    return KVARN_ERR_INVALID_ARG;
+  if (batch > 65535 || num_kv_heads > 65535) return KVARN_ERR_UNSUPPORTED;
+  return launch_snapkv_gather(static_cast<const __half*>(k), static_cast<const __half*>(v),
+                              stride_b, stride_t, stride_h, batch, max_seq, num_kv_heads,
+                              indices, capacity, static_cast<__half*>(k_out), static_cast<__half*>(v_out),
+                              (cudaStream_t)stream) == cudaSuccess
+             ? KVARN_OK
+             : KVARN_ERR_LAUNCH;
+}
+
 int kvarn_dequantize_pages(const void* records, int64_t n, float* yk, float* yv,
                            kvarn_stream_t stream) {
   if (n < 0) return KVARN_ERR_INVALID_ARG;

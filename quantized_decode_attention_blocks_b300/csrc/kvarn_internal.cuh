@@ -148,6 +148,44 @@ cudaError_t launch_dequantize(const uint8_t* rec, int64_t n, float* yk, float* y
 bool encode_fp16_map_4d(CUtensorMap* map, const void* base, const uint64_t dims[4],
                         const uint64_t strides[3], const uint32_t box[4]);
 
+// Tensor map over fp16 [B][S][Hkv][128] (element strides sb, st, sh) with
+// boxes of 64 channels x 128 tokens of one (head, sequence), 128-byte swizzle;
+// the three outer dimensions ordered by stride, *roles = the map dimension of
+// the head (bits 0-1) and of the token (bits 2-3).  False if the driver
+// rejects it.
+bool encode_kv_tile_map(CUtensorMap* map, const void* base, int64_t sb, int64_t st, int64_t sh,
+                        int batch, int tokens, int hkv, int* roles);
+
+// SnapKV-style selection: scores of the observation window over the prefix.
+struct SnapArgs {
+  const __half* q;            // [B][W][Hq][128] window queries
+  int W;                      // window tokens
+  int batch, max_seq, hq, hkv, g;
+  int roles;                  // tensor-map dimensions of (head, token) for k
+  const int32_t* seq_lens;    // prompt lengths n (window included)
+  float scale_log2;           // softmax scale * log2(e)
+  int nrt;                    // 128-row tiles of the W x g window rows
+  int nchunks;                // token chunks per sequence
+  float* stats;               // [B][Hkv][nrt][nchunks][128]{m, Z} (workspace)
+  float* votes;               // [B][Hkv][max_seq]
+  int32_t* status;
+};
+constexpr int kSnapChunkTiles = 16;   // 2048 tokens per CTA
+cudaError_t launch_snapkv_scores(const SnapArgs& a, const CUtensorMap& tm, int mode,
+                                 cudaStream_t s);
+struct SnapSelectArgs {
+  const float* votes;         // [B][Hkv][max_seq]
+  float* pooled;              // [B][Hkv][max_seq] (workspace)
+  const int32_t* seq_lens;
+  int batch, hkv, max_seq, W, capacity, kernel;
+  int32_t* indices;           // [B][Hkv][capacity]
+};
+cudaError_t launch_snapkv_select(const SnapSelectArgs& a, cudaStream_t s);
+cudaError_t launch_snapkv_gather(const __half* k, const __half* v, int64_t sb, int64_t st,
+                                 int64_t sh, int batch, int max_seq, int hkv,
+                                 const int32_t* indices, int capacity, __half* k_out,
+                                 __half* v_out, cudaStream_t s);
+
 // The FP16 paged cache the quantized one is compared with.
 constexpr int kF16PageBytes = 2 * kT * kD * 2;   // K then V, [128 tokens][128] fp16 each
 

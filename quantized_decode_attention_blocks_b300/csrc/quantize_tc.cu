@@ -839,6 +839,11 @@ cudaError_t launch_tiles(const CUtensorMap& mk, const CUtensorMap& mv, const QTi
 
 }  // namespace
 
+bool encode_kv_tile_map(CUtensorMap* map, const void* base, int64_t sb, int64_t st, int64_t sh,
+                        int batch, int tokens, int hkv, int* roles) {
+  return encode_tile_map(map, base, sb, st, sh, batch, tokens, hkv, roles);
+}
+
 bool encode_fp16_map_4d(CUtensorMap* map, const void* base, const uint64_t dims[4],
                         const uint64_t strides[3], const uint32_t box[4]) {
   EncodeTiledFn fn = encode_fn();

@@ -83,6 +83,10 @@ SIGNATURES = {
     "kvarn_fp8_decode_workspace_bytes": (ctypes.c_size_t, [_I, _I, _I, _I]),
     "kvarn_fp8_decode_attention": (_I, [_P, _I, _I, _P, _L, _P, _I, _P, _I, _I,
                                         ctypes.c_float, _P, _P, ctypes.c_size_t, _P, _P]),
+    "kvarn_snapkv_workspace_bytes": (ctypes.c_size_t, [ctypes.POINTER(Config), _I, _I, _I]),
+    "kvarn_snapkv_select": (_I, [ctypes.POINTER(Config), _P, _I, _P, _L, _L, _L, _P, _I, _I, _I,
+                                 _I, ctypes.c_float, _P, _P, _P, ctypes.c_size_t, _P, _P]),
+    "kvarn_snapkv_gather": (_I, [_P, _P, _L, _L, _L, _I, _I, _I, _P, _I, _P, _P, _P]),
     "kvarn_status_string": (ctypes.c_char_p, [_I]),
     "kvarn_version": (ctypes.c_char_p, []),
 }
@@ -509,3 +513,57 @@ def kvarn_fp8_decode_attention(q: torch.Tensor, num_kv_heads: int, pool: torch.T
             _ptr(out), _ptr(workspace), ws_bytes, _ptr(status), _stream(stream, dev)),
             "kvarn_fp8_decode_attention")
     return out
+
+
+# ------------------------------------------------- SnapKV-style selection --
+
+def snapkv_workspace_bytes(cfg: Config, batch: int, window: int, max_seq: int) -> int:
+    return lib().kvarn_snapkv_workspace_bytes(ctypes.byref(cfg), batch, window, max_seq)
+
+
+def kvarn_snapkv_select(cfg: Config, q_window: torch.Tensor, k: torch.Tensor,
+                        seq_lens: torch.Tensor, max_seq: int, capacity: int,
+                        votes: torch.Tensor, indices: torch.Tensor, workspace: torch.Tensor,
+                        pool_kernel: int = 7, softmax_scale: float = None,
+                        status: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+    """q_window fp16 [B][W][Hq][128]; k fp16 [B][S][Hkv][128] (dense last dim);
+    votes float32 [B][Hkv][max_seq]; indices int32 [B][Hkv][capacity]."""
+    dev = _arg(q_window, "q_window", torch.float16, (None, None, cfg.num_q_heads, HEAD_DIM))
+    B, W = q_window.shape[0], q_window.shape[1]
+    _arg(k, "k", torch.float16, (B, _AtLeast(max_seq), cfg.num_kv_heads, HEAD_DIM), device=dev,
+         contiguous=False)
+    if k.stride(3) != 1:
+        raise ValueError("k must have a dense last dimension")
+    _arg(seq_lens, "seq_lens", torch.int32, (_AtLeast(B),), device=dev)
+    _arg(votes, "votes", torch.float32, (B, cfg.num_kv_heads, max_seq), device=dev)
+    _arg(indices, "indices", torch.int32, (B, cfg.num_kv_heads, capacity), device=dev)
+    _arg(workspace, "workspace", None, device=dev)
+    _status(dev, status)
+    if softmax_scale is None:
+        softmax_scale = HEAD_DIM ** -0.5
+    ws_bytes = workspace.numel() * workspace.element_size()
+    with _on(dev):
+        _check(lib().kvarn_snapkv_select(
+            ctypes.byref(cfg), _ptr(q_window), W, _ptr(k), k.stride(0), k.stride(1), k.stride(2),
+            _ptr(seq_lens), B, int(max_seq), int(capacity), int(pool_kernel),
+            float(softmax_scale), _ptr(votes), _ptr(indices), _ptr(workspace), ws_bytes,
+            _ptr(status), _stream(stream, dev)), "kvarn_snapkv_select")
+    return indices
+
+
+def kvarn_snapkv_gather(k: torch.Tensor, v: torch.Tensor, indices: torch.Tensor,
+                        k_out: torch.Tensor, v_out: torch.Tensor, stream=None) -> None:
+    """k, v fp16 [B][S][Hkv][128]; indices int32 [B][Hkv][C]; k_out, v_out
+    fp16 [B][C][Hkv][128]."""
+    hkv = k.shape[2]
+    dev = _kv_pair(k, v, hkv)
+    B = k.shape[0]
+    C = indices.shape[-1]
+    _arg(indices, "indices", torch.int32, (B, hkv, C), device=dev)
+    _arg(k_out, "k_out", torch.float16, (B, C, hkv, HEAD_DIM), device=dev)
+    _arg(v_out, "v_out", torch.float16, (B, C, hkv, HEAD_DIM), device=dev)
+    with _on(dev):
+        _check(lib().kvarn_snapkv_gather(
+            _ptr(k), _ptr(v), k.stride(0), k.stride(1), k.stride(2), B, k.shape[1], hkv,
+            _ptr(indices), C,
+            _ptr(k_out), _ptr(v_out), _stream(stream, dev)), "kvarn_snapkv_gather")

@@ -257,3 +257,39 @@ def test_host_validation_fp16_cache():
         assert dec() == K.ERR_LAUNCH                  # no device to plan for
     assert dec(batch=0) == K.OK
     assert kv.fp16_decode_workspace_bytes(8, 3, 1, 5000) == 0      # bad group
+
+
+def test_host_validation_snapkv():
+    # SnapKV-style selection and gather: every call here is invalid (or has
+    # nothing to do), so none reaches a launch
+    L = kv.lib()
+    c = _cfg()
+    P = ctypes.c_void_p
+    a16, mis = P(4096), P(4100)
+    ws = kv.snapkv_workspace_bytes(c, 2, 32, 5000)
+    # statistics: 2 x 2 heads x 2 row tiles (32 x 4 rows) x 3 chunks x 1 KB,
+    # pooled votes: 2 x 2 x 5000 floats
+    assert ws == 2 * 2 * 1 * 3 * 1024 + ((2 * 2 * 5000 * 4 + 255) & ~255)
+    assert kv.snapkv_workspace_bytes(c, 0, 32, 5000) == 0
+    sel = lambda **kw: L.kvarn_snapkv_select(
+        ctypes.byref(c), kw.get("q", a16), kw.get("W", 32), kw.get("k", a16), 5000 * 256, 256,
+        128, kw.get("lens", a16), kw.get("batch", 2), 5000, kw.get("cap", 1024),
+        kw.get("kern", 7), kw.get("scale", 0.088), kw.get("votes", a16), kw.get("idx", a16),
+        kw.get("ws", a16), kw.get("ws_bytes", ws), None, None)
+    assert sel(q=None) == K.ERR_INVALID_ARG
+    assert sel(k=mis) == K.ERR_INVALID_ARG
+    assert sel(votes=P(4098)) == K.ERR_INVALID_ARG
+    assert sel(W=0) == K.ERR_INVALID_ARG
+    assert sel(cap=31) == K.ERR_INVALID_ARG           # smaller than the window
+    assert sel(kern=4) == K.ERR_INVALID_ARG           # even pooling width
+    assert sel(scale=0.0) == K.ERR_INVALID_ARG
+    assert sel(ws_bytes=ws - 1) == K.ERR_WORKSPACE
+    assert sel(batch=0, q=None) == K.OK
+    gat = lambda **kw: L.kvarn_snapkv_gather(
+        kw.get("k", a16), a16, 5000 * 256, kw.get("st", 256), 128, 2, 5000, kw.get("hkv", 2),
+        a16, kw.get("cap", 1024), kw.get("ko", a16), a16, None)
+    assert gat(k=None) == K.ERR_INVALID_ARG
+    assert gat(ko=mis) == K.ERR_INVALID_ARG
+    assert gat(st=100) == K.ERR_INVALID_ARG
+    assert gat(hkv=0) == K.ERR_INVALID_ARG
+    assert gat(cap=0, k=None) == K.OK
