@@ -250,7 +250,7 @@ class Unit:
                                        status=self.status)
 
 
-def build_units(w, dev, rank):
+def build_units(w, dev, rank, max_units=0):
     """The units one step runs, and the units the timed launches rotate over.
 
     A model with several layers: one unit per layer, every layer's pages in
@@ -276,6 +276,8 @@ def build_units(w, dev, rank):
     if w.layers > 1:
         return units, w.layers
     nrep = max(2, min(8, -(-int(2.5 * L2_BYTES) // max(units[0].bytes_decode, 1))))
+    if max_units > 0:
+        nrep = min(nrep, max_units)
     for i in range(1, nrep):
         units += one_model(synth.scaled(w, seed=w.seed + 1000 * i))
     return units, 1
@@ -338,7 +340,7 @@ def run_gpu(args, rank, world):
     dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0)))
     torch.cuda.set_device(dev)
     w = synth.WORKLOADS[args.workload]
-    units, per_step = build_units(w, dev, rank)
+    units, per_step = build_units(w, dev, rank, args.units)
     nu = len(units)
     stream = torch.cuda.current_stream()
     flush = torch.empty(512 * 1024 * 1024, dtype=torch.uint8, device=dev)
@@ -411,7 +413,8 @@ def run_gpu(args, rank, world):
     e2e = measure_e2e(units[:per_step], args, stream)
     # the chunked-prefill kernel on its own workload (not part of the step)
     chunk = measure_chunk(args, dev, stream) if not args.no_chunk else None
-    return units[:per_step], ms, ms_step, ms_fused, wall, clocks, e2e, ms_cold, nu, chunk
+    snap = measure_snapkv(args, dev, stream) if not args.no_chunk else None
+    return units[:per_step], ms, ms_step, ms_fused, wall, clocks, e2e, ms_cold, nu, chunk, snap
 
 
 def measured_tensor_peak():
@@ -480,6 +483,73 @@ def measure_chunk(args, dev, stream):
             "roofline": {"bound": "tensor", "achieved": tflops, "peak": peak,
                          "peak_kind": f"{kind} bf16_tflops (burst; fp16 runs at the bf16 rate)",
                          "unit": "TFLOP/s", "frac": tflops / peak, "traffic": None}}
+
+
+def measure_snapkv(args, dev, stream):
+    """SnapKV-style selection (kvarn_snapkv_select, then kvarn_snapkv_gather)
+    on its own workload: 16 prompts of 4096 tokens of the Llama-3-8B-like
+    layer (8 KV heads, 32 query heads), a 32-token observation window and a
+    1024-token budget per KV head, pooling width 7.  HBM-bound: the
+    algorithmic bytes of the selection are the prompt's keys read once plus
+    the window queries, the votes and the kept positions; those of the gather
+    are the kept K and V rows read and written."""
+    import quantized_decode_attention_blocks_b300 as kv
+    w = synth.WORKLOADS["llama3_8b_layer"]
+    B, S, W, C = 16, 4096, 32, 1024
+    cfg = kv.config_from_string("k4v2_g128", w.hq, w.hkv)
+    reps = []
+    for r in range(2):   # two replicas, rotated: 2 x 134 MB of keys, above L2
+        wr = synth.scaled(w, batch=B, seq=S, seed=w.seed + 700 + r)
+        k, v = synth.kv(wr, device=dev)
+        g = torch.Generator(device=dev)
+        g.manual_seed(1900 + r)
+        qw = torch.randn((B, W, w.hq, D), generator=g, device=dev).to(torch.float16)
+        reps.append(dict(k=k, v=v, qw=qw, lens=torch.full((B,), S, dtype=torch.int32, device=dev),
+                         votes=torch.empty((B, w.hkv, S), device=dev),
+                         idx=torch.empty((B, w.hkv, C), dtype=torch.int32, device=dev),
+                         ko=torch.empty((B, C, w.hkv, D), dtype=torch.float16, device=dev),
+                         vo=torch.empty((B, C, w.hkv, D), dtype=torch.float16, device=dev),
+                         ws=torch.empty(kv.snapkv_workspace_bytes(cfg, B, W, S), dtype=torch.uint8,
+                                        device=dev),
+                         st=torch.zeros(1, dtype=torch.int32, device=dev)))
+
+    def select(i):
+        r = reps[i % 2]
+        kv.kvarn_snapkv_select(cfg, r["qw"], r["k"], r["lens"], S, C, r["votes"], r["idx"],
+                               r["ws"], status=r["st"])
+
+    def gather(i):
+        r = reps[i % 2]
+        kv.kvarn_snapkv_gather(r["k"], r["v"], r["idx"], r["ko"], r["vo"])
+
+    for i in range(max(args.warmup, 3)):
+        select(i)
+        gather(i)
+    torch.cuda.synchronize()
+    n = max(4, min(args.steps, 20))
+    ms_sel = time_graph(select, n, stream) / n
+    ms_gat = time_graph(gather, n, stream) / n
+    for r in reps:
+        if int(r["st"].item()) != 0:
+            raise RuntimeError(f"snapkv status {int(r['st'].item())}")
+    sel_bytes = B * S * w.hkv * D * 2 + B * W * w.hq * D * 2 + B * w.hkv * S * 4 + B * w.hkv * C * 4
+    gat_bytes = 2 * 2 * B * C * w.hkv * D * 2 + B * w.hkv * C * 4
+    peak, kind = measured_peaks()
+    sel_gbs = sel_bytes / (ms_sel * 1e-3) / 1e9
+    gat_gbs = gat_bytes / (ms_gat * 1e-3) / 1e9
+    return {"workload": "llama3_8b_layer SnapKV-style selection: 16 prompts x 4096 tokens, "
+                        "window 32, 1024 kept per KV head, pooling 7; 8 KV heads, 32 query "
+                        "heads, head_dim 128",
+            "select_us": ms_sel * 1e3, "gather_us": ms_gat * 1e3,
+            "launches": "select: scores (statistics), scores (votes), pooling + selection; "
+                        "gather: one",
+            "gather_gbs": gat_gbs, "gather_frac_of_hbm": gat_gbs / peak,
+            "roofline": {"bound": "hbm", "kernel": "select (three launches)", "achieved": sel_gbs,
+                         "peak": peak, "peak_kind": f"{kind} hbm_gbs (burst copy)",
+                         "unit": "GB/s", "frac": sel_gbs / peak, "traffic": None,
+                         "algorithmic_bytes_per_call": sel_bytes,
+                         "note": "the two score launches each read the keys, so 2x the "
+                                 "algorithmic key bytes move"}}
 
 
 def measure_e2e(step_units, args, stream):
@@ -599,7 +669,12 @@ def main():
     ap.add_argument("--impl", default="kvarn", choices=["kvarn", "reference"])
     ap.add_argument("--workload", default="qwen25_15b", choices=sorted(synth.WORKLOADS))
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--no-chunk", action="store_true", help="skip the chunked-prefill line")
+    ap.add_argument("--units", type=int, default=0,
+                    help="at most this many rotated replicas of a one-layer workload "
+                         "(default: enough to keep the working set above L2; counter "
+                         "captures under ncu use 1)")
+    ap.add_argument("--no-chunk", action="store_true",
+                    help="skip the chunked-prefill and SnapKV lines")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
@@ -611,7 +686,8 @@ def main():
         return 0
     if world > 1:
         torch.distributed.init_process_group("nccl")
-    units, ms, ms_step, ms_fused, wall, clocks, e2e, ms_cold, nu, chunk = run_gpu(args, rank, world)
+    units, ms, ms_step, ms_fused, wall, clocks, e2e, ms_cold, nu, chunk, snap = run_gpu(
+        args, rank, world)
     if world > 1:
         torch.distributed.destroy_process_group()
     if rank != 0:
@@ -691,6 +767,7 @@ def main():
                             "us_per_launch": per_launch["decode"]},
         "e2e": e2e,
         "chunk_prefill": chunk,
+        "snapkv": snap,
         "gpu_launches": LAUNCHES_PER_STEP * L * args.steps,
         "clocks": clocks,
         "wall_s_timed_region": wall,

@@ -148,8 +148,11 @@ __device__ __forceinline__ constexpr float vpos_inv(int kb, int f) {
                        : (f ? 1.f / 16 : 0.25f);
 }
 
+// Three CTAs per SM for one head tile; for two (groups of 5-8 query heads)
+// the doubled score, probability and accumulator fragments need more than the
+// 168 registers a third CTA would leave, so two CTAs run with no spills.
 template <int NT>
-__global__ void __launch_bounds__(kThreads, 3) decode_mma_kernel(DecodeArgs a) {
+__global__ void __launch_bounds__(kThreads, NT == 1 ? 3 : 2) decode_mma_kernel(DecodeArgs a) {
   extern __shared__ __align__(128) uint8_t smem_raw[];
   MmaSmem<NT>& S = *reinterpret_cast<MmaSmem<NT>*>(smem_raw);
   constexpr int G = 4 * NT;
@@ -863,11 +866,12 @@ int decode_mma_warps() { return kWarps; }
 
 int decode_mma_max_cluster() { return kMaxClusterSplits; }
 
-// Resident CTAs per SM, from the shared-memory footprint (228 KB per SM, 1 KB
-// reserved per CTA).  Host-only arithmetic: no CUDA call.
+// Resident CTAs per SM: the shared-memory footprint (228 KB per SM, 1 KB
+// reserved per CTA) and the launch bounds of the kernel.  Host-only
+// arithmetic: no CUDA call.
 int decode_mma_ctas_per_sm(int g) {
   const int bytes = g <= 4 ? (int)sizeof(MmaSmem<1>) : (int)sizeof(MmaSmem<2>);
-  return 233472 / (bytes + 1024);
+  return min(233472 / (bytes + 1024), g <= 4 ? 3 : 2);
 }
 
 cudaError_t launch_decode_mma(const DecodeArgs& a, cudaStream_t s) {
