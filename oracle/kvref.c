@@ -64,6 +64,17 @@
  *   [13824,14848)  V per-token {s', z'} fp32 pairs
  *   [14848,15360)  V per-channel c_d fp32
  * Pool = [num_pages][num_kv_heads][15360 bytes].
+ *
+ * Format variant "_m16" (fp16 metadata; SURVEY's 108 B per token-head): the
+ * same codes, the same fp32 arithmetic, and every stored s', z', c_d rounded
+ * once more to fp16 (IEEE binary16, round to nearest even, overflow to
+ * infinity).  Record of 13824 bytes:
+ *   [0,     8192)  K codes (as above)
+ *   [8192,  8704)  K per-token {s', z'} fp16 pairs, token t at 8192 + 4 t
+ *   [8704,  8960)  K per-channel c_d fp16
+ *   [8960, 13056)  V codes (the same permutation)
+ *   [13056,13568)  V per-token {s', z'} fp16 pairs
+ *   [13568,13824)  V per-channel c_d fp16
  */
 #include <math.h>
 #include <stdint.h>
@@ -79,6 +90,28 @@
 #define OFF_VCODES 9728
 #define OFF_VSZ 13824
 #define OFF_VC 14848
+#define REC_BYTES_M16 13824
+
+/* Offsets of the record parts for the two metadata widths. */
+typedef struct {
+    long rec, kcodes, ksz, kc, vcodes, vsz, vc;
+    int msz;   /* bytes of one stored metadata value: 4 (fp32) or 2 (fp16) */
+} rec_layout;
+
+static rec_layout layout_of(int meta16)
+{
+    rec_layout L;
+    if (!meta16) {
+        L.rec = REC_BYTES; L.kcodes = OFF_KCODES; L.ksz = OFF_KSZ; L.kc = OFF_KC;
+        L.vcodes = OFF_VCODES; L.vsz = OFF_VSZ; L.vc = OFF_VC; L.msz = 4;
+    } else {
+        L.rec = REC_BYTES_M16; L.kcodes = 0; L.ksz = 8192; L.kc = 8704;
+        L.vcodes = 8960; L.vsz = 13056; L.vc = 13568; L.msz = 2;
+    }
+    return L;
+}
+
+long kvref_record_bytes(int meta16) { return layout_of(meta16).rec; }
 
 /* ------------------------------------------------------------------ */
 /* fp16 <-> double, written out from the IEEE-754 binary16 definition */
@@ -98,6 +131,35 @@ double kvref_half_to_double(uint16_t h)
         v = ldexp((double)(1024 + mant), expo - 25);
     }
     return sign ? -v : v;
+}
+
+/* float -> binary16, round to nearest even, from the definition: the value
+ * is an integer multiple of the fp16 spacing 2^(e - 10) of its binade (2^-24
+ * for the subnormals); the exact quotient is rounded to the nearest integer,
+ * ties to the even one, and a result of 2^11 spacings carries into the next
+ * binade.  Beyond the largest finite value (65504, or from 65520 on after
+ * rounding) the result is infinity; NaN stays NaN. */
+uint16_t kvref_f32_to_f16(float f)
+{
+    double x = (double)f, a = fabs(x), m, fl;
+    uint16_t sign = signbit(x) ? 0x8000 : 0;
+    int e;
+    if (isnan(x)) return (uint16_t)(sign | 0x7e00);
+    if (a == 0.0) return sign;
+    e = (int)floor(log2(a));
+    if (ldexp(1.0, e) > a) e -= 1;          /* guard the log2 rounding */
+    if (ldexp(1.0, e + 1) <= a) e += 1;
+    if (e < -14) e = -14;                    /* subnormal spacing 2^-24 */
+    m = ldexp(a, 10 - e);                    /* spacings of 2^(e - 10), exact */
+    fl = floor(m);
+    if (m - fl > 0.5 || (m - fl == 0.5 && fmod(fl, 2.0) != 0.0)) fl += 1.0;
+    if (fl >= 2048.0) {                      /* carried into the next binade */
+        fl /= 2.0;
+        e += 1;
+    }
+    if (e > 15) return (uint16_t)(sign | 0x7c00);
+    if (fl < 1024.0) return (uint16_t)(sign | (uint16_t)fl);          /* subnormal */
+    return (uint16_t)(sign | (uint16_t)((e + 15) << 10) | (uint16_t)(fl - 1024.0));
 }
 
 /* ------------------------------------------------------------------ */
@@ -308,64 +370,107 @@ void kvref_v_code_pos(int c, int t, int *byte, int *shift)
     *shift = 2 * (crumb % 4);
 }
 
-/* is_v = 0: K part (4-bit, token-major); is_v = 1: V part (2-bit, permuted). */
-void kvref_pack_part(uint8_t *rec, int is_v, const uint8_t *q, const float *s32,
-                     const float *z32, const float *c32)
+static void put_meta(uint8_t *p, float v, int meta16)
 {
+    if (meta16) {
+        uint16_t h = kvref_f32_to_f16(v);
+        memcpy(p, &h, 2);
+    } else {
+        put_f32(p, v);
+    }
+}
+
+static float get_meta(const uint8_t *p, int meta16)
+{
+    if (meta16) {
+        uint16_t h;
+        memcpy(&h, p, 2);
+        return (float)kvref_half_to_double(h);   /* exact */
+    }
+    return get_f32(p);
+}
+
+/* is_v = 0: K part (4-bit, token-major); is_v = 1: V part (2-bit, permuted).
+ * meta16: the "_m16" record (metadata stored as fp16). */
+void kvref_pack_part_fmt(uint8_t *rec, int is_v, const uint8_t *q, const float *s32,
+                         const float *z32, const float *c32, int meta16)
+{
+    rec_layout L = layout_of(meta16);
+    long sz = is_v ? L.vsz : L.ksz, cc = is_v ? L.vc : L.kc;
     int t, d, j;
     if (!is_v) {
         for (t = 0; t < NTOK; ++t)
             for (j = 0; j < NCH / 2; ++j)
-                rec[OFF_KCODES + t * 64 + j] =
+                rec[L.kcodes + t * 64 + j] =
                     (uint8_t)((q[t * NCH + 2 * j] & 15) | ((q[t * NCH + 2 * j + 1] & 15) << 4));
     } else {
-        memset(rec + OFF_VCODES, 0, NTOK * NCH / 4);
+        memset(rec + L.vcodes, 0, NTOK * NCH / 4);
         for (t = 0; t < NTOK; ++t)
             for (d = 0; d < NCH; ++d) {
                 int byte, shift;
                 kvref_v_code_pos(d, t, &byte, &shift);
-                rec[OFF_VCODES + byte] |= (uint8_t)((q[t * NCH + d] & 3) << shift);
+                rec[L.vcodes + byte] |= (uint8_t)((q[t * NCH + d] & 3) << shift);
             }
     }
     for (t = 0; t < NTOK; ++t) {
-        put_f32(rec + (is_v ? OFF_VSZ : OFF_KSZ) + 8 * t, s32[t]);
-        put_f32(rec + (is_v ? OFF_VSZ : OFF_KSZ) + 8 * t + 4, z32[t]);
+        put_meta(rec + sz + 2 * L.msz * t, s32[t], meta16);
+        put_meta(rec + sz + 2 * L.msz * t + L.msz, z32[t], meta16);
     }
-    for (d = 0; d < NCH; ++d) put_f32(rec + (is_v ? OFF_VC : OFF_KC) + 4 * d, c32[d]);
+    for (d = 0; d < NCH; ++d) put_meta(rec + cc + L.msz * d, c32[d], meta16);
 }
 
-/* Inverse of kvref_pack_part for the codes and metadata. */
-void kvref_unpack_part(const uint8_t *rec, int is_v, uint8_t *q, float *s32, float *z32,
-                       float *c32)
+void kvref_pack_part(uint8_t *rec, int is_v, const uint8_t *q, const float *s32,
+                     const float *z32, const float *c32)
 {
+    kvref_pack_part_fmt(rec, is_v, q, s32, z32, c32, 0);
+}
+
+/* Inverse of kvref_pack_part_fmt for the codes and metadata (fp16 metadata
+ * returned as the floats it represents). */
+void kvref_unpack_part_fmt(const uint8_t *rec, int is_v, uint8_t *q, float *s32, float *z32,
+                           float *c32, int meta16)
+{
+    rec_layout L = layout_of(meta16);
+    long sz = is_v ? L.vsz : L.ksz, cc = is_v ? L.vc : L.kc;
     int t, d;
     for (t = 0; t < NTOK; ++t) {
         for (d = 0; d < NCH; ++d) {
             if (!is_v) {
-                uint8_t byte = rec[OFF_KCODES + t * 64 + d / 2];
+                uint8_t byte = rec[L.kcodes + t * 64 + d / 2];
                 q[t * NCH + d] = (uint8_t)((byte >> (4 * (d % 2))) & 15);
             } else {
                 int byte, shift;
                 kvref_v_code_pos(d, t, &byte, &shift);
-                q[t * NCH + d] = (uint8_t)((rec[OFF_VCODES + byte] >> shift) & 3);
+                q[t * NCH + d] = (uint8_t)((rec[L.vcodes + byte] >> shift) & 3);
             }
         }
-        s32[t] = get_f32(rec + (is_v ? OFF_VSZ : OFF_KSZ) + 8 * t);
-        z32[t] = get_f32(rec + (is_v ? OFF_VSZ : OFF_KSZ) + 8 * t + 4);
+        s32[t] = get_meta(rec + sz + 2 * L.msz * t, meta16);
+        z32[t] = get_meta(rec + sz + 2 * L.msz * t + L.msz, meta16);
     }
-    for (d = 0; d < NCH; ++d) c32[d] = get_f32(rec + (is_v ? OFF_VC : OFF_KC) + 4 * d);
+    for (d = 0; d < NCH; ++d) c32[d] = get_meta(rec + cc + L.msz * d, meta16);
+}
+
+void kvref_unpack_part(const uint8_t *rec, int is_v, uint8_t *q, float *s32, float *z32,
+                       float *c32)
+{
+    kvref_unpack_part_fmt(rec, is_v, q, s32, z32, c32, 0);
 }
 
 /* Dequantized rotated tile yhat_td = c_d (s'_t q_td + z'_t), from a record. */
-void kvref_dequant_part(const uint8_t *rec, int is_v, double *yhat)
+void kvref_dequant_part_fmt(const uint8_t *rec, int is_v, int meta16, double *yhat)
 {
     uint8_t q[NTOK * NCH];
     float s32[NTOK], z32[NTOK], c32[NCH];
     int t, d;
-    kvref_unpack_part(rec, is_v, q, s32, z32, c32);
+    kvref_unpack_part_fmt(rec, is_v, q, s32, z32, c32, meta16);
     for (t = 0; t < NTOK; ++t)
         for (d = 0; d < NCH; ++d)
             yhat[t * NCH + d] = (double)c32[d] * ((double)s32[t] * q[t * NCH + d] + (double)z32[t]);
+}
+
+void kvref_dequant_part(const uint8_t *rec, int is_v, double *yhat)
+{
+    kvref_dequant_part_fmt(rec, is_v, 0, yhat);
 }
 
 /* ------------------------------------------------------------------ */
@@ -376,9 +481,9 @@ void kvref_dequant_part(const uint8_t *rec, int is_v, double *yhat)
  * the K (is_v = 0, 4 bits) or V (is_v = 1, 2 bits) part of `rec`.  The
  * optional outputs expose every intermediate for the tests:
  * Y (rotated), a, b (log scales), q (codes), u (pre-rounding values). */
-void kvref_quantize_tile_stat(const uint16_t *x, long ld_tok, int is_v, int iters, int stat,
-                              uint8_t *rec, double *Y_out, double *a_out, double *b_out,
-                              uint8_t *q_out, double *u_out)
+void kvref_quantize_tile_fmt(const uint16_t *x, long ld_tok, int is_v, int iters, int stat,
+                             int meta16, uint8_t *rec, double *Y_out, double *a_out,
+                             double *b_out, uint8_t *q_out, double *u_out)
 {
     static double H[NCH * NCH];
     static int have_h = 0;
@@ -399,12 +504,20 @@ void kvref_quantize_tile_stat(const uint16_t *x, long ld_tok, int is_v, int iter
     for (t = 0; t < NTOK; ++t) r[t] = exp(a[t]);
     for (d = 0; d < NCH; ++d) c32[d] = (float)exp(b[d]);
     kvref_rtn(Y, r, c32, bits, q, s32, z32, u_out);
-    if (rec) kvref_pack_part(rec, is_v, q, s32, z32, c32);
+    if (rec) kvref_pack_part_fmt(rec, is_v, q, s32, z32, c32, meta16);
     if (Y_out) memcpy(Y_out, Y, sizeof(double) * NTOK * NCH);
     if (a_out) memcpy(a_out, a, sizeof(a));
     if (b_out) memcpy(b_out, b, sizeof(b));
     if (q_out) memcpy(q_out, q, sizeof(q));
     free(Y);
+}
+
+void kvref_quantize_tile_stat(const uint16_t *x, long ld_tok, int is_v, int iters, int stat,
+                              uint8_t *rec, double *Y_out, double *a_out, double *b_out,
+                              uint8_t *q_out, double *u_out)
+{
+    kvref_quantize_tile_fmt(x, ld_tok, is_v, iters, stat, 0, rec, Y_out, a_out, b_out, q_out,
+                            u_out);
 }
 
 void kvref_quantize_tile(const uint16_t *x, long ld_tok, int is_v, int iters, uint8_t *rec,
@@ -424,13 +537,14 @@ void kvref_quantize_tile(const uint16_t *x, long ld_tok, int is_v, int iters, ui
  * tail_k, tail_v: fp16 [B][Hkv][128 slots][128].  u_k, u_v (nullable):
  * pre-rounding values, [B][max_blocks][Hkv][128][128] doubles, for the
  * boundary rule.  Returns 0, or -1 on a page id outside [0, num_pages). */
-int kvref_quantize_blocks_stat(const uint16_t *k, const uint16_t *v, long sb, long st, long sh,
-                               int B, const int32_t *seq_lens, const int32_t *block_table,
-                               int max_blocks, int hkv, int iters, int stat, uint8_t *pool,
-                               long num_pages, uint16_t *tail_k, uint16_t *tail_v, double *u_k,
-                               double *u_v)
+int kvref_quantize_blocks_fmt(const uint16_t *k, const uint16_t *v, long sb, long st, long sh,
+                              int B, const int32_t *seq_lens, const int32_t *block_table,
+                              int max_blocks, int hkv, int iters, int stat, int meta16,
+                              uint8_t *pool, long num_pages, uint16_t *tail_k, uint16_t *tail_v,
+                              double *u_k, double *u_v)
 {
     int bad = 0;
+    const long rec_bytes = layout_of(meta16).rec;
     long item, n_items = (long)B * max_blocks * hkv;
 #pragma omp parallel for schedule(dynamic, 4) reduction(| : bad)
     for (item = 0; item < n_items; ++item) {
@@ -444,11 +558,11 @@ int kvref_quantize_blocks_stat(const uint16_t *k, const uint16_t *v, long sb, lo
         if (j >= nfull) continue;
         page = block_table[(long)b * max_blocks + j];
         if (page < 0 || page >= num_pages) { bad = 1; continue; }
-        rec = pool + (page * hkv + h) * (long)REC_BYTES;
-        kvref_quantize_tile_stat(k + b * sb + (long)j * NTOK * st + h * sh, st, 0, iters, stat,
-                                 rec, NULL, NULL, NULL, NULL, u_k ? u_k + uoff : NULL);
-        kvref_quantize_tile_stat(v + b * sb + (long)j * NTOK * st + h * sh, st, 1, iters, stat,
-                                 rec, NULL, NULL, NULL, NULL, u_v ? u_v + uoff : NULL);
+        rec = pool + (page * hkv + h) * rec_bytes;
+        kvref_quantize_tile_fmt(k + b * sb + (long)j * NTOK * st + h * sh, st, 0, iters, stat,
+                                meta16, rec, NULL, NULL, NULL, NULL, u_k ? u_k + uoff : NULL);
+        kvref_quantize_tile_fmt(v + b * sb + (long)j * NTOK * st + h * sh, st, 1, iters, stat,
+                                meta16, rec, NULL, NULL, NULL, NULL, u_v ? u_v + uoff : NULL);
     }
     {
         int b, h, s, d;
@@ -468,6 +582,17 @@ int kvref_quantize_blocks_stat(const uint16_t *k, const uint16_t *v, long sb, lo
     return bad ? -1 : 0;
 }
 
+int kvref_quantize_blocks_stat(const uint16_t *k, const uint16_t *v, long sb, long st, long sh,
+                               int B, const int32_t *seq_lens, const int32_t *block_table,
+                               int max_blocks, int hkv, int iters, int stat, uint8_t *pool,
+                               long num_pages, uint16_t *tail_k, uint16_t *tail_v, double *u_k,
+                               double *u_v)
+{
+    return kvref_quantize_blocks_fmt(k, v, sb, st, sh, B, seq_lens, block_table, max_blocks,
+                                     hkv, iters, stat, 0, pool, num_pages, tail_k, tail_v, u_k,
+                                     u_v);
+}
+
 int kvref_quantize_blocks(const uint16_t *k, const uint16_t *v, long sb, long st, long sh,
                           int B, const int32_t *seq_lens, const int32_t *block_table,
                           int max_blocks, int hkv, int iters, uint8_t *pool, long num_pages,
@@ -480,12 +605,13 @@ int kvref_quantize_blocks(const uint16_t *k, const uint16_t *v, long sb, long st
 /* Decode-time append: token `pos[b]` (the length before the append) goes to
  * tail slot pos mod 128; when that slot is 127 the now-full tail is quantized
  * into page block_table[b][pos / 128].  pos < 0 marks an idle slot. */
-int kvref_append_token_stat(const uint16_t *k_new, const uint16_t *v_new, const int32_t *pos,
-                            int B, const int32_t *block_table, int max_blocks, int hkv,
-                            int iters, int stat, uint8_t *pool, long num_pages,
-                            uint16_t *tail_k, uint16_t *tail_v)
+int kvref_append_token_fmt(const uint16_t *k_new, const uint16_t *v_new, const int32_t *pos,
+                           int B, const int32_t *block_table, int max_blocks, int hkv,
+                           int iters, int stat, int meta16, uint8_t *pool, long num_pages,
+                           uint16_t *tail_k, uint16_t *tail_v)
 {
     int b, bad = 0;
+    const long rec_bytes = layout_of(meta16).rec;
     for (b = 0; b < B; ++b) {
         int p = pos[b], h, d, slot;
         if (p < 0) continue;
@@ -504,15 +630,26 @@ int kvref_append_token_stat(const uint16_t *k_new, const uint16_t *v_new, const 
             page = block_table[(long)b * max_blocks + p / NTOK];
             if (page < 0 || page >= num_pages) { bad = 1; continue; }
             for (h = 0; h < hkv; ++h) {
-                uint8_t *rec = pool + (page * hkv + h) * (long)REC_BYTES;
+                uint8_t *rec = pool + (page * hkv + h) * rec_bytes;
                 const uint16_t *tk = tail_k + ((long)b * hkv + h) * NTOK * NCH;
                 const uint16_t *tv = tail_v + ((long)b * hkv + h) * NTOK * NCH;
-                kvref_quantize_tile_stat(tk, NCH, 0, iters, stat, rec, NULL, NULL, NULL, NULL, NULL);
-                kvref_quantize_tile_stat(tv, NCH, 1, iters, stat, rec, NULL, NULL, NULL, NULL, NULL);
+                kvref_quantize_tile_fmt(tk, NCH, 0, iters, stat, meta16, rec, NULL, NULL, NULL,
+                                        NULL, NULL);
+                kvref_quantize_tile_fmt(tv, NCH, 1, iters, stat, meta16, rec, NULL, NULL, NULL,
+                                        NULL, NULL);
             }
         }
     }
     return bad ? -1 : 0;
+}
+
+int kvref_append_token_stat(const uint16_t *k_new, const uint16_t *v_new, const int32_t *pos,
+                            int B, const int32_t *block_table, int max_blocks, int hkv,
+                            int iters, int stat, uint8_t *pool, long num_pages,
+                            uint16_t *tail_k, uint16_t *tail_v)
+{
+    return kvref_append_token_fmt(k_new, v_new, pos, B, block_table, max_blocks, hkv, iters,
+                                  stat, 0, pool, num_pages, tail_k, tail_v);
 }
 
 int kvref_append_token(const uint16_t *k_new, const uint16_t *v_new, const int32_t *pos, int B,
@@ -536,11 +673,13 @@ int kvref_append_token(const uint16_t *k_new, const uint16_t *v_new, const int32
  *   accumulated in rotated space and rotated back once: o = H o_rot + o_tail.
  * q: fp16 [B][Hq][128].  out: double [B][Hq][128].  A sequence of length 0
  * yields a zero output.  Returns -1 on a page id outside [0, num_pages). */
-int kvref_decode_attention(const uint16_t *q, const uint8_t *pool, long num_pages,
-                           const int32_t *block_table, int max_blocks, const int32_t *seq_lens,
-                           int B, int hq, int hkv, const uint16_t *tail_k, const uint16_t *tail_v,
-                           double scale, int route, double *out)
+int kvref_decode_attention_fmt(const uint16_t *q, const uint8_t *pool, long num_pages,
+                               const int32_t *block_table, int max_blocks,
+                               const int32_t *seq_lens, int B, int hq, int hkv,
+                               const uint16_t *tail_k, const uint16_t *tail_v, double scale,
+                               int route, int meta16, double *out)
 {
+    const long rec_bytes = layout_of(meta16).rec;
     static double H[NCH * NCH];
     static int have_h = 0;
     int bad = 0;
@@ -573,7 +712,7 @@ int kvref_decode_attention(const uint16_t *q, const uint8_t *pool, long num_page
         for (j = 0; j < nfull; ++j) {
             long page = block_table[(long)b * max_blocks + j];
             if (page < 0 || page >= num_pages) { pagebad = 1; break; }
-            kvref_dequant_part(pool + (page * hkv + kvh) * (long)REC_BYTES, 0, yk);
+            kvref_dequant_part_fmt(pool + (page * hkv + kvh) * rec_bytes, 0, meta16, yk);
             for (t = 0; t < NTOK; ++t) {
                 double s = 0.0;
                 if (route == 0) {
@@ -607,7 +746,7 @@ int kvref_decode_attention(const uint16_t *q, const uint8_t *pool, long num_page
         for (d = 0; d < NCH; ++d) { acc[d] = 0.0; acc_tail[d] = 0.0; }
         for (j = 0; j < nfull; ++j) {
             long page = block_table[(long)b * max_blocks + j];
-            kvref_dequant_part(pool + (page * hkv + kvh) * (long)REC_BYTES, 1, yv);
+            kvref_dequant_part_fmt(pool + (page * hkv + kvh) * rec_bytes, 1, meta16, yv);
             for (t = 0; t < NTOK; ++t) {
                 double p = scores[j * NTOK + t];
                 if (route == 0) {
@@ -641,6 +780,15 @@ int kvref_decode_attention(const uint16_t *q, const uint8_t *pool, long num_page
         free(scores); free(yk); free(yv);
     }
     return bad ? -1 : 0;
+}
+
+int kvref_decode_attention(const uint16_t *q, const uint8_t *pool, long num_pages,
+                           const int32_t *block_table, int max_blocks, const int32_t *seq_lens,
+                           int B, int hq, int hkv, const uint16_t *tail_k, const uint16_t *tail_v,
+                           double scale, int route, double *out)
+{
+    return kvref_decode_attention_fmt(q, pool, num_pages, block_table, max_blocks, seq_lens, B,
+                                      hq, hkv, tail_k, tail_v, scale, route, 0, out);
 }
 
 /* ------------------------------------------------------------------ */

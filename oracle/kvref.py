@@ -25,6 +25,11 @@ SRC_PATH = os.path.join(HERE, "kvref.c")
 NCH = 128
 NTOK = 128
 REC_BYTES = 15360
+REC_BYTES_M16 = 13824      # format variant "_m16": metadata stored as fp16
+
+
+def rec_bytes(meta16: bool = False) -> int:
+    return REC_BYTES_M16 if meta16 else REC_BYTES
 
 _lib = None
 
@@ -53,6 +58,25 @@ def lib():
         L.kvref_sinkhorn_stat.argtypes = [P, ctypes.c_int, ctypes.c_int, P, P, P]
         L.kvref_rtn.argtypes = [P, P, P, ctypes.c_int, P, P, P, P]
         L.kvref_pack_part.argtypes = [P, ctypes.c_int, P, P, P, P]
+        L.kvref_pack_part_fmt.argtypes = [P, ctypes.c_int, P, P, P, P, ctypes.c_int]
+        L.kvref_unpack_part_fmt.argtypes = [P, ctypes.c_int, P, P, P, P, ctypes.c_int]
+        L.kvref_dequant_part_fmt.argtypes = [P, ctypes.c_int, ctypes.c_int, P]
+        L.kvref_f32_to_f16.argtypes = [ctypes.c_float]
+        L.kvref_f32_to_f16.restype = ctypes.c_uint16
+        L.kvref_record_bytes.argtypes = [ctypes.c_int]
+        L.kvref_record_bytes.restype = ctypes.c_long
+        L.kvref_quantize_tile_fmt.argtypes = [P, ctypes.c_long, ctypes.c_int, ctypes.c_int,
+                                              ctypes.c_int, ctypes.c_int, P, P, P, P, P, P]
+        L.kvref_quantize_blocks_fmt.argtypes = [P, P, ctypes.c_long, ctypes.c_long, ctypes.c_long,
+                                                ctypes.c_int, P, P, ctypes.c_int, ctypes.c_int,
+                                                ctypes.c_int, ctypes.c_int, ctypes.c_int, P,
+                                                ctypes.c_long, P, P, P, P]
+        L.kvref_append_token_fmt.argtypes = [P, P, P, ctypes.c_int, P, ctypes.c_int, ctypes.c_int,
+                                             ctypes.c_int, ctypes.c_int, ctypes.c_int, P,
+                                             ctypes.c_long, P, P]
+        L.kvref_decode_attention_fmt.argtypes = [P, P, ctypes.c_long, P, ctypes.c_int, P,
+                                                 ctypes.c_int, ctypes.c_int, ctypes.c_int, P, P,
+                                                 ctypes.c_double, ctypes.c_int, ctypes.c_int, P]
         L.kvref_unpack_part.argtypes = [P, ctypes.c_int, P, P, P, P]
         L.kvref_dequant_part.argtypes = [P, ctypes.c_int, P]
         L.kvref_quantize_tile.argtypes = [P, ctypes.c_long, ctypes.c_int, ctypes.c_int, P, P, P,
@@ -150,47 +174,55 @@ def rtn(Y, r, c32, bits: int):
     return q, s, z, u
 
 
-def pack_part(rec, is_v: bool, q, s32, z32, c32):
-    lib().kvref_pack_part(_p(rec), int(is_v), _p(_c(q, np.uint8)), _p(_c(s32, np.float32)),
-                          _p(_c(z32, np.float32)), _p(_c(c32, np.float32)))
+def f32_to_f16(x: float) -> int:
+    """binary16 bits of the float32 value x, round to nearest even."""
+    return int(lib().kvref_f32_to_f16(float(np.float32(x))))
 
 
-def unpack_part(rec, is_v: bool):
+def pack_part(rec, is_v: bool, q, s32, z32, c32, meta16: bool = False):
+    lib().kvref_pack_part_fmt(_p(rec), int(is_v), _p(_c(q, np.uint8)), _p(_c(s32, np.float32)),
+                              _p(_c(z32, np.float32)), _p(_c(c32, np.float32)), int(meta16))
+
+
+def unpack_part(rec, is_v: bool, meta16: bool = False):
     q = np.zeros((NTOK, NCH), dtype=np.uint8)
     s = np.zeros(NTOK, dtype=np.float32)
     z = np.zeros(NTOK, dtype=np.float32)
     c = np.zeros(NCH, dtype=np.float32)
-    lib().kvref_unpack_part(_p(_c(rec, np.uint8)), int(is_v), _p(q), _p(s), _p(z), _p(c))
+    lib().kvref_unpack_part_fmt(_p(_c(rec, np.uint8)), int(is_v), _p(q), _p(s), _p(z), _p(c),
+                                int(meta16))
     return q, s, z, c
 
 
-def dequant_part(rec, is_v: bool) -> np.ndarray:
+def dequant_part(rec, is_v: bool, meta16: bool = False) -> np.ndarray:
     y = np.zeros((NTOK, NCH), dtype=np.float64)
-    lib().kvref_dequant_part(_p(_c(rec, np.uint8)), int(is_v), _p(y))
+    lib().kvref_dequant_part_fmt(_p(_c(rec, np.uint8)), int(is_v), int(meta16), _p(y))
     return y
 
 
-def quantize_tile(x, is_v: bool, iters: int, rms: bool = False):
+def quantize_tile(x, is_v: bool, iters: int, rms: bool = False, meta16: bool = False):
     """All four stages on one tile; returns a dict of every intermediate."""
     xb = _bits16(x).reshape(NTOK, NCH)
-    rec = np.zeros(REC_BYTES, dtype=np.uint8)
+    rec = np.zeros(rec_bytes(meta16), dtype=np.uint8)
     Y = np.zeros((NTOK, NCH))
     a = np.zeros(NTOK)
     b = np.zeros(NCH)
     q = np.zeros((NTOK, NCH), dtype=np.uint8)
     u = np.zeros((NTOK, NCH))
-    lib().kvref_quantize_tile_stat(_p(xb), NCH, int(is_v), iters, int(rms), _p(rec), _p(Y),
-                                   _p(a), _p(b), _p(q), _p(u))
+    lib().kvref_quantize_tile_fmt(_p(xb), NCH, int(is_v), iters, int(rms), int(meta16), _p(rec),
+                                  _p(Y), _p(a), _p(b), _p(q), _p(u))
     return {"rec": rec, "Y": Y, "a": a, "b": b, "q": q, "u": u}
 
 
 # ------------------------------------------------------------ whole ops --
 
 def quantize_blocks(k, v, seq_lens, block_table, num_pages: int, iters: int, pool=None,
-                    tail_k=None, tail_v=None, want_u: bool = False, rms: bool = False):
+                    tail_k=None, tail_v=None, want_u: bool = False, rms: bool = False,
+                    meta16: bool = False):
     """Prefill: k, v fp16 [B][S][Hkv][128] (contiguous).  Returns a dict with
-    the pool [num_pages][Hkv][15360] uint8, the fp16 tails [B][Hkv][128][128]
-    and, with want_u, the pre-rounding values [B][max_blocks][Hkv][128][128]."""
+    the pool [num_pages][Hkv][15360] uint8 ([..][13824] with meta16), the fp16
+    tails [B][Hkv][128][128] and, with want_u, the pre-rounding values
+    [B][max_blocks][Hkv][128][128]."""
     kb = _bits16(k)
     vb = _bits16(v)
     B, S, hkv, d = kb.shape
@@ -199,7 +231,7 @@ def quantize_blocks(k, v, seq_lens, block_table, num_pages: int, iters: int, poo
     block_table = _c(block_table, np.int32)
     max_blocks = block_table.shape[1]
     if pool is None:
-        pool = np.zeros((num_pages, hkv, REC_BYTES), dtype=np.uint8)
+        pool = np.zeros((num_pages, hkv, rec_bytes(meta16)), dtype=np.uint8)
     if tail_k is None:
         tail_k = np.zeros((B, hkv, NTOK, NCH), dtype=np.uint16)
     if tail_v is None:
@@ -208,15 +240,16 @@ def quantize_blocks(k, v, seq_lens, block_table, num_pages: int, iters: int, poo
     if want_u:
         u_k = np.zeros((B, max_blocks, hkv, NTOK, NCH))
         u_v = np.zeros((B, max_blocks, hkv, NTOK, NCH))
-    rc = lib().kvref_quantize_blocks_stat(_p(kb), _p(vb), S * hkv * NCH, hkv * NCH, NCH, B,
-                                          _p(seq_lens), _p(block_table), max_blocks, hkv, iters,
-                                          int(rms), _p(pool), num_pages, _p(tail_k), _p(tail_v),
-                                          _p(u_k), _p(u_v))
+    assert pool.shape[-1] == rec_bytes(meta16)
+    rc = lib().kvref_quantize_blocks_fmt(_p(kb), _p(vb), S * hkv * NCH, hkv * NCH, NCH, B,
+                                         _p(seq_lens), _p(block_table), max_blocks, hkv, iters,
+                                         int(rms), int(meta16), _p(pool), num_pages, _p(tail_k),
+                                         _p(tail_v), _p(u_k), _p(u_v))
     return {"rc": rc, "pool": pool, "tail_k": tail_k, "tail_v": tail_v, "u_k": u_k, "u_v": u_v}
 
 
 def append_token(k_new, v_new, pos, block_table, iters: int, pool, tail_k, tail_v,
-                 rms: bool = False):
+                 rms: bool = False, meta16: bool = False):
     """Decode-time append (in place on pool / tails).  Returns the status."""
     kb = _bits16(k_new)
     vb = _bits16(v_new)
@@ -224,13 +257,14 @@ def append_token(k_new, v_new, pos, block_table, iters: int, pool, tail_k, tail_
     pos = _c(pos, np.int32)
     block_table = _c(block_table, np.int32)
     assert pool.flags["C_CONTIGUOUS"] and tail_k.flags["C_CONTIGUOUS"]
-    return lib().kvref_append_token_stat(_p(kb), _p(vb), _p(pos), B, _p(block_table),
-                                         block_table.shape[1], hkv, iters, int(rms), _p(pool),
-                                         pool.shape[0], _p(tail_k), _p(tail_v))
+    assert pool.shape[-1] == rec_bytes(meta16)
+    return lib().kvref_append_token_fmt(_p(kb), _p(vb), _p(pos), B, _p(block_table),
+                                        block_table.shape[1], hkv, iters, int(rms), int(meta16),
+                                        _p(pool), pool.shape[0], _p(tail_k), _p(tail_v))
 
 
 def decode_attention(q, pool, block_table, seq_lens, tail_k, tail_v, hq: int, hkv: int,
-                     scale: float = 1.0 / np.sqrt(128.0), route: int = 1):
+                     scale: float = 1.0 / np.sqrt(128.0), route: int = 1, meta16: bool = False):
     """Decode attention, float64 output [B][Hq][128].  route 0 = textbook
     (un-rotate every token), route 1 = rotated space with one final H."""
     qb = _bits16(q)
@@ -239,10 +273,11 @@ def decode_attention(q, pool, block_table, seq_lens, tail_k, tail_v, hq: int, hk
     block_table = _c(block_table, np.int32)
     seq_lens = _c(seq_lens, np.int32)
     out = np.zeros((B, hq, NCH))
-    rc = lib().kvref_decode_attention(_p(qb), _p(pool), pool.shape[0], _p(block_table),
-                                      block_table.shape[1], _p(seq_lens), B, hq, hkv,
-                                      _p(_bits16(tail_k)), _p(_bits16(tail_v)), float(scale),
-                                      int(route), _p(out))
+    assert pool.shape[-1] == rec_bytes(meta16)
+    rc = lib().kvref_decode_attention_fmt(_p(qb), _p(pool), pool.shape[0], _p(block_table),
+                                          block_table.shape[1], _p(seq_lens), B, hq, hkv,
+                                          _p(_bits16(tail_k)), _p(_bits16(tail_v)), float(scale),
+                                          int(route), int(meta16), _p(out))
     if rc != 0:
         raise ValueError("oracle: page id outside the pool")
     return out
@@ -283,7 +318,7 @@ def attention_fp16(q, k, v, seq_lens, hq: int, hkv: int,
 
 
 def chunk_attention(q, start, chunk_lens, pool, block_table, tail_k, tail_v, hq: int, hkv: int,
-                    scale: float = 1.0 / np.sqrt(128.0)) -> np.ndarray:
+                    scale: float = 1.0 / np.sqrt(128.0), meta16: bool = False) -> np.ndarray:
     """Attention of a chunk of new query tokens over the quantized cache
     (chunked prefill), float64 output [B][M][Hq][128].
 
@@ -325,8 +360,8 @@ def chunk_attention(q, start, chunk_lens, pool, block_table, tail_k, tail_v, hq:
             if page < 0 or page >= pool.shape[0]:
                 raise ValueError("oracle: page id outside the pool")
             for h in range(hkv):
-                K[h, j * NTOK:(j + 1) * NTOK] = dequant_part(pool[page, h], False) @ H
-                V[h, j * NTOK:(j + 1) * NTOK] = dequant_part(pool[page, h], True) @ H
+                K[h, j * NTOK:(j + 1) * NTOK] = dequant_part(pool[page, h], False, meta16) @ H
+                V[h, j * NTOK:(j + 1) * NTOK] = dequant_part(pool[page, h], True, meta16) @ H
         r = n - nfull * NTOK
         K[:, nfull * NTOK:] = tk[b, :, :r]
         V[:, nfull * NTOK:] = tv[b, :, :r]

@@ -870,3 +870,121 @@ def test_snapkv_keeps_the_cluster_around_a_planted_key(oracle):
     assert votes[0, 0].argmax() == 100
     idx = oracle.snapkv_select(votes, np.array([300]), window=16, capacity=40, kernel=7)
     assert set(range(97, 104)) <= set(idx[0, 0].tolist())
+
+
+# ------------------------------------------- format variant: fp16 metadata --
+# Format variant "_m16" (the metadata of the KVarN record stored as fp16,
+# 108 B per token-head instead of 120): the KVarN page (blog.edumints.com),
+# "KVarN Nasil Calisir?", stage "Kuantize Edilmis Onbellek", fixes the codes;
+# the metadata width is a reading.  Pinned against numpy's own float16
+# rounding, the fp32 record, and attention on the dequantized cache.
+
+def test_f32_to_f16_matches_numpy_rounding(oracle):
+    rng = np.random.default_rng(41)
+    vals = np.concatenate([
+        rng.standard_normal(3000) * np.exp(rng.uniform(-20, 12, 3000)),   # every binade
+        rng.uniform(-1e-7, 1e-7, 500),                                     # subnormals
+        np.array([0.0, -0.0, 1.0, -2.0, 65504.0, 65519.99, 65520.0, 1e6, -1e6, 2.0 ** -24,
+                  2.0 ** -25, 1.5 * 2.0 ** -25, 2.0 ** -14 - 2.0 ** -25, 6.1e-5]),
+    ]).astype(np.float32)
+    # exact ties between two fp16 neighbours, both parities
+    base = rng.integers(0x0400, 0x7BFF, 400).astype(np.uint16).view(np.float16).astype(np.float64)
+    ulp = np.spacing(base.astype(np.float16)).astype(np.float64)
+    ties = (base + 0.5 * ulp).astype(np.float32)
+    with np.errstate(over="ignore"):
+        for x in np.concatenate([vals, ties]):
+            want = int(np.array([x], np.float32).astype(np.float16).view(np.uint16)[0])
+            assert oracle.f32_to_f16(x) == want, (x, hex(want))
+
+
+def test_m16_record_is_the_fp32_record_with_fp16_metadata(oracle):
+    x = _tile(42)
+    for is_v in (False, True):
+        a = oracle.quantize_tile(x, is_v, 2)
+        b = oracle.quantize_tile(x, is_v, 2, meta16=True)
+        assert b["rec"].size == oracle.REC_BYTES_M16 == 108 * 128
+        q32, s32, z32, c32 = oracle.unpack_part(a["rec"], is_v)
+        q16, s16, z16, c16 = oracle.unpack_part(b["rec"], is_v, meta16=True)
+        assert np.array_equal(q32, q16)                      # the same codes
+        for m32, m16 in ((s32, s16), (z32, z16), (c32, c16)):
+            assert np.array_equal(m32.astype(np.float16).astype(np.float32), m16)
+        # the raw bytes at the stated offsets: codes, {s', z'} pairs, c
+        rec = b["rec"]
+        if not is_v:
+            assert np.array_equal(rec[:8192], a["rec"][:8192])
+            sz = rec[8192:8704].view(np.float16).reshape(128, 2)
+            cc = rec[8704:8960].view(np.float16)
+        else:
+            assert np.array_equal(rec[8960:13056], a["rec"][9728:13824])
+            sz = rec[13056:13568].view(np.float16).reshape(128, 2)
+            cc = rec[13568:13824].view(np.float16)
+        assert np.array_equal(sz[:, 0], s32.astype(np.float16))
+        assert np.array_equal(sz[:, 1], z32.astype(np.float16))
+        assert np.array_equal(cc, c32.astype(np.float16))
+
+
+def test_m16_dequant_within_fp16_rounding_of_the_fp32_record(oracle):
+    x = _tile(43)
+    for is_v in (False, True):
+        a = oracle.quantize_tile(x, is_v, 2)
+        b = oracle.quantize_tile(x, is_v, 2, meta16=True)
+        y32 = oracle.dequant_part(a["rec"], is_v)
+        y16 = oracle.dequant_part(b["rec"], is_v, meta16=True)
+        q, s, z, c = oracle.unpack_part(a["rec"], is_v)
+        s, z, c = (np.abs(t.astype(np.float64)) for t in (s, z, c))
+        # each of c, s', z' moves by at most half an fp16 ulp (2^-11 relative)
+        u = 2.0 ** -11
+        bound = c[None, :] * (s[:, None] * q + z[:, None]) * (2 * u + u * u) + 1e-12
+        assert np.all(np.abs(y16 - y32) <= bound)
+        assert np.abs(y16 - y32).max() > 0                   # the rounding is really there
+
+
+def test_m16_attention_matches_torch_softmax_on_dequantized_cache(oracle):
+    w = synth.scaled(synth.WORKLOADS["llama3_8b_layer"], batch=2, seq=517, hkv=2, hq=4, seed=44)
+    k, v = synth.kv(w)
+    k, v = k.numpy(), v.numpy()
+    lens = np.array([300, 517], np.int32)
+    table = np.array([[5, 1, 3, 7, 0], [2, 6, 4, 8, 9]], np.int32)
+    st = oracle.quantize_blocks(k, v, lens, table, 10, 2, meta16=True)
+    assert st["pool"].shape == (10, 2, 13824) and st["rc"] == 0
+    q = synth.queries(w).numpy()
+    o1 = oracle.decode_attention(q, st["pool"], table, lens, st["tail_k"], st["tail_v"], 4, 2,
+                                 meta16=True)
+    o0 = oracle.decode_attention(q, st["pool"], table, lens, st["tail_k"], st["tail_v"], 4, 2,
+                                 route=0, meta16=True)
+    assert np.abs(o0 - o1).max() <= 1e-12 * np.abs(o0).max()
+    H = torch.tensor(oracle.hadamard(128))
+    for b in range(2):
+        n = int(lens[b])
+        nfull = n // 128
+        for h in range(4):
+            keys, vals = [], []
+            for j in range(nfull):
+                rec = st["pool"][table[b, j], h // 2]
+                keys.append(torch.tensor(oracle.dequant_part(rec, False, True)) @ H)
+                vals.append(torch.tensor(oracle.dequant_part(rec, True, True)) @ H)
+            keys.append(torch.tensor(k[b, nfull * 128:n, h // 2].astype(np.float64)))
+            vals.append(torch.tensor(v[b, nfull * 128:n, h // 2].astype(np.float64)))
+            ref = torch.nn.functional.scaled_dot_product_attention(
+                torch.tensor(q[b, h].astype(np.float64))[None, None, None],
+                torch.cat(keys)[None, None], torch.cat(vals)[None, None])[0, 0, 0].numpy()
+            assert np.abs(o1[b, h] - ref).max() <= 1e-12 * max(1.0, np.abs(ref).max())
+    # and the fp32-metadata cache of the same tokens gives nearly the same output
+    st32 = oracle.quantize_blocks(k, v, lens, table, 10, 2)
+    o32 = oracle.decode_attention(q, st32["pool"], table, lens, st32["tail_k"], st32["tail_v"],
+                                  4, 2)
+    assert np.abs(o32 - o1).max() <= 1e-2 * np.abs(o32).max()
+
+
+def test_m16_append_fills_page_like_prefill(oracle):
+    w = synth.scaled(synth.WORKLOADS["llama3_8b_layer"], batch=1, seq=256, hkv=2, hq=4, seed=45)
+    k, v = synth.kv(w)
+    k, v = k.numpy(), v.numpy()
+    table = np.array([[1, 0]], np.int32)
+    ref = oracle.quantize_blocks(k, v, np.array([256], np.int32), table, 2, 2, meta16=True)
+    st = oracle.quantize_blocks(k, v, np.array([250], np.int32), table, 2, 2, meta16=True)
+    for t in range(250, 256):
+        rc = oracle.append_token(k[:, t], v[:, t], np.array([t], np.int32), table, 2, st["pool"],
+                                 st["tail_k"], st["tail_v"], meta16=True)
+        assert rc == 0
+    assert np.array_equal(st["pool"], ref["pool"])
