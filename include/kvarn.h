@@ -41,7 +41,18 @@
  *                 fetch each tensor-core fragment with one 16-byte load)
  *   [13824,14848) V {s', z'} fp32 per token
  *   [14848,15360) V column scale c_d fp32
- * Pool = [num_pages][num_kv_heads][KVARN_PAGE_BYTES].  The newest len mod 128
+ * Format variant "_m16" (config meta_fp16 = 1; 108 bytes per token-head
+ * instead of 120): the same codes and the same fp32 arithmetic, with every
+ * stored s', z', c_d rounded once more to fp16 (round to nearest even; a
+ * value beyond fp16's range becomes infinity, so inputs whose scales exceed
+ * it need the fp32 format).  Record of KVARN_PAGE_BYTES_M16 bytes:
+ *   [0,     8192) K codes (as above)
+ *   [8192,  8704) K {s', z'} fp16 per token (token t at 8192 + 4 t)
+ *   [8704,  8960) K column scale c_d fp16
+ *   [8960, 13056) V codes (the same permutation)
+ *   [13056,13568) V {s', z'} fp16 per token
+ *   [13568,13824) V column scale c_d fp16
+ * Pool = [num_pages][num_kv_heads][kvarn_page_bytes(cfg)].  The newest len mod 128
  * tokens of a sequence stay fp16 in a caller-owned tail buffer
  * [B][num_kv_heads][128 slots][128] per K and V.
  *
@@ -78,6 +89,7 @@ typedef struct CUstream_st *kvarn_stream_t; /* identical to cudaStream_t */
 #define KVARN_HEAD_DIM 128
 #define KVARN_BLOCK_TOKENS 128
 #define KVARN_PAGE_BYTES 15360
+#define KVARN_PAGE_BYTES_M16 13824
 
 /* return codes */
 #define KVARN_OK 0
@@ -104,19 +116,25 @@ typedef struct {
                            the uncentred root mean square (Sinkhorn-Knopp on
                            the squares; only all-zero rows/columns skipped).
                            The page record is the same either way. */
+    int meta_fp16;      /* 0: fp32 metadata (default); 1: format variant "_m16",
+                           metadata stored as fp16 (KVARN_PAGE_BYTES_M16) */
 } kvarn_config_t;
 
 /* Fills *out from a format string: "k4v2_g128" or "kvarn_k4v2_g128" (the
- * KVarN page's --kv-cache-dtype value), optionally followed by "_rms" (the
- * uncentred statistic) and then "_s<K>" to set the Sinkhorn iteration count.  Returns KVARN_ERR_UNSUPPORTED for any other
- * format, KVARN_ERR_INVALID_ARG for bad head counts or a null pointer. */
+ * KVarN page's --kv-cache-dtype value), optionally followed by the variant
+ * suffixes "_rms" (the uncentred statistic) and "_m16" (fp16 metadata), each
+ * at most once and in either order, and then "_s<K>" to set the Sinkhorn
+ * iteration count.  Returns KVARN_ERR_UNSUPPORTED for any other format,
+ * KVARN_ERR_INVALID_ARG for bad head counts or a null pointer. */
 int kvarn_config_from_string(const char *s, int num_q_heads, int num_kv_heads,
                              kvarn_config_t *out);
 
 /* KVARN_OK if the configuration is one this library runs. */
 int kvarn_config_validate(const kvarn_config_t *cfg);
 
-/* Bytes of one page record (per page and KV head): 15360. 0 on a bad config. */
+/* Bytes of one page record (per page and KV head): KVARN_PAGE_BYTES (15360),
+ * or KVARN_PAGE_BYTES_M16 (13824) for the "_m16" format; 0 on a bad config.
+ * Every call that takes a pool reads it with this record size. */
 size_t kvarn_page_bytes(const kvarn_config_t *cfg);
 
 /* Prefill quantization ("KVarN Nasil Calisir?", all four stages).
@@ -313,7 +331,8 @@ int kvarn_snapkv_gather(const void *k, const void *v, int64_t stride_b, int64_t 
                         const int32_t *indices, int capacity, void *k_out, void *v_out,
                         kvarn_stream_t stream);
 
-/* Diagnosis: dequantizes `n` page records into float32 rotated-space tiles.
+/* Diagnosis: dequantizes `n` page records of the fp32-metadata format into
+ * float32 rotated-space tiles.
  *   records   [n][15360] bytes (e.g. pool + page*Hkv*15360, one record per
  *             (page, head) in order)
  *   yk, yv    float32 [n][128 tokens][128 channels]:

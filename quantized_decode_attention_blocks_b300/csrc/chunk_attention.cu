@@ -152,11 +152,13 @@ __device__ __forceinline__ float code_f(uint32_t q) {   // small integer -> floa
 // row), t0 = lane >> 4; dequant warp dw takes the token pairs p = dw, dw + 3,
 // ... of 64, token 2p + t0.  The code loads hit 32 banks, the column scales
 // of the lane's chunk are loaded once.  rk: the record's K part.
+template <bool M16>
 __device__ __forceinline__ void dequant_k(const uint8_t* rk, uint8_t* kh, uint8_t* kl, int dw,
                                           int lane) {
+  using F = RecFmt<M16>;
   const int cc = lane & 15, t0 = lane >> 4;
-  const float4 ca = reinterpret_cast<const float4*>(rk + kOffKC)[2 * cc];
-  const float4 cb = reinterpret_cast<const float4*>(rk + kOffKC)[2 * cc + 1];
+  const float4 ca = F::get_c4(rk + F::kc, 2 * cc);
+  const float4 cb = F::get_c4(rk + F::kc, 2 * cc + 1);
   const float cs[8] = {ca.x, ca.y, ca.z, ca.w, cb.x, cb.y, cb.z, cb.w};
   // four token pairs per step: independent loads and math in flight
   constexpr int kStep = 4 * kDeqWarps;
@@ -168,7 +170,7 @@ __device__ __forceinline__ void dequant_k(const uint8_t* rk, uint8_t* kh, uint8_
     for (int u = 0; u < 4; ++u) {
       const int t = 2 * min(p0 + kDeqWarps * u, kT / 2 - 1) + t0;
       w[u] = *reinterpret_cast<const uint32_t*>(rk + kOffKCodes + 64 * t + 4 * cc);
-      sz[u] = *reinterpret_cast<const float2*>(rk + kOffKSZ + 8 * t);
+      sz[u] = F::get_sz(rk + F::ksz, t);
     }
 #pragma unroll
     for (int u = 0; u < 4; ++u) {
@@ -196,13 +198,14 @@ __device__ __forceinline__ void dequant_k(const uint8_t* rk, uint8_t* kh, uint8_
 // 128m + 16r + 4j + 2e + h of the permuted V code layout: channel
 // c = 16m + 8e + r, tokens 16k + 8f + 2j + s for k = 4h .. 4h + 3.  The lanes
 // of one store differ in (r, j), i.e. in 32 banks.
-template <int NW>
+template <int NW, bool M16>
 __device__ __forceinline__ void dequant_v(const uint8_t* rv, uint8_t* vh, uint8_t* vl, int dw,
                                           int lane) {
+  using F = RecFmt<M16>;
   const int j2 = lane & 3, r = lane >> 2;
-  const uint8_t* vsz = rv + (kOffVSZ - kKPart);
-  const uint32_t* words = reinterpret_cast<const uint32_t*>(rv + (kOffVCodes - kKPart));
-  const float* vc = reinterpret_cast<const float*>(rv + (kOffVC - kKPart));
+  const uint8_t* vsz = rv + (F::vsz - F::kpart);
+  const uint32_t* words = reinterpret_cast<const uint32_t*>(rv);   // V codes open the V part
+  const uint8_t* vc = rv + (F::vc - F::kpart);
 #pragma unroll 1
   for (int hb = 0; hb < 2; ++hb) {
     float2 sz[4][2][2];
@@ -212,14 +215,13 @@ __device__ __forceinline__ void dequant_v(const uint8_t* rv, uint8_t* vh, uint8_
       for (int f = 0; f < 2; ++f)
 #pragma unroll
         for (int s = 0; s < 2; ++s)
-          sz[kk][f][s] = *reinterpret_cast<const float2*>(
-              vsz + 8 * (16 * (4 * hb + kk) + 8 * f + 2 * j2 + s));
+          sz[kk][f][s] = F::get_sz(vsz, 16 * (4 * hb + kk) + 8 * f + 2 * j2 + s);
 #pragma unroll 2
     for (int k2 = dw; k2 < 16; k2 += NW) {
       const int m = k2 >> 1, e = k2 & 1;
       const int c = 16 * m + 8 * e + r;
       const uint32_t w = words[128 * m + 16 * r + 4 * j2 + 2 * e + hb];
-      const float cd = vc[c];
+      const float cd = F::get_c(vc, c);
 #pragma unroll
       for (int kk = 0; kk < 4; ++kk)
 #pragma unroll
@@ -241,8 +243,11 @@ __device__ __forceinline__ void dequant_v(const uint8_t* rv, uint8_t* vh, uint8_
   }
 }
 
+// M16: the "_m16" record (metadata stored as fp16); otherwise fp32.
+template <bool M16>
 __global__ void __launch_bounds__(kCThreads, 1)
     chunk_attention_kernel(const ChunkArgs a) {
+  using F = RecFmt<M16>;
   extern __shared__ uint8_t smem_raw[];
   CSmem& S = *reinterpret_cast<CSmem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                        ~static_cast<uintptr_t>(1023));
@@ -395,7 +400,7 @@ __global__ void __launch_bounds__(kCThreads, 1)
       // ---- this block's values into V^ ----
       if (page) {
         wait(&S.raw_full[j & 1], (j >> 1) & 1);
-        dequant_v<kSoftWarps>(S.raw[j & 1] + kKPart, S.vh, S.vl, warp, lane);
+        dequant_v<kSoftWarps, M16>(S.raw[j & 1] + F::kpart, S.vh, S.vl, warp, lane);
       } else {
         // the fp16 tail, rotated: column t = tid of V^ [channel][token]
         const int t = tid;
@@ -486,15 +491,15 @@ __global__ void __launch_bounds__(kCThreads, 1)
     // ================= dequant warps: page records in, keys into K^ =================
     const int dt = tid - kDeq0, dw = dt >> 5;
     auto rec_of = [&](int j) {
-      return a.pool + ((int64_t)trow[j] * a.hkv + kvh) * (int64_t)kRec;
+      return a.pool + ((int64_t)trow[j] * a.hkv + kvh) * (int64_t)F::bytes;
     };
     // loads issued and seen complete per buffer (thread dt == 0), as
     // count0 | count1 << 16 so that no array sits in local memory
     uint32_t issued = 0, seen = 0;
     auto issue = [&](int j) {
       uint64_t* bar = &S.raw_full[j & 1];
-      mbar_arrive_expect_tx(bar, kRec);
-      bulk_g2s(S.raw[j & 1], rec_of(j), kRec, bar);
+      mbar_arrive_expect_tx(bar, F::bytes);
+      bulk_g2s(S.raw[j & 1], rec_of(j), F::bytes, bar);
       issued += 1u << (16 * (j & 1));
     };
     const int npages = min(nblk, nfull);
@@ -511,7 +516,7 @@ __global__ void __launch_bounds__(kCThreads, 1)
       }
       if (j > 0) wait(&S.sdone[(j - 1) & 1], ((j - 1) >> 1) & 1);   // S of block j-1 read K^
       if (page) {
-        dequant_k(S.raw[j & 1], S.kh, S.kl, dw, lane);
+        dequant_k<M16>(S.raw[j & 1], S.kh, S.kl, dw, lane);
       } else {
         // the fp16 tail, rotated into the pages' space: yhat = H x / sqrt(128)
 #pragma unroll 1
@@ -621,18 +626,23 @@ __global__ void __launch_bounds__(kCThreads, 1)
   if (warp == 0) tmem_dealloc(tmem, kCTmemCols);
 }
 
+template <bool M16>
+cudaError_t launch_chunk(const ChunkArgs& args, cudaStream_t s) {
+  static std::atomic<uint64_t> smem_set{0};
+  cudaError_t e = ensure_dynamic_smem(chunk_attention_kernel<M16>, kCSmemBytes, smem_set);
+  if (e != cudaSuccess) return e;
+  if (args.ntq <= 0 || args.batch <= 0) return cudaSuccess;
+  dim3 grid(args.ntq, args.hkv, args.batch);
+  chunk_attention_kernel<M16><<<grid, kCThreads, kCSmemBytes, s>>>(args);
+  return cudaGetLastError();
+}
+
 }  // namespace
 
 int chunk_rows_per_tile(int g) { return 128 / g; }
 
 cudaError_t launch_chunk_attention(const ChunkArgs& args, cudaStream_t s) {
-  static std::atomic<uint64_t> smem_set{0};
-  cudaError_t e = ensure_dynamic_smem(chunk_attention_kernel, kCSmemBytes, smem_set);
-  if (e != cudaSuccess) return e;
-  if (args.ntq <= 0 || args.batch <= 0) return cudaSuccess;
-  dim3 grid(args.ntq, args.hkv, args.batch);
-  chunk_attention_kernel<<<grid, kCThreads, kCSmemBytes, s>>>(args);
-  return cudaGetLastError();
+  return args.meta16 ? launch_chunk<true>(args, s) : launch_chunk<false>(args, s);
 }
 
 }  // namespace kvarn

@@ -51,7 +51,7 @@ constexpr float kTwo24 = 16777216.0f;
 
 template <int NT>
 struct __align__(128) MmaSmem {
-  uint8_t rec[kWarps][kRec];     // per warp: K part at 0, V part at kKPart
+  uint8_t rec[kWarps][kRec];     // per warp: K part at 0, V part at the format's kpart
   float qrot[4 * NT][kD];        // H q per (padded) query head of the group
   float qplain[4 * NT][kD];      // q itself, for the fp16 tail
   uint64_t bar[kWarps][2];       // per warp: 0 = K part landed, 1 = V part landed
@@ -151,8 +151,10 @@ __device__ __forceinline__ constexpr float vpos_inv(int kb, int f) {
 // Three CTAs per SM for one head tile; for two (groups of 5-8 query heads)
 // the doubled score, probability and accumulator fragments need more than the
 // 168 registers a third CTA would leave, so two CTAs run with no spills.
-template <int NT>
+// M16: the "_m16" record (metadata stored as fp16); otherwise fp32.
+template <int NT, bool M16>
 __global__ void __launch_bounds__(kThreads, NT == 1 ? 3 : 2) decode_mma_kernel(DecodeArgs a) {
+  using F = RecFmt<M16>;
   extern __shared__ __align__(128) uint8_t smem_raw[];
   MmaSmem<NT>& S = *reinterpret_cast<MmaSmem<NT>*>(smem_raw);
   constexpr int G = 4 * NT;
@@ -176,7 +178,7 @@ __global__ void __launch_bounds__(kThreads, NT == 1 ? 3 : 2) decode_mma_kernel(D
   const bool has_tail = split == nsb - 1 && rem > 0;
 
   uint8_t* const kst = S.rec[warp];
-  uint8_t* const vst = S.rec[warp] + kKPart;
+  uint8_t* const vst = S.rec[warp] + F::kpart;
   uint64_t* const kbar = &S.bar[warp][0];
   uint64_t* const vbar = &S.bar[warp][1];
   if (lane == 0) {
@@ -201,17 +203,17 @@ __global__ void __launch_bounds__(kThreads, NT == 1 ? 3 : 2) decode_mma_kernel(D
     }
     return p;
   };
-  auto rec_of = [&](int64_t page) { return a.pool + (page * a.hkv + kvh) * (int64_t)kRec; };
+  auto rec_of = [&](int64_t page) { return a.pool + (page * a.hkv + kvh) * (int64_t)F::bytes; };
   auto issue_k = [&](int64_t page) {
     if (lane == 0) {
-      mbar_arrive_expect_tx(kbar, kKPart);
-      bulk_g2s(kst, rec_of(page), kKPart, kbar);
+      mbar_arrive_expect_tx(kbar, F::kpart);
+      bulk_g2s(kst, rec_of(page), F::kpart, kbar);
     }
   };
   auto issue_v = [&](int64_t page) {
     if (lane == 0) {
-      mbar_arrive_expect_tx(vbar, kVPart);
-      bulk_g2s(vst, rec_of(page) + kKPart, kVPart, vbar);
+      mbar_arrive_expect_tx(vbar, F::vpart);
+      bulk_g2s(vst, rec_of(page) + F::kpart, F::vpart, vbar);
     }
   };
 
@@ -304,13 +306,13 @@ __global__ void __launch_bounds__(kThreads, NT == 1 ? 3 : 2) decode_mma_kernel(D
       for (int nt = 0; nt < NT; ++nt) {
         const int h = 4 * nt + (r >> 1);
         const float4* qv = reinterpret_cast<const float4*>(S.qrot[h]);
-        const float4* cv = reinterpret_cast<const float4*>(kst + kOffKC + 128 * qi);
+        const uint8_t* cv = kst + F::kc;   // c of channels 32 qi + 4k .. : float4 8 qi + k
         float v[32];
         float am0 = 0.f, am1 = 0.f;
         float2 s0 = make_float2(0.f, 0.f), s1 = s0;
 #pragma unroll
         for (int k = 0; k < 8; ++k) {
-          const float4 q4 = qv[(8 * qi + k) ^ qi], c4 = cv[k];
+          const float4 q4 = qv[(8 * qi + k) ^ qi], c4 = F::get_c4(cv, 8 * qi + k);
           const float2 p0 = __fmul2_rn(make_float2(q4.x, q4.y), make_float2(c4.x, c4.y));
           const float2 p1 = __fmul2_rn(make_float2(q4.z, q4.w), make_float2(c4.z, c4.w));
           v[4 * k + 0] = p0.x;
@@ -387,8 +389,8 @@ __global__ void __launch_bounds__(kThreads, NT == 1 ? 3 : 2) decode_mma_kernel(D
 #pragma unroll
         for (int i = 0; i < MTG; ++i) {
           const int mt = m0 + i, tA = 16 * mt + r, tB = tA + 8;
-          const float2 szA = *reinterpret_cast<const float2*>(kst + kOffKSZ + 8 * tA);
-          const float2 szB = *reinterpret_cast<const float2*>(kst + kOffKSZ + 8 * tB);
+          const float2 szA = F::get_sz(kst + F::ksz, tA);
+          const float2 szB = F::get_sz(kst + F::ksz, tB);
 #pragma unroll
           for (int nt = 0; nt < NT; ++nt) {
             sc[nt][2 * mt] = fmaf(szA.x * sA[nt], d[nt][i][0] + d[nt][i][1], szA.y * sZ[nt]);
@@ -443,8 +445,7 @@ __global__ void __launch_bounds__(kThreads, NT == 1 ? 3 : 2) decode_mma_kernel(D
       float sm4[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
       for (int j = 0; j < 16; ++j) {
-        szv[j] = *reinterpret_cast<const float2*>(vst + (kOffVSZ - kKPart) +
-                                                  8 * (16 * (j >> 1) + 8 * (j & 1) + r));
+        szv[j] = F::get_sz(vst + (F::vsz - F::kpart), 16 * (j >> 1) + 8 * (j & 1) + r);
         sm4[j & 3] = fmaxf(sm4[j & 3], szv[j].x);
       }
       float smax = fmaxf(fmaxf(sm4[0], sm4[1]), fmaxf(sm4[2], sm4[3]));
@@ -473,14 +474,14 @@ __global__ void __launch_bounds__(kThreads, NT == 1 ? 3 : 2) decode_mma_kernel(D
       // ---- value sum: V codes (A, rows = channels) x P' (B).  MCG channel
       // tiles at a time, k-tile outer, so that their chains interleave ----
       const float fin = finv * kTwo24;
-      const float* cvv = reinterpret_cast<const float*>(vst + (kOffVC - kKPart));
+      const uint8_t* cvv = vst + (F::vc - F::kpart);
       constexpr int MCG = NT == 1 ? 8 : 4;
 #pragma unroll
       for (int c0 = 0; c0 < 8; c0 += MCG) {
         uint4 vw[MCG];   // words (e, h) = 00, 01, 10, 11 of channels 16mc + r, + 8
 #pragma unroll
         for (int i = 0; i < MCG; ++i)
-          vw[i] = *reinterpret_cast<const uint4*>(vst + (kOffVCodes - kKPart) + 512 * (c0 + i) +
+          vw[i] = *reinterpret_cast<const uint4*>(vst + 512 * (c0 + i) +
                                                   16 * lane);
         float d[NT][MCG][4];
 #pragma unroll
@@ -515,7 +516,7 @@ __global__ void __launch_bounds__(kThreads, NT == 1 ? 3 : 2) decode_mma_kernel(D
 #pragma unroll
         for (int i = 0; i < MCG; ++i) {
           const int mc = c0 + i;
-          const float cvA = cvv[16 * mc + r], cvB = cvv[16 * mc + 8 + r];
+          const float cvA = F::get_c(cvv, 16 * mc + r), cvB = F::get_c(cvv, 16 * mc + 8 + r);
 #pragma unroll
           for (int nt = 0; nt < NT; ++nt) {
             oacc[nt][2 * mc] = fmaf(oacc[nt][2 * mc], alpha[nt],
@@ -833,11 +834,11 @@ __global__ void __launch_bounds__(kThreads, NT == 1 ? 3 : 2) decode_mma_kernel(D
   if (tid == 0) a.ws_count[(int64_t)b * a.hkv + kvh] = 0;
 }
 
-template <int NT>
+template <int NT, bool M16>
 cudaError_t launch_nt(const DecodeArgs& args, cudaStream_t s) {
   static std::atomic<uint64_t> smem_set{0};
   const int smem = (int)sizeof(MmaSmem<NT>);
-  cudaError_t e = ensure_dynamic_smem(decode_mma_kernel<NT>, smem, smem_set);
+  cudaError_t e = ensure_dynamic_smem(decode_mma_kernel<NT, M16>, smem, smem_set);
   if (e != cudaSuccess) return e;
   DecodeArgs a = args;
   a.cluster = decode_uses_cluster(a.g, a.nsplit);
@@ -855,7 +856,7 @@ cudaError_t launch_nt(const DecodeArgs& args, cudaStream_t s) {
     cfg.attrs = attr;
     cfg.numAttrs = 1;
   }
-  return cudaLaunchKernelEx(&cfg, decode_mma_kernel<NT>, a);
+  return cudaLaunchKernelEx(&cfg, decode_mma_kernel<NT, M16>, a);
 }
 
 }  // namespace
@@ -875,7 +876,8 @@ int decode_mma_ctas_per_sm(int g) {
 }
 
 cudaError_t launch_decode_mma(const DecodeArgs& a, cudaStream_t s) {
-  return a.g <= 4 ? launch_nt<1>(a, s) : launch_nt<2>(a, s);
+  if (a.meta16) return a.g <= 4 ? launch_nt<1, true>(a, s) : launch_nt<2, true>(a, s);
+  return a.g <= 4 ? launch_nt<1, false>(a, s) : launch_nt<2, false>(a, s);
 }
 
 }  // namespace kvarn

@@ -73,7 +73,10 @@ __device__ void fwht_rows(float (*v)[kD], int g) {
 }
 
 // grid: (nsplit, hkv, batch); block 128.
+// M16: the "_m16" record (metadata stored as fp16); otherwise fp32.
+template <bool M16>
 __global__ void __launch_bounds__(kThreads) decode_simple_kernel(DecodeArgs a) {
+  using F = RecFmt<M16>;
   extern __shared__ __align__(16) uint8_t smem_raw[];
   DecodeSmem& S = *reinterpret_cast<DecodeSmem*>(smem_raw);
   const int split = blockIdx.x, kvh = blockIdx.y, b = blockIdx.z;
@@ -119,13 +122,14 @@ __global__ void __launch_bounds__(kThreads) decode_simple_kernel(DecodeArgs a) {
         if (tid == 0) report(a.status, KVARN_STATUS_BAD_PAGE);
         continue;
       }
-      const uint4* src = reinterpret_cast<const uint4*>(a.pool + (page * a.hkv + kvh) * (int64_t)kRec);
+      const uint4* src =
+          reinterpret_cast<const uint4*>(a.pool + (page * a.hkv + kvh) * (int64_t)F::bytes);
       uint4* dst = reinterpret_cast<uint4*>(S.rec);
-      for (int i = tid; i < kRec / 16; i += kThreads) dst[i] = __ldg(src + i);
+      for (int i = tid; i < F::bytes / 16; i += kThreads) dst[i] = __ldg(src + i);
       __syncthreads();
       // qc = H q * c^K (thread = channel), and its sum per head
       {
-        const float ck = reinterpret_cast<const float*>(S.rec + kOffKC)[tid];
+        const float ck = F::get_c(S.rec + F::kc, tid);
         float part[kMaxG];
         for (int h = 0; h < g; ++h) {
           const float x = S.qrot[h][tid] * ck;
@@ -137,7 +141,7 @@ __global__ void __launch_bounds__(kThreads) decode_simple_kernel(DecodeArgs a) {
       // scores (thread = token)
       {
         const uint32_t* row = reinterpret_cast<const uint32_t*>(S.rec + kOffKCodes + 64 * tid);
-        const float2 sz = reinterpret_cast<const float2*>(S.rec + kOffKSZ)[tid];
+        const float2 sz = F::get_sz(S.rec + F::ksz, tid);
         for (int h = 0; h < g; ++h) sc[h] = 0.f;
         for (int w = 0; w < 16; ++w) {
           const uint32_t word = row[w];
@@ -179,7 +183,7 @@ __global__ void __launch_bounds__(kThreads) decode_simple_kernel(DecodeArgs a) {
     float p[kMaxG];
     for (int h = 0; h < g; ++h) p[h] = sc[h] == -INFINITY ? 0.f : __expf(sc[h] - S.m[h]);
     if (u < nfull) {
-      const float2 szv = reinterpret_cast<const float2*>(S.rec + kOffVSZ)[tid];
+      const float2 szv = F::get_sz(S.rec + F::vsz, tid);
       float zp[kMaxG];
       for (int h = 0; h < g; ++h) {
         S.pw[h][tid] = p[h] * szv.x;
@@ -192,8 +196,8 @@ __global__ void __launch_bounds__(kThreads) decode_simple_kernel(DecodeArgs a) {
       // value sum (thread = channel d), rotated space
       {
         const int d = tid;
-        const uint32_t* vw = reinterpret_cast<const uint32_t*>(S.rec + kOffVCodes);
-        const float cv = reinterpret_cast<const float*>(S.rec + kOffVC)[d];
+        const uint32_t* vw = reinterpret_cast<const uint32_t*>(S.rec + F::kpart);
+        const float cv = F::get_c(S.rec + F::vc, d);
         float pv[kMaxG];
         for (int h = 0; h < g; ++h) pv[h] = 0.f;
         for (int w = 0; w < 8; ++w) {
@@ -280,16 +284,21 @@ __global__ void __launch_bounds__(kThreads) decode_simple_kernel(DecodeArgs a) {
   if (tid == 0) a.ws_count[(int64_t)b * a.hkv + kvh] = 0;
 }
 
+template <bool M16>
+cudaError_t launch_simple(const DecodeArgs& a, cudaStream_t s) {
+  static std::atomic<uint64_t> smem_set{0};
+  const int smem = (int)sizeof(DecodeSmem);
+  cudaError_t e = ensure_dynamic_smem(decode_simple_kernel<M16>, smem, smem_set);
+  if (e != cudaSuccess) return e;
+  dim3 grid(a.nsplit, a.hkv, a.batch);
+  decode_simple_kernel<M16><<<grid, kThreads, smem, s>>>(a);
+  return cudaGetLastError();
+}
+
 }  // namespace
 
 cudaError_t launch_decode_simple(const DecodeArgs& a, cudaStream_t s) {
-  static std::atomic<uint64_t> smem_set{0};
-  const int smem = (int)sizeof(DecodeSmem);
-  cudaError_t e = ensure_dynamic_smem(decode_simple_kernel, smem, smem_set);
-  if (e != cudaSuccess) return e;
-  dim3 grid(a.nsplit, a.hkv, a.batch);
-  decode_simple_kernel<<<grid, kThreads, smem, s>>>(a);
-  return cudaGetLastError();
+  return a.meta16 ? launch_simple<true>(a, s) : launch_simple<false>(a, s);
 }
 
 }  // namespace kvarn

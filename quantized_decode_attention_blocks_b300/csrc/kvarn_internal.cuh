@@ -25,6 +25,68 @@ constexpr int kOffVSZ = 13824;
 constexpr int kOffVC = 14848;
 constexpr int kKPart = 9728;      // K part: [0, 9728)
 constexpr int kVPart = kRec - kKPart;  // V part: [9728, 15360)
+// The two record formats: kvarn_k4v2_g128 (fp32 metadata, the constants
+// above) and the "_m16" variant, the same codes with s', z' and c_d stored as
+// fp16 (round to nearest even), 108 B per token-head:
+//   [0, 8192) K codes, [8192, 8704) K {s', z'} fp16 pairs, [8704, 8960) K c_d,
+//   [8960, 13056) V codes, [13056, 13568) V {s', z'}, [13568, 13824) V c_d.
+// The accessors take the address of the field (record part + offset).
+template <bool M16>
+struct RecFmt {
+  static constexpr int bytes = M16 ? 13824 : 15360;
+  static constexpr int kpart = M16 ? 8960 : 9728;   // K part [0, kpart)
+  static constexpr int vpart = bytes - kpart;       // V part [kpart, bytes)
+  static constexpr int ksz = 8192;
+  static constexpr int kc = M16 ? 8704 : 9216;
+  static constexpr int vsz = M16 ? 13056 : 13824;   // from the record start
+  static constexpr int vc = M16 ? 13568 : 14848;
+  // {s', z'} of token t
+  static __device__ __forceinline__ float2 get_sz(const uint8_t* f, int t) {
+    if constexpr (M16)
+      return __half22float2(reinterpret_cast<const __half2*>(f)[t]);
+    else
+      return reinterpret_cast<const float2*>(f)[t];
+  }
+  static __device__ __forceinline__ void put_sz(uint8_t* f, int t, float s, float z) {
+    if constexpr (M16)
+      reinterpret_cast<__half2*>(f)[t] = __floats2half2_rn(s, z);
+    else
+      reinterpret_cast<float2*>(f)[t] = make_float2(s, z);
+  }
+  // c_d of channel d, and of channels 4 i .. 4 i + 3
+  static __device__ __forceinline__ float get_c(const uint8_t* f, int d) {
+    if constexpr (M16)
+      return __half2float(reinterpret_cast<const __half*>(f)[d]);
+    else
+      return reinterpret_cast<const float*>(f)[d];
+  }
+  static __device__ __forceinline__ float4 get_c4(const uint8_t* f, int i) {
+    if constexpr (M16) {
+      const uint2 u = reinterpret_cast<const uint2*>(f)[i];
+      const float2 a = __half22float2(*reinterpret_cast<const __half2*>(&u.x));
+      const float2 b = __half22float2(*reinterpret_cast<const __half2*>(&u.y));
+      return make_float4(a.x, a.y, b.x, b.y);
+    } else {
+      return reinterpret_cast<const float4*>(f)[i];
+    }
+  }
+  static __device__ __forceinline__ void put_c(uint8_t* f, int d, float c) {
+    if constexpr (M16)
+      reinterpret_cast<__half*>(f)[d] = __float2half_rn(c);
+    else
+      reinterpret_cast<float*>(f)[d] = c;
+  }
+};
+static_assert(RecFmt<false>::bytes == kRec && RecFmt<false>::kpart == kKPart &&
+                  RecFmt<false>::ksz == kOffKSZ && RecFmt<false>::kc == kOffKC &&
+                  RecFmt<false>::vsz == kOffVSZ && RecFmt<false>::vc == kOffVC &&
+                  RecFmt<false>::kpart == kOffVCodes,
+              "the fp32 format is the one the constants above describe");
+static_assert(RecFmt<true>::kpart % 16 == 0 && RecFmt<true>::vpart % 16 == 0 &&
+                  RecFmt<true>::bytes % 16 == 0 && RecFmt<true>::vsz % 16 == 0 &&
+                  RecFmt<true>::vc % 16 == 0 && RecFmt<true>::kc % 16 == 0,
+              "bulk copies and vector loads need 16-byte parts and fields");
+
 // Split-K partial state per (sequence, query head, split): m, l, 2 pad, o[128]
 // (o 16-byte aligned).
 constexpr int kPartStride = 4 + kD;
@@ -76,6 +138,7 @@ struct QuantizeArgs {
   int64_t sb, st, sh;       // element strides of k / v
   int batch, hkv, iters, max_seq;
   int rms;                  // Sinkhorn statistic: 0 centred std, 1 uncentred RMS
+  int meta16;               // record format: 0 fp32 metadata, 1 fp16 ("_m16")
   const int32_t* seq_lens;
   const int32_t* block_table;
   int max_blocks;
@@ -92,6 +155,7 @@ struct AppendArgs {
   const int32_t* pos;
   int batch, hkv, iters;
   int rms;
+  int meta16;
   const int32_t* block_table;
   int max_blocks;
   uint8_t* pool;
@@ -118,6 +182,7 @@ struct DecodeArgs {
   int pages_per_split;
   int nsplit;
   int cluster;        // 1: the nsplit CTAs of a (sequence, KV head) form a cluster
+  int meta16;         // record format: 0 fp32 metadata, 1 fp16 ("_m16")
   int32_t* status;
 };
 
@@ -242,6 +307,7 @@ struct ChunkArgs {
   const __half* tail_v;
   float scale_log2;           // softmax scale * log2(e)
   __half* out;                // [batch][M][hq][128]
+  int meta16;                 // record format: 0 fp32 metadata, 1 fp16 ("_m16")
   int32_t* status;
 };
 int chunk_rows_per_tile(int g);

@@ -327,6 +327,8 @@ __device__ __forceinline__ uint32_t hs_bits(int n, int k) {
   return (__popc(n & k) & 1) ? 0xBC00u : 0x3C00u;
 }
 
+// M16: the "_m16" record (metadata stored as fp16); otherwise fp32.
+template <bool M16>
 __global__ void __launch_bounds__(kQThreads, 1)
     quantize_tc_kernel(const __grid_constant__ CUtensorMap tmk,
                        const __grid_constant__ CUtensorMap tmv, const QTileArgs a,
@@ -435,7 +437,7 @@ __global__ void __launch_bounds__(kQThreads, 1)
     if (a.mode != 0)
       page = in_table ? (int64_t)a.block_table[(int64_t)tl.b * a.max_blocks + tl.j] : -1;
     if (in_table && page >= 0 && page < a.num_pages)
-      info.rec = (long long)((page * a.hkv + tl.h) * (int64_t)kRec);
+      info.rec = (long long)((page * a.hkv + tl.h) * (int64_t)RecFmt<M16>::bytes);
     else
       report(a.status, in_table ? KVARN_STATUS_BAD_PAGE : KVARN_STATUS_BAD_LENGTH);
     const CUtensorMap* tm = tl.part ? &tmv : &tmk;
@@ -621,7 +623,7 @@ __global__ void __launch_bounds__(kQThreads, 1)
       // K: token-major, 64 bytes per token; nibble e of word w = channel 8w + e.
       // The fragment of a row is the channels 32q .. 32q + 31: its words 4q ..
       // 4q + 3, nibble 2 (k & 3) + b of word 4q + (k >> 2) from column pair k.
-      if (lower) reinterpret_cast<float*>(out + kOffKC)[row] = cc[row];
+      if (lower) RecFmt<M16>::put_c(out + RecFmt<M16>::kc, row, cc[row]);
       {
         float mn[2], mx[2];
 #pragma unroll
@@ -646,8 +648,8 @@ __global__ void __launch_bounds__(kQThreads, 1)
           const float inv = range > 0.f ? __fdividef(15.f, range) : 0.f;
           const int t = frow(e);
           if (q == 0)
-            *reinterpret_cast<float2*>(out + kOffKSZ + 8 * t) =
-                make_float2(range * (kInvSqrt128 / 15.f), lo * kInvSqrt128);
+            RecFmt<M16>::put_sz(out + RecFmt<M16>::ksz, t, range * (kInvSqrt128 / 15.f),
+                                lo * kInvSqrt128);
           // u = (x - min) (15 / range) + 1.5 * 2^23: the code in the low bits
           const float2 nm = make_float2(-lo, -lo), iv = make_float2(inv, inv);
           uint32_t acc[4];
@@ -667,7 +669,8 @@ __global__ void __launch_bounds__(kQThreads, 1)
       // V: the per-token min and 3 / range from Y, then each thread packs
       // whole words of its channels from Y^T: the fragment columns (tokens)
       // 8k + 2q + b are crumb (k & 7) + 8b of word v_word(channel, q, k >> 3)
-      if (lower) reinterpret_cast<float*>(out + (kOffVC - kKPart))[row] = cc[row];
+      if (lower)
+        RecFmt<M16>::put_c(out + (RecFmt<M16>::vc - RecFmt<M16>::kpart), row, cc[row]);
       {
         float mn[2], mx[2];
 #pragma unroll
@@ -691,13 +694,13 @@ __global__ void __launch_bounds__(kQThreads, 1)
           if (q == 0) {
             S.vmin[wg][t] = lo;
             S.vinv[wg][t] = range > 0.f ? __fdividef(3.f, range) : 0.f;
-            *reinterpret_cast<float2*>(out + (kOffVSZ - kKPart) + 8 * t) =
-                make_float2(range * (kInvSqrt128 / 3.f), lo * kInvSqrt128);
+            RecFmt<M16>::put_sz(out + (RecFmt<M16>::vsz - RecFmt<M16>::kpart), t,
+                                range * (kInvSqrt128 / 3.f), lo * kInvSqrt128);
           }
         }
       }
       named_sync(bar_id, kWGThreads);
-      uint32_t* vw = reinterpret_cast<uint32_t*>(out + (kOffVCodes - kKPart));
+      uint32_t* vw = reinterpret_cast<uint32_t*>(out);   // V codes open the V part
       {
         tmem_ld256(tYT, v);
         tmem_wait_ld();
@@ -747,7 +750,8 @@ __global__ void __launch_bounds__(kQThreads, 1)
     tc_fence_before();
     named_sync(bar_id, kWGThreads);
     if (leader && cur.rec >= 0) {
-      bulk_s2g(a.pool + cur.rec + (part ? kKPart : 0), out, part ? kVPart : kKPart);
+      bulk_s2g(a.pool + cur.rec + (part ? RecFmt<M16>::kpart : 0), out,
+               part ? RecFmt<M16>::vpart : RecFmt<M16>::kpart);
       bulk_commit();
     }
     stage ^= 1;
@@ -823,17 +827,18 @@ bool encode_tile_map(CUtensorMap* map, const void* base, int64_t sb, int64_t st,
 
 constexpr int kQSmemBytes = (int)sizeof(QSmem) + 1024;
 
+template <bool M16>
 cudaError_t launch_tiles(const CUtensorMap& mk, const CUtensorMap& mv, const QTileArgs& qa,
                          const QCopyArgs& cp, cudaStream_t s) {
   static std::atomic<uint64_t> smem_set{0};
-  cudaError_t e = ensure_dynamic_smem(quantize_tc_kernel, kQSmemBytes, smem_set);
+  cudaError_t e = ensure_dynamic_smem(quantize_tc_kernel<M16>, kQSmemBytes, smem_set);
   if (e != cudaSuccess) return e;
   const int sms = device_sm_count();
   if (sms <= 0) return cudaErrorNoDevice;
   const int want = (qa.ntiles + kWG - 1) / kWG;
   // one CTA at least: with no tile to quantize it still does the copies
   const int grid = want < 1 ? 1 : want < sms ? want : sms;
-  quantize_tc_kernel<<<grid, kQThreads, kQSmemBytes, s>>>(mk, mv, qa, cp);
+  quantize_tc_kernel<M16><<<grid, kQThreads, kQSmemBytes, s>>>(mk, mv, qa, cp);
   return cudaGetLastError();
 }
 
@@ -896,7 +901,7 @@ cudaError_t launch_quantize_blocks(const QuantizeArgs& a, cudaStream_t s) {
     qa.roles = rk;
   }
   // the tiles and the leftover-token copies, one launch
-  return launch_tiles(mk, mv, qa, cp, s);
+  return a.meta16 ? launch_tiles<true>(mk, mv, qa, cp, s) : launch_tiles<false>(mk, mv, qa, cp, s);
 }
 
 cudaError_t launch_append_token(const AppendArgs& a, cudaStream_t s) {
@@ -930,7 +935,7 @@ cudaError_t launch_append_token(const AppendArgs& a, cudaStream_t s) {
       !encode_tile_map(&mv, a.tail_v, sb, kD, sh, a.batch, kT, a.hkv, &rv))
     return cudaErrorInvalidValue;
   qa.roles = rk;
-  return launch_tiles(mk, mv, qa, cp, s);
+  return a.meta16 ? launch_tiles<true>(mk, mv, qa, cp, s) : launch_tiles<false>(mk, mv, qa, cp, s);
 }
 
 }  // namespace kvarn

@@ -20,6 +20,7 @@ LIB_PATH = os.path.join(HERE, "libkvarn.so")
 HEAD_DIM = 128
 BLOCK_TOKENS = 128
 PAGE_BYTES = 15360
+PAGE_BYTES_M16 = 13824     # KVARN_PAGE_BYTES_M16: format variant "_m16"
 FP8_PAGE_BYTES = 33792     # KVARN_FP8_PAGE_BYTES
 FP16_PAGE_BYTES = 65536            # KVARN_FP16_PAGE_BYTES
 NOALLOC_SCRATCH_BYTES = 4 << 20   # KVARN_NOALLOC_SCRATCH_BYTES
@@ -44,11 +45,17 @@ class Config(ctypes.Structure):
     _fields_ = [("head_dim", ctypes.c_int), ("block_tokens", ctypes.c_int),
                 ("group", ctypes.c_int), ("k_bits", ctypes.c_int), ("v_bits", ctypes.c_int),
                 ("sinkhorn_iters", ctypes.c_int), ("num_q_heads", ctypes.c_int),
-                ("num_kv_heads", ctypes.c_int), ("sinkhorn_rms", ctypes.c_int)]
+                ("num_kv_heads", ctypes.c_int), ("sinkhorn_rms", ctypes.c_int),
+                ("meta_fp16", ctypes.c_int)]
 
     @property
     def g(self) -> int:
         return self.num_q_heads // self.num_kv_heads
+
+    @property
+    def page_bytes(self) -> int:
+        """Bytes of one page record of this format (kvarn_page_bytes)."""
+        return PAGE_BYTES_M16 if self.meta_fp16 else PAGE_BYTES
 
 
 # every symbol include/kvarn.h declares, with its ctypes signature
@@ -229,7 +236,7 @@ def page_bytes(cfg: Config) -> int:
 # --------------------------------------------------------------- allocation --
 
 def alloc_pool(cfg: Config, num_pages: int, device="cuda") -> torch.Tensor:
-    return torch.zeros((num_pages, cfg.num_kv_heads, PAGE_BYTES), dtype=torch.uint8,
+    return torch.zeros((num_pages, cfg.num_kv_heads, cfg.page_bytes), dtype=torch.uint8,
                        device=device)
 
 
@@ -270,7 +277,7 @@ def kvarn_quantize_blocks(cfg: Config, k: torch.Tensor, v: torch.Tensor, seq_len
     dev = _kv_pair(k, v, cfg.num_kv_heads)
     B = k.shape[0]
     _lens_table(dev, B, seq_lens, "seq_lens", block_table)
-    _arg(pool, "pool", torch.uint8, (None, cfg.num_kv_heads, PAGE_BYTES), device=dev)
+    _arg(pool, "pool", torch.uint8, (None, cfg.num_kv_heads, cfg.page_bytes), device=dev)
     _tails(dev, cfg, B, tail_k, tail_v)
     _status(dev, status)
     with _on(dev):
@@ -290,7 +297,7 @@ def kvarn_append_token(cfg: Config, k_new: torch.Tensor, v_new: torch.Tensor, po
     _arg(v_new, "v_new", torch.float16, tuple(k_new.shape), device=dev)
     B = k_new.shape[0]
     _lens_table(dev, B, pos, "pos", block_table)
-    _arg(pool, "pool", torch.uint8, (None, cfg.num_kv_heads, PAGE_BYTES), device=dev)
+    _arg(pool, "pool", torch.uint8, (None, cfg.num_kv_heads, cfg.page_bytes), device=dev)
     _tails(dev, cfg, B, tail_k, tail_v)
     _status(dev, status)
     with _on(dev):
@@ -305,7 +312,7 @@ def _decode_args(cfg, q, pool, block_table, seq_lens, tail_k, tail_v, out, statu
     _arg(out, "out", torch.float16, tuple(q.shape), device=dev)
     B = q.shape[0]
     _lens_table(dev, B, seq_lens, "seq_lens", block_table)
-    _arg(pool, "pool", torch.uint8, (None, cfg.num_kv_heads, PAGE_BYTES), device=dev)
+    _arg(pool, "pool", torch.uint8, (None, cfg.num_kv_heads, cfg.page_bytes), device=dev)
     _tails(dev, cfg, B, tail_k, tail_v)
     _status(dev, status)
     return dev
@@ -344,7 +351,7 @@ def kvarn_chunk_attention(cfg: Config, q: torch.Tensor, start: torch.Tensor,
     B = q.shape[0]
     _lens_table(dev, B, start, "start", block_table)
     _arg(chunk_lens, "chunk_lens", torch.int32, (_AtLeast(B),), device=dev)
-    _arg(pool, "pool", torch.uint8, (None, cfg.num_kv_heads, PAGE_BYTES), device=dev)
+    _arg(pool, "pool", torch.uint8, (None, cfg.num_kv_heads, cfg.page_bytes), device=dev)
     _tails(dev, cfg, B, tail_k, tail_v)
     _status(dev, status)
     if softmax_scale is None:

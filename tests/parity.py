@@ -5,6 +5,10 @@
     1e-4 of all elements;
   * s' and c: |gpu - ref| <= 1e-5 |ref| (1e-12 absolute when ref = 0);
   * z': |gpu - ref| <= 1e-5 (|z'| + s' (2^b - 1));
+  * fp16 metadata (format "_m16"): equal to the oracle's fp16 value, or one
+    fp16 spacing away from it with the oracle's fp32 value within 1e-5
+    (relative) of the midpoint between the two (a rounding boundary of the
+    second rounding);
   * attention output (fp16): |gpu - ref| <= 2e-3 + 1e-3 |ref| elementwise, the
     oracle being fed the GPU's own pool so that decode is judged apart from
     boundary flips in quantization.
@@ -23,14 +27,33 @@ def near_boundary(u):
     return np.abs(u - np.floor(u) - 0.5) < BOUNDARY
 
 
-def compare_record(got: np.ndarray, ref: np.ndarray, u_k=None, u_v=None, stats=None):
-    """Compares one 15360-byte record (GPU) with the oracle's.  u_k, u_v:
-    oracle pre-rounding values [128][128] (token, channel).  Returns a dict."""
+def _compare_meta16(tag, got16, ref16, ref32):
+    """fp16 metadata: the same rounding of nearly the same fp32 value."""
+    g, r = got16.astype(np.float64), ref16.astype(np.float64)
+    same = g == r
+    if same.all():
+        return
+    r32 = ref32.astype(np.float64)
+    spacing = np.spacing(ref16.astype(np.float16)).astype(np.float64)
+    mid = 0.5 * (g + r)
+    near = (np.abs(g - r) <= spacing * 1.0000001) & (np.abs(r32 - mid) <= 1e-5 * np.abs(mid))
+    bad = ~same & ~near
+    assert not bad.any(), (f"{tag}: {int(bad.sum())} fp16 values differ away from a rounding "
+                           f"boundary, e.g. gpu={g[bad][:3]}, ref={r[bad][:3]}, "
+                           f"ref fp32={r32[bad][:3]}")
+
+
+def compare_record(got: np.ndarray, ref: np.ndarray, u_k=None, u_v=None, stats=None,
+                   meta16: bool = False, ref32: np.ndarray = None):
+    """Compares one record (GPU) with the oracle's.  u_k, u_v: oracle
+    pre-rounding values [128][128] (token, channel).  meta16: the "_m16"
+    format, whose metadata is judged against ref32, the oracle's record of
+    the same tile in the fp32 format.  Returns a dict."""
     out = {} if stats is None else stats
     for is_v, u in ((False, u_k), (True, u_v)):
         bits = 2 if is_v else 4
-        qg, sg, zg, cg = kvref.unpack_part(got, is_v)
-        qr, sr, zr, cr = kvref.unpack_part(ref, is_v)
+        qg, sg, zg, cg = kvref.unpack_part(got, is_v, meta16)
+        qr, sr, zr, cr = kvref.unpack_part(ref, is_v, meta16)
         tag = "v" if is_v else "k"
         diff = qg != qr
         n_diff = int(diff.sum())
@@ -43,6 +66,11 @@ def compare_record(got: np.ndarray, ref: np.ndarray, u_k=None, u_v=None, stats=N
                                    f"ref={qr[bad][:4]}")
         out[f"{tag}_flips"] = out.get(f"{tag}_flips", 0) + n_diff
         out[f"{tag}_codes"] = out.get(f"{tag}_codes", 0) + qg.size
+        if meta16:
+            _, s32, z32, c32 = kvref.unpack_part(ref32, is_v)
+            for name, g_, r_, r32 in (("s", sg, sr, s32), ("z", zg, zr, z32), ("c", cg, cr, c32)):
+                _compare_meta16(f"{tag}.{name}", g_, r_, r32)
+            continue
         for name, g_, r_ in (("s", sg, sr), ("c", cg, cr)):
             g64, r64 = g_.astype(np.float64), r_.astype(np.float64)
             tol = np.where(r64 == 0, 1e-12, 1e-5 * np.abs(r64))

@@ -36,7 +36,8 @@ def test_library_exports_every_declared_symbol():
 
 def test_header_constants_match_binding():
     text = open(HEADER).read()
-    for name, val in (("KVARN_PAGE_BYTES", K.PAGE_BYTES), ("KVARN_OK", K.OK),
+    for name, val in (("KVARN_PAGE_BYTES", K.PAGE_BYTES),
+                      ("KVARN_PAGE_BYTES_M16", K.PAGE_BYTES_M16), ("KVARN_OK", K.OK),
                       ("KVARN_ERR_INVALID_ARG", K.ERR_INVALID_ARG),
                       ("KVARN_ERR_UNSUPPORTED", K.ERR_UNSUPPORTED),
                       ("KVARN_ERR_WORKSPACE", K.ERR_WORKSPACE), ("KVARN_ERR_LAUNCH", K.ERR_LAUNCH),
@@ -63,6 +64,17 @@ def test_config_parsing():
             kv.config_from_string(bad, 12, 2)
     r.sinkhorn_rms = 2
     assert kv.config_validate(r) == K.ERR_UNSUPPORTED
+    # the fp16-metadata variant, alone or with "_rms", either order
+    assert c.meta_fp16 == 0
+    for fmt in ("k4v2_g128_m16", "kvarn_k4v2_g128_m16_s3", "k4v2_g128_rms_m16", "k4v2_g128_m16_rms_s1"):
+        m = kv.config_from_string(fmt, 12, 2)
+        assert m.meta_fp16 == 1 and m.sinkhorn_rms == ("rms" in fmt)
+        assert kv.page_bytes(m) == 13824 == 108 * 128 == m.page_bytes
+    for bad in ("k4v2_g128_m16_m16", "k4v2_g128_rms_rms", "k4v2_g128_s2_m16", "k4v2_g128_m8"):
+        with pytest.raises(kv.KvarnError):
+            kv.config_from_string(bad, 12, 2)
+    m.meta_fp16 = 3
+    assert kv.config_validate(m) == K.ERR_UNSUPPORTED
     for bad in ("k4v4_g128", "k4v2_g64", "k4v2_g128_x", "k4v2_g128_s", "k4v2_g128_s999"):
         with pytest.raises(kv.KvarnError) as e:
             kv.config_from_string(bad, 32, 8)

@@ -21,7 +21,8 @@ from workloads import synth
 pytestmark = pytest.mark.gpu
 
 
-def _case(starts, chunk_lens, M, hq, hkv, seed, perm=True, table=None, num_pages=None):
+def _case(starts, chunk_lens, M, hq, hkv, seed, perm=True, table=None, num_pages=None,
+          m16=False):
     starts = np.asarray(starts, dtype=np.int64)
     cls = np.asarray(chunk_lens, dtype=np.int64)
     n = starts + cls
@@ -29,7 +30,7 @@ def _case(starts, chunk_lens, M, hq, hkv, seed, perm=True, table=None, num_pages
     S = max(int(n.max()), 1)
     w = synth.scaled(synth.WORKLOADS["llama3_8b_layer"], batch=B, seq=S, hkv=hkv, hq=hq)
     k, v = synth.kv(w, layer=seed, device=DEV)
-    cfg = config(hq, hkv)
+    cfg = config(hq, hkv, m16=m16)
     mb = (S + 127) // 128
     if table is None:
         g = torch.Generator().manual_seed(seed)
@@ -47,7 +48,7 @@ def _case(starts, chunk_lens, M, hq, hkv, seed, perm=True, table=None, num_pages
                              table.to(DEV), tk, tv, out, status=status)
     torch.cuda.synchronize()
     return dict(cfg=cfg, q=q, out=out, status=status, st=st, pool=pool, tk=tk, tv=tv,
-                table=table, starts=starts, cls=cls, hq=hq, hkv=hkv)
+                table=table, starts=starts, cls=cls, hq=hq, hkv=hkv, m16=m16)
 
 
 def _check(c):
@@ -57,7 +58,7 @@ def _check(c):
     assert np.isfinite(got).all()
     ref = kvref.chunk_attention(host(c["q"]), c["starts"], c["cls"], host(c["pool"]),
                                 host(c["table"]), host(c["tk"]), host(c["tv"]), c["hq"],
-                                c["hkv"])
+                                c["hkv"], meta16=c["m16"])
     for b, cl in enumerate(c["cls"]):
         assert not got[b, int(cl):].any(), "rows past the chunk must be zeros"
     return parity.compare_attention(got, ref)
@@ -68,6 +69,12 @@ def test_chunks_ragged_with_pages_and_tail(hq, hkv):
     # chunks that start mid-page, inside the first block, at zero, and end in
     # the fp16 tail; several query tiles per (sequence, KV head) for g <= 4
     _check(_case([250, 100, 0, 300], [150, 60, 60, 1], 150, hq, hkv, seed=1))
+
+
+@pytest.mark.parametrize("hq,hkv", [(8, 2), (12, 2)])
+def test_m16_format(hq, hkv):
+    # format variant "_m16" (fp16 metadata): ragged chunks over pages and tail
+    _check(_case([250, 100, 0, 300], [150, 60, 60, 1], 150, hq, hkv, seed=8, m16=True))
 
 
 def test_chunk_of_whole_pages_and_inside_the_tail():

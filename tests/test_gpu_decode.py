@@ -17,11 +17,11 @@ from workloads import synth
 pytestmark = pytest.mark.gpu
 
 
-def _run(w, lens, table, num_pages, q=None, max_seq=None):
+def _run(w, lens, table, num_pages, q=None, max_seq=None, m16=False):
     max_seq = int(lens.max()) if max_seq is None else max_seq
     S = max(int(lens.max()), 1)
     k, v = synth.kv(w, device=DEV, seq=S)
-    cfg = config(w.hq, w.hkv)
+    cfg = config(w.hq, w.hkv, m16=m16)
     pool, tk, tv, st = prefill(cfg, k, v, lens, table, num_pages, max_seq=max_seq)
     if q is None:
         q = synth.queries(w)
@@ -29,7 +29,7 @@ def _run(w, lens, table, num_pages, q=None, max_seq=None):
     torch.cuda.synchronize()
     assert int(st.item()) == 0 and int(st2.item()) == 0
     ref = kvref.decode_attention(host(q), host(pool), host(table), host(lens), host(tk),
-                                 host(tv), w.hq, w.hkv, route=1)
+                                 host(tv), w.hq, w.hkv, route=1, meta16=m16)
     res = parity.compare_attention(host(out), ref)
     res.update(got=host(out).astype(np.float64), ref=ref)
     return res, (cfg, q, pool, table, lens, tk, tv, out, ws, max_seq)
@@ -47,6 +47,33 @@ def test_group_sizes_and_ragged_lengths(hq, hkv):
     g = torch.Generator().manual_seed(11)
     table = torch.randperm(B * mb, generator=g).to(torch.int32).reshape(B, mb)
     _run(w, lens, table, B * mb)
+
+
+@pytest.mark.parametrize("hq,hkv", [(1, 1), (4, 2), (6, 2), (8, 2), (12, 2), (32, 8)])
+def test_m16_format_group_sizes(hq, hkv):
+    # format variant "_m16" (fp16 metadata): both head-tile counts of the
+    # tensor-core kernel (g = 1..4: one, g = 6: two), over ragged lengths on
+    # permuted pages
+    lens = torch.tensor([0, 1, 127, 128, 129, 300, 1000, 2048], dtype=torch.int32)
+    B = len(lens)
+    w = synth.scaled(synth.WORKLOADS["llama3_8b_layer"], batch=B, seq=2048, hkv=hkv, hq=hq)
+    mb = 16
+    g = torch.Generator().manual_seed(61)
+    table = torch.randperm(B * mb, generator=g).to(torch.int32).reshape(B, mb)
+    _run(w, lens, table, B * mb, m16=True)
+
+
+def test_m16_format_cuda_core_kernel_and_many_splits():
+    # g = 16 runs on the CUDA-core kernel; one long sequence takes the
+    # workspace merge
+    w = synth.scaled(synth.WORKLOADS["long_context"], batch=2, seq=9000, hkv=1, hq=16)
+    lens = torch.tensor([9000, 333], dtype=torch.int32)
+    table = torch.arange(2 * 71, dtype=torch.int32).reshape(2, 71)
+    _run(w, lens, table, 2 * 71, m16=True)
+    w = synth.scaled(synth.WORKLOADS["long_context"], batch=1, seq=20000, hkv=2, hq=8)
+    lens = torch.tensor([20000], dtype=torch.int32)
+    table = torch.arange(157, dtype=torch.int32).reshape(1, 157)
+    _run(w, lens, table, 157, m16=True)
 
 
 def test_no_bias_common_to_all_channels():

@@ -15,16 +15,18 @@ from workloads import synth
 pytestmark = pytest.mark.gpu
 
 
-def _check_prefill(w, lens, table, num_pages, iters=2, k=None, v=None, rms=False):
+def _check_prefill(w, lens, table, num_pages, iters=2, k=None, v=None, rms=False, m16=False):
     if k is None:
         k, v = synth.kv(w, device=DEV)
-    cfg = config(w.hq, w.hkv, iters, rms=rms)
+    cfg = config(w.hq, w.hkv, iters, rms=rms, m16=m16)
     pool, tk, tv, status = prefill(cfg, k, v, lens, table, num_pages, max_seq=w.seq)
     torch.cuda.synchronize()
     assert int(status.item()) == 0
     kh, vh = host(k), host(v)
     ref = kvref.quantize_blocks(kh, vh, host(lens), host(table), num_pages, iters, want_u=True,
-                                rms=rms)
+                                rms=rms, meta16=m16)
+    ref32 = (kvref.quantize_blocks(kh, vh, host(lens), host(table), num_pages, iters, rms=rms)
+             if m16 else None)
     got_pool = host(pool)
     stats = {}
     nfull = host(lens) // 128
@@ -33,7 +35,8 @@ def _check_prefill(w, lens, table, num_pages, iters=2, k=None, v=None, rms=False
             page = int(table[b, j])
             for h in range(w.hkv):
                 parity.compare_record(got_pool[page, h], ref["pool"][page, h],
-                                      ref["u_k"][b, j, h], ref["u_v"][b, j, h], stats)
+                                      ref["u_k"][b, j, h], ref["u_v"][b, j, h], stats, meta16=m16,
+                                      ref32=ref32["pool"][page, h] if m16 else None)
     parity.check_flip_rate(stats)
     _check_prefill.last = (pool, tk, tv, cfg)
     # leftover tokens copied verbatim into the tails
@@ -190,3 +193,18 @@ def test_bad_page_sets_status_and_skips():
                                  max_seq=256)
     torch.cuda.synchronize()
     assert int(status.item()) & 2          # KVARN_STATUS_BAD_LENGTH
+
+
+@pytest.mark.parametrize("rms", [False, True])
+def test_m16_variant(rms):
+    # format variant "_m16" (fp16 metadata, 13824-byte records): the same
+    # codes as the fp32 format, the metadata rounded once more to fp16; ragged
+    # lengths on permuted pages
+    w = synth.scaled(synth.WORKLOADS["llama3_8b_layer"], batch=3, seq=1100, hkv=2, hq=8)
+    lens = torch.tensor([1100, 300, 640], dtype=torch.int32)
+    g = torch.Generator().manual_seed(71)
+    table = torch.randperm(3 * 9, generator=g).to(torch.int32).reshape(3, 9)
+    stats = _check_prefill(w, lens, table, 27, rms=rms, m16=True)
+    assert stats["k_codes"] == (8 + 2 + 5) * 2 * 128 * 128
+    pool = _check_prefill.last[0]
+    assert pool.shape[-1] == 13824
