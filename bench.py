@@ -414,7 +414,9 @@ def run_gpu(args, rank, world):
     # the chunked-prefill kernel on its own workload (not part of the step)
     chunk = measure_chunk(args, dev, stream) if not args.no_chunk else None
     snap = measure_snapkv(args, dev, stream) if not args.no_chunk else None
-    return units[:per_step], ms, ms_step, ms_fused, wall, clocks, e2e, ms_cold, nu, chunk, snap
+    variants = measure_variants(args, dev, stream) if not args.no_chunk else None
+    return (units[:per_step], ms, ms_step, ms_fused, wall, clocks, e2e, ms_cold, nu, chunk, snap,
+            variants)
 
 
 def measured_tensor_peak():
@@ -483,6 +485,74 @@ def measure_chunk(args, dev, stream):
             "roofline": {"bound": "tensor", "achieved": tflops, "peak": peak,
                          "peak_kind": f"{kind} bf16_tflops (burst; fp16 runs at the bf16 rate)",
                          "unit": "TFLOP/s", "frac": tflops / peak, "traffic": None}}
+
+
+def measure_variants(args, dev, stream):
+    """The format variants on the Llama-3-8B-like layer (16 x 4096 tokens, 8 KV
+    heads, 32 query heads), three rotated replicas: "_m16" (fp16 metadata,
+    108 B per token-head: quantize and decode) and "_rms" (the uncentred
+    Sinkhorn statistic: quantize; its records decode like the default's).
+    Algorithmic bytes as for the default format, with the record size of the
+    variant."""
+    import quantized_decode_attention_blocks_b300 as kv
+    w = synth.WORKLOADS["llama3_8b_layer"]
+    out = {}
+    peak, kind = measured_peaks()
+    for fmt, rec, do_decode in (("k4v2_g128_m16", 13824, True), ("k4v2_g128_rms", REC, False)):
+        cfg = kv.config_from_string(fmt, w.hq, w.hkv)
+        reps = []
+        for r in range(3):
+            wr = synth.scaled(w, seed=w.seed + 1000 * r)
+            k, v = synth.kv(wr, device=dev)
+            lens = synth.seq_lens(wr, device=dev)
+            tables, n = synth.block_tables(wr, device=dev)
+            pool = kv.alloc_pool(cfg, n, dev)
+            tk, tv = kv.alloc_tails(cfg, w.batch, dev)
+            q = synth.queries(wr, device=dev)
+            reps.append(dict(k=k, v=v, lens=lens, table=tables[0].contiguous(), pool=pool, tk=tk,
+                             tv=tv, q=q, out=torch.empty((w.batch, w.hq, D), dtype=torch.float16,
+                                                         device=dev),
+                             ws=kv.alloc_decode_workspace(cfg, w.batch, w.seq, dev),
+                             st=torch.zeros(1, dtype=torch.int32, device=dev)))
+
+        def quant(i):
+            r = reps[i % 3]
+            kv.kvarn_quantize_blocks(cfg, r["k"], r["v"], r["lens"], w.seq, r["table"], r["pool"],
+                                     r["tk"], r["tv"], r["st"])
+
+        def dec(i):
+            r = reps[i % 3]
+            kv.kvarn_decode_attention(cfg, r["q"], r["pool"], r["table"], r["lens"], w.seq,
+                                      r["tk"], r["tv"], r["out"], r["ws"], status=r["st"])
+
+        for i in range(max(args.warmup, 3)):
+            quant(i)
+            dec(i)
+        torch.cuda.synchronize()
+        n = max(6, min(args.steps, 24))
+        ms_q = time_graph(quant, n, stream) / n
+        ms_d = time_graph(dec, n, stream) / n if do_decode else None
+        for r in reps:
+            if int(r["st"].item()) != 0:
+                raise RuntimeError(f"{fmt} status {int(r['st'].item())}")
+        lens = reps[0]["lens"].cpu().numpy().astype(np.int64)
+        full = int((lens // T).sum()) * T * w.hkv
+        bq = full * (FP16_TOKEN_HEAD + rec // T) + int((lens % T).sum()) * w.hkv * 2 * FP16_TOKEN_HEAD
+        e = {"record_bytes": rec, "bytes_per_token_head": rec // T,
+             "quantize_us": ms_q * 1e3, "quantize_gbs": bq / (ms_q * 1e-3) / 1e9,
+             "quantize_frac_of_hbm": bq / (ms_q * 1e-3) / 1e9 / peak}
+        if do_decode:
+            bd = int((lens // T).sum()) * w.hkv * rec + int((lens % T).sum()) * w.hkv * \
+                FP16_TOKEN_HEAD + 2 * w.batch * w.hq * D * 2
+            e.update(decode_us=ms_d * 1e3, decode_gbs=bd / (ms_d * 1e-3) / 1e9,
+                     decode_frac_of_hbm=bd / (ms_d * 1e-3) / 1e9 / peak)
+        out[fmt] = e
+        del reps
+        torch.cuda.empty_cache()
+    out["workload"] = ("llama3_8b_layer: 16 x 4096 tokens, 8 KV heads, 32 query heads, three "
+                       "rotated replicas")
+    out["peak"] = f"{peak} GB/s, {kind} hbm_gbs (burst copy)"
+    return out
 
 
 def measure_snapkv(args, dev, stream):
@@ -674,7 +744,7 @@ def main():
                          "(default: enough to keep the working set above L2; counter "
                          "captures under ncu use 1)")
     ap.add_argument("--no-chunk", action="store_true",
-                    help="skip the chunked-prefill and SnapKV lines")
+                    help="skip the chunked-prefill, SnapKV and format-variant lines")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
@@ -686,8 +756,8 @@ def main():
         return 0
     if world > 1:
         torch.distributed.init_process_group("nccl")
-    units, ms, ms_step, ms_fused, wall, clocks, e2e, ms_cold, nu, chunk, snap = run_gpu(
-        args, rank, world)
+    (units, ms, ms_step, ms_fused, wall, clocks, e2e, ms_cold, nu, chunk, snap,
+     variants) = run_gpu(args, rank, world)
     if world > 1:
         torch.distributed.destroy_process_group()
     if rank != 0:
@@ -768,6 +838,7 @@ def main():
         "e2e": e2e,
         "chunk_prefill": chunk,
         "snapkv": snap,
+        "format_variants": variants,
         "gpu_launches": LAUNCHES_PER_STEP * L * args.steps,
         "clocks": clocks,
         "wall_s_timed_region": wall,
