@@ -75,6 +75,20 @@
  *   [8960, 13056)  V codes (the same permutation)
  *   [13056,13568)  V per-token {s', z'} fp16 pairs
  *   [13568,13824)  V per-channel c_d fp16
+ *
+ * Format variant "_pc" (per-channel grouping; SURVEY's "per-channel
+ * grouping"): after the same rotation and normalization, one RTN group is
+ * one channel's 128 tokens of the tile, so s_d, z_d are per channel and the
+ * row scale r_t cannot be folded into them; it is stored per token.  With
+ * x_td = Y_td / (r_t c_d): z_d = min_t x_td, s_d = (max_t - min_t) / (2^b - 1),
+ * q = rint((x - z_d) / s_d), and yhat_td = r_t (cs_d q_td + cz_d) with
+ * cs_d = fp32(c_d s_d), cz_d = fp32(c_d z_d).  Record of 15360 bytes:
+ *   [0,     8192)  K codes (as above)
+ *   [8192,  8704)  K per-token r_t fp32
+ *   [8704,  9728)  K per-channel {cs_d, cz_d} fp32 pairs
+ *   [9728, 13824)  V codes (the same permutation)
+ *   [13824,14336)  V per-token r_t fp32
+ *   [14336,15360)  V per-channel {cs_d, cz_d} fp32 pairs
  */
 #include <math.h>
 #include <stdint.h>
@@ -98,20 +112,25 @@ typedef struct {
     int msz;   /* bytes of one stored metadata value: 4 (fp32) or 2 (fp16) */
 } rec_layout;
 
-static rec_layout layout_of(int meta16)
+/* fmt: 0 = fp32 metadata, 1 = "_m16" (fp16 metadata), 2 = "_pc" (per-channel
+ * groups; ksz / vsz hold r_t, kc / vc the {cs, cz} pairs) */
+static rec_layout layout_of(int fmt)
 {
     rec_layout L;
-    if (!meta16) {
-        L.rec = REC_BYTES; L.kcodes = OFF_KCODES; L.ksz = OFF_KSZ; L.kc = OFF_KC;
-        L.vcodes = OFF_VCODES; L.vsz = OFF_VSZ; L.vc = OFF_VC; L.msz = 4;
-    } else {
+    if (fmt == 1) {
         L.rec = REC_BYTES_M16; L.kcodes = 0; L.ksz = 8192; L.kc = 8704;
         L.vcodes = 8960; L.vsz = 13056; L.vc = 13568; L.msz = 2;
+    } else if (fmt == 2) {
+        L.rec = REC_BYTES; L.kcodes = 0; L.ksz = 8192; L.kc = 8704;
+        L.vcodes = 9728; L.vsz = 13824; L.vc = 14336; L.msz = 4;
+    } else {
+        L.rec = REC_BYTES; L.kcodes = OFF_KCODES; L.ksz = OFF_KSZ; L.kc = OFF_KC;
+        L.vcodes = OFF_VCODES; L.vsz = OFF_VSZ; L.vc = OFF_VC; L.msz = 4;
     }
     return L;
 }
 
-long kvref_record_bytes(int meta16) { return layout_of(meta16).rec; }
+long kvref_record_bytes(int fmt) { return layout_of(fmt).rec; }
 
 /* ------------------------------------------------------------------ */
 /* fp16 <-> double, written out from the IEEE-754 binary16 definition */
@@ -348,6 +367,42 @@ void kvref_rtn(const double *Y, const double *r, const float *c32, int bits,
     }
 }
 
+/* Format "_pc": RTN with one group per channel (over the 128 tokens of the
+ * tile).  Outputs the codes, r32_t = fp32(r_t), and per channel
+ * cs32_d = fp32(c_d s_d), cz32_d = fp32(c_d z_d); u as in kvref_rtn. */
+void kvref_rtn_pc(const double *Y, const double *r, const float *c32, int bits, uint8_t *q,
+                  float *r32, float *cs32, float *cz32, double *u)
+{
+    int t, d;
+    int qmax = (1 << bits) - 1;
+    for (t = 0; t < NTOK; ++t) r32[t] = (float)r[t];
+    for (d = 0; d < NCH; ++d) {
+        double mn = INFINITY, mx = -INFINITY, s, z;
+        for (t = 0; t < NTOK; ++t) {
+            double x = Y[t * NCH + d] / (r[t] * (double)c32[d]);
+            if (x < mn) mn = x;
+            if (x > mx) mx = x;
+        }
+        z = mn;
+        s = (mx - mn) / qmax;
+        cs32[d] = (float)((double)c32[d] * s);
+        cz32[d] = (float)((double)c32[d] * z);
+        for (t = 0; t < NTOK; ++t) {
+            double x = Y[t * NCH + d] / (r[t] * (double)c32[d]);
+            double ud = 0.0;
+            long qi = 0;
+            if (s > 0.0) {
+                ud = (x - z) / s;
+                qi = (long)nearbyint(ud);          /* ties to even */
+                if (qi < 0) qi = 0;
+                if (qi > qmax) qi = qmax;
+            }
+            q[t * NCH + d] = (uint8_t)qi;
+            if (u) u[t * NCH + d] = ud;
+        }
+    }
+}
+
 /* ------------------------------------------------------------------ */
 /* Packing into a page record                                          */
 /* ------------------------------------------------------------------ */
@@ -456,16 +511,59 @@ void kvref_unpack_part(const uint8_t *rec, int is_v, uint8_t *q, float *s32, flo
     kvref_unpack_part_fmt(rec, is_v, q, s32, z32, c32, 0);
 }
 
-/* Dequantized rotated tile yhat_td = c_d (s'_t q_td + z'_t), from a record. */
-void kvref_dequant_part_fmt(const uint8_t *rec, int is_v, int meta16, double *yhat)
+/* Format "_pc": codes as in the other formats, r_t per token, {cs_d, cz_d}
+ * per channel. */
+void kvref_pack_part_pc(uint8_t *rec, int is_v, const uint8_t *q, const float *r32,
+                        const float *cs32, const float *cz32)
 {
-    uint8_t q[NTOK * NCH];
+    rec_layout L = layout_of(2);
+    long rr = is_v ? L.vsz : L.ksz, cc = is_v ? L.vc : L.kc;
+    float zero[NTOK];
+    int t, d;
+    memset(zero, 0, sizeof(zero));
+    /* the codes: the shared packer, metadata overwritten below */
+    kvref_pack_part_fmt(rec, is_v, q, zero, zero, zero, 0);
+    for (t = 0; t < NTOK; ++t) put_f32(rec + rr + 4 * t, r32[t]);
+    for (d = 0; d < NCH; ++d) {
+        put_f32(rec + cc + 8 * d, cs32[d]);
+        put_f32(rec + cc + 8 * d + 4, cz32[d]);
+    }
+}
+
+void kvref_unpack_part_pc(const uint8_t *rec, int is_v, uint8_t *q, float *r32, float *cs32,
+                          float *cz32)
+{
+    rec_layout L = layout_of(2);
+    long rr = is_v ? L.vsz : L.ksz, cc = is_v ? L.vc : L.kc;
     float s32[NTOK], z32[NTOK], c32[NCH];
     int t, d;
-    kvref_unpack_part_fmt(rec, is_v, q, s32, z32, c32, meta16);
+    kvref_unpack_part_fmt(rec, is_v, q, s32, z32, c32, 0);   /* the codes */
+    for (t = 0; t < NTOK; ++t) r32[t] = get_f32(rec + rr + 4 * t);
+    for (d = 0; d < NCH; ++d) {
+        cs32[d] = get_f32(rec + cc + 8 * d);
+        cz32[d] = get_f32(rec + cc + 8 * d + 4);
+    }
+}
+
+/* Dequantized rotated tile from a record: yhat_td = c_d (s'_t q_td + z'_t), or
+ * for "_pc" yhat_td = r_t (cs_d q_td + cz_d). */
+void kvref_dequant_part_fmt(const uint8_t *rec, int is_v, int fmt, double *yhat)
+{
+    uint8_t q[NTOK * NCH];
+    float a32[NTOK], b32[NTOK > NCH ? NTOK : NCH], c32[NCH];
+    int t, d;
+    if (fmt == 2) {
+        kvref_unpack_part_pc(rec, is_v, q, a32, b32, c32);
+        for (t = 0; t < NTOK; ++t)
+            for (d = 0; d < NCH; ++d)
+                yhat[t * NCH + d] =
+                    (double)a32[t] * ((double)b32[d] * q[t * NCH + d] + (double)c32[d]);
+        return;
+    }
+    kvref_unpack_part_fmt(rec, is_v, q, a32, b32, c32, fmt);
     for (t = 0; t < NTOK; ++t)
         for (d = 0; d < NCH; ++d)
-            yhat[t * NCH + d] = (double)c32[d] * ((double)s32[t] * q[t * NCH + d] + (double)z32[t]);
+            yhat[t * NCH + d] = (double)c32[d] * ((double)a32[t] * q[t * NCH + d] + (double)b32[t]);
 }
 
 void kvref_dequant_part(const uint8_t *rec, int is_v, double *yhat)
@@ -482,7 +580,7 @@ void kvref_dequant_part(const uint8_t *rec, int is_v, double *yhat)
  * optional outputs expose every intermediate for the tests:
  * Y (rotated), a, b (log scales), q (codes), u (pre-rounding values). */
 void kvref_quantize_tile_fmt(const uint16_t *x, long ld_tok, int is_v, int iters, int stat,
-                             int meta16, uint8_t *rec, double *Y_out, double *a_out,
+                             int fmt, uint8_t *rec, double *Y_out, double *a_out,
                              double *b_out, uint8_t *q_out, double *u_out)
 {
     static double H[NCH * NCH];
@@ -503,8 +601,14 @@ void kvref_quantize_tile_fmt(const uint16_t *x, long ld_tok, int is_v, int iters
     kvref_sinkhorn_stat(Y, iters, stat, a, b, NULL);
     for (t = 0; t < NTOK; ++t) r[t] = exp(a[t]);
     for (d = 0; d < NCH; ++d) c32[d] = (float)exp(b[d]);
-    kvref_rtn(Y, r, c32, bits, q, s32, z32, u_out);
-    if (rec) kvref_pack_part_fmt(rec, is_v, q, s32, z32, c32, meta16);
+    if (fmt == 2) {
+        float r32[NTOK], cs32[NCH], cz32[NCH];
+        kvref_rtn_pc(Y, r, c32, bits, q, r32, cs32, cz32, u_out);
+        if (rec) kvref_pack_part_pc(rec, is_v, q, r32, cs32, cz32);
+    } else {
+        kvref_rtn(Y, r, c32, bits, q, s32, z32, u_out);
+        if (rec) kvref_pack_part_fmt(rec, is_v, q, s32, z32, c32, fmt);
+    }
     if (Y_out) memcpy(Y_out, Y, sizeof(double) * NTOK * NCH);
     if (a_out) memcpy(a_out, a, sizeof(a));
     if (b_out) memcpy(b_out, b, sizeof(b));
@@ -539,12 +643,12 @@ void kvref_quantize_tile(const uint16_t *x, long ld_tok, int is_v, int iters, ui
  * boundary rule.  Returns 0, or -1 on a page id outside [0, num_pages). */
 int kvref_quantize_blocks_fmt(const uint16_t *k, const uint16_t *v, long sb, long st, long sh,
                               int B, const int32_t *seq_lens, const int32_t *block_table,
-                              int max_blocks, int hkv, int iters, int stat, int meta16,
+                              int max_blocks, int hkv, int iters, int stat, int fmt,
                               uint8_t *pool, long num_pages, uint16_t *tail_k, uint16_t *tail_v,
                               double *u_k, double *u_v)
 {
     int bad = 0;
-    const long rec_bytes = layout_of(meta16).rec;
+    const long rec_bytes = layout_of(fmt).rec;
     long item, n_items = (long)B * max_blocks * hkv;
 #pragma omp parallel for schedule(dynamic, 4) reduction(| : bad)
     for (item = 0; item < n_items; ++item) {
@@ -560,9 +664,9 @@ int kvref_quantize_blocks_fmt(const uint16_t *k, const uint16_t *v, long sb, lon
         if (page < 0 || page >= num_pages) { bad = 1; continue; }
         rec = pool + (page * hkv + h) * rec_bytes;
         kvref_quantize_tile_fmt(k + b * sb + (long)j * NTOK * st + h * sh, st, 0, iters, stat,
-                                meta16, rec, NULL, NULL, NULL, NULL, u_k ? u_k + uoff : NULL);
+                                fmt, rec, NULL, NULL, NULL, NULL, u_k ? u_k + uoff : NULL);
         kvref_quantize_tile_fmt(v + b * sb + (long)j * NTOK * st + h * sh, st, 1, iters, stat,
-                                meta16, rec, NULL, NULL, NULL, NULL, u_v ? u_v + uoff : NULL);
+                                fmt, rec, NULL, NULL, NULL, NULL, u_v ? u_v + uoff : NULL);
     }
     {
         int b, h, s, d;
@@ -607,11 +711,11 @@ int kvref_quantize_blocks(const uint16_t *k, const uint16_t *v, long sb, long st
  * into page block_table[b][pos / 128].  pos < 0 marks an idle slot. */
 int kvref_append_token_fmt(const uint16_t *k_new, const uint16_t *v_new, const int32_t *pos,
                            int B, const int32_t *block_table, int max_blocks, int hkv,
-                           int iters, int stat, int meta16, uint8_t *pool, long num_pages,
+                           int iters, int stat, int fmt, uint8_t *pool, long num_pages,
                            uint16_t *tail_k, uint16_t *tail_v)
 {
     int b, bad = 0;
-    const long rec_bytes = layout_of(meta16).rec;
+    const long rec_bytes = layout_of(fmt).rec;
     for (b = 0; b < B; ++b) {
         int p = pos[b], h, d, slot;
         if (p < 0) continue;
@@ -633,9 +737,9 @@ int kvref_append_token_fmt(const uint16_t *k_new, const uint16_t *v_new, const i
                 uint8_t *rec = pool + (page * hkv + h) * rec_bytes;
                 const uint16_t *tk = tail_k + ((long)b * hkv + h) * NTOK * NCH;
                 const uint16_t *tv = tail_v + ((long)b * hkv + h) * NTOK * NCH;
-                kvref_quantize_tile_fmt(tk, NCH, 0, iters, stat, meta16, rec, NULL, NULL, NULL,
+                kvref_quantize_tile_fmt(tk, NCH, 0, iters, stat, fmt, rec, NULL, NULL, NULL,
                                         NULL, NULL);
-                kvref_quantize_tile_fmt(tv, NCH, 1, iters, stat, meta16, rec, NULL, NULL, NULL,
+                kvref_quantize_tile_fmt(tv, NCH, 1, iters, stat, fmt, rec, NULL, NULL, NULL,
                                         NULL, NULL);
             }
         }
@@ -677,9 +781,9 @@ int kvref_decode_attention_fmt(const uint16_t *q, const uint8_t *pool, long num_
                                const int32_t *block_table, int max_blocks,
                                const int32_t *seq_lens, int B, int hq, int hkv,
                                const uint16_t *tail_k, const uint16_t *tail_v, double scale,
-                               int route, int meta16, double *out)
+                               int route, int fmt, double *out)
 {
-    const long rec_bytes = layout_of(meta16).rec;
+    const long rec_bytes = layout_of(fmt).rec;
     static double H[NCH * NCH];
     static int have_h = 0;
     int bad = 0;
@@ -712,7 +816,7 @@ int kvref_decode_attention_fmt(const uint16_t *q, const uint8_t *pool, long num_
         for (j = 0; j < nfull; ++j) {
             long page = block_table[(long)b * max_blocks + j];
             if (page < 0 || page >= num_pages) { pagebad = 1; break; }
-            kvref_dequant_part_fmt(pool + (page * hkv + kvh) * rec_bytes, 0, meta16, yk);
+            kvref_dequant_part_fmt(pool + (page * hkv + kvh) * rec_bytes, 0, fmt, yk);
             for (t = 0; t < NTOK; ++t) {
                 double s = 0.0;
                 if (route == 0) {
@@ -746,7 +850,7 @@ int kvref_decode_attention_fmt(const uint16_t *q, const uint8_t *pool, long num_
         for (d = 0; d < NCH; ++d) { acc[d] = 0.0; acc_tail[d] = 0.0; }
         for (j = 0; j < nfull; ++j) {
             long page = block_table[(long)b * max_blocks + j];
-            kvref_dequant_part_fmt(pool + (page * hkv + kvh) * rec_bytes, 1, meta16, yv);
+            kvref_dequant_part_fmt(pool + (page * hkv + kvh) * rec_bytes, 1, fmt, yv);
             for (t = 0; t < NTOK; ++t) {
                 double p = scores[j * NTOK + t];
                 if (route == 0) {

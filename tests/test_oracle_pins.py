@@ -988,3 +988,111 @@ def test_m16_append_fills_page_like_prefill(oracle):
                                  st["tail_k"], st["tail_v"], meta16=True)
         assert rc == 0
     assert np.array_equal(st["pool"], ref["pool"])
+
+
+# ---------------------------------------- format variant: per-channel groups --
+# Format variant "_pc" (SURVEY's "per-channel grouping"): after the same
+# rotation and normalization, one RTN group is one channel's 128 tokens; the
+# row scale r_t is stored per token and c_d folds into the per-channel scale
+# and zero (yhat_td = r_t (cs_d q_td + cz_d)).  The KVarN page (blog.edumints.com,
+# "KVarN Nasil Calisir?", stage "Kuantize Edilmis Onbellek") fixes per-token
+# groups; the variant is a reading.
+
+def test_pc_rtn_is_the_per_token_rtn_of_the_transposed_tile(oracle):
+    # with r exactly representable in fp32, swapping the roles of tokens and
+    # channels (and of r and c) turns per-channel groups into per-token ones:
+    # the same x_td, so the same codes and the same scale and zero products
+    rng = np.random.default_rng(51)
+    Y = rng.standard_normal((128, 128)) * np.exp(rng.standard_normal(128))[None, :]
+    r = np.exp(rng.standard_normal(128)).astype(np.float32).astype(np.float64)
+    c32 = np.exp(0.5 * rng.standard_normal(128)).astype(np.float32)
+    for bits in (4, 2):
+        q, r32, cs, cz, u = oracle.rtn_pc(Y, r, c32, bits)
+        qt, st, zt, ut = oracle.rtn(Y.T.copy(), c32.astype(np.float64), r.astype(np.float32), bits)
+        assert np.array_equal(q, qt.T) and np.array_equal(u, ut.T)
+        assert np.array_equal(cs, st) and np.array_equal(cz, zt)
+        assert np.array_equal(r32, r.astype(np.float32))
+
+
+def test_pc_rtn_half_step_bound_and_endpoints(oracle):
+    x = _tile(52)
+    for is_v, bits in ((False, 4), (True, 2)):
+        out = oracle.quantize_tile(x, is_v, 2, pc=True)
+        q, r, cs, cz = oracle.unpack_part_pc(out["rec"], is_v)
+        yhat = oracle.dequant_part(out["rec"], is_v, pc=True)
+        r64, cs64 = r.astype(np.float64), cs.astype(np.float64)
+        half = 0.5 * np.abs(r64)[:, None] * np.abs(cs64)[None, :]
+        slack = 1e-6 * (np.abs(out["Y"]) + np.abs(yhat)) + 1e-9
+        assert np.all(np.abs(out["Y"] - yhat) <= half + slack)
+        # every channel uses both ends of its range
+        assert np.all(q.min(axis=0) == 0) and np.all(q.max(axis=0) == 2 ** bits - 1)
+
+
+def test_pc_record_bytes_at_the_stated_offsets(oracle):
+    x = _tile(53)
+    for is_v, qmax in ((False, 15), (True, 3)):
+        out = oracle.quantize_tile(x, is_v, 2, pc=True)
+        rec = out["rec"]
+        assert rec.size == 15360
+        codes = (9728, 13824) if is_v else (0, 8192)
+        rr = rec[(13824 if is_v else 8192):(14336 if is_v else 8704)].view(np.float32)
+        pairs = rec[(14336 if is_v else 8704):(15360 if is_v else 9728)].view(np.float32)
+        pairs = pairs.reshape(128, 2)
+        a = np.exp(out["a"])
+        c32 = np.exp(out["b"]).astype(np.float32)
+        assert np.array_equal(rr, a.astype(np.float32))                 # r_t = e^{a_t}
+        # the code region is the shared packer's output for these codes
+        rec_q = np.zeros(15360, np.uint8)
+        oracle.pack_part(rec_q, is_v, out["q"], np.zeros(128, np.float32),
+                         np.zeros(128, np.float32), np.zeros(128, np.float32))
+        assert np.array_equal(rec[codes[0]:codes[1]], rec_q[codes[0]:codes[1]])
+        # {cs_d, cz_d} = c_d times the channel's step and minimum
+        xd = out["Y"] / (a[:, None] * c32.astype(np.float64)[None, :])
+        step = (xd.max(axis=0) - xd.min(axis=0)) / qmax
+        assert np.allclose(pairs[:, 0] / c32, step, rtol=1e-6)
+        assert np.allclose(pairs[:, 1] / c32, xd.min(axis=0), rtol=1e-6, atol=1e-12)
+
+
+def test_pc_attention_matches_torch_sdpa_on_dequantized_cache(oracle):
+    w = synth.scaled(synth.WORKLOADS["llama3_8b_layer"], batch=2, seq=517, hkv=2, hq=4, seed=54)
+    k, v = synth.kv(w)
+    k, v = k.numpy(), v.numpy()
+    lens = np.array([300, 517], np.int32)
+    table = np.array([[5, 1, 3, 7, 0], [2, 6, 4, 8, 9]], np.int32)
+    st = oracle.quantize_blocks(k, v, lens, table, 10, 2, pc=True)
+    assert st["rc"] == 0
+    q = synth.queries(w).numpy()
+    o1 = oracle.decode_attention(q, st["pool"], table, lens, st["tail_k"], st["tail_v"], 4, 2,
+                                 pc=True)
+    o0 = oracle.decode_attention(q, st["pool"], table, lens, st["tail_k"], st["tail_v"], 4, 2,
+                                 route=0, pc=True)
+    assert np.abs(o0 - o1).max() <= 1e-12 * np.abs(o0).max()
+    H = torch.tensor(oracle.hadamard(128))
+    for b in range(2):
+        n = int(lens[b])
+        nfull = n // 128
+        for h in range(4):
+            keys, vals = [], []
+            for j in range(nfull):
+                rec = st["pool"][table[b, j], h // 2]
+                keys.append(torch.tensor(oracle.dequant_part(rec, False, pc=True)) @ H)
+                vals.append(torch.tensor(oracle.dequant_part(rec, True, pc=True)) @ H)
+            keys.append(torch.tensor(k[b, nfull * 128:n, h // 2].astype(np.float64)))
+            vals.append(torch.tensor(v[b, nfull * 128:n, h // 2].astype(np.float64)))
+            ref = torch.nn.functional.scaled_dot_product_attention(
+                torch.tensor(q[b, h].astype(np.float64))[None, None, None],
+                torch.cat(keys)[None, None], torch.cat(vals)[None, None])[0, 0, 0].numpy()
+            assert np.abs(o1[b, h] - ref).max() <= 1e-12 * max(1.0, np.abs(ref).max())
+
+
+def test_pc_append_fills_page_like_prefill(oracle):
+    w = synth.scaled(synth.WORKLOADS["llama3_8b_layer"], batch=1, seq=256, hkv=2, hq=4, seed=55)
+    k, v = synth.kv(w)
+    k, v = k.numpy(), v.numpy()
+    table = np.array([[1, 0]], np.int32)
+    ref = oracle.quantize_blocks(k, v, np.array([256], np.int32), table, 2, 2, pc=True)
+    st = oracle.quantize_blocks(k, v, np.array([250], np.int32), table, 2, 2, pc=True)
+    for t in range(250, 256):
+        assert oracle.append_token(k[:, t], v[:, t], np.array([t], np.int32), table, 2,
+                                   st["pool"], st["tail_k"], st["tail_v"], pc=True) == 0
+    assert np.array_equal(st["pool"], ref["pool"])
