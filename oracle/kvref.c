@@ -206,18 +206,25 @@ void kvref_hadamard(int n, double *H)
     for (i = 0; i < n * n; ++i) H[i] /= sqrt((double)n);
 }
 
-/* Y = X H^T as an explicit matrix product: y_t = H x_t for every token row.
+/* Y = X H^T, y_t = H x_t for every token row, as an explicit matrix product
+ * taken in two exact-then-rounded steps: each row of H is (+-1) / sqrt(n), so
+ * y_td = (sum_j sign(H_dj) x_tj) / sqrt(n).  The signed sum of fp16 inputs is
+ * exact in float64 (every fp16 value is a multiple of 2^-24 below 2^16, so
+ * any sum of 128 of them fits in 53 bits); the division rounds once.  A
+ * rotated value that is zero in exact arithmetic is therefore exactly zero
+ * here, which the skip rules of the normalization rely on.
  * x: NTOK x NCH fp16 bit patterns, token t at x + t * ld_tok.  Y: NTOK x NCH. */
 void kvref_rotate_tile(const uint16_t *x, long ld_tok, const double *H, double *Y)
 {
     int t, d, j;
     double xt[NCH];
+    const double root = sqrt((double)NCH);
     for (t = 0; t < NTOK; ++t) {
         for (j = 0; j < NCH; ++j) xt[j] = kvref_half_to_double(x[t * ld_tok + j]);
         for (d = 0; d < NCH; ++d) {
             double acc = 0.0;
-            for (j = 0; j < NCH; ++j) acc += H[d * NCH + j] * xt[j];
-            Y[t * NCH + d] = acc;
+            for (j = 0; j < NCH; ++j) acc += H[d * NCH + j] > 0.0 ? xt[j] : -xt[j];
+            Y[t * NCH + d] = acc / root;
         }
     }
 }

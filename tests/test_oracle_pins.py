@@ -1096,3 +1096,25 @@ def test_pc_append_fills_page_like_prefill(oracle):
         assert oracle.append_token(k[:, t], v[:, t], np.array([t], np.int32), table, 2,
                                    st["pool"], st["tail_k"], st["tail_v"], pc=True) == 0
     assert np.array_equal(st["pool"], ref["pool"])
+
+
+def test_rotation_of_a_constant_tile_is_exact(oracle):
+    # H x for a constant x is (sqrt(128) x0, 0, ..., 0): the zero channels
+    # must come out exactly zero, since the skip rules of the normalization
+    # (and the "_rms" rule above all: only all-zero columns are skipped) act
+    # on exact zeros
+    for v in (1.5, -0.3, 65504.0):
+        Y = oracle.rotate_tile(np.full((128, 128), v, np.float16))
+        assert np.all(Y[:, 1:] == 0.0)
+        assert np.allclose(Y[:, 0], np.sqrt(128.0) * np.float64(np.float16(v)), rtol=1e-15)
+
+
+def test_rms_variant_constant_tile_closed_form(oracle):
+    # y_t = (v sqrt(128), 0, ...): row 1 gives r = |v|, column 1 c_0 = sqrt(128)
+    # (the zero columns are skipped), row 2 r = |v| / sqrt(128), column 2
+    # c_0 = 128
+    for v in (1.5, -2.0):
+        Y = oracle.rotate_tile(np.full((128, 128), v, np.float16))
+        a, b, _ = oracle.sinkhorn(Y, 2, rms=True)
+        assert np.allclose(np.exp(a), abs(v) / np.sqrt(128.0), rtol=1e-12)
+        assert np.isclose(np.exp(b[0]), 128.0, rtol=1e-12) and np.all(b[1:] == 0.0)
