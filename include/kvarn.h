@@ -52,6 +52,18 @@
  *   [8960, 13056) V codes (the same permutation)
  *   [13056,13568) V {s', z'} fp16 per token
  *   [13568,13824) V column scale c_d fp16
+ * Format variant "_pc" (config per_channel = 1; fp32 metadata, 15360 bytes):
+ * after the same rotation and normalization, one RTN group is one channel's
+ * 128 tokens of the tile, so the row scale r_t is stored per token and c_d
+ * folds into the per-channel scale and zero: with x_td = Y_td / (r_t c_d),
+ * z_d = min_t x_td, s_d = (max_t - min_t) / (2^bits - 1), and
+ * yhat_td = r_t * (cs_d * q_td + cz_d), cs_d = c_d s_d, cz_d = c_d z_d:
+ *   [0,     8192) K codes (as above)
+ *   [8192,  8704) K r_t fp32 per token
+ *   [8704,  9728) K {cs_d, cz_d} fp32 per channel
+ *   [9728, 13824) V codes (the same permutation)
+ *   [13824,14336) V r_t fp32 per token
+ *   [14336,15360) V {cs_d, cz_d} fp32 per channel
  * Pool = [num_pages][num_kv_heads][kvarn_page_bytes(cfg)].  The newest len mod 128
  * tokens of a sequence stay fp16 in a caller-owned tail buffer
  * [B][num_kv_heads][128 slots][128] per K and V.
@@ -118,13 +130,15 @@ typedef struct {
                            The page record is the same either way. */
     int meta_fp16;      /* 0: fp32 metadata (default); 1: format variant "_m16",
                            metadata stored as fp16 (KVARN_PAGE_BYTES_M16) */
+    int per_channel;    /* 0: per-token RTN groups (default); 1: format variant
+                           "_pc", per-channel groups (fp32 metadata only) */
 } kvarn_config_t;
 
 /* Fills *out from a format string: "k4v2_g128" or "kvarn_k4v2_g128" (the
  * KVarN page's --kv-cache-dtype value), optionally followed by the variant
- * suffixes "_rms" (the uncentred statistic) and "_m16" (fp16 metadata), each
- * at most once and in either order, and then "_s<K>" to set the Sinkhorn
- * iteration count.  Returns KVARN_ERR_UNSUPPORTED for any other format,
+ * suffixes "_rms" (the uncentred statistic), "_m16" (fp16 metadata) and "_pc"
+ * (per-channel groups; not with "_m16"), each at most once and in any order,
+ * and then "_s<K>" to set the Sinkhorn iteration count.  Returns KVARN_ERR_UNSUPPORTED for any other format,
  * KVARN_ERR_INVALID_ARG for bad head counts or a null pointer. */
 int kvarn_config_from_string(const char *s, int num_q_heads, int num_kv_heads,
                              kvarn_config_t *out);

@@ -81,6 +81,8 @@ int kvarn_config_validate(const kvarn_config_t* c) {
   if (c->sinkhorn_iters < 0 || c->sinkhorn_iters > kMaxIters) return KVARN_ERR_UNSUPPORTED;
   if (c->sinkhorn_rms != 0 && c->sinkhorn_rms != 1) return KVARN_ERR_UNSUPPORTED;
   if (c->meta_fp16 != 0 && c->meta_fp16 != 1) return KVARN_ERR_UNSUPPORTED;
+  if (c->per_channel != 0 && c->per_channel != 1) return KVARN_ERR_UNSUPPORTED;
+  if (c->per_channel && c->meta_fp16) return KVARN_ERR_UNSUPPORTED;   // fp32 metadata only
   return KVARN_OK;
 }
 
@@ -88,7 +90,7 @@ int kvarn_config_from_string(const char* s, int hq, int hkv, kvarn_config_t* out
   if (!s || !out) return KVARN_ERR_INVALID_ARG;
   if (!strncmp(s, "kvarn_", 6)) s += 6;
   if (strncmp(s, "k4v2_g128", 9)) return KVARN_ERR_UNSUPPORTED;
-  int iters = 2, rms = 0, m16 = 0;
+  int iters = 2, rms = 0, m16 = 0, pc = 0;
   const char* rest = s + 9;
   // the variant suffixes, each at most once and in either order, then "_s<K>"
   for (;;) {
@@ -98,6 +100,9 @@ int kvarn_config_from_string(const char* s, int hq, int hkv, kvarn_config_t* out
     } else if (!m16 && !strncmp(rest, "_m16", 4)) {
       m16 = 1;
       rest += 4;
+    } else if (!pc && !strncmp(rest, "_pc", 3) && (rest[3] == 0 || rest[3] == '_')) {
+      pc = 1;
+      rest += 3;
     } else {
       break;
     }
@@ -120,6 +125,7 @@ int kvarn_config_from_string(const char* s, int hq, int hkv, kvarn_config_t* out
   c.sinkhorn_iters = iters;
   c.sinkhorn_rms = rms;
   c.meta_fp16 = m16;
+  c.per_channel = pc;
   c.num_q_heads = hq;
   c.num_kv_heads = hkv;
   const int rc = kvarn_config_validate(&c);
@@ -130,7 +136,7 @@ int kvarn_config_from_string(const char* s, int hq, int hkv, kvarn_config_t* out
 
 size_t kvarn_page_bytes(const kvarn_config_t* c) {
   if (kvarn_config_validate(c) != KVARN_OK) return 0;
-  return c->meta_fp16 ? (size_t)RecFmt<true>::bytes : (size_t)RecFmt<false>::bytes;
+  return c->meta_fp16 ? (size_t)RecFmt<kFmtM16>::bytes : (size_t)RecFmt<kFmtF32>::bytes;
 }
 
 int kvarn_quantize_blocks(const kvarn_config_t* cfg, const void* k, const void* v,
@@ -162,7 +168,7 @@ int kvarn_quantize_blocks(const kvarn_config_t* cfg, const void* k, const void* 
   a.hkv = cfg->num_kv_heads;
   a.iters = cfg->sinkhorn_iters;
   a.rms = cfg->sinkhorn_rms;
-  a.meta16 = cfg->meta_fp16;
+  a.fmt = fmt_of(cfg->meta_fp16, cfg->per_channel);
   a.max_seq = max_seq;
   a.seq_lens = seq_lens;
   a.block_table = block_table;
@@ -199,7 +205,7 @@ int kvarn_append_token(const kvarn_config_t* cfg, const void* k_new, const void*
   a.hkv = cfg->num_kv_heads;
   a.iters = cfg->sinkhorn_iters;
   a.rms = cfg->sinkhorn_rms;
-  a.meta16 = cfg->meta_fp16;
+  a.fmt = fmt_of(cfg->meta_fp16, cfg->per_channel);
   a.block_table = block_table;
   a.max_blocks = max_blocks;
   a.pool = static_cast<uint8_t*>(pool);
@@ -279,7 +285,7 @@ int kvarn_decode_attention(const kvarn_config_t* cfg, const void* q, const void*
   a.pages_per_split = p.pages_per_split;
   a.nsplit = p.nsplit;
   a.cluster = 0;   // the kernel's launcher decides
-  a.meta16 = cfg->meta_fp16;
+  a.fmt = fmt_of(cfg->meta_fp16, cfg->per_channel);
   a.status = status;
   cudaError_t e = decode_mma_supported(a.g) ? launch_decode_mma(a, (cudaStream_t)stream)
                                             : launch_decode_simple(a, (cudaStream_t)stream);
@@ -328,7 +334,7 @@ int kvarn_chunk_attention(const kvarn_config_t* cfg, const void* q, int chunk_ma
   a.tail_v = static_cast<const __half*>(tail_v);
   a.scale_log2 = softmax_scale * 1.4426950408889634f;
   a.out = static_cast<__half*>(out);
-  a.meta16 = cfg->meta_fp16;
+  a.fmt = fmt_of(cfg->meta_fp16, cfg->per_channel);
   a.status = status;
   return launch_chunk_attention(a, (cudaStream_t)stream) == cudaSuccess ? KVARN_OK
                                                                          : KVARN_ERR_LAUNCH;

@@ -152,14 +152,23 @@ __device__ __forceinline__ float code_f(uint32_t q) {   // small integer -> floa
 // row), t0 = lane >> 4; dequant warp dw takes the token pairs p = dw, dw + 3,
 // ... of 64, token 2p + t0.  The code loads hit 32 banks, the column scales
 // of the lane's chunk are loaded once.  rk: the record's K part.
-template <bool M16>
+template <int FMT>
 __device__ __forceinline__ void dequant_k(const uint8_t* rk, uint8_t* kh, uint8_t* kl, int dw,
                                           int lane) {
-  using F = RecFmt<M16>;
+  using F = RecFmt<FMT>;
   const int cc = lane & 15, t0 = lane >> 4;
-  const float4 ca = F::get_c4(rk + F::kc, 2 * cc);
-  const float4 cb = F::get_c4(rk + F::kc, 2 * cc + 1);
+  // beta (c, or cs for the per-channel format) and delta (c, or cz) of the
+  // lane's 8 channels
+  const float4 ca = F::get_b4(rk + F::kc, 2 * cc);
+  const float4 cb = F::get_b4(rk + F::kc, 2 * cc + 1);
   const float cs[8] = {ca.x, ca.y, ca.z, ca.w, cb.x, cb.y, cb.z, cb.w};
+  float cz[8];
+  if constexpr (F::pc) {
+    const float4 za = F::get_d4(rk + F::kc, 2 * cc);
+    const float4 zb = F::get_d4(rk + F::kc, 2 * cc + 1);
+    cz[0] = za.x; cz[1] = za.y; cz[2] = za.z; cz[3] = za.w;
+    cz[4] = zb.x; cz[5] = zb.y; cz[6] = zb.z; cz[7] = zb.w;
+  }
   // four token pairs per step: independent loads and math in flight
   constexpr int kStep = 4 * kDeqWarps;
 #pragma unroll 1
@@ -181,9 +190,15 @@ __device__ __forceinline__ void dequant_k(const uint8_t* rk, uint8_t* kh, uint8_
       for (int k = 0; k < 8; k += 2) {
         const float2 q2 = make_float2(code_f((w[u] >> (4 * k)) & 15u),
                                       code_f((w[u] >> (4 * k + 4)) & 15u));
-        const float2 v = __fmul2_rn(make_float2(cs[k], cs[k + 1]),
-                                    __ffma2_rn(make_float2(sz[u].x, sz[u].x), q2,
-                                               make_float2(sz[u].y, sz[u].y)));
+        float2 v;
+        if constexpr (F::pc)   // r_t (cs_d q + cz_d)
+          v = __fmul2_rn(make_float2(sz[u].x, sz[u].x),
+                         __ffma2_rn(make_float2(cs[k], cs[k + 1]), q2,
+                                    make_float2(cz[k], cz[k + 1])));
+        else                   // c_d (s'_t q + z'_t)
+          v = __fmul2_rn(make_float2(cs[k], cs[k + 1]),
+                         __ffma2_rn(make_float2(sz[u].x, sz[u].x), q2,
+                                    make_float2(sz[u].y, sz[u].y)));
         y[k] = v.x;
         y[k + 1] = v.y;
       }
@@ -198,10 +213,10 @@ __device__ __forceinline__ void dequant_k(const uint8_t* rk, uint8_t* kh, uint8_
 // 128m + 16r + 4j + 2e + h of the permuted V code layout: channel
 // c = 16m + 8e + r, tokens 16k + 8f + 2j + s for k = 4h .. 4h + 3.  The lanes
 // of one store differ in (r, j), i.e. in 32 banks.
-template <int NW, bool M16>
+template <int NW, int FMT>
 __device__ __forceinline__ void dequant_v(const uint8_t* rv, uint8_t* vh, uint8_t* vl, int dw,
                                           int lane) {
-  using F = RecFmt<M16>;
+  using F = RecFmt<FMT>;
   const int j2 = lane & 3, r = lane >> 2;
   const uint8_t* vsz = rv + (F::vsz - F::kpart);
   const uint32_t* words = reinterpret_cast<const uint32_t*>(rv);   // V codes open the V part
@@ -221,16 +236,21 @@ __device__ __forceinline__ void dequant_v(const uint8_t* rv, uint8_t* vh, uint8_
       const int m = k2 >> 1, e = k2 & 1;
       const int c = 16 * m + 8 * e + r;
       const uint32_t w = words[128 * m + 16 * r + 4 * j2 + 2 * e + hb];
-      const float cd = F::get_c(vc, c);
+      const float2 bd = F::get_bd(vc, c);   // (c, c), or (cs, cz) per channel
 #pragma unroll
       for (int kk = 0; kk < 4; ++kk)
 #pragma unroll
         for (int f = 0; f < 2; ++f) {
           const int i0 = 2 * kk + f;   // crumb of s = 0; s = 1 is crumb i0 + 8
-          const float y0 =
-              cd * fmaf(sz[kk][f][0].x, code_f((w >> (2 * i0)) & 3u), sz[kk][f][0].y);
-          const float y1 =
-              cd * fmaf(sz[kk][f][1].x, code_f((w >> (2 * i0 + 16)) & 3u), sz[kk][f][1].y);
+          const float q0 = code_f((w >> (2 * i0)) & 3u), q1 = code_f((w >> (2 * i0 + 16)) & 3u);
+          float y0, y1;
+          if constexpr (F::pc) {   // r_t (cs_d q + cz_d)
+            y0 = sz[kk][f][0].x * fmaf(bd.x, q0, bd.y);
+            y1 = sz[kk][f][1].x * fmaf(bd.x, q1, bd.y);
+          } else {                 // c_d (s'_t q + z'_t)
+            y0 = bd.x * fmaf(sz[kk][f][0].x, q0, sz[kk][f][0].y);
+            y1 = bd.x * fmaf(sz[kk][f][1].x, q1, sz[kk][f][1].y);
+          }
           const int u = 2 * (4 * hb + kk) + f;   // tokens 8u .. 8u + 7; these are 2 j2, 2 j2 + 1
           const uint32_t off =
               (uint32_t)((u >> 3) * kOpBox + c * 128 + (((u & 7) ^ (c & 7)) << 4) + 4 * j2);
@@ -243,11 +263,11 @@ __device__ __forceinline__ void dequant_v(const uint8_t* rv, uint8_t* vh, uint8_
   }
 }
 
-// M16: the "_m16" record (metadata stored as fp16); otherwise fp32.
-template <bool M16>
+// FMT: the record format (RecFmt).
+template <int FMT>
 __global__ void __launch_bounds__(kCThreads, 1)
     chunk_attention_kernel(const ChunkArgs a) {
-  using F = RecFmt<M16>;
+  using F = RecFmt<FMT>;
   extern __shared__ uint8_t smem_raw[];
   CSmem& S = *reinterpret_cast<CSmem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                        ~static_cast<uintptr_t>(1023));
@@ -400,7 +420,7 @@ __global__ void __launch_bounds__(kCThreads, 1)
       // ---- this block's values into V^ ----
       if (page) {
         wait(&S.raw_full[j & 1], (j >> 1) & 1);
-        dequant_v<kSoftWarps, M16>(S.raw[j & 1] + F::kpart, S.vh, S.vl, warp, lane);
+        dequant_v<kSoftWarps, FMT>(S.raw[j & 1] + F::kpart, S.vh, S.vl, warp, lane);
       } else {
         // the fp16 tail, rotated: column t = tid of V^ [channel][token]
         const int t = tid;
@@ -516,7 +536,7 @@ __global__ void __launch_bounds__(kCThreads, 1)
       }
       if (j > 0) wait(&S.sdone[(j - 1) & 1], ((j - 1) >> 1) & 1);   // S of block j-1 read K^
       if (page) {
-        dequant_k<M16>(S.raw[j & 1], S.kh, S.kl, dw, lane);
+        dequant_k<FMT>(S.raw[j & 1], S.kh, S.kl, dw, lane);
       } else {
         // the fp16 tail, rotated into the pages' space: yhat = H x / sqrt(128)
 #pragma unroll 1
@@ -626,14 +646,14 @@ __global__ void __launch_bounds__(kCThreads, 1)
   if (warp == 0) tmem_dealloc(tmem, kCTmemCols);
 }
 
-template <bool M16>
+template <int FMT>
 cudaError_t launch_chunk(const ChunkArgs& args, cudaStream_t s) {
   static std::atomic<uint64_t> smem_set{0};
-  cudaError_t e = ensure_dynamic_smem(chunk_attention_kernel<M16>, kCSmemBytes, smem_set);
+  cudaError_t e = ensure_dynamic_smem(chunk_attention_kernel<FMT>, kCSmemBytes, smem_set);
   if (e != cudaSuccess) return e;
   if (args.ntq <= 0 || args.batch <= 0) return cudaSuccess;
   dim3 grid(args.ntq, args.hkv, args.batch);
-  chunk_attention_kernel<M16><<<grid, kCThreads, kCSmemBytes, s>>>(args);
+  chunk_attention_kernel<FMT><<<grid, kCThreads, kCSmemBytes, s>>>(args);
   return cudaGetLastError();
 }
 
@@ -642,7 +662,9 @@ cudaError_t launch_chunk(const ChunkArgs& args, cudaStream_t s) {
 int chunk_rows_per_tile(int g) { return 128 / g; }
 
 cudaError_t launch_chunk_attention(const ChunkArgs& args, cudaStream_t s) {
-  return args.meta16 ? launch_chunk<true>(args, s) : launch_chunk<false>(args, s);
+  if (args.fmt == kFmtM16) return launch_chunk<kFmtM16>(args, s);
+  if (args.fmt == kFmtPC) return launch_chunk<kFmtPC>(args, s);
+  return launch_chunk<kFmtF32>(args, s);
 }
 
 }  // namespace kvarn

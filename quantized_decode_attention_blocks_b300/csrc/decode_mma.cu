@@ -151,10 +151,13 @@ __device__ __forceinline__ constexpr float vpos_inv(int kb, int f) {
 // Three CTAs per SM for one head tile; for two (groups of 5-8 query heads)
 // the doubled score, probability and accumulator fragments need more than the
 // 168 registers a third CTA would leave, so two CTAs run with no spills.
-// M16: the "_m16" record (metadata stored as fp16); otherwise fp32.
-template <int NT, bool M16>
+// FMT: the record format (RecFmt).  A page token dequantizes as
+// yhat_td = alpha_t beta_d q_td + gamma_t delta_d, so the score is
+// alpha_t sum_d (q~_d beta_d) q_td + gamma_t sum_d q~_d delta_d and the value
+// sum beta_d sum_t (p_t alpha_t) q_td + delta_d sum_t p_t gamma_t.
+template <int NT, int FMT>
 __global__ void __launch_bounds__(kThreads, NT == 1 ? 3 : 2) decode_mma_kernel(DecodeArgs a) {
-  using F = RecFmt<M16>;
+  using F = RecFmt<FMT>;
   extern __shared__ __align__(128) uint8_t smem_raw[];
   MmaSmem<NT>& S = *reinterpret_cast<MmaSmem<NT>*>(smem_raw);
   constexpr int G = 4 * NT;
@@ -306,13 +309,13 @@ __global__ void __launch_bounds__(kThreads, NT == 1 ? 3 : 2) decode_mma_kernel(D
       for (int nt = 0; nt < NT; ++nt) {
         const int h = 4 * nt + (r >> 1);
         const float4* qv = reinterpret_cast<const float4*>(S.qrot[h]);
-        const uint8_t* cv = kst + F::kc;   // c of channels 32 qi + 4k .. : float4 8 qi + k
+        const uint8_t* cv = kst + F::kc;   // beta, delta of channels 32 qi + 4k .. (8 qi + k)
         float v[32];
         float am0 = 0.f, am1 = 0.f;
         float2 s0 = make_float2(0.f, 0.f), s1 = s0;
 #pragma unroll
         for (int k = 0; k < 8; ++k) {
-          const float4 q4 = qv[(8 * qi + k) ^ qi], c4 = F::get_c4(cv, 8 * qi + k);
+          const float4 q4 = qv[(8 * qi + k) ^ qi], c4 = F::get_b4(cv, 8 * qi + k);
           const float2 p0 = __fmul2_rn(make_float2(q4.x, q4.y), make_float2(c4.x, c4.y));
           const float2 p1 = __fmul2_rn(make_float2(q4.z, q4.w), make_float2(c4.z, c4.w));
           v[4 * k + 0] = p0.x;
@@ -321,8 +324,14 @@ __global__ void __launch_bounds__(kThreads, NT == 1 ? 3 : 2) decode_mma_kernel(D
           v[4 * k + 3] = p1.y;
           am0 = max3(am0, fabsf(p0.x), fabsf(p0.y));
           am1 = max3(am1, fabsf(p1.x), fabsf(p1.y));
-          s0 = __fadd2_rn(s0, p0);
-          s1 = __fadd2_rn(s1, p1);
+          if constexpr (F::pc) {   // the constant term takes delta, not beta
+            const float4 d4 = F::get_d4(cv, 8 * qi + k);
+            s0 = __ffma2_rn(make_float2(q4.x, q4.y), make_float2(d4.x, d4.y), s0);
+            s1 = __ffma2_rn(make_float2(q4.z, q4.w), make_float2(d4.z, d4.w), s1);
+          } else {
+            s0 = __fadd2_rn(s0, p0);
+            s1 = __fadd2_rn(s1, p1);
+          }
         }
         float amax = fmaxf(am0, am1);
         const float2 s01 = __fadd2_rn(s0, s1);
@@ -516,13 +525,19 @@ __global__ void __launch_bounds__(kThreads, NT == 1 ? 3 : 2) decode_mma_kernel(D
 #pragma unroll
         for (int i = 0; i < MCG; ++i) {
           const int mc = c0 + i;
-          const float cvA = F::get_c(cvv, 16 * mc + r), cvB = F::get_c(cvv, 16 * mc + 8 + r);
+          const float2 bdA = F::get_bd(cvv, 16 * mc + r), bdB = F::get_bd(cvv, 16 * mc + 8 + r);
 #pragma unroll
           for (int nt = 0; nt < NT; ++nt) {
-            oacc[nt][2 * mc] = fmaf(oacc[nt][2 * mc], alpha[nt],
-                                    cvA * fmaf(d[nt][i][0] + d[nt][i][1], fin, zpage[nt]));
-            oacc[nt][2 * mc + 1] = fmaf(oacc[nt][2 * mc + 1], alpha[nt],
-                                        cvB * fmaf(d[nt][i][2] + d[nt][i][3], fin, zpage[nt]));
+            float uA, uB;
+            if constexpr (F::pc) {
+              uA = fmaf(bdA.x, (d[nt][i][0] + d[nt][i][1]) * fin, bdA.y * zpage[nt]);
+              uB = fmaf(bdB.x, (d[nt][i][2] + d[nt][i][3]) * fin, bdB.y * zpage[nt]);
+            } else {   // beta = delta = c
+              uA = bdA.x * fmaf(d[nt][i][0] + d[nt][i][1], fin, zpage[nt]);
+              uB = bdB.x * fmaf(d[nt][i][2] + d[nt][i][3], fin, zpage[nt]);
+            }
+            oacc[nt][2 * mc] = fmaf(oacc[nt][2 * mc], alpha[nt], uA);
+            oacc[nt][2 * mc + 1] = fmaf(oacc[nt][2 * mc + 1], alpha[nt], uB);
           }
         }
       }
@@ -834,11 +849,11 @@ __global__ void __launch_bounds__(kThreads, NT == 1 ? 3 : 2) decode_mma_kernel(D
   if (tid == 0) a.ws_count[(int64_t)b * a.hkv + kvh] = 0;
 }
 
-template <int NT, bool M16>
+template <int NT, int FMT>
 cudaError_t launch_nt(const DecodeArgs& args, cudaStream_t s) {
   static std::atomic<uint64_t> smem_set{0};
   const int smem = (int)sizeof(MmaSmem<NT>);
-  cudaError_t e = ensure_dynamic_smem(decode_mma_kernel<NT, M16>, smem, smem_set);
+  cudaError_t e = ensure_dynamic_smem(decode_mma_kernel<NT, FMT>, smem, smem_set);
   if (e != cudaSuccess) return e;
   DecodeArgs a = args;
   a.cluster = decode_uses_cluster(a.g, a.nsplit);
@@ -856,7 +871,7 @@ cudaError_t launch_nt(const DecodeArgs& args, cudaStream_t s) {
     cfg.attrs = attr;
     cfg.numAttrs = 1;
   }
-  return cudaLaunchKernelEx(&cfg, decode_mma_kernel<NT, M16>, a);
+  return cudaLaunchKernelEx(&cfg, decode_mma_kernel<NT, FMT>, a);
 }
 
 }  // namespace
@@ -876,8 +891,9 @@ int decode_mma_ctas_per_sm(int g) {
 }
 
 cudaError_t launch_decode_mma(const DecodeArgs& a, cudaStream_t s) {
-  if (a.meta16) return a.g <= 4 ? launch_nt<1, true>(a, s) : launch_nt<2, true>(a, s);
-  return a.g <= 4 ? launch_nt<1, false>(a, s) : launch_nt<2, false>(a, s);
+  if (a.fmt == kFmtM16) return a.g <= 4 ? launch_nt<1, kFmtM16>(a, s) : launch_nt<2, kFmtM16>(a, s);
+  if (a.fmt == kFmtPC) return a.g <= 4 ? launch_nt<1, kFmtPC>(a, s) : launch_nt<2, kFmtPC>(a, s);
+  return a.g <= 4 ? launch_nt<1, kFmtF32>(a, s) : launch_nt<2, kFmtF32>(a, s);
 }
 
 }  // namespace kvarn

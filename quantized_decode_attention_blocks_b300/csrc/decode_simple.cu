@@ -73,10 +73,10 @@ __device__ void fwht_rows(float (*v)[kD], int g) {
 }
 
 // grid: (nsplit, hkv, batch); block 128.
-// M16: the "_m16" record (metadata stored as fp16); otherwise fp32.
-template <bool M16>
+// FMT: the record format (RecFmt): yhat_td = alpha_t beta_d q_td + gamma_t delta_d.
+template <int FMT>
 __global__ void __launch_bounds__(kThreads) decode_simple_kernel(DecodeArgs a) {
-  using F = RecFmt<M16>;
+  using F = RecFmt<FMT>;
   extern __shared__ __align__(16) uint8_t smem_raw[];
   DecodeSmem& S = *reinterpret_cast<DecodeSmem*>(smem_raw);
   const int split = blockIdx.x, kvh = blockIdx.y, b = blockIdx.z;
@@ -127,14 +127,14 @@ __global__ void __launch_bounds__(kThreads) decode_simple_kernel(DecodeArgs a) {
       uint4* dst = reinterpret_cast<uint4*>(S.rec);
       for (int i = tid; i < F::bytes / 16; i += kThreads) dst[i] = __ldg(src + i);
       __syncthreads();
-      // qc = H q * c^K (thread = channel), and its sum per head
+      // qc = H q * beta^K (thread = channel), and sum_d H q * delta^K per head
       {
-        const float ck = F::get_c(S.rec + F::kc, tid);
+        const float2 bd = F::get_bd(S.rec + F::kc, tid);
         float part[kMaxG];
         for (int h = 0; h < g; ++h) {
-          const float x = S.qrot[h][tid] * ck;
+          const float x = S.qrot[h][tid] * bd.x;
           S.qc[h][tid] = x;
-          part[h] = x;
+          part[h] = F::pc ? S.qrot[h][tid] * bd.y : x;
         }
         block_reduce<false>(S, part, g, S.sq);
       }
@@ -197,7 +197,7 @@ __global__ void __launch_bounds__(kThreads) decode_simple_kernel(DecodeArgs a) {
       {
         const int d = tid;
         const uint32_t* vw = reinterpret_cast<const uint32_t*>(S.rec + F::kpart);
-        const float cv = F::get_c(S.rec + F::vc, d);
+        const float2 bdv = F::get_bd(S.rec + F::vc, d);
         float pv[kMaxG];
         for (int h = 0; h < g; ++h) pv[h] = 0.f;
         for (int w = 0; w < 8; ++w) {
@@ -211,7 +211,8 @@ __global__ void __launch_bounds__(kThreads) decode_simple_kernel(DecodeArgs a) {
           }
         }
         for (int h = 0; h < g; ++h) {
-          acc[h] = fmaf(acc[h], S.alpha[h], cv * (pv[h] + S.zs[h]));
+          const float u = F::pc ? fmaf(bdv.x, pv[h], bdv.y * S.zs[h]) : bdv.x * (pv[h] + S.zs[h]);
+          acc[h] = fmaf(acc[h], S.alpha[h], u);
           acc_tail[h] *= S.alpha[h];
         }
       }
@@ -284,21 +285,23 @@ __global__ void __launch_bounds__(kThreads) decode_simple_kernel(DecodeArgs a) {
   if (tid == 0) a.ws_count[(int64_t)b * a.hkv + kvh] = 0;
 }
 
-template <bool M16>
+template <int FMT>
 cudaError_t launch_simple(const DecodeArgs& a, cudaStream_t s) {
   static std::atomic<uint64_t> smem_set{0};
   const int smem = (int)sizeof(DecodeSmem);
-  cudaError_t e = ensure_dynamic_smem(decode_simple_kernel<M16>, smem, smem_set);
+  cudaError_t e = ensure_dynamic_smem(decode_simple_kernel<FMT>, smem, smem_set);
   if (e != cudaSuccess) return e;
   dim3 grid(a.nsplit, a.hkv, a.batch);
-  decode_simple_kernel<M16><<<grid, kThreads, smem, s>>>(a);
+  decode_simple_kernel<FMT><<<grid, kThreads, smem, s>>>(a);
   return cudaGetLastError();
 }
 
 }  // namespace
 
 cudaError_t launch_decode_simple(const DecodeArgs& a, cudaStream_t s) {
-  return a.meta16 ? launch_simple<true>(a, s) : launch_simple<false>(a, s);
+  if (a.fmt == kFmtM16) return launch_simple<kFmtM16>(a, s);
+  if (a.fmt == kFmtPC) return launch_simple<kFmtPC>(a, s);
+  return launch_simple<kFmtF32>(a, s);
 }
 
 }  // namespace kvarn

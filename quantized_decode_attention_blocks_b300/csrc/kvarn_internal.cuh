@@ -25,67 +25,115 @@ constexpr int kOffVSZ = 13824;
 constexpr int kOffVC = 14848;
 constexpr int kKPart = 9728;      // K part: [0, 9728)
 constexpr int kVPart = kRec - kKPart;  // V part: [9728, 15360)
-// The two record formats: kvarn_k4v2_g128 (fp32 metadata, the constants
-// above) and the "_m16" variant, the same codes with s', z' and c_d stored as
-// fp16 (round to nearest even), 108 B per token-head:
+// The record formats, all with the codes above: 0 = kvarn_k4v2_g128 (fp32
+// metadata, the constants above); 1 = "_m16", s', z' and c_d stored as fp16
+// (round to nearest even), 108 B per token-head:
 //   [0, 8192) K codes, [8192, 8704) K {s', z'} fp16 pairs, [8704, 8960) K c_d,
-//   [8960, 13056) V codes, [13056, 13568) V {s', z'}, [13568, 13824) V c_d.
-// The accessors take the address of the field (record part + offset).
-template <bool M16>
+//   [8960, 13056) V codes, [13056, 13568) V {s', z'}, [13568, 13824) V c_d;
+// 2 = "_pc", one RTN group per channel (over the tile's 128 tokens), the row
+// scale r_t stored per token and c_d folded into the per-channel scale and
+// zero: yhat_td = r_t (cs_d q_td + cz_d):
+//   [0, 8192) K codes, [8192, 8704) K r_t fp32, [8704, 9728) K {cs_d, cz_d}
+//   fp32 pairs, [9728, 13824) V codes, [13824, 14336) V r_t, [14336, 15360) V
+//   {cs_d, cz_d}.
+// Every format dequantizes as yhat_td = alpha_t beta_d q_td + gamma_t delta_d:
+// (alpha, gamma) = (s', z') and beta = delta = c_d for formats 0 and 1,
+// alpha = gamma = r_t and (beta, delta) = (cs_d, cz_d) for format 2.  The
+// accessors take the address of the field (record part + offset).
+constexpr int kFmtF32 = 0, kFmtM16 = 1, kFmtPC = 2;
+template <int FMT>
 struct RecFmt {
-  static constexpr int bytes = M16 ? 13824 : 15360;
-  static constexpr int kpart = M16 ? 8960 : 9728;   // K part [0, kpart)
+  static constexpr bool m16 = FMT == kFmtM16;
+  static constexpr bool pc = FMT == kFmtPC;
+  static constexpr int bytes = m16 ? 13824 : 15360;
+  static constexpr int kpart = m16 ? 8960 : 9728;   // K part [0, kpart)
   static constexpr int vpart = bytes - kpart;       // V part [kpart, bytes)
-  static constexpr int ksz = 8192;
-  static constexpr int kc = M16 ? 8704 : 9216;
-  static constexpr int vsz = M16 ? 13056 : 13824;   // from the record start
-  static constexpr int vc = M16 ? 13568 : 14848;
-  // {s', z'} of token t
+  static constexpr int ksz = 8192;                  // per-token fields
+  static constexpr int kc = m16 ? 8704 : pc ? 8704 : 9216;     // per-channel fields
+  static constexpr int vsz = m16 ? 13056 : 13824;   // from the record start
+  static constexpr int vc = m16 ? 13568 : pc ? 14336 : 14848;
+  // (alpha_t, gamma_t) of token t
   static __device__ __forceinline__ float2 get_sz(const uint8_t* f, int t) {
-    if constexpr (M16)
+    if constexpr (m16) {
       return __half22float2(reinterpret_cast<const __half2*>(f)[t]);
-    else
+    } else if constexpr (pc) {
+      const float r = reinterpret_cast<const float*>(f)[t];
+      return make_float2(r, r);
+    } else {
       return reinterpret_cast<const float2*>(f)[t];
+    }
   }
   static __device__ __forceinline__ void put_sz(uint8_t* f, int t, float s, float z) {
-    if constexpr (M16)
+    static_assert(!pc, "the per-channel format stores r_t (put_r)");
+    if constexpr (m16)
       reinterpret_cast<__half2*>(f)[t] = __floats2half2_rn(s, z);
     else
       reinterpret_cast<float2*>(f)[t] = make_float2(s, z);
   }
-  // c_d of channel d, and of channels 4 i .. 4 i + 3
-  static __device__ __forceinline__ float get_c(const uint8_t* f, int d) {
-    if constexpr (M16)
-      return __half2float(reinterpret_cast<const __half*>(f)[d]);
-    else
-      return reinterpret_cast<const float*>(f)[d];
+  static __device__ __forceinline__ void put_r(uint8_t* f, int t, float r) {
+    static_assert(pc, "only the per-channel format stores r_t");
+    reinterpret_cast<float*>(f)[t] = r;
   }
-  static __device__ __forceinline__ float4 get_c4(const uint8_t* f, int i) {
-    if constexpr (M16) {
+  // (beta_d, delta_d) of channel d
+  static __device__ __forceinline__ float2 get_bd(const uint8_t* f, int d) {
+    if constexpr (pc) {
+      return reinterpret_cast<const float2*>(f)[d];
+    } else {
+      const float c = m16 ? __half2float(reinterpret_cast<const __half*>(f)[d])
+                          : reinterpret_cast<const float*>(f)[d];
+      return make_float2(c, c);
+    }
+  }
+  // beta of channels 4 i .. 4 i + 3, and delta of the same channels
+  static __device__ __forceinline__ float4 get_b4(const uint8_t* f, int i) {
+    if constexpr (m16) {
       const uint2 u = reinterpret_cast<const uint2*>(f)[i];
       const float2 a = __half22float2(*reinterpret_cast<const __half2*>(&u.x));
       const float2 b = __half22float2(*reinterpret_cast<const __half2*>(&u.y));
       return make_float4(a.x, a.y, b.x, b.y);
+    } else if constexpr (pc) {
+      const float4 p0 = reinterpret_cast<const float4*>(f)[2 * i];
+      const float4 p1 = reinterpret_cast<const float4*>(f)[2 * i + 1];
+      return make_float4(p0.x, p0.z, p1.x, p1.z);
     } else {
       return reinterpret_cast<const float4*>(f)[i];
     }
   }
+  static __device__ __forceinline__ float4 get_d4(const uint8_t* f, int i) {
+    if constexpr (pc) {
+      const float4 p0 = reinterpret_cast<const float4*>(f)[2 * i];
+      const float4 p1 = reinterpret_cast<const float4*>(f)[2 * i + 1];
+      return make_float4(p0.y, p0.w, p1.y, p1.w);
+    } else {
+      return get_b4(f, i);
+    }
+  }
   static __device__ __forceinline__ void put_c(uint8_t* f, int d, float c) {
-    if constexpr (M16)
+    static_assert(!pc, "the per-channel format stores {cs, cz} (put_bd)");
+    if constexpr (m16)
       reinterpret_cast<__half*>(f)[d] = __float2half_rn(c);
     else
       reinterpret_cast<float*>(f)[d] = c;
   }
+  static __device__ __forceinline__ void put_bd(uint8_t* f, int d, float cs, float cz) {
+    static_assert(pc, "only the per-channel format stores {cs, cz}");
+    reinterpret_cast<float2*>(f)[d] = make_float2(cs, cz);
+  }
 };
-static_assert(RecFmt<false>::bytes == kRec && RecFmt<false>::kpart == kKPart &&
-                  RecFmt<false>::ksz == kOffKSZ && RecFmt<false>::kc == kOffKC &&
-                  RecFmt<false>::vsz == kOffVSZ && RecFmt<false>::vc == kOffVC &&
-                  RecFmt<false>::kpart == kOffVCodes,
+static_assert(RecFmt<kFmtF32>::bytes == kRec && RecFmt<kFmtF32>::kpart == kKPart &&
+                  RecFmt<kFmtF32>::ksz == kOffKSZ && RecFmt<kFmtF32>::kc == kOffKC &&
+                  RecFmt<kFmtF32>::vsz == kOffVSZ && RecFmt<kFmtF32>::vc == kOffVC &&
+                  RecFmt<kFmtF32>::kpart == kOffVCodes,
               "the fp32 format is the one the constants above describe");
-static_assert(RecFmt<true>::kpart % 16 == 0 && RecFmt<true>::vpart % 16 == 0 &&
-                  RecFmt<true>::bytes % 16 == 0 && RecFmt<true>::vsz % 16 == 0 &&
-                  RecFmt<true>::vc % 16 == 0 && RecFmt<true>::kc % 16 == 0,
+static_assert(RecFmt<kFmtM16>::kpart % 16 == 0 && RecFmt<kFmtM16>::vpart % 16 == 0 &&
+                  RecFmt<kFmtM16>::bytes % 16 == 0 && RecFmt<kFmtM16>::vsz % 16 == 0 &&
+                  RecFmt<kFmtM16>::vc % 16 == 0 && RecFmt<kFmtM16>::kc % 16 == 0 &&
+                  RecFmt<kFmtPC>::kc % 16 == 0 && RecFmt<kFmtPC>::vc % 16 == 0,
               "bulk copies and vector loads need 16-byte parts and fields");
+// The format code of a configuration.
+__host__ __device__ constexpr int fmt_of(int meta16, int per_channel) {
+  return per_channel ? kFmtPC : meta16 ? kFmtM16 : kFmtF32;
+}
 
 // Split-K partial state per (sequence, query head, split): m, l, 2 pad, o[128]
 // (o 16-byte aligned).
@@ -138,7 +186,7 @@ struct QuantizeArgs {
   int64_t sb, st, sh;       // element strides of k / v
   int batch, hkv, iters, max_seq;
   int rms;                  // Sinkhorn statistic: 0 centred std, 1 uncentred RMS
-  int meta16;               // record format: 0 fp32 metadata, 1 fp16 ("_m16")
+  int fmt;                  // record format (kFmtF32, kFmtM16, kFmtPC)
   const int32_t* seq_lens;
   const int32_t* block_table;
   int max_blocks;
@@ -155,7 +203,7 @@ struct AppendArgs {
   const int32_t* pos;
   int batch, hkv, iters;
   int rms;
-  int meta16;
+  int fmt;                  // record format
   const int32_t* block_table;
   int max_blocks;
   uint8_t* pool;
@@ -182,7 +230,7 @@ struct DecodeArgs {
   int pages_per_split;
   int nsplit;
   int cluster;        // 1: the nsplit CTAs of a (sequence, KV head) form a cluster
-  int meta16;         // record format: 0 fp32 metadata, 1 fp16 ("_m16")
+  int fmt;            // record format (kFmtF32, kFmtM16, kFmtPC)
   int32_t* status;
 };
 
@@ -307,7 +355,7 @@ struct ChunkArgs {
   const __half* tail_v;
   float scale_log2;           // softmax scale * log2(e)
   __half* out;                // [batch][M][hq][128]
-  int meta16;                 // record format: 0 fp32 metadata, 1 fp16 ("_m16")
+  int fmt;                    // record format (kFmtF32, kFmtM16, kFmtPC)
   int32_t* status;
 };
 int chunk_rows_per_tile(int g);

@@ -327,8 +327,9 @@ __device__ __forceinline__ uint32_t hs_bits(int n, int k) {
   return (__popc(n & k) & 1) ? 0xBC00u : 0x3C00u;
 }
 
-// M16: the "_m16" record (metadata stored as fp16); otherwise fp32.
-template <bool M16>
+// FMT: the record format (RecFmt): fp32 or fp16 ("_m16") metadata with
+// per-token groups, or per-channel groups ("_pc").
+template <int FMT>
 __global__ void __launch_bounds__(kQThreads, 1)
     quantize_tc_kernel(const __grid_constant__ CUtensorMap tmk,
                        const __grid_constant__ CUtensorMap tmv, const QTileArgs a,
@@ -437,7 +438,7 @@ __global__ void __launch_bounds__(kQThreads, 1)
     if (a.mode != 0)
       page = in_table ? (int64_t)a.block_table[(int64_t)tl.b * a.max_blocks + tl.j] : -1;
     if (in_table && page >= 0 && page < a.num_pages)
-      info.rec = (long long)((page * a.hkv + tl.h) * (int64_t)RecFmt<M16>::bytes);
+      info.rec = (long long)((page * a.hkv + tl.h) * (int64_t)RecFmt<FMT>::bytes);
     else
       report(a.status, in_table ? KVARN_STATUS_BAD_PAGE : KVARN_STATUS_BAD_LENGTH);
     const CUtensorMap* tm = tl.part ? &tmv : &tmk;
@@ -614,6 +615,92 @@ __global__ void __launch_bounds__(kQThreads, 1)
       named_sync(bar_id, kWGThreads);
     }
     const float2 mg = make_float2(kMagic, kMagic);
+    if constexpr (RecFmt<FMT>::pc) {
+      // per-channel groups: x_td = Y_td / (r_t c_d) = (Y_td ra_t) cb_d, the
+      // range of each channel (a row n of Y^T) over the tile's tokens, then
+      // the codes: V from the same Y^T fragment, K (token-major) from Y with
+      // the channels' minima and 1 / step published in shared memory.  Both
+      // passes form x by the same two products, so they see the same values.
+      using F = RecFmt<FMT>;
+      const float qmax = part ? 3.f : 15.f;
+      uint8_t* const meta = out + (part ? F::vc - F::kpart : F::kc);
+      float2 wr[16];
+      frag_weights(ra, q, wr);
+      float v[64];
+      tmem_ld256(tYT, v);
+      tmem_wait_ld();
+      float lo[2], inv[2];
+#pragma unroll
+      for (int e = 0; e < 2; ++e) {
+        const float cbe = cb[frow(e)];
+        const float2 cb2 = make_float2(cbe, cbe);
+        float mn = INFINITY, mx = -INFINITY;
+#pragma unroll
+        for (int k = 0; k < 16; ++k) {
+          const float2 x = __fmul2_rn(__fmul2_rn(pair(v, k, e), wr[k]), cb2);
+          v[4 * k + 2 * e] = x.x;
+          v[4 * k + 2 * e + 1] = x.y;
+          mn = min3f(mn, x.x, x.y);
+          mx = max3f(mx, x.x, x.y);
+        }
+        lo[e] = quad_min(mn);
+        const float range = quad_max(mx) - lo[e];
+        inv[e] = range > 0.f ? __fdividef(qmax, range) : 0.f;
+        if (q == 0) {
+          const int n = frow(e), ch = chan_of(n);
+          S.vmin[wg][n] = lo[e];
+          S.vinv[wg][n] = inv[e];
+          F::put_bd(meta, ch, cc[ch] * (range / qmax), cc[ch] * lo[e]);
+        }
+      }
+      // r_t = 1 / (ra_t sqrt(128)) in the oracle's units (ra is in units of Y)
+      if (lower) F::put_r(out + (part ? F::vsz - F::kpart : F::ksz), row, kInvSqrt128 / ra[row]);
+      if (part) {
+        // V: whole words of the thread's channels, crumb (k & 7) + 8b of word
+        // v_word(channel, q, k >> 3) from token column 8k + 2q + b
+        uint32_t* vw = reinterpret_cast<uint32_t*>(out);
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+          const float2 nm = make_float2(-lo[e], -lo[e]), iv = make_float2(inv[e], inv[e]);
+          uint32_t acc[2] = {0u - kMagicV, 0u - kMagicV};
+#pragma unroll
+          for (int k = 0; k < 16; ++k) {
+            const float2 f = __ffma2_rn(__fadd2_rn(pair(v, k, e), nm), iv, mg);
+            acc[k >> 3] += __float_as_uint(f.x) << (2 * (k & 7));
+            acc[k >> 3] += __float_as_uint(f.y) << (2 * (k & 7) + 16);
+          }
+          *reinterpret_cast<uint2*>(vw + v_word(chan_of(frow(e)), q, 0)) =
+              make_uint2(acc[0], acc[1]);
+        }
+      } else {
+        // K: token rows of Y, the channels' minima and 1 / step by column
+        named_sync(bar_id, kWGThreads);
+        float2 wc[16];
+        frag_weights(cb, q, wc);
+        tmem_ld256(tY, v);
+        tmem_wait_ld();
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+          const int t = frow(e);
+          const float2 ra2 = make_float2(ra[t], ra[t]);
+          uint32_t acc[4];
+#pragma unroll
+          for (int j = 0; j < 4; ++j) acc[j] = 0u - kMagicK;
+#pragma unroll
+          for (int k = 0; k < 16; ++k) {
+            const float2 x = __fmul2_rn(__fmul2_rn(pair(v, k, e), ra2), wc[k]);
+            const float2 m2 = *reinterpret_cast<const float2*>(S.vmin[wg] + 8 * k + 2 * q);
+            const float2 i2 = *reinterpret_cast<const float2*>(S.vinv[wg] + 8 * k + 2 * q);
+            const float2 f =
+                __ffma2_rn(__fadd2_rn(x, make_float2(-m2.x, -m2.y)), i2, mg);
+            acc[k >> 2] += __float_as_uint(f.x) << (8 * (k & 3));
+            acc[k >> 2] += __float_as_uint(f.y) << (8 * (k & 3) + 4);
+          }
+          *reinterpret_cast<uint4*>(out + kOffKCodes + 64 * t + 16 * q) =
+              make_uint4(acc[0], acc[1], acc[2], acc[3]);
+        }
+      }
+    } else {
     float2 w[16];
     frag_weights(cb, q, w);
     float v[64];
@@ -623,7 +710,7 @@ __global__ void __launch_bounds__(kQThreads, 1)
       // K: token-major, 64 bytes per token; nibble e of word w = channel 8w + e.
       // The fragment of a row is the channels 32q .. 32q + 31: its words 4q ..
       // 4q + 3, nibble 2 (k & 3) + b of word 4q + (k >> 2) from column pair k.
-      if (lower) RecFmt<M16>::put_c(out + RecFmt<M16>::kc, row, cc[row]);
+      if (lower) RecFmt<FMT>::put_c(out + RecFmt<FMT>::kc, row, cc[row]);
       {
         float mn[2], mx[2];
 #pragma unroll
@@ -648,7 +735,7 @@ __global__ void __launch_bounds__(kQThreads, 1)
           const float inv = range > 0.f ? __fdividef(15.f, range) : 0.f;
           const int t = frow(e);
           if (q == 0)
-            RecFmt<M16>::put_sz(out + RecFmt<M16>::ksz, t, range * (kInvSqrt128 / 15.f),
+            RecFmt<FMT>::put_sz(out + RecFmt<FMT>::ksz, t, range * (kInvSqrt128 / 15.f),
                                 lo * kInvSqrt128);
           // u = (x - min) (15 / range) + 1.5 * 2^23: the code in the low bits
           const float2 nm = make_float2(-lo, -lo), iv = make_float2(inv, inv);
@@ -670,7 +757,7 @@ __global__ void __launch_bounds__(kQThreads, 1)
       // whole words of its channels from Y^T: the fragment columns (tokens)
       // 8k + 2q + b are crumb (k & 7) + 8b of word v_word(channel, q, k >> 3)
       if (lower)
-        RecFmt<M16>::put_c(out + (RecFmt<M16>::vc - RecFmt<M16>::kpart), row, cc[row]);
+        RecFmt<FMT>::put_c(out + (RecFmt<FMT>::vc - RecFmt<FMT>::kpart), row, cc[row]);
       {
         float mn[2], mx[2];
 #pragma unroll
@@ -694,7 +781,7 @@ __global__ void __launch_bounds__(kQThreads, 1)
           if (q == 0) {
             S.vmin[wg][t] = lo;
             S.vinv[wg][t] = range > 0.f ? __fdividef(3.f, range) : 0.f;
-            RecFmt<M16>::put_sz(out + (RecFmt<M16>::vsz - RecFmt<M16>::kpart), t,
+            RecFmt<FMT>::put_sz(out + (RecFmt<FMT>::vsz - RecFmt<FMT>::kpart), t,
                                 range * (kInvSqrt128 / 3.f), lo * kInvSqrt128);
           }
         }
@@ -731,6 +818,7 @@ __global__ void __launch_bounds__(kQThreads, 1)
               make_uint2(acc[e][0], acc[e][1]);
       }
     }
+    }   // per-token groups
     // the first row step sums of the next tile, whose input is already in the
     // other stage (no MMA reads it yet)
     have_r1 = false;
@@ -750,8 +838,8 @@ __global__ void __launch_bounds__(kQThreads, 1)
     tc_fence_before();
     named_sync(bar_id, kWGThreads);
     if (leader && cur.rec >= 0) {
-      bulk_s2g(a.pool + cur.rec + (part ? RecFmt<M16>::kpart : 0), out,
-               part ? RecFmt<M16>::vpart : RecFmt<M16>::kpart);
+      bulk_s2g(a.pool + cur.rec + (part ? RecFmt<FMT>::kpart : 0), out,
+               part ? RecFmt<FMT>::vpart : RecFmt<FMT>::kpart);
       bulk_commit();
     }
     stage ^= 1;
@@ -827,19 +915,26 @@ bool encode_tile_map(CUtensorMap* map, const void* base, int64_t sb, int64_t st,
 
 constexpr int kQSmemBytes = (int)sizeof(QSmem) + 1024;
 
-template <bool M16>
+template <int FMT>
 cudaError_t launch_tiles(const CUtensorMap& mk, const CUtensorMap& mv, const QTileArgs& qa,
                          const QCopyArgs& cp, cudaStream_t s) {
   static std::atomic<uint64_t> smem_set{0};
-  cudaError_t e = ensure_dynamic_smem(quantize_tc_kernel<M16>, kQSmemBytes, smem_set);
+  cudaError_t e = ensure_dynamic_smem(quantize_tc_kernel<FMT>, kQSmemBytes, smem_set);
   if (e != cudaSuccess) return e;
   const int sms = device_sm_count();
   if (sms <= 0) return cudaErrorNoDevice;
   const int want = (qa.ntiles + kWG - 1) / kWG;
   // one CTA at least: with no tile to quantize it still does the copies
   const int grid = want < 1 ? 1 : want < sms ? want : sms;
-  quantize_tc_kernel<M16><<<grid, kQThreads, kQSmemBytes, s>>>(mk, mv, qa, cp);
+  quantize_tc_kernel<FMT><<<grid, kQThreads, kQSmemBytes, s>>>(mk, mv, qa, cp);
   return cudaGetLastError();
+}
+
+cudaError_t launch_fmt(int fmt, const CUtensorMap& mk, const CUtensorMap& mv,
+                       const QTileArgs& qa, const QCopyArgs& cp, cudaStream_t s) {
+  if (fmt == kFmtM16) return launch_tiles<kFmtM16>(mk, mv, qa, cp, s);
+  if (fmt == kFmtPC) return launch_tiles<kFmtPC>(mk, mv, qa, cp, s);
+  return launch_tiles<kFmtF32>(mk, mv, qa, cp, s);
 }
 
 }  // namespace
@@ -901,7 +996,7 @@ cudaError_t launch_quantize_blocks(const QuantizeArgs& a, cudaStream_t s) {
     qa.roles = rk;
   }
   // the tiles and the leftover-token copies, one launch
-  return a.meta16 ? launch_tiles<true>(mk, mv, qa, cp, s) : launch_tiles<false>(mk, mv, qa, cp, s);
+  return launch_fmt(a.fmt, mk, mv, qa, cp, s);
 }
 
 cudaError_t launch_append_token(const AppendArgs& a, cudaStream_t s) {
@@ -935,7 +1030,7 @@ cudaError_t launch_append_token(const AppendArgs& a, cudaStream_t s) {
       !encode_tile_map(&mv, a.tail_v, sb, kD, sh, a.batch, kT, a.hkv, &rv))
     return cudaErrorInvalidValue;
   qa.roles = rk;
-  return a.meta16 ? launch_tiles<true>(mk, mv, qa, cp, s) : launch_tiles<false>(mk, mv, qa, cp, s);
+  return launch_fmt(a.fmt, mk, mv, qa, cp, s);
 }
 
 }  // namespace kvarn

@@ -46,7 +46,7 @@ class Config(ctypes.Structure):
                 ("group", ctypes.c_int), ("k_bits", ctypes.c_int), ("v_bits", ctypes.c_int),
                 ("sinkhorn_iters", ctypes.c_int), ("num_q_heads", ctypes.c_int),
                 ("num_kv_heads", ctypes.c_int), ("sinkhorn_rms", ctypes.c_int),
-                ("meta_fp16", ctypes.c_int)]
+                ("meta_fp16", ctypes.c_int), ("per_channel", ctypes.c_int)]
 
     @property
     def g(self) -> int:

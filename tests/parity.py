@@ -43,17 +43,39 @@ def _compare_meta16(tag, got16, ref16, ref32):
                            f"ref fp32={r32[bad][:3]}")
 
 
+def _compare_pc(tag, got, ref, is_v, bits):
+    """Format "_pc" metadata: r_t and cs_d within 1e-5 relative, cz_d within
+    1e-5 (|cz| + cs (2^b - 1)) (the z' rule with the per-channel step)."""
+    _, rg, csg, czg = kvref.unpack_part_pc(got, is_v)
+    _, rr, csr, czr = kvref.unpack_part_pc(ref, is_v)
+    for name, g_, r_ in (("r", rg, rr), ("cs", csg, csr)):
+        g64, r64 = g_.astype(np.float64), r_.astype(np.float64)
+        tol = np.where(r64 == 0, 1e-12, 1e-5 * np.abs(r64))
+        err = np.abs(g64 - r64)
+        assert np.all(err <= tol), (f"{tag}.{name}: worst rel err "
+                                    f"{(err / np.maximum(np.abs(r64), 1e-30)).max():.3e}")
+    tolz = np.maximum(1e-5 * (np.abs(czr.astype(np.float64))
+                              + np.abs(csr.astype(np.float64)) * (2 ** bits - 1)), 1e-12)
+    errz = np.abs(czg.astype(np.float64) - czr.astype(np.float64))
+    assert np.all(errz <= tolz), f"{tag}.cz: worst err {errz.max():.3e}"
+
+
 def compare_record(got: np.ndarray, ref: np.ndarray, u_k=None, u_v=None, stats=None,
-                   meta16: bool = False, ref32: np.ndarray = None):
+                   meta16: bool = False, ref32: np.ndarray = None, pc: bool = False):
     """Compares one record (GPU) with the oracle's.  u_k, u_v: oracle
     pre-rounding values [128][128] (token, channel).  meta16: the "_m16"
     format, whose metadata is judged against ref32, the oracle's record of
-    the same tile in the fp32 format.  Returns a dict."""
+    the same tile in the fp32 format; pc: the "_pc" format.  Returns a dict."""
     out = {} if stats is None else stats
     for is_v, u in ((False, u_k), (True, u_v)):
         bits = 2 if is_v else 4
-        qg, sg, zg, cg = kvref.unpack_part(got, is_v, meta16)
-        qr, sr, zr, cr = kvref.unpack_part(ref, is_v, meta16)
+        if pc:
+            qg = kvref.unpack_part_pc(got, is_v)[0]
+            qr = kvref.unpack_part_pc(ref, is_v)[0]
+            sg = zg = cg = sr = zr = cr = None
+        else:
+            qg, sg, zg, cg = kvref.unpack_part(got, is_v, meta16)
+            qr, sr, zr, cr = kvref.unpack_part(ref, is_v, meta16)
         tag = "v" if is_v else "k"
         diff = qg != qr
         n_diff = int(diff.sum())
@@ -66,6 +88,9 @@ def compare_record(got: np.ndarray, ref: np.ndarray, u_k=None, u_v=None, stats=N
                                    f"ref={qr[bad][:4]}")
         out[f"{tag}_flips"] = out.get(f"{tag}_flips", 0) + n_diff
         out[f"{tag}_codes"] = out.get(f"{tag}_codes", 0) + qg.size
+        if pc:
+            _compare_pc(tag, got, ref, is_v, bits)
+            continue
         if meta16:
             _, s32, z32, c32 = kvref.unpack_part(ref32, is_v)
             for name, g_, r_, r32 in (("s", sg, sr, s32), ("z", zg, zr, z32), ("c", cg, cr, c32)):

@@ -75,6 +75,16 @@ def test_config_parsing():
             kv.config_from_string(bad, 12, 2)
     m.meta_fp16 = 3
     assert kv.config_validate(m) == K.ERR_UNSUPPORTED
+    # per-channel groups, alone or with "_rms", any order; never with "_m16"
+    for fmt in ("k4v2_g128_pc", "k4v2_g128_rms_pc_s3", "k4v2_g128_pc_rms"):
+        p = kv.config_from_string(fmt, 12, 2)
+        assert p.per_channel == 1 and p.meta_fp16 == 0 and p.sinkhorn_rms == ("rms" in fmt)
+        assert kv.page_bytes(p) == 15360
+    for bad in ("k4v2_g128_pc_m16", "k4v2_g128_m16_pc", "k4v2_g128_pcx", "k4v2_g128_pc_pc"):
+        with pytest.raises(kv.KvarnError):
+            kv.config_from_string(bad, 12, 2)
+    p.meta_fp16 = 1
+    assert kv.config_validate(p) == K.ERR_UNSUPPORTED
     for bad in ("k4v4_g128", "k4v2_g64", "k4v2_g128_x", "k4v2_g128_s", "k4v2_g128_s999"):
         with pytest.raises(kv.KvarnError) as e:
             kv.config_from_string(bad, 32, 8)

@@ -22,7 +22,7 @@ pytestmark = pytest.mark.gpu
 
 
 def _case(starts, chunk_lens, M, hq, hkv, seed, perm=True, table=None, num_pages=None,
-          m16=False):
+          m16=False, pc=False):
     starts = np.asarray(starts, dtype=np.int64)
     cls = np.asarray(chunk_lens, dtype=np.int64)
     n = starts + cls
@@ -30,7 +30,7 @@ def _case(starts, chunk_lens, M, hq, hkv, seed, perm=True, table=None, num_pages
     S = max(int(n.max()), 1)
     w = synth.scaled(synth.WORKLOADS["llama3_8b_layer"], batch=B, seq=S, hkv=hkv, hq=hq)
     k, v = synth.kv(w, layer=seed, device=DEV)
-    cfg = config(hq, hkv, m16=m16)
+    cfg = config(hq, hkv, m16=m16, pc=pc)
     mb = (S + 127) // 128
     if table is None:
         g = torch.Generator().manual_seed(seed)
@@ -48,7 +48,7 @@ def _case(starts, chunk_lens, M, hq, hkv, seed, perm=True, table=None, num_pages
                              table.to(DEV), tk, tv, out, status=status)
     torch.cuda.synchronize()
     return dict(cfg=cfg, q=q, out=out, status=status, st=st, pool=pool, tk=tk, tv=tv,
-                table=table, starts=starts, cls=cls, hq=hq, hkv=hkv, m16=m16)
+                table=table, starts=starts, cls=cls, hq=hq, hkv=hkv, m16=m16, pc=pc)
 
 
 def _check(c):
@@ -58,7 +58,7 @@ def _check(c):
     assert np.isfinite(got).all()
     ref = kvref.chunk_attention(host(c["q"]), c["starts"], c["cls"], host(c["pool"]),
                                 host(c["table"]), host(c["tk"]), host(c["tv"]), c["hq"],
-                                c["hkv"], meta16=c["m16"])
+                                c["hkv"], meta16=c["m16"], pc=c["pc"])
     for b, cl in enumerate(c["cls"]):
         assert not got[b, int(cl):].any(), "rows past the chunk must be zeros"
     return parity.compare_attention(got, ref)
@@ -75,6 +75,12 @@ def test_chunks_ragged_with_pages_and_tail(hq, hkv):
 def test_m16_format(hq, hkv):
     # format variant "_m16" (fp16 metadata): ragged chunks over pages and tail
     _check(_case([250, 100, 0, 300], [150, 60, 60, 1], 150, hq, hkv, seed=8, m16=True))
+
+
+@pytest.mark.parametrize("hq,hkv", [(8, 2), (12, 2)])
+def test_pc_format(hq, hkv):
+    # format variant "_pc" (per-channel groups)
+    _check(_case([250, 100, 0, 300], [150, 60, 60, 1], 150, hq, hkv, seed=9, pc=True))
 
 
 def test_chunk_of_whole_pages_and_inside_the_tail():
