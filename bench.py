@@ -490,15 +490,17 @@ def measure_chunk(args, dev, stream):
 def measure_variants(args, dev, stream):
     """The format variants on the Llama-3-8B-like layer (16 x 4096 tokens, 8 KV
     heads, 32 query heads), three rotated replicas: "_m16" (fp16 metadata,
-    108 B per token-head: quantize and decode) and "_rms" (the uncentred
-    Sinkhorn statistic: quantize; its records decode like the default's).
+    108 B per token-head) and "_pc" (per-channel groups), quantize and
+    decode; "_rms" (the uncentred Sinkhorn statistic), quantize (its records
+    decode like the default's).
     Algorithmic bytes as for the default format, with the record size of the
     variant."""
     import quantized_decode_attention_blocks_b300 as kv
     w = synth.WORKLOADS["llama3_8b_layer"]
     out = {}
     peak, kind = measured_peaks()
-    for fmt, rec, do_decode in (("k4v2_g128_m16", 13824, True), ("k4v2_g128_rms", REC, False)):
+    for fmt, rec, do_decode in (("k4v2_g128_m16", 13824, True), ("k4v2_g128_pc", REC, True),
+                                ("k4v2_g128_rms", REC, False)):
         cfg = kv.config_from_string(fmt, w.hq, w.hkv)
         reps = []
         for r in range(3):
