@@ -89,6 +89,17 @@
  *   [9728, 13824)  V codes (the same permutation)
  *   [13824,14336)  V per-token r_t fp32
  *   [14336,15360)  V per-channel {cs_d, cz_d} fp32 pairs
+ *
+ * Format variant "k4v2_g64" (group size 64; SURVEY's "G = 64"): the same
+ * stages with two RTN groups per token, channels 0-63 and 64-127, each with
+ * its own {s', z'} (the row scale folded in as in the default).  Record of
+ * 17408 bytes (136 B per token-head):
+ *   [0,     8192)  K codes (as above)
+ *   [8192, 10240)  K {s'_0, z'_0, s'_1, z'_1} fp32 per token (token t at 8192 + 16 t)
+ *   [10240,10752)  K per-channel c_d fp32
+ *   [10752,14848)  V codes (the same permutation)
+ *   [14848,16896)  V {s'_0, z'_0, s'_1, z'_1} fp32 per token
+ *   [16896,17408)  V per-channel c_d fp32
  */
 #include <math.h>
 #include <stdint.h>
@@ -105,6 +116,8 @@
 #define OFF_VSZ 13824
 #define OFF_VC 14848
 #define REC_BYTES_M16 13824
+#define REC_BYTES_G64 17408
+#define G64 64
 
 /* Offsets of the record parts for the two metadata widths. */
 typedef struct {
@@ -113,7 +126,8 @@ typedef struct {
 } rec_layout;
 
 /* fmt: 0 = fp32 metadata, 1 = "_m16" (fp16 metadata), 2 = "_pc" (per-channel
- * groups; ksz / vsz hold r_t, kc / vc the {cs, cz} pairs) */
+ * groups; ksz / vsz hold r_t, kc / vc the {cs, cz} pairs), 3 = "g64" (two
+ * groups per token; ksz / vsz hold two {s', z'} pairs per token) */
 static rec_layout layout_of(int fmt)
 {
     rec_layout L;
@@ -123,6 +137,9 @@ static rec_layout layout_of(int fmt)
     } else if (fmt == 2) {
         L.rec = REC_BYTES; L.kcodes = 0; L.ksz = 8192; L.kc = 8704;
         L.vcodes = 9728; L.vsz = 13824; L.vc = 14336; L.msz = 4;
+    } else if (fmt == 3) {
+        L.rec = REC_BYTES_G64; L.kcodes = 0; L.ksz = 8192; L.kc = 10240;
+        L.vcodes = 10752; L.vsz = 14848; L.vc = 16896; L.msz = 4;
     } else {
         L.rec = REC_BYTES; L.kcodes = OFF_KCODES; L.ksz = OFF_KSZ; L.kc = OFF_KC;
         L.vcodes = OFF_VCODES; L.vsz = OFF_VSZ; L.vc = OFF_VC; L.msz = 4;
@@ -410,6 +427,44 @@ void kvref_rtn_pc(const double *Y, const double *r, const float *c32, int bits, 
     }
 }
 
+/* Format "g64": RTN with two groups of 64 channels per token.  s32, z32:
+ * [NTOK][2] (group g of token t at 2 t + g); u as in kvref_rtn. */
+void kvref_rtn_g64(const double *Y, const double *r, const float *c32, int bits, uint8_t *q,
+                   float *s32, float *z32, double *u)
+{
+    int t, d, g;
+    int qmax = (1 << bits) - 1;
+    for (t = 0; t < NTOK; ++t) {
+        for (g = 0; g < NCH / G64; ++g) {
+            double xn[G64];
+            double mn = INFINITY, mx = -INFINITY, s, z;
+            for (d = 0; d < G64; ++d) {
+                int c = g * G64 + d;
+                xn[d] = Y[t * NCH + c] / (r[t] * (double)c32[c]);
+                if (xn[d] < mn) mn = xn[d];
+                if (xn[d] > mx) mx = xn[d];
+            }
+            z = mn;
+            s = (mx - mn) / qmax;
+            s32[2 * t + g] = (float)(r[t] * s);
+            z32[2 * t + g] = (float)(r[t] * z);
+            for (d = 0; d < G64; ++d) {
+                int c = g * G64 + d;
+                double ud = 0.0;
+                long qi = 0;
+                if (s > 0.0) {
+                    ud = (xn[d] - z) / s;
+                    qi = (long)nearbyint(ud);      /* ties to even */
+                    if (qi < 0) qi = 0;
+                    if (qi > qmax) qi = qmax;
+                }
+                q[t * NCH + c] = (uint8_t)qi;
+                if (u) u[t * NCH + c] = ud;
+            }
+        }
+    }
+}
+
 /* ------------------------------------------------------------------ */
 /* Packing into a page record                                          */
 /* ------------------------------------------------------------------ */
@@ -552,13 +607,72 @@ void kvref_unpack_part_pc(const uint8_t *rec, int is_v, uint8_t *q, float *r32, 
     }
 }
 
+/* Format "g64": codes as in the other formats (at this format's offsets), two
+ * {s', z'} pairs per token, c_d per channel.  s32, z32: [NTOK][2]. */
+void kvref_pack_part_g64(uint8_t *rec, int is_v, const uint8_t *q, const float *s32,
+                         const float *z32, const float *c32)
+{
+    rec_layout L = layout_of(3), L0 = layout_of(0);
+    long sz = is_v ? L.vsz : L.ksz, cc = is_v ? L.vc : L.kc;
+    uint8_t tmp[REC_BYTES];
+    float zero[NTOK];
+    int t, d, g;
+    memset(zero, 0, sizeof(zero));
+    /* the codes: the shared packer into a scratch record, copied across */
+    kvref_pack_part_fmt(tmp, is_v, q, zero, zero, zero, 0);
+    if (is_v)
+        memcpy(rec + L.vcodes, tmp + L0.vcodes, NTOK * NCH / 4);
+    else
+        memcpy(rec + L.kcodes, tmp + L0.kcodes, NTOK * NCH / 2);
+    for (t = 0; t < NTOK; ++t)
+        for (g = 0; g < 2; ++g) {
+            put_f32(rec + sz + 16 * t + 8 * g, s32[2 * t + g]);
+            put_f32(rec + sz + 16 * t + 8 * g + 4, z32[2 * t + g]);
+        }
+    for (d = 0; d < NCH; ++d) put_f32(rec + cc + 4 * d, c32[d]);
+}
+
+void kvref_unpack_part_g64(const uint8_t *rec, int is_v, uint8_t *q, float *s32, float *z32,
+                           float *c32)
+{
+    rec_layout L = layout_of(3), L0 = layout_of(0);
+    long sz = is_v ? L.vsz : L.ksz, cc = is_v ? L.vc : L.kc;
+    uint8_t tmp[REC_BYTES];
+    float a[NTOK], b[NTOK], c[NCH];
+    int t, d, g;
+    memset(tmp, 0, sizeof(tmp));
+    if (is_v)
+        memcpy(tmp + L0.vcodes, rec + L.vcodes, NTOK * NCH / 4);
+    else
+        memcpy(tmp + L0.kcodes, rec + L.kcodes, NTOK * NCH / 2);
+    kvref_unpack_part_fmt(tmp, is_v, q, a, b, c, 0);   /* the codes */
+    for (t = 0; t < NTOK; ++t)
+        for (g = 0; g < 2; ++g) {
+            s32[2 * t + g] = get_f32(rec + sz + 16 * t + 8 * g);
+            z32[2 * t + g] = get_f32(rec + sz + 16 * t + 8 * g + 4);
+        }
+    for (d = 0; d < NCH; ++d) c32[d] = get_f32(rec + cc + 4 * d);
+}
+
 /* Dequantized rotated tile from a record: yhat_td = c_d (s'_t q_td + z'_t), or
- * for "_pc" yhat_td = r_t (cs_d q_td + cz_d). */
+ * for "_pc" yhat_td = r_t (cs_d q_td + cz_d), or for "g64"
+ * yhat_td = c_d (s'_{t,g} q_td + z'_{t,g}) with g = d / 64. */
 void kvref_dequant_part_fmt(const uint8_t *rec, int is_v, int fmt, double *yhat)
 {
     uint8_t q[NTOK * NCH];
     float a32[NTOK], b32[NTOK > NCH ? NTOK : NCH], c32[NCH];
     int t, d;
+    if (fmt == 3) {
+        float s2[2 * NTOK], z2[2 * NTOK];
+        kvref_unpack_part_g64(rec, is_v, q, s2, z2, c32);
+        for (t = 0; t < NTOK; ++t)
+            for (d = 0; d < NCH; ++d) {
+                int g = d / G64;
+                yhat[t * NCH + d] = (double)c32[d] * ((double)s2[2 * t + g] * q[t * NCH + d] +
+                                                      (double)z2[2 * t + g]);
+            }
+        return;
+    }
     if (fmt == 2) {
         kvref_unpack_part_pc(rec, is_v, q, a32, b32, c32);
         for (t = 0; t < NTOK; ++t)
@@ -612,6 +726,10 @@ void kvref_quantize_tile_fmt(const uint16_t *x, long ld_tok, int is_v, int iters
         float r32[NTOK], cs32[NCH], cz32[NCH];
         kvref_rtn_pc(Y, r, c32, bits, q, r32, cs32, cz32, u_out);
         if (rec) kvref_pack_part_pc(rec, is_v, q, r32, cs32, cz32);
+    } else if (fmt == 3) {
+        float s2[2 * NTOK], z2[2 * NTOK];
+        kvref_rtn_g64(Y, r, c32, bits, q, s2, z2, u_out);
+        if (rec) kvref_pack_part_g64(rec, is_v, q, s2, z2, c32);
     } else {
         kvref_rtn(Y, r, c32, bits, q, s32, z32, u_out);
         if (rec) kvref_pack_part_fmt(rec, is_v, q, s32, z32, c32, fmt);

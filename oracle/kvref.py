@@ -26,17 +26,19 @@ NCH = 128
 NTOK = 128
 REC_BYTES = 15360
 REC_BYTES_M16 = 13824      # format variant "_m16": metadata stored as fp16
+REC_BYTES_G64 = 17408      # format variant "k4v2_g64": two groups per token
 
 
-def rec_bytes(meta16: bool = False, pc: bool = False) -> int:
-    return REC_BYTES_M16 if meta16 and not pc else REC_BYTES
+def _fmt(meta16: bool = False, pc: bool = False, g64: bool = False) -> int:
+    """Record format code of the C oracle: 0 fp32 metadata, 1 "_m16", 2 "_pc",
+    3 "g64"; the variants do not combine."""
+    if int(meta16) + int(pc) + int(g64) > 1:
+        raise ValueError("the _m16, _pc and g64 variants do not combine")
+    return 3 if g64 else 2 if pc else 1 if meta16 else 0
 
 
-def _fmt(meta16: bool, pc: bool) -> int:
-    """Record format code of the C oracle: 0 fp32 metadata, 1 "_m16", 2 "_pc"."""
-    if meta16 and pc:
-        raise ValueError("the _pc variant has fp32 metadata only")
-    return 2 if pc else 1 if meta16 else 0
+def rec_bytes(meta16: bool = False, pc: bool = False, g64: bool = False) -> int:
+    return {0: REC_BYTES, 1: REC_BYTES_M16, 2: REC_BYTES, 3: REC_BYTES_G64}[_fmt(meta16, pc, g64)]
 
 _lib = None
 
@@ -71,6 +73,9 @@ def lib():
         L.kvref_pack_part_pc.argtypes = [P, ctypes.c_int, P, P, P, P]
         L.kvref_unpack_part_pc.argtypes = [P, ctypes.c_int, P, P, P, P]
         L.kvref_rtn_pc.argtypes = [P, P, P, ctypes.c_int, P, P, P, P, P]
+        L.kvref_rtn_g64.argtypes = [P, P, P, ctypes.c_int, P, P, P, P]
+        L.kvref_pack_part_g64.argtypes = [P, ctypes.c_int, P, P, P, P]
+        L.kvref_unpack_part_g64.argtypes = [P, ctypes.c_int, P, P, P, P]
         L.kvref_f32_to_f16.argtypes = [ctypes.c_float]
         L.kvref_f32_to_f16.restype = ctypes.c_uint16
         L.kvref_record_bytes.argtypes = [ctypes.c_int]
@@ -232,23 +237,47 @@ def rtn_pc(Y, r, c32, bits: int):
     return q, r32, cs, cz, u
 
 
-def dequant_part(rec, is_v: bool, meta16: bool = False, pc: bool = False) -> np.ndarray:
+def rtn_g64(Y, r, c32, bits: int):
+    """Format "g64": RTN with two groups of 64 channels per token;
+    (q, s32 [128][2], z32 [128][2], u)."""
+    Y = _c(Y, np.float64)
+    q = np.zeros((NTOK, NCH), dtype=np.uint8)
+    s = np.zeros((NTOK, 2), dtype=np.float32)
+    z = np.zeros((NTOK, 2), dtype=np.float32)
+    u = np.zeros((NTOK, NCH))
+    lib().kvref_rtn_g64(_p(Y), _p(_c(r, np.float64)), _p(_c(c32, np.float32)), bits, _p(q),
+                        _p(s), _p(z), _p(u))
+    return q, s, z, u
+
+
+def unpack_part_g64(rec, is_v: bool):
+    """Format "g64": (codes, s' [128][2], z' [128][2], c)."""
+    q = np.zeros((NTOK, NCH), dtype=np.uint8)
+    s = np.zeros((NTOK, 2), dtype=np.float32)
+    z = np.zeros((NTOK, 2), dtype=np.float32)
+    c = np.zeros(NCH, dtype=np.float32)
+    lib().kvref_unpack_part_g64(_p(_c(rec, np.uint8)), int(is_v), _p(q), _p(s), _p(z), _p(c))
+    return q, s, z, c
+
+
+def dequant_part(rec, is_v: bool, meta16: bool = False, pc: bool = False,
+                 g64: bool = False) -> np.ndarray:
     y = np.zeros((NTOK, NCH), dtype=np.float64)
-    lib().kvref_dequant_part_fmt(_p(_c(rec, np.uint8)), int(is_v), _fmt(meta16, pc), _p(y))
+    lib().kvref_dequant_part_fmt(_p(_c(rec, np.uint8)), int(is_v), _fmt(meta16, pc, g64), _p(y))
     return y
 
 
 def quantize_tile(x, is_v: bool, iters: int, rms: bool = False, meta16: bool = False,
-                  pc: bool = False):
+                  pc: bool = False, g64: bool = False):
     """All four stages on one tile; returns a dict of every intermediate."""
     xb = _bits16(x).reshape(NTOK, NCH)
-    rec = np.zeros(rec_bytes(meta16, pc), dtype=np.uint8)
+    rec = np.zeros(rec_bytes(meta16, pc, g64), dtype=np.uint8)
     Y = np.zeros((NTOK, NCH))
     a = np.zeros(NTOK)
     b = np.zeros(NCH)
     q = np.zeros((NTOK, NCH), dtype=np.uint8)
     u = np.zeros((NTOK, NCH))
-    lib().kvref_quantize_tile_fmt(_p(xb), NCH, int(is_v), iters, int(rms), _fmt(meta16, pc),
+    lib().kvref_quantize_tile_fmt(_p(xb), NCH, int(is_v), iters, int(rms), _fmt(meta16, pc, g64),
                                   _p(rec), _p(Y), _p(a), _p(b), _p(q), _p(u))
     return {"rec": rec, "Y": Y, "a": a, "b": b, "q": q, "u": u}
 
@@ -257,7 +286,7 @@ def quantize_tile(x, is_v: bool, iters: int, rms: bool = False, meta16: bool = F
 
 def quantize_blocks(k, v, seq_lens, block_table, num_pages: int, iters: int, pool=None,
                     tail_k=None, tail_v=None, want_u: bool = False, rms: bool = False,
-                    meta16: bool = False, pc: bool = False):
+                    meta16: bool = False, pc: bool = False, g64: bool = False):
     """Prefill: k, v fp16 [B][S][Hkv][128] (contiguous).  Returns a dict with
     the pool [num_pages][Hkv][15360] uint8 ([..][13824] with meta16), the fp16
     tails [B][Hkv][128][128] and, with want_u, the pre-rounding values
@@ -270,7 +299,7 @@ def quantize_blocks(k, v, seq_lens, block_table, num_pages: int, iters: int, poo
     block_table = _c(block_table, np.int32)
     max_blocks = block_table.shape[1]
     if pool is None:
-        pool = np.zeros((num_pages, hkv, rec_bytes(meta16, pc)), dtype=np.uint8)
+        pool = np.zeros((num_pages, hkv, rec_bytes(meta16, pc, g64)), dtype=np.uint8)
     if tail_k is None:
         tail_k = np.zeros((B, hkv, NTOK, NCH), dtype=np.uint16)
     if tail_v is None:
@@ -279,16 +308,16 @@ def quantize_blocks(k, v, seq_lens, block_table, num_pages: int, iters: int, poo
     if want_u:
         u_k = np.zeros((B, max_blocks, hkv, NTOK, NCH))
         u_v = np.zeros((B, max_blocks, hkv, NTOK, NCH))
-    assert pool.shape[-1] == rec_bytes(meta16, pc)
+    assert pool.shape[-1] == rec_bytes(meta16, pc, g64)
     rc = lib().kvref_quantize_blocks_fmt(_p(kb), _p(vb), S * hkv * NCH, hkv * NCH, NCH, B,
                                          _p(seq_lens), _p(block_table), max_blocks, hkv, iters,
-                                         int(rms), _fmt(meta16, pc), _p(pool), num_pages, _p(tail_k),
+                                         int(rms), _fmt(meta16, pc, g64), _p(pool), num_pages, _p(tail_k),
                                          _p(tail_v), _p(u_k), _p(u_v))
     return {"rc": rc, "pool": pool, "tail_k": tail_k, "tail_v": tail_v, "u_k": u_k, "u_v": u_v}
 
 
 def append_token(k_new, v_new, pos, block_table, iters: int, pool, tail_k, tail_v,
-                 rms: bool = False, meta16: bool = False, pc: bool = False):
+                 rms: bool = False, meta16: bool = False, pc: bool = False, g64: bool = False):
     """Decode-time append (in place on pool / tails).  Returns the status."""
     kb = _bits16(k_new)
     vb = _bits16(v_new)
@@ -296,15 +325,15 @@ def append_token(k_new, v_new, pos, block_table, iters: int, pool, tail_k, tail_
     pos = _c(pos, np.int32)
     block_table = _c(block_table, np.int32)
     assert pool.flags["C_CONTIGUOUS"] and tail_k.flags["C_CONTIGUOUS"]
-    assert pool.shape[-1] == rec_bytes(meta16, pc)
+    assert pool.shape[-1] == rec_bytes(meta16, pc, g64)
     return lib().kvref_append_token_fmt(_p(kb), _p(vb), _p(pos), B, _p(block_table),
-                                        block_table.shape[1], hkv, iters, int(rms), _fmt(meta16, pc),
+                                        block_table.shape[1], hkv, iters, int(rms), _fmt(meta16, pc, g64),
                                         _p(pool), pool.shape[0], _p(tail_k), _p(tail_v))
 
 
 def decode_attention(q, pool, block_table, seq_lens, tail_k, tail_v, hq: int, hkv: int,
                      scale: float = 1.0 / np.sqrt(128.0), route: int = 1, meta16: bool = False,
-                     pc: bool = False):
+                     pc: bool = False, g64: bool = False):
     """Decode attention, float64 output [B][Hq][128].  route 0 = textbook
     (un-rotate every token), route 1 = rotated space with one final H."""
     qb = _bits16(q)
@@ -313,11 +342,11 @@ def decode_attention(q, pool, block_table, seq_lens, tail_k, tail_v, hq: int, hk
     block_table = _c(block_table, np.int32)
     seq_lens = _c(seq_lens, np.int32)
     out = np.zeros((B, hq, NCH))
-    assert pool.shape[-1] == rec_bytes(meta16, pc)
+    assert pool.shape[-1] == rec_bytes(meta16, pc, g64)
     rc = lib().kvref_decode_attention_fmt(_p(qb), _p(pool), pool.shape[0], _p(block_table),
                                           block_table.shape[1], _p(seq_lens), B, hq, hkv,
                                           _p(_bits16(tail_k)), _p(_bits16(tail_v)), float(scale),
-                                          int(route), _fmt(meta16, pc), _p(out))
+                                          int(route), _fmt(meta16, pc, g64), _p(out))
     if rc != 0:
         raise ValueError("oracle: page id outside the pool")
     return out
@@ -359,7 +388,7 @@ def attention_fp16(q, k, v, seq_lens, hq: int, hkv: int,
 
 def chunk_attention(q, start, chunk_lens, pool, block_table, tail_k, tail_v, hq: int, hkv: int,
                     scale: float = 1.0 / np.sqrt(128.0), meta16: bool = False,
-                    pc: bool = False) -> np.ndarray:
+                    pc: bool = False, g64: bool = False) -> np.ndarray:
     """Attention of a chunk of new query tokens over the quantized cache
     (chunked prefill), float64 output [B][M][Hq][128].
 
@@ -401,8 +430,10 @@ def chunk_attention(q, start, chunk_lens, pool, block_table, tail_k, tail_v, hq:
             if page < 0 or page >= pool.shape[0]:
                 raise ValueError("oracle: page id outside the pool")
             for h in range(hkv):
-                K[h, j * NTOK:(j + 1) * NTOK] = dequant_part(pool[page, h], False, meta16, pc) @ H
-                V[h, j * NTOK:(j + 1) * NTOK] = dequant_part(pool[page, h], True, meta16, pc) @ H
+                K[h, j * NTOK:(j + 1) * NTOK] = dequant_part(pool[page, h], False, meta16, pc,
+                                                             g64) @ H
+                V[h, j * NTOK:(j + 1) * NTOK] = dequant_part(pool[page, h], True, meta16, pc,
+                                                             g64) @ H
         r = n - nfull * NTOK
         K[:, nfull * NTOK:] = tk[b, :, :r]
         V[:, nfull * NTOK:] = tv[b, :, :r]

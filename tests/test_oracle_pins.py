@@ -1118,3 +1118,110 @@ def test_rms_variant_constant_tile_closed_form(oracle):
         a, b, _ = oracle.sinkhorn(Y, 2, rms=True)
         assert np.allclose(np.exp(a), abs(v) / np.sqrt(128.0), rtol=1e-12)
         assert np.isclose(np.exp(b[0]), 128.0, rtol=1e-12) and np.all(b[1:] == 0.0)
+
+
+# ---------------------------------------------- format variant: group size 64 --
+# Format variant "k4v2_g64" (SURVEY's "G = 64"; the KVarN page names the
+# format kvarn_k4v2_g128 in "Yazilim Gelistirme ve Ogrenme Acisindan Pratik
+# Cikarimlar", g the group size): two RTN groups per token, channels 0-63 and
+# 64-127, each with its own scale and zero; everything else as the default.
+
+def test_g64_rtn_is_the_g128_rtn_of_each_half(oracle):
+    # a row whose two halves are the same 64 values has the same range in each
+    # half as in the whole row: g64 and g128 then give the same codes, and
+    # each group's {s', z'} equals the row's
+    rng = np.random.default_rng(61)
+    half = rng.standard_normal((128, 64)) * np.exp(rng.standard_normal(64))[None, :]
+    Y = np.concatenate([half, half], axis=1)
+    r = np.exp(rng.standard_normal(128))
+    c_half = np.exp(0.5 * rng.standard_normal(64)).astype(np.float32)
+    c32 = np.concatenate([c_half, c_half])
+    for bits in (4, 2):
+        q64, s64, z64, u64 = oracle.rtn_g64(Y, r, c32, bits)
+        q, s, z, u = oracle.rtn(Y, r, c32, bits)
+        assert np.array_equal(q64, q) and np.array_equal(u64, u)
+        for g in (0, 1):
+            assert np.array_equal(s64[:, g], s) and np.array_equal(z64[:, g], z)
+
+
+def test_g64_half_step_bound_and_group_endpoints(oracle):
+    x = _tile(62)
+    for is_v, bits in ((False, 4), (True, 2)):
+        out = oracle.quantize_tile(x, is_v, 2, g64=True)
+        q, s, z, c = oracle.unpack_part_g64(out["rec"], is_v)
+        yhat = oracle.dequant_part(out["rec"], is_v, g64=True)
+        sg = np.repeat(np.abs(s.astype(np.float64)), 64, axis=1)      # [t][d] step of d's group
+        half = 0.5 * sg * c.astype(np.float64)[None, :]
+        slack = 1e-6 * (np.abs(out["Y"]) + np.abs(yhat)) + 1e-9
+        assert np.all(np.abs(out["Y"] - yhat) <= half + slack)
+        for g in (0, 1):
+            qg = q[:, 64 * g:64 * (g + 1)]
+            assert np.all(qg.min(axis=1) == 0) and np.all(qg.max(axis=1) == 2 ** bits - 1)
+
+
+def test_g64_record_bytes_at_the_stated_offsets(oracle):
+    x = _tile(63)
+    for is_v in (False, True):
+        out = oracle.quantize_tile(x, is_v, 2, g64=True)
+        rec = out["rec"]
+        assert rec.size == 17408 == 136 * 128
+        codes = (10752, 14848) if is_v else (0, 8192)
+        sz = rec[(14848 if is_v else 8192):(16896 if is_v else 10240)].view(np.float32)
+        cc = rec[(16896 if is_v else 10240):(17408 if is_v else 10752)].view(np.float32)
+        r = np.exp(out["a"])
+        c32 = np.exp(out["b"]).astype(np.float32)
+        q, s, z, u = oracle.rtn_g64(out["Y"], r, c32, 2 if is_v else 4)
+        assert np.array_equal(q, out["q"])
+        assert np.array_equal(sz.reshape(128, 2, 2)[:, :, 0], s)
+        assert np.array_equal(sz.reshape(128, 2, 2)[:, :, 1], z)
+        assert np.array_equal(cc, c32)
+        rec_q = np.zeros(15360, np.uint8)
+        oracle.pack_part(rec_q, is_v, out["q"], np.zeros(128, np.float32),
+                         np.zeros(128, np.float32), np.zeros(128, np.float32))
+        lo = 9728 if is_v else 0
+        assert np.array_equal(rec[codes[0]:codes[1]], rec_q[lo:lo + codes[1] - codes[0]])
+
+
+def test_g64_attention_matches_torch_sdpa_on_dequantized_cache(oracle):
+    w = synth.scaled(synth.WORKLOADS["llama3_8b_layer"], batch=2, seq=517, hkv=2, hq=4, seed=64)
+    k, v = synth.kv(w)
+    k, v = k.numpy(), v.numpy()
+    lens = np.array([300, 517], np.int32)
+    table = np.array([[5, 1, 3, 7, 0], [2, 6, 4, 8, 9]], np.int32)
+    st = oracle.quantize_blocks(k, v, lens, table, 10, 2, g64=True)
+    assert st["rc"] == 0 and st["pool"].shape == (10, 2, 17408)
+    q = synth.queries(w).numpy()
+    o1 = oracle.decode_attention(q, st["pool"], table, lens, st["tail_k"], st["tail_v"], 4, 2,
+                                 g64=True)
+    o0 = oracle.decode_attention(q, st["pool"], table, lens, st["tail_k"], st["tail_v"], 4, 2,
+                                 route=0, g64=True)
+    assert np.abs(o0 - o1).max() <= 1e-12 * np.abs(o0).max()
+    H = torch.tensor(oracle.hadamard(128))
+    for b in range(2):
+        n = int(lens[b])
+        nfull = n // 128
+        for h in range(4):
+            keys, vals = [], []
+            for j in range(nfull):
+                rec = st["pool"][table[b, j], h // 2]
+                keys.append(torch.tensor(oracle.dequant_part(rec, False, g64=True)) @ H)
+                vals.append(torch.tensor(oracle.dequant_part(rec, True, g64=True)) @ H)
+            keys.append(torch.tensor(k[b, nfull * 128:n, h // 2].astype(np.float64)))
+            vals.append(torch.tensor(v[b, nfull * 128:n, h // 2].astype(np.float64)))
+            ref = torch.nn.functional.scaled_dot_product_attention(
+                torch.tensor(q[b, h].astype(np.float64))[None, None, None],
+                torch.cat(keys)[None, None], torch.cat(vals)[None, None])[0, 0, 0].numpy()
+            assert np.abs(o1[b, h] - ref).max() <= 1e-12 * max(1.0, np.abs(ref).max())
+
+
+def test_g64_append_fills_page_like_prefill(oracle):
+    w = synth.scaled(synth.WORKLOADS["llama3_8b_layer"], batch=1, seq=256, hkv=2, hq=4, seed=65)
+    k, v = synth.kv(w)
+    k, v = k.numpy(), v.numpy()
+    table = np.array([[1, 0]], np.int32)
+    ref = oracle.quantize_blocks(k, v, np.array([256], np.int32), table, 2, 2, g64=True)
+    st = oracle.quantize_blocks(k, v, np.array([250], np.int32), table, 2, 2, g64=True)
+    for t in range(250, 256):
+        assert oracle.append_token(k[:, t], v[:, t], np.array([t], np.int32), table, 2,
+                                   st["pool"], st["tail_k"], st["tail_v"], g64=True) == 0
+    assert np.array_equal(st["pool"], ref["pool"])
