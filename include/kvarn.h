@@ -64,6 +64,16 @@
  *   [9728, 13824) V codes (the same permutation)
  *   [13824,14336) V r_t fp32 per token
  *   [14336,15360) V {cs_d, cz_d} fp32 per channel
+ * Format variant "k4v2_g64" (config group = 64; fp32 metadata, 17408 bytes,
+ * 136 B per token-head): the same stages with two RTN groups per token,
+ * channels 0-63 and 64-127, each with its own {s', z'} (row scale folded in):
+ *   [0,     8192) K codes (as above)
+ *   [8192, 10240) K {s'_0, z'_0, s'_1, z'_1} fp32 per token (token t at 8192 + 16 t)
+ *   [10240,10752) K column scale c_d fp32
+ *   [10752,14848) V codes (the same permutation)
+ *   [14848,16896) V {s'_0, z'_0, s'_1, z'_1} fp32 per token
+ *   [16896,17408) V column scale c_d fp32
+ * kvarn_chunk_attention does not take this format (KVARN_ERR_UNSUPPORTED).
  * Pool = [num_pages][num_kv_heads][kvarn_page_bytes(cfg)].  The newest len mod 128
  * tokens of a sequence stay fp16 in a caller-owned tail buffer
  * [B][num_kv_heads][128 slots][128] per K and V.
@@ -102,6 +112,7 @@ typedef struct CUstream_st *kvarn_stream_t; /* identical to cudaStream_t */
 #define KVARN_BLOCK_TOKENS 128
 #define KVARN_PAGE_BYTES 15360
 #define KVARN_PAGE_BYTES_M16 13824
+#define KVARN_PAGE_BYTES_G64 17408
 
 /* return codes */
 #define KVARN_OK 0
@@ -118,7 +129,9 @@ typedef struct CUstream_st *kvarn_stream_t; /* identical to cudaStream_t */
 typedef struct {
     int head_dim;       /* 128 */
     int block_tokens;   /* 128 */
-    int group;          /* 128: quantization group = one token's channels */
+    int group;          /* 128: quantization group = one token's channels; 64:
+                           format variant "k4v2_g64", two groups per token
+                           (fp32 metadata, not with "_pc") */
     int k_bits;         /* 4 */
     int v_bits;         /* 2 */
     int sinkhorn_iters; /* 0..64; 2 from the iteration-selection rule */
@@ -135,7 +148,8 @@ typedef struct {
 } kvarn_config_t;
 
 /* Fills *out from a format string: "k4v2_g128" or "kvarn_k4v2_g128" (the
- * KVarN page's --kv-cache-dtype value), optionally followed by the variant
+ * KVarN page's --kv-cache-dtype value), or "k4v2_g64" / "kvarn_k4v2_g64" for
+ * groups of 64 channels, optionally followed by the variant
  * suffixes "_rms" (the uncentred statistic), "_m16" (fp16 metadata) and "_pc"
  * (per-channel groups; not with "_m16"), each at most once and in any order,
  * and then "_s<K>" to set the Sinkhorn iteration count.  Returns KVARN_ERR_UNSUPPORTED for any other format,
@@ -147,7 +161,8 @@ int kvarn_config_from_string(const char *s, int num_q_heads, int num_kv_heads,
 int kvarn_config_validate(const kvarn_config_t *cfg);
 
 /* Bytes of one page record (per page and KV head): KVARN_PAGE_BYTES (15360),
- * or KVARN_PAGE_BYTES_M16 (13824) for the "_m16" format; 0 on a bad config.
+ * KVARN_PAGE_BYTES_M16 (13824) for the "_m16" format, or KVARN_PAGE_BYTES_G64
+ * (17408) for groups of 64; 0 on a bad config.
  * Every call that takes a pool reads it with this record size. */
 size_t kvarn_page_bytes(const kvarn_config_t *cfg);
 

@@ -75,23 +75,33 @@ int kvarn_config_validate(const kvarn_config_t* c) {
   if (c->num_q_heads <= 0 || c->num_kv_heads <= 0 || c->num_q_heads % c->num_kv_heads)
     return KVARN_ERR_INVALID_ARG;
   if (c->num_q_heads / c->num_kv_heads > kMaxG) return KVARN_ERR_UNSUPPORTED;
-  if (c->head_dim != kD || c->block_tokens != kT || c->group != kD || c->k_bits != 4 ||
-      c->v_bits != 2)
+  if (c->head_dim != kD || c->block_tokens != kT || (c->group != kD && c->group != 64) ||
+      c->k_bits != 4 || c->v_bits != 2)
     return KVARN_ERR_UNSUPPORTED;
   if (c->sinkhorn_iters < 0 || c->sinkhorn_iters > kMaxIters) return KVARN_ERR_UNSUPPORTED;
   if (c->sinkhorn_rms != 0 && c->sinkhorn_rms != 1) return KVARN_ERR_UNSUPPORTED;
   if (c->meta_fp16 != 0 && c->meta_fp16 != 1) return KVARN_ERR_UNSUPPORTED;
   if (c->per_channel != 0 && c->per_channel != 1) return KVARN_ERR_UNSUPPORTED;
   if (c->per_channel && c->meta_fp16) return KVARN_ERR_UNSUPPORTED;   // fp32 metadata only
+  if (c->group == 64 && (c->per_channel || c->meta_fp16)) return KVARN_ERR_UNSUPPORTED;
   return KVARN_OK;
 }
 
 int kvarn_config_from_string(const char* s, int hq, int hkv, kvarn_config_t* out) {
   if (!s || !out) return KVARN_ERR_INVALID_ARG;
   if (!strncmp(s, "kvarn_", 6)) s += 6;
-  if (strncmp(s, "k4v2_g128", 9)) return KVARN_ERR_UNSUPPORTED;
+  int group;
+  const char* rest;
+  if (!strncmp(s, "k4v2_g128", 9)) {
+    group = kD;
+    rest = s + 9;
+  } else if (!strncmp(s, "k4v2_g64", 8)) {
+    group = 64;
+    rest = s + 8;
+  } else {
+    return KVARN_ERR_UNSUPPORTED;
+  }
   int iters = 2, rms = 0, m16 = 0, pc = 0;
-  const char* rest = s + 9;
   // the variant suffixes, each at most once and in either order, then "_s<K>"
   for (;;) {
     if (!rms && !strncmp(rest, "_rms", 4)) {
@@ -119,7 +129,7 @@ int kvarn_config_from_string(const char* s, int hq, int hkv, kvarn_config_t* out
   kvarn_config_t c;
   c.head_dim = kD;
   c.block_tokens = kT;
-  c.group = kD;
+  c.group = group;
   c.k_bits = 4;
   c.v_bits = 2;
   c.sinkhorn_iters = iters;
@@ -136,6 +146,7 @@ int kvarn_config_from_string(const char* s, int hq, int hkv, kvarn_config_t* out
 
 size_t kvarn_page_bytes(const kvarn_config_t* c) {
   if (kvarn_config_validate(c) != KVARN_OK) return 0;
+  if (c->group == 64) return (size_t)RecFmt<kFmtG64>::bytes;
   return c->meta_fp16 ? (size_t)RecFmt<kFmtM16>::bytes : (size_t)RecFmt<kFmtF32>::bytes;
 }
 
@@ -168,7 +179,7 @@ int kvarn_quantize_blocks(const kvarn_config_t* cfg, const void* k, const void* 
   a.hkv = cfg->num_kv_heads;
   a.iters = cfg->sinkhorn_iters;
   a.rms = cfg->sinkhorn_rms;
-  a.fmt = fmt_of(cfg->meta_fp16, cfg->per_channel);
+  a.fmt = fmt_of(cfg->meta_fp16, cfg->per_channel, cfg->group);
   a.max_seq = max_seq;
   a.seq_lens = seq_lens;
   a.block_table = block_table;
@@ -205,7 +216,7 @@ int kvarn_append_token(const kvarn_config_t* cfg, const void* k_new, const void*
   a.hkv = cfg->num_kv_heads;
   a.iters = cfg->sinkhorn_iters;
   a.rms = cfg->sinkhorn_rms;
-  a.fmt = fmt_of(cfg->meta_fp16, cfg->per_channel);
+  a.fmt = fmt_of(cfg->meta_fp16, cfg->per_channel, cfg->group);
   a.block_table = block_table;
   a.max_blocks = max_blocks;
   a.pool = static_cast<uint8_t*>(pool);
@@ -285,7 +296,7 @@ int kvarn_decode_attention(const kvarn_config_t* cfg, const void* q, const void*
   a.pages_per_split = p.pages_per_split;
   a.nsplit = p.nsplit;
   a.cluster = 0;   // the kernel's launcher decides
-  a.fmt = fmt_of(cfg->meta_fp16, cfg->per_channel);
+  a.fmt = fmt_of(cfg->meta_fp16, cfg->per_channel, cfg->group);
   a.status = status;
   cudaError_t e = decode_mma_supported(a.g) ? launch_decode_mma(a, (cudaStream_t)stream)
                                             : launch_decode_simple(a, (cudaStream_t)stream);
@@ -310,6 +321,9 @@ int kvarn_chunk_attention(const kvarn_config_t* cfg, const void* q, int chunk_ma
       !aligned16(out))
     return KVARN_ERR_INVALID_ARG;
   if (!(softmax_scale > 0.f) || softmax_scale != softmax_scale) return KVARN_ERR_INVALID_ARG;
+  // the g64 record (17408 bytes) does not fit the kernel's two record buffers
+  // next to its six operand tiles
+  if (cfg->group == 64) return KVARN_ERR_UNSUPPORTED;
   const int g = cfg->num_q_heads / cfg->num_kv_heads;
   const int tq = chunk_rows_per_tile(g);
   const int64_t ntq = ((int64_t)chunk_max + tq - 1) / tq;
@@ -334,7 +348,7 @@ int kvarn_chunk_attention(const kvarn_config_t* cfg, const void* q, int chunk_ma
   a.tail_v = static_cast<const __half*>(tail_v);
   a.scale_log2 = softmax_scale * 1.4426950408889634f;
   a.out = static_cast<__half*>(out);
-  a.fmt = fmt_of(cfg->meta_fp16, cfg->per_channel);
+  a.fmt = fmt_of(cfg->meta_fp16, cfg->per_channel, cfg->group);
   a.status = status;
   return launch_chunk_attention(a, (cudaStream_t)stream) == cudaSuccess ? KVARN_OK
                                                                          : KVARN_ERR_LAUNCH;

@@ -51,7 +51,7 @@ constexpr float kTwo24 = 16777216.0f;
 
 template <int NT>
 struct __align__(128) MmaSmem {
-  uint8_t rec[kWarps][kRec];     // per warp: K part at 0, V part at the format's kpart
+  uint8_t rec[kWarps][kRecMax];  // per warp: K part at 0, V part at the format's kpart
   float qrot[4 * NT][kD];        // H q per (padded) query head of the group
   float qplain[4 * NT][kD];      // q itself, for the fp16 tail
   uint64_t bar[kWarps][2];       // per warp: 0 = K part landed, 1 = V part landed
@@ -158,6 +158,7 @@ __device__ __forceinline__ constexpr float vpos_inv(int kb, int f) {
 template <int NT, int FMT>
 __global__ void __launch_bounds__(kThreads, NT == 1 ? 3 : 2) decode_mma_kernel(DecodeArgs a) {
   using F = RecFmt<FMT>;
+  constexpr int NG = F::g64 ? 2 : 1;     // channel groups with their own s', z'
   extern __shared__ __align__(128) uint8_t smem_raw[];
   MmaSmem<NT>& S = *reinterpret_cast<MmaSmem<NT>*>(smem_raw);
   constexpr int G = 4 * NT;
@@ -297,113 +298,137 @@ __global__ void __launch_bounds__(kThreads, NT == 1 ? 3 : 2) decode_mma_kernel(D
       kph ^= 1;
       k_busy = false;
 
-      // ---- query-side B fragments: qc = q~ * cK, scaled, split hi / lo ----
-      // B column n = r: head 4nt + (r >> 1), hi part (r even) or lo part (r
-      // odd); k rows 2qi.. of k-tile kb hold channels 32qi + c0, c0 + 4 with
+      // ---- per channel group (one for the per-token formats, two for g64,
+      // whose groups of 64 channels carry their own s', z'): query-side B
+      // fragments, then the scores of the group's k-tiles ----
+      // B fragments: qc = q~ * beta^K, scaled, split hi / lo.  B column n = r:
+      // head 4nt + (r >> 1), hi part (r even) or lo part (r odd); k rows 2qi..
+      // of k-tile kb hold channels g0 + c0, c0 + 4 with g0 the lane's first
+      // channel of the group (32 qi; for g64 64 gi + 16 qi) and
       // c0 = 8 (kb >> 1) + 2 (kb & 1) + slot.  The slot-1 channels meet codes
       // carrying 16x (nibble at bits 4-7) and are pre-scaled by 1/16.
-      uint32_t bq[NT][8][2];
-      float sA[NT], sZ[NT];
+      constexpr int KB = 8 / NG;             // k-tiles per group
+      constexpr int CPL = 32 / NG;           // channels per lane per group
       const bool odd = r & 1;
 #pragma unroll
-      for (int nt = 0; nt < NT; ++nt) {
-        const int h = 4 * nt + (r >> 1);
-        const float4* qv = reinterpret_cast<const float4*>(S.qrot[h]);
-        const uint8_t* cv = kst + F::kc;   // beta, delta of channels 32 qi + 4k .. (8 qi + k)
-        float v[32];
-        float am0 = 0.f, am1 = 0.f;
-        float2 s0 = make_float2(0.f, 0.f), s1 = s0;
+      for (int gi = 0; gi < NG; ++gi) {
+        uint32_t bq[NT][KB][2];
+        float sA[NT], sZ[NT];
 #pragma unroll
-        for (int k = 0; k < 8; ++k) {
-          const float4 q4 = qv[(8 * qi + k) ^ qi], c4 = F::get_b4(cv, 8 * qi + k);
-          const float2 p0 = __fmul2_rn(make_float2(q4.x, q4.y), make_float2(c4.x, c4.y));
-          const float2 p1 = __fmul2_rn(make_float2(q4.z, q4.w), make_float2(c4.z, c4.w));
-          v[4 * k + 0] = p0.x;
-          v[4 * k + 1] = p0.y;
-          v[4 * k + 2] = p1.x;
-          v[4 * k + 3] = p1.y;
-          am0 = max3(am0, fabsf(p0.x), fabsf(p0.y));
-          am1 = max3(am1, fabsf(p1.x), fabsf(p1.y));
-          if constexpr (F::pc) {   // the constant term takes delta, not beta
-            const float4 d4 = F::get_d4(cv, 8 * qi + k);
-            s0 = __ffma2_rn(make_float2(q4.x, q4.y), make_float2(d4.x, d4.y), s0);
-            s1 = __ffma2_rn(make_float2(q4.z, q4.w), make_float2(d4.z, d4.w), s1);
-          } else {
-            s0 = __fadd2_rn(s0, p0);
-            s1 = __fadd2_rn(s1, p1);
+        for (int nt = 0; nt < NT; ++nt) {
+          const int h = 4 * nt + (r >> 1);
+          const float4* qv = reinterpret_cast<const float4*>(S.qrot[h]);
+          const uint8_t* cv = kst + F::kc;   // beta, delta of the lane's channels
+          float v[CPL];
+          float am0 = 0.f, am1 = 0.f;
+          float2 s0 = make_float2(0.f, 0.f), s1 = s0;
+#pragma unroll
+          for (int k = 0; k < CPL / 4; ++k) {
+            const int ch = (NG == 1 ? 32 * qi : 64 * gi + 16 * qi) + 4 * k;
+            const int idx = ch >> 2;
+            const float4 q4 = qv[((idx ^ (ch >> 5)) & 7) | (idx & ~7)];   // qrot_pos
+            const float4 c4 = F::get_b4(cv, idx);
+            const float2 p0 = __fmul2_rn(make_float2(q4.x, q4.y), make_float2(c4.x, c4.y));
+            const float2 p1 = __fmul2_rn(make_float2(q4.z, q4.w), make_float2(c4.z, c4.w));
+            v[4 * k + 0] = p0.x;
+            v[4 * k + 1] = p0.y;
+            v[4 * k + 2] = p1.x;
+            v[4 * k + 3] = p1.y;
+            am0 = max3(am0, fabsf(p0.x), fabsf(p0.y));
+            am1 = max3(am1, fabsf(p1.x), fabsf(p1.y));
+            if constexpr (F::pc) {   // the constant term takes delta, not beta
+              const float4 d4 = F::get_d4(cv, idx);
+              s0 = __ffma2_rn(make_float2(q4.x, q4.y), make_float2(d4.x, d4.y), s0);
+              s1 = __ffma2_rn(make_float2(q4.z, q4.w), make_float2(d4.z, d4.w), s1);
+            } else {
+              s0 = __fadd2_rn(s0, p0);
+              s1 = __fadd2_rn(s1, p1);
+            }
           }
-        }
-        float amax = fmaxf(am0, am1);
-        const float2 s01 = __fadd2_rn(s0, s1);
-        float sum = s01.x + s01.y;
-        amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
-        amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
-        sum += __shfl_xor_sync(0xffffffffu, sum, 1);
-        sum += __shfl_xor_sync(0xffffffffu, sum, 2);
-        float scl, inv;
-        pow2_scale(amax, scl, inv);
-        const float scl16 = scl * 0.0625f;
+          float amax = fmaxf(am0, am1);
+          const float2 s01 = __fadd2_rn(s0, s1);
+          float sum = s01.x + s01.y;
+          amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
+          amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
+          sum += __shfl_xor_sync(0xffffffffu, sum, 1);
+          sum += __shfl_xor_sync(0xffffffffu, sum, 2);
+          float scl, inv;
+          pow2_scale(amax, scl, inv);
+          const float scl16 = scl * 0.0625f;
 #pragma unroll
-        for (int kb = 0; kb < 8; ++kb) {
+          for (int kb = 0; kb < KB; ++kb) {
 #pragma unroll
-          for (int slot = 0; slot < 2; ++slot) {
-            const int c0 = 8 * (kb >> 1) + 2 * (kb & 1) + slot;
-            const float f = slot ? scl16 : scl;
-            // |x| < 2^15 (slot 0) or 2^11 (slot 1): grid 16 or 1, i.e. 16
-            // in the units of the code it meets
-            const float2 x = __fmul2_rn(make_float2(v[c0], v[c0 + 4]), make_float2(f, f));
-            const float2 h = grid_hi2(x, slot ? kMagic1 : 16.f * kMagic1);
-            const float2 o = odd ? __ffma2_rn(h, make_float2(-1.f, -1.f), x) : h;   // lo | hi
-            bq[nt][kb][slot] = pack2(o.x, o.y);
+            for (int slot = 0; slot < 2; ++slot) {
+              const int c0 = 8 * (kb >> 1) + 2 * (kb & 1) + slot;
+              const float f = slot ? scl16 : scl;
+              // |x| < 2^15 (slot 0) or 2^11 (slot 1): grid 16 or 1, i.e. 16
+              // in the units of the code it meets
+              const float2 x = __fmul2_rn(make_float2(v[c0], v[c0 + 4]), make_float2(f, f));
+              const float2 hg = grid_hi2(x, slot ? kMagic1 : 16.f * kMagic1);
+              const float2 o = odd ? __ffma2_rn(hg, make_float2(-1.f, -1.f), x) : hg;   // lo | hi
+              bq[nt][kb][slot] = pack2(o.x, o.y);
+            }
           }
+          // this lane's score column pair (2qi, 2qi+1) is head 4nt + qi, held
+          // by lanes with r = 2qi: fetch that head's scale and sum
+          sA[nt] = __shfl_sync(0xffffffffu, inv, 8 * qi) * (kTwo24 * sl2);
+          sZ[nt] = __shfl_sync(0xffffffffu, sum, 8 * qi) * sl2;
         }
-        // this lane's score column pair (2qi, 2qi+1) is head 4nt + qi, held
-        // by lanes with r = 2qi: fetch that head's scale and sum
-        sA[nt] = __shfl_sync(0xffffffffu, inv, 8 * qi) * (kTwo24 * sl2);
-        sZ[nt] = __shfl_sync(0xffffffffu, sum, 8 * qi) * sl2;
-      }
 
-      // ---- scores: K codes (A, rows = tokens) x qc (B).  MTG token tiles at
-      // a time, k-tile outer, so that MTG accumulator chains interleave ----
-      constexpr int MTG = NT == 1 ? 8 : 4;
+        // ---- scores: K codes (A, rows = tokens) x qc (B).  MTG token tiles
+        // at a time, k-tile outer, so that MTG accumulator chains interleave.
+        // The lane's code words of a token row: 4 words at 16 qi (one group)
+        // or 2 words at 32 gi + 8 qi (g64) ----
+        constexpr int MTG = NT == 1 ? 8 : 4;
 #pragma unroll
-      for (int m0 = 0; m0 < 8; m0 += MTG) {
-        uint4 kw[MTG][2];
-#pragma unroll
-        for (int i = 0; i < MTG; ++i) {
-          const int tA = 16 * (m0 + i) + r;
-          kw[i][0] = *reinterpret_cast<const uint4*>(kst + kOffKCodes + 64 * tA + 16 * qi);
-          kw[i][1] = *reinterpret_cast<const uint4*>(kst + kOffKCodes + 64 * (tA + 8) + 16 * qi);
-        }
-        float d[NT][MTG][4];
-#pragma unroll
-        for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-          for (int i = 0; i < MTG; ++i) d[nt][i][0] = d[nt][i][1] = d[nt][i][2] = d[nt][i][3] = 0.f;
-#pragma unroll
-        for (int kb = 0; kb < 8; ++kb) {
+        for (int m0 = 0; m0 < 8; m0 += MTG) {
+          uint4 kw[MTG][2];
 #pragma unroll
           for (int i = 0; i < MTG; ++i) {
-            uint32_t wa = word_of(kw[i][0], kb >> 1), wb = word_of(kw[i][1], kb >> 1);
-            if (kb & 1) {
-              wa >>= 8;
-              wb >>= 8;
+            const int tA = 16 * (m0 + i) + r;
+            if constexpr (NG == 1) {
+              kw[i][0] = *reinterpret_cast<const uint4*>(kst + kOffKCodes + 64 * tA + 16 * qi);
+              kw[i][1] = *reinterpret_cast<const uint4*>(kst + kOffKCodes + 64 * (tA + 8) + 16 * qi);
+            } else {
+              const uint2 wA = *reinterpret_cast<const uint2*>(kst + 64 * tA + 32 * gi + 8 * qi);
+              const uint2 wB =
+                  *reinterpret_cast<const uint2*>(kst + 64 * (tA + 8) + 32 * gi + 8 * qi);
+              kw[i][0] = make_uint4(wA.x, wA.y, 0u, 0u);
+              kw[i][1] = make_uint4(wB.x, wB.y, 0u, 0u);
             }
-            const uint32_t A[4] = {wa & 0x000F000Fu, wb & 0x000F000Fu, wa & 0x00F000F0u,
-                                   wb & 0x00F000F0u};
-#pragma unroll
-            for (int nt = 0; nt < NT; ++nt) mma_16816(d[nt][i], A, bq[nt][kb][0], bq[nt][kb][1]);
           }
-        }
+          float d[NT][MTG][4];
 #pragma unroll
-        for (int i = 0; i < MTG; ++i) {
-          const int mt = m0 + i, tA = 16 * mt + r, tB = tA + 8;
-          const float2 szA = F::get_sz(kst + F::ksz, tA);
-          const float2 szB = F::get_sz(kst + F::ksz, tB);
+          for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
-          for (int nt = 0; nt < NT; ++nt) {
-            sc[nt][2 * mt] = fmaf(szA.x * sA[nt], d[nt][i][0] + d[nt][i][1], szA.y * sZ[nt]);
-            sc[nt][2 * mt + 1] = fmaf(szB.x * sA[nt], d[nt][i][2] + d[nt][i][3], szB.y * sZ[nt]);
+            for (int i = 0; i < MTG; ++i) d[nt][i][0] = d[nt][i][1] = d[nt][i][2] = d[nt][i][3] = 0.f;
+#pragma unroll
+          for (int kb = 0; kb < KB; ++kb) {
+#pragma unroll
+            for (int i = 0; i < MTG; ++i) {
+              uint32_t wa = word_of(kw[i][0], kb >> 1), wb = word_of(kw[i][1], kb >> 1);
+              if (kb & 1) {
+                wa >>= 8;
+                wb >>= 8;
+              }
+              const uint32_t A[4] = {wa & 0x000F000Fu, wb & 0x000F000Fu, wa & 0x00F000F0u,
+                                     wb & 0x00F000F0u};
+#pragma unroll
+              for (int nt = 0; nt < NT; ++nt) mma_16816(d[nt][i], A, bq[nt][kb][0], bq[nt][kb][1]);
+            }
+          }
+#pragma unroll
+          for (int i = 0; i < MTG; ++i) {
+            const int mt = m0 + i, tA = 16 * mt + r, tB = tA + 8;
+            const float2 szA = F::get_sz_g(kst + F::ksz, tA, gi);
+            const float2 szB = F::get_sz_g(kst + F::ksz, tB, gi);
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt) {
+              const float xA = fmaf(szA.x * sA[nt], d[nt][i][0] + d[nt][i][1], szA.y * sZ[nt]);
+              const float xB = fmaf(szB.x * sA[nt], d[nt][i][2] + d[nt][i][3], szB.y * sZ[nt]);
+              sc[nt][2 * mt] = gi == 0 ? xA : sc[nt][2 * mt] + xA;
+              sc[nt][2 * mt + 1] = gi == 0 ? xB : sc[nt][2 * mt + 1] + xB;
+            }
           }
         }
       }
@@ -448,96 +473,100 @@ __global__ void __launch_bounds__(kThreads, NT == 1 ? 3 : 2) decode_mma_kernel(D
       vph ^= 1;
       v_busy = false;
 
-      // ---- P' = p s'V (scaled, hi | lo) transposed into B fragments ----
+      // ---- per channel group (two for g64): P' = p s'V (scaled, hi | lo)
+      // transposed into B fragments, then the value sums of the group's
+      // channel tiles (16 channels each; channels 64 gi .. for g64) ----
       // score slot j of this lane is token 16 (j >> 1) + 8 (j & 1) + r
-      float2 szv[16];
-      float sm4[4] = {0.f, 0.f, 0.f, 0.f};
+      const uint8_t* cvv = vst + (F::vc - F::kpart);
 #pragma unroll
-      for (int j = 0; j < 16; ++j) {
-        szv[j] = F::get_sz(vst + (F::vsz - F::kpart), 16 * (j >> 1) + 8 * (j & 1) + r);
-        sm4[j & 3] = fmaxf(sm4[j & 3], szv[j].x);
-      }
-      float smax = fmaxf(fmaxf(sm4[0], sm4[1]), fmaxf(sm4[2], sm4[3]));
-      smax = warp_max_r(smax);
-      float fs, finv;
-      pow2_scale(smax, fs, finv);
-      float sf[16];
-#pragma unroll
-      for (int j = 0; j < 16; ++j) sf[j] = szv[j].x * (fs * vpos_inv(j >> 1, j & 1));
-      uint32_t bp[NT][8][2];
-      float zpage[NT];
-#pragma unroll
-      for (int nt = 0; nt < NT; ++nt) {
-        float zq[4] = {0.f, 0.f, 0.f, 0.f};
+      for (int gi = 0; gi < NG; ++gi) {
+        float2 szv[16];
+        float sm4[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
         for (int j = 0; j < 16; ++j) {
-          // x <= 2^15 / 4^pos for a code carrying 4^pos: grid 16 / 4^pos
-          const float x = sc[nt][j] * sf[j];
-          const float hi = grid_hi(x, (16.f * kMagic1) * vpos_inv(j >> 1, j & 1));
-          bp[nt][j >> 1][j & 1] = movm_trans(pack2(hi, x - hi));
-          zq[j & 3] = fmaf(sc[nt][j], szv[j].y, zq[j & 3]);
+          szv[j] = F::get_sz_g(vst + (F::vsz - F::kpart), 16 * (j >> 1) + 8 * (j & 1) + r, gi);
+          sm4[j & 3] = fmaxf(sm4[j & 3], szv[j].x);
         }
-        zpage[nt] = warp_sum_r((zq[0] + zq[1]) + (zq[2] + zq[3]));
-      }
+        float smax = fmaxf(fmaxf(sm4[0], sm4[1]), fmaxf(sm4[2], sm4[3]));
+        smax = warp_max_r(smax);
+        float fs, finv;
+        pow2_scale(smax, fs, finv);
+        float sf[16];
+#pragma unroll
+        for (int j = 0; j < 16; ++j) sf[j] = szv[j].x * (fs * vpos_inv(j >> 1, j & 1));
+        uint32_t bp[NT][8][2];
+        float zpage[NT];
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) {
+          float zq[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+          for (int j = 0; j < 16; ++j) {
+            // x <= 2^15 / 4^pos for a code carrying 4^pos: grid 16 / 4^pos
+            const float x = sc[nt][j] * sf[j];
+            const float hi = grid_hi(x, (16.f * kMagic1) * vpos_inv(j >> 1, j & 1));
+            bp[nt][j >> 1][j & 1] = movm_trans(pack2(hi, x - hi));
+            zq[j & 3] = fmaf(sc[nt][j], szv[j].y, zq[j & 3]);
+          }
+          zpage[nt] = warp_sum_r((zq[0] + zq[1]) + (zq[2] + zq[3]));
+        }
 
-      // ---- value sum: V codes (A, rows = channels) x P' (B).  MCG channel
-      // tiles at a time, k-tile outer, so that their chains interleave ----
-      const float fin = finv * kTwo24;
-      const uint8_t* cvv = vst + (F::vc - F::kpart);
-      constexpr int MCG = NT == 1 ? 8 : 4;
+        // ---- value sum: V codes (A, rows = channels) x P' (B).  MCG channel
+        // tiles at a time, k-tile outer, so that their chains interleave ----
+        const float fin = finv * kTwo24;
+        constexpr int MCG = (NT == 1 ? 8 : 4) / NG;
 #pragma unroll
-      for (int c0 = 0; c0 < 8; c0 += MCG) {
-        uint4 vw[MCG];   // words (e, h) = 00, 01, 10, 11 of channels 16mc + r, + 8
+        for (int c0 = 8 * gi / NG; c0 < 8 * (gi + 1) / NG; c0 += MCG) {
+          uint4 vw[MCG];   // words (e, h) = 00, 01, 10, 11 of channels 16mc + r, + 8
 #pragma unroll
-        for (int i = 0; i < MCG; ++i)
-          vw[i] = *reinterpret_cast<const uint4*>(vst + 512 * (c0 + i) +
-                                                  16 * lane);
-        float d[NT][MCG][4];
+          for (int i = 0; i < MCG; ++i)
+            vw[i] = *reinterpret_cast<const uint4*>(vst + 512 * (c0 + i) + 16 * lane);
+          float d[NT][MCG][4];
 #pragma unroll
-        for (int nt = 0; nt < NT; ++nt)
+          for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
-          for (int i = 0; i < MCG; ++i) d[nt][i][0] = d[nt][i][1] = d[nt][i][2] = d[nt][i][3] = 0.f;
+            for (int i = 0; i < MCG; ++i) d[nt][i][0] = d[nt][i][1] = d[nt][i][2] = d[nt][i][3] = 0.f;
 #pragma unroll
-        for (int hh = 0; hh < 2; ++hh) {
+          for (int hh = 0; hh < 2; ++hh) {
 #pragma unroll
-          for (int jj = 0; jj < 4; ++jj) {
-            const int kb = 4 * hh + jj;
+            for (int jj = 0; jj < 4; ++jj) {
+              const int kb = 4 * hh + jj;
 #pragma unroll
-            for (int i = 0; i < MCG; ++i) {
-              const uint32_t e0 = word_of(vw[i], hh), e1 = word_of(vw[i], 2 + hh);
-              uint32_t A[4];
-              if (jj == 0) {
-                A[0] = e0 & cmask(0); A[1] = e1 & cmask(0); A[2] = e0 & cmask(1); A[3] = e1 & cmask(1);
-              } else if (jj == 1) {
-                A[0] = e0 & cmask(2); A[1] = e1 & cmask(2); A[2] = e0 & cmask(3); A[3] = e1 & cmask(3);
-              } else if (jj == 2) {
-                A[0] = e0 & cmask(4); A[1] = e1 & cmask(4);
-                A[2] = (e0 >> 10) & cmask(0); A[3] = (e1 >> 10) & cmask(0);
-              } else {
-                A[0] = (e0 >> 10) & cmask(1); A[1] = (e1 >> 10) & cmask(1);
-                A[2] = (e0 >> 10) & cmask(2); A[3] = (e1 >> 10) & cmask(2);
+              for (int i = 0; i < MCG; ++i) {
+                const uint32_t e0 = word_of(vw[i], hh), e1 = word_of(vw[i], 2 + hh);
+                uint32_t A[4];
+                if (jj == 0) {
+                  A[0] = e0 & cmask(0); A[1] = e1 & cmask(0); A[2] = e0 & cmask(1); A[3] = e1 & cmask(1);
+                } else if (jj == 1) {
+                  A[0] = e0 & cmask(2); A[1] = e1 & cmask(2); A[2] = e0 & cmask(3); A[3] = e1 & cmask(3);
+                } else if (jj == 2) {
+                  A[0] = e0 & cmask(4); A[1] = e1 & cmask(4);
+                  A[2] = (e0 >> 10) & cmask(0); A[3] = (e1 >> 10) & cmask(0);
+                } else {
+                  A[0] = (e0 >> 10) & cmask(1); A[1] = (e1 >> 10) & cmask(1);
+                  A[2] = (e0 >> 10) & cmask(2); A[3] = (e1 >> 10) & cmask(2);
+                }
+#pragma unroll
+                for (int nt = 0; nt < NT; ++nt) mma_16816(d[nt][i], A, bp[nt][kb][0], bp[nt][kb][1]);
               }
-#pragma unroll
-              for (int nt = 0; nt < NT; ++nt) mma_16816(d[nt][i], A, bp[nt][kb][0], bp[nt][kb][1]);
             }
           }
-        }
 #pragma unroll
-        for (int i = 0; i < MCG; ++i) {
-          const int mc = c0 + i;
-          const float2 bdA = F::get_bd(cvv, 16 * mc + r), bdB = F::get_bd(cvv, 16 * mc + 8 + r);
+          for (int i = 0; i < MCG; ++i) {
+            const int mc = c0 + i;
+            const float2 bdA = F::get_bd(cvv, 16 * mc + r), bdB = F::get_bd(cvv, 16 * mc + 8 + r);
 #pragma unroll
-          for (int nt = 0; nt < NT; ++nt) {
-            float uA, uB;
-            if constexpr (F::pc) {
-              uA = fmaf(bdA.x, (d[nt][i][0] + d[nt][i][1]) * fin, bdA.y * zpage[nt]);
-              uB = fmaf(bdB.x, (d[nt][i][2] + d[nt][i][3]) * fin, bdB.y * zpage[nt]);
-            } else {   // beta = delta = c
-              uA = bdA.x * fmaf(d[nt][i][0] + d[nt][i][1], fin, zpage[nt]);
-              uB = bdB.x * fmaf(d[nt][i][2] + d[nt][i][3], fin, zpage[nt]);
+            for (int nt = 0; nt < NT; ++nt) {
+              float uA, uB;
+              if constexpr (F::pc) {
+                uA = fmaf(bdA.x, (d[nt][i][0] + d[nt][i][1]) * fin, bdA.y * zpage[nt]);
+                uB = fmaf(bdB.x, (d[nt][i][2] + d[nt][i][3]) * fin, bdB.y * zpage[nt]);
+              } else {   // beta = delta = c
+                uA = bdA.x * fmaf(d[nt][i][0] + d[nt][i][1], fin, zpage[nt]);
+                uB = bdB.x * fmaf(d[nt][i][2] + d[nt][i][3], fin, zpage[nt]);
+              }
+              oacc[nt][2 * mc] = fmaf(oacc[nt][2 * mc], alpha[nt], uA);
+              oacc[nt][2 * mc + 1] = fmaf(oacc[nt][2 * mc + 1], alpha[nt], uB);
             }
-            oacc[nt][2 * mc] = fmaf(oacc[nt][2 * mc], alpha[nt], uA);
-            oacc[nt][2 * mc + 1] = fmaf(oacc[nt][2 * mc + 1], alpha[nt], uB);
           }
         }
       }
@@ -893,6 +922,7 @@ int decode_mma_ctas_per_sm(int g) {
 cudaError_t launch_decode_mma(const DecodeArgs& a, cudaStream_t s) {
   if (a.fmt == kFmtM16) return a.g <= 4 ? launch_nt<1, kFmtM16>(a, s) : launch_nt<2, kFmtM16>(a, s);
   if (a.fmt == kFmtPC) return a.g <= 4 ? launch_nt<1, kFmtPC>(a, s) : launch_nt<2, kFmtPC>(a, s);
+  if (a.fmt == kFmtG64) return a.g <= 4 ? launch_nt<1, kFmtG64>(a, s) : launch_nt<2, kFmtG64>(a, s);
   return a.g <= 4 ? launch_nt<1, kFmtF32>(a, s) : launch_nt<2, kFmtF32>(a, s);
 }
 

@@ -22,13 +22,14 @@ namespace {
 constexpr int kThreads = 128;
 
 struct __align__(16) DecodeSmem {
-  uint8_t rec[kRec];
+  uint8_t rec[kRecMax];
   float qrot[kMaxG][kD];   // H q, per head
   float qraw[kMaxG][kD];   // q, per head (tail scores)
   float qc[kMaxG][kD];     // H q * c^K, per page
   float pw[kMaxG][kT];     // p_t * s'^V_t, per page
+  float pw1[kMaxG][kT];    //   of the second channel group (g64)
   float red[kThreads / 32][kMaxG];
-  float m[kMaxG], l[kMaxG], alpha[kMaxG], sq[kMaxG], zs[kMaxG];
+  float m[kMaxG], l[kMaxG], alpha[kMaxG], sq[kMaxG], zs[kMaxG], sq1[kMaxG], zs1[kMaxG];
   int ticket;
 };
 
@@ -130,29 +131,46 @@ __global__ void __launch_bounds__(kThreads) decode_simple_kernel(DecodeArgs a) {
       // qc = H q * beta^K (thread = channel), and sum_d H q * delta^K per head
       {
         const float2 bd = F::get_bd(S.rec + F::kc, tid);
-        float part[kMaxG];
+        float part[kMaxG], part1[kMaxG];
         for (int h = 0; h < g; ++h) {
           const float x = S.qrot[h][tid] * bd.x;
           S.qc[h][tid] = x;
           part[h] = F::pc ? S.qrot[h][tid] * bd.y : x;
+          if (F::g64) {   // channel groups 0-63 and 64-127
+            part1[h] = tid >= 64 ? part[h] : 0.f;
+            part[h] = tid < 64 ? part[h] : 0.f;
+          }
         }
         block_reduce<false>(S, part, g, S.sq);
+        if (F::g64) block_reduce<false>(S, part1, g, S.sq1);
       }
       // scores (thread = token)
       {
         const uint32_t* row = reinterpret_cast<const uint32_t*>(S.rec + kOffKCodes + 64 * tid);
-        const float2 sz = F::get_sz(S.rec + F::ksz, tid);
-        for (int h = 0; h < g; ++h) sc[h] = 0.f;
+        const float2 sz = F::get_sz_g(S.rec + F::ksz, tid, 0);
+        float sc1[kMaxG];
+        for (int h = 0; h < g; ++h) sc[h] = sc1[h] = 0.f;
         for (int w = 0; w < 16; ++w) {
           const uint32_t word = row[w];
 #pragma unroll
           for (int e = 0; e < 8; ++e) {
             const float code = (float)((word >> (4 * e)) & 15u);
             const int d = 8 * w + e;
-            for (int h = 0; h < g; ++h) sc[h] = fmaf(S.qc[h][d], code, sc[h]);
+            if (F::g64 && w >= 8) {   // channels 64..127: the second group
+              for (int h = 0; h < g; ++h) sc1[h] = fmaf(S.qc[h][d], code, sc1[h]);
+            } else {
+              for (int h = 0; h < g; ++h) sc[h] = fmaf(S.qc[h][d], code, sc[h]);
+            }
           }
         }
-        for (int h = 0; h < g; ++h) sc[h] = a.scale * fmaf(sz.x, sc[h], sz.y * S.sq[h]);
+        if (F::g64) {
+          const float2 sz1 = F::get_sz_g(S.rec + F::ksz, tid, 1);
+          for (int h = 0; h < g; ++h)
+            sc[h] = a.scale * (fmaf(sz.x, sc[h], sz.y * S.sq[h]) +
+                               fmaf(sz1.x, sc1[h], sz1.y * S.sq1[h]));
+        } else {
+          for (int h = 0; h < g; ++h) sc[h] = a.scale * fmaf(sz.x, sc[h], sz.y * S.sq[h]);
+        }
       }
     } else {
       // fp16 tail tokens 0..rem-1 (thread = token), plain space
@@ -183,13 +201,21 @@ __global__ void __launch_bounds__(kThreads) decode_simple_kernel(DecodeArgs a) {
     float p[kMaxG];
     for (int h = 0; h < g; ++h) p[h] = sc[h] == -INFINITY ? 0.f : __expf(sc[h] - S.m[h]);
     if (u < nfull) {
-      const float2 szv = F::get_sz(S.rec + F::vsz, tid);
+      const float2 szv = F::get_sz_g(S.rec + F::vsz, tid, 0);
       float zp[kMaxG];
       for (int h = 0; h < g; ++h) {
         S.pw[h][tid] = p[h] * szv.x;
         zp[h] = p[h] * szv.y;
       }
       block_reduce<false>(S, zp, g, S.zs);
+      if (F::g64) {   // the second channel group's s', z'
+        const float2 szv1 = F::get_sz_g(S.rec + F::vsz, tid, 1);
+        for (int h = 0; h < g; ++h) {
+          S.pw1[h][tid] = p[h] * szv1.x;
+          zp[h] = p[h] * szv1.y;
+        }
+        block_reduce<false>(S, zp, g, S.zs1);
+      }
       block_reduce<false>(S, p, g, S.sq);  // S.sq: the page's sum of p per head
       if (tid < g) S.l[tid] = S.l[tid] * S.alpha[tid] + S.sq[tid];
       __syncthreads();
@@ -198,6 +224,10 @@ __global__ void __launch_bounds__(kThreads) decode_simple_kernel(DecodeArgs a) {
         const int d = tid;
         const uint32_t* vw = reinterpret_cast<const uint32_t*>(S.rec + F::kpart);
         const float2 bdv = F::get_bd(S.rec + F::vc, d);
+        // the channel's group: its s'^V-weighted probabilities and z' sum
+        const bool second = F::g64 && d >= 64;
+        float (*pw)[kT] = second ? S.pw1 : S.pw;
+        const float* zs = second ? S.zs1 : S.zs;
         float pv[kMaxG];
         for (int h = 0; h < g; ++h) pv[h] = 0.f;
         for (int w = 0; w < 8; ++w) {
@@ -207,11 +237,11 @@ __global__ void __launch_bounds__(kThreads) decode_simple_kernel(DecodeArgs a) {
           for (int e = 0; e < 16; ++e) {
             const float code = (float)((word >> (2 * e)) & 3u);
             const int t = v_token(j, hh, e);
-            for (int h = 0; h < g; ++h) pv[h] = fmaf(S.pw[h][t], code, pv[h]);
+            for (int h = 0; h < g; ++h) pv[h] = fmaf(pw[h][t], code, pv[h]);
           }
         }
         for (int h = 0; h < g; ++h) {
-          const float u = F::pc ? fmaf(bdv.x, pv[h], bdv.y * S.zs[h]) : bdv.x * (pv[h] + S.zs[h]);
+          const float u = F::pc ? fmaf(bdv.x, pv[h], bdv.y * zs[h]) : bdv.x * (pv[h] + zs[h]);
           acc[h] = fmaf(acc[h], S.alpha[h], u);
           acc_tail[h] *= S.alpha[h];
         }
@@ -301,6 +331,7 @@ cudaError_t launch_simple(const DecodeArgs& a, cudaStream_t s) {
 cudaError_t launch_decode_simple(const DecodeArgs& a, cudaStream_t s) {
   if (a.fmt == kFmtM16) return launch_simple<kFmtM16>(a, s);
   if (a.fmt == kFmtPC) return launch_simple<kFmtPC>(a, s);
+  if (a.fmt == kFmtG64) return launch_simple<kFmtG64>(a, s);
   return launch_simple<kFmtF32>(a, s);
 }
 

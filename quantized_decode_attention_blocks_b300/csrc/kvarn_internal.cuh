@@ -36,24 +36,47 @@ constexpr int kVPart = kRec - kKPart;  // V part: [9728, 15360)
 //   [0, 8192) K codes, [8192, 8704) K r_t fp32, [8704, 9728) K {cs_d, cz_d}
 //   fp32 pairs, [9728, 13824) V codes, [13824, 14336) V r_t, [14336, 15360) V
 //   {cs_d, cz_d}.
+// 3 = "k4v2_g64", two RTN groups per token (channels 0-63, 64-127), each with
+// its own {s', z'} (the row scale folded in):
+//   [0, 8192) K codes, [8192, 10240) K {s'_0, z'_0, s'_1, z'_1} fp32 per
+//   token, [10240, 10752) K c_d, [10752, 14848) V codes, [14848, 16896) V
+//   {s', z'} x 2, [16896, 17408) V c_d.
 // Every format dequantizes as yhat_td = alpha_t beta_d q_td + gamma_t delta_d:
-// (alpha, gamma) = (s', z') and beta = delta = c_d for formats 0 and 1,
-// alpha = gamma = r_t and (beta, delta) = (cs_d, cz_d) for format 2.  The
-// accessors take the address of the field (record part + offset).
-constexpr int kFmtF32 = 0, kFmtM16 = 1, kFmtPC = 2;
+// (alpha, gamma) = (s', z') (of d's group for format 3) and beta = delta = c_d
+// for formats 0, 1 and 3, alpha = gamma = r_t and (beta, delta) = (cs_d, cz_d)
+// for format 2.  The accessors take the address of the field (record part +
+// offset).
+constexpr int kFmtF32 = 0, kFmtM16 = 1, kFmtPC = 2, kFmtG64 = 3;
+constexpr int kRecMax = 17408;    // the largest record (format 3)
 template <int FMT>
 struct RecFmt {
   static constexpr bool m16 = FMT == kFmtM16;
   static constexpr bool pc = FMT == kFmtPC;
-  static constexpr int bytes = m16 ? 13824 : 15360;
-  static constexpr int kpart = m16 ? 8960 : 9728;   // K part [0, kpart)
+  static constexpr bool g64 = FMT == kFmtG64;
+  static constexpr int bytes = m16 ? 13824 : g64 ? 17408 : 15360;
+  static constexpr int kpart = m16 ? 8960 : g64 ? 10752 : 9728;   // K part [0, kpart)
   static constexpr int vpart = bytes - kpart;       // V part [kpart, bytes)
   static constexpr int ksz = 8192;                  // per-token fields
-  static constexpr int kc = m16 ? 8704 : pc ? 8704 : 9216;     // per-channel fields
-  static constexpr int vsz = m16 ? 13056 : 13824;   // from the record start
-  static constexpr int vc = m16 ? 13568 : pc ? 14336 : 14848;
+  static constexpr int kc = m16 ? 8704 : pc ? 8704 : g64 ? 10240 : 9216;   // per-channel fields
+  static constexpr int vsz = m16 ? 13056 : g64 ? 14848 : 13824;   // from the record start
+  static constexpr int vc = m16 ? 13568 : pc ? 14336 : g64 ? 16896 : 14848;
+  // (alpha_t, gamma_t) of token t for the channels of group g (g = 0 unless
+  // g64)
+  static __device__ __forceinline__ float2 get_sz_g(const uint8_t* f, int t, int g) {
+    if constexpr (g64)
+      return reinterpret_cast<const float2*>(f)[2 * t + g];
+    else
+      return get_sz(f, t);
+  }
+  static __device__ __forceinline__ void put_sz_g(uint8_t* f, int t, int g, float s, float z) {
+    if constexpr (g64)
+      reinterpret_cast<float2*>(f)[2 * t + g] = make_float2(s, z);
+    else
+      put_sz(f, t, s, z);
+  }
   // (alpha_t, gamma_t) of token t
   static __device__ __forceinline__ float2 get_sz(const uint8_t* f, int t) {
+    static_assert(!g64, "the g64 format has two pairs per token (get_sz_g)");
     if constexpr (m16) {
       return __half22float2(reinterpret_cast<const __half2*>(f)[t]);
     } else if constexpr (pc) {
@@ -65,6 +88,7 @@ struct RecFmt {
   }
   static __device__ __forceinline__ void put_sz(uint8_t* f, int t, float s, float z) {
     static_assert(!pc, "the per-channel format stores r_t (put_r)");
+    static_assert(!g64, "the g64 format has two pairs per token (put_sz_g)");
     if constexpr (m16)
       reinterpret_cast<__half2*>(f)[t] = __floats2half2_rn(s, z);
     else
@@ -128,11 +152,14 @@ static_assert(RecFmt<kFmtF32>::bytes == kRec && RecFmt<kFmtF32>::kpart == kKPart
 static_assert(RecFmt<kFmtM16>::kpart % 16 == 0 && RecFmt<kFmtM16>::vpart % 16 == 0 &&
                   RecFmt<kFmtM16>::bytes % 16 == 0 && RecFmt<kFmtM16>::vsz % 16 == 0 &&
                   RecFmt<kFmtM16>::vc % 16 == 0 && RecFmt<kFmtM16>::kc % 16 == 0 &&
-                  RecFmt<kFmtPC>::kc % 16 == 0 && RecFmt<kFmtPC>::vc % 16 == 0,
+                  RecFmt<kFmtPC>::kc % 16 == 0 && RecFmt<kFmtPC>::vc % 16 == 0 &&
+                  RecFmt<kFmtG64>::kpart % 16 == 0 && RecFmt<kFmtG64>::vpart % 16 == 0 &&
+                  RecFmt<kFmtG64>::kc % 16 == 0 && RecFmt<kFmtG64>::vsz % 16 == 0 &&
+                  RecFmt<kFmtG64>::vc % 16 == 0 && RecFmt<kFmtG64>::bytes == kRecMax,
               "bulk copies and vector loads need 16-byte parts and fields");
 // The format code of a configuration.
-__host__ __device__ constexpr int fmt_of(int meta16, int per_channel) {
-  return per_channel ? kFmtPC : meta16 ? kFmtM16 : kFmtF32;
+__host__ __device__ constexpr int fmt_of(int meta16, int per_channel, int group) {
+  return group == 64 ? kFmtG64 : per_channel ? kFmtPC : meta16 ? kFmtM16 : kFmtF32;
 }
 
 // Split-K partial state per (sequence, query head, split): m, l, 2 pad, o[128]

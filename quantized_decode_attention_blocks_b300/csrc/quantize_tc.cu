@@ -80,13 +80,14 @@ struct TileInfo {
 struct __align__(1024) QSmem {
   uint8_t hs[kTileBytes];                // +-1 Sylvester matrix, fp16, swizzled
   uint8_t x[kWG][2][kTileBytes];         // input tiles, 2 stages per pipeline
-  __align__(128) uint8_t out[kWG][kKPart];   // packed record part, staged for the bulk store
+  __align__(128) uint8_t out[kWG][RecFmt<kFmtG64>::kpart];   // packed record part (the
+                                                             // largest), staged for the bulk store
   __align__(16) float ra[kWG][kT];       // 1 / r_t, in units of Y
   float r1part[kWG][2][kT];              // first row step of the next tile: half sums
   float r1x0[kWG][kT];                   //   and channel 0
   __align__(16) float cb[kWG][kD];       // 1 / c, indexed by Y column (channel chan_of(n))
-  __align__(16) float vmin[kWG][kT];     // V: per-token min of x
-  __align__(16) float vinv[kWG][kT];     // V: per-token 3 / (max - min)
+  __align__(16) float vmin[kWG][2 * kT]; // V: per-token (and group) min of x
+  __align__(16) float vinv[kWG][2 * kT]; // V: per-token (and group) 3 / (max - min)
   __align__(16) float cc[kWG][kD];       // c_d, natural channel order
   TileInfo info[kWG][2];                 // tile held in each stage
   uint64_t full[kWG][2];                 // stage loaded (producer -> pipeline)
@@ -212,6 +213,19 @@ __device__ __forceinline__ float quad_min(float x) {
 __device__ __forceinline__ float quad_max(float x) {
   x = fmaxf(x, __shfl_xor_sync(0xffffffffu, x, 1));
   return fmaxf(x, __shfl_xor_sync(0xffffffffu, x, 2));
+}
+
+// Minimum and maximum over the threads holding one RTN group of a fragment
+// row: the quad (128 channels), or a pair of it (groups of 64 channels).
+template <bool G64>
+__device__ __forceinline__ float grp_min(float x) {
+  if constexpr (G64) return fminf(x, __shfl_xor_sync(0xffffffffu, x, 1));
+  else return quad_min(x);
+}
+template <bool G64>
+__device__ __forceinline__ float grp_max(float x) {
+  if constexpr (G64) return fmaxf(x, __shfl_xor_sync(0xffffffffu, x, 1));
+  else return quad_max(x);
 }
 
 // The weights of this thread's fragment columns 8k + 2q + b (f indexed by
@@ -730,13 +744,15 @@ __global__ void __launch_bounds__(kQThreads, 1)
           }
 #pragma unroll
         for (int e = 0; e < 2; ++e) {
-          const float lo = quad_min(mn[e]), hi = quad_max(mx[e]);
+          // the thread's channels 32q .. 32q + 31 lie in group q >> 1 of g64
+          constexpr bool G64 = RecFmt<FMT>::g64;
+          const float lo = grp_min<G64>(mn[e]), hi = grp_max<G64>(mx[e]);
           const float range = hi - lo;
           const float inv = range > 0.f ? __fdividef(15.f, range) : 0.f;
           const int t = frow(e);
-          if (q == 0)
-            RecFmt<FMT>::put_sz(out + RecFmt<FMT>::ksz, t, range * (kInvSqrt128 / 15.f),
-                                lo * kInvSqrt128);
+          if ((q & (G64 ? 1 : 3)) == 0)
+            RecFmt<FMT>::put_sz_g(out + RecFmt<FMT>::ksz, t, G64 ? q >> 1 : 0,
+                                  range * (kInvSqrt128 / 15.f), lo * kInvSqrt128);
           // u = (x - min) (15 / range) + 1.5 * 2^23: the code in the low bits
           const float2 nm = make_float2(-lo, -lo), iv = make_float2(inv, inv);
           uint32_t acc[4];
@@ -775,14 +791,16 @@ __global__ void __launch_bounds__(kQThreads, 1)
           }
 #pragma unroll
         for (int e = 0; e < 2; ++e) {
-          const float lo = quad_min(mn[e]), hi = quad_max(mx[e]);
+          constexpr bool G64 = RecFmt<FMT>::g64;
+          const float lo = grp_min<G64>(mn[e]), hi = grp_max<G64>(mx[e]);
           const float range = hi - lo;
           const int t = frow(e);
-          if (q == 0) {
-            S.vmin[wg][t] = lo;
-            S.vinv[wg][t] = range > 0.f ? __fdividef(3.f, range) : 0.f;
-            RecFmt<FMT>::put_sz(out + (RecFmt<FMT>::vsz - RecFmt<FMT>::kpart), t,
-                                range * (kInvSqrt128 / 3.f), lo * kInvSqrt128);
+          if ((q & (G64 ? 1 : 3)) == 0) {
+            const int grp = G64 ? q >> 1 : 0;
+            S.vmin[wg][grp * kT + t] = lo;
+            S.vinv[wg][grp * kT + t] = range > 0.f ? __fdividef(3.f, range) : 0.f;
+            RecFmt<FMT>::put_sz_g(out + (RecFmt<FMT>::vsz - RecFmt<FMT>::kpart), t, grp,
+                                  range * (kInvSqrt128 / 3.f), lo * kInvSqrt128);
           }
         }
       }
@@ -793,19 +811,23 @@ __global__ void __launch_bounds__(kQThreads, 1)
         tmem_wait_ld();
         float2 cd2[2];
         uint32_t acc[2][2];
+        int gofs[2];   // the row's channel group (g64) in the per-token arrays
 #pragma unroll
         for (int e = 0; e < 2; ++e) {
           const float cd = cb[frow(e)];
           cd2[e] = make_float2(cd, cd);
           acc[e][0] = acc[e][1] = 0u - kMagicV;
+          gofs[e] = RecFmt<FMT>::g64 ? (chan_of(frow(e)) >> 6) * kT : 0;
         }
 #pragma unroll
         for (int k = 0; k < 16; ++k) {
-          const float2 m2 = *reinterpret_cast<const float2*>(S.vmin[wg] + 8 * k + 2 * q);
-          const float2 i2 = *reinterpret_cast<const float2*>(S.vinv[wg] + 8 * k + 2 * q);
-          const float2 nm = make_float2(-m2.x, -m2.y);
 #pragma unroll
           for (int e = 0; e < 2; ++e) {
+            const float2 m2 =
+                *reinterpret_cast<const float2*>(S.vmin[wg] + gofs[e] + 8 * k + 2 * q);
+            const float2 i2 =
+                *reinterpret_cast<const float2*>(S.vinv[wg] + gofs[e] + 8 * k + 2 * q);
+            const float2 nm = make_float2(-m2.x, -m2.y);
             const float2 d = __ffma2_rn(pair(v, k, e), cd2[e], nm);
             const float2 f = __ffma2_rn(d, i2, mg);
             acc[e][k >> 3] += __float_as_uint(f.x) << (2 * (k & 7));
@@ -934,6 +956,7 @@ cudaError_t launch_fmt(int fmt, const CUtensorMap& mk, const CUtensorMap& mv,
                        const QTileArgs& qa, const QCopyArgs& cp, cudaStream_t s) {
   if (fmt == kFmtM16) return launch_tiles<kFmtM16>(mk, mv, qa, cp, s);
   if (fmt == kFmtPC) return launch_tiles<kFmtPC>(mk, mv, qa, cp, s);
+  if (fmt == kFmtG64) return launch_tiles<kFmtG64>(mk, mv, qa, cp, s);
   return launch_tiles<kFmtF32>(mk, mv, qa, cp, s);
 }
 

@@ -21,6 +21,7 @@ HEAD_DIM = 128
 BLOCK_TOKENS = 128
 PAGE_BYTES = 15360
 PAGE_BYTES_M16 = 13824     # KVARN_PAGE_BYTES_M16: format variant "_m16"
+PAGE_BYTES_G64 = 17408     # KVARN_PAGE_BYTES_G64: format variant "k4v2_g64"
 FP8_PAGE_BYTES = 33792     # KVARN_FP8_PAGE_BYTES
 FP16_PAGE_BYTES = 65536            # KVARN_FP16_PAGE_BYTES
 NOALLOC_SCRATCH_BYTES = 4 << 20   # KVARN_NOALLOC_SCRATCH_BYTES
@@ -55,6 +56,8 @@ class Config(ctypes.Structure):
     @property
     def page_bytes(self) -> int:
         """Bytes of one page record of this format (kvarn_page_bytes)."""
+        if self.group == 64:
+            return PAGE_BYTES_G64
         return PAGE_BYTES_M16 if self.meta_fp16 else PAGE_BYTES
 
 

@@ -49,19 +49,36 @@ def _compare_pc(tag, got, ref, is_v, bits):
     _, rg, csg, czg = kvref.unpack_part_pc(got, is_v)
     _, rr, csr, czr = kvref.unpack_part_pc(ref, is_v)
     for name, g_, r_ in (("r", rg, rr), ("cs", csg, csr)):
-        g64, r64 = g_.astype(np.float64), r_.astype(np.float64)
-        tol = np.where(r64 == 0, 1e-12, 1e-5 * np.abs(r64))
-        err = np.abs(g64 - r64)
+        gd, rd = g_.astype(np.float64), r_.astype(np.float64)
+        tol = np.where(rd == 0, 1e-12, 1e-5 * np.abs(rd))
+        err = np.abs(gd - rd)
         assert np.all(err <= tol), (f"{tag}.{name}: worst rel err "
-                                    f"{(err / np.maximum(np.abs(r64), 1e-30)).max():.3e}")
+                                    f"{(err / np.maximum(np.abs(rd), 1e-30)).max():.3e}")
     tolz = np.maximum(1e-5 * (np.abs(czr.astype(np.float64))
                               + np.abs(csr.astype(np.float64)) * (2 ** bits - 1)), 1e-12)
     errz = np.abs(czg.astype(np.float64) - czr.astype(np.float64))
     assert np.all(errz <= tolz), f"{tag}.cz: worst err {errz.max():.3e}"
 
 
+def _compare_g64(tag, got, ref, is_v, bits):
+    """Format "g64": the s', c and z' rules of the default format, per group."""
+    _, sg, zg, cg = kvref.unpack_part_g64(got, is_v)
+    _, sr, zr, cr = kvref.unpack_part_g64(ref, is_v)
+    for name, g_, r_ in (("s", sg, sr), ("c", cg, cr)):
+        gd, rd = g_.astype(np.float64), r_.astype(np.float64)
+        tol = np.where(rd == 0, 1e-12, 1e-5 * np.abs(rd))
+        err = np.abs(gd - rd)
+        assert np.all(err <= tol), (f"{tag}.{name}: worst rel err "
+                                    f"{(err / np.maximum(np.abs(rd), 1e-30)).max():.3e}")
+    tolz = np.maximum(1e-5 * (np.abs(zr.astype(np.float64))
+                              + sr.astype(np.float64) * (2 ** bits - 1)), 1e-12)
+    errz = np.abs(zg.astype(np.float64) - zr.astype(np.float64))
+    assert np.all(errz <= tolz), f"{tag}.z: worst err {errz.max():.3e}"
+
+
 def compare_record(got: np.ndarray, ref: np.ndarray, u_k=None, u_v=None, stats=None,
-                   meta16: bool = False, ref32: np.ndarray = None, pc: bool = False):
+                   meta16: bool = False, ref32: np.ndarray = None, pc: bool = False,
+                   g64: bool = False):
     """Compares one record (GPU) with the oracle's.  u_k, u_v: oracle
     pre-rounding values [128][128] (token, channel).  meta16: the "_m16"
     format, whose metadata is judged against ref32, the oracle's record of
@@ -69,10 +86,10 @@ def compare_record(got: np.ndarray, ref: np.ndarray, u_k=None, u_v=None, stats=N
     out = {} if stats is None else stats
     for is_v, u in ((False, u_k), (True, u_v)):
         bits = 2 if is_v else 4
-        if pc:
-            qg = kvref.unpack_part_pc(got, is_v)[0]
-            qr = kvref.unpack_part_pc(ref, is_v)[0]
-            sg = zg = cg = sr = zr = cr = None
+        if pc or g64:
+            unpack = kvref.unpack_part_pc if pc else kvref.unpack_part_g64
+            qg = unpack(got, is_v)[0]
+            qr = unpack(ref, is_v)[0]
         else:
             qg, sg, zg, cg = kvref.unpack_part(got, is_v, meta16)
             qr, sr, zr, cr = kvref.unpack_part(ref, is_v, meta16)
@@ -91,17 +108,20 @@ def compare_record(got: np.ndarray, ref: np.ndarray, u_k=None, u_v=None, stats=N
         if pc:
             _compare_pc(tag, got, ref, is_v, bits)
             continue
+        if g64:
+            _compare_g64(tag, got, ref, is_v, bits)
+            continue
         if meta16:
             _, s32, z32, c32 = kvref.unpack_part(ref32, is_v)
             for name, g_, r_, r32 in (("s", sg, sr, s32), ("z", zg, zr, z32), ("c", cg, cr, c32)):
                 _compare_meta16(f"{tag}.{name}", g_, r_, r32)
             continue
         for name, g_, r_ in (("s", sg, sr), ("c", cg, cr)):
-            g64, r64 = g_.astype(np.float64), r_.astype(np.float64)
-            tol = np.where(r64 == 0, 1e-12, 1e-5 * np.abs(r64))
-            err = np.abs(g64 - r64)
+            gd, rd = g_.astype(np.float64), r_.astype(np.float64)
+            tol = np.where(rd == 0, 1e-12, 1e-5 * np.abs(rd))
+            err = np.abs(gd - rd)
             assert np.all(err <= tol), (f"{tag}.{name}: worst rel err "
-                                        f"{(err / np.maximum(np.abs(r64), 1e-30)).max():.3e}")
+                                        f"{(err / np.maximum(np.abs(rd), 1e-30)).max():.3e}")
         tolz = 1e-5 * (np.abs(zr.astype(np.float64)) + sr.astype(np.float64) * (2 ** bits - 1))
         tolz = np.maximum(tolz, 1e-12)
         errz = np.abs(zg.astype(np.float64) - zr.astype(np.float64))

@@ -37,7 +37,8 @@ def test_library_exports_every_declared_symbol():
 def test_header_constants_match_binding():
     text = open(HEADER).read()
     for name, val in (("KVARN_PAGE_BYTES", K.PAGE_BYTES),
-                      ("KVARN_PAGE_BYTES_M16", K.PAGE_BYTES_M16), ("KVARN_OK", K.OK),
+                      ("KVARN_PAGE_BYTES_M16", K.PAGE_BYTES_M16),
+                      ("KVARN_PAGE_BYTES_G64", K.PAGE_BYTES_G64), ("KVARN_OK", K.OK),
                       ("KVARN_ERR_INVALID_ARG", K.ERR_INVALID_ARG),
                       ("KVARN_ERR_UNSUPPORTED", K.ERR_UNSUPPORTED),
                       ("KVARN_ERR_WORKSPACE", K.ERR_WORKSPACE), ("KVARN_ERR_LAUNCH", K.ERR_LAUNCH),
@@ -85,7 +86,14 @@ def test_config_parsing():
             kv.config_from_string(bad, 12, 2)
     p.meta_fp16 = 1
     assert kv.config_validate(p) == K.ERR_UNSUPPORTED
-    for bad in ("k4v4_g128", "k4v2_g64", "k4v2_g128_x", "k4v2_g128_s", "k4v2_g128_s999"):
+    # groups of 64 channels: "k4v2_g64", with "_rms" but not "_m16" / "_pc"
+    g = kv.config_from_string("kvarn_k4v2_g64_rms_s3", 12, 2)
+    assert g.group == 64 and g.sinkhorn_rms == 1 and g.sinkhorn_iters == 3
+    assert kv.page_bytes(g) == 17408 == 136 * 128 == g.page_bytes
+    for bad in ("k4v2_g64_m16", "k4v2_g64_pc", "k4v2_g32"):
+        with pytest.raises(kv.KvarnError):
+            kv.config_from_string(bad, 12, 2)
+    for bad in ("k4v4_g128", "k4v2_g96", "k4v2_g128_x", "k4v2_g128_s", "k4v2_g128_s999"):
         with pytest.raises(kv.KvarnError) as e:
             kv.config_from_string(bad, 32, 8)
         assert e.value.code == K.ERR_UNSUPPORTED

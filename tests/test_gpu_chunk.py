@@ -153,3 +153,18 @@ def test_chunk_prefill_workload_sampled():
                                     np.arange(mb, dtype=np.int32)[None], host(tk[b:b + 1]),
                                     host(tv[b:b + 1]), w.hq, w.hkv)
         parity.compare_attention(host(out[b:b + 1]).astype(np.float64), ref)
+
+
+def test_g64_format_is_refused():
+    # the g64 record does not fit the kernel's record buffers: the call says
+    # so before any launch
+    cfg = config(8, 2, g64=True)
+    q = torch.zeros((1, 4, 8, 128), dtype=torch.float16, device=DEV)
+    pool = kv.alloc_pool(cfg, 2, DEV)
+    tk, tv = kv.alloc_tails(cfg, 1, DEV)
+    one = torch.tensor([4], dtype=torch.int32, device=DEV)
+    with pytest.raises(kv.KvarnError) as e:
+        kv.kvarn_chunk_attention(cfg, q, one * 0, one, 4, pool,
+                                 torch.zeros((1, 1), dtype=torch.int32, device=DEV), tk, tv,
+                                 torch.empty_like(q))
+    assert e.value.code == kv.kvarn.ERR_UNSUPPORTED
