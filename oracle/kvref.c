@@ -100,6 +100,18 @@
  *   [10752,14848)  V codes (the same permutation)
  *   [14848,16896)  V {s'_0, z'_0, s'_1, z'_1} fp32 per token
  *   [16896,17408)  V per-channel c_d fp32
+ *
+ * Format variant "k4v4_g128" (4-bit values; SURVEY's "K4V4"): the same stages
+ * with 4-bit RTN on V as on K.  The V codes are a fixed permutation of
+ * channel-major order chosen like the 2-bit one (see kvref_v4_code_pos):
+ * with channel c = 16m + 8e + r and token t = 16k + 8f + 2j + s, the code of
+ * (c, t) is nibble n = 4s + 2(k mod 2) + f of 32-bit word
+ * 256m + 32r + 8j + 4e + floor(k/2).  Record of 19456 bytes (152 B per
+ * token-head):
+ *   [0,     9728)  the K part (as in the default)
+ *   [9728, 17920)  V codes, 4 bits each, 2048 little-endian 32-bit words
+ *   [17920,18944)  V {s', z'} fp32 per token
+ *   [18944,19456)  V per-channel c_d fp32
  */
 #include <math.h>
 #include <stdint.h>
@@ -117,6 +129,7 @@
 #define OFF_VC 14848
 #define REC_BYTES_M16 13824
 #define REC_BYTES_G64 17408
+#define REC_BYTES_V4 19456
 #define G64 64
 
 /* Offsets of the record parts for the two metadata widths. */
@@ -140,6 +153,9 @@ static rec_layout layout_of(int fmt)
     } else if (fmt == 3) {
         L.rec = REC_BYTES_G64; L.kcodes = 0; L.ksz = 8192; L.kc = 10240;
         L.vcodes = 10752; L.vsz = 14848; L.vc = 16896; L.msz = 4;
+    } else if (fmt == 4) {
+        L.rec = REC_BYTES_V4; L.kcodes = 0; L.ksz = 8192; L.kc = 9216;
+        L.vcodes = 9728; L.vsz = 17920; L.vc = 18944; L.msz = 4;
     } else {
         L.rec = REC_BYTES; L.kcodes = OFF_KCODES; L.ksz = OFF_KSZ; L.kc = OFF_KC;
         L.vcodes = OFF_VCODES; L.vsz = OFF_VSZ; L.vc = OFF_VC; L.msz = 4;
@@ -507,15 +523,39 @@ static float get_meta(const uint8_t *p, int meta16)
     return get_f32(p);
 }
 
-/* is_v = 0: K part (4-bit, token-major); is_v = 1: V part (2-bit, permuted).
- * meta16: the "_m16" record (metadata stored as fp16). */
-void kvref_pack_part_fmt(uint8_t *rec, int is_v, const uint8_t *q, const float *s32,
-                         const float *z32, const float *c32, int meta16)
+/* Where the 4-bit V code of channel c, token t lives inside the V code
+ * region of the "k4v4_g128" record: byte offset and bit shift.  Digits as in
+ * kvref_v_code_pos; word 256m + 32r + 8j + 4e + floor(k/2), nibble
+ * 4s + 2(k mod 2) + f (nibble n at bits 4n of the little-endian word). */
+void kvref_v4_code_pos(int c, int t, int *byte, int *shift)
 {
-    rec_layout L = layout_of(meta16);
+    int m = c / 16, e = (c / 8) % 2, r = c % 8;
+    int k = t / 16, f = (t / 8) % 2, j = (t / 2) % 4, s = t % 2;
+    int word = 256 * m + 32 * r + 8 * j + 4 * e + k / 2;
+    int nib = 4 * s + 2 * (k % 2) + f;
+    *byte = 4 * word + nib / 2;
+    *shift = 4 * (nib % 2);
+}
+
+/* is_v = 0: K part (4-bit, token-major); is_v = 1: V part (2-bit, permuted;
+ * 4-bit for fmt 4).  fmt: the record format (layout_of); fmt 1 stores the
+ * metadata as fp16. */
+void kvref_pack_part_fmt(uint8_t *rec, int is_v, const uint8_t *q, const float *s32,
+                         const float *z32, const float *c32, int fmt)
+{
+    rec_layout L = layout_of(fmt);
     long sz = is_v ? L.vsz : L.ksz, cc = is_v ? L.vc : L.kc;
+    const int meta16 = fmt == 1;
     int t, d, j;
-    if (!is_v) {
+    if (is_v && fmt == 4) {
+        memset(rec + L.vcodes, 0, NTOK * NCH / 2);
+        for (t = 0; t < NTOK; ++t)
+            for (d = 0; d < NCH; ++d) {
+                int byte, shift;
+                kvref_v4_code_pos(d, t, &byte, &shift);
+                rec[L.vcodes + byte] |= (uint8_t)((q[t * NCH + d] & 15) << shift);
+            }
+    } else if (!is_v) {
         for (t = 0; t < NTOK; ++t)
             for (j = 0; j < NCH / 2; ++j)
                 rec[L.kcodes + t * 64 + j] =
@@ -545,14 +585,19 @@ void kvref_pack_part(uint8_t *rec, int is_v, const uint8_t *q, const float *s32,
 /* Inverse of kvref_pack_part_fmt for the codes and metadata (fp16 metadata
  * returned as the floats it represents). */
 void kvref_unpack_part_fmt(const uint8_t *rec, int is_v, uint8_t *q, float *s32, float *z32,
-                           float *c32, int meta16)
+                           float *c32, int fmt)
 {
-    rec_layout L = layout_of(meta16);
+    rec_layout L = layout_of(fmt);
     long sz = is_v ? L.vsz : L.ksz, cc = is_v ? L.vc : L.kc;
+    const int meta16 = fmt == 1;
     int t, d;
     for (t = 0; t < NTOK; ++t) {
         for (d = 0; d < NCH; ++d) {
-            if (!is_v) {
+            if (is_v && fmt == 4) {
+                int byte, shift;
+                kvref_v4_code_pos(d, t, &byte, &shift);
+                q[t * NCH + d] = (uint8_t)((rec[L.vcodes + byte] >> shift) & 15);
+            } else if (!is_v) {
                 uint8_t byte = rec[L.kcodes + t * 64 + d / 2];
                 q[t * NCH + d] = (uint8_t)((byte >> (4 * (d % 2))) & 15);
             } else {
@@ -710,7 +755,7 @@ void kvref_quantize_tile_fmt(const uint16_t *x, long ld_tok, int is_v, int iters
     double a[NTOK], b[NCH], r[NTOK];
     float c32[NCH], s32[NTOK], z32[NTOK];
     uint8_t q[NTOK * NCH];
-    int t, d, bits = is_v ? 2 : 4;
+    int t, d, bits = is_v && fmt != 4 ? 2 : 4;
 #pragma omp critical(kvref_h)
     {
         if (!have_h) {

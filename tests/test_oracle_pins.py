@@ -1225,3 +1225,98 @@ def test_g64_append_fills_page_like_prefill(oracle):
         assert oracle.append_token(k[:, t], v[:, t], np.array([t], np.int32), table, 2,
                                    st["pool"], st["tail_k"], st["tail_v"], g64=True) == 0
     assert np.array_equal(st["pool"], ref["pool"])
+
+
+# --------------------------------------------- format variant: 4-bit values --
+# Format variant "k4v4_g128" (SURVEY's "K4V4"): the KVarN page fixes 4-bit
+# keys and 2-bit values ("Kuantize Edilmis Onbellek"); the variant quantizes
+# values at 4 bits too, with a 4-bit V code permutation of its own.
+
+def test_v4_code_positions_golden_and_a_bijection(oracle):
+    g = json.load(open(os.path.join(GOLDEN, "pack_v4_examples.json")))
+    for ex in g["examples"]:
+        assert oracle.v4_code_pos(ex["channel"], ex["token"]) == (ex["byte"], ex["shift"]), \
+            ex["_derivation"]
+    seen = set()
+    for c in range(128):
+        for t in range(128):
+            byte, shift = oracle.v4_code_pos(c, t)
+            assert 0 <= byte < 8192 and shift in (0, 4)
+            seen.add((byte, shift))
+    assert len(seen) == 128 * 128
+
+
+def test_v4_values_quantize_like_keys(oracle):
+    # at 4 bits the V part runs the same stages as the K part: the same codes,
+    # scales and zeros for the same tile
+    x = _tile(71)
+    k = oracle.quantize_tile(x, False, 2)
+    v = oracle.quantize_tile(x, True, 2, v4=True)
+    assert np.array_equal(k["q"], v["q"]) and v["q"].max() == 15
+    qk, sk, zk, ck = oracle.unpack_part(k["rec"], False)
+    qv, sv, zv, cv = oracle.unpack_part(v["rec"], True, v4=True)
+    assert np.array_equal(qk, qv)
+    assert np.array_equal(sk, sv) and np.array_equal(zk, zv) and np.array_equal(ck, cv)
+    assert v["rec"].size == 19456 == 152 * 128
+    # the V part's bytes at the stated offsets
+    rec = v["rec"]
+    assert np.array_equal(rec[17920:18944].view(np.float32).reshape(128, 2)[:, 0], sv)
+    assert np.array_equal(rec[18944:19456].view(np.float32), cv)
+    for c, t in ((0, 0), (37, 90), (127, 127), (64, 3)):
+        byte, shift = oracle.v4_code_pos(c, t)
+        assert (rec[9728 + byte] >> shift) & 15 == qv[t, c]
+
+
+def test_v4_half_step_bound(oracle):
+    x = _tile(72)
+    out = oracle.quantize_tile(x, True, 2, v4=True)
+    q, s, z, c = oracle.unpack_part(out["rec"], True, v4=True)
+    yhat = oracle.dequant_part(out["rec"], True, v4=True)
+    half = 0.5 * np.abs(s.astype(np.float64))[:, None] * c.astype(np.float64)[None, :]
+    slack = 1e-6 * (np.abs(out["Y"]) + np.abs(yhat)) + 1e-9
+    assert np.all(np.abs(out["Y"] - yhat) <= half + slack)
+
+
+def test_v4_attention_matches_torch_sdpa_on_dequantized_cache(oracle):
+    w = synth.scaled(synth.WORKLOADS["llama3_8b_layer"], batch=2, seq=517, hkv=2, hq=4, seed=74)
+    k, v = synth.kv(w)
+    k, v = k.numpy(), v.numpy()
+    lens = np.array([300, 517], np.int32)
+    table = np.array([[5, 1, 3, 7, 0], [2, 6, 4, 8, 9]], np.int32)
+    st = oracle.quantize_blocks(k, v, lens, table, 10, 2, v4=True)
+    assert st["rc"] == 0 and st["pool"].shape == (10, 2, 19456)
+    q = synth.queries(w).numpy()
+    o1 = oracle.decode_attention(q, st["pool"], table, lens, st["tail_k"], st["tail_v"], 4, 2,
+                                 v4=True)
+    o0 = oracle.decode_attention(q, st["pool"], table, lens, st["tail_k"], st["tail_v"], 4, 2,
+                                 route=0, v4=True)
+    assert np.abs(o0 - o1).max() <= 1e-12 * np.abs(o0).max()
+    H = torch.tensor(oracle.hadamard(128))
+    for b in range(2):
+        n = int(lens[b])
+        nfull = n // 128
+        for h in range(4):
+            keys, vals = [], []
+            for j in range(nfull):
+                rec = st["pool"][table[b, j], h // 2]
+                keys.append(torch.tensor(oracle.dequant_part(rec, False, v4=True)) @ H)
+                vals.append(torch.tensor(oracle.dequant_part(rec, True, v4=True)) @ H)
+            keys.append(torch.tensor(k[b, nfull * 128:n, h // 2].astype(np.float64)))
+            vals.append(torch.tensor(v[b, nfull * 128:n, h // 2].astype(np.float64)))
+            ref = torch.nn.functional.scaled_dot_product_attention(
+                torch.tensor(q[b, h].astype(np.float64))[None, None, None],
+                torch.cat(keys)[None, None], torch.cat(vals)[None, None])[0, 0, 0].numpy()
+            assert np.abs(o1[b, h] - ref).max() <= 1e-12 * max(1.0, np.abs(ref).max())
+
+
+def test_v4_append_fills_page_like_prefill(oracle):
+    w = synth.scaled(synth.WORKLOADS["llama3_8b_layer"], batch=1, seq=256, hkv=2, hq=4, seed=75)
+    k, v = synth.kv(w)
+    k, v = k.numpy(), v.numpy()
+    table = np.array([[1, 0]], np.int32)
+    ref = oracle.quantize_blocks(k, v, np.array([256], np.int32), table, 2, 2, v4=True)
+    st = oracle.quantize_blocks(k, v, np.array([250], np.int32), table, 2, 2, v4=True)
+    for t in range(250, 256):
+        assert oracle.append_token(k[:, t], v[:, t], np.array([t], np.int32), table, 2,
+                                   st["pool"], st["tail_k"], st["tail_v"], v4=True) == 0
+    assert np.array_equal(st["pool"], ref["pool"])
