@@ -74,6 +74,16 @@
  *   [14848,16896) V {s'_0, z'_0, s'_1, z'_1} fp32 per token
  *   [16896,17408) V column scale c_d fp32
  * kvarn_chunk_attention does not take this format (KVARN_ERR_UNSUPPORTED).
+ * Format variant "k4v4_g128" (config v_bits = 4; fp32 metadata, 19456 bytes,
+ * 152 B per token-head): the same stages with 4-bit RTN on V as on K.  The K
+ * part is as above; the V part holds 4-bit codes in their own permutation:
+ * with channel c = 16m + 8e + r and token t = 16k + 8f + 2j + s, the code of
+ * (c, t) is nibble 4s + 2(k mod 2) + f (bits 4n of a little-endian word) of
+ * word 256m + 32r + 8j + 4e + floor(k/2):
+ *   [9728, 17920) V codes, 2048 32-bit words
+ *   [17920,18944) V {s', z'} fp32 per token
+ *   [18944,19456) V column scale c_d fp32
+ * kvarn_chunk_attention does not take this format either.
  * Pool = [num_pages][num_kv_heads][kvarn_page_bytes(cfg)].  The newest len mod 128
  * tokens of a sequence stay fp16 in a caller-owned tail buffer
  * [B][num_kv_heads][128 slots][128] per K and V.
@@ -113,6 +123,7 @@ typedef struct CUstream_st *kvarn_stream_t; /* identical to cudaStream_t */
 #define KVARN_PAGE_BYTES 15360
 #define KVARN_PAGE_BYTES_M16 13824
 #define KVARN_PAGE_BYTES_G64 17408
+#define KVARN_PAGE_BYTES_V4 19456
 
 /* return codes */
 #define KVARN_OK 0
@@ -133,7 +144,8 @@ typedef struct {
                            format variant "k4v2_g64", two groups per token
                            (fp32 metadata, not with "_pc") */
     int k_bits;         /* 4 */
-    int v_bits;         /* 2 */
+    int v_bits;         /* 2; 4: format variant "k4v4_g128" (fp32 metadata,
+                           groups of 128, not with "_pc") */
     int sinkhorn_iters; /* 0..64; 2 from the iteration-selection rule */
     int num_q_heads;    /* Hq, a multiple of num_kv_heads */
     int num_kv_heads;   /* Hkv; Hq / Hkv <= 16 */
@@ -149,7 +161,8 @@ typedef struct {
 
 /* Fills *out from a format string: "k4v2_g128" or "kvarn_k4v2_g128" (the
  * KVarN page's --kv-cache-dtype value), or "k4v2_g64" / "kvarn_k4v2_g64" for
- * groups of 64 channels, optionally followed by the variant
+ * groups of 64 channels, or "k4v4_g128" for 4-bit values, optionally
+ * followed by the variant
  * suffixes "_rms" (the uncentred statistic), "_m16" (fp16 metadata) and "_pc"
  * (per-channel groups; not with "_m16"), each at most once and in any order,
  * and then "_s<K>" to set the Sinkhorn iteration count.  Returns KVARN_ERR_UNSUPPORTED for any other format,
@@ -161,8 +174,9 @@ int kvarn_config_from_string(const char *s, int num_q_heads, int num_kv_heads,
 int kvarn_config_validate(const kvarn_config_t *cfg);
 
 /* Bytes of one page record (per page and KV head): KVARN_PAGE_BYTES (15360),
- * KVARN_PAGE_BYTES_M16 (13824) for the "_m16" format, or KVARN_PAGE_BYTES_G64
- * (17408) for groups of 64; 0 on a bad config.
+ * KVARN_PAGE_BYTES_M16 (13824) for the "_m16" format, KVARN_PAGE_BYTES_G64
+ * (17408) for groups of 64, or KVARN_PAGE_BYTES_V4 (19456) for 4-bit values;
+ * 0 on a bad config.
  * Every call that takes a pool reads it with this record size. */
 size_t kvarn_page_bytes(const kvarn_config_t *cfg);
 

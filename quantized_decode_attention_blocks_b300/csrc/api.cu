@@ -10,7 +10,8 @@ namespace kvarn {
 cudaError_t launch_decode_simple(const DecodeArgs& a, cudaStream_t s);
 cudaError_t launch_decode_mma(const DecodeArgs& a, cudaStream_t s);
 bool decode_mma_supported(int g);
-int decode_mma_ctas_per_sm(int g);
+int decode_mma_ctas_per_sm(int g, int fmt);
+int decode_simple_ctas_per_sm();
 int decode_mma_warps();
 int decode_mma_max_cluster();
 
@@ -36,7 +37,7 @@ bool decode_uses_cluster(int g, int nsplit) {
   return decode_mma_supported(g) && nsplit >= 2 && nsplit <= decode_mma_max_cluster();
 }
 
-DecodePlan decode_plan(int batch, int hq, int hkv, int max_seq, int num_sms) {
+DecodePlan decode_plan(int batch, int hq, int hkv, int max_seq, int num_sms, int fmt) {
   DecodePlan p{};
   // Work unit = one page of one (sequence, KV head); the fp16 tail rides with
   // the split that holds the last page.  The number of splits per (sequence,
@@ -47,7 +48,8 @@ DecodePlan decode_plan(int batch, int hq, int hkv, int max_seq, int num_sms) {
   const bool mma = decode_mma_supported(g);
   const int64_t units = max_seq / kT > 0 ? (int64_t)max_seq / kT : 1;
   const int64_t groups = (int64_t)batch * hkv;
-  const int64_t slots = (int64_t)(num_sms > 0 ? num_sms : 1) * (mma ? decode_mma_ctas_per_sm(g) : 4);
+  const int64_t slots = (int64_t)(num_sms > 0 ? num_sms : 1) *
+                        (mma ? decode_mma_ctas_per_sm(g, fmt) : decode_simple_ctas_per_sm());
   const int64_t min_pages = mma ? decode_mma_warps() : 2;
   int64_t ns = slots / groups;
   const int64_t ns_cap = (units + min_pages - 1) / min_pages;
@@ -76,7 +78,7 @@ int kvarn_config_validate(const kvarn_config_t* c) {
     return KVARN_ERR_INVALID_ARG;
   if (c->num_q_heads / c->num_kv_heads > kMaxG) return KVARN_ERR_UNSUPPORTED;
   if (c->head_dim != kD || c->block_tokens != kT || (c->group != kD && c->group != 64) ||
-      c->k_bits != 4 || c->v_bits != 2)
+      c->k_bits != 4 || (c->v_bits != 2 && c->v_bits != 4))
     return KVARN_ERR_UNSUPPORTED;
   if (c->sinkhorn_iters < 0 || c->sinkhorn_iters > kMaxIters) return KVARN_ERR_UNSUPPORTED;
   if (c->sinkhorn_rms != 0 && c->sinkhorn_rms != 1) return KVARN_ERR_UNSUPPORTED;
@@ -84,13 +86,15 @@ int kvarn_config_validate(const kvarn_config_t* c) {
   if (c->per_channel != 0 && c->per_channel != 1) return KVARN_ERR_UNSUPPORTED;
   if (c->per_channel && c->meta_fp16) return KVARN_ERR_UNSUPPORTED;   // fp32 metadata only
   if (c->group == 64 && (c->per_channel || c->meta_fp16)) return KVARN_ERR_UNSUPPORTED;
+  if (c->v_bits == 4 && (c->group != kD || c->per_channel || c->meta_fp16))
+    return KVARN_ERR_UNSUPPORTED;
   return KVARN_OK;
 }
 
 int kvarn_config_from_string(const char* s, int hq, int hkv, kvarn_config_t* out) {
   if (!s || !out) return KVARN_ERR_INVALID_ARG;
   if (!strncmp(s, "kvarn_", 6)) s += 6;
-  int group;
+  int group, vbits = 2;
   const char* rest;
   if (!strncmp(s, "k4v2_g128", 9)) {
     group = kD;
@@ -98,6 +102,10 @@ int kvarn_config_from_string(const char* s, int hq, int hkv, kvarn_config_t* out
   } else if (!strncmp(s, "k4v2_g64", 8)) {
     group = 64;
     rest = s + 8;
+  } else if (!strncmp(s, "k4v4_g128", 9)) {
+    group = kD;
+    vbits = 4;
+    rest = s + 9;
   } else {
     return KVARN_ERR_UNSUPPORTED;
   }
@@ -131,7 +139,7 @@ int kvarn_config_from_string(const char* s, int hq, int hkv, kvarn_config_t* out
   c.block_tokens = kT;
   c.group = group;
   c.k_bits = 4;
-  c.v_bits = 2;
+  c.v_bits = vbits;
   c.sinkhorn_iters = iters;
   c.sinkhorn_rms = rms;
   c.meta_fp16 = m16;
@@ -147,6 +155,7 @@ int kvarn_config_from_string(const char* s, int hq, int hkv, kvarn_config_t* out
 size_t kvarn_page_bytes(const kvarn_config_t* c) {
   if (kvarn_config_validate(c) != KVARN_OK) return 0;
   if (c->group == 64) return (size_t)RecFmt<kFmtG64>::bytes;
+  if (c->v_bits == 4) return (size_t)RecFmt<kFmtV4>::bytes;
   return c->meta_fp16 ? (size_t)RecFmt<kFmtM16>::bytes : (size_t)RecFmt<kFmtF32>::bytes;
 }
 
@@ -179,7 +188,7 @@ int kvarn_quantize_blocks(const kvarn_config_t* cfg, const void* k, const void* 
   a.hkv = cfg->num_kv_heads;
   a.iters = cfg->sinkhorn_iters;
   a.rms = cfg->sinkhorn_rms;
-  a.fmt = fmt_of(cfg->meta_fp16, cfg->per_channel, cfg->group);
+  a.fmt = cfg_fmt(cfg);
   a.max_seq = max_seq;
   a.seq_lens = seq_lens;
   a.block_table = block_table;
@@ -216,7 +225,7 @@ int kvarn_append_token(const kvarn_config_t* cfg, const void* k_new, const void*
   a.hkv = cfg->num_kv_heads;
   a.iters = cfg->sinkhorn_iters;
   a.rms = cfg->sinkhorn_rms;
-  a.fmt = fmt_of(cfg->meta_fp16, cfg->per_channel, cfg->group);
+  a.fmt = cfg_fmt(cfg);
   a.block_table = block_table;
   a.max_blocks = max_blocks;
   a.pool = static_cast<uint8_t*>(pool);
@@ -237,7 +246,8 @@ int kvarn_decode_split_plan(const kvarn_config_t* cfg, int batch, int max_seq, i
     num_sms = device_sm_count();
     if (num_sms <= 0) return KVARN_ERR_LAUNCH;
   }
-  const DecodePlan p = decode_plan(batch, cfg->num_q_heads, cfg->num_kv_heads, max_seq, num_sms);
+  const DecodePlan p =
+      decode_plan(batch, cfg->num_q_heads, cfg->num_kv_heads, max_seq, num_sms, cfg_fmt(cfg));
   if (pages_per_split) *pages_per_split = p.pages_per_split;
   if (nsplit) *nsplit = p.nsplit;
   if (workspace_bytes) *workspace_bytes = p.part_bytes + p.count_bytes;
@@ -270,7 +280,8 @@ int kvarn_decode_attention(const kvarn_config_t* cfg, const void* q, const void*
   if (batch > 65535 || cfg->num_kv_heads > 65535) return KVARN_ERR_UNSUPPORTED;
   const int sms = device_sm_count();
   if (sms <= 0) return KVARN_ERR_LAUNCH;
-  const DecodePlan p = decode_plan(batch, cfg->num_q_heads, cfg->num_kv_heads, max_seq, sms);
+  const DecodePlan p =
+      decode_plan(batch, cfg->num_q_heads, cfg->num_kv_heads, max_seq, sms, cfg_fmt(cfg));
   if (p.nsplit > 1 && (!workspace || workspace_bytes < p.part_bytes + p.count_bytes))
     return KVARN_ERR_WORKSPACE;
   DecodeArgs a;
@@ -296,7 +307,7 @@ int kvarn_decode_attention(const kvarn_config_t* cfg, const void* q, const void*
   a.pages_per_split = p.pages_per_split;
   a.nsplit = p.nsplit;
   a.cluster = 0;   // the kernel's launcher decides
-  a.fmt = fmt_of(cfg->meta_fp16, cfg->per_channel, cfg->group);
+  a.fmt = cfg_fmt(cfg);
   a.status = status;
   cudaError_t e = decode_mma_supported(a.g) ? launch_decode_mma(a, (cudaStream_t)stream)
                                             : launch_decode_simple(a, (cudaStream_t)stream);
@@ -321,9 +332,9 @@ int kvarn_chunk_attention(const kvarn_config_t* cfg, const void* q, int chunk_ma
       !aligned16(out))
     return KVARN_ERR_INVALID_ARG;
   if (!(softmax_scale > 0.f) || softmax_scale != softmax_scale) return KVARN_ERR_INVALID_ARG;
-  // the g64 record (17408 bytes) does not fit the kernel's two record buffers
-  // next to its six operand tiles
-  if (cfg->group == 64) return KVARN_ERR_UNSUPPORTED;
+  // the g64 and k4v4 records (17408, 19456 bytes) do not fit the kernel's two
+  // record buffers next to its six operand tiles
+  if (cfg->group == 64 || cfg->v_bits == 4) return KVARN_ERR_UNSUPPORTED;
   const int g = cfg->num_q_heads / cfg->num_kv_heads;
   const int tq = chunk_rows_per_tile(g);
   const int64_t ntq = ((int64_t)chunk_max + tq - 1) / tq;
@@ -348,7 +359,7 @@ int kvarn_chunk_attention(const kvarn_config_t* cfg, const void* q, int chunk_ma
   a.tail_v = static_cast<const __half*>(tail_v);
   a.scale_log2 = softmax_scale * 1.4426950408889634f;
   a.out = static_cast<__half*>(out);
-  a.fmt = fmt_of(cfg->meta_fp16, cfg->per_channel, cfg->group);
+  a.fmt = cfg_fmt(cfg);
   a.status = status;
   return launch_chunk_attention(a, (cudaStream_t)stream) == cudaSuccess ? KVARN_OK
                                                                          : KVARN_ERR_LAUNCH;

@@ -49,9 +49,10 @@ constexpr uint64_t kWaitLimitNs = 2000000000ull;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kTwo24 = 16777216.0f;
 
-template <int NT>
+// RB: the record format's bytes (RecFmt<FMT>::bytes)
+template <int NT, int RB>
 struct __align__(128) MmaSmem {
-  uint8_t rec[kWarps][kRecMax];  // per warp: K part at 0, V part at the format's kpart
+  uint8_t rec[kWarps][RB];       // per warp: K part at 0, V part at the format's kpart
   float qrot[4 * NT][kD];        // H q per (padded) query head of the group
   float qplain[4 * NT][kD];      // q itself, for the fp16 tail
   uint64_t bar[kWarps][2];       // per warp: 0 = K part landed, 1 = V part landed
@@ -160,7 +161,7 @@ __global__ void __launch_bounds__(kThreads, NT == 1 ? 3 : 2) decode_mma_kernel(D
   using F = RecFmt<FMT>;
   constexpr int NG = F::g64 ? 2 : 1;     // channel groups with their own s', z'
   extern __shared__ __align__(128) uint8_t smem_raw[];
-  MmaSmem<NT>& S = *reinterpret_cast<MmaSmem<NT>*>(smem_raw);
+  MmaSmem<NT, F::bytes>& S = *reinterpret_cast<MmaSmem<NT, F::bytes>*>(smem_raw);
   constexpr int G = 4 * NT;
   const int split = blockIdx.x, kvh = blockIdx.y, b = blockIdx.z;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -492,8 +493,11 @@ __global__ void __launch_bounds__(kThreads, NT == 1 ? 3 : 2) decode_mma_kernel(D
         float fs, finv;
         pow2_scale(smax, fs, finv);
         float sf[16];
+        // 1 / (power of two carried by the V code of score slot j): the 2-bit
+        // crumb positions, or for 4-bit codes nibble 0 (k rows 0-7) or 1 (x16)
+        auto pos_inv = [](int kb, int f) { return F::v4 ? (f ? 0.0625f : 1.f) : vpos_inv(kb, f); };
 #pragma unroll
-        for (int j = 0; j < 16; ++j) sf[j] = szv[j].x * (fs * vpos_inv(j >> 1, j & 1));
+        for (int j = 0; j < 16; ++j) sf[j] = szv[j].x * (fs * pos_inv(j >> 1, j & 1));
         uint32_t bp[NT][8][2];
         float zpage[NT];
 #pragma unroll
@@ -503,7 +507,7 @@ __global__ void __launch_bounds__(kThreads, NT == 1 ? 3 : 2) decode_mma_kernel(D
           for (int j = 0; j < 16; ++j) {
             // x <= 2^15 / 4^pos for a code carrying 4^pos: grid 16 / 4^pos
             const float x = sc[nt][j] * sf[j];
-            const float hi = grid_hi(x, (16.f * kMagic1) * vpos_inv(j >> 1, j & 1));
+            const float hi = grid_hi(x, (16.f * kMagic1) * pos_inv(j >> 1, j & 1));
             bp[nt][j >> 1][j & 1] = movm_trans(pack2(hi, x - hi));
             zq[j & 3] = fmaf(sc[nt][j], szv[j].y, zq[j & 3]);
           }
@@ -513,13 +517,22 @@ __global__ void __launch_bounds__(kThreads, NT == 1 ? 3 : 2) decode_mma_kernel(D
         // ---- value sum: V codes (A, rows = channels) x P' (B).  MCG channel
         // tiles at a time, k-tile outer, so that their chains interleave ----
         const float fin = finv * kTwo24;
-        constexpr int MCG = (NT == 1 ? 8 : 4) / NG;
+        constexpr int MCG = (NT == 1 ? 8 : 4) / NG / (F::v4 ? 2 : 1);
 #pragma unroll
         for (int c0 = 8 * gi / NG; c0 < 8 * (gi + 1) / NG; c0 += MCG) {
-          uint4 vw[MCG];   // words (e, h) = 00, 01, 10, 11 of channels 16mc + r, + 8
+          // 2-bit: words (e, h) = 00, 01, 10, 11 of channels 16mc + r, + 8.
+          // 4-bit: words p = 0..3 of channel 16mc + r (vw) and of 16mc + 8 + r
+          // (vw4), v4_word(c, lane & 3, p)
+          uint4 vw[MCG], vw4[F::v4 ? MCG : 1];
 #pragma unroll
-          for (int i = 0; i < MCG; ++i)
-            vw[i] = *reinterpret_cast<const uint4*>(vst + 512 * (c0 + i) + 16 * lane);
+          for (int i = 0; i < MCG; ++i) {
+            if constexpr (F::v4) {
+              vw[i] = *reinterpret_cast<const uint4*>(vst + 1024 * (c0 + i) + 32 * lane);
+              vw4[i] = *reinterpret_cast<const uint4*>(vst + 1024 * (c0 + i) + 32 * lane + 16);
+            } else {
+              vw[i] = *reinterpret_cast<const uint4*>(vst + 512 * (c0 + i) + 16 * lane);
+            }
+          }
           float d[NT][MCG][4];
 #pragma unroll
           for (int nt = 0; nt < NT; ++nt)
@@ -532,8 +545,22 @@ __global__ void __launch_bounds__(kThreads, NT == 1 ? 3 : 2) decode_mma_kernel(D
               const int kb = 4 * hh + jj;
 #pragma unroll
               for (int i = 0; i < MCG; ++i) {
-                const uint32_t e0 = word_of(vw[i], hh), e1 = word_of(vw[i], 2 + hh);
                 uint32_t A[4];
+                if constexpr (F::v4) {
+                  // k-tile kb: word kb >> 1, nibbles 0, 4 (a0, a1) and 1, 5
+                  // (a2, a3; x16) after a shift by 8 for odd kb
+                  uint32_t w0 = word_of(vw[i], kb >> 1), w1 = word_of(vw4[i], kb >> 1);
+                  if (kb & 1) {
+                    w0 >>= 8;
+                    w1 >>= 8;
+                  }
+                  A[0] = w0 & 0x000F000Fu; A[1] = w1 & 0x000F000Fu;
+                  A[2] = w0 & 0x00F000F0u; A[3] = w1 & 0x00F000F0u;
+#pragma unroll
+                  for (int nt = 0; nt < NT; ++nt) mma_16816(d[nt][i], A, bp[nt][kb][0], bp[nt][kb][1]);
+                  continue;
+                }
+                const uint32_t e0 = word_of(vw[i], hh), e1 = word_of(vw[i], 2 + hh);
                 if (jj == 0) {
                   A[0] = e0 & cmask(0); A[1] = e1 & cmask(0); A[2] = e0 & cmask(1); A[3] = e1 & cmask(1);
                 } else if (jj == 1) {
@@ -881,7 +908,7 @@ __global__ void __launch_bounds__(kThreads, NT == 1 ? 3 : 2) decode_mma_kernel(D
 template <int NT, int FMT>
 cudaError_t launch_nt(const DecodeArgs& args, cudaStream_t s) {
   static std::atomic<uint64_t> smem_set{0};
-  const int smem = (int)sizeof(MmaSmem<NT>);
+  const int smem = (int)sizeof(MmaSmem<NT, RecFmt<FMT>::bytes>);
   cudaError_t e = ensure_dynamic_smem(decode_mma_kernel<NT, FMT>, smem, smem_set);
   if (e != cudaSuccess) return e;
   DecodeArgs a = args;
@@ -914,15 +941,26 @@ int decode_mma_max_cluster() { return kMaxClusterSplits; }
 // Resident CTAs per SM: the shared-memory footprint (228 KB per SM, 1 KB
 // reserved per CTA) and the launch bounds of the kernel.  Host-only
 // arithmetic: no CUDA call.
-int decode_mma_ctas_per_sm(int g) {
-  const int bytes = g <= 4 ? (int)sizeof(MmaSmem<1>) : (int)sizeof(MmaSmem<2>);
+template <int RB>
+int ctas_for(int g) {
+  const int bytes = g <= 4 ? (int)sizeof(MmaSmem<1, RB>) : (int)sizeof(MmaSmem<2, RB>);
   return min(233472 / (bytes + 1024), g <= 4 ? 3 : 2);
+}
+
+int decode_mma_ctas_per_sm(int g, int fmt) {
+  switch (fmt) {
+    case kFmtM16: return ctas_for<RecFmt<kFmtM16>::bytes>(g);
+    case kFmtG64: return ctas_for<RecFmt<kFmtG64>::bytes>(g);
+    case kFmtV4: return ctas_for<RecFmt<kFmtV4>::bytes>(g);
+    default: return ctas_for<RecFmt<kFmtF32>::bytes>(g);   // fp32 and per-channel records
+  }
 }
 
 cudaError_t launch_decode_mma(const DecodeArgs& a, cudaStream_t s) {
   if (a.fmt == kFmtM16) return a.g <= 4 ? launch_nt<1, kFmtM16>(a, s) : launch_nt<2, kFmtM16>(a, s);
   if (a.fmt == kFmtPC) return a.g <= 4 ? launch_nt<1, kFmtPC>(a, s) : launch_nt<2, kFmtPC>(a, s);
   if (a.fmt == kFmtG64) return a.g <= 4 ? launch_nt<1, kFmtG64>(a, s) : launch_nt<2, kFmtG64>(a, s);
+  if (a.fmt == kFmtV4) return a.g <= 4 ? launch_nt<1, kFmtV4>(a, s) : launch_nt<2, kFmtV4>(a, s);
   return a.g <= 4 ? launch_nt<1, kFmtF32>(a, s) : launch_nt<2, kFmtF32>(a, s);
 }
 

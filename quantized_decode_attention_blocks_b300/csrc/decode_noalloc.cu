@@ -112,7 +112,8 @@ extern "C" int kvarn_decode_attention_noalloc(const kvarn_config_t* cfg, const v
 
   const int sms = device_sm_count();
   if (sms <= 0) return KVARN_ERR_LAUNCH;
-  const DecodePlan p = decode_plan(batch, cfg->num_q_heads, cfg->num_kv_heads, max_seq, sms);
+  const DecodePlan p = decode_plan(batch, cfg->num_q_heads, cfg->num_kv_heads, max_seq, sms,
+                                     cfg_fmt(cfg));
   const size_t need = p.part_bytes + p.count_bytes;
   if (need > kScratchBytes) return KVARN_ERR_WORKSPACE;   // beyond the built-in scratch
   void* ws = nullptr;

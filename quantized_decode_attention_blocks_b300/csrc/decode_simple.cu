@@ -230,14 +230,30 @@ __global__ void __launch_bounds__(kThreads) decode_simple_kernel(DecodeArgs a) {
         const float* zs = second ? S.zs1 : S.zs;
         float pv[kMaxG];
         for (int h = 0; h < g; ++h) pv[h] = 0.f;
-        for (int w = 0; w < 8; ++w) {
-          const int j = w >> 1, hh = w & 1;
-          const uint32_t word = vw[v_word(d, j, hh)];
+        if constexpr (F::v4) {
+          // 4-bit codes: words p of token digit j; nibble n = 4s + u holds token
+          // 16 (2p + (u >> 1)) + 8 (u & 1) + 2j + s
+          for (int w = 0; w < 16; ++w) {
+            const int j = w >> 2, pp = w & 3;
+            const uint32_t word = vw[v4_word(d, j, pp)];
 #pragma unroll
-          for (int e = 0; e < 16; ++e) {
-            const float code = (float)((word >> (2 * e)) & 3u);
-            const int t = v_token(j, hh, e);
-            for (int h = 0; h < g; ++h) pv[h] = fmaf(pw[h][t], code, pv[h]);
+            for (int n = 0; n < 8; ++n) {
+              const float code = (float)((word >> (4 * n)) & 15u);
+              const int u = n & 3;
+              const int t = 16 * (2 * pp + (u >> 1)) + 8 * (u & 1) + 2 * j + (n >> 2);
+              for (int h = 0; h < g; ++h) pv[h] = fmaf(pw[h][t], code, pv[h]);
+            }
+          }
+        } else {
+          for (int w = 0; w < 8; ++w) {
+            const int j = w >> 1, hh = w & 1;
+            const uint32_t word = vw[v_word(d, j, hh)];
+#pragma unroll
+            for (int e = 0; e < 16; ++e) {
+              const float code = (float)((word >> (2 * e)) & 3u);
+              const int t = v_token(j, hh, e);
+              for (int h = 0; h < g; ++h) pv[h] = fmaf(pw[h][t], code, pv[h]);
+            }
           }
         }
         for (int h = 0; h < g; ++h) {
@@ -328,10 +344,18 @@ cudaError_t launch_simple(const DecodeArgs& a, cudaStream_t s) {
 
 }  // namespace
 
+// Resident CTAs per SM of the CUDA-core decode: its shared memory (228 KB
+// per SM, 1 KB reserved per CTA), at most 4.  Host-only arithmetic.
+int decode_simple_ctas_per_sm() {
+  const int n = 233472 / ((int)sizeof(DecodeSmem) + 1024);
+  return n < 4 ? n : 4;
+}
+
 cudaError_t launch_decode_simple(const DecodeArgs& a, cudaStream_t s) {
   if (a.fmt == kFmtM16) return launch_simple<kFmtM16>(a, s);
   if (a.fmt == kFmtPC) return launch_simple<kFmtPC>(a, s);
   if (a.fmt == kFmtG64) return launch_simple<kFmtG64>(a, s);
+  if (a.fmt == kFmtV4) return launch_simple<kFmtV4>(a, s);
   return launch_simple<kFmtF32>(a, s);
 }
 

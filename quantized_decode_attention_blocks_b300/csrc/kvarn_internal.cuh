@@ -41,25 +41,37 @@ constexpr int kVPart = kRec - kKPart;  // V part: [9728, 15360)
 //   [0, 8192) K codes, [8192, 10240) K {s'_0, z'_0, s'_1, z'_1} fp32 per
 //   token, [10240, 10752) K c_d, [10752, 14848) V codes, [14848, 16896) V
 //   {s', z'} x 2, [16896, 17408) V c_d.
+// 4 = "k4v4_g128", 4-bit values: the K part as in format 0, then V codes
+//   [9728, 17920) (2048 words: the code of channel c = 16m + 8e + r, token
+//   t = 16k + 8f + 2j + s is nibble 4s + 2(k & 1) + f of word
+//   256m + 32r + 8j + 4e + (k >> 1), see v4_word), [17920, 18944) V {s', z'}
+//   fp32 per token, [18944, 19456) V c_d.
 // Every format dequantizes as yhat_td = alpha_t beta_d q_td + gamma_t delta_d:
 // (alpha, gamma) = (s', z') (of d's group for format 3) and beta = delta = c_d
 // for formats 0, 1 and 3, alpha = gamma = r_t and (beta, delta) = (cs_d, cz_d)
 // for format 2.  The accessors take the address of the field (record part +
 // offset).
-constexpr int kFmtF32 = 0, kFmtM16 = 1, kFmtPC = 2, kFmtG64 = 3;
-constexpr int kRecMax = 17408;    // the largest record (format 3)
+constexpr int kFmtF32 = 0, kFmtM16 = 1, kFmtPC = 2, kFmtG64 = 3, kFmtV4 = 4;
+constexpr int kRecMax = 19456;    // the largest record (format 4)
+// Word of the 4-bit V code region holding channel c, token-digit j and
+// word p = k >> 1 (format 4); its nibble 4s + 2(k & 1) + f holds the token.
+__host__ __device__ constexpr int v4_word(int c, int j, int p) {
+  return 256 * (c >> 4) + 32 * (c & 7) + 8 * j + 4 * ((c >> 3) & 1) + p;
+}
 template <int FMT>
 struct RecFmt {
   static constexpr bool m16 = FMT == kFmtM16;
   static constexpr bool pc = FMT == kFmtPC;
   static constexpr bool g64 = FMT == kFmtG64;
-  static constexpr int bytes = m16 ? 13824 : g64 ? 17408 : 15360;
+  static constexpr bool v4 = FMT == kFmtV4;
+  static constexpr int bytes = m16 ? 13824 : g64 ? 17408 : v4 ? 19456 : 15360;
   static constexpr int kpart = m16 ? 8960 : g64 ? 10752 : 9728;   // K part [0, kpart)
   static constexpr int vpart = bytes - kpart;       // V part [kpart, bytes)
   static constexpr int ksz = 8192;                  // per-token fields
   static constexpr int kc = m16 ? 8704 : pc ? 8704 : g64 ? 10240 : 9216;   // per-channel fields
-  static constexpr int vsz = m16 ? 13056 : g64 ? 14848 : 13824;   // from the record start
-  static constexpr int vc = m16 ? 13568 : pc ? 14336 : g64 ? 16896 : 14848;
+  static constexpr int vsz = m16 ? 13056 : g64 ? 14848 : v4 ? 17920 : 13824;   // from the start
+  static constexpr int vc = m16 ? 13568 : pc ? 14336 : g64 ? 16896 : v4 ? 18944 : 14848;
+  static constexpr int vbits = v4 ? 4 : 2;
   // (alpha_t, gamma_t) of token t for the channels of group g (g = 0 unless
   // g64)
   static __device__ __forceinline__ float2 get_sz_g(const uint8_t* f, int t, int g) {
@@ -155,11 +167,16 @@ static_assert(RecFmt<kFmtM16>::kpart % 16 == 0 && RecFmt<kFmtM16>::vpart % 16 ==
                   RecFmt<kFmtPC>::kc % 16 == 0 && RecFmt<kFmtPC>::vc % 16 == 0 &&
                   RecFmt<kFmtG64>::kpart % 16 == 0 && RecFmt<kFmtG64>::vpart % 16 == 0 &&
                   RecFmt<kFmtG64>::kc % 16 == 0 && RecFmt<kFmtG64>::vsz % 16 == 0 &&
-                  RecFmt<kFmtG64>::vc % 16 == 0 && RecFmt<kFmtG64>::bytes == kRecMax,
+                  RecFmt<kFmtG64>::vc % 16 == 0 && RecFmt<kFmtV4>::vsz % 16 == 0 &&
+                  RecFmt<kFmtV4>::vc % 16 == 0 && RecFmt<kFmtV4>::bytes == kRecMax,
               "bulk copies and vector loads need 16-byte parts and fields");
 // The format code of a configuration.
-__host__ __device__ constexpr int fmt_of(int meta16, int per_channel, int group) {
-  return group == 64 ? kFmtG64 : per_channel ? kFmtPC : meta16 ? kFmtM16 : kFmtF32;
+__host__ __device__ constexpr int fmt_of(int meta16, int per_channel, int group, int v_bits) {
+  return v_bits == 4 ? kFmtV4 : group == 64 ? kFmtG64 : per_channel ? kFmtPC
+         : meta16 ? kFmtM16 : kFmtF32;
+}
+inline int cfg_fmt(const kvarn_config_t* c) {
+  return fmt_of(c->meta_fp16, c->per_channel, c->group, c->v_bits);
 }
 
 // Split-K partial state per (sequence, query head, split): m, l, 2 pad, o[128]
@@ -271,7 +288,8 @@ struct DecodePlan {
   size_t count_bytes;  // ticket region
 };
 // `num_sms`: streaming multiprocessors the plan fills (device_sm_count()).
-DecodePlan decode_plan(int batch, int hq, int hkv, int max_seq, int num_sms);
+// `fmt`: the record format, which sets the kernel's shared memory per CTA.
+DecodePlan decode_plan(int batch, int hq, int hkv, int max_seq, int num_sms, int fmt);
 // Whether the decode launch merges the splits of a (sequence, KV head) inside
 // a thread-block cluster (no workspace tickets are then read).
 bool decode_uses_cluster(int g, int nsplit);

@@ -798,9 +798,10 @@ __global__ void __launch_bounds__(kQThreads, 1)
           if ((q & (G64 ? 1 : 3)) == 0) {
             const int grp = G64 ? q >> 1 : 0;
             S.vmin[wg][grp * kT + t] = lo;
-            S.vinv[wg][grp * kT + t] = range > 0.f ? __fdividef(3.f, range) : 0.f;
+            constexpr float vq = RecFmt<FMT>::v4 ? 15.f : 3.f;   // 2^bits - 1 of V
+            S.vinv[wg][grp * kT + t] = range > 0.f ? __fdividef(vq, range) : 0.f;
             RecFmt<FMT>::put_sz_g(out + (RecFmt<FMT>::vsz - RecFmt<FMT>::kpart), t, grp,
-                                  range * (kInvSqrt128 / 3.f), lo * kInvSqrt128);
+                                  range * (kInvSqrt128 / vq), lo * kInvSqrt128);
           }
         }
       }
@@ -809,14 +810,19 @@ __global__ void __launch_bounds__(kQThreads, 1)
       {
         tmem_ld256(tYT, v);
         tmem_wait_ld();
+        // 2-bit: 2 words per row, crumb (k & 7) + 8b of word k >> 3; 4-bit:
+        // 4 words per row, nibble (k & 3) + 4b of word k >> 2
+        constexpr bool V4 = RecFmt<FMT>::v4;
+        constexpr int NWV = V4 ? 4 : 2;
         float2 cd2[2];
-        uint32_t acc[2][2];
+        uint32_t acc[2][NWV];
         int gofs[2];   // the row's channel group (g64) in the per-token arrays
 #pragma unroll
         for (int e = 0; e < 2; ++e) {
           const float cd = cb[frow(e)];
           cd2[e] = make_float2(cd, cd);
-          acc[e][0] = acc[e][1] = 0u - kMagicV;
+#pragma unroll
+          for (int j = 0; j < NWV; ++j) acc[e][j] = 0u - (V4 ? kMagicK : kMagicV);
           gofs[e] = RecFmt<FMT>::g64 ? (chan_of(frow(e)) >> 6) * kT : 0;
         }
 #pragma unroll
@@ -830,14 +836,24 @@ __global__ void __launch_bounds__(kQThreads, 1)
             const float2 nm = make_float2(-m2.x, -m2.y);
             const float2 d = __ffma2_rn(pair(v, k, e), cd2[e], nm);
             const float2 f = __ffma2_rn(d, i2, mg);
-            acc[e][k >> 3] += __float_as_uint(f.x) << (2 * (k & 7));
-            acc[e][k >> 3] += __float_as_uint(f.y) << (2 * (k & 7) + 16);
+            if constexpr (V4) {
+              acc[e][k >> 2] += __float_as_uint(f.x) << (4 * (k & 3));
+              acc[e][k >> 2] += __float_as_uint(f.y) << (4 * (k & 3) + 16);
+            } else {
+              acc[e][k >> 3] += __float_as_uint(f.x) << (2 * (k & 7));
+              acc[e][k >> 3] += __float_as_uint(f.y) << (2 * (k & 7) + 16);
+            }
           }
         }
 #pragma unroll
-        for (int e = 0; e < 2; ++e)
-          *reinterpret_cast<uint2*>(vw + v_word(chan_of(frow(e)), q, 0)) =
-              make_uint2(acc[e][0], acc[e][1]);
+        for (int e = 0; e < 2; ++e) {
+          if constexpr (V4)
+            *reinterpret_cast<uint4*>(vw + v4_word(chan_of(frow(e)), q, 0)) =
+                make_uint4(acc[e][0], acc[e][1], acc[e][2], acc[e][3]);
+          else
+            *reinterpret_cast<uint2*>(vw + v_word(chan_of(frow(e)), q, 0)) =
+                make_uint2(acc[e][0], acc[e][1]);
+        }
       }
     }
     }   // per-token groups
@@ -957,6 +973,7 @@ cudaError_t launch_fmt(int fmt, const CUtensorMap& mk, const CUtensorMap& mv,
   if (fmt == kFmtM16) return launch_tiles<kFmtM16>(mk, mv, qa, cp, s);
   if (fmt == kFmtPC) return launch_tiles<kFmtPC>(mk, mv, qa, cp, s);
   if (fmt == kFmtG64) return launch_tiles<kFmtG64>(mk, mv, qa, cp, s);
+  if (fmt == kFmtV4) return launch_tiles<kFmtV4>(mk, mv, qa, cp, s);
   return launch_tiles<kFmtF32>(mk, mv, qa, cp, s);
 }
 

@@ -78,21 +78,21 @@ def _compare_g64(tag, got, ref, is_v, bits):
 
 def compare_record(got: np.ndarray, ref: np.ndarray, u_k=None, u_v=None, stats=None,
                    meta16: bool = False, ref32: np.ndarray = None, pc: bool = False,
-                   g64: bool = False):
+                   g64: bool = False, v4: bool = False):
     """Compares one record (GPU) with the oracle's.  u_k, u_v: oracle
     pre-rounding values [128][128] (token, channel).  meta16: the "_m16"
     format, whose metadata is judged against ref32, the oracle's record of
     the same tile in the fp32 format; pc: the "_pc" format.  Returns a dict."""
     out = {} if stats is None else stats
     for is_v, u in ((False, u_k), (True, u_v)):
-        bits = 2 if is_v else 4
+        bits = 2 if is_v and not v4 else 4
         if pc or g64:
             unpack = kvref.unpack_part_pc if pc else kvref.unpack_part_g64
             qg = unpack(got, is_v)[0]
             qr = unpack(ref, is_v)[0]
         else:
-            qg, sg, zg, cg = kvref.unpack_part(got, is_v, meta16)
-            qr, sr, zr, cr = kvref.unpack_part(ref, is_v, meta16)
+            qg, sg, zg, cg = kvref.unpack_part(got, is_v, meta16, v4)
+            qr, sr, zr, cr = kvref.unpack_part(ref, is_v, meta16, v4)
         tag = "v" if is_v else "k"
         diff = qg != qr
         n_diff = int(diff.sum())

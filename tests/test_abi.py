@@ -38,7 +38,8 @@ def test_header_constants_match_binding():
     text = open(HEADER).read()
     for name, val in (("KVARN_PAGE_BYTES", K.PAGE_BYTES),
                       ("KVARN_PAGE_BYTES_M16", K.PAGE_BYTES_M16),
-                      ("KVARN_PAGE_BYTES_G64", K.PAGE_BYTES_G64), ("KVARN_OK", K.OK),
+                      ("KVARN_PAGE_BYTES_G64", K.PAGE_BYTES_G64),
+                      ("KVARN_PAGE_BYTES_V4", K.PAGE_BYTES_V4), ("KVARN_OK", K.OK),
                       ("KVARN_ERR_INVALID_ARG", K.ERR_INVALID_ARG),
                       ("KVARN_ERR_UNSUPPORTED", K.ERR_UNSUPPORTED),
                       ("KVARN_ERR_WORKSPACE", K.ERR_WORKSPACE), ("KVARN_ERR_LAUNCH", K.ERR_LAUNCH),
@@ -93,7 +94,14 @@ def test_config_parsing():
     for bad in ("k4v2_g64_m16", "k4v2_g64_pc", "k4v2_g32"):
         with pytest.raises(kv.KvarnError):
             kv.config_from_string(bad, 12, 2)
-    for bad in ("k4v4_g128", "k4v2_g96", "k4v2_g128_x", "k4v2_g128_s", "k4v2_g128_s999"):
+    # 4-bit values: "k4v4_g128", with "_rms" but not "_m16" / "_pc"
+    v4 = kv.config_from_string("kvarn_k4v4_g128_rms", 12, 2)
+    assert v4.v_bits == 4 and v4.group == 128 and v4.sinkhorn_rms == 1
+    assert kv.page_bytes(v4) == 19456 == 152 * 128 == v4.page_bytes
+    for bad in ("k4v4_g128_m16", "k4v4_g128_pc", "k4v4_g64"):
+        with pytest.raises(kv.KvarnError):
+            kv.config_from_string(bad, 12, 2)
+    for bad in ("k8v4_g128", "k4v2_g96", "k4v2_g128_x", "k4v2_g128_s", "k4v2_g128_s999"):
         with pytest.raises(kv.KvarnError) as e:
             kv.config_from_string(bad, 32, 8)
         assert e.value.code == K.ERR_UNSUPPORTED
@@ -132,8 +140,8 @@ def test_split_plan_fills_one_wave_and_covers_every_page(sms, g):
     # The plan follows the SM count it is given: it cuts each (sequence, KV
     # head) into at most as many splits as keep the whole grid resident (the
     # tensor-core kernel fits 3 CTAs per SM for g <= 4 and 2 for g = 5..8, the
-    # CUDA-core one 4), covers every page, and leaves no split empty.
-    per_sm = 3 if g <= 4 else 2 if g <= 8 else 4
+    # CUDA-core one 3), covers every page, and leaves no split empty.
+    per_sm = 3 if g <= 4 else 2 if g <= 8 else 3
     for hkv in (1, 2, 8):
         c = kv.config_from_string("k4v2_g128", g * hkv, hkv)
         for batch in (1, 3, 16, 64, 1000):

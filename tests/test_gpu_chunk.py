@@ -155,10 +155,11 @@ def test_chunk_prefill_workload_sampled():
         parity.compare_attention(host(out[b:b + 1]).astype(np.float64), ref)
 
 
-def test_g64_format_is_refused():
-    # the g64 record does not fit the kernel's record buffers: the call says
-    # so before any launch
-    cfg = config(8, 2, g64=True)
+@pytest.mark.parametrize("fmt", ["g64", "v4"])
+def test_g64_and_v4_formats_are_refused(fmt):
+    # the g64 and k4v4 records do not fit the kernel's record buffers: the
+    # call says so before any launch
+    cfg = config(8, 2, g64=fmt == "g64", v4=fmt == "v4")
     q = torch.zeros((1, 4, 8, 128), dtype=torch.float16, device=DEV)
     pool = kv.alloc_pool(cfg, 2, DEV)
     tk, tv = kv.alloc_tails(cfg, 1, DEV)
