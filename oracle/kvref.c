@@ -65,7 +65,7 @@
  *   [14848,15360)  V per-channel c_d fp32
  * Pool = [num_pages][num_kv_heads][15360 bytes].
  *
- * Format variant "_m16" (fp16 metadata; SURVEY's 108 B per token-head): the
+ * Format variant "_m16" (fp16 metadata, 108 B per token-head): the
  * same codes, the same fp32 arithmetic, and every stored s', z', c_d rounded
  * once more to fp16 (IEEE binary16, round to nearest even, overflow to
  * infinity).  Record of 13824 bytes:
@@ -76,8 +76,7 @@
  *   [13056,13568)  V per-token {s', z'} fp16 pairs
  *   [13568,13824)  V per-channel c_d fp16
  *
- * Format variant "_pc" (per-channel grouping; SURVEY's "per-channel
- * grouping"): after the same rotation and normalization, one RTN group is
+ * Format variant "_pc" (per-channel grouping): after the same rotation and normalization, one RTN group is
  * one channel's 128 tokens of the tile, so s_d, z_d are per channel and the
  * row scale r_t cannot be folded into them; it is stored per token.  With
  * x_td = Y_td / (r_t c_d): z_d = min_t x_td, s_d = (max_t - min_t) / (2^b - 1),
@@ -90,7 +89,8 @@
  *   [13824,14336)  V per-token r_t fp32
  *   [14336,15360)  V per-channel {cs_d, cz_d} fp32 pairs
  *
- * Format variant "k4v2_g64" (group size 64; SURVEY's "G = 64"): the same
+ * Format variant "k4v2_g64" (group size 64, the "g" of the KVarN page's format
+ * name kvarn_k4v2_g128): the same
  * stages with two RTN groups per token, channels 0-63 and 64-127, each with
  * its own {s', z'} (the row scale folded in as in the default).  Record of
  * 17408 bytes (136 B per token-head):
@@ -101,7 +101,8 @@
  *   [14848,16896)  V {s'_0, z'_0, s'_1, z'_1} fp32 per token
  *   [16896,17408)  V per-channel c_d fp32
  *
- * Format variant "k4v4_g128" (4-bit values; SURVEY's "K4V4"): the same stages
+ * Format variant "k4v4_g128" (4-bit values, the "v" of the format name): the
+ * same stages
  * with 4-bit RTN on V as on K.  The V codes are a fixed permutation of
  * channel-major order chosen like the 2-bit one (see kvref_v4_code_pos):
  * with channel c = 16m + 8e + r and token t = 16k + 8f + 2j + s, the code of
@@ -112,6 +113,18 @@
  *   [9728, 17920)  V codes, 4 bits each, 2048 little-endian 32-bit words
  *   [17920,18944)  V {s', z'} fp32 per token
  *   [18944,19456)  V per-channel c_d fp32
+ *
+ * Format variant "k8v4_g128" (8-bit keys, 4-bit values): the same stages
+ * with 8-bit RTN on K and 4-bit RTN on V.  K codes are token-major, one byte
+ * per channel, the 16-byte chunks of odd tokens swapped pairwise: the code of
+ * (channel d, token t) is byte 128 t + (d XOR 16 (t mod 2)) (see
+ * kvref_k8_code_pos).  V codes as in "k4v4_g128".  Record of 27648 bytes (216 B per token-head):
+ *   [0,    16384)  K codes
+ *   [16384,17408)  K {s', z'} fp32 per token
+ *   [17408,17920)  K per-channel c_d fp32
+ *   [17920,26112)  V codes (the 4-bit permutation)
+ *   [26112,27136)  V {s', z'} fp32 per token
+ *   [27136,27648)  V per-channel c_d fp32
  */
 #include <math.h>
 #include <stdint.h>
@@ -130,6 +143,7 @@
 #define REC_BYTES_M16 13824
 #define REC_BYTES_G64 17408
 #define REC_BYTES_V4 19456
+#define REC_BYTES_K8 27648
 #define G64 64
 
 /* Offsets of the record parts for the two metadata widths. */
@@ -156,6 +170,9 @@ static rec_layout layout_of(int fmt)
     } else if (fmt == 4) {
         L.rec = REC_BYTES_V4; L.kcodes = 0; L.ksz = 8192; L.kc = 9216;
         L.vcodes = 9728; L.vsz = 17920; L.vc = 18944; L.msz = 4;
+    } else if (fmt == 5) {
+        L.rec = REC_BYTES_K8; L.kcodes = 0; L.ksz = 16384; L.kc = 17408;
+        L.vcodes = 17920; L.vsz = 26112; L.vc = 27136; L.msz = 4;
     } else {
         L.rec = REC_BYTES; L.kcodes = OFF_KCODES; L.ksz = OFF_KSZ; L.kc = OFF_KC;
         L.vcodes = OFF_VCODES; L.vsz = OFF_VSZ; L.vc = OFF_VC; L.msz = 4;
@@ -527,6 +544,12 @@ static float get_meta(const uint8_t *p, int meta16)
  * region of the "k4v4_g128" record: byte offset and bit shift.  Digits as in
  * kvref_v_code_pos; word 256m + 32r + 8j + 4e + floor(k/2), nibble
  * 4s + 2(k mod 2) + f (nibble n at bits 4n of the little-endian word). */
+/* Byte of the 8-bit K code of channel d, token t (format "k8v4_g128"). */
+int kvref_k8_code_pos(int d, int t)
+{
+    return NCH * t + (d ^ (16 * (t & 1)));
+}
+
 void kvref_v4_code_pos(int c, int t, int *byte, int *shift)
 {
     int m = c / 16, e = (c / 8) % 2, r = c % 8;
@@ -547,7 +570,10 @@ void kvref_pack_part_fmt(uint8_t *rec, int is_v, const uint8_t *q, const float *
     long sz = is_v ? L.vsz : L.ksz, cc = is_v ? L.vc : L.kc;
     const int meta16 = fmt == 1;
     int t, d, j;
-    if (is_v && fmt == 4) {
+    if (!is_v && fmt == 5) {
+        for (t = 0; t < NTOK; ++t)
+            for (d = 0; d < NCH; ++d) rec[L.kcodes + kvref_k8_code_pos(d, t)] = q[t * NCH + d];
+    } else if (is_v && (fmt == 4 || fmt == 5)) {
         memset(rec + L.vcodes, 0, NTOK * NCH / 2);
         for (t = 0; t < NTOK; ++t)
             for (d = 0; d < NCH; ++d) {
@@ -593,7 +619,9 @@ void kvref_unpack_part_fmt(const uint8_t *rec, int is_v, uint8_t *q, float *s32,
     int t, d;
     for (t = 0; t < NTOK; ++t) {
         for (d = 0; d < NCH; ++d) {
-            if (is_v && fmt == 4) {
+            if (!is_v && fmt == 5) {
+                q[t * NCH + d] = rec[L.kcodes + kvref_k8_code_pos(d, t)];
+            } else if (is_v && (fmt == 4 || fmt == 5)) {
                 int byte, shift;
                 kvref_v4_code_pos(d, t, &byte, &shift);
                 q[t * NCH + d] = (uint8_t)((rec[L.vcodes + byte] >> shift) & 15);
@@ -755,7 +783,7 @@ void kvref_quantize_tile_fmt(const uint16_t *x, long ld_tok, int is_v, int iters
     double a[NTOK], b[NCH], r[NTOK];
     float c32[NCH], s32[NTOK], z32[NTOK];
     uint8_t q[NTOK * NCH];
-    int t, d, bits = is_v && fmt != 4 ? 2 : 4;
+    int t, d, bits = is_v ? (fmt == 4 || fmt == 5 ? 4 : 2) : (fmt == 5 ? 8 : 4);
 #pragma omp critical(kvref_h)
     {
         if (!have_h) {

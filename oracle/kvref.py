@@ -28,19 +28,22 @@ REC_BYTES = 15360
 REC_BYTES_M16 = 13824      # format variant "_m16": metadata stored as fp16
 REC_BYTES_G64 = 17408      # format variant "k4v2_g64": two groups per token
 REC_BYTES_V4 = 19456       # format variant "k4v4_g128": 4-bit values
+REC_BYTES_K8 = 27648       # format variant "k8v4_g128": 8-bit keys, 4-bit values
 
 
-def _fmt(meta16: bool = False, pc: bool = False, g64: bool = False, v4: bool = False) -> int:
+def _fmt(meta16: bool = False, pc: bool = False, g64: bool = False, v4: bool = False,
+         k8: bool = False) -> int:
     """Record format code of the C oracle: 0 fp32 metadata, 1 "_m16", 2 "_pc",
-    3 "g64", 4 "k4v4"; the variants do not combine."""
-    if int(meta16) + int(pc) + int(g64) + int(v4) > 1:
-        raise ValueError("the _m16, _pc, g64 and k4v4 variants do not combine")
-    return 4 if v4 else 3 if g64 else 2 if pc else 1 if meta16 else 0
+    3 "g64", 4 "k4v4", 5 "k8v4"; the variants do not combine."""
+    if int(meta16) + int(pc) + int(g64) + int(v4) + int(k8) > 1:
+        raise ValueError("the _m16, _pc, g64, k4v4 and k8v4 variants do not combine")
+    return 5 if k8 else 4 if v4 else 3 if g64 else 2 if pc else 1 if meta16 else 0
 
 
-def rec_bytes(meta16: bool = False, pc: bool = False, g64: bool = False, v4: bool = False) -> int:
+def rec_bytes(meta16: bool = False, pc: bool = False, g64: bool = False, v4: bool = False,
+              k8: bool = False) -> int:
     return {0: REC_BYTES, 1: REC_BYTES_M16, 2: REC_BYTES, 3: REC_BYTES_G64,
-            4: REC_BYTES_V4}[_fmt(meta16, pc, g64, v4)]
+            4: REC_BYTES_V4, 5: REC_BYTES_K8}[_fmt(meta16, pc, g64, v4, k8)]
 
 _lib = None
 
@@ -77,6 +80,8 @@ def lib():
         L.kvref_rtn_pc.argtypes = [P, P, P, ctypes.c_int, P, P, P, P, P]
         L.kvref_rtn_g64.argtypes = [P, P, P, ctypes.c_int, P, P, P, P]
         L.kvref_v4_code_pos.argtypes = [ctypes.c_int, ctypes.c_int, P, P]
+        L.kvref_k8_code_pos.argtypes = [ctypes.c_int, ctypes.c_int]
+        L.kvref_k8_code_pos.restype = ctypes.c_int
         L.kvref_pack_part_g64.argtypes = [P, ctypes.c_int, P, P, P, P]
         L.kvref_unpack_part_g64.argtypes = [P, ctypes.c_int, P, P, P, P]
         L.kvref_f32_to_f16.argtypes = [ctypes.c_float]
@@ -204,19 +209,25 @@ def v4_code_pos(c: int, t: int):
     return byte.value, shift.value
 
 
-def pack_part(rec, is_v: bool, q, s32, z32, c32, meta16: bool = False, v4: bool = False):
+def k8_code_pos(d: int, t: int) -> int:
+    """Format "k8v4": byte of the 8-bit K code of (channel, token)."""
+    return lib().kvref_k8_code_pos(d, t)
+
+
+def pack_part(rec, is_v: bool, q, s32, z32, c32, meta16: bool = False, v4: bool = False,
+              k8: bool = False):
     lib().kvref_pack_part_fmt(_p(rec), int(is_v), _p(_c(q, np.uint8)), _p(_c(s32, np.float32)),
                               _p(_c(z32, np.float32)), _p(_c(c32, np.float32)),
-                              _fmt(meta16, v4=v4))
+                              _fmt(meta16, v4=v4, k8=k8))
 
 
-def unpack_part(rec, is_v: bool, meta16: bool = False, v4: bool = False):
+def unpack_part(rec, is_v: bool, meta16: bool = False, v4: bool = False, k8: bool = False):
     q = np.zeros((NTOK, NCH), dtype=np.uint8)
     s = np.zeros(NTOK, dtype=np.float32)
     z = np.zeros(NTOK, dtype=np.float32)
     c = np.zeros(NCH, dtype=np.float32)
     lib().kvref_unpack_part_fmt(_p(_c(rec, np.uint8)), int(is_v), _p(q), _p(s), _p(z), _p(c),
-                                _fmt(meta16, v4=v4))
+                                _fmt(meta16, v4=v4, k8=k8))
     return q, s, z, c
 
 
@@ -272,24 +283,24 @@ def unpack_part_g64(rec, is_v: bool):
 
 
 def dequant_part(rec, is_v: bool, meta16: bool = False, pc: bool = False,
-                 g64: bool = False, v4: bool = False) -> np.ndarray:
+                 g64: bool = False, v4: bool = False, k8: bool = False) -> np.ndarray:
     y = np.zeros((NTOK, NCH), dtype=np.float64)
-    lib().kvref_dequant_part_fmt(_p(_c(rec, np.uint8)), int(is_v), _fmt(meta16, pc, g64, v4),
+    lib().kvref_dequant_part_fmt(_p(_c(rec, np.uint8)), int(is_v), _fmt(meta16, pc, g64, v4, k8),
                                  _p(y))
     return y
 
 
 def quantize_tile(x, is_v: bool, iters: int, rms: bool = False, meta16: bool = False,
-                  pc: bool = False, g64: bool = False, v4: bool = False):
+                  pc: bool = False, g64: bool = False, v4: bool = False, k8: bool = False):
     """All four stages on one tile; returns a dict of every intermediate."""
     xb = _bits16(x).reshape(NTOK, NCH)
-    rec = np.zeros(rec_bytes(meta16, pc, g64, v4), dtype=np.uint8)
+    rec = np.zeros(rec_bytes(meta16, pc, g64, v4, k8), dtype=np.uint8)
     Y = np.zeros((NTOK, NCH))
     a = np.zeros(NTOK)
     b = np.zeros(NCH)
     q = np.zeros((NTOK, NCH), dtype=np.uint8)
     u = np.zeros((NTOK, NCH))
-    lib().kvref_quantize_tile_fmt(_p(xb), NCH, int(is_v), iters, int(rms), _fmt(meta16, pc, g64, v4),
+    lib().kvref_quantize_tile_fmt(_p(xb), NCH, int(is_v), iters, int(rms), _fmt(meta16, pc, g64, v4, k8),
                                   _p(rec), _p(Y), _p(a), _p(b), _p(q), _p(u))
     return {"rec": rec, "Y": Y, "a": a, "b": b, "q": q, "u": u}
 
@@ -299,7 +310,7 @@ def quantize_tile(x, is_v: bool, iters: int, rms: bool = False, meta16: bool = F
 def quantize_blocks(k, v, seq_lens, block_table, num_pages: int, iters: int, pool=None,
                     tail_k=None, tail_v=None, want_u: bool = False, rms: bool = False,
                     meta16: bool = False, pc: bool = False, g64: bool = False,
-                    v4: bool = False):
+                    v4: bool = False, k8: bool = False):
     """Prefill: k, v fp16 [B][S][Hkv][128] (contiguous).  Returns a dict with
     the pool [num_pages][Hkv][15360] uint8 ([..][13824] with meta16), the fp16
     tails [B][Hkv][128][128] and, with want_u, the pre-rounding values
@@ -312,7 +323,7 @@ def quantize_blocks(k, v, seq_lens, block_table, num_pages: int, iters: int, poo
     block_table = _c(block_table, np.int32)
     max_blocks = block_table.shape[1]
     if pool is None:
-        pool = np.zeros((num_pages, hkv, rec_bytes(meta16, pc, g64, v4)), dtype=np.uint8)
+        pool = np.zeros((num_pages, hkv, rec_bytes(meta16, pc, g64, v4, k8)), dtype=np.uint8)
     if tail_k is None:
         tail_k = np.zeros((B, hkv, NTOK, NCH), dtype=np.uint16)
     if tail_v is None:
@@ -321,10 +332,10 @@ def quantize_blocks(k, v, seq_lens, block_table, num_pages: int, iters: int, poo
     if want_u:
         u_k = np.zeros((B, max_blocks, hkv, NTOK, NCH))
         u_v = np.zeros((B, max_blocks, hkv, NTOK, NCH))
-    assert pool.shape[-1] == rec_bytes(meta16, pc, g64, v4)
+    assert pool.shape[-1] == rec_bytes(meta16, pc, g64, v4, k8)
     rc = lib().kvref_quantize_blocks_fmt(_p(kb), _p(vb), S * hkv * NCH, hkv * NCH, NCH, B,
                                          _p(seq_lens), _p(block_table), max_blocks, hkv, iters,
-                                         int(rms), _fmt(meta16, pc, g64, v4), _p(pool), num_pages,
+                                         int(rms), _fmt(meta16, pc, g64, v4, k8), _p(pool), num_pages,
                                          _p(tail_k),
                                          _p(tail_v), _p(u_k), _p(u_v))
     return {"rc": rc, "pool": pool, "tail_k": tail_k, "tail_v": tail_v, "u_k": u_k, "u_v": u_v}
@@ -332,7 +343,7 @@ def quantize_blocks(k, v, seq_lens, block_table, num_pages: int, iters: int, poo
 
 def append_token(k_new, v_new, pos, block_table, iters: int, pool, tail_k, tail_v,
                  rms: bool = False, meta16: bool = False, pc: bool = False, g64: bool = False,
-                 v4: bool = False):
+                 v4: bool = False, k8: bool = False):
     """Decode-time append (in place on pool / tails).  Returns the status."""
     kb = _bits16(k_new)
     vb = _bits16(v_new)
@@ -340,16 +351,16 @@ def append_token(k_new, v_new, pos, block_table, iters: int, pool, tail_k, tail_
     pos = _c(pos, np.int32)
     block_table = _c(block_table, np.int32)
     assert pool.flags["C_CONTIGUOUS"] and tail_k.flags["C_CONTIGUOUS"]
-    assert pool.shape[-1] == rec_bytes(meta16, pc, g64, v4)
+    assert pool.shape[-1] == rec_bytes(meta16, pc, g64, v4, k8)
     return lib().kvref_append_token_fmt(_p(kb), _p(vb), _p(pos), B, _p(block_table),
                                         block_table.shape[1], hkv, iters, int(rms),
-                                        _fmt(meta16, pc, g64, v4),
+                                        _fmt(meta16, pc, g64, v4, k8),
                                         _p(pool), pool.shape[0], _p(tail_k), _p(tail_v))
 
 
 def decode_attention(q, pool, block_table, seq_lens, tail_k, tail_v, hq: int, hkv: int,
                      scale: float = 1.0 / np.sqrt(128.0), route: int = 1, meta16: bool = False,
-                     pc: bool = False, g64: bool = False, v4: bool = False):
+                     pc: bool = False, g64: bool = False, v4: bool = False, k8: bool = False):
     """Decode attention, float64 output [B][Hq][128].  route 0 = textbook
     (un-rotate every token), route 1 = rotated space with one final H."""
     qb = _bits16(q)
@@ -358,11 +369,11 @@ def decode_attention(q, pool, block_table, seq_lens, tail_k, tail_v, hq: int, hk
     block_table = _c(block_table, np.int32)
     seq_lens = _c(seq_lens, np.int32)
     out = np.zeros((B, hq, NCH))
-    assert pool.shape[-1] == rec_bytes(meta16, pc, g64, v4)
+    assert pool.shape[-1] == rec_bytes(meta16, pc, g64, v4, k8)
     rc = lib().kvref_decode_attention_fmt(_p(qb), _p(pool), pool.shape[0], _p(block_table),
                                           block_table.shape[1], _p(seq_lens), B, hq, hkv,
                                           _p(_bits16(tail_k)), _p(_bits16(tail_v)), float(scale),
-                                          int(route), _fmt(meta16, pc, g64, v4), _p(out))
+                                          int(route), _fmt(meta16, pc, g64, v4, k8), _p(out))
     if rc != 0:
         raise ValueError("oracle: page id outside the pool")
     return out
@@ -404,7 +415,8 @@ def attention_fp16(q, k, v, seq_lens, hq: int, hkv: int,
 
 def chunk_attention(q, start, chunk_lens, pool, block_table, tail_k, tail_v, hq: int, hkv: int,
                     scale: float = 1.0 / np.sqrt(128.0), meta16: bool = False,
-                    pc: bool = False, g64: bool = False, v4: bool = False) -> np.ndarray:
+                    pc: bool = False, g64: bool = False, v4: bool = False,
+                    k8: bool = False) -> np.ndarray:
     """Attention of a chunk of new query tokens over the quantized cache
     (chunked prefill), float64 output [B][M][Hq][128].
 
@@ -447,9 +459,9 @@ def chunk_attention(q, start, chunk_lens, pool, block_table, tail_k, tail_v, hq:
                 raise ValueError("oracle: page id outside the pool")
             for h in range(hkv):
                 K[h, j * NTOK:(j + 1) * NTOK] = dequant_part(pool[page, h], False, meta16, pc,
-                                                             g64, v4) @ H
+                                                             g64, v4, k8) @ H
                 V[h, j * NTOK:(j + 1) * NTOK] = dequant_part(pool[page, h], True, meta16, pc,
-                                                             g64, v4) @ H
+                                                             g64, v4, k8) @ H
         r = n - nfull * NTOK
         K[:, nfull * NTOK:] = tk[b, :, :r]
         V[:, nfull * NTOK:] = tv[b, :, :r]

@@ -991,7 +991,7 @@ def test_m16_append_fills_page_like_prefill(oracle):
 
 
 # ---------------------------------------- format variant: per-channel groups --
-# Format variant "_pc" (SURVEY's "per-channel grouping"): after the same
+# Format variant "_pc" (per-channel grouping): after the same
 # rotation and normalization, one RTN group is one channel's 128 tokens; the
 # row scale r_t is stored per token and c_d folds into the per-channel scale
 # and zero (yhat_td = r_t (cs_d q_td + cz_d)).  The KVarN page (blog.edumints.com,
@@ -1121,7 +1121,7 @@ def test_rms_variant_constant_tile_closed_form(oracle):
 
 
 # ---------------------------------------------- format variant: group size 64 --
-# Format variant "k4v2_g64" (SURVEY's "G = 64"; the KVarN page names the
+# Format variant "k4v2_g64" (group size 64; the KVarN page names the
 # format kvarn_k4v2_g128 in "Yazilim Gelistirme ve Ogrenme Acisindan Pratik
 # Cikarimlar", g the group size): two RTN groups per token, channels 0-63 and
 # 64-127, each with its own scale and zero; everything else as the default.
@@ -1228,7 +1228,7 @@ def test_g64_append_fills_page_like_prefill(oracle):
 
 
 # --------------------------------------------- format variant: 4-bit values --
-# Format variant "k4v4_g128" (SURVEY's "K4V4"): the KVarN page fixes 4-bit
+# Format variant "k4v4_g128" (4-bit values): the KVarN page fixes 4-bit
 # keys and 2-bit values ("Kuantize Edilmis Onbellek"); the variant quantizes
 # values at 4 bits too, with a 4-bit V code permutation of its own.
 
@@ -1319,4 +1319,102 @@ def test_v4_append_fills_page_like_prefill(oracle):
     for t in range(250, 256):
         assert oracle.append_token(k[:, t], v[:, t], np.array([t], np.int32), table, 2,
                                    st["pool"], st["tail_k"], st["tail_v"], v4=True) == 0
+    assert np.array_equal(st["pool"], ref["pool"])
+
+
+# ------------------------------------ format variant: 8-bit keys, 4-bit values --
+# Format variant "k8v4_g128" (8-bit keys, 4-bit values, the "k" and "v" of the
+# KVarN page's format name kvarn_k4v2_g128): the same stages with 8-bit RTN on
+# K; V as in "k4v4_g128".  K codes are token-major bytes, the 16-byte chunks
+# of odd tokens swapped pairwise.
+
+def test_k8_code_positions_golden_and_a_bijection(oracle):
+    g = json.load(open(os.path.join(GOLDEN, "pack_k8_examples.json")))
+    for ex in g["examples"]:
+        assert oracle.k8_code_pos(ex["channel"], ex["token"]) == ex["byte"], ex["_derivation"]
+    seen = {oracle.k8_code_pos(d, t) for d in range(128) for t in range(128)}
+    assert seen == set(range(128 * 128))
+
+
+def test_k8_keys_share_zero_and_range_with_k4(oracle):
+    # the normalization does not depend on the bit width: for the same tile the
+    # 8-bit keys have the 4-bit keys' zero and c_d and a step 15/255 of theirs;
+    # every token's codes reach 0 and 255; the V part is the k4v4 V part
+    x = _tile(81)
+    k4 = oracle.quantize_tile(x, False, 2)
+    k8 = oracle.quantize_tile(x, False, 2, k8=True)
+    assert np.array_equal(k4["a"], k8["a"]) and np.array_equal(k4["b"], k8["b"])
+    q4, s4, z4, c4 = oracle.unpack_part(k4["rec"], False)
+    q8, s8, z8, c8 = oracle.unpack_part(k8["rec"], False, k8=True)
+    assert np.array_equal(z4, z8) and np.array_equal(c4, c8)
+    assert np.allclose(s8.astype(np.float64) * 255, s4.astype(np.float64) * 15, rtol=2e-7)
+    assert np.array_equal(q8, k8["q"]) and np.all(q8.min(axis=1) == 0) and np.all(q8.max(axis=1) == 255)
+    # 8-bit codes round the same values on a 17x finer grid
+    assert np.all(np.abs(q8 / 255.0 - q4 / 15.0) <= 0.5 / 15 + 0.5 / 255 + 1e-12)
+    rec = k8["rec"]
+    assert rec.size == 27648 == 216 * 128
+    assert np.array_equal(rec[16384:17408].view(np.float32).reshape(128, 2)[:, 0], s8)
+    assert np.array_equal(rec[17408:17920].view(np.float32), c8)
+    for d, t in ((0, 0), (17, 1), (127, 126), (64, 99)):
+        assert rec[oracle.k8_code_pos(d, t)] == q8[t, d]
+    v4 = oracle.quantize_tile(x, True, 2, v4=True)
+    v8 = oracle.quantize_tile(x, True, 2, k8=True)
+    assert np.array_equal(v4["rec"][9728:], v8["rec"][17920:])
+
+
+def test_k8_half_step_bound(oracle):
+    x = _tile(82)
+    out = oracle.quantize_tile(x, False, 2, k8=True)
+    q, s, z, c = oracle.unpack_part(out["rec"], False, k8=True)
+    yhat = oracle.dequant_part(out["rec"], False, k8=True)
+    half = 0.5 * np.abs(s.astype(np.float64))[:, None] * c.astype(np.float64)[None, :]
+    slack = 1e-6 * (np.abs(out["Y"]) + np.abs(yhat)) + 1e-9
+    assert np.all(np.abs(out["Y"] - yhat) <= half + slack)
+    # and 17x tighter than the 4-bit keys on average
+    e4 = np.abs(out["Y"] - oracle.dequant_part(oracle.quantize_tile(x, False, 2)["rec"], False))
+    assert np.abs(out["Y"] - yhat).mean() < e4.mean() / 10
+
+
+def test_k8_attention_matches_torch_sdpa_on_dequantized_cache(oracle):
+    w = synth.scaled(synth.WORKLOADS["llama3_8b_layer"], batch=2, seq=517, hkv=2, hq=4, seed=84)
+    k, v = synth.kv(w)
+    k, v = k.numpy(), v.numpy()
+    lens = np.array([300, 517], np.int32)
+    table = np.array([[5, 1, 3, 7, 0], [2, 6, 4, 8, 9]], np.int32)
+    st = oracle.quantize_blocks(k, v, lens, table, 10, 2, k8=True)
+    assert st["rc"] == 0 and st["pool"].shape == (10, 2, 27648)
+    q = synth.queries(w).numpy()
+    o1 = oracle.decode_attention(q, st["pool"], table, lens, st["tail_k"], st["tail_v"], 4, 2,
+                                 k8=True)
+    o0 = oracle.decode_attention(q, st["pool"], table, lens, st["tail_k"], st["tail_v"], 4, 2,
+                                 route=0, k8=True)
+    assert np.abs(o0 - o1).max() <= 1e-12 * np.abs(o0).max()
+    H = torch.tensor(oracle.hadamard(128))
+    for b in range(2):
+        n = int(lens[b])
+        nfull = n // 128
+        for h in range(4):
+            keys, vals = [], []
+            for j in range(nfull):
+                rec = st["pool"][table[b, j], h // 2]
+                keys.append(torch.tensor(oracle.dequant_part(rec, False, k8=True)) @ H)
+                vals.append(torch.tensor(oracle.dequant_part(rec, True, k8=True)) @ H)
+            keys.append(torch.tensor(k[b, nfull * 128:n, h // 2].astype(np.float64)))
+            vals.append(torch.tensor(v[b, nfull * 128:n, h // 2].astype(np.float64)))
+            ref = torch.nn.functional.scaled_dot_product_attention(
+                torch.tensor(q[b, h].astype(np.float64))[None, None, None],
+                torch.cat(keys)[None, None], torch.cat(vals)[None, None])[0, 0, 0].numpy()
+            assert np.abs(o1[b, h] - ref).max() <= 1e-12 * max(1.0, np.abs(ref).max())
+
+
+def test_k8_append_fills_page_like_prefill(oracle):
+    w = synth.scaled(synth.WORKLOADS["llama3_8b_layer"], batch=1, seq=256, hkv=2, hq=4, seed=85)
+    k, v = synth.kv(w)
+    k, v = k.numpy(), v.numpy()
+    table = np.array([[1, 0]], np.int32)
+    ref = oracle.quantize_blocks(k, v, np.array([256], np.int32), table, 2, 2, k8=True)
+    st = oracle.quantize_blocks(k, v, np.array([250], np.int32), table, 2, 2, k8=True)
+    for t in range(250, 256):
+        assert oracle.append_token(k[:, t], v[:, t], np.array([t], np.int32), table, 2,
+                                   st["pool"], st["tail_k"], st["tail_v"], k8=True) == 0
     assert np.array_equal(st["pool"], ref["pool"])
