@@ -491,8 +491,9 @@ def measure_variants(args, dev, stream):
     """The format variants on the Llama-3-8B-like layer (16 x 4096 tokens, 8 KV
     heads, 32 query heads), three rotated replicas: "_m16" (fp16 metadata,
     108 B per token-head), "_pc" (per-channel groups), "k4v2_g64" (two
-    groups per token, 136 B per token-head) and "k4v4_g128" (4-bit values,
-    152 B per token-head), quantize and decode; "_rms" (the uncentred Sinkhorn statistic), quantize (its records
+    groups per token, 136 B per token-head), "k4v4_g128" (4-bit values,
+    152 B per token-head) and "k8v4_g128" (8-bit keys, 4-bit values, 216 B
+    per token-head), quantize and decode; "_rms" (the uncentred Sinkhorn statistic), quantize (its records
     decode like the default's).
     Algorithmic bytes as for the default format, with the record size of the
     variant."""
@@ -502,7 +503,7 @@ def measure_variants(args, dev, stream):
     peak, kind = measured_peaks()
     for fmt, rec, do_decode in (("k4v2_g128_m16", 13824, True), ("k4v2_g128_pc", REC, True),
                                 ("k4v2_g64", 17408, True), ("k4v4_g128", 19456, True),
-                                ("k4v2_g128_rms", REC, False)):
+                                ("k8v4_g128", 27648, True), ("k4v2_g128_rms", REC, False)):
         cfg = kv.config_from_string(fmt, w.hq, w.hkv)
         reps = []
         for r in range(3):

@@ -84,6 +84,18 @@
  *   [17920,18944) V {s', z'} fp32 per token
  *   [18944,19456) V column scale c_d fp32
  * kvarn_chunk_attention does not take this format either.
+ * Format variant "k8v4_g128" (config k_bits = 8, v_bits = 4; fp32 metadata,
+ * 27648 bytes, 216 B per token-head): 8-bit RTN on K (2^8 - 1 steps), V as in
+ * "k4v4_g128".  K codes are one byte per channel, token-major rows of 128
+ * bytes whose 16-byte chunks trade places pairwise in odd tokens: channel d
+ * of token t is byte 128 t + (d XOR 16 (t mod 2)):
+ *   [0,    16384) K codes
+ *   [16384,17408) K {s', z'} fp32 per token
+ *   [17408,17920) K column scale c_d fp32
+ *   [17920,26112) V codes (the 4-bit permutation above)
+ *   [26112,27136) V {s', z'} fp32 per token
+ *   [27136,27648) V column scale c_d fp32
+ * kvarn_chunk_attention does not take this format either.
  * Pool = [num_pages][num_kv_heads][kvarn_page_bytes(cfg)].  The newest len mod 128
  * tokens of a sequence stay fp16 in a caller-owned tail buffer
  * [B][num_kv_heads][128 slots][128] per K and V.
@@ -124,11 +136,12 @@ typedef struct CUstream_st *kvarn_stream_t; /* identical to cudaStream_t */
 #define KVARN_PAGE_BYTES_M16 13824
 #define KVARN_PAGE_BYTES_G64 17408
 #define KVARN_PAGE_BYTES_V4 19456
+#define KVARN_PAGE_BYTES_K8 27648
 
 /* return codes */
 #define KVARN_OK 0
 #define KVARN_ERR_INVALID_ARG (-1) /* null/misaligned pointer, bad size or stride */
-#define KVARN_ERR_UNSUPPORTED (-2) /* a config other than k4v2_g128, head_dim 128 */
+#define KVARN_ERR_UNSUPPORTED (-2) /* a format or shape this library does not run */
 #define KVARN_ERR_WORKSPACE (-3)   /* decode workspace missing or too small */
 #define KVARN_ERR_LAUNCH (-4)      /* the CUDA launch itself failed */
 
@@ -143,7 +156,8 @@ typedef struct {
     int group;          /* 128: quantization group = one token's channels; 64:
                            format variant "k4v2_g64", two groups per token
                            (fp32 metadata, not with "_pc") */
-    int k_bits;         /* 4 */
+    int k_bits;         /* 4; 8: format variant "k8v4_g128" (with v_bits = 4,
+                           fp32 metadata, groups of 128) */
     int v_bits;         /* 2; 4: format variant "k4v4_g128" (fp32 metadata,
                            groups of 128, not with "_pc") */
     int sinkhorn_iters; /* 0..64; 2 from the iteration-selection rule */
@@ -161,8 +175,8 @@ typedef struct {
 
 /* Fills *out from a format string: "k4v2_g128" or "kvarn_k4v2_g128" (the
  * KVarN page's --kv-cache-dtype value), or "k4v2_g64" / "kvarn_k4v2_g64" for
- * groups of 64 channels, or "k4v4_g128" for 4-bit values, optionally
- * followed by the variant
+ * groups of 64 channels, or "k4v4_g128" for 4-bit values, or "k8v4_g128"
+ * for 8-bit keys and 4-bit values, optionally followed by the variant
  * suffixes "_rms" (the uncentred statistic), "_m16" (fp16 metadata) and "_pc"
  * (per-channel groups; not with "_m16"), each at most once and in any order,
  * and then "_s<K>" to set the Sinkhorn iteration count.  Returns KVARN_ERR_UNSUPPORTED for any other format,
@@ -175,8 +189,9 @@ int kvarn_config_validate(const kvarn_config_t *cfg);
 
 /* Bytes of one page record (per page and KV head): KVARN_PAGE_BYTES (15360),
  * KVARN_PAGE_BYTES_M16 (13824) for the "_m16" format, KVARN_PAGE_BYTES_G64
- * (17408) for groups of 64, or KVARN_PAGE_BYTES_V4 (19456) for 4-bit values;
- * 0 on a bad config.
+ * (17408) for groups of 64, KVARN_PAGE_BYTES_V4 (19456) for 4-bit values, or
+ * KVARN_PAGE_BYTES_K8 (27648) for 8-bit keys with 4-bit values; 0 on a bad
+ * config.
  * Every call that takes a pool reads it with this record size. */
 size_t kvarn_page_bytes(const kvarn_config_t *cfg);
 

@@ -78,7 +78,7 @@ int kvarn_config_validate(const kvarn_config_t* c) {
     return KVARN_ERR_INVALID_ARG;
   if (c->num_q_heads / c->num_kv_heads > kMaxG) return KVARN_ERR_UNSUPPORTED;
   if (c->head_dim != kD || c->block_tokens != kT || (c->group != kD && c->group != 64) ||
-      c->k_bits != 4 || (c->v_bits != 2 && c->v_bits != 4))
+      (c->k_bits != 4 && c->k_bits != 8) || (c->v_bits != 2 && c->v_bits != 4))
     return KVARN_ERR_UNSUPPORTED;
   if (c->sinkhorn_iters < 0 || c->sinkhorn_iters > kMaxIters) return KVARN_ERR_UNSUPPORTED;
   if (c->sinkhorn_rms != 0 && c->sinkhorn_rms != 1) return KVARN_ERR_UNSUPPORTED;
@@ -88,13 +88,14 @@ int kvarn_config_validate(const kvarn_config_t* c) {
   if (c->group == 64 && (c->per_channel || c->meta_fp16)) return KVARN_ERR_UNSUPPORTED;
   if (c->v_bits == 4 && (c->group != kD || c->per_channel || c->meta_fp16))
     return KVARN_ERR_UNSUPPORTED;
+  if (c->k_bits == 8 && c->v_bits != 4) return KVARN_ERR_UNSUPPORTED;   // "k8v4_g128" only
   return KVARN_OK;
 }
 
 int kvarn_config_from_string(const char* s, int hq, int hkv, kvarn_config_t* out) {
   if (!s || !out) return KVARN_ERR_INVALID_ARG;
   if (!strncmp(s, "kvarn_", 6)) s += 6;
-  int group, vbits = 2;
+  int group, kbits = 4, vbits = 2;
   const char* rest;
   if (!strncmp(s, "k4v2_g128", 9)) {
     group = kD;
@@ -104,6 +105,11 @@ int kvarn_config_from_string(const char* s, int hq, int hkv, kvarn_config_t* out
     rest = s + 8;
   } else if (!strncmp(s, "k4v4_g128", 9)) {
     group = kD;
+    vbits = 4;
+    rest = s + 9;
+  } else if (!strncmp(s, "k8v4_g128", 9)) {
+    group = kD;
+    kbits = 8;
     vbits = 4;
     rest = s + 9;
   } else {
@@ -138,7 +144,7 @@ int kvarn_config_from_string(const char* s, int hq, int hkv, kvarn_config_t* out
   c.head_dim = kD;
   c.block_tokens = kT;
   c.group = group;
-  c.k_bits = 4;
+  c.k_bits = kbits;
   c.v_bits = vbits;
   c.sinkhorn_iters = iters;
   c.sinkhorn_rms = rms;
@@ -155,6 +161,7 @@ int kvarn_config_from_string(const char* s, int hq, int hkv, kvarn_config_t* out
 size_t kvarn_page_bytes(const kvarn_config_t* c) {
   if (kvarn_config_validate(c) != KVARN_OK) return 0;
   if (c->group == 64) return (size_t)RecFmt<kFmtG64>::bytes;
+  if (c->k_bits == 8) return (size_t)RecFmt<kFmtK8>::bytes;
   if (c->v_bits == 4) return (size_t)RecFmt<kFmtV4>::bytes;
   return c->meta_fp16 ? (size_t)RecFmt<kFmtM16>::bytes : (size_t)RecFmt<kFmtF32>::bytes;
 }
@@ -332,8 +339,8 @@ int kvarn_chunk_attention(const kvarn_config_t* cfg, const void* q, int chunk_ma
       !aligned16(out))
     return KVARN_ERR_INVALID_ARG;
   if (!(softmax_scale > 0.f) || softmax_scale != softmax_scale) return KVARN_ERR_INVALID_ARG;
-  // the g64 and k4v4 records (17408, 19456 bytes) do not fit the kernel's two
-  // record buffers next to its six operand tiles
+  // the g64, k4v4 and k8v4 records (17408, 19456, 27648 bytes) do not fit the
+  // kernel's two record buffers next to its six operand tiles
   if (cfg->group == 64 || cfg->v_bits == 4) return KVARN_ERR_UNSUPPORTED;
   const int g = cfg->num_q_heads / cfg->num_kv_heads;
   const int tq = chunk_rows_per_tile(g);

@@ -156,8 +156,11 @@ __device__ __forceinline__ constexpr float vpos_inv(int kb, int f) {
 // yhat_td = alpha_t beta_d q_td + gamma_t delta_d, so the score is
 // alpha_t sum_d (q~_d beta_d) q_td + gamma_t sum_d q~_d delta_d and the value
 // sum beta_d sum_t (p_t alpha_t) q_td + delta_d sum_t p_t gamma_t.
+// The 27648-byte records of 8-bit keys leave shared memory for two CTAs per
+// SM with one head tile and one with two, which may take every register.
 template <int NT, int FMT>
-__global__ void __launch_bounds__(kThreads, NT == 1 ? 3 : 2) decode_mma_kernel(DecodeArgs a) {
+__global__ void __launch_bounds__(kThreads, FMT == kFmtK8 ? 3 - NT : NT == 1 ? 3 : 2)
+    decode_mma_kernel(DecodeArgs a) {
   using F = RecFmt<FMT>;
   constexpr int NG = F::g64 ? 2 : 1;     // channel groups with their own s', z'
   extern __shared__ __align__(128) uint8_t smem_raw[];
@@ -360,12 +363,18 @@ __global__ void __launch_bounds__(kThreads, NT == 1 ? 3 : 2) decode_mma_kernel(D
           for (int kb = 0; kb < KB; ++kb) {
 #pragma unroll
             for (int slot = 0; slot < 2; ++slot) {
-              const int c0 = 8 * (kb >> 1) + 2 * (kb & 1) + slot;
-              const float f = slot ? scl16 : scl;
+              // 8-bit codes (bytes 4 (kb & 3) .. of the lane's 16-byte chunk
+              // kb >> 2): k rows 2qi, 2qi + 1 | 2qi + 8, 2qi + 9 hold
+              // channels 4 kb + 2 slot + 0, 1, both at bit 0 of their half
+              const int c0 = F::k8 ? 4 * kb + 2 * slot : 8 * (kb >> 1) + 2 * (kb & 1) + slot;
+              const int c1 = F::k8 ? c0 + 1 : c0 + 4;
+              const float f = slot && !F::k8 ? scl16 : scl;
               // |x| < 2^15 (slot 0) or 2^11 (slot 1): grid 16 or 1, i.e. 16
-              // in the units of the code it meets
-              const float2 x = __fmul2_rn(make_float2(v[c0], v[c0 + 4]), make_float2(f, f));
-              const float2 hg = grid_hi2(x, slot ? kMagic1 : 16.f * kMagic1);
+              // in the units of the 4-bit code it meets; for 8-bit codes
+              // grid 256, so that a hi product spans 15 bits as with 4-bit
+              const float2 x = __fmul2_rn(make_float2(v[c0], v[c1]), make_float2(f, f));
+              const float2 hg =
+                  grid_hi2(x, F::k8 ? 256.f * kMagic1 : slot ? kMagic1 : 16.f * kMagic1);
               const float2 o = odd ? __ffma2_rn(hg, make_float2(-1.f, -1.f), x) : hg;   // lo | hi
               bq[nt][kb][slot] = pack2(o.x, o.y);
             }
@@ -379,43 +388,68 @@ __global__ void __launch_bounds__(kThreads, NT == 1 ? 3 : 2) decode_mma_kernel(D
         // ---- scores: K codes (A, rows = tokens) x qc (B).  MTG token tiles
         // at a time, k-tile outer, so that MTG accumulator chains interleave.
         // The lane's code words of a token row: 4 words at 16 qi (one group)
-        // or 2 words at 32 gi + 8 qi (g64) ----
+        // or 2 words at 32 gi + 8 qi (g64); 8-bit codes: its 16-byte chunks
+        // 2qi, 2qi + 1 (k8_byte), one per half of the k-tiles ----
         constexpr int MTG = NT == 1 ? 8 : 4;
+        constexpr int NH = F::k8 ? 2 : 1;
 #pragma unroll
         for (int m0 = 0; m0 < 8; m0 += MTG) {
-          uint4 kw[MTG][2];
-#pragma unroll
-          for (int i = 0; i < MTG; ++i) {
-            const int tA = 16 * (m0 + i) + r;
-            if constexpr (NG == 1) {
-              kw[i][0] = *reinterpret_cast<const uint4*>(kst + kOffKCodes + 64 * tA + 16 * qi);
-              kw[i][1] = *reinterpret_cast<const uint4*>(kst + kOffKCodes + 64 * (tA + 8) + 16 * qi);
-            } else {
-              const uint2 wA = *reinterpret_cast<const uint2*>(kst + 64 * tA + 32 * gi + 8 * qi);
-              const uint2 wB =
-                  *reinterpret_cast<const uint2*>(kst + 64 * (tA + 8) + 32 * gi + 8 * qi);
-              kw[i][0] = make_uint4(wA.x, wA.y, 0u, 0u);
-              kw[i][1] = make_uint4(wB.x, wB.y, 0u, 0u);
-            }
-          }
           float d[NT][MTG][4];
 #pragma unroll
           for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
             for (int i = 0; i < MTG; ++i) d[nt][i][0] = d[nt][i][1] = d[nt][i][2] = d[nt][i][3] = 0.f;
 #pragma unroll
-          for (int kb = 0; kb < KB; ++kb) {
+          for (int hk = 0; hk < NH; ++hk) {
+            uint4 kw[MTG][2];
 #pragma unroll
             for (int i = 0; i < MTG; ++i) {
-              uint32_t wa = word_of(kw[i][0], kb >> 1), wb = word_of(kw[i][1], kb >> 1);
-              if (kb & 1) {
-                wa >>= 8;
-                wb >>= 8;
+              const int tA = 16 * (m0 + i) + r;
+              if constexpr (F::k8) {
+                const int ofs = 16 * ((2 * qi + hk) ^ (r & 1));   // tA, tA + 8: parity of r
+                kw[i][0] = *reinterpret_cast<const uint4*>(kst + 128 * tA + ofs);
+                kw[i][1] = *reinterpret_cast<const uint4*>(kst + 128 * (tA + 8) + ofs);
+              } else if constexpr (NG == 1) {
+                kw[i][0] = *reinterpret_cast<const uint4*>(kst + kOffKCodes + 64 * tA + 16 * qi);
+                kw[i][1] =
+                    *reinterpret_cast<const uint4*>(kst + kOffKCodes + 64 * (tA + 8) + 16 * qi);
+              } else {
+                const uint2 wA = *reinterpret_cast<const uint2*>(kst + 64 * tA + 32 * gi + 8 * qi);
+                const uint2 wB =
+                    *reinterpret_cast<const uint2*>(kst + 64 * (tA + 8) + 32 * gi + 8 * qi);
+                kw[i][0] = make_uint4(wA.x, wA.y, 0u, 0u);
+                kw[i][1] = make_uint4(wB.x, wB.y, 0u, 0u);
               }
-              const uint32_t A[4] = {wa & 0x000F000Fu, wb & 0x000F000Fu, wa & 0x00F000F0u,
-                                     wb & 0x00F000F0u};
+            }
 #pragma unroll
-              for (int nt = 0; nt < NT; ++nt) mma_16816(d[nt][i], A, bq[nt][kb][0], bq[nt][kb][1]);
+            for (int kk = 0; kk < KB / NH; ++kk) {
+              const int kb = (KB / NH) * hk + kk;
+#pragma unroll
+              for (int i = 0; i < MTG; ++i) {
+                uint32_t A[4];
+                if constexpr (F::k8) {
+                  // bytes 0, 1 (a0, a1) and 2, 3 (a2, a3) of word kk, each
+                  // moved to bit 0 of a 16-bit half
+                  const uint32_t wa = word_of(kw[i][0], kk), wb = word_of(kw[i][1], kk);
+                  A[0] = __byte_perm(wa, 0u, 0x4140);
+                  A[1] = __byte_perm(wb, 0u, 0x4140);
+                  A[2] = __byte_perm(wa, 0u, 0x4342);
+                  A[3] = __byte_perm(wb, 0u, 0x4342);
+                } else {
+                  uint32_t wa = word_of(kw[i][0], kb >> 1), wb = word_of(kw[i][1], kb >> 1);
+                  if (kb & 1) {
+                    wa >>= 8;
+                    wb >>= 8;
+                  }
+                  A[0] = wa & 0x000F000Fu;
+                  A[1] = wb & 0x000F000Fu;
+                  A[2] = wa & 0x00F000F0u;
+                  A[3] = wb & 0x00F000F0u;
+                }
+#pragma unroll
+                for (int nt = 0; nt < NT; ++nt)
+                  mma_16816(d[nt][i], A, bq[nt][kb][0], bq[nt][kb][1]);
+              }
             }
           }
 #pragma unroll
@@ -957,6 +991,7 @@ int decode_mma_ctas_per_sm(int g, int fmt) {
     case kFmtM16: return ctas_for<RecFmt<kFmtM16>::bytes>(g);
     case kFmtG64: return ctas_for<RecFmt<kFmtG64>::bytes>(g);
     case kFmtV4: return ctas_for<RecFmt<kFmtV4>::bytes>(g);
+    case kFmtK8: return ctas_for<RecFmt<kFmtK8>::bytes>(g);
     default: return ctas_for<RecFmt<kFmtF32>::bytes>(g);   // fp32 and per-channel records
   }
 }
@@ -966,6 +1001,7 @@ cudaError_t launch_decode_mma(const DecodeArgs& a, cudaStream_t s) {
   if (a.fmt == kFmtPC) return a.g <= 4 ? launch_nt<1, kFmtPC>(a, s) : launch_nt<2, kFmtPC>(a, s);
   if (a.fmt == kFmtG64) return a.g <= 4 ? launch_nt<1, kFmtG64>(a, s) : launch_nt<2, kFmtG64>(a, s);
   if (a.fmt == kFmtV4) return a.g <= 4 ? launch_nt<1, kFmtV4>(a, s) : launch_nt<2, kFmtV4>(a, s);
+  if (a.fmt == kFmtK8) return a.g <= 4 ? launch_nt<1, kFmtK8>(a, s) : launch_nt<2, kFmtK8>(a, s);
   return a.g <= 4 ? launch_nt<1, kFmtF32>(a, s) : launch_nt<2, kFmtF32>(a, s);
 }
 

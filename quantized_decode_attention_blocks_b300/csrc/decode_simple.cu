@@ -146,20 +146,34 @@ __global__ void __launch_bounds__(kThreads) decode_simple_kernel(DecodeArgs a) {
       }
       // scores (thread = token)
       {
-        const uint32_t* row = reinterpret_cast<const uint32_t*>(S.rec + kOffKCodes + 64 * tid);
+        const uint32_t* row =
+            reinterpret_cast<const uint32_t*>(S.rec + kOffKCodes + (F::k8 ? 128 : 64) * tid);
         const float2 sz = F::get_sz_g(S.rec + F::ksz, tid, 0);
         float sc1[kMaxG];
         for (int h = 0; h < g; ++h) sc[h] = sc1[h] = 0.f;
-        for (int w = 0; w < 16; ++w) {
-          const uint32_t word = row[w];
+        if constexpr (F::k8) {
+          // byte e of word w is channel (4w + e) ^ 16 (t & 1) (k8_byte)
+          for (int w = 0; w < 32; ++w) {
+            const uint32_t word = row[w];
 #pragma unroll
-          for (int e = 0; e < 8; ++e) {
-            const float code = (float)((word >> (4 * e)) & 15u);
-            const int d = 8 * w + e;
-            if (F::g64 && w >= 8) {   // channels 64..127: the second group
-              for (int h = 0; h < g; ++h) sc1[h] = fmaf(S.qc[h][d], code, sc1[h]);
-            } else {
+            for (int e = 0; e < 4; ++e) {
+              const float code = (float)((word >> (8 * e)) & 255u);
+              const int d = (4 * w + e) ^ (16 * (tid & 1));
               for (int h = 0; h < g; ++h) sc[h] = fmaf(S.qc[h][d], code, sc[h]);
+            }
+          }
+        } else {
+          for (int w = 0; w < 16; ++w) {
+            const uint32_t word = row[w];
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+              const float code = (float)((word >> (4 * e)) & 15u);
+              const int d = 8 * w + e;
+              if (F::g64 && w >= 8) {   // channels 64..127: the second group
+                for (int h = 0; h < g; ++h) sc1[h] = fmaf(S.qc[h][d], code, sc1[h]);
+              } else {
+                for (int h = 0; h < g; ++h) sc[h] = fmaf(S.qc[h][d], code, sc[h]);
+              }
             }
           }
         }
@@ -344,6 +358,8 @@ cudaError_t launch_simple(const DecodeArgs& a, cudaStream_t s) {
 
 }  // namespace
 
+static_assert(sizeof(DecodeSmem) <= 232448, "one CTA's shared memory is at most 227 KB");
+
 // Resident CTAs per SM of the CUDA-core decode: its shared memory (228 KB
 // per SM, 1 KB reserved per CTA), at most 4.  Host-only arithmetic.
 int decode_simple_ctas_per_sm() {
@@ -356,6 +372,7 @@ cudaError_t launch_decode_simple(const DecodeArgs& a, cudaStream_t s) {
   if (a.fmt == kFmtPC) return launch_simple<kFmtPC>(a, s);
   if (a.fmt == kFmtG64) return launch_simple<kFmtG64>(a, s);
   if (a.fmt == kFmtV4) return launch_simple<kFmtV4>(a, s);
+  if (a.fmt == kFmtK8) return launch_simple<kFmtK8>(a, s);
   return launch_simple<kFmtF32>(a, s);
 }
 

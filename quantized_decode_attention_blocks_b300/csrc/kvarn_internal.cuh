@@ -46,13 +46,23 @@ constexpr int kVPart = kRec - kKPart;  // V part: [9728, 15360)
 //   t = 16k + 8f + 2j + s is nibble 4s + 2(k & 1) + f of word
 //   256m + 32r + 8j + 4e + (k >> 1), see v4_word), [17920, 18944) V {s', z'}
 //   fp32 per token, [18944, 19456) V c_d.
+// 5 = "k8v4_g128", 8-bit keys and 4-bit values: K codes [0, 16384), one byte
+//   per channel, token-major, the 16-byte chunks of odd tokens swapped
+//   pairwise (channel d of token t at byte 128 t + (d ^ 16 (t & 1)), see
+//   k8_byte), [16384, 17408) K {s', z'} fp32 per token, [17408, 17920) K c_d,
+//   then the V part of format 4: [17920, 26112) V codes, [26112, 27136) V
+//   {s', z'}, [27136, 27648) V c_d.
 // Every format dequantizes as yhat_td = alpha_t beta_d q_td + gamma_t delta_d:
 // (alpha, gamma) = (s', z') (of d's group for format 3) and beta = delta = c_d
-// for formats 0, 1 and 3, alpha = gamma = r_t and (beta, delta) = (cs_d, cz_d)
+// for formats 0, 1, 3, 4 and 5, alpha = gamma = r_t and (beta, delta) = (cs_d, cz_d)
 // for format 2.  The accessors take the address of the field (record part +
 // offset).
-constexpr int kFmtF32 = 0, kFmtM16 = 1, kFmtPC = 2, kFmtG64 = 3, kFmtV4 = 4;
-constexpr int kRecMax = 19456;    // the largest record (format 4)
+constexpr int kFmtF32 = 0, kFmtM16 = 1, kFmtPC = 2, kFmtG64 = 3, kFmtV4 = 4, kFmtK8 = 5;
+constexpr int kRecMax = 27648;    // the largest record (format 5)
+// Byte of the 8-bit K code of channel d, token t (format 5).  In odd tokens
+// the 16-byte chunks trade places, so that the eight rows of a decode warp's
+// 16-byte loads (two tokens per quarter warp) fall in different banks.
+__host__ __device__ constexpr int k8_byte(int d, int t) { return 128 * t + (d ^ (16 * (t & 1))); }
 // Word of the 4-bit V code region holding channel c, token-digit j and
 // word p = k >> 1 (format 4); its nibble 4s + 2(k & 1) + f holds the token.
 __host__ __device__ constexpr int v4_word(int c, int j, int p) {
@@ -63,14 +73,16 @@ struct RecFmt {
   static constexpr bool m16 = FMT == kFmtM16;
   static constexpr bool pc = FMT == kFmtPC;
   static constexpr bool g64 = FMT == kFmtG64;
-  static constexpr bool v4 = FMT == kFmtV4;
-  static constexpr int bytes = m16 ? 13824 : g64 ? 17408 : v4 ? 19456 : 15360;
-  static constexpr int kpart = m16 ? 8960 : g64 ? 10752 : 9728;   // K part [0, kpart)
+  static constexpr bool k8 = FMT == kFmtK8;        // 8-bit keys
+  static constexpr bool v4 = FMT == kFmtV4 || k8;  // 4-bit values
+  static constexpr int bytes = m16 ? 13824 : g64 ? 17408 : k8 ? 27648 : v4 ? 19456 : 15360;
+  static constexpr int kpart = m16 ? 8960 : g64 ? 10752 : k8 ? 17920 : 9728;   // K part [0, kpart)
   static constexpr int vpart = bytes - kpart;       // V part [kpart, bytes)
-  static constexpr int ksz = 8192;                  // per-token fields
-  static constexpr int kc = m16 ? 8704 : pc ? 8704 : g64 ? 10240 : 9216;   // per-channel fields
-  static constexpr int vsz = m16 ? 13056 : g64 ? 14848 : v4 ? 17920 : 13824;   // from the start
-  static constexpr int vc = m16 ? 13568 : pc ? 14336 : g64 ? 16896 : v4 ? 18944 : 14848;
+  static constexpr int ksz = k8 ? 16384 : 8192;     // per-token fields
+  static constexpr int kc = m16 ? 8704 : pc ? 8704 : g64 ? 10240 : k8 ? 17408 : 9216;   // per-channel
+  static constexpr int vsz = m16 ? 13056 : g64 ? 14848 : k8 ? 26112 : v4 ? 17920 : 13824;   // from the start
+  static constexpr int vc = m16 ? 13568 : pc ? 14336 : g64 ? 16896 : k8 ? 27136 : v4 ? 18944 : 14848;
+  static constexpr int kbits = k8 ? 8 : 4;
   static constexpr int vbits = v4 ? 4 : 2;
   // (alpha_t, gamma_t) of token t for the channels of group g (g = 0 unless
   // g64)
@@ -168,15 +180,19 @@ static_assert(RecFmt<kFmtM16>::kpart % 16 == 0 && RecFmt<kFmtM16>::vpart % 16 ==
                   RecFmt<kFmtG64>::kpart % 16 == 0 && RecFmt<kFmtG64>::vpart % 16 == 0 &&
                   RecFmt<kFmtG64>::kc % 16 == 0 && RecFmt<kFmtG64>::vsz % 16 == 0 &&
                   RecFmt<kFmtG64>::vc % 16 == 0 && RecFmt<kFmtV4>::vsz % 16 == 0 &&
-                  RecFmt<kFmtV4>::vc % 16 == 0 && RecFmt<kFmtV4>::bytes == kRecMax,
+                  RecFmt<kFmtV4>::vc % 16 == 0 && RecFmt<kFmtK8>::kpart % 16 == 0 &&
+                  RecFmt<kFmtK8>::vsz % 16 == 0 && RecFmt<kFmtK8>::vc % 16 == 0 &&
+                  RecFmt<kFmtK8>::kc % 16 == 0 && RecFmt<kFmtK8>::vpart == RecFmt<kFmtV4>::vpart &&
+                  RecFmt<kFmtK8>::bytes == kRecMax,
               "bulk copies and vector loads need 16-byte parts and fields");
 // The format code of a configuration.
-__host__ __device__ constexpr int fmt_of(int meta16, int per_channel, int group, int v_bits) {
-  return v_bits == 4 ? kFmtV4 : group == 64 ? kFmtG64 : per_channel ? kFmtPC
-         : meta16 ? kFmtM16 : kFmtF32;
+__host__ __device__ constexpr int fmt_of(int meta16, int per_channel, int group, int v_bits,
+                                         int k_bits = 4) {
+  return k_bits == 8 ? kFmtK8 : v_bits == 4 ? kFmtV4 : group == 64 ? kFmtG64
+         : per_channel ? kFmtPC : meta16 ? kFmtM16 : kFmtF32;
 }
 inline int cfg_fmt(const kvarn_config_t* c) {
-  return fmt_of(c->meta_fp16, c->per_channel, c->group, c->v_bits);
+  return fmt_of(c->meta_fp16, c->per_channel, c->group, c->v_bits, c->k_bits);
 }
 
 // Split-K partial state per (sequence, query head, split): m, l, 2 pad, o[128]

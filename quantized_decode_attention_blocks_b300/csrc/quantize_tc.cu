@@ -66,8 +66,10 @@ constexpr uint64_t kQWaitNs = 2000000000ull;
 constexpr uint32_t kIdesc = (1u << 4) | ((128u >> 3) << 17) | ((128u >> 4) << 24);
 constexpr float kMagic = 12582912.0f;             // 1.5 * 2^23
 constexpr uint32_t kMagicBits = 0x4B400000u;
-// kMagicBits summed over the eight nibble (sixteen crumb) positions of a word
+// kMagicBits summed over the eight nibble (sixteen crumb, four byte)
+// positions of a word
 constexpr uint32_t kMagicK = kMagicBits * 0x11111111u;
+constexpr uint32_t kMagicB = kMagicBits * 0x01010101u;
 constexpr uint32_t kMagicV = kMagicBits * 0x55555555u;
 
 // Tile handed from a pipeline's leader thread to its other threads.
@@ -80,8 +82,8 @@ struct TileInfo {
 struct __align__(1024) QSmem {
   uint8_t hs[kTileBytes];                // +-1 Sylvester matrix, fp16, swizzled
   uint8_t x[kWG][2][kTileBytes];         // input tiles, 2 stages per pipeline
-  __align__(128) uint8_t out[kWG][RecFmt<kFmtG64>::kpart];   // packed record part (the
-                                                             // largest), staged for the bulk store
+  __align__(128) uint8_t out[kWG][RecFmt<kFmtK8>::kpart];   // packed record part (the
+                                                            // largest), staged for the bulk store
   __align__(16) float ra[kWG][kT];       // 1 / r_t, in units of Y
   float r1part[kWG][2][kT];              // first row step of the next tile: half sums
   float r1x0[kWG][kT];                   //   and channel 0
@@ -748,24 +750,46 @@ __global__ void __launch_bounds__(kQThreads, 1)
           constexpr bool G64 = RecFmt<FMT>::g64;
           const float lo = grp_min<G64>(mn[e]), hi = grp_max<G64>(mx[e]);
           const float range = hi - lo;
-          const float inv = range > 0.f ? __fdividef(15.f, range) : 0.f;
+          constexpr float kq = RecFmt<FMT>::k8 ? 255.f : 15.f;   // 2^bits - 1 of K
+          const float inv = range > 0.f ? __fdividef(kq, range) : 0.f;
           const int t = frow(e);
           if ((q & (G64 ? 1 : 3)) == 0)
             RecFmt<FMT>::put_sz_g(out + RecFmt<FMT>::ksz, t, G64 ? q >> 1 : 0,
-                                  range * (kInvSqrt128 / 15.f), lo * kInvSqrt128);
-          // u = (x - min) (15 / range) + 1.5 * 2^23: the code in the low bits
+                                  range * (kInvSqrt128 / kq), lo * kInvSqrt128);
+          // u = (x - min) (kq / range) + 1.5 * 2^23: the code in the low bits
           const float2 nm = make_float2(-lo, -lo), iv = make_float2(inv, inv);
-          uint32_t acc[4];
+          if constexpr (RecFmt<FMT>::k8) {
+            // 8-bit: the row's channels 32q .. 32q + 31 are bytes of its
+            // chunks 2q, 2q + 1 (swapped in odd tokens): byte 2 (k & 1) + b
+            // of word k >> 1 from column pair k
+            uint32_t acc[8];
 #pragma unroll
-          for (int j = 0; j < 4; ++j) acc[j] = 0u - kMagicK;
+            for (int j = 0; j < 8; ++j) acc[j] = 0u - kMagicB;
 #pragma unroll
-          for (int k = 0; k < 16; ++k) {
-            const float2 f = __ffma2_rn(__fadd2_rn(pair(v, k, e), nm), iv, mg);
-            acc[k >> 2] += __float_as_uint(f.x) << (8 * (k & 3));
-            acc[k >> 2] += __float_as_uint(f.y) << (8 * (k & 3) + 4);
+            for (int k = 0; k < 16; ++k) {
+              const float2 f = __ffma2_rn(__fadd2_rn(pair(v, k, e), nm), iv, mg);
+              acc[k >> 1] += __float_as_uint(f.x) << (16 * (k & 1));
+              acc[k >> 1] += __float_as_uint(f.y) << (16 * (k & 1) + 8);
+            }
+            uint8_t* const row_out = out + kOffKCodes + 128 * t;
+            const int sw = t & 1;
+            *reinterpret_cast<uint4*>(row_out + 16 * ((2 * q) ^ sw)) =
+                make_uint4(acc[0], acc[1], acc[2], acc[3]);
+            *reinterpret_cast<uint4*>(row_out + 16 * ((2 * q + 1) ^ sw)) =
+                make_uint4(acc[4], acc[5], acc[6], acc[7]);
+          } else {
+            uint32_t acc[4];
+#pragma unroll
+            for (int j = 0; j < 4; ++j) acc[j] = 0u - kMagicK;
+#pragma unroll
+            for (int k = 0; k < 16; ++k) {
+              const float2 f = __ffma2_rn(__fadd2_rn(pair(v, k, e), nm), iv, mg);
+              acc[k >> 2] += __float_as_uint(f.x) << (8 * (k & 3));
+              acc[k >> 2] += __float_as_uint(f.y) << (8 * (k & 3) + 4);
+            }
+            *reinterpret_cast<uint4*>(out + kOffKCodes + 64 * t + 16 * q) =
+                make_uint4(acc[0], acc[1], acc[2], acc[3]);
           }
-          *reinterpret_cast<uint4*>(out + kOffKCodes + 64 * t + 16 * q) =
-              make_uint4(acc[0], acc[1], acc[2], acc[3]);
         }
       }
     } else {
@@ -952,6 +976,7 @@ bool encode_tile_map(CUtensorMap* map, const void* base, int64_t sb, int64_t st,
 }
 
 constexpr int kQSmemBytes = (int)sizeof(QSmem) + 1024;
+static_assert(kQSmemBytes <= 232448, "one CTA's shared memory is at most 227 KB");
 
 template <int FMT>
 cudaError_t launch_tiles(const CUtensorMap& mk, const CUtensorMap& mv, const QTileArgs& qa,
@@ -974,6 +999,7 @@ cudaError_t launch_fmt(int fmt, const CUtensorMap& mk, const CUtensorMap& mv,
   if (fmt == kFmtPC) return launch_tiles<kFmtPC>(mk, mv, qa, cp, s);
   if (fmt == kFmtG64) return launch_tiles<kFmtG64>(mk, mv, qa, cp, s);
   if (fmt == kFmtV4) return launch_tiles<kFmtV4>(mk, mv, qa, cp, s);
+  if (fmt == kFmtK8) return launch_tiles<kFmtK8>(mk, mv, qa, cp, s);
   return launch_tiles<kFmtF32>(mk, mv, qa, cp, s);
 }
 

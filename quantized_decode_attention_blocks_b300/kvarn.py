@@ -23,6 +23,7 @@ PAGE_BYTES = 15360
 PAGE_BYTES_M16 = 13824     # KVARN_PAGE_BYTES_M16: format variant "_m16"
 PAGE_BYTES_G64 = 17408     # KVARN_PAGE_BYTES_G64: format variant "k4v2_g64"
 PAGE_BYTES_V4 = 19456      # KVARN_PAGE_BYTES_V4: format variant "k4v4_g128"
+PAGE_BYTES_K8 = 27648      # KVARN_PAGE_BYTES_K8: format variant "k8v4_g128"
 FP8_PAGE_BYTES = 33792     # KVARN_FP8_PAGE_BYTES
 FP16_PAGE_BYTES = 65536            # KVARN_FP16_PAGE_BYTES
 NOALLOC_SCRATCH_BYTES = 4 << 20   # KVARN_NOALLOC_SCRATCH_BYTES
@@ -59,6 +60,8 @@ class Config(ctypes.Structure):
         """Bytes of one page record of this format (kvarn_page_bytes)."""
         if self.group == 64:
             return PAGE_BYTES_G64
+        if self.k_bits == 8:
+            return PAGE_BYTES_K8
         if self.v_bits == 4:
             return PAGE_BYTES_V4
         return PAGE_BYTES_M16 if self.meta_fp16 else PAGE_BYTES

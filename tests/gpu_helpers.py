@@ -9,8 +9,10 @@ import quantized_decode_attention_blocks_b300 as kv
 DEV = torch.device("cuda:0") if torch.cuda.is_available() else None
 
 
-def config(hq, hkv, iters=None, rms=False, m16=False, pc=False, g64=False, v4=False):
-    fmt = (("k4v2_g64" if g64 else "k4v4_g128" if v4 else "k4v2_g128") + ("_rms" if rms else "")
+def config(hq, hkv, iters=None, rms=False, m16=False, pc=False, g64=False, v4=False,
+           k8=False):
+    fmt = (("k4v2_g64" if g64 else "k8v4_g128" if k8 else "k4v4_g128" if v4 else "k4v2_g128")
+           + ("_rms" if rms else "")
            + ("_m16" if m16 else "") + ("_pc" if pc else "")
            + ("" if iters is None else f"_s{iters}"))
     return kv.config_from_string(fmt, hq, hkv)

@@ -2,7 +2,9 @@
 
   * codes: bit-exact, except elements whose oracle pre-rounding value u lies
     within 1e-5 of a rounding boundary (k + 1/2); such flips must be at most
-    1e-4 of all elements;
+    1e-4 of all elements.  For 8-bit codes ("k8v4") u spans 0..255 instead
+    of 0..15 and fp32 carries 17 times the absolute error there, so the
+    window is 1e-5 x 255 / 15;
   * s' and c: |gpu - ref| <= 1e-5 |ref| (1e-12 absolute when ref = 0);
   * z': |gpu - ref| <= 1e-5 (|z'| + s' (2^b - 1));
   * fp16 metadata (format "_m16"): equal to the oracle's fp16 value, or one
@@ -23,8 +25,9 @@ BOUNDARY = 1e-5
 FLIP_RATE = 1e-4
 
 
-def near_boundary(u):
-    return np.abs(u - np.floor(u) - 0.5) < BOUNDARY
+def near_boundary(u, bits: int = 4):
+    window = BOUNDARY * (255 / 15 if bits == 8 else 1)
+    return np.abs(u - np.floor(u) - 0.5) < window
 
 
 def _compare_meta16(tag, got16, ref16, ref32):
@@ -78,31 +81,34 @@ def _compare_g64(tag, got, ref, is_v, bits):
 
 def compare_record(got: np.ndarray, ref: np.ndarray, u_k=None, u_v=None, stats=None,
                    meta16: bool = False, ref32: np.ndarray = None, pc: bool = False,
-                   g64: bool = False, v4: bool = False):
+                   g64: bool = False, v4: bool = False, k8: bool = False):
     """Compares one record (GPU) with the oracle's.  u_k, u_v: oracle
     pre-rounding values [128][128] (token, channel).  meta16: the "_m16"
     format, whose metadata is judged against ref32, the oracle's record of
     the same tile in the fp32 format; pc: the "_pc" format.  Returns a dict."""
     out = {} if stats is None else stats
     for is_v, u in ((False, u_k), (True, u_v)):
-        bits = 2 if is_v and not v4 else 4
+        bits = (4 if v4 or k8 else 2) if is_v else (8 if k8 else 4)
         if pc or g64:
             unpack = kvref.unpack_part_pc if pc else kvref.unpack_part_g64
             qg = unpack(got, is_v)[0]
             qr = unpack(ref, is_v)[0]
         else:
-            qg, sg, zg, cg = kvref.unpack_part(got, is_v, meta16, v4)
-            qr, sr, zr, cr = kvref.unpack_part(ref, is_v, meta16, v4)
+            qg, sg, zg, cg = kvref.unpack_part(got, is_v, meta16, v4, k8=k8)
+            qr, sr, zr, cr = kvref.unpack_part(ref, is_v, meta16, v4, k8=k8)
         tag = "v" if is_v else "k"
         diff = qg != qr
         n_diff = int(diff.sum())
         if n_diff:
             assert u is not None, f"{tag}: {n_diff} code mismatches and no u to judge them"
-            ok = near_boundary(u)
+            ok = near_boundary(u, bits)
             bad = diff & ~ok
             assert not bad.any(), (f"{tag}: {int(bad.sum())} code mismatches away from a "
                                    f"rounding boundary, e.g. u={u[bad][:4]}, gpu={qg[bad][:4]}, "
                                    f"ref={qr[bad][:4]}")
+        if n_diff:   # the widest distance from a boundary among the flips
+            dist = float(np.abs(u[diff] - np.floor(u[diff]) - 0.5).max())
+            out[f"{tag}_flip_dist"] = max(out.get(f"{tag}_flip_dist", 0.0), dist)
         out[f"{tag}_flips"] = out.get(f"{tag}_flips", 0) + n_diff
         out[f"{tag}_codes"] = out.get(f"{tag}_codes", 0) + qg.size
         if pc:

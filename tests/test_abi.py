@@ -39,7 +39,8 @@ def test_header_constants_match_binding():
     for name, val in (("KVARN_PAGE_BYTES", K.PAGE_BYTES),
                       ("KVARN_PAGE_BYTES_M16", K.PAGE_BYTES_M16),
                       ("KVARN_PAGE_BYTES_G64", K.PAGE_BYTES_G64),
-                      ("KVARN_PAGE_BYTES_V4", K.PAGE_BYTES_V4), ("KVARN_OK", K.OK),
+                      ("KVARN_PAGE_BYTES_V4", K.PAGE_BYTES_V4),
+                      ("KVARN_PAGE_BYTES_K8", K.PAGE_BYTES_K8), ("KVARN_OK", K.OK),
                       ("KVARN_ERR_INVALID_ARG", K.ERR_INVALID_ARG),
                       ("KVARN_ERR_UNSUPPORTED", K.ERR_UNSUPPORTED),
                       ("KVARN_ERR_WORKSPACE", K.ERR_WORKSPACE), ("KVARN_ERR_LAUNCH", K.ERR_LAUNCH),
@@ -101,7 +102,16 @@ def test_config_parsing():
     for bad in ("k4v4_g128_m16", "k4v4_g128_pc", "k4v4_g64"):
         with pytest.raises(kv.KvarnError):
             kv.config_from_string(bad, 12, 2)
-    for bad in ("k8v4_g128", "k4v2_g96", "k4v2_g128_x", "k4v2_g128_s", "k4v2_g128_s999"):
+    # 8-bit keys, 4-bit values: "k8v4_g128", with "_rms" but not "_m16" / "_pc"
+    k8 = kv.config_from_string("kvarn_k8v4_g128_rms_s1", 12, 2)
+    assert (k8.k_bits, k8.v_bits, k8.group, k8.sinkhorn_rms, k8.sinkhorn_iters) == (8, 4, 128, 1, 1)
+    assert kv.page_bytes(k8) == 27648 == 216 * 128 == k8.page_bytes
+    for bad in ("k8v4_g128_m16", "k8v4_g128_pc", "k8v4_g64", "k8v2_g128"):
+        with pytest.raises(kv.KvarnError):
+            kv.config_from_string(bad, 12, 2)
+    k8.v_bits = 2
+    assert kv.config_validate(k8) == K.ERR_UNSUPPORTED
+    for bad in ("k2v2_g128", "k4v2_g96", "k4v2_g128_x", "k4v2_g128_s", "k4v2_g128_s999"):
         with pytest.raises(kv.KvarnError) as e:
             kv.config_from_string(bad, 32, 8)
         assert e.value.code == K.ERR_UNSUPPORTED
@@ -151,6 +161,19 @@ def test_split_plan_fills_one_wave_and_covers_every_page(sms, g):
                 assert pps * ns >= pages and pps * (ns - 1) < pages
                 assert ns == 1 or batch * hkv * ns <= sms * per_sm
                 assert (ws == 0) == (ns == 1)
+
+
+def test_split_plan_of_8bit_keys_follows_its_shared_memory():
+    # the 27648-byte records of "k8v4_g128" leave shared memory for two
+    # tensor-core CTAs per SM with one head tile (g <= 4) and one with two,
+    # and the plan sizes its wave by that
+    for g in (1, 4, 6, 8):
+        per_sm = 2 if g <= 4 else 1
+        c = kv.config_from_string("k8v4_g128", g * 2, 2)
+        for batch in (1, 3, 16):
+            pps, ns, ws = kv.decode_split_plan(c, batch, 131072, B300_SMS)
+            assert ns > 1 and batch * 2 * ns <= B300_SMS * per_sm
+            assert pps * ns >= 1024 and pps * (ns - 1) < 1024
 
 
 def test_split_plan_grows_with_the_sm_count():

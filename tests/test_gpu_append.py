@@ -13,17 +13,18 @@ from workloads import synth
 pytestmark = pytest.mark.gpu
 
 
-@pytest.mark.parametrize("m16,pc,g64,v4", [(False, False, False, False),
-                                           (True, False, False, False),
-                                           (False, True, False, False),
-                                           (False, False, True, False),
-                                           (False, False, False, True)])
-def test_append_fills_pages_like_prefill(m16, pc, g64, v4):
+@pytest.mark.parametrize("m16,pc,g64,v4,k8", [(False, False, False, False, False),
+                                              (True, False, False, False, False),
+                                              (False, True, False, False, False),
+                                              (False, False, True, False, False),
+                                              (False, False, False, True, False),
+                                              (False, False, False, False, True)])
+def test_append_fills_pages_like_prefill(m16, pc, g64, v4, k8):
     # m16: format variant "_m16" (fp16 metadata, 13824-byte records); pc:
     # format variant "_pc" (per-channel groups)
     w = synth.scaled(synth.WORKLOADS["llama3_8b_layer"], batch=3, seq=384, hkv=2, hq=8)
     k, v = synth.kv(w, device=DEV)
-    cfg = config(w.hq, w.hkv, m16=m16, pc=pc, g64=g64, v4=v4)
+    cfg = config(w.hq, w.hkv, m16=m16, pc=pc, g64=g64, v4=v4, k8=k8)
     table = torch.arange(9, dtype=torch.int32).reshape(3, 3)
     lens = torch.tensor([384, 384, 384], dtype=torch.int32)
     ref_pool, _, _, _ = prefill(cfg, k, v, lens, table, 9)
@@ -46,7 +47,7 @@ def test_append_fills_pages_like_prefill(m16, pc, g64, v4):
     assert torch.equal(tk[1, :, :72], k[1, 128:200].transpose(0, 1))
     # and against the oracle (boundary rule)
     ref = kvref.quantize_blocks(host(k), host(v), host(lens), host(table), 9, 2, want_u=True,
-                                meta16=m16, pc=pc, g64=g64, v4=v4)
+                                meta16=m16, pc=pc, g64=g64, v4=v4, k8=k8)
     ref32 = kvref.quantize_blocks(host(k), host(v), host(lens), host(table), 9, 2) if m16 else None
     stats = {}
     for b in (0, 2):
@@ -57,7 +58,7 @@ def test_append_fills_pages_like_prefill(m16, pc, g64, v4):
                                       ref["u_k"][b, j, h], ref["u_v"][b, j, h], stats,
                                       meta16=m16,
                                       ref32=ref32["pool"][page, h] if m16 else None, pc=pc,
-                                      g64=g64, v4=v4)
+                                      g64=g64, v4=v4, k8=k8)
     parity.check_flip_rate(stats)
 
 

@@ -155,11 +155,11 @@ def test_chunk_prefill_workload_sampled():
         parity.compare_attention(host(out[b:b + 1]).astype(np.float64), ref)
 
 
-@pytest.mark.parametrize("fmt", ["g64", "v4"])
-def test_g64_and_v4_formats_are_refused(fmt):
-    # the g64 and k4v4 records do not fit the kernel's record buffers: the
-    # call says so before any launch
-    cfg = config(8, 2, g64=fmt == "g64", v4=fmt == "v4")
+@pytest.mark.parametrize("fmt", ["g64", "v4", "k8"])
+def test_g64_v4_and_k8_formats_are_refused(fmt):
+    # the g64, k4v4 and k8v4 records do not fit the kernel's record buffers:
+    # the call says so before any launch
+    cfg = config(8, 2, g64=fmt == "g64", v4=fmt == "v4", k8=fmt == "k8")
     q = torch.zeros((1, 4, 8, 128), dtype=torch.float16, device=DEV)
     pool = kv.alloc_pool(cfg, 2, DEV)
     tk, tv = kv.alloc_tails(cfg, 1, DEV)

@@ -18,11 +18,11 @@ pytestmark = pytest.mark.gpu
 
 
 def _run(w, lens, table, num_pages, q=None, max_seq=None, m16=False, pc=False, g64=False,
-         v4=False):
+         v4=False, k8=False):
     max_seq = int(lens.max()) if max_seq is None else max_seq
     S = max(int(lens.max()), 1)
     k, v = synth.kv(w, device=DEV, seq=S)
-    cfg = config(w.hq, w.hkv, m16=m16, pc=pc, g64=g64, v4=v4)
+    cfg = config(w.hq, w.hkv, m16=m16, pc=pc, g64=g64, v4=v4, k8=k8)
     pool, tk, tv, st = prefill(cfg, k, v, lens, table, num_pages, max_seq=max_seq)
     if q is None:
         q = synth.queries(w)
@@ -31,7 +31,7 @@ def _run(w, lens, table, num_pages, q=None, max_seq=None, m16=False, pc=False, g
     assert int(st.item()) == 0 and int(st2.item()) == 0
     ref = kvref.decode_attention(host(q), host(pool), host(table), host(lens), host(tk),
                                  host(tv), w.hq, w.hkv, route=1, meta16=m16, pc=pc, g64=g64,
-                                 v4=v4)
+                                 v4=v4, k8=k8)
     res = parity.compare_attention(host(out), ref)
     res.update(got=host(out).astype(np.float64), ref=ref)
     return res, (cfg, q, pool, table, lens, tk, tv, out, ws, max_seq)
@@ -115,6 +115,26 @@ def test_v4_format_group_sizes(hq, hkv):
     g = torch.Generator().manual_seed(65)
     table = torch.randperm(B * mb, generator=g).to(torch.int32).reshape(B, mb)
     _run(w, lens, table, B * mb, v4=True)
+
+
+@pytest.mark.parametrize("hq,hkv", [(1, 1), (4, 2), (6, 2), (8, 2), (12, 2), (32, 8), (16, 1)])
+def test_k8_format_group_sizes(hq, hkv):
+    # format variant "k8v4_g128" (8-bit keys): one and two head tiles of the
+    # tensor-core kernel and the CUDA-core kernel (g = 16)
+    lens = torch.tensor([0, 1, 127, 128, 129, 300, 1000, 2048], dtype=torch.int32)
+    B = len(lens)
+    w = synth.scaled(synth.WORKLOADS["llama3_8b_layer"], batch=B, seq=2048, hkv=hkv, hq=hq)
+    mb = 16
+    g = torch.Generator().manual_seed(66)
+    table = torch.randperm(B * mb, generator=g).to(torch.int32).reshape(B, mb)
+    _run(w, lens, table, B * mb, k8=True)
+
+
+def test_k8_format_many_splits():
+    w = synth.scaled(synth.WORKLOADS["long_context"], batch=1, seq=20000, hkv=2, hq=8)
+    lens = torch.tensor([20000], dtype=torch.int32)
+    table = torch.arange(157, dtype=torch.int32).reshape(1, 157)
+    _run(w, lens, table, 157, k8=True)
 
 
 def test_v4_format_many_splits():

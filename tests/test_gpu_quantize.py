@@ -16,16 +16,16 @@ pytestmark = pytest.mark.gpu
 
 
 def _check_prefill(w, lens, table, num_pages, iters=2, k=None, v=None, rms=False, m16=False,
-                   pc=False, g64=False, v4=False):
+                   pc=False, g64=False, v4=False, k8=False):
     if k is None:
         k, v = synth.kv(w, device=DEV)
-    cfg = config(w.hq, w.hkv, iters, rms=rms, m16=m16, pc=pc, g64=g64, v4=v4)
+    cfg = config(w.hq, w.hkv, iters, rms=rms, m16=m16, pc=pc, g64=g64, v4=v4, k8=k8)
     pool, tk, tv, status = prefill(cfg, k, v, lens, table, num_pages, max_seq=w.seq)
     torch.cuda.synchronize()
     assert int(status.item()) == 0
     kh, vh = host(k), host(v)
     ref = kvref.quantize_blocks(kh, vh, host(lens), host(table), num_pages, iters, want_u=True,
-                                rms=rms, meta16=m16, pc=pc, g64=g64, v4=v4)
+                                rms=rms, meta16=m16, pc=pc, g64=g64, v4=v4, k8=k8)
     ref32 = (kvref.quantize_blocks(kh, vh, host(lens), host(table), num_pages, iters, rms=rms)
              if m16 else None)
     got_pool = host(pool)
@@ -38,7 +38,7 @@ def _check_prefill(w, lens, table, num_pages, iters=2, k=None, v=None, rms=False
                 parity.compare_record(got_pool[page, h], ref["pool"][page, h],
                                       ref["u_k"][b, j, h], ref["u_v"][b, j, h], stats, meta16=m16,
                                       ref32=ref32["pool"][page, h] if m16 else None, pc=pc,
-                                      g64=g64, v4=v4)
+                                      g64=g64, v4=v4, k8=k8)
     parity.check_flip_rate(stats)
     _check_prefill.last = (pool, tk, tv, cfg)
     # leftover tokens copied verbatim into the tails
@@ -257,3 +257,21 @@ def test_v4_variant(rms, iters):
     table = torch.randperm(3 * 9, generator=g).to(torch.int32).reshape(3, 9)
     _check_prefill(w, lens, table, 27, iters=iters, k=k, v=v, rms=rms, v4=True)
     assert _check_prefill.last[0].shape[-1] == 19456
+
+
+@pytest.mark.parametrize("rms,iters", [(False, 2), (True, 2), (False, 0)])
+def test_k8_variant(rms, iters):
+    # format variant "k8v4_g128" (8-bit keys, 4-bit values): ragged lengths on
+    # permuted pages, the special tiles included
+    w = synth.scaled(synth.WORKLOADS["llama3_8b_layer"], batch=3, seq=1100, hkv=2, hq=8)
+    k, v = synth.kv(w, device=DEV)
+    k[0, :128, 0] = 0                       # a zero tile
+    v[1, :128, 1] = 1.5                     # a constant tile
+    k[2, 300, 1, 7] = 30000.0               # a single outlier (in K)
+    lens = torch.tensor([1100, 300, 640], dtype=torch.int32)
+    g = torch.Generator().manual_seed(76)
+    table = torch.randperm(3 * 9, generator=g).to(torch.int32).reshape(3, 9)
+    stats = _check_prefill(w, lens, table, 27, iters=iters, k=k, v=v, rms=rms, k8=True)
+    assert _check_prefill.last[0].shape[-1] == 27648
+    print(f"k8 boundary flips: {stats['k_flips']} of {stats['k_codes']} K codes, "
+          f"widest {stats.get('k_flip_dist', 0.0):.2e} from a boundary")
