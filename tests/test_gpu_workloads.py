@@ -206,3 +206,70 @@ def test_mixed_serving_full_size_with_appends():
             filled += 1
     assert filled > 0
     parity.check_flip_rate(stats)
+
+
+_KPART = {"m16": 8960, "pc": 9728, "g64": 10752, "v4": 9728, "k8": 17920}
+
+
+@pytest.mark.parametrize("variant", ["rms", "m16", "pc", "g64", "v4", "k8"])
+def test_format_variants_at_the_llama_like_size(variant):
+    # every format variant the bench times, at the size and in the launch
+    # configuration it is timed in: one prefill, one append, one decode;
+    # sampled whole tiles and whole sequences against the oracle
+    w = synth.WORKLOADS["llama3_8b_layer"]
+    rng = np.random.default_rng(300 + len(variant))
+    rms = variant == "rms"
+    fmt = {} if rms else {("meta16" if variant == "m16" else variant): True}
+    cfg = config(w.hq, w.hkv, rms=rms, **({} if rms else {variant: True}))
+    k, v = synth.kv(w, device=DEV)
+    lens = synth.seq_lens(w, device=DEV)
+    tables, num_pages = synth.block_tables(w, device=DEV)
+    table = tables[0].contiguous()
+    pool = kv.alloc_pool(cfg, num_pages, DEV)
+    tk, tv = kv.alloc_tails(cfg, w.batch, DEV)
+    st = torch.zeros(1, dtype=torch.int32, device=DEV)
+    kv.kvarn_quantize_blocks(cfg, k, v, lens, w.seq, table, pool, tk, tv, st)
+    kn, vn = synth.new_tokens(w, 0, device=DEV)
+    kv.kvarn_append_token(cfg, kn, vn, lens, table, pool, tk, tv, st)
+    lens1 = lens + 1
+    q = synth.queries(w, device=DEV)
+    out, st2 = _decode(cfg, q, pool, table, lens1, w.seq + 1, tk, tv)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0 and int(st2.item()) == 0
+    assert torch.isfinite(out.float()).all()
+    # sampled tiles
+    kpart = _KPART.get(variant, 9728)
+    lens_np = host(lens).astype(np.int64)
+    tab = host(table)
+    stats = {}
+    for _ in range(6):
+        b = int(rng.integers(w.batch))
+        j = int(rng.integers(lens_np[b] // 128))
+        h = int(rng.integers(w.hkv))
+        tkb = bits16(k[b, 128 * j:128 * j + 128, h])
+        tvb = bits16(v[b, 128 * j:128 * j + 128, h])
+        rk = kvref.quantize_tile(tkb, False, ITERS, rms=rms, **fmt)
+        rv = kvref.quantize_tile(tvb, True, ITERS, rms=rms, **fmt)
+        ref = rk["rec"].copy()
+        ref[kpart:] = rv["rec"][kpart:]
+        ref32 = None
+        if variant == "m16":
+            r32k = kvref.quantize_tile(tkb, False, ITERS)["rec"]
+            ref32 = r32k.copy()
+            ref32[9728:] = kvref.quantize_tile(tvb, True, ITERS)["rec"][9728:]
+        got = host(pool[int(tab[b, j]), h])
+        parity.compare_record(got, ref, rk["u"], rv["u"], stats, meta16=variant == "m16",
+                              ref32=ref32, pc=variant == "pc", g64=variant == "g64",
+                              v4=variant == "v4", k8=variant == "k8")
+    parity.check_flip_rate(stats)
+    # sampled whole sequences of decode
+    seqs = sorted(rng.choice(w.batch, size=2, replace=False).tolist())
+    sel = torch.tensor(seqs, dtype=torch.long, device=DEV)
+    tsel = table[sel]
+    used = torch.unique(tsel[tsel >= 0])
+    remap = torch.full((pool.shape[0],), -1, dtype=torch.int32, device=DEV)
+    remap[used] = torch.arange(used.numel(), dtype=torch.int32, device=DEV)
+    tab_c = torch.where(tsel >= 0, remap[tsel.clamp(min=0).long()], tsel)
+    ref = kvref.decode_attention(host(q[sel]), host(pool[used]), host(tab_c), host(lens1[sel]),
+                                 host(tk[sel]), host(tv[sel]), w.hq, w.hkv, route=1, **fmt)
+    parity.compare_attention(host(out[sel]), ref)
