@@ -398,6 +398,21 @@ int kvarn_snapkv_gather(const void *k, const void *v, int64_t stride_b, int64_t 
 int kvarn_dequantize_pages(const void *records, int64_t n, float *yk, float *yv,
                            kvarn_stream_t stream);
 
+/* Diagnosis for every record format: dequantizes `n` page records of the
+ * format `cfg` names ("KVarN Nasil Calisir?", the inverse of stage
+ * "Kuantize Edilmis Onbellek") into float32 rotated-space tiles.
+ *   records   [n][kvarn_page_bytes(cfg)] bytes, 16-byte aligned (device)
+ *   yk, yv    float32 [n][128 tokens][128 channels] (device), written:
+ *             yhat_td = alpha_t beta_d q_td + gamma_t delta_d, with
+ *             (alpha, gamma) = (s', z') of the token (of the channel's
+ *             group for groups of 64) and beta = delta = c_d, or for "_pc"
+ *             alpha = gamma = r_t and (beta, delta) = (cs_d, cz_d); fp16
+ *             metadata ("_m16") is widened to fp32 first.
+ * Returns KVARN_ERR_UNSUPPORTED for a bad config, KVARN_ERR_INVALID_ARG for
+ * n < 0, a null or misaligned pointer; one launch on `stream`. */
+int kvarn_dequantize_records(const kvarn_config_t *cfg, const void *records, int64_t n,
+                             float *yk, float *yv, kvarn_stream_t stream);
+
 /* ---- The FP16 paged cache the quantized one is measured against ----
  * The KVarN page (blog.edumints.com) states its capacity and throughput gains
  * relative to an FP16 KV cache; these calls are that baseline on the same

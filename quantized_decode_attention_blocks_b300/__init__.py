@@ -11,7 +11,7 @@ from .kvarn import (Config, KvarnError, alloc_decode_workspace, alloc_fp16_decod
                     kvarn_fp16_decode_attention, kvarn_fp16_write_blocks,
                     config_from_string, config_validate, decode_split_plan, decode_workspace_bytes,
                     kvarn_append_token, kvarn_chunk_attention, kvarn_decode_attention,
-                    kvarn_decode_attention_noalloc, kvarn_dequantize_pages,
+                    kvarn_decode_attention_noalloc, kvarn_dequantize_pages, kvarn_dequantize_records,
                     kvarn_quantize_blocks, lib, page_bytes, status_string, version)
 
 __all__ = ["Config", "KvarnError", "alloc_decode_workspace", "alloc_fp16_decode_workspace",
@@ -22,5 +22,5 @@ __all__ = ["Config", "KvarnError", "alloc_decode_workspace", "alloc_fp16_decode_
            "kvarn_fp16_decode_attention", "kvarn_fp16_write_blocks",
            "config_from_string", "config_validate", "decode_split_plan", "decode_workspace_bytes",
            "kvarn_append_token", "kvarn_chunk_attention", "kvarn_decode_attention",
-           "kvarn_decode_attention_noalloc", "kvarn_dequantize_pages",
+           "kvarn_decode_attention_noalloc", "kvarn_dequantize_pages", "kvarn_dequantize_records",
            "kvarn_quantize_blocks", "lib", "page_bytes", "status_string", "version"]

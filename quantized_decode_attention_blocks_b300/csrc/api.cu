@@ -654,7 +654,21 @@ int kvarn_dequantize_pages(const void* records, int64_t n, float* yk, float* yv,
   if (n == 0) return KVARN_OK;
   if (!records || !yk || !yv || !aligned16(records) || n > 0x7fffffff)
     return KVARN_ERR_INVALID_ARG;
-  return launch_dequantize(static_cast<const uint8_t*>(records), n, yk, yv,
+  return launch_dequantize(kFmtF32, static_cast<const uint8_t*>(records), n, yk, yv,
+                           (cudaStream_t)stream) == cudaSuccess
+             ? KVARN_OK
+             : KVARN_ERR_LAUNCH;
+}
+
+int kvarn_dequantize_records(const kvarn_config_t* cfg, const void* records, int64_t n,
+                             float* yk, float* yv, kvarn_stream_t stream) {
+  const int rc = kvarn_config_validate(cfg);
+  if (rc != KVARN_OK) return rc;
+  if (n < 0) return KVARN_ERR_INVALID_ARG;
+  if (n == 0) return KVARN_OK;
+  if (!records || !yk || !yv || !aligned16(records) || n > 0x7fffffff)
+    return KVARN_ERR_INVALID_ARG;
+  return launch_dequantize(cfg_fmt(cfg), static_cast<const uint8_t*>(records), n, yk, yv,
                            (cudaStream_t)stream) == cudaSuccess
              ? KVARN_OK
              : KVARN_ERR_LAUNCH;

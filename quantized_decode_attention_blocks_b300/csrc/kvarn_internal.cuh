@@ -313,7 +313,7 @@ bool decode_uses_cluster(int g, int nsplit);
 cudaError_t launch_quantize_blocks(const QuantizeArgs& a, cudaStream_t s);
 cudaError_t launch_append_token(const AppendArgs& a, cudaStream_t s);
 cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t s);
-cudaError_t launch_dequantize(const uint8_t* rec, int64_t n, float* yk, float* yv,
+cudaError_t launch_dequantize(int fmt, const uint8_t* rec, int64_t n, float* yk, float* yv,
                               cudaStream_t s);
 
 // A 4-D tensor map over fp16 data with 128-byte swizzle (dims and box

@@ -89,6 +89,7 @@ SIGNATURES = {
     "kvarn_chunk_attention": (_I, [ctypes.POINTER(Config), _P, _I, _P, _P, _I, _I, _P, _L, _P,
                                    _I, _P, _P, ctypes.c_float, _P, _P, _P]),
     "kvarn_dequantize_pages": (_I, [_P, _L, _P, _P, _P]),
+    "kvarn_dequantize_records": (_I, [_P, _P, _L, _P, _P, _P]),
     "kvarn_fp16_write_blocks": (_I, [_P, _P, _L, _L, _L, _I, _I, _P, _I, _P, _I, _P, _L, _P,
                                      _P]),
     "kvarn_fp16_decode_workspace_bytes": (ctypes.c_size_t, [_I, _I, _I, _I]),
@@ -403,6 +404,20 @@ def kvarn_dequantize_pages(records: torch.Tensor, stream=None):
     with _on(dev):
         _check(lib().kvarn_dequantize_pages(_ptr(records), n, _ptr(yk), _ptr(yv),
                                             _stream(stream, dev)), "kvarn_dequantize_pages")
+    return yk, yv
+
+
+def kvarn_dequantize_records(cfg: Config, records: torch.Tensor, stream=None):
+    """records: uint8 [n][cfg.page_bytes] (contiguous) -> (yk, yv) float32
+    [n][128][128], for any record format."""
+    dev = _arg(records, "records", torch.uint8, (None, cfg.page_bytes))
+    n = records.shape[0]
+    yk = torch.empty((n, BLOCK_TOKENS, HEAD_DIM), dtype=torch.float32, device=dev)
+    yv = torch.empty_like(yk)
+    with _on(dev):
+        _check(lib().kvarn_dequantize_records(ctypes.byref(cfg), _ptr(records), n, _ptr(yk),
+                                              _ptr(yv), _stream(stream, dev)),
+               "kvarn_dequantize_records")
     return yk, yv
 
 

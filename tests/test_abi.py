@@ -268,6 +268,13 @@ def test_host_validation_append_and_decode():
     assert dec(batch=0) == K.OK
     assert L.kvarn_dequantize_pages(a16, -1, a16, a16, None) == K.ERR_INVALID_ARG
     assert L.kvarn_dequantize_pages(None, 3, a16, a16, None) == K.ERR_INVALID_ARG
+    k8 = kv.config_from_string("k8v4_g128", 8, 2)
+    assert L.kvarn_dequantize_records(ctypes.byref(k8), a16, -1, a16, a16, None) == K.ERR_INVALID_ARG
+    assert L.kvarn_dequantize_records(ctypes.byref(k8), None, 3, a16, a16, None) == K.ERR_INVALID_ARG
+    assert L.kvarn_dequantize_records(ctypes.byref(k8), a16, 0, a16, a16, None) == K.OK
+    k8.k_bits = 6
+    assert L.kvarn_dequantize_records(ctypes.byref(k8), a16, 3, a16, a16, None) == K.ERR_UNSUPPORTED
+    assert L.kvarn_dequantize_records(None, a16, 3, a16, a16, None) == K.ERR_INVALID_ARG
 
 
 def test_binding_refuses_cpu_tensors():

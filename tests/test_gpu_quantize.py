@@ -179,6 +179,33 @@ def test_dequantize_pages_matches_oracle():
             assert np.all(np.abs(got - ref) <= 1e-6 * np.abs(ref) + 1e-30)
 
 
+@pytest.mark.parametrize("variant", ["f32", "m16", "pc", "g64", "v4", "k8"])
+def test_dequantize_records_of_every_format_match_oracle(variant):
+    # kvarn_dequantize_records against the oracle's dequantization of the same
+    # records, for each record format; the tolerance is relative to the
+    # largest value of the element's row and column (the two terms of yhat can
+    # cancel)
+    import quantized_decode_attention_blocks_b300 as kv
+    w = synth.scaled(synth.WORKLOADS["llama3_8b_layer"], batch=1, seq=256, hkv=2, hq=8)
+    k, v = synth.kv(w, device=DEV)
+    fmt = {} if variant == "f32" else {variant: True}
+    cfg = config(w.hq, w.hkv, **fmt)
+    pool, _, _, _ = prefill(cfg, k, v, torch.tensor([256], dtype=torch.int32),
+                            torch.tensor([[0, 1]], dtype=torch.int32), 2)
+    nb = cfg.page_bytes
+    yk, yv = kv.kvarn_dequantize_records(cfg, pool.reshape(-1, nb))
+    torch.cuda.synchronize()
+    recs = host(pool).reshape(-1, nb)
+    okw = {} if variant == "f32" else {("meta16" if variant == "m16" else variant): True}
+    for i in range(recs.shape[0]):
+        for is_v, y in ((False, yk), (True, yv)):
+            ref = kvref.dequant_part(recs[i], is_v, **okw)
+            got = host(y[i]).astype(np.float64)
+            a = np.abs(ref)
+            scale = np.maximum(a.max(axis=1, keepdims=True), a.max(axis=0, keepdims=True))
+            assert np.all(np.abs(got - ref) <= 2e-6 * (a + scale)), (variant, is_v, i)
+
+
 def test_bad_page_sets_status_and_skips():
     w = synth.scaled(synth.WORKLOADS["llama3_8b_layer"], batch=2, seq=256, hkv=2, hq=8)
     k, v = synth.kv(w, device=DEV)
