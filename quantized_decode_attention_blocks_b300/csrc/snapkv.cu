@@ -383,22 +383,39 @@ __global__ void __launch_bounds__(kSelThreads) snapkv_select_kernel(SnapSelectAr
   for (int i = tid; i < a.W; i += kSelThreads) out[keep + i] = npre + i;
 }
 
-// Kept tokens into the compact cache: grid (capacity, hkv, batch), 32 threads
-// (lanes 0-15 copy the K row, 16-31 the V row); a position outside
-// [0, max_seq) (the -1 padding) gives zeros.
-__global__ void __launch_bounds__(32)
+// Kept tokens into the compact cache: grid (ceil(capacity / 32), hkv, batch),
+// 8 warps of 4 kept tokens each; lanes 0-15 copy a K row, 16-31 its V row
+// (16 bytes each), the four rows' loads issued before their stores.  A
+// position outside [0, max_seq) (the -1 padding) gives zeros.
+constexpr int kGatherRows = 4;     // kept tokens per warp
+constexpr int kGatherWarps = 8;
+__global__ void __launch_bounds__(32 * kGatherWarps)
     snapkv_gather_kernel(const __half* __restrict__ k, const __half* __restrict__ v, int64_t sb,
                          int64_t st, int64_t sh, int max_seq, int hkv,
                          const int32_t* __restrict__ idx, int capacity, __half* __restrict__ ko,
                          __half* __restrict__ vo) {
-  const int j = blockIdx.x, h = blockIdx.y, b = blockIdx.z, lane = threadIdx.x;
-  int t = idx[((int64_t)b * hkv + h) * capacity + j];
-  if (t >= max_seq) t = -1;
+  const int h = blockIdx.y, b = blockIdx.z, lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int j0 = (blockIdx.x * kGatherWarps + warp) * kGatherRows;
+  const int32_t* irow = idx + ((int64_t)b * hkv + h) * capacity;
+  int tl = -1;
+  if (lane < kGatherRows && j0 + lane < capacity) tl = irow[j0 + lane];
   const int part = lane >> 4, c = lane & 15;
-  const __half* src = (part ? v : k) + (int64_t)b * sb + (int64_t)h * sh + (int64_t)t * st;
-  __half* dst = (part ? vo : ko) + (((int64_t)b * capacity + j) * hkv + h) * kD;
-  reinterpret_cast<uint4*>(dst)[c] =
-      t >= 0 ? __ldg(reinterpret_cast<const uint4*>(src) + c) : make_uint4(0u, 0u, 0u, 0u);
+  const __half* base = (part ? v : k) + (int64_t)b * sb + (int64_t)h * sh;
+  uint4 row[kGatherRows];
+#pragma unroll
+  for (int i = 0; i < kGatherRows; ++i) {
+    const int t = __shfl_sync(0xffffffffu, tl, i);
+    row[i] = make_uint4(0u, 0u, 0u, 0u);
+    if (t >= 0 && t < max_seq)
+      row[i] = __ldg(reinterpret_cast<const uint4*>(base + (int64_t)t * st) + c);
+  }
+#pragma unroll
+  for (int i = 0; i < kGatherRows; ++i) {
+    const int j = j0 + i;
+    if (j >= capacity) break;
+    __half* dst = (part ? vo : ko) + (((int64_t)b * capacity + j) * hkv + h) * kD;
+    reinterpret_cast<uint4*>(dst)[c] = row[i];
+  }
 }
 
 }  // namespace
@@ -423,9 +440,10 @@ cudaError_t launch_snapkv_gather(const __half* k, const __half* v, int64_t sb, i
                                  int64_t sh, int batch, int max_seq, int hkv,
                                  const int32_t* indices, int capacity, __half* k_out,
                                  __half* v_out, cudaStream_t s) {
-  dim3 grid(capacity, hkv, batch);
-  snapkv_gather_kernel<<<grid, 32, 0, s>>>(k, v, sb, st, sh, max_seq, hkv, indices, capacity,
-                                           k_out, v_out);
+  constexpr int per_cta = kGatherWarps * kGatherRows;
+  dim3 grid((capacity + per_cta - 1) / per_cta, hkv, batch);
+  snapkv_gather_kernel<<<grid, 32 * kGatherWarps, 0, s>>>(k, v, sb, st, sh, max_seq, hkv, indices,
+                                                          capacity, k_out, v_out);
   return cudaGetLastError();
 }
 
