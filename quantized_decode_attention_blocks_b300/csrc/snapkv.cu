@@ -349,15 +349,35 @@ __global__ void __launch_bounds__(kSelThreads) snapkv_select_kernel(SnapSelectAr
       if ((key & mask) == prefix) atomicAdd(&hist[(key >> shift) & 255u], 1);
     }
     __syncthreads();
-    if (tid == 0) {
-      int cum = 0, rem = sh_remaining;
-      for (int bin = 255; bin >= 0; --bin) {
-        if (cum + hist[bin] >= rem) {
-          sh_prefix = prefix | ((uint32_t)bin << shift);
-          sh_remaining = rem - cum;
-          break;
+    if (tid < 32) {
+      // the first bin, from the top, at which the running count reaches
+      // `rem`: lane l holds bins 255 - 8l .. 248 - 8l, a warp scan gives the
+      // count above each lane's bins, and the one lane whose bins cross `rem`
+      // walks them
+      const int rem = sh_remaining;
+      int c[8], sum = 0;
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        c[i] = hist[255 - 8 * tid - i];
+        sum += c[i];
+      }
+      int incl = sum;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, incl, o);
+        if (tid >= o) incl += y;
+      }
+      int cum = incl - sum;
+      if (cum < rem && rem <= incl) {
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          if (cum + c[i] >= rem) {
+            sh_prefix = prefix | ((uint32_t)(255 - 8 * tid - i) << shift);
+            sh_remaining = rem - cum;
+            break;
+          }
+          cum += c[i];
         }
-        cum += hist[bin];
       }
     }
     mask |= 255u << shift;
