@@ -76,18 +76,27 @@ def source_hash(name):
         return hashlib.sha256(f.read()).hexdigest()[:16]
 
 
-def ncu_traffic(kernel_key, src_name):
-    """Per-launch DRAM bytes recorded from an ncu capture (profiles/traffic.json),
-    or None when absent or when the kernel source changed since the capture."""
+def ncu_traffic(kernel_key, src_name, workload, alg_bytes):
+    """Per-launch DRAM bytes from an ncu capture (profiles/traffic.json) for a
+    launch of `alg_bytes` algorithmic bytes: the capture of this workload, or
+    else one of another workload scaled by the ratio of algorithmic bytes (the
+    kernels' traffic grows with the tiles or pages processed).  None when no
+    capture matches the kernel's current source.  Returns (bytes, source)."""
     p = os.path.join(ROOT, "profiles", "traffic.json")
     if not os.path.exists(p):
-        return None
+        return None, None
     with open(p) as f:
         d = json.load(f)
-    e = d.get(kernel_key)
-    if not e or e.get("source_sha256_16") != source_hash(src_name):
-        return None
-    return e.get("dram_bytes_per_launch")
+    cands = [e for k, e in d.items() if k == kernel_key or k.startswith(kernel_key + "@")]
+    cands = [e for e in cands if e.get("source_sha256_16") == source_hash(src_name)
+             and e.get("algorithmic_bytes_per_launch")]
+    if not cands:
+        return None, None
+    e = next((e for e in cands if e.get("workload") == workload), cands[0])
+    ratio = alg_bytes / e["algorithmic_bytes_per_launch"]
+    src = f"ncu capture of {e['workload']}" + ("" if e.get("workload") == workload
+                                                else f", scaled by {ratio:.4g}")
+    return e["dram_bytes_per_launch"] * ratio, src
 
 
 class ClockSampler:
@@ -785,8 +794,8 @@ def main():
     f8_gbs = bd8 / (ms["decode_fp8"] * 1e-3) / 1e9
     dom = "quantize" if ms["quantize"] >= ms["decode"] else "decode"
     dom_gbs = q_gbs if dom == "quantize" else d_gbs
-    traffic_q = ncu_traffic("quantize_tc_kernel", "quantize_tc.cu")
-    traffic_d = ncu_traffic("decode_mma_kernel", "decode_mma.cu")
+    traffic_q, tsrc_q = ncu_traffic("quantize_tc_kernel", "quantize_tc.cu", w.name, bq // L)
+    traffic_d, tsrc_d = ncu_traffic("decode_mma_kernel", "decode_mma.cu", w.name, bd // L)
     per_launch = {k: ms[k] / L * 1e3 for k in ms}
     line = {
         "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world,
@@ -834,10 +843,11 @@ def main():
                      "peak_kind": f"{peak_kind} hbm_gbs (burst copy)", "unit": "GB/s",
                      "frac": dom_gbs / peak,
                      "traffic": traffic_q if dom == "quantize" else traffic_d,
+                     "traffic_source": tsrc_q if dom == "quantize" else tsrc_d,
                      "algorithmic_bytes_per_launch": (bq if dom == "quantize" else bd) // L,
                      "us_per_launch": per_launch[dom]},
         "roofline_decode": {"bound": "hbm", "achieved": d_gbs, "peak": peak, "unit": "GB/s",
-                            "frac": d_gbs / peak, "traffic": traffic_d,
+                            "frac": d_gbs / peak, "traffic": traffic_d, "traffic_source": tsrc_d,
                             "algorithmic_bytes_per_launch": bd // L,
                             "us_per_launch": per_launch["decode"]},
         "e2e": e2e,
