@@ -73,7 +73,6 @@
  *   [10752,14848) V codes (the same permutation)
  *   [14848,16896) V {s'_0, z'_0, s'_1, z'_1} fp32 per token
  *   [16896,17408) V column scale c_d fp32
- * kvarn_chunk_attention does not take this format (KVARN_ERR_UNSUPPORTED).
  * Format variant "k4v4_g128" (config v_bits = 4; fp32 metadata, 19456 bytes,
  * 152 B per token-head): the same stages with 4-bit RTN on V as on K.  The K
  * part is as above; the V part holds 4-bit codes in their own permutation:
@@ -83,7 +82,6 @@
  *   [9728, 17920) V codes, 2048 32-bit words
  *   [17920,18944) V {s', z'} fp32 per token
  *   [18944,19456) V column scale c_d fp32
- * kvarn_chunk_attention does not take this format either.
  * Format variant "k8v4_g128" (config k_bits = 8, v_bits = 4; fp32 metadata,
  * 27648 bytes, 216 B per token-head): 8-bit RTN on K (2^8 - 1 steps), V as in
  * "k4v4_g128".  K codes are one byte per channel, token-major rows of 128
@@ -95,7 +93,6 @@
  *   [17920,26112) V codes (the 4-bit permutation above)
  *   [26112,27136) V {s', z'} fp32 per token
  *   [27136,27648) V column scale c_d fp32
- * kvarn_chunk_attention does not take this format either.
  * Pool = [num_pages][num_kv_heads][kvarn_page_bytes(cfg)].  The newest len mod 128
  * tokens of a sequence stay fp16 in a caller-owned tail buffer
  * [B][num_kv_heads][128 slots][128] per K and V.
@@ -324,8 +321,10 @@ int kvarn_decode_attention_noalloc(const kvarn_config_t *cfg, const void *q, con
  * No workspace.  A page id outside the pool is reported
  * (KVARN_STATUS_BAD_PAGE) and the query tiles that would read it give zeros.
  * The work is one CTA per 128 query rows (128 / (Hq/Hkv) tokens of one KV
- * head's query group) and KV head; it uses 229 KB of shared memory and 256
- * TMEM columns, so one CTA runs per SM. */
+ * head's query group) and KV head; it uses up to 227 KB of shared memory and
+ * 256 TMEM columns, so one CTA runs per SM.  Every record format is taken;
+ * the 15360-byte (and smaller) records stream two pages ahead, the larger
+ * ones ("k4v2_g64", "k4v4_g128", "k8v4_g128") one page at a time. */
 int kvarn_chunk_attention(const kvarn_config_t *cfg, const void *q, int chunk_max,
                           const int32_t *start, const int32_t *chunk_lens, int batch,
                           int max_seq, const void *pool, int64_t num_pages,

@@ -339,9 +339,6 @@ int kvarn_chunk_attention(const kvarn_config_t* cfg, const void* q, int chunk_ma
       !aligned16(out))
     return KVARN_ERR_INVALID_ARG;
   if (!(softmax_scale > 0.f) || softmax_scale != softmax_scale) return KVARN_ERR_INVALID_ARG;
-  // the g64, k4v4 and k8v4 records (17408, 19456, 27648 bytes) do not fit the
-  // kernel's two record buffers next to its six operand tiles
-  if (cfg->group == 64 || cfg->v_bits == 4) return KVARN_ERR_UNSUPPORTED;
   const int g = cfg->num_q_heads / cfg->num_kv_heads;
   const int tq = chunk_rows_per_tile(g);
   const int64_t ntq = ((int64_t)chunk_max + tq - 1) / tq;

@@ -59,6 +59,9 @@ constexpr uint64_t kCWaitNs = 2000000000ull;
 constexpr uint32_t kCIdesc = (1u << 4) | ((128u >> 3) << 17) | ((128u >> 4) << 24);
 constexpr float kLazy = 8.f;                          // log2 units
 
+// RB: the record format's bytes; NRAW: page records in flight (two where
+// they fit beside the six operands, else one).
+template <int RB, int NRAW>
 struct __align__(1024) CSmem {
   uint8_t qh[kOp];        // A of S: q~ high part   [row][channel]
   uint8_t ql[kOp];        //         q~ low part
@@ -66,18 +69,31 @@ struct __align__(1024) CSmem {
   uint8_t kl[kOp];        //         yhatK low
   uint8_t vh[kOp];        // B of PV: yhatV high    [channel][token]
   uint8_t vl[kOp];        //          yhatV low
-  uint8_t raw[2][kRec];   // page records in flight
-  uint64_t raw_full[2];
+  uint8_t raw[NRAW][RB];  // page records in flight
+  uint64_t raw_full[NRAW];
   uint64_t sdone[2];      // S of a block ready, per S buffer
-  uint64_t rawfree[2];    // a page buffer's keys and values are dequantized
+  uint64_t rawfree[NRAW]; // a page buffer's keys and values are dequantized
   uint64_t qready, kready, vready, pready, pvdone, drain;
   uint32_t tmem_base;
   int abort;
 };
-static_assert(offsetof(CSmem, raw) % 16 == 0 && offsetof(CSmem, raw_full) % 8 == 0,
-              "bulk copies and barriers need these alignments");
-constexpr int kCSmemBytes = (int)sizeof(CSmem) + 1024;
-static_assert(kCSmemBytes <= 232448, "shared memory of one CTA");
+// records in flight for a format: two for the 15360-byte (and smaller)
+// records, one for the records of groups of 64, 4-bit values or 8-bit keys
+template <int FMT>
+constexpr int raw_buffers() {
+  return (int)sizeof(CSmem<RecFmt<FMT>::bytes, 2>) + 1024 <= 232448 ? 2 : 1;
+}
+template <int FMT>
+constexpr int chunk_smem_bytes() {
+  return (int)sizeof(CSmem<RecFmt<FMT>::bytes, raw_buffers<FMT>()>) + 1024;
+}
+static_assert(raw_buffers<kFmtF32>() == 2 && raw_buffers<kFmtM16>() == 2 &&
+                  raw_buffers<kFmtPC>() == 2 && raw_buffers<kFmtG64>() == 1 &&
+                  raw_buffers<kFmtV4>() == 1 && raw_buffers<kFmtK8>() == 1,
+              "the large records are single-buffered");
+static_assert(chunk_smem_bytes<kFmtF32>() <= 232448 && chunk_smem_bytes<kFmtK8>() <= 232448 &&
+                  chunk_smem_bytes<kFmtG64>() <= 232448 && chunk_smem_bytes<kFmtV4>() <= 232448,
+              "shared memory of one CTA");
 
 // Byte offset of the 16-byte chunk holding elements 8c .. 8c + 7 (c < 16) of
 // row r of a 128 x 128 fp16 operand in the 128-byte swizzled K-major layout:
@@ -173,13 +189,20 @@ __device__ __forceinline__ void dequant_k(const uint8_t* rk, uint8_t* kh, uint8_
   constexpr int kStep = 4 * kDeqWarps;
 #pragma unroll 1
   for (int p0 = dw; p0 < kT / 2; p0 += kStep) {
-    uint32_t w[4];
+    uint32_t w[4], w2[4];   // the 8 codes: nibbles of w, or bytes of w, w2 (8-bit keys)
     float2 sz[4];
 #pragma unroll
     for (int u = 0; u < 4; ++u) {
       const int t = 2 * min(p0 + kDeqWarps * u, kT / 2 - 1) + t0;
-      w[u] = *reinterpret_cast<const uint32_t*>(rk + kOffKCodes + 64 * t + 4 * cc);
-      sz[u] = F::get_sz(rk + F::ksz, t);
+      if constexpr (F::k8) {   // channels 8 cc .. of token t: 8 bytes at k8_byte(8 cc, t)
+        const uint2 b8 = *reinterpret_cast<const uint2*>(rk + k8_byte(8 * cc, t));
+        w[u] = b8.x;
+        w2[u] = b8.y;
+      } else {
+        w[u] = *reinterpret_cast<const uint32_t*>(rk + kOffKCodes + 64 * t + 4 * cc);
+        w2[u] = 0u;
+      }
+      sz[u] = F::get_sz_g(rk + F::ksz, t, F::g64 ? cc >> 3 : 0);   // the chunk's group
     }
 #pragma unroll
     for (int u = 0; u < 4; ++u) {
@@ -188,8 +211,14 @@ __device__ __forceinline__ void dequant_k(const uint8_t* rk, uint8_t* kh, uint8_
       float y[8];
 #pragma unroll
       for (int k = 0; k < 8; k += 2) {
-        const float2 q2 = make_float2(code_f((w[u] >> (4 * k)) & 15u),
-                                      code_f((w[u] >> (4 * k + 4)) & 15u));
+        float2 q2;
+        if constexpr (F::k8) {
+          const uint32_t wk = k < 4 ? w[u] : w2[u];
+          q2 = make_float2(code_f((wk >> (8 * (k & 3))) & 255u),
+                           code_f((wk >> (8 * (k & 3) + 8)) & 255u));
+        } else {
+          q2 = make_float2(code_f((w[u] >> (4 * k)) & 15u), code_f((w[u] >> (4 * k + 4)) & 15u));
+        }
         float2 v;
         if constexpr (F::pc)   // r_t (cs_d q + cz_d)
           v = __fmul2_rn(make_float2(sz[u].x, sz[u].x),
@@ -221,8 +250,48 @@ __device__ __forceinline__ void dequant_v(const uint8_t* rv, uint8_t* vh, uint8_
   const uint8_t* vsz = rv + (F::vsz - F::kpart);
   const uint32_t* words = reinterpret_cast<const uint32_t*>(rv);   // V codes open the V part
   const uint8_t* vc = rv + (F::vc - F::kpart);
+  if constexpr (F::v4) {
+    // 4-bit codes: words p = 0..3 of (channel, j), nibble 4s + 2(k & 1) + f
+    // of word p holding token 16k + 8f + 2j + s for k = 2p, 2p + 1
+#pragma unroll 1
+    for (int p = 0; p < 4; ++p) {
+      float2 sz[2][2][2];
+#pragma unroll
+      for (int kk = 0; kk < 2; ++kk)
+#pragma unroll
+        for (int f = 0; f < 2; ++f)
+#pragma unroll
+          for (int s = 0; s < 2; ++s)
+            sz[kk][f][s] = F::get_sz(vsz, 16 * (2 * p + kk) + 8 * f + 2 * j2 + s);
+#pragma unroll 2
+      for (int k2 = dw; k2 < 16; k2 += NW) {
+        const int m = k2 >> 1, e = k2 & 1;
+        const int c = 16 * m + 8 * e + r;
+        const uint32_t w = words[v4_word(c, j2, p)];
+        const float cd = F::get_bd(vc, c).x;
+#pragma unroll
+        for (int kk = 0; kk < 2; ++kk)
+#pragma unroll
+          for (int f = 0; f < 2; ++f) {
+            const int i0 = 2 * kk + f;   // nibble of s = 0; s = 1 is nibble i0 + 4
+            const float q0 = code_f((w >> (4 * i0)) & 15u), q1 = code_f((w >> (4 * i0 + 16)) & 15u);
+            const float y0 = cd * fmaf(sz[kk][f][0].x, q0, sz[kk][f][0].y);
+            const float y1 = cd * fmaf(sz[kk][f][1].x, q1, sz[kk][f][1].y);
+            const int u = 2 * (2 * p + kk) + f;   // tokens 8u .. 8u + 7
+            const uint32_t off =
+                (uint32_t)((u >> 3) * kOpBox + c * 128 + (((u & 7) ^ (c & 7)) << 4) + 4 * j2);
+            uint32_t hi, lo;
+            split2(y0, y1, hi, lo);
+            *reinterpret_cast<uint32_t*>(vh + off) = hi;
+            *reinterpret_cast<uint32_t*>(vl + off) = lo;
+          }
+      }
+    }
+  } else {
 #pragma unroll 1
   for (int hb = 0; hb < 2; ++hb) {
+    // the tokens' {s', z'} (of group 0 for groups of 64: group 1 is read
+    // per channel below)
     float2 sz[4][2][2];
 #pragma unroll
     for (int kk = 0; kk < 4; ++kk)
@@ -230,7 +299,7 @@ __device__ __forceinline__ void dequant_v(const uint8_t* rv, uint8_t* vh, uint8_
       for (int f = 0; f < 2; ++f)
 #pragma unroll
         for (int s = 0; s < 2; ++s)
-          sz[kk][f][s] = F::get_sz(vsz, 16 * (4 * hb + kk) + 8 * f + 2 * j2 + s);
+          sz[kk][f][s] = F::get_sz_g(vsz, 16 * (4 * hb + kk) + 8 * f + 2 * j2 + s, 0);
 #pragma unroll 2
     for (int k2 = dw; k2 < 16; k2 += NW) {
       const int m = k2 >> 1, e = k2 & 1;
@@ -243,13 +312,19 @@ __device__ __forceinline__ void dequant_v(const uint8_t* rv, uint8_t* vh, uint8_
         for (int f = 0; f < 2; ++f) {
           const int i0 = 2 * kk + f;   // crumb of s = 0; s = 1 is crumb i0 + 8
           const float q0 = code_f((w >> (2 * i0)) & 3u), q1 = code_f((w >> (2 * i0 + 16)) & 3u);
+          float2 sz0 = sz[kk][f][0], sz1 = sz[kk][f][1];
+          if (F::g64 && c >= 64) {   // the second channel group's {s', z'}
+            const int tok = 16 * (4 * hb + kk) + 8 * f + 2 * j2;
+            sz0 = F::get_sz_g(vsz, tok, 1);
+            sz1 = F::get_sz_g(vsz, tok + 1, 1);
+          }
           float y0, y1;
           if constexpr (F::pc) {   // r_t (cs_d q + cz_d)
-            y0 = sz[kk][f][0].x * fmaf(bd.x, q0, bd.y);
-            y1 = sz[kk][f][1].x * fmaf(bd.x, q1, bd.y);
+            y0 = sz0.x * fmaf(bd.x, q0, bd.y);
+            y1 = sz1.x * fmaf(bd.x, q1, bd.y);
           } else {                 // c_d (s'_t q + z'_t)
-            y0 = bd.x * fmaf(sz[kk][f][0].x, q0, sz[kk][f][0].y);
-            y1 = bd.x * fmaf(sz[kk][f][1].x, q1, sz[kk][f][1].y);
+            y0 = bd.x * fmaf(sz0.x, q0, sz0.y);
+            y1 = bd.x * fmaf(sz1.x, q1, sz1.y);
           }
           const int u = 2 * (4 * hb + kk) + f;   // tokens 8u .. 8u + 7; these are 2 j2, 2 j2 + 1
           const uint32_t off =
@@ -261,6 +336,7 @@ __device__ __forceinline__ void dequant_v(const uint8_t* rv, uint8_t* vh, uint8_
         }
     }
   }
+  }   // 2-bit codes
 }
 
 // FMT: the record format (RecFmt).
@@ -268,9 +344,14 @@ template <int FMT>
 __global__ void __launch_bounds__(kCThreads, 1)
     chunk_attention_kernel(const ChunkArgs a) {
   using F = RecFmt<FMT>;
+  constexpr int NRAW = raw_buffers<FMT>();
+  using Smem = CSmem<F::bytes, NRAW>;
   extern __shared__ uint8_t smem_raw[];
-  CSmem& S = *reinterpret_cast<CSmem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
-                                       ~static_cast<uintptr_t>(1023));
+  Smem& S = *reinterpret_cast<Smem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                     ~static_cast<uintptr_t>(1023));
+  // record buffer of block j and the parity of its use
+  auto rb = [](int j) { return NRAW == 2 ? j & 1 : 0; };
+  auto rph = [](int j) { return (uint32_t)((NRAW == 2 ? j >> 1 : j) & 1); };
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int b = blockIdx.z, kvh = blockIdx.y;
   const int tile = a.ntq - 1 - (int)blockIdx.x;   // longest tiles first
@@ -313,10 +394,10 @@ __global__ void __launch_bounds__(kCThreads, 1)
   }
 
   if (tid == 0) {
-    mbar_init(&S.raw_full[0], 1);
-    mbar_init(&S.raw_full[1], 1);
-    mbar_init(&S.rawfree[0], kSoftWarps + kDeqWarps);
-    mbar_init(&S.rawfree[1], kSoftWarps + kDeqWarps);
+    for (int x = 0; x < NRAW; ++x) {
+      mbar_init(&S.raw_full[x], 1);
+      mbar_init(&S.rawfree[x], kSoftWarps + kDeqWarps);
+    }
     mbar_init(&S.qready, kSoftWarps);
     mbar_init(&S.kready, kDeqWarps);
     mbar_init(&S.vready, kSoftWarps);
@@ -419,8 +500,8 @@ __global__ void __launch_bounds__(kCThreads, 1)
       }
       // ---- this block's values into V^ ----
       if (page) {
-        wait(&S.raw_full[j & 1], (j >> 1) & 1);
-        dequant_v<kSoftWarps, FMT>(S.raw[j & 1] + F::kpart, S.vh, S.vl, warp, lane);
+        wait(&S.raw_full[rb(j)], rph(j));
+        dequant_v<kSoftWarps, FMT>(S.raw[rb(j)] + F::kpart, S.vh, S.vl, warp, lane);
       } else {
         // the fp16 tail, rotated: column t = tid of V^ [channel][token]
         const int t = tid;
@@ -448,7 +529,7 @@ __global__ void __launch_bounds__(kCThreads, 1)
       __syncwarp();
       if (lane == 0) {
         mbar_arrive(&S.vready);
-        if (page) mbar_arrive(&S.rawfree[j & 1]);
+        if (page) mbar_arrive(&S.rawfree[rb(j)]);
       }
       // ---- pass 2: P = 2^(S - m) as fp16 pairs into TMEM ----
       const bool any = m_ref != -INFINITY;
@@ -517,26 +598,26 @@ __global__ void __launch_bounds__(kCThreads, 1)
     // count0 | count1 << 16 so that no array sits in local memory
     uint32_t issued = 0, seen = 0;
     auto issue = [&](int j) {
-      uint64_t* bar = &S.raw_full[j & 1];
+      uint64_t* bar = &S.raw_full[rb(j)];
       mbar_arrive_expect_tx(bar, F::bytes);
-      bulk_g2s(S.raw[j & 1], rec_of(j), F::bytes, bar);
-      issued += 1u << (16 * (j & 1));
+      bulk_g2s(S.raw[rb(j)], rec_of(j), F::bytes, bar);
+      issued += 1u << (16 * rb(j));
     };
     const int npages = min(nblk, nfull);
     if (dt == 0) {
       if (0 < npages) issue(0);
-      if (1 < npages) issue(1);
+      if (NRAW == 2 && 1 < npages) issue(1);
     }
     const __half* tkb = a.tail_k + ((int64_t)b * a.hkv + kvh) * kT * kD;
     for (int j = 0; j < nblk; ++j) {
       const bool page = j < nfull;
       if (page) {
-        wait(&S.raw_full[j & 1], (j >> 1) & 1);
-        if (dt == 0 && !*reinterpret_cast<volatile int*>(&S.abort)) seen += 1u << (16 * (j & 1));
+        wait(&S.raw_full[rb(j)], rph(j));
+        if (dt == 0 && !*reinterpret_cast<volatile int*>(&S.abort)) seen += 1u << (16 * rb(j));
       }
       if (j > 0) wait(&S.sdone[(j - 1) & 1], ((j - 1) >> 1) & 1);   // S of block j-1 read K^
       if (page) {
-        dequant_k<FMT>(S.raw[j & 1], S.kh, S.kl, dw, lane);
+        dequant_k<FMT>(S.raw[rb(j)], S.kh, S.kl, dw, lane);
       } else {
         // the fp16 tail, rotated into the pages' space: yhat = H x / sqrt(128)
 #pragma unroll 1
@@ -559,19 +640,21 @@ __global__ void __launch_bounds__(kCThreads, 1)
       __syncwarp();
       if (lane == 0) {
         mbar_arrive(&S.kready);
-        if (page) mbar_arrive(&S.rawfree[j & 1]);
+        if (page) mbar_arrive(&S.rawfree[rb(j)]);
       }
-      // the buffer of block j - 1 is free once its values are dequantized
-      // too: load block j + 1 into it
-      if (dt == 0 && j >= 1 && j + 1 < npages && !*reinterpret_cast<volatile int*>(&S.abort)) {
-        wait(&S.rawfree[(j - 1) & 1], ((j - 1) >> 1) & 1);
+      // the buffer of block j + 1 - NRAW is free once its values are
+      // dequantized too: load block j + 1 into it (with one buffer, that is
+      // block j itself)
+      if (dt == 0 && j + 1 >= NRAW && j + 1 < npages &&
+          !*reinterpret_cast<volatile int*>(&S.abort)) {
+        wait(&S.rawfree[rb(j + 1 - NRAW)], rph(j + 1 - NRAW));
         issue(j + 1);
       }
     }
     if (dt == 0) {
       // copies still in flight (a wait gave up) land before the CTA leaves
 #pragma unroll
-      for (int s2 = 0; s2 < 2; ++s2)
+      for (int s2 = 0; s2 < NRAW; ++s2)
         for (int k = (int)((seen >> (16 * s2)) & 0xFFFF); k < (int)((issued >> (16 * s2)) & 0xFFFF);
              ++k)
           mbar_wait_bounded(&S.raw_full[s2], (uint32_t)(k & 1), kCWaitNs);
@@ -649,11 +732,12 @@ __global__ void __launch_bounds__(kCThreads, 1)
 template <int FMT>
 cudaError_t launch_chunk(const ChunkArgs& args, cudaStream_t s) {
   static std::atomic<uint64_t> smem_set{0};
-  cudaError_t e = ensure_dynamic_smem(chunk_attention_kernel<FMT>, kCSmemBytes, smem_set);
+  constexpr int smem = chunk_smem_bytes<FMT>();
+  cudaError_t e = ensure_dynamic_smem(chunk_attention_kernel<FMT>, smem, smem_set);
   if (e != cudaSuccess) return e;
   if (args.ntq <= 0 || args.batch <= 0) return cudaSuccess;
   dim3 grid(args.ntq, args.hkv, args.batch);
-  chunk_attention_kernel<FMT><<<grid, kCThreads, kCSmemBytes, s>>>(args);
+  chunk_attention_kernel<FMT><<<grid, kCThreads, smem, s>>>(args);
   return cudaGetLastError();
 }
 
@@ -664,6 +748,9 @@ int chunk_rows_per_tile(int g) { return 128 / g; }
 cudaError_t launch_chunk_attention(const ChunkArgs& args, cudaStream_t s) {
   if (args.fmt == kFmtM16) return launch_chunk<kFmtM16>(args, s);
   if (args.fmt == kFmtPC) return launch_chunk<kFmtPC>(args, s);
+  if (args.fmt == kFmtG64) return launch_chunk<kFmtG64>(args, s);
+  if (args.fmt == kFmtV4) return launch_chunk<kFmtV4>(args, s);
+  if (args.fmt == kFmtK8) return launch_chunk<kFmtK8>(args, s);
   return launch_chunk<kFmtF32>(args, s);
 }
 

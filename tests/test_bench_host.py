@@ -52,16 +52,37 @@ def _record(tree, src_text, entry):
 def test_traffic_only_while_the_source_matches_the_capture(tree):
     src = "__global__ void k() {}\n"
     h = hashlib.sha256(src.encode()).hexdigest()[:16]
-    _record(tree, src, {"k": {"dram_bytes_per_launch": 1234.0, "source_sha256_16": h}})
-    assert bench.ncu_traffic("k", "k.cu") == 1234.0
+    _record(tree, src, {"k": {"dram_bytes_per_launch": 1234.0, "source_sha256_16": h,
+                              "workload": "w1", "algorithmic_bytes_per_launch": 1000}})
+    assert bench.ncu_traffic("k", "k.cu", "w1", 1000) == (1234.0, "ncu capture of w1")
     # any edit to the source since the capture: the figure no longer applies
     (tree / "quantized_decode_attention_blocks_b300" / "csrc" / "k.cu").write_text(src + " ")
-    assert bench.ncu_traffic("k", "k.cu") is None
-    assert bench.ncu_traffic("other", "k.cu") is None
+    assert bench.ncu_traffic("k", "k.cu", "w1", 1000) == (None, None)
+    assert bench.ncu_traffic("other", "k.cu", "w1", 1000) == (None, None)
+
+
+def test_traffic_of_the_own_workload_else_scaled(tree):
+    # the capture of the bench's workload is taken as it is; another
+    # workload's is scaled by the ratio of algorithmic bytes per launch
+    src = "__global__ void k() {}\n"
+    h = hashlib.sha256(src.encode()).hexdigest()[:16]
+    _record(tree, src, {
+        "k": {"dram_bytes_per_launch": 950.0, "source_sha256_16": h, "workload": "small",
+              "algorithmic_bytes_per_launch": 1000},
+        "k@big": {"dram_bytes_per_launch": 3900.0, "source_sha256_16": h, "workload": "big",
+                  "algorithmic_bytes_per_launch": 4000}})
+    assert bench.ncu_traffic("k", "k.cu", "big", 4000) == (3900.0, "ncu capture of big")
+    assert bench.ncu_traffic("k", "k.cu", "small", 1000) == (950.0, "ncu capture of small")
+    b, src_note = bench.ncu_traffic("k", "k.cu", "third", 2000)
+    assert b in (1900.0, 1950.0) and "scaled by" in src_note
+    # a capture without its algorithmic bytes cannot be scaled: not used
+    _record(tree, src, {"k": {"dram_bytes_per_launch": 950.0, "source_sha256_16": h,
+                              "workload": "small"}})
+    assert bench.ncu_traffic("k", "k.cu", "small", 1000) == (None, None)
 
 
 def test_traffic_absent_without_a_record(tree):
-    assert bench.ncu_traffic("k", "k.cu") is None
+    assert bench.ncu_traffic("k", "k.cu", "w1", 1000) == (None, None)
 
 
 def test_peak_is_the_measured_copy_bandwidth_else_the_fallback(tree):

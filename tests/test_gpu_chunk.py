@@ -22,7 +22,7 @@ pytestmark = pytest.mark.gpu
 
 
 def _case(starts, chunk_lens, M, hq, hkv, seed, perm=True, table=None, num_pages=None,
-          m16=False, pc=False):
+          m16=False, pc=False, g64=False, v4=False, k8=False):
     starts = np.asarray(starts, dtype=np.int64)
     cls = np.asarray(chunk_lens, dtype=np.int64)
     n = starts + cls
@@ -30,7 +30,7 @@ def _case(starts, chunk_lens, M, hq, hkv, seed, perm=True, table=None, num_pages
     S = max(int(n.max()), 1)
     w = synth.scaled(synth.WORKLOADS["llama3_8b_layer"], batch=B, seq=S, hkv=hkv, hq=hq)
     k, v = synth.kv(w, layer=seed, device=DEV)
-    cfg = config(hq, hkv, m16=m16, pc=pc)
+    cfg = config(hq, hkv, m16=m16, pc=pc, g64=g64, v4=v4, k8=k8)
     mb = (S + 127) // 128
     if table is None:
         g = torch.Generator().manual_seed(seed)
@@ -48,7 +48,8 @@ def _case(starts, chunk_lens, M, hq, hkv, seed, perm=True, table=None, num_pages
                              table.to(DEV), tk, tv, out, status=status)
     torch.cuda.synchronize()
     return dict(cfg=cfg, q=q, out=out, status=status, st=st, pool=pool, tk=tk, tv=tv,
-                table=table, starts=starts, cls=cls, hq=hq, hkv=hkv, m16=m16, pc=pc)
+                table=table, starts=starts, cls=cls, hq=hq, hkv=hkv, m16=m16, pc=pc,
+                fmt=dict(g64=g64, v4=v4, k8=k8))
 
 
 def _check(c):
@@ -58,7 +59,7 @@ def _check(c):
     assert np.isfinite(got).all()
     ref = kvref.chunk_attention(host(c["q"]), c["starts"], c["cls"], host(c["pool"]),
                                 host(c["table"]), host(c["tk"]), host(c["tv"]), c["hq"],
-                                c["hkv"], meta16=c["m16"], pc=c["pc"])
+                                c["hkv"], meta16=c["m16"], pc=c["pc"], **c["fmt"])
     for b, cl in enumerate(c["cls"]):
         assert not got[b, int(cl):].any(), "rows past the chunk must be zeros"
     return parity.compare_attention(got, ref)
@@ -156,16 +157,16 @@ def test_chunk_prefill_workload_sampled():
 
 
 @pytest.mark.parametrize("fmt", ["g64", "v4", "k8"])
-def test_g64_v4_and_k8_formats_are_refused(fmt):
-    # the g64, k4v4 and k8v4 records do not fit the kernel's record buffers:
-    # the call says so before any launch
-    cfg = config(8, 2, g64=fmt == "g64", v4=fmt == "v4", k8=fmt == "k8")
-    q = torch.zeros((1, 4, 8, 128), dtype=torch.float16, device=DEV)
-    pool = kv.alloc_pool(cfg, 2, DEV)
-    tk, tv = kv.alloc_tails(cfg, 1, DEV)
-    one = torch.tensor([4], dtype=torch.int32, device=DEV)
-    with pytest.raises(kv.KvarnError) as e:
-        kv.kvarn_chunk_attention(cfg, q, one * 0, one, 4, pool,
-                                 torch.zeros((1, 1), dtype=torch.int32, device=DEV), tk, tv,
-                                 torch.empty_like(q))
-    assert e.value.code == kv.kvarn.ERR_UNSUPPORTED
+@pytest.mark.parametrize("hq,hkv", [(8, 2), (12, 2)])
+def test_large_record_formats(fmt, hq, hkv):
+    # formats "k4v2_g64", "k4v4_g128" and "k8v4_g128": one page record in
+    # flight (two do not fit beside the six operands); ragged chunks over
+    # pages and tail
+    _check(_case([250, 100, 0, 300], [150, 60, 60, 1], 150, hq, hkv, seed=10,
+                 **{fmt: True}))
+
+
+@pytest.mark.parametrize("fmt", ["g64", "k8"])
+def test_large_record_formats_long_prefix(fmt):
+    # 16 blocks through the single record buffer
+    _check(_case([2000, 1500], [200, 64], 200, 16, 4, seed=11, **{fmt: True}))
