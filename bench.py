@@ -439,6 +439,18 @@ def measured_tensor_peak():
 
 
 def measure_chunk(args, dev, stream):
+    """Chunked-prefill attention on its own workload for the default format,
+    and the same for the formats whose records stream one page at a time."""
+    res = measure_chunk_fmt(args, dev, stream, "k4v2_g128")
+    res["format_variants"] = {}
+    for fmt in ("k4v2_g64", "k4v4_g128", "k8v4_g128"):
+        r = measure_chunk_fmt(args, dev, stream, fmt)
+        res["format_variants"][fmt] = {"us_per_launch": r["us_per_launch"],
+                                       "frac": r["roofline"]["frac"]}
+    return res
+
+
+def measure_chunk_fmt(args, dev, stream, fmt):
     """Chunked-prefill attention (kvarn_chunk_attention) on its own workload:
     16 sequences of the Llama-3-8B-like layer (8 KV heads, 32 query heads),
     3584 cached tokens each plus a 512-token chunk, so the cache holds 4096
@@ -449,7 +461,7 @@ def measure_chunk(args, dev, stream):
     w = synth.WORKLOADS["llama3_8b_layer"]
     B, M, start = 16, 512, 3584
     S = start + M
-    cfg = kv.config_from_string("k4v2_g128", w.hq, w.hkv)
+    cfg = kv.config_from_string(fmt, w.hq, w.hkv)
     mb = S // T
     reps = []
     for r in range(2):   # two replicas, rotated, so no launch finds its q in L2
