@@ -412,6 +412,17 @@ int kvarn_dequantize_pages(const void *records, int64_t n, float *yk, float *yv,
 int kvarn_dequantize_records(const kvarn_config_t *cfg, const void *records, int64_t n,
                              float *yk, float *yv, kvarn_stream_t stream);
 
+/* Diagnosis of the bounded waits: every wait of the library's kernels on an
+ * mbarrier (a bulk copy landing, an MMA completing, a peer warp's arrival)
+ * gives up after a time limit, reports KVARN_STATUS_TIMEOUT and lets the
+ * kernel end, instead of hanging the GPU.  This call runs that same wait in
+ * a one-warp kernel on a barrier of its own that receives its one arrival
+ * first (arrive = 1: no timeout) or never (arrive = 0: the wait runs out
+ * after limit_us microseconds and KVARN_STATUS_TIMEOUT is OR-ed into
+ * *status).  status: device int32, not null; limit_us in [1, 1000000].
+ * Returns KVARN_ERR_INVALID_ARG for bad arguments; one launch on `stream`. */
+int kvarn_wait_check(int32_t *status, int arrive, uint32_t limit_us, kvarn_stream_t stream);
+
 /* ---- The FP16 paged cache the quantized one is measured against ----
  * The KVarN page (blog.edumints.com) states its capacity and throughput gains
  * relative to an FP16 KV cache; these calls are that baseline on the same

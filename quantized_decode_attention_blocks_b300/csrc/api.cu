@@ -657,6 +657,15 @@ int kvarn_dequantize_pages(const void* records, int64_t n, float* yk, float* yv,
              : KVARN_ERR_LAUNCH;
 }
 
+int kvarn_wait_check(int32_t* status, int arrive, uint32_t limit_us, kvarn_stream_t stream) {
+  if (!status || (arrive != 0 && arrive != 1) || limit_us == 0 || limit_us > 1000000u)
+    return KVARN_ERR_INVALID_ARG;
+  return launch_wait_check(status, (uint64_t)limit_us * 1000u, arrive, (cudaStream_t)stream) ==
+                 cudaSuccess
+             ? KVARN_OK
+             : KVARN_ERR_LAUNCH;
+}
+
 int kvarn_dequantize_records(const kvarn_config_t* cfg, const void* records, int64_t n,
                              float* yk, float* yv, kvarn_stream_t stream) {
   const int rc = kvarn_config_validate(cfg);

@@ -422,6 +422,8 @@ struct ChunkArgs {
 int chunk_rows_per_tile(int g);
 cudaError_t launch_chunk_attention(const ChunkArgs& a, cudaStream_t s);
 
+cudaError_t launch_wait_check(int32_t* status, uint64_t limit_ns, int arrive, cudaStream_t s);
+
 __device__ __forceinline__ void report(int32_t* status, int bits) {
   if (status) atomicOr(status, bits);
 }

@@ -90,6 +90,7 @@ SIGNATURES = {
                                    _I, _P, _P, ctypes.c_float, _P, _P, _P]),
     "kvarn_dequantize_pages": (_I, [_P, _L, _P, _P, _P]),
     "kvarn_dequantize_records": (_I, [_P, _P, _L, _P, _P, _P]),
+    "kvarn_wait_check": (_I, [_P, _I, ctypes.c_uint32, _P]),
     "kvarn_fp16_write_blocks": (_I, [_P, _P, _L, _L, _L, _I, _I, _P, _I, _P, _I, _P, _L, _P,
                                      _P]),
     "kvarn_fp16_decode_workspace_bytes": (ctypes.c_size_t, [_I, _I, _I, _I]),

@@ -275,6 +275,11 @@ def test_host_validation_append_and_decode():
     k8.k_bits = 6
     assert L.kvarn_dequantize_records(ctypes.byref(k8), a16, 3, a16, a16, None) == K.ERR_UNSUPPORTED
     assert L.kvarn_dequantize_records(None, a16, 3, a16, a16, None) == K.ERR_INVALID_ARG
+    # the bounded-wait check: arguments refused before any launch
+    assert L.kvarn_wait_check(None, 0, 1000, None) == K.ERR_INVALID_ARG
+    assert L.kvarn_wait_check(a16, 2, 1000, None) == K.ERR_INVALID_ARG
+    assert L.kvarn_wait_check(a16, 0, 0, None) == K.ERR_INVALID_ARG
+    assert L.kvarn_wait_check(a16, 0, 1000001, None) == K.ERR_INVALID_ARG
 
 
 def test_binding_refuses_cpu_tensors():
