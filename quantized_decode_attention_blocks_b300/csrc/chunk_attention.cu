@@ -70,9 +70,10 @@ struct __align__(1024) CSmem {
   uint8_t vh[kOp];        // B of PV: yhatV high    [channel][token]
   uint8_t vl[kOp];        //          yhatV low
   uint8_t raw[NRAW][RB];  // page records in flight
-  uint64_t raw_full[NRAW];
+  uint64_t raw_full[2];   // per buffer; with one buffer: [0] its K part, [1] its V part
   uint64_t sdone[2];      // S of a block ready, per S buffer
-  uint64_t rawfree[NRAW]; // a page buffer's keys and values are dequantized
+  uint64_t rawfree[2];    // a buffer's keys and values (one buffer: its keys; its values)
+                          // are dequantized
   uint64_t qready, kready, vready, pready, pvdone, drain;
   uint32_t tmem_base;
   int abort;
@@ -394,9 +395,11 @@ __global__ void __launch_bounds__(kCThreads, 1)
   }
 
   if (tid == 0) {
-    for (int x = 0; x < NRAW; ++x) {
+    for (int x = 0; x < 2; ++x) {
       mbar_init(&S.raw_full[x], 1);
-      mbar_init(&S.rawfree[x], kSoftWarps + kDeqWarps);
+      // two buffers: both kinds of warps free a record; one buffer: the
+      // dequant warps free its K part, the softmax warps its V part
+      mbar_init(&S.rawfree[x], NRAW == 2 ? kSoftWarps + kDeqWarps : x == 0 ? kDeqWarps : kSoftWarps);
     }
     mbar_init(&S.qready, kSoftWarps);
     mbar_init(&S.kready, kDeqWarps);
@@ -425,10 +428,22 @@ __global__ void __launch_bounds__(kCThreads, 1)
     }
   };
   const int rem = n - nfull * kT;
+  auto rec_of = [&](int j) {
+    return a.pool + ((int64_t)trow[j] * a.hkv + kvh) * (int64_t)F::bytes;
+  };
+  const int npages = min(nblk, nfull);
+  // one record buffer: its K and V parts stream separately, the dequant
+  // warps loading the next K part and the softmax warps the next V part as
+  // soon as their own part of the current record is dequantized
+  auto issue_v = [&](int j) {
+    mbar_arrive_expect_tx(&S.raw_full[1], F::vpart);
+    bulk_g2s(S.raw[0] + F::kpart, rec_of(j) + F::kpart, F::vpart, &S.raw_full[1]);
+  };
 
   if (warp < kSoftWarps) {
     // ================= softmax warps: row r = TMEM lane r =================
     const int r = tid, i = i0 + r / g, hh = r % g;
+    uint32_t vissued = 0, vseen = 0;   // one buffer: V parts loaded / seen by tid 0
     const bool valid = r < tq * g && i < cl;
     const int Pr = valid ? start + i : -1;         // last key position of the row
     {
@@ -500,7 +515,12 @@ __global__ void __launch_bounds__(kCThreads, 1)
       }
       // ---- this block's values into V^ ----
       if (page) {
-        wait(&S.raw_full[rb(j)], rph(j));
+        if constexpr (NRAW == 2) {
+          wait(&S.raw_full[rb(j)], rph(j));
+        } else {
+          wait(&S.raw_full[1], j & 1);
+          if (tid == 0 && !*reinterpret_cast<volatile int*>(&S.abort)) ++vseen;
+        }
         dequant_v<kSoftWarps, FMT>(S.raw[rb(j)] + F::kpart, S.vh, S.vl, warp, lane);
       } else {
         // the fp16 tail, rotated: column t = tid of V^ [channel][token]
@@ -529,7 +549,13 @@ __global__ void __launch_bounds__(kCThreads, 1)
       __syncwarp();
       if (lane == 0) {
         mbar_arrive(&S.vready);
-        if (page) mbar_arrive(&S.rawfree[rb(j)]);
+        if (page) mbar_arrive(&S.rawfree[NRAW == 2 ? rb(j) : 1]);
+      }
+      if (NRAW == 1 && page && tid == 0 && j + 1 < npages &&
+          !*reinterpret_cast<volatile int*>(&S.abort)) {
+        wait(&S.rawfree[1], j & 1);   // every softmax warp read this V part
+        issue_v(j + 1);
+        ++vissued;
       }
       // ---- pass 2: P = 2^(S - m) as fp16 pairs into TMEM ----
       const bool any = m_ref != -INFINITY;
@@ -588,25 +614,30 @@ __global__ void __launch_bounds__(kCThreads, 1)
         for (int c = 0; c < 16; ++c) dst[c] = make_uint4(0u, 0u, 0u, 0u);
       }
     }
+    if (NRAW == 1 && tid == 0) {
+      // V parts still in flight (a wait gave up) land before the CTA leaves:
+      // the first was issued by the dequant warps, the others here
+      const uint32_t total = (npages > 0 ? 1u : 0u) + vissued;
+      for (uint32_t k = vseen; k < total; ++k) mbar_wait_bounded(&S.raw_full[1], k & 1, kCWaitNs);
+    }
   } else if (warp < kSoftWarps + kDeqWarps) {
     // ================= dequant warps: page records in, keys into K^ =================
     const int dt = tid - kDeq0, dw = dt >> 5;
-    auto rec_of = [&](int j) {
-      return a.pool + ((int64_t)trow[j] * a.hkv + kvh) * (int64_t)F::bytes;
-    };
     // loads issued and seen complete per buffer (thread dt == 0), as
     // count0 | count1 << 16 so that no array sits in local memory
     uint32_t issued = 0, seen = 0;
+    // the record of block j (two buffers), or its K part (one buffer)
     auto issue = [&](int j) {
+      constexpr uint32_t bytes = NRAW == 2 ? F::bytes : F::kpart;
       uint64_t* bar = &S.raw_full[rb(j)];
-      mbar_arrive_expect_tx(bar, F::bytes);
-      bulk_g2s(S.raw[rb(j)], rec_of(j), F::bytes, bar);
+      mbar_arrive_expect_tx(bar, bytes);
+      bulk_g2s(S.raw[rb(j)], rec_of(j), bytes, bar);
       issued += 1u << (16 * rb(j));
     };
-    const int npages = min(nblk, nfull);
     if (dt == 0) {
       if (0 < npages) issue(0);
       if (NRAW == 2 && 1 < npages) issue(1);
+      if (NRAW == 1 && 0 < npages) issue_v(0);
     }
     const __half* tkb = a.tail_k + ((int64_t)b * a.hkv + kvh) * kT * kD;
     for (int j = 0; j < nblk; ++j) {
@@ -642,9 +673,10 @@ __global__ void __launch_bounds__(kCThreads, 1)
         mbar_arrive(&S.kready);
         if (page) mbar_arrive(&S.rawfree[rb(j)]);
       }
-      // the buffer of block j + 1 - NRAW is free once its values are
-      // dequantized too: load block j + 1 into it (with one buffer, that is
-      // block j itself)
+      // two buffers: the buffer of block j - 1 is free once its values are
+      // dequantized too, load block j + 1 into it; one buffer: the K part
+      // of block j is free once every dequant warp read it, load the next K
+      // part into it
       if (dt == 0 && j + 1 >= NRAW && j + 1 < npages &&
           !*reinterpret_cast<volatile int*>(&S.abort)) {
         wait(&S.rawfree[rb(j + 1 - NRAW)], rph(j + 1 - NRAW));
