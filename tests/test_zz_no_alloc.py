@@ -46,7 +46,7 @@ def test_noalloc_rejects_requests_beyond_its_scratch():
     assert kv.lib().kvarn_decode_attention_noalloc(*args) == K.ERR_WORKSPACE
 
 
-def _noalloc_twice(lens, max_seq, hkv, hq, seed):
+def _noalloc_twice(lens, max_seq, hkv, hq, seed, **fmt):
     """Prefills a seeded cache, then calls the no-alloc decode twice through
     the C ABI and checks both outputs against the float64 oracle (fed the
     GPU's own pool) and against kvarn_decode_attention."""
@@ -58,7 +58,7 @@ def _noalloc_twice(lens, max_seq, hkv, hq, seed):
     lens = torch.tensor(lens, dtype=torch.int32)
     w = synth.scaled(synth.WORKLOADS["long_context"], batch=B, seq=max_seq, hkv=hkv, hq=hq)
     k, v = synth.kv(w, layer=seed, device=DEV)
-    cfg = config(w.hq, w.hkv)
+    cfg = config(w.hq, w.hkv, **fmt)
     mb = (max_seq + 127) // 128
     g = torch.Generator().manual_seed(seed)
     table = torch.randperm(B * mb, generator=g).to(torch.int32).reshape(B, mb)
@@ -71,8 +71,9 @@ def _noalloc_twice(lens, max_seq, hkv, hq, seed):
     ws = kv.alloc_decode_workspace(cfg, B, max_seq, DEV)
     kv.kvarn_decode_attention(cfg, q, pool, tdev, ldev, max_seq, tk, tv, ref, ws, status=st)
     torch.cuda.synchronize()
+    okw = {("meta16" if k == "m16" else k): v for k, v in fmt.items()}
     want_oracle = kvref.decode_attention(host(q), host(pool), host(table), host(lens), host(tk),
-                                         host(tv), w.hq, w.hkv)
+                                         host(tv), w.hq, w.hkv, **okw)
     want_cuda = ref.float().cpu().numpy().astype(np.float64)
 
     L = kv.lib()
@@ -109,3 +110,11 @@ def test_noalloc_matches_oracle_twice_with_cluster_merge():
     # KV head), merged inside a thread-block cluster (no tickets are read)
     plan = _noalloc_twice([1536] * 12 + [1400, 1290, 700, 5], 1536, hkv=8, hq=32, seed=11)
     assert 2 <= plan[1] <= 4
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("variant", ["m16", "pc", "g64", "v4", "k8"])
+def test_noalloc_format_variants(variant):
+    # every record format through the built-in scratch (ticket merge)
+    plan = _noalloc_twice([9000, 4000, 130], 9000, hkv=2, hq=8, seed=13, **{variant: True})
+    assert plan[1] > 4
