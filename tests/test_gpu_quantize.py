@@ -110,8 +110,11 @@ def test_strided_input():
     _check_prefill(w, lens, table, 4, k=k, v=v)
 
 
-def test_special_tiles():
-    # zero tile, constant tile, a huge random-sign outlier channel, fp16 extremes
+@pytest.mark.parametrize("variant", ["f32", "m16", "pc", "g64", "v4", "k8"])
+def test_special_tiles(variant):
+    # zero tile, constant tile, a huge random-sign outlier channel, fp16
+    # extremes, in every record format
+    fmt = {} if variant == "f32" else {variant: True}
     w = synth.scaled(synth.WORKLOADS["llama3_8b_layer"], batch=1, seq=512, hkv=1, hq=1)
     k, v = synth.kv(w, device=DEV)
     k[0, :128] = 0
@@ -123,7 +126,7 @@ def test_special_tiles():
     v[0, 384:512] = torch.where(v[0, 384:512] > 0, 65504.0, -65504.0).half()
     lens = torch.tensor([512], dtype=torch.int32)
     table = torch.tensor([[3, 2, 1, 0]], dtype=torch.int32)
-    _check_prefill(w, lens, table, 4, k=k, v=v)
+    _check_prefill(w, lens, table, 4, k=k, v=v, **fmt)
 
 
 def test_ill_conditioned_constant_offset_tile():
