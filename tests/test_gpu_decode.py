@@ -158,7 +158,8 @@ def test_pc_format_many_splits():
     _run(w, lens, table, 157, pc=True)
 
 
-def test_no_bias_common_to_all_channels():
+@pytest.mark.parametrize("variant", ["f32", "m16", "pc", "g64", "v4", "k8"])
+def test_no_bias_common_to_all_channels(variant):
     # Every (sequence, head) of a Llama-3-8B layer at 1024 tokens: whole pages,
     # no fp16 tail.  An error shared by all 128 rotated channels lands on
     # output channel 0 alone (the first row of H is constant), where it would
@@ -168,7 +169,7 @@ def test_no_bias_common_to_all_channels():
     w = synth.scaled(synth.WORKLOADS["llama3_8b_layer"], batch=16, seq=1024, hkv=8, hq=32)
     lens = torch.full((16,), 1024, dtype=torch.int32)
     table = torch.arange(16 * 8, dtype=torch.int32).reshape(16, 8)
-    res, _ = _run(w, lens, table, 16 * 8)
+    res, _ = _run(w, lens, table, 16 * 8, **({} if variant == "f32" else {variant: True}))
     e0 = res["got"][:, :, 0] - res["ref"][:, :, 0]
     assert abs(e0.mean()) <= 1.5e-4, f"channel-0 mean signed error {e0.mean():.2e}"
     rest = res["got"][:, :, 1:] - res["ref"][:, :, 1:]

@@ -94,7 +94,8 @@ def test_rms_variant(iters):
     parity.compare_attention(host(out), ref)
 
 
-def test_strided_input():
+@pytest.mark.parametrize("variant", ["f32", "g64", "k8"])
+def test_strided_input(variant):
     # K/V as views into a [B][S][2*Hkv][128] buffer (every other head), and a
     # batch stride larger than S*Hkv*128
     w = synth.scaled(synth.WORKLOADS["llama3_8b_layer"], batch=2, seq=256, hkv=4, hq=8)
@@ -107,7 +108,7 @@ def test_strided_input():
     v = big_v[:, :256, ::2]
     lens = torch.tensor([256, 200], dtype=torch.int32)
     table = torch.tensor([[0, 1], [2, 3]], dtype=torch.int32)
-    _check_prefill(w, lens, table, 4, k=k, v=v)
+    _check_prefill(w, lens, table, 4, k=k, v=v, **({} if variant == "f32" else {variant: True}))
 
 
 @pytest.mark.parametrize("variant", ["f32", "m16", "pc", "g64", "v4", "k8"])
