@@ -9,8 +9,9 @@
 // keys and values are stored rotated, y = H x, and the orthonormal rotation
 // keeps scores, so with q~ = H q
 //     s_it = q~_i . yhatK_t,   o_i = H (sum_t p_it yhatV_t) / sum_t p_it,
-// yhat_td = c_d (s'_t q_td + z'_t) for a page token; a token of the fp16 tail
-// is rotated on the way in (yhat = H x).
+// yhat_td = c_d (s'_t q_td + z'_t) for a page token (r_t (cs_d q_td + cz_d)
+// for per-channel groups; the {s', z'} of the channel's group for groups of
+// 64); a token of the fp16 tail is rotated on the way in (yhat = H x).
 //
 // CTA = one tile of 128 query rows of one (sequence, KV head): row r holds
 // query token i0 + r / g of head r mod g of the KV head's group.  It walks the
@@ -28,8 +29,11 @@
 // Roles: warps 0-3 build Q~ once and run the softmax (thread r = TMEM lane r =
 // row r); between the two passes over a block's scores they also dequantize
 // its values into the V^ (hi, lo) operands.  Warps 4-6 bring each page record
-// in with one bulk copy (two buffers, one block ahead) and dequantize its keys
-// into the K^ (hi, lo) operands (the fp16 tail is rotated on the way in).  One
+// in with one bulk copy (two buffers, one block ahead; for the records of more
+// than 15360 bytes one buffer, whose K part they load and whose V part the
+// softmax warps load, each as soon as its part of the record before is read)
+// and dequantize its keys into the K^ (hi, lo) operands (the fp16 tail is
+// rotated on the way in).  One
 // thread of warp 7 issues the MMAs, polling for whichever of the next S (one
 // block ahead, two S buffers in TMEM) or the next PV has its inputs ready, so
 // the tensor cores work on the next block's scores while the softmax warps
