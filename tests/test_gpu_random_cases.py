@@ -1,0 +1,95 @@
+"""Seeded random decode and chunk cases over the record formats, GQA groups,
+ragged lengths and permuted block tables, each against the float64 oracle
+(fed the GPU's own pool).  "KV Cache Nasil Calisir?" and "Paged Attention
+(vLLM)" (yapayzekasozluk.tr); the KVarN page (blog.edumints.com)."""
+import numpy as np
+import pytest
+import torch
+
+import quantized_decode_attention_blocks_b300 as kv
+from oracle import kvref
+from tests import parity
+from tests.gpu_helpers import DEV, config, decode, host, prefill
+from workloads import synth
+
+pytestmark = pytest.mark.gpu
+
+VARIANTS = ["f32", "m16", "pc", "g64", "v4", "k8"]
+
+
+def _case(seed):
+    rng = np.random.default_rng(seed)
+    variant = VARIANTS[seed % len(VARIANTS)]
+    hkv = int(rng.choice([1, 2, 4]))
+    g = int(rng.integers(1, 9))
+    B = int(rng.integers(1, 7))
+    max_seq = int(rng.integers(1, 3000))
+    lens = rng.integers(0, max_seq + 1, size=B)
+    lens[int(rng.integers(B))] = max_seq
+    return variant, hkv, g, B, max_seq, lens
+
+
+@pytest.mark.parametrize("seed", range(24))
+def test_random_decode_case(seed):
+    variant, hkv, g, B, max_seq, lens = _case(seed)
+    fmt = {} if variant == "f32" else {variant: True}
+    w = synth.scaled(synth.WORKLOADS["llama3_8b_layer"], batch=B, seq=max_seq, hkv=hkv,
+                     hq=g * hkv, seed=300 + seed)
+    k, v = synth.kv(w, device=DEV)
+    cfg = config(w.hq, w.hkv, **fmt)
+    mb = max((max_seq + 127) // 128, 1)
+    perm = torch.randperm(B * mb, generator=torch.Generator().manual_seed(seed))
+    table = perm.to(torch.int32).reshape(B, mb)
+    lt = torch.tensor(lens, dtype=torch.int32)
+    pool, tk, tv, st = prefill(cfg, k, v, lt, table, B * mb, max_seq=max_seq)
+    q = synth.queries(w).to(DEV)
+    out, st2, _ = decode(cfg, q, pool, table, lt, tk, tv, max_seq=max_seq)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0 and int(st2.item()) == 0
+    okw = {("meta16" if variant == "m16" else variant): True} if fmt else {}
+    ref = kvref.decode_attention(host(q), host(pool), host(table), host(lt), host(tk), host(tv),
+                                 w.hq, w.hkv, **okw)
+    parity.compare_attention(host(out).astype(np.float64), ref)
+
+
+@pytest.mark.parametrize("seed", range(12))
+def test_random_chunk_case(seed):
+    # a chunk of new tokens per sequence after a random cached prefix, the
+    # chunk's tokens appended to the cache before the call
+    rng = np.random.default_rng(1000 + seed)
+    variant = VARIANTS[seed % len(VARIANTS)]
+    fmt = {} if variant == "f32" else {variant: True}
+    hkv = int(rng.choice([1, 2]))
+    g = int(rng.integers(1, 9))
+    B = int(rng.integers(1, 4))
+    M = int(rng.integers(1, 200))
+    starts = rng.integers(0, 1500, size=B)
+    cls = rng.integers(0, M + 1, size=B)
+    cls[int(rng.integers(B))] = M
+    n = starts + cls
+    S = max(int(n.max()), 1)
+    w = synth.scaled(synth.WORKLOADS["llama3_8b_layer"], batch=B, seq=S, hkv=hkv, hq=g * hkv,
+                     seed=700 + seed)
+    k, v = synth.kv(w, device=DEV)
+    cfg = config(w.hq, w.hkv, **fmt)
+    mb = (S + 127) // 128
+    table = torch.randperm(B * mb, generator=torch.Generator().manual_seed(seed)).to(
+        torch.int32).reshape(B, mb)
+    lens = torch.tensor(n, dtype=torch.int32)
+    pool, tk, tv, st = prefill(cfg, k, v, lens, table, B * mb, max_seq=S)
+    gq = torch.Generator(device=DEV).manual_seed(2000 + seed)
+    q = torch.randn((B, M, w.hq, 128), generator=gq, device=DEV).to(torch.float16)
+    out = torch.full_like(q, float("nan"))
+    status = torch.zeros(1, dtype=torch.int32, device=DEV)
+    kv.kvarn_chunk_attention(cfg, q, torch.tensor(starts, dtype=torch.int32, device=DEV),
+                             torch.tensor(cls, dtype=torch.int32, device=DEV), S, pool,
+                             table.to(DEV), tk, tv, out, status=status)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0 and int(status.item()) == 0
+    okw = {("meta16" if variant == "m16" else variant): True} if fmt else {}
+    ref = kvref.chunk_attention(host(q), starts, cls, host(pool), host(table), host(tk),
+                                host(tv), w.hq, w.hkv, **okw)
+    got = host(out).astype(np.float64)
+    for b, c in enumerate(cls):
+        assert not got[b, int(c):].any()
+    parity.compare_attention(got, ref)
