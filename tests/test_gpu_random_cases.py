@@ -93,3 +93,44 @@ def test_random_chunk_case(seed):
     for b, c in enumerate(cls):
         assert not got[b, int(c):].any()
     parity.compare_attention(got, ref)
+
+
+@pytest.mark.parametrize("seed", range(6))
+def test_random_append_case(seed):
+    # sequences of random lengths each take 1..150 decode-time appends; the
+    # pages they fill equal the prefill of the final lengths bit for bit, the
+    # tails hold the leftover tokens
+    rng = np.random.default_rng(3000 + seed)
+    variant = VARIANTS[seed % len(VARIANTS)]
+    fmt = {} if variant == "f32" else {variant: True}
+    B, hkv = int(rng.integers(1, 5)), int(rng.choice([1, 2]))
+    steps = int(rng.integers(1, 151))
+    start = rng.integers(0, 400, size=B)
+    S = int(start.max()) + steps
+    w = synth.scaled(synth.WORKLOADS["llama3_8b_layer"], batch=B, seq=S, hkv=hkv, hq=2 * hkv,
+                     seed=900 + seed)
+    k, v = synth.kv(w, device=DEV)
+    cfg = config(w.hq, w.hkv, **fmt)
+    mb = (S + 127) // 128
+    table = torch.randperm(B * mb, generator=torch.Generator().manual_seed(seed)).to(
+        torch.int32).reshape(B, mb)
+    pool, tk, tv, st = prefill(cfg, k, v, torch.tensor(start, dtype=torch.int32), table,
+                               B * mb, max_seq=S)
+    tdev = table.to(DEV)
+    for s in range(steps):
+        pos = torch.tensor(start + s, dtype=torch.int32, device=DEV)
+        kn = torch.stack([k[b, int(start[b]) + s] for b in range(B)]).contiguous()
+        vn = torch.stack([v[b, int(start[b]) + s] for b in range(B)]).contiguous()
+        kv.kvarn_append_token(cfg, kn, vn, pos, tdev, pool, tk, tv, st)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    final = torch.tensor(start + steps, dtype=torch.int32)
+    ref_pool, ref_tk, ref_tv, st2 = prefill(cfg, k, v, final, table, B * mb, max_seq=S)
+    torch.cuda.synchronize()
+    for b in range(B):
+        nfull = int(final[b]) // 128
+        pages = table[b, :nfull].long()
+        assert torch.equal(pool[pages], ref_pool[pages]), (variant, b)
+        rem = int(final[b]) % 128
+        assert torch.equal(tk[b, :, :rem], ref_tk[b, :, :rem])
+        assert torch.equal(tv[b, :, :rem], ref_tv[b, :, :rem])
