@@ -134,3 +134,19 @@ def test_random_append_case(seed):
         rem = int(final[b]) % 128
         assert torch.equal(tk[b, :, :rem], ref_tk[b, :, :rem])
         assert torch.equal(tv[b, :, :rem], ref_tv[b, :, :rem])
+
+
+@pytest.mark.parametrize("seed", range(6))
+def test_random_snapkv_case(seed):
+    # SnapKV-style selection over random prompt lengths, windows, capacities
+    # and pooling kernels, through the same checks as its own tests
+    from tests.test_gpu_snapkv import _check, _run
+    rng = np.random.default_rng(5000 + seed)
+    hkv = int(rng.choice([1, 2, 8]))
+    g = int(rng.choice([1, 2, 4, 8]))
+    W = int(rng.choice([8, 16, 32, 64]))
+    B = int(rng.integers(1, 5))
+    lens = [int(x) for x in rng.integers(W, 3000, size=B)]
+    capacity = int(rng.integers(W + 1, 1200))
+    kern = int(rng.choice([1, 3, 5, 7]))
+    _check(_run(lens, W, capacity, g * hkv, hkv, seed=40 + seed, kern=kern))
