@@ -99,6 +99,20 @@ def ncu_traffic(kernel_key, src_name, workload, alg_bytes):
     return e["dram_bytes_per_launch"] * ratio, src
 
 
+def ncu_traffic_exact(kernel_key, src_name):
+    """DRAM bytes of one launch from the ncu capture of a bench-own workload
+    (profiles/traffic.json, no scaling), or None when the kernel source changed
+    since."""
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(p):
+        return None
+    with open(p) as f:
+        e = json.load(f).get(kernel_key)
+    if not e or e.get("source_sha256_16") != source_hash(src_name):
+        return None
+    return e.get("dram_bytes_per_launch")
+
+
 class ClockSampler:
     """Samples nvidia-smi SM clocks and throttle reasons during the timed region."""
 
@@ -505,7 +519,10 @@ def measure_chunk_fmt(args, dev, stream, fmt):
                           "algorithmic FLOPs run on the tensor cores",
             "roofline": {"bound": "tensor", "achieved": tflops, "peak": peak,
                          "peak_kind": f"{kind} bf16_tflops (burst; fp16 runs at the bf16 rate)",
-                         "unit": "TFLOP/s", "frac": tflops / peak, "traffic": None}}
+                         "unit": "TFLOP/s", "frac": tflops / peak,
+                         "traffic": (ncu_traffic_exact("chunk_attention_kernel",
+                                                       "chunk_attention.cu")
+                                     if fmt == "k4v2_g128" else None)}}
 
 
 def measure_variants(args, dev, stream):
@@ -643,6 +660,8 @@ def measure_snapkv(args, dev, stream):
             "roofline": {"bound": "hbm", "kernel": "select (three launches)", "achieved": sel_gbs,
                          "peak": peak, "peak_kind": f"{kind} hbm_gbs (burst copy)",
                          "unit": "GB/s", "frac": sel_gbs / peak, "traffic": None,
+                         "traffic_votes_launch": ncu_traffic_exact("snapkv_scores_kernel",
+                                                                   "snapkv.cu"),
                          "algorithmic_bytes_per_call": sel_bytes,
                          "note": "the two score launches each read the keys, so 2x the "
                                  "algorithmic key bytes move"}}
