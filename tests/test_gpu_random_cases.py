@@ -150,3 +150,25 @@ def test_random_snapkv_case(seed):
     capacity = int(rng.integers(W + 1, 1200))
     kern = int(rng.choice([1, 3, 5, 7]))
     _check(_run(lens, W, capacity, g * hkv, hkv, seed=40 + seed, kern=kern))
+
+
+@pytest.mark.parametrize("seed", range(6))
+def test_random_quantize_case(seed):
+    # prefill of random lengths on permuted pages, random Sinkhorn iteration
+    # count and statistic, every record against the oracle's
+    from tests.test_gpu_quantize import _check_prefill
+    rng = np.random.default_rng(7000 + seed)
+    variant = VARIANTS[(seed + 3) % len(VARIANTS)]
+    fmt = {} if variant == "f32" else {variant: True}
+    B, hkv = int(rng.integers(1, 4)), int(rng.choice([1, 2, 4]))
+    S = int(rng.integers(128, 1400))
+    lens = torch.tensor(rng.integers(0, S + 1, size=B), dtype=torch.int32)
+    lens[int(rng.integers(B))] = S
+    iters = int(rng.integers(0, 5))
+    rms = bool(rng.integers(0, 2))
+    w = synth.scaled(synth.WORKLOADS["llama3_8b_layer"], batch=B, seq=S, hkv=hkv, hq=hkv,
+                     seed=800 + seed)
+    mb = (S + 127) // 128
+    table = torch.randperm(B * mb, generator=torch.Generator().manual_seed(seed)).to(
+        torch.int32).reshape(B, mb)
+    _check_prefill(w, lens, table, B * mb, iters=iters, rms=rms, **fmt)
