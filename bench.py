@@ -667,50 +667,107 @@ def measure_snapkv(args, dev, stream):
                                  "algorithmic key bytes move"}}
 
 
-def measure_e2e(step_units, args, stream):
-    """One step through the Python API from pinned host memory: per layer the
-    H2D copies of K, V, the new token and the query, the three calls, and the
-    D2H copy of the output, all inside the timed region."""
+def make_e2e_step(step_units, stream, copy_streams=2):
+    """The end-to-end step through the Python API from pinned host memory: per
+    layer the H2D copies of K, V, the new token and the query, the three calls,
+    and the D2H copy of the output.  Returns (step, host): step(kernels=True)
+    issues one step; host[i]["out"] receives layer i's output.
+
+    The host link, not the kernels, bounds this step (a layer's fp16 K and V
+    cross it in milliseconds, its kernels take well under one), so K and V
+    cross on `copy_streams` streams of their own into two alternating device
+    buffers: layer i's K and V cross while layer i - 1 computes.  They wait
+    for the quantize two layers back, the last reader of that buffer."""
     host = []
     for u in step_units:
         host.append({"k": u.k.cpu().pin_memory(), "v": u.v.cpu().pin_memory(),
                      "kn": u.kn.cpu().pin_memory(), "vn": u.vn.cpu().pin_memory(),
                      "q": u.q.cpu().pin_memory(),
                      "out": torch.empty(u.out.shape, dtype=torch.float16).pin_memory()})
-    kd = torch.empty_like(step_units[0].k)
-    vd = torch.empty_like(step_units[0].v)
+    bufs = [(torch.empty_like(step_units[0].k), torch.empty_like(step_units[0].v))
+            for _ in range(2)]
+    cstreams = [torch.cuda.Stream(device=stream.device) for _ in range(copy_streams)]
+    for cs in cstreams:
+        cs.wait_stream(stream)
+    done = []   # events after the quantize of the last two layers issued
 
-    def step():
+    def step(kernels=True):
         for u, h in zip(step_units, host):
-            kd.copy_(h["k"], non_blocking=True)
-            vd.copy_(h["v"], non_blocking=True)
+            kd, vd = bufs[0]
+            bufs.reverse()
+            copied = []
+            for j, cs in enumerate(cstreams):
+                if len(done) == 2:   # that buffer's last reader
+                    cs.wait_event(done[0])
+                with torch.cuda.stream(cs):
+                    if j == 0:
+                        kd.copy_(h["k"], non_blocking=True)
+                    if j == len(cstreams) - 1:
+                        vd.copy_(h["v"], non_blocking=True)
+                    ev = torch.cuda.Event()
+                    ev.record(cs)
+                copied.append(ev)
+            # the new token and the query are a few KB: they cross on the
+            # compute stream, behind the previous step's users of u.kn, u.q
             u.kn.copy_(h["kn"], non_blocking=True)
             u.vn.copy_(h["vn"], non_blocking=True)
             u.q.copy_(h["q"], non_blocking=True)
-            u.kv.kvarn_quantize_blocks(u.cfg, kd, vd, u.lens, u.max_seq, u.table, u.pool,
-                                       u.tk, u.tv, u.status)
-            u.append()
-            u.decode()
+            for ev in copied:
+                stream.wait_event(ev)
+            if kernels:
+                u.kv.kvarn_quantize_blocks(u.cfg, kd, vd, u.lens, u.max_seq, u.table, u.pool,
+                                           u.tk, u.tv, u.status)
+            ev = torch.cuda.Event()
+            ev.record(stream)
+            done.append(ev)
+            del done[:-2]
+            if kernels:
+                u.append()
+                u.decode()
             h["out"].copy_(u.out, non_blocking=True)
+
+    step.copy_streams = cstreams
+    return step, host
+
+
+def measure_e2e(step_units, args, stream, copy_streams=2):
+    """Times make_e2e_step's step (everything inside the timed region), and
+    the same step's copies alone, the floor the host link sets."""
+    step, host = make_e2e_step(step_units, stream, copy_streams)
+    cstreams = step.copy_streams
+
+    def timed(kernels):
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for cs in cstreams:   # no copy starts before the timed region does
+            cs.wait_event(e0)
+        for _ in range(n):
+            step(kernels)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        return e0.elapsed_time(e1) / n
 
     for _ in range(max(1, min(args.warmup, 2))):
         step()
     torch.cuda.synchronize()
-    e0 = torch.cuda.Event(enable_timing=True)
-    e1 = torch.cuda.Event(enable_timing=True)
     n = max(1, min(args.steps, 3))
-    e0.record(stream)
-    for _ in range(n):
-        step()
-    e1.record(stream)
-    torch.cuda.synchronize()
-    ms = e0.elapsed_time(e1) / n
+    ms = timed(True)
+    # the same step's copies with no kernel between them: the link's own time
+    # for these bytes, the floor of the end-to-end step
+    ms_copies = timed(False)
     h2d = sum((h["k"].numel() + h["v"].numel() + h["kn"].numel() + h["vn"].numel()
                + h["q"].numel()) * 2 for h in host)
     d2h = sum(h["out"].numel() * 2 for h in host)
     total = sum(u.bytes_quantize + u.bytes_append + u.bytes_decode for u in step_units)
+    link = (h2d + d2h) / (ms_copies * 1e-3) / 1e9
+    achieved = (h2d + d2h) / (ms * 1e-3) / 1e9
     return {"value": total / (ms * 1e-3) / 1e9, "unit": "GB/s", "ms_per_step": ms,
-            "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h)}
+            "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
+            "copy_streams": copy_streams, "overlap": "H2D of layer i with kernels of layer i-1",
+            "roofline": {"bound": "host link", "achieved": achieved, "peak": link, "unit": "GB/s",
+                         "frac": achieved / link, "ms_copies_only": ms_copies,
+                         "peak_kind": "measured here: the same step's copies with no kernels"}}
 
 
 # ------------------------------------------------------ CPU (oracle) arm --

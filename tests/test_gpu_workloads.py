@@ -273,3 +273,37 @@ def test_format_variants_at_the_llama_like_size(variant):
     ref = kvref.decode_attention(host(q[sel]), host(pool[used]), host(tab_c), host(lens1[sel]),
                                  host(tk[sel]), host(tv[sel]), w.hq, w.hkv, route=1, **fmt)
     parity.compare_attention(host(out[sel]), ref)
+
+
+def test_end_to_end_step_matches_the_resident_step():
+    """The bench's end-to-end step, whose K and V cross from pinned host memory
+    on copy streams into two alternating device buffers while the previous
+    layer computes, leaves every layer the output, pages and tails of the same
+    step run on device-resident inputs, bit for bit: no copy overwrites a
+    buffer before its quantize has read it."""
+    import bench
+    w = synth.scaled(synth.WORKLOADS["qwen25_15b"], layers=6, batch=4, seq=1000)
+    units, per_step = bench.build_units(w, DEV, 0)
+    assert per_step == 6
+    for u in units:
+        u.quantize()
+        u.append()
+        u.decode()
+    torch.cuda.synchronize()
+    ref_out = [u.out.clone() for u in units]
+    ref_tails = [(u.tk.clone(), u.tv.clone()) for u in units]
+    ref_pool = units[0].pool.clone()
+    units[0].pool.zero_()
+    for u in units:
+        u.out.zero_()
+        u.tk.zero_()
+        u.tv.zero_()
+    step, hostbufs = bench.make_e2e_step(units, torch.cuda.current_stream())
+    for _ in range(3):   # the third step's copies wait on the second's kernels
+        step()
+    torch.cuda.synchronize()
+    assert all(int(u.status.item()) == 0 for u in units)
+    assert torch.equal(units[0].pool, ref_pool)
+    for u, h, o, (tk, tv) in zip(units, hostbufs, ref_out, ref_tails):
+        assert torch.equal(h["out"].to(DEV).view(torch.int16), o.view(torch.int16))
+        assert torch.equal(u.tk, tk) and torch.equal(u.tv, tv)
