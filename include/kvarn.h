@@ -227,10 +227,15 @@ int kvarn_append_token(const kvarn_config_t *cfg, const void *k_new, const void 
 /* The split-K plan decode uses for (batch, max_seq) on a GPU with `num_sms`
  * streaming multiprocessors (num_sms <= 0: the current device's count).  The
  * pages of each (sequence, KV head) are cut into *nsplit runs of
- * *pages_per_split pages, as many as keep the whole grid resident at once;
- * *workspace_bytes is the decode workspace that plan needs (0: none).  Any
- * output pointer may be NULL.  Host arithmetic only when num_sms > 0 (no CUDA
- * call); KVARN_ERR_LAUNCH when num_sms <= 0 and no device answers. */
+ * *pages_per_split pages, as many as keep the whole grid resident at once.
+ * When the (sequence, KV head) pairs alone outnumber the CTAs one wave holds
+ * (at most 8 query heads per KV head), the grid runs in several waves and
+ * runs are cut to at most 32 pages instead, as far as the partial states fit
+ * KVARN_NOALLOC_SCRATCH_BYTES, so that long sequences of a ragged batch do
+ * not straggle.  *workspace_bytes is the decode workspace that plan needs
+ * (0: none).  Any output pointer may be NULL.  Host arithmetic only when
+ * num_sms > 0 (no CUDA call); KVARN_ERR_LAUNCH when num_sms <= 0 and no
+ * device answers. */
 int kvarn_decode_split_plan(const kvarn_config_t *cfg, int batch, int max_seq, int num_sms,
                             int *pages_per_split, int *nsplit, size_t *workspace_bytes);
 
@@ -256,7 +261,7 @@ size_t kvarn_decode_workspace_bytes(const kvarn_config_t *cfg, int batch, int ma
  * The work is split across CTAs along each sequence's pages (split-K) and the
  * partial softmax states are merged with a log-sum-exp in the same launch:
  * inside a thread-block cluster (distributed shared memory) when a sequence
- * has 2 to 4 splits, through the workspace otherwise.  The launch uses
+ * has 2 to 4 splits in a grid of one wave, through the workspace otherwise.  The launch uses
  * thread-block clusters, so the GPU must be able to co-schedule up to 4 CTAs
  * of the kernel; a launch failure returns KVARN_ERR_LAUNCH. */
 int kvarn_decode_attention(const kvarn_config_t *cfg, const void *q, const void *pool,
@@ -267,11 +272,11 @@ int kvarn_decode_attention(const kvarn_config_t *cfg, const void *q, const void 
                            int32_t *status, kvarn_stream_t stream);
 
 /* Size of the scratch array built into the library for
- * kvarn_decode_attention_noalloc: 4 MiB, held on every GPU that loads it.
- * Every configuration with Hq/Hkv <= 8 fits in it whatever its batch and
- * lengths (the split plan keeps the grid to one wave); larger groups with
- * long sequences may not. */
-#define KVARN_NOALLOC_SCRATCH_BYTES (4u << 20)
+ * kvarn_decode_attention_noalloc: 16 MiB, held on every GPU that loads it.
+ * On a 148-SM B300 every configuration with Hq/Hkv <= 16 fits in it whatever
+ * its batch and lengths (a plan of one wave needs at most 3.8 MB, and a plan
+ * of several waves is sized to it); a GPU with many more SMs may plan more. */
+#define KVARN_NOALLOC_SCRATCH_BYTES (16u << 20)
 
 /* Decode attention without any caller-provided workspace.  The pages have no
  * counterpart to this call; it exists for callers that cannot allocate GPU

@@ -11,6 +11,7 @@ cudaError_t launch_decode_simple(const DecodeArgs& a, cudaStream_t s);
 cudaError_t launch_decode_mma(const DecodeArgs& a, cudaStream_t s);
 bool decode_mma_supported(int g);
 int decode_mma_ctas_per_sm(int g, int fmt);
+int decode_mma_resident_per_sm(int g, int fmt);
 int decode_simple_ctas_per_sm();
 int decode_mma_warps();
 int decode_mma_max_cluster();
@@ -33,9 +34,12 @@ int device_sm_count() {
   return n;
 }
 
-bool decode_uses_cluster(int g, int nsplit) {
-  return decode_mma_supported(g) && nsplit >= 2 && nsplit <= decode_mma_max_cluster();
-}
+// A grid with more (sequence, KV head) groups than resident CTAs runs in
+// several waves, balanced by the hardware scheduler; there the plan cuts long
+// sequences into runs of at most this many pages, so that no long run keeps
+// its SM busy after the rest of the grid is done (mixed serving, 128 lengths
+// in [1K, 32K], one CTA per group: 490 us; runs of 32-48 pages: 418 us).
+constexpr int64_t kWavePages = 32;
 
 DecodePlan decode_plan(int batch, int hq, int hkv, int max_seq, int num_sms, int fmt) {
   DecodePlan p{};
@@ -55,9 +59,27 @@ DecodePlan decode_plan(int batch, int hq, int hkv, int max_seq, int num_sms, int
   const int64_t ns_cap = (units + min_pages - 1) / min_pages;
   if (ns > ns_cap) ns = ns_cap;
   if (ns < 1) ns = 1;
+  // Several waves (tensor-core kernel; the pairs alone outnumber the CTAs
+  // that can be resident, e.g. three per SM for one head tile): runs of at
+  // most kWavePages pages, as many as keep the partial states within the
+  // no-alloc scratch; these splits merge through the workspace, since a
+  // cluster whose CTAs hold runs of very different lengths keeps its slots
+  // busy for the longest.  (48 x 8 pairs of 8K tokens fit one wave of three
+  // per SM: split in two they decode in 88 us instead of 82.)
+  const bool waves =
+      mma && groups > (int64_t)(num_sms > 0 ? num_sms : 1) * decode_mma_resident_per_sm(g, fmt);
+  if (waves) {
+    const int64_t per_split = groups * g * kPartStride * (int64_t)sizeof(float);
+    const int64_t counts = (groups * (int64_t)sizeof(int) + 255) & ~(int64_t)255;
+    const int64_t room = ((int64_t)KVARN_NOALLOC_SCRATCH_BYTES - counts - 256) / per_split;
+    const int64_t want = (units + kWavePages - 1) / kWavePages;
+    ns = want < room ? want : room;
+    if (ns < 1) ns = 1;
+  }
   const int64_t pps = (units + ns - 1) / ns;
   p.pages_per_split = (int)pps;
   p.nsplit = (int)((units + pps - 1) / pps);
+  p.cluster = mma && !waves && p.nsplit >= 2 && p.nsplit <= decode_mma_max_cluster();
   if (p.nsplit > 1) {
     p.part_bytes = (size_t)batch * hq * p.nsplit * kPartStride * sizeof(float);
     p.part_bytes = (p.part_bytes + 255) & ~(size_t)255;
@@ -313,7 +335,7 @@ int kvarn_decode_attention(const kvarn_config_t* cfg, const void* q, const void*
                    : nullptr;
   a.pages_per_split = p.pages_per_split;
   a.nsplit = p.nsplit;
-  a.cluster = 0;   // the kernel's launcher decides
+  a.cluster = p.cluster ? 1 : 0;
   a.fmt = cfg_fmt(cfg);
   a.status = status;
   cudaError_t e = decode_mma_supported(a.g) ? launch_decode_mma(a, (cudaStream_t)stream)

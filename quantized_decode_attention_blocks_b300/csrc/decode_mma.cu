@@ -945,8 +945,7 @@ cudaError_t launch_nt(const DecodeArgs& args, cudaStream_t s) {
   const int smem = (int)sizeof(MmaSmem<NT, RecFmt<FMT>::bytes>);
   cudaError_t e = ensure_dynamic_smem(decode_mma_kernel<NT, FMT>, smem, smem_set);
   if (e != cudaSuccess) return e;
-  DecodeArgs a = args;
-  a.cluster = decode_uses_cluster(a.g, a.nsplit);
+  const DecodeArgs& a = args;   // a.cluster: the plan's choice of merge
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(a.nsplit, a.hkv, a.batch);
   cfg.blockDim = dim3(kThreads);
@@ -984,6 +983,26 @@ template <int RB>
 int ctas_for(int g) {
   const int bytes = g <= 4 ? (int)sizeof(MmaSmem<1, RB>) : (int)sizeof(MmaSmem<2, RB>);
   return min(233472 / (bytes + 1024), 2);
+}
+
+// CTAs per SM that can be resident at once: the shared-memory footprint and
+// the launch bounds (the register budget), without the plan's cap of two.
+template <int RB, int FMT>
+int resident_for(int g) {
+  const int nt = g <= 4 ? 1 : 2;
+  const int bytes = nt == 1 ? (int)sizeof(MmaSmem<1, RB>) : (int)sizeof(MmaSmem<2, RB>);
+  const int lb = FMT == kFmtK8 ? 3 - nt : nt == 1 ? 3 : 2;
+  return min(233472 / (bytes + 1024), lb);
+}
+
+int decode_mma_resident_per_sm(int g, int fmt) {
+  switch (fmt) {
+    case kFmtM16: return resident_for<RecFmt<kFmtM16>::bytes, kFmtM16>(g);
+    case kFmtG64: return resident_for<RecFmt<kFmtG64>::bytes, kFmtG64>(g);
+    case kFmtV4: return resident_for<RecFmt<kFmtV4>::bytes, kFmtV4>(g);
+    case kFmtK8: return resident_for<RecFmt<kFmtK8>::bytes, kFmtK8>(g);
+    default: return resident_for<RecFmt<kFmtF32>::bytes, kFmtF32>(g);
+  }
 }
 
 int decode_mma_ctas_per_sm(int g, int fmt) {

@@ -123,7 +123,7 @@ extern "C" int kvarn_decode_attention_noalloc(const kvarn_config_t* cfg, const v
     // the arrival tickets must start at zero whatever an earlier call left;
     // a plan that merges its splits inside a thread-block cluster never reads
     // them, so it needs no clearing
-    if (!decode_uses_cluster(cfg->num_q_heads / cfg->num_kv_heads, p.nsplit) &&
+    if (!p.cluster &&
         cudaMemsetAsync(static_cast<unsigned char*>(ws) + p.part_bytes, 0, p.count_bytes,
                         (cudaStream_t)stream) != cudaSuccess)
       return KVARN_ERR_LAUNCH;

@@ -300,15 +300,13 @@ struct DecodeArgs {
 struct DecodePlan {
   int pages_per_split;
   int nsplit;
+  bool cluster;        // splits merged inside a thread-block cluster (no tickets read)
   size_t part_bytes;   // partial-state region
   size_t count_bytes;  // ticket region
 };
 // `num_sms`: streaming multiprocessors the plan fills (device_sm_count()).
 // `fmt`: the record format, which sets the kernel's shared memory per CTA.
 DecodePlan decode_plan(int batch, int hq, int hkv, int max_seq, int num_sms, int fmt);
-// Whether the decode launch merges the splits of a (sequence, KV head) inside
-// a thread-block cluster (no workspace tickets are then read).
-bool decode_uses_cluster(int g, int nsplit);
 
 cudaError_t launch_quantize_blocks(const QuantizeArgs& a, cudaStream_t s);
 cudaError_t launch_append_token(const AppendArgs& a, cudaStream_t s);

@@ -26,7 +26,7 @@ PAGE_BYTES_V4 = 19456      # KVARN_PAGE_BYTES_V4: format variant "k4v4_g128"
 PAGE_BYTES_K8 = 27648      # KVARN_PAGE_BYTES_K8: format variant "k8v4_g128"
 FP8_PAGE_BYTES = 33792     # KVARN_FP8_PAGE_BYTES
 FP16_PAGE_BYTES = 65536            # KVARN_FP16_PAGE_BYTES
-NOALLOC_SCRATCH_BYTES = 4 << 20   # KVARN_NOALLOC_SCRATCH_BYTES
+NOALLOC_SCRATCH_BYTES = 16 << 20   # KVARN_NOALLOC_SCRATCH_BYTES
 
 OK = 0
 ERR_INVALID_ARG = -1

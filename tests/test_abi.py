@@ -150,17 +150,44 @@ def test_split_plan_fills_one_wave_and_covers_every_page(sms, g):
     # The plan follows the SM count it is given: it cuts each (sequence, KV
     # head) into at most as many splits as keep the whole grid resident (the
     # tensor-core kernel is planned at 2 CTAs per SM, the CUDA-core one at 3),
-    # covers every page, and leaves no split empty.
+    # covers every page, and leaves no split empty.  When the pairs alone
+    # outnumber one wave (tensor-core kernel), runs are cut to at most 32
+    # pages as far as the partial states fit the no-alloc scratch.
     per_sm = 2 if g <= 8 else 3
+    resident = 3 if g <= 4 else 2   # one head tile: three fit an SM
     for hkv in (1, 2, 8):
         c = kv.config_from_string("k4v2_g128", g * hkv, hkv)
-        for batch in (1, 3, 16, 64, 1000):
+        for batch in (1, 3, 16, 48, 64, 1000):
             for max_seq in (100, 128, 4097, 131072):
                 pps, ns, ws = kv.decode_split_plan(c, batch, max_seq, sms)
                 pages = max(max_seq // 128, 1)
                 assert pps * ns >= pages and pps * (ns - 1) < pages
-                assert ns == 1 or batch * hkv * ns <= sms * per_sm
                 assert (ws == 0) == (ns == 1)
+                if batch * hkv <= sms * resident or g > 8:
+                    assert ns == 1 or batch * hkv * ns <= sms * per_sm
+                else:
+                    assert ws <= K.NOALLOC_SCRATCH_BYTES
+                    more = ns + 1   # one more split would pass the scratch
+                    assert pps <= 32 or (batch * g * hkv * more * 132 * 4
+                                         > K.NOALLOC_SCRATCH_BYTES - 256 - 4 * batch * hkv)
+
+
+def test_split_plan_of_a_ragged_serving_batch_runs_in_several_waves():
+    # 128 sequences of up to 32768 tokens, 8 KV heads: 1024 (sequence, KV
+    # head) pairs against 296 resident CTAs.  One CTA per pair would leave the
+    # longest sequences straggling; the plan cuts them into runs of about 32
+    # pages whose partial states fit the no-alloc scratch.
+    c = kv.config_from_string("k4v2_g128", 32, 8)
+    pps, ns, ws = kv.decode_split_plan(c, 128, 32768, B300_SMS)
+    assert ns > 4 and pps <= 48
+    assert 0 < ws <= K.NOALLOC_SCRATCH_BYTES
+    # a batch that fills one wave keeps the one-wave plan, also where its
+    # pairs fill more than the plan's two CTAs per SM but fit the three that
+    # can be resident
+    pps, ns, ws = kv.decode_split_plan(c, 16, 4096, B300_SMS)
+    assert (pps, ns) == (16, 2)
+    assert kv.decode_split_plan(c, 48, 8192, B300_SMS)[:2] == (64, 1)
+    assert kv.decode_split_plan(c, 64, 8192, B300_SMS)[:2] == (32, 2)
 
 
 def test_split_plan_of_8bit_keys_follows_its_shared_memory():
@@ -182,11 +209,12 @@ def test_split_plan_grows_with_the_sm_count():
     assert n[0] < n[1] < n[2]
 
 
-@pytest.mark.parametrize("g", [1, 2, 4, 6, 8])
-def test_noalloc_scratch_covers_every_group_up_to_eight(g):
-    # the split plan keeps the grid to one wave, so the partial states of every
-    # (batch, length) with at most 8 query heads per KV head fit in the
-    # built-in scratch of the no-alloc decode (a host-only computation)
+@pytest.mark.parametrize("g", [1, 2, 4, 6, 8, 12, 16])
+def test_noalloc_scratch_covers_every_group_up_to_sixteen(g):
+    # a plan of one wave, or one of several waves sized to the scratch: the
+    # partial states of every (batch, length) with at most 16 query heads per
+    # KV head fit in the built-in scratch of the no-alloc decode on a B300 (a
+    # host-only computation)
     for hkv in (1, 2, 8, 32):
         c = kv.config_from_string("k4v2_g128", g * hkv, hkv)
         for batch in (1, 3, 64, 1000, 65535):

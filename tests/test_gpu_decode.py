@@ -239,3 +239,34 @@ def test_scale_argument():
     ref = kvref.decode_attention(host(q), host(pool), host(table), host(lens), host(tk), host(tv),
                                  8, 2, scale=0.3, route=1)
     parity.compare_attention(host(out), ref)
+
+
+@pytest.mark.parametrize("hq,hkv", [(4, 1), (12, 2)])
+def test_ragged_batch_that_runs_in_several_waves(hq, hkv):
+    # More (sequence, KV head) pairs than resident CTAs: the plan cuts the
+    # long sequences into runs of at most 32 pages merged through the
+    # workspace (no clusters), while short sequences end in their first run.
+    # Whole sequences of every length class are checked against the oracle.
+    import quantized_decode_attention_blocks_b300 as kv
+    from tests.test_gpu_workloads import _check_sampled_decode
+    B = 600 if hkv == 1 else 300
+    max_seq = 6000
+    g = torch.Generator().manual_seed(97 + hq)
+    lens = torch.randint(1, max_seq + 1, (B,), generator=g, dtype=torch.int32)
+    lens[:4] = torch.tensor([max_seq, 4096, 129, 0], dtype=torch.int32)
+    w = synth.scaled(synth.WORKLOADS["llama3_8b_layer"], batch=B, seq=max_seq, hkv=hkv, hq=hq)
+    cfg = config(hq, hkv)
+    pps, ns, _ = kv.decode_split_plan(cfg, B, max_seq, 0)
+    assert ns > 1 and pps <= 32   # the several-waves plan
+    mb = (max_seq + 127) // 128
+    table = torch.randperm(B * mb, generator=g).to(torch.int32).reshape(B, mb)
+    k, v = synth.kv(w, device=DEV)
+    pool, tk, tv, st = prefill(cfg, k, v, lens, table, B * mb, max_seq=max_seq)
+    del k, v
+    q = synth.queries(w)
+    out, st2, _ = decode(cfg, q, pool, table, lens, tk, tv, max_seq=max_seq)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0 and int(st2.item()) == 0
+    seqs = [0, 1, 2, 3] + sorted(torch.randperm(B - 4, generator=g)[:12].add(4).tolist())
+    _check_sampled_decode(cfg, q.to(DEV), out, pool, table.to(DEV), lens.to(DEV), tk, tv, seqs)
+    assert not torch.isnan(out.float()).any()

@@ -26,22 +26,23 @@ def _ptr(t):
 
 def test_noalloc_rejects_requests_beyond_its_scratch():
     # On a B300 (148 SMs) every request fits the built-in scratch: one wave of
-    # split CTAs with at most 16 query heads per KV head stays under 4 MiB.
-    # A device with more SMs plans more splits; a request whose partial
+    # split CTAs with at most 16 query heads per KV head stays under 16 MiB.
+    # A device with many more SMs plans more splits; a request whose partial
     # states pass the scratch must be refused before touching the GPU.  The
     # call here only runs where it cannot launch (no device: it cannot plan
     # and says so); on a GPU whose plan fits, it is not made at all, since its
     # pointers are fake.
     cfg = kv.config_from_string("k4v2_g128", 16, 1)
-    assert kv.decode_split_plan(cfg, 1, 131072, 148)[2] <= K.NOALLOC_SCRATCH_BYTES
-    assert kv.decode_split_plan(cfg, 1, 131072, 400)[2] > K.NOALLOC_SCRATCH_BYTES
+    S = 1 << 22
+    assert kv.decode_split_plan(cfg, 1, S, 148)[2] <= K.NOALLOC_SCRATCH_BYTES
+    assert kv.decode_split_plan(cfg, 1, S, 2000)[2] > K.NOALLOC_SCRATCH_BYTES
     fake = ctypes.c_void_p(4096)
-    args = (ctypes.byref(cfg), fake, fake, 1 << 20, fake, 1024, fake, 1, 131072, fake, fake,
+    args = (ctypes.byref(cfg), fake, fake, 1 << 20, fake, S // 128, fake, 1, S, fake, fake,
             ctypes.c_float(128 ** -0.5), fake, None, None)
     if not torch.cuda.is_available():
         assert kv.lib().kvarn_decode_attention_noalloc(*args) == K.ERR_LAUNCH
         return
-    if kv.decode_split_plan(cfg, 1, 131072, 0)[2] <= K.NOALLOC_SCRATCH_BYTES:
+    if kv.decode_split_plan(cfg, 1, S, 0)[2] <= K.NOALLOC_SCRATCH_BYTES:
         pytest.skip("every request fits the scratch on this device")
     assert kv.lib().kvarn_decode_attention_noalloc(*args) == K.ERR_WORKSPACE
 
