@@ -209,6 +209,22 @@ def test_split_plan_grows_with_the_sm_count():
     assert n[0] < n[1] < n[2]
 
 
+@pytest.mark.parametrize("fmt", ["k4v2_g128_m16", "k4v2_g128_pc", "k4v2_g64", "k4v4_g128",
+                                 "k8v4_g128"])
+def test_several_wave_plans_of_every_format_fit_the_scratch(fmt):
+    # every record format sets its own resident CTAs per SM; a ragged batch
+    # of many pairs is cut into short runs, its partial states within the
+    # no-alloc scratch
+    for g in (1, 4, 6, 8):
+        c = kv.config_from_string(fmt, g * 8, 8)
+        for batch in (64, 128, 1000):
+            for max_seq in (8192, 32768, 131072):
+                pps, ns, ws = kv.decode_split_plan(c, batch, max_seq, B300_SMS)
+                pages = max_seq // 128
+                assert pps * ns >= pages and pps * (ns - 1) < pages
+                assert ws <= K.NOALLOC_SCRATCH_BYTES
+
+
 @pytest.mark.parametrize("g", [1, 2, 4, 6, 8, 12, 16])
 def test_noalloc_scratch_covers_every_group_up_to_sixteen(g):
     # a plan of one wave, or one of several waves sized to the scratch: the
