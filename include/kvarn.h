@@ -228,11 +228,11 @@ int kvarn_append_token(const kvarn_config_t *cfg, const void *k_new, const void 
  * streaming multiprocessors (num_sms <= 0: the current device's count).  The
  * pages of each (sequence, KV head) are cut into *nsplit runs of
  * *pages_per_split pages, as many as keep the whole grid resident at once.
- * When the (sequence, KV head) pairs alone outnumber the CTAs one wave holds
- * (at most 8 query heads per KV head), the grid runs in several waves and
- * runs are cut to at most 32 pages instead, as far as the partial states fit
- * KVARN_NOALLOC_SCRATCH_BYTES, so that long sequences of a ragged batch do
- * not straggle.  *workspace_bytes is the decode workspace that plan needs
+ * When the (sequence, KV head) pairs alone outnumber the CTAs that can be
+ * resident at once (at most 8 query heads per KV head), the grid runs in
+ * several waves and runs are cut to at most 32 pages instead, as far as the
+ * partial states fit KVARN_NOALLOC_SCRATCH_BYTES, so that long sequences of
+ * a ragged batch do not straggle.  *workspace_bytes is the decode workspace that plan needs
  * (0: none).  Any output pointer may be NULL.  Host arithmetic only when
  * num_sms > 0 (no CUDA call); KVARN_ERR_LAUNCH when num_sms <= 0 and no
  * device answers. */
@@ -261,9 +261,10 @@ size_t kvarn_decode_workspace_bytes(const kvarn_config_t *cfg, int batch, int ma
  * The work is split across CTAs along each sequence's pages (split-K) and the
  * partial softmax states are merged with a log-sum-exp in the same launch:
  * inside a thread-block cluster (distributed shared memory) when a sequence
- * has 2 to 4 splits in a grid of one wave, through the workspace otherwise.  The launch uses
- * thread-block clusters, so the GPU must be able to co-schedule up to 4 CTAs
- * of the kernel; a launch failure returns KVARN_ERR_LAUNCH. */
+ * has 2 to 4 splits in a grid of one wave, through the workspace
+ * otherwise.  The launch then uses thread-block clusters, so the GPU must be
+ * able to co-schedule up to 4 CTAs of the kernel; a launch failure returns
+ * KVARN_ERR_LAUNCH. */
 int kvarn_decode_attention(const kvarn_config_t *cfg, const void *q, const void *pool,
                            int64_t num_pages, const int32_t *block_table, int max_blocks,
                            const int32_t *seq_lens, int batch, int max_seq,
