@@ -241,8 +241,10 @@ def test_scale_argument():
     parity.compare_attention(host(out), ref)
 
 
-@pytest.mark.parametrize("hq,hkv", [(4, 1), (12, 2)])
-def test_ragged_batch_that_runs_in_several_waves(hq, hkv):
+@pytest.mark.parametrize("hq,hkv,fmt", [(4, 1, {}), (12, 2, {}), (4, 1, {"k8": True}),
+                                        (8, 2, {"g64": True}), (4, 1, {"v4": True}),
+                                        (6, 1, {"m16": True})])
+def test_ragged_batch_that_runs_in_several_waves(hq, hkv, fmt):
     # More (sequence, KV head) pairs than resident CTAs: the plan cuts the
     # long sequences into runs of at most 32 pages merged through the
     # workspace (no clusters), while short sequences end in their first run.
@@ -255,7 +257,7 @@ def test_ragged_batch_that_runs_in_several_waves(hq, hkv):
     lens = torch.randint(1, max_seq + 1, (B,), generator=g, dtype=torch.int32)
     lens[:4] = torch.tensor([max_seq, 4096, 129, 0], dtype=torch.int32)
     w = synth.scaled(synth.WORKLOADS["llama3_8b_layer"], batch=B, seq=max_seq, hkv=hkv, hq=hq)
-    cfg = config(hq, hkv)
+    cfg = config(hq, hkv, **fmt)
     pps, ns, _ = kv.decode_split_plan(cfg, B, max_seq, 0)
     assert ns > 1 and pps <= 32   # the several-waves plan
     mb = (max_seq + 127) // 128
@@ -268,5 +270,6 @@ def test_ragged_batch_that_runs_in_several_waves(hq, hkv):
     torch.cuda.synchronize()
     assert int(st.item()) == 0 and int(st2.item()) == 0
     seqs = [0, 1, 2, 3] + sorted(torch.randperm(B - 4, generator=g)[:12].add(4).tolist())
-    _check_sampled_decode(cfg, q.to(DEV), out, pool, table.to(DEV), lens.to(DEV), tk, tv, seqs)
+    _check_sampled_decode(cfg, q.to(DEV), out, pool, table.to(DEV), lens.to(DEV), tk, tv, seqs,
+                          **fmt)
     assert not torch.isnan(out.float()).any()

@@ -55,8 +55,9 @@ def _check_sampled_tiles(k, v, lens, table, pool, rng, n, stats):
         parity.compare_record(got, ref, u_k, u_v, stats)
 
 
-def _check_sampled_decode(cfg, q, out, pool, table, lens, tk, tv, seqs):
-    """Whole sequences `seqs`: the oracle reads a compact copy of just their pages."""
+def _check_sampled_decode(cfg, q, out, pool, table, lens, tk, tv, seqs, **fmt):
+    """Whole sequences `seqs`: the oracle reads a compact copy of just their
+    pages.  `fmt`: the record format's oracle flags (m16, pc, g64, v4, k8)."""
     sel = torch.tensor(seqs, dtype=torch.long, device=DEV)
     tab = table[sel]
     used = torch.unique(tab[tab >= 0])
@@ -65,7 +66,8 @@ def _check_sampled_decode(cfg, q, out, pool, table, lens, tk, tv, seqs):
     tab_c = torch.where(tab >= 0, remap[tab.clamp(min=0).long()], tab)
     ref = kvref.decode_attention(host(q[sel]), host(pool[used]), host(tab_c), host(lens[sel]),
                                  host(tk[sel]), host(tv[sel]), cfg.num_q_heads,
-                                 cfg.num_kv_heads, route=1)
+                                 cfg.num_kv_heads, route=1,
+                                 **{("meta16" if k == "m16" else k): v for k, v in fmt.items()})
     return parity.compare_attention(host(out[sel]), ref)
 
 
